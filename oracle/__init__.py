@@ -1,0 +1,306 @@
+"""Plain fp64 CPU oracle for the routed MoE layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does: it
+shares no code, headers or helpers with this oracle.
+
+The arithmetic lives in ``moe_oracle.c`` (plain loops, fp64, one token at a
+time, OpenMP over tokens only).  This module compiles it with gcc, loads it
+with ctypes and converts numpy / torch-CPU arrays to the C calling
+convention.  Float tensors may be bfloat16 (passed as raw 16-bit patterns,
+converted exactly inside C) or float64; one call uses one or the other.
+
+Page references (title, section):
+  "HyperParallel加速DeepSeek-V4.1多模态1M长序列训练", §2.3 MegaKernel
+      (MegaGate, MegaMoE bullets) -- routing, dispatch, expert FFN, return;
+  "MindSpore HyperParallel一键开箱DeepSeek-V4.1-Flash", §01 -- shared expert;
+  "Twinkle x 昇腾，率先实现Deepseek-V4系列模型高效训练", FSDP2-4D section --
+      TopKRouter / HashRouter outputs and the combine by routing weight.
+
+Parity pins: see tests/test_oracle_*.py.  None of the functions is pinned by
+a value printed on the pages (they print none); all are pinned by brute
+force, closed forms, invariants, library routines and finite differences.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp contraction off so x86 and Arm agree)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_D = ctypes.c_double
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            sig = {
+                "orc_num_threads": ([], _I),
+                "orc_set_num_threads": ([_I], None),
+                "orc_gate_logits": ([_P, _P, _I, _P, _I, _P, _I, _I, _I, _P], None),
+                "orc_route": ([_P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _I, _D, _I,
+                               _P, _P, _P, _P], None),
+                "orc_permute": ([_P, _I, _I, _I, _P, _P, _P, _P], None),
+                "orc_expert_rows": ([_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _D, _I,
+                                     _P, _P], None),
+                "orc_layer_forward": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I,
+                                       _I, _P, _I, _I, _I, _I, _D, _D, _I,
+                                       _P, _P, _P, _P, _P, _P], None),
+                "orc_layer_backward": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
+                                        _I, _I, _P, _I, _I, _I, _I, _D, _D, _I,
+                                        _P, _P, _P], None),
+                "orc_expert_wgrad": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _D, _I,
+                                      _I, _P, _P], None),
+                "orc_expert_wgrad_entries": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I,
+                                              _D, _I, _I, _I, _P, _P, _P, _P], None),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+# --------------------------------------------------------------- helpers
+
+def _to_np(a):
+    """torch tensor or numpy array -> contiguous numpy array (bf16 -> uint16 bits)."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype == torch.bfloat16:
+                return a.view(torch.int16).numpy().view(np.uint16)
+            return a.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(a)
+
+
+def _floats(*arrays):
+    """Convert the float tensors of one call to a common C form: all bf16 bit
+    patterns (flag 1) or all float64 (flag 0)."""
+    conv = [_to_np(a) for a in arrays]
+    if all(c.dtype == np.uint16 for c in conv):
+        return conv, 1
+    return [np.ascontiguousarray(c, dtype=np.float64) if c.dtype != np.uint16 else
+            _bf16_bits_to_f64(c) for c in conv], 0
+
+
+def _bf16_bits_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _opt(a, dtype):
+    if a is None:
+        return None
+    return np.ascontiguousarray(_to_np(a), dtype=dtype)
+
+
+def _tok(tok, n_default):
+    if tok is None:
+        return None, n_default
+    t = np.ascontiguousarray(_to_np(tok), dtype=np.int64)
+    return t, int(t.shape[0])
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().orc_set_num_threads(int(n))
+
+
+# ------------------------------------------------------------- the steps
+
+def gate_logits(x, W_g, offset=None, tok=None, exact=False):
+    """z = x W_g^T (+ offset), fp64 accumulation, rounded to fp32 unless exact."""
+    (xn, wn), bf = _floats(x, W_g)
+    E, d = wn.shape
+    tk, n = _tok(tok, xn.shape[0])
+    off = _opt(offset, np.float32)
+    z = np.empty((n, E), np.float64)
+    _load().orc_gate_logits(_ptr(xn), _ptr(wn), bf, _ptr(off), n, _ptr(tk), d, E, int(exact),
+                            _ptr(z))
+    return z
+
+
+def route(z, bias, k, rho, is_vision=None, mode=0, input_ids=None, tid2eid=None, tok=None,
+          exact=False):
+    """Routing of tokens from their logits z [n, E].
+
+    Returns ids int32 [n,k], w [n,k], s_sel [n,k], margin [n] (fp64 arrays holding
+    fp32 values unless exact)."""
+    zn = np.ascontiguousarray(_to_np(z), dtype=np.float64)
+    n, E = zn.shape
+    tk, _ = _tok(tok, n)
+    b = np.ascontiguousarray(_to_np(bias), dtype=np.float32).reshape(-1)
+    if b.shape[0] == E:
+        b = np.concatenate([b, b])
+    vis = _opt(is_vision, np.uint8)
+    ii = _opt(input_ids, np.int32)
+    tab = _opt(tid2eid, np.int32)
+    vocab = 0 if tab is None else int(tab.shape[0])
+    ids = np.empty((n, k), np.int32)
+    w = np.empty((n, k), np.float64)
+    s = np.empty((n, k), np.float64)
+    m = np.empty((n,), np.float64)
+    _load().orc_route(_ptr(zn), _ptr(b), _ptr(vis), int(mode), _ptr(ii), _ptr(tab), vocab, n,
+                      _ptr(tk), E, k, float(rho), int(exact), _ptr(ids), _ptr(w), _ptr(s),
+                      _ptr(m))
+    return ids, w, s, m
+
+
+def permute(ids, E):
+    """Stable expert-major permutation: counts, offsets [E+1], row_token, slot_row."""
+    idn = np.ascontiguousarray(_to_np(ids), dtype=np.int32)
+    T, k = idn.shape
+    counts = np.empty((E,), np.int32)
+    offsets = np.empty((E + 1,), np.int32)
+    row_token = np.empty((T * k,), np.int32)
+    slot_row = np.empty((T * k,), np.int32)
+    _load().orc_permute(_ptr(idn), T, E, k, _ptr(counts), _ptr(offsets), _ptr(row_token),
+                        _ptr(slot_row))
+    return counts, offsets, row_token, slot_row
+
+
+def expert_rows(x, W13, W2, row_tok, row_exp, row_w, clamp, exact=False):
+    """Per-row expert FFN: y[r] = row_w[r] * W2[e] h(x[row_tok[r]]); returns (h, y)."""
+    (xn, w13, w2), bf = _floats(x, W13, W2)
+    d = xn.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    re = np.ascontiguousarray(_to_np(row_exp), dtype=np.int32)
+    rw = _opt(row_w, np.float64)
+    n = rt.shape[0]
+    h = np.empty((n, I), np.float64)
+    y = np.empty((n, d), np.float64)
+    _load().orc_expert_rows(_ptr(xn), _ptr(w13), _ptr(w2), bf, n, _ptr(rt), _ptr(re), _ptr(rw),
+                            d, I, float(clamp), int(exact), _ptr(h), _ptr(y))
+    return h, y
+
+
+def _route_args(bias, E, is_vision, input_ids, tid2eid, offset):
+    b = np.ascontiguousarray(_to_np(bias), dtype=np.float32).reshape(-1)
+    if b.shape[0] == E:
+        b = np.concatenate([b, b])
+    tab = _opt(tid2eid, np.int32)
+    return (b, _opt(is_vision, np.uint8), _opt(input_ids, np.int32), tab,
+            0 if tab is None else int(tab.shape[0]), _opt(offset, np.float32))
+
+
+def layer_forward(x, W_g, W13, W2, bias, k, rho, clamp, is_vision=None, mode=0,
+                  input_ids=None, tid2eid=None, offset=None, tok=None, exact=False):
+    """Forward of the layer for the listed tokens (all when tok is None).
+
+    Returns dict(z, ids, w, s_sel, margin, y)."""
+    (xn, wg, w13, w2), bf = _floats(x, W_g, W13, W2)
+    E, d = wg.shape
+    I = w2.shape[-1]
+    b, vis, ii, tab, vocab, off = _route_args(bias, E, is_vision, input_ids, tid2eid, offset)
+    tk, n = _tok(tok, xn.shape[0])
+    z = np.empty((n, E), np.float64)
+    ids = np.empty((n, k), np.int32)
+    w = np.empty((n, k), np.float64)
+    s = np.empty((n, k), np.float64)
+    m = np.empty((n,), np.float64)
+    y = np.empty((n, d), np.float64)
+    _load().orc_layer_forward(_ptr(xn), _ptr(wg), _ptr(w13), _ptr(w2), bf, _ptr(off), _ptr(b),
+                              _ptr(vis), int(mode), _ptr(ii), _ptr(tab), vocab, n, _ptr(tk),
+                              d, E, k, I, float(rho), float(clamp), int(exact), _ptr(z),
+                              _ptr(ids), _ptr(w), _ptr(s), _ptr(m), _ptr(y))
+    return dict(z=z, ids=ids, w=w, s_sel=s, margin=m, y=y)
+
+
+def layer_backward(x, W_g, W13, W2, dY, bias, k, rho, clamp, is_vision=None, mode=0,
+                   input_ids=None, tid2eid=None, offset=None, tok=None, exact=False):
+    """Token-local backward for the listed tokens: dict(dX [n,d], dz [n,E], dw [n,k])."""
+    (xn, wg, w13, w2, dy), bf = _floats(x, W_g, W13, W2, dY)
+    E, d = wg.shape
+    I = w2.shape[-1]
+    b, vis, ii, tab, vocab, off = _route_args(bias, E, is_vision, input_ids, tid2eid, offset)
+    tk, n = _tok(tok, xn.shape[0])
+    dX = np.empty((n, d), np.float64)
+    dz = np.empty((n, E), np.float64)
+    dw = np.empty((n, k), np.float64)
+    _load().orc_layer_backward(_ptr(xn), _ptr(wg), _ptr(w13), _ptr(w2), _ptr(dy), bf, _ptr(off),
+                               _ptr(b), _ptr(vis), int(mode), _ptr(ii), _ptr(tab), vocab, n,
+                               _ptr(tk), d, E, k, I, float(rho), float(clamp), int(exact),
+                               _ptr(dX), _ptr(dz), _ptr(dw))
+    return dict(dX=dX, dz=dz, dw=dw)
+
+
+def expert_wgrad(x, W13, W2, dY, e, row_tok, row_w, clamp, exact=False, want=("dW13", "dW2"),
+                 store_bf16=False):
+    """Full weight gradients of expert e from its rows: dict(dW13 [2I,d], dW2 [d,I]).
+
+    store_bf16 rounds the stored per-row factors [dg|du] and w*h to bf16."""
+    (xn, w13, w2, dy), bf = _floats(x, W13, W2, dY)
+    d = xn.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    rw = np.ascontiguousarray(_to_np(row_w), dtype=np.float64)
+    out = {}
+    g13 = np.empty((2 * I, d), np.float64) if "dW13" in want else None
+    g2 = np.empty((d, I), np.float64) if "dW2" in want else None
+    _load().orc_expert_wgrad(_ptr(xn), _ptr(w13), _ptr(w2), _ptr(dy), bf, int(e), rt.shape[0],
+                             _ptr(rt), _ptr(rw), d, I, float(clamp), int(exact),
+                             int(store_bf16), _ptr(g13), _ptr(g2))
+    if g13 is not None:
+        out["dW13"] = g13
+    if g2 is not None:
+        out["dW2"] = g2
+    return out
+
+
+def expert_wgrad_entries(x, W13, W2, dY, e, row_tok, row_w, clamp, kind, qa, qb, exact=False,
+                         store_bf16=False):
+    """Sampled weight-gradient entries of expert e (kind 0: dW2[qa,qb]; 1: dW13[qa,qb])."""
+    (xn, w13, w2, dy), bf = _floats(x, W13, W2, dY)
+    d = xn.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    rw = np.ascontiguousarray(_to_np(row_w), dtype=np.float64)
+    kd = np.ascontiguousarray(kind, dtype=np.int32)
+    a = np.ascontiguousarray(qa, dtype=np.int32)
+    b = np.ascontiguousarray(qb, dtype=np.int32)
+    out = np.empty((kd.shape[0],), np.float64)
+    _load().orc_expert_wgrad_entries(_ptr(xn), _ptr(w13), _ptr(w2), _ptr(dy), bf, int(e),
+                                     rt.shape[0], _ptr(rt), _ptr(rw), d, I, float(clamp),
+                                     int(exact), int(store_bf16), kd.shape[0], _ptr(kd),
+                                     _ptr(a), _ptr(b), _ptr(out))
+    return out

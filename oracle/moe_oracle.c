@@ -1,0 +1,583 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle for the routed MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark do.  It shares no code with the CUDA path.
+ *
+ * Sources (page title, section):
+ *   [HP41]  "HyperParallel加速DeepSeek-V4.1多模态1M长序列训练",
+ *           §2.3 MegaKernel -- MegaGate bullet (score, bias ranking, top-k,
+ *           score extraction, normalisation and scaling; separate text and
+ *           vision routing bias; fused backward of the normalisation chain;
+ *           the projection matmul stays a library GEMM) and MegaMoE bullet
+ *           (token dispatch, two expert matmuls, SwiGLU with clamp, result
+ *           return); §01 item 5 (native multimodal MoE, separate text/vision
+ *           load balance).
+ *   [HPF]   "MindSpore HyperParallel一键开箱DeepSeek-V4.1-Flash", §01
+ *           (1 shared + 384 routed experts per MoE layer, 6 active).
+ *   [TW]    "Twinkle x 昇腾，率先实现Deepseek-V4系列模型高效训练",
+ *           "FSDP2-4D并行引擎适配" (TopKRouter returns router logits, routing
+ *           weights and selected experts; HashRouter takes ids from
+ *           tid2eid[input_ids] and still weights them with the gate logits;
+ *           dispatch, local expert compute, return and combine by routing
+ *           weight).
+ *
+ * The pages print no formulas, so every function below is the plain
+ * definition of the step they name, in fp64, one token at a time.  Numeric
+ * choices the pages leave open (sigmoid scoring, clamp value, routed scaling,
+ * the rounding points of the interface) are parameters or are stated at the
+ * function.  Parity pins: every function is pinned by the CPU tests against
+ * brute force, closed forms, invariants, library routines and finite
+ * differences; none is pinned by a number the pages print (they print none).
+ *
+ * Float tensors (x, W_g, W13, W2, dY) are passed as `const void*` plus one
+ * flag `bf`: bf=1 means raw bfloat16 bit patterns (uint16), bf=0 means
+ * double.  The conversion of bf16 to double is exact.
+ *
+ * `exact`=1 turns off every interface rounding (fp32 logits, scores, keys and
+ * weights; bf16 intermediate h) so that the chain is a smooth fp64 function
+ * for finite-difference checks.  `exact`=0 rounds at the interface points:
+ * z, s, key and w to fp32, h to bf16.
+ *
+ * Weight layouts (row-major):
+ *   W_g  [E, d]
+ *   W13  [E+1, 2I, d]  rows 0..I-1 = gate projection, I..2I-1 = up projection;
+ *                      group E is the shared expert
+ *   W2   [E+1, d, I]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ scalars */
+
+static double bf16_to_f64(uint16_t v)
+{
+    uint32_t u = (uint32_t)v << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double ld(const void *p, size_t i, int bf)
+{
+    return bf ? bf16_to_f64(((const uint16_t *)p)[i]) : ((const double *)p)[i];
+}
+
+static double dot(const void *a, size_t ia, const void *b, size_t ib, int n, int bf)
+{
+    double s = 0.0;
+    if (bf) {
+        const uint16_t *pa = (const uint16_t *)a + ia, *pb = (const uint16_t *)b + ib;
+        for (int i = 0; i < n; ++i) s += bf16_to_f64(pa[i]) * bf16_to_f64(pb[i]);
+    } else {
+        const double *pa = (const double *)a + ia, *pb = (const double *)b + ib;
+        for (int i = 0; i < n; ++i) s += pa[i] * pb[i];
+    }
+    return s;
+}
+
+/* Round to the nearest fp32 (ties to even, the C default rounding mode). */
+static double r32(double v) { return (double)(float)v; }
+
+/* Round to the nearest bfloat16 value (8 significant bits, ties to even),
+ * written from the format's definition: scale so that one unit in the last
+ * place is 1, round to the nearest integer, scale back. */
+static double rbf16(double v)
+{
+    if (v == 0.0 || !isfinite(v)) return v;
+    int ex;
+    frexp(v, &ex);               /* v = m * 2^ex, 0.5 <= |m| < 1 */
+    if (ex < -125) ex = -125;    /* subnormal range keeps the fixed quantum */
+    double quantum = ldexp(1.0, ex - 8);
+    return nearbyint(v / quantum) * quantum;
+}
+
+/* Logistic sigmoid, the score function of the routing step. */
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* silu(a) = a * sigmoid(a) */
+static double silu(double a) { return a * sigmoid(a); }
+
+/* d silu / d a = s + a s (1 - s), s = sigmoid(a) */
+static double dsilu(double a)
+{
+    double s = sigmoid(a);
+    return s + a * s * (1.0 - s);
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------ gate (F1) */
+
+/* z[t,e] = sum_i x[t,i] W_g[e,i] + offset[e]           ([HP41] §2.3 MegaGate:
+ * the projection is an ordinary matmul ahead of the routing pipeline).
+ * `offset` (nullable) is a per-expert logit shift used by workloads with a
+ * prescribed expert-load skew; it has no gradient.  tok (nullable) lists the
+ * token rows of x to use; z has one row per listed token. */
+void orc_gate_logits(const void *x, const void *Wg, int bf, const float *offset,
+                     int n, const int64_t *tok, int d, int E, int exact, double *z)
+{
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int r = 0; r < n; ++r) {
+        int64_t t = tok ? tok[r] : r;
+        for (int e = 0; e < E; ++e) {
+            double v = dot(x, (size_t)t * d, Wg, (size_t)e * d, d, bf);
+            if (offset) v += (double)offset[e];
+            z[(size_t)r * E + e] = exact ? v : r32(v);
+        }
+    }
+}
+
+/* ------------------------------------------------------------ route (F2) */
+
+/* Routing of one token ([HP41] §2.3 MegaGate; [TW] FSDP2-4D section).
+ *   s_e   = sigmoid(z_e)                                  (score)
+ *   key_e = s_e + b[m, e], m = 1 for a vision token else 0 (bias ranking,
+ *                                                         per-modality bias)
+ *   ids   = the k experts with the largest key, in descending key order,
+ *           equal keys ordered by the lower expert id     (top-k)
+ *   hash mode: ids = tid2eid[input_id], bias unused       ([TW] HashRouter)
+ *   s_j   = s at ids_j (unbiased)                         (score extraction)
+ *   w_j   = rho * s_j / sum_i s_i                         (normalise, scale)
+ * `margin` = the smallest difference between consecutive keys among the
+ * k+1 largest (top-k mode; +inf in hash mode or when k == E): a selection
+ * whose margin is tiny can legitimately flip under a last-bit change of z. */
+static void route_token(const double *zt, const float *bias, int vis, int mode,
+                        const int32_t *table_row, int E, int k, double rho, int exact,
+                        int32_t *ids, double *w, double *ssel, double *margin,
+                        char *taken)
+{
+    if (mode == 0) {
+        memset(taken, 0, (size_t)E);
+        double prev = 0.0;
+        *margin = INFINITY;
+        int rounds = k < E ? k + 1 : k;
+        for (int j = 0; j < rounds; ++j) {
+            int best = -1;
+            double bk = -INFINITY;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                double s = sigmoid(zt[e]);
+                if (!exact) s = r32(s);
+                double key = s + (double)bias[(size_t)vis * E + e];
+                if (!exact) key = r32(key);
+                if (best < 0 || key > bk) { best = e; bk = key; }  /* strict: lowest id wins ties */
+            }
+            if (j > 0 && prev - bk < *margin) *margin = prev - bk;
+            prev = bk;
+            if (j < k) { ids[j] = best; taken[best] = 1; }
+        }
+    } else {
+        for (int j = 0; j < k; ++j) ids[j] = table_row[j];
+        *margin = INFINITY;
+    }
+    double S = 0.0;
+    for (int j = 0; j < k; ++j) {
+        double s = sigmoid(zt[ids[j]]);
+        if (!exact) s = r32(s);
+        ssel[j] = s;
+        S += s;
+    }
+    for (int j = 0; j < k; ++j) {
+        double v = S > 0.0 ? rho * ssel[j] / S : 0.0;
+        w[j] = exact ? v : r32(v);
+    }
+}
+
+/* Route n tokens given their logits z[n,E].  mode 0 = top-k, 1 = hash.
+ * is_vision (nullable = all text) and input_ids are indexed by the token
+ * numbers in tok (nullable = 0..n-1).  tid2eid is [vocab, k]. */
+void orc_route(const double *z, const float *bias, const uint8_t *is_vision, int mode,
+               const int32_t *input_ids, const int32_t *tid2eid, int vocab,
+               int n, const int64_t *tok, int E, int k, double rho, int exact,
+               int32_t *ids, double *w, double *ssel, double *margin)
+{
+#pragma omp parallel
+    {
+        char *taken = (char *)malloc((size_t)E);
+#pragma omp for schedule(static)
+        for (int r = 0; r < n; ++r) {
+            int64_t t = tok ? tok[r] : r;
+            int vis = is_vision ? (is_vision[t] != 0) : 0;
+            const int32_t *row = NULL;
+            if (mode == 1) {
+                int32_t id = input_ids[t];
+                if (id < 0 || id >= vocab) id = 0;  /* callers validate; keep in bounds */
+                row = tid2eid + (size_t)id * k;
+            }
+            route_token(z + (size_t)r * E, bias, vis, mode, row, E, k, rho, exact,
+                        ids + (size_t)r * k, w + (size_t)r * k, ssel + (size_t)r * k,
+                        margin + r, taken);
+        }
+        free(taken);
+    }
+}
+
+/* --------------------------------------------------------- permute (F3) */
+
+/* Expert-contiguous permutation of the T*k routed slots ([HP41] §2.3 MegaMoE
+ * "token dispatch"; [TW] FSDP2-4D: selected experts become global expert ids
+ * of one unified dispatch).  Rows are ordered by expert, then token, then slot
+ * position -- the plain stable order, built by the plain triple loop.
+ *   counts[e]           = number of slots routed to e
+ *   offsets[e]          = first row of expert e (offsets[E] = T*k)
+ *   row_token[row]      = token of that row
+ *   slot_row[t*k + j]   = row that holds slot j of token t */
+void orc_permute(const int32_t *ids, int T, int E, int k, int32_t *counts,
+                 int32_t *offsets, int32_t *row_token, int32_t *slot_row)
+{
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (long s = 0; s < (long)T * k; ++s) counts[ids[s]]++;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int32_t row = 0;
+    for (int e = 0; e < E; ++e)
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j)
+                if (ids[(size_t)t * k + j] == e) {
+                    row_token[row] = t;
+                    slot_row[(size_t)t * k + j] = row;
+                    ++row;
+                }
+}
+
+/* ------------------------------------------------------ expert FFN (F4/F5) */
+
+/* One expert on one input row ([HP41] §2.3 MegaMoE: two expert matmuls around
+ * SwiGLU with the clamp V4.1 needs):
+ *   g = W13[e, 0:I] x,   u = W13[e, I:2I] x
+ *   h = silu(min(g, c)) * clamp(u, -c, c)      (h rounded to bf16 unless exact)
+ *   o = W2[e] h                                 (length d)
+ * Optional outputs g, u, h (length I) and o (length d). */
+static void ffn_row(const void *x, size_t xoff, const void *W13, const void *W2, int bf,
+                    int e, int d, int I, double c, int exact,
+                    double *g, double *u, double *h, double *o)
+{
+    size_t w13 = (size_t)e * 2 * I * d, w2 = (size_t)e * d * I;
+    for (int i = 0; i < I; ++i) {
+        double gi = dot(x, xoff, W13, w13 + (size_t)i * d, d, bf);
+        double ui = dot(x, xoff, W13, w13 + (size_t)(I + i) * d, d, bf);
+        double a = gi < c ? gi : c;
+        double b = ui < -c ? -c : (ui > c ? c : ui);
+        double hi = silu(a) * b;
+        g[i] = gi;
+        u[i] = ui;
+        h[i] = exact ? hi : rbf16(hi);
+    }
+    if (o)
+        for (int n = 0; n < d; ++n) {
+            double acc = 0.0;
+            for (int i = 0; i < I; ++i) acc += h[i] * ld(W2, w2 + (size_t)n * I + i, bf);
+            o[n] = acc;
+        }
+}
+
+/* Expert FFN over a list of rows with per-row expert and weight:
+ *   y[r] = row_w[r] * W2[e_r] h(x[row_tok[r]])
+ * h[r] (length I) is returned as well.  This is the per-expert computation of
+ * the dispatched rows, without any layer around it. */
+void orc_expert_rows(const void *x, const void *W13, const void *W2, int bf,
+                     int n, const int64_t *row_tok, const int32_t *row_exp,
+                     const double *row_w, int d, int I, double c, int exact,
+                     double *h, double *y)
+{
+#pragma omp parallel
+    {
+        double *g = (double *)malloc(sizeof(double) * (size_t)I * 2);
+        double *u = g + I;
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n; ++r) {
+            ffn_row(x, (size_t)row_tok[r] * d, W13, W2, bf, row_exp[r], d, I, c, exact,
+                    g, u, h + (size_t)r * I, o);
+            double wr = row_w ? row_w[r] : 1.0;
+            for (int m = 0; m < d; ++m) y[(size_t)r * d + m] = wr * o[m];
+        }
+        free(g);
+        free(o);
+    }
+}
+
+/* ------------------------------------------------------- layer forward */
+
+/* Forward of the whole layer for the listed tokens (F1, F2, F4-F6):
+ *   y_t = shared(x_t) + sum_j w_j expert_{ids_j}(x_t)
+ * ([HPF] §01: one always-on shared expert plus k routed experts; [TW] FSDP2-4D:
+ * the expert results come back and are combined by routing weight).  The
+ * dispatch permutation (F3) does not change the value of y_t, so it is
+ * checked on its own by orc_permute.  Outputs: z[n,E], ids/w/ssel[n,k],
+ * margin[n], y[n,d]. */
+void orc_layer_forward(const void *x, const void *Wg, const void *W13, const void *W2, int bf,
+                       const float *offset, const float *bias, const uint8_t *is_vision,
+                       int mode, const int32_t *input_ids, const int32_t *tid2eid, int vocab,
+                       int n, const int64_t *tok, int d, int E, int k, int I,
+                       double rho, double c, int exact,
+                       double *z, int32_t *ids, double *w, double *ssel, double *margin,
+                       double *y)
+{
+    orc_gate_logits(x, Wg, bf, offset, n, tok, d, E, exact, z);
+    orc_route(z, bias, is_vision, mode, input_ids, tid2eid, vocab, n, tok, E, k, rho, exact,
+              ids, w, ssel, margin);
+#pragma omp parallel
+    {
+        double *g = (double *)malloc(sizeof(double) * (size_t)I * 3);
+        double *u = g + I, *h = g + 2 * I;
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n; ++r) {
+            int64_t t = tok ? tok[r] : r;
+            double *yt = y + (size_t)r * d;
+            ffn_row(x, (size_t)t * d, W13, W2, bf, E, d, I, c, exact, g, u, h, o);
+            for (int m = 0; m < d; ++m) yt[m] = o[m];
+            for (int j = 0; j < k; ++j) {
+                ffn_row(x, (size_t)t * d, W13, W2, bf, ids[(size_t)r * k + j], d, I, c, exact,
+                        g, u, h, o);
+                double wj = w[(size_t)r * k + j];
+                for (int m = 0; m < d; ++m) yt[m] += wj * o[m];
+            }
+        }
+        free(g);
+        free(o);
+    }
+}
+
+/* ------------------------------------------------------- layer backward */
+
+/* Backward of one expert on one row, for upstream gradient dy (length d) and
+ * routing weight wr.  Chain rule of ffn_row, with the clamp gradients passing
+ * where the argument equals the bound (torch.clamp convention):
+ *   dA = W2[e]^T dy                       (length I)
+ *   dw = <h, dA>                          (gradient of the routing weight)
+ *   dH = wr dA
+ *   dg = dH * clamp(u) * silu'(min(g,c)) * [g <= c]
+ *   du = dH * silu(min(g,c)) * [-c <= u <= c]
+ *   dx = W13[e, 0:I]^T dg + W13[e, I:2I]^T du   (accumulated into dx)
+ * dgu (length 2I, nullable) receives [dg | du]. */
+static double ffn_row_backward(const void *x, size_t xoff, const void *dY, size_t dyoff,
+                               const void *W13, const void *W2, int bf, int e, int d, int I,
+                               double c, int exact, double wr, double *g, double *u,
+                               double *h, double *dA, double *dgu, double *dx)
+{
+    ffn_row(x, xoff, W13, W2, bf, e, d, I, c, exact, g, u, h, NULL);
+    size_t w13 = (size_t)e * 2 * I * d, w2 = (size_t)e * d * I;
+    for (int i = 0; i < I; ++i) dA[i] = 0.0;
+    for (int m = 0; m < d; ++m) {
+        double dym = ld(dY, dyoff + m, bf);
+        if (dym == 0.0) continue;
+        for (int i = 0; i < I; ++i) dA[i] += dym * ld(W2, w2 + (size_t)m * I + i, bf);
+    }
+    double dw = 0.0;
+    for (int i = 0; i < I; ++i) dw += h[i] * dA[i];
+    for (int i = 0; i < I; ++i) {
+        double dH = wr * dA[i];
+        double a = g[i] < c ? g[i] : c;
+        double b = u[i] < -c ? -c : (u[i] > c ? c : u[i]);
+        double dg = g[i] <= c ? dH * b * dsilu(a) : 0.0;
+        double du = (u[i] >= -c && u[i] <= c) ? dH * silu(a) : 0.0;
+        if (dgu) { dgu[i] = dg; dgu[I + i] = du; }
+        if (dx)
+            for (int m = 0; m < d; ++m)
+                dx[m] += dg * ld(W13, w13 + (size_t)i * d + m, bf) +
+                         du * ld(W13, w13 + (size_t)(I + i) * d + m, bf);
+    }
+    return dw;
+}
+
+/* Backward of the routing weights (the normalisation chain fused by MegaGate,
+ * [HP41] §2.3).  With w_j = rho s_j / S, S = sum_i s_i, the Jacobian is
+ *   dw_j/ds_m = rho (delta_jm / S - s_j / S^2),
+ * so ds_m = sum_j dw_j dw_j/ds_m, and through the sigmoid
+ *   dz_m = ds_m s_m (1 - s_m).
+ * The bias only ranks, so it receives no gradient; unselected experts get
+ * dz = 0.  (s here is the unrounded sigmoid of z.) */
+static void route_backward(const double *zt, const int32_t *ids, const double *dw, int k,
+                           double rho, double *dz_sel)
+{
+    double s[64], S = 0.0;
+    for (int j = 0; j < k; ++j) { s[j] = sigmoid(zt[ids[j]]); S += s[j]; }
+    for (int m = 0; m < k; ++m) {
+        double ds = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double jac = rho * ((j == m ? 1.0 / S : 0.0) - s[j] / (S * S));
+            ds += dw[j] * jac;
+        }
+        dz_sel[m] = ds * s[m] * (1.0 - s[m]);
+    }
+}
+
+/* Token-local backward of the layer for the listed tokens, given upstream
+ * dY[n_tok rows of the full dY, indexed by token].  Outputs per listed token:
+ *   dX[n,d]  (through the shared expert, the k routed experts and the gate)
+ *   dz[n,E]  (logit gradient; zero off the selection)
+ *   dw[n,k]  (routing-weight gradient)
+ * Routing (ids, w) is recomputed here from x exactly as the forward does. */
+void orc_layer_backward(const void *x, const void *Wg, const void *W13, const void *W2,
+                        const void *dY, int bf, const float *offset, const float *bias,
+                        const uint8_t *is_vision, int mode, const int32_t *input_ids,
+                        const int32_t *tid2eid, int vocab, int n, const int64_t *tok,
+                        int d, int E, int k, int I, double rho, double c, int exact,
+                        double *dX, double *dz, double *dw)
+{
+    double *z = (double *)malloc(sizeof(double) * (size_t)n * E);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)n * k);
+    double *w = (double *)malloc(sizeof(double) * (size_t)n * k);
+    double *ssel = (double *)malloc(sizeof(double) * (size_t)n * k);
+    double *margin = (double *)malloc(sizeof(double) * (size_t)n);
+    orc_gate_logits(x, Wg, bf, offset, n, tok, d, E, exact, z);
+    orc_route(z, bias, is_vision, mode, input_ids, tid2eid, vocab, n, tok, E, k, rho, exact,
+              ids, w, ssel, margin);
+#pragma omp parallel
+    {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)I * 4);
+        double *g = buf, *u = buf + I, *h = buf + 2 * I, *dA = buf + 3 * I;
+        double dzs[64];
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n; ++r) {
+            int64_t t = tok ? tok[r] : r;
+            double *dxt = dX + (size_t)r * d;
+            for (int m = 0; m < d; ++m) dxt[m] = 0.0;
+            ffn_row_backward(x, (size_t)t * d, dY, (size_t)t * d, W13, W2, bf, E, d, I, c,
+                             exact, 1.0, g, u, h, dA, NULL, dxt);
+            for (int j = 0; j < k; ++j)
+                dw[(size_t)r * k + j] = ffn_row_backward(
+                    x, (size_t)t * d, dY, (size_t)t * d, W13, W2, bf, ids[(size_t)r * k + j],
+                    d, I, c, exact, w[(size_t)r * k + j], g, u, h, dA, NULL, dxt);
+            route_backward(z + (size_t)r * E, ids + (size_t)r * k, dw + (size_t)r * k, k, rho,
+                           dzs);
+            double *dzt = dz + (size_t)r * E;
+            for (int e = 0; e < E; ++e) dzt[e] = 0.0;
+            for (int j = 0; j < k; ++j) dzt[ids[(size_t)r * k + j]] += dzs[j];
+            for (int e = 0; e < E; ++e) {
+                if (dzt[e] == 0.0) continue;
+                for (int m = 0; m < d; ++m) dxt[m] += dzt[e] * ld(Wg, (size_t)e * d + m, bf);
+            }
+        }
+        free(buf);
+    }
+    free(z); free(ids); free(w); free(ssel); free(margin);
+}
+
+/* Weight gradients of one expert e from the rows routed to it:
+ *   dW2[e]  = sum_r dy_r (w_r h_r)^T           [d, I]
+ *   dW13[e] = sum_r [dg_r | du_r] x_r^T        [2I, d]
+ * rows: n_rows rows with token row_tok[r] and weight row_w[r] (the shared
+ * expert uses every token with weight 1).  Either output may be NULL.  Full
+ * matrices: for experts with few rows only.
+ * store_bf16 = 1 rounds the two per-row factors that a bf16 training step
+ * stores between its backward matmuls -- [dg | du] and w h -- to bf16 before
+ * the sums (the sums themselves stay fp64).  Over thousands of rows these
+ * roundings do not average away against a max-abs criterion, so a check of
+ * a bf16 implementation compares like with like. */
+void orc_expert_wgrad(const void *x, const void *W13, const void *W2, const void *dY, int bf,
+                      int e, int n_rows, const int64_t *row_tok, const double *row_w,
+                      int d, int I, double c, int exact, int store_bf16, double *dW13,
+                      double *dW2)
+{
+    double *G = (double *)malloc(sizeof(double) * (size_t)n_rows * 2 * I);  /* dgu rows */
+    double *H = (double *)malloc(sizeof(double) * (size_t)n_rows * I);      /* w h rows */
+#pragma omp parallel
+    {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)I * 4);
+        double *g = buf, *u = buf + I, *h = buf + 2 * I, *dA = buf + 3 * I;
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n_rows; ++r) {
+            size_t t = (size_t)row_tok[r];
+            double *Gr = G + (size_t)r * 2 * I;
+            ffn_row_backward(x, t * d, dY, t * d, W13, W2, bf, e, d, I, c, exact, row_w[r],
+                             g, u, h, dA, Gr, NULL);
+            for (int i = 0; i < I; ++i) {
+                double v = row_w[r] * h[i];
+                H[(size_t)r * I + i] = store_bf16 ? rbf16(v) : v;
+            }
+            if (store_bf16)
+                for (int i = 0; i < 2 * I; ++i) Gr[i] = rbf16(Gr[i]);
+        }
+        free(buf);
+    }
+    if (dW2) {
+#pragma omp parallel for schedule(static)
+        for (int m = 0; m < d; ++m)
+            for (int i = 0; i < I; ++i) {
+                double acc = 0.0;
+                for (int r = 0; r < n_rows; ++r)
+                    acc += ld(dY, (size_t)row_tok[r] * d + m, bf) * H[(size_t)r * I + i];
+                dW2[(size_t)m * I + i] = acc;
+            }
+    }
+    if (dW13) {
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j < 2 * I; ++j)
+            for (int m = 0; m < d; ++m) {
+                double acc = 0.0;
+                for (int r = 0; r < n_rows; ++r)
+                    acc += G[(size_t)r * 2 * I + j] * ld(x, (size_t)row_tok[r] * d + m, bf);
+                dW13[(size_t)j * d + m] = acc;
+            }
+    }
+    free(G);
+    free(H);
+}
+
+/* Sampled entries of the same weight gradients (store_bf16 as above), each
+ * computed on its own from every row of expert e (for experts with many rows):
+ *   dW2[e][n][i]  = sum_r dy_r[n] w_r h_r[i]
+ *   dW13[e][j][m] = sum_r dgu_r[j] x_r[m]
+ * kind[q] = 0 for a dW2 entry (a = n, b = i), 1 for a dW13 entry (a = j, b = m). */
+void orc_expert_wgrad_entries(const void *x, const void *W13, const void *W2, const void *dY,
+                              int bf, int e, int n_rows, const int64_t *row_tok,
+                              const double *row_w, int d, int I, double c, int exact,
+                              int store_bf16, int nq, const int32_t *kind, const int32_t *qa,
+                              const int32_t *qb, double *out)
+{
+    size_t w13 = (size_t)e * 2 * I * d, w2 = (size_t)e * d * I;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < nq; ++q) {
+        int i = kind[q] == 0 ? qb[q] : (qa[q] % I);
+        double acc = 0.0;
+        for (int r = 0; r < n_rows; ++r) {
+            size_t t = (size_t)row_tok[r];
+            double gi = dot(x, t * d, W13, w13 + (size_t)i * d, d, bf);
+            double ui = dot(x, t * d, W13, w13 + (size_t)(I + i) * d, d, bf);
+            double a = gi < c ? gi : c;
+            double b = ui < -c ? -c : (ui > c ? c : ui);
+            double hi = silu(a) * b;
+            if (!exact) hi = rbf16(hi);
+            if (kind[q] == 0) {
+                double hw = row_w[r] * hi;
+                if (store_bf16) hw = rbf16(hw);
+                acc += ld(dY, t * d + qa[q], bf) * hw;
+            } else {
+                double dAi = 0.0;
+                for (int m = 0; m < d; ++m) dAi += ld(dY, t * d + m, bf) * ld(W2, w2 + (size_t)m * I + i, bf);
+                double dH = row_w[r] * dAi;
+                double gr = qa[q] < I ? (gi <= c ? dH * b * dsilu(a) : 0.0)
+                                      : ((ui >= -c && ui <= c) ? dH * silu(a) : 0.0);
+                if (store_bf16) gr = rbf16(gr);
+                acc += gr * ld(x, t * d + qb[q], bf);
+            }
+        }
+        out[q] = acc;
+    }
+}
