@@ -34,9 +34,9 @@ VISION_BLOCK = 576
 # Scale of the per-expert logit offsets that skew the expert load towards a
 # Zipf(1.1) rank-frequency law: offset[e] = -ZIPF_LAMBDA * s * ln(rank[e]).
 # Calibrated once with the oracle's routing on full-width synthetic inputs by
-# oracle/calibrate_zipf.py (least-squares slope of log count against log rank
+# `python -m oracle.calibrate_zipf` (least-squares slope of log count against log rank
 # over ranks 2..384 within 0.05 of -1.1).
-ZIPF_LAMBDA = 1.0
+ZIPF_LAMBDA = 0.4767
 
 
 @dataclass(frozen=True)

@@ -181,8 +181,9 @@ static void route_token(const double *zt, const float *bias, int vis, int mode,
                 if (taken[e]) continue;
                 double s = sigmoid(zt[e]);
                 if (!exact) s = r32(s);
-                double key = s + (double)bias[(size_t)vis * E + e];
-                if (!exact) key = r32(key);
+                float b = bias[(size_t)vis * E + e];
+                /* one fp32 round-to-nearest add of the fp32 score and bias */
+                double key = exact ? s + (double)b : (double)((float)s + b);
                 if (best < 0 || key > bk) { best = e; bk = key; }  /* strict: lowest id wins ties */
             }
             if (j > 0 && prev - bk < *margin) *margin = prev - bk;
