@@ -1,0 +1,426 @@
+"""Benchmark of the routed MoE layer on GB300: one JSON line on stdout.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one forward pass of the whole layer (gate projection + routing,
+dispatch, the two grouped expert GEMMs with the shared expert, combine) over
+one batch of the full-width workload (T=4096 tokens, d=4096, 384 routed
+experts top-6 + 1 shared, I=2048, bf16).  Inputs are seeded synthetic tensors
+made on the device; they are resident in HBM when the timed region starts.
+The forward+backward of the T=8192 workload is measured as well and reported
+under "fwd_bwd".  N > 1 runs N independent replicas (one per GPU), since the
+single-GPU layer has no exchange step: value = all ranks' tokens / max time.
+
+--impl reference times the CPU oracle (the plain fp64 implementation the
+tests compare against) on the host cores, on a bounded sample of tokens of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MoE layer tokens/s (fwd, fwd+bwd) at 1 GB300; grouped-GEMM % of BF16 tensor peak")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FWD_LAUNCHES = 9      # gate GEMM, route, hist, scan, scatter, gather, GEMM1, GEMM2, combine
+BWD_LAUNCHES = 9      # gather dY, dgrad2, wgrad2, dgrad1, wgrad1, router bwd, dX, dW_g (2)
+BWD_RECOMPUTE_EXTRA = 2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get(
+            "bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workloads
+
+def layer_inputs(wl, device, weights=None):
+    from moe_expert_layer_04_gb300 import workloads as W
+    inp = W.make_inputs(wl, device=device, with_weights=weights is None)
+    if weights is not None:
+        inp.update(weights)
+    return inp
+
+
+def fwd_algorithmic_bytes(D, counts):
+    """Minimum HBM bytes of the expert GEMMs for one forward: every expert
+    with at least one row streams its weights once; activations read/written
+    once (x_perm rows in, h out for GEMM 1; h in, y_perm out for GEMM 2)."""
+    used = int((counts > 0).sum()) + 1          # + the shared expert
+    w13 = used * 2 * D.I * D.d * 2
+    w2 = used * D.d * D.I * 2
+    g1 = w13 + D.R * D.d * 2 + D.R * D.I * 2
+    g2 = w2 + D.R * D.I * 2 + D.R * D.d * 2
+    return g1, g2
+
+
+def fwd_flops(D):
+    return 2 * D.T * D.d * D.E + 6 * D.R * D.d * D.I
+
+
+# ------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    hbm, bf16, bf16_sus, peak_src = peaks()
+
+    wl = W.WORKLOADS[args.workload]
+    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+    inp = layer_inputs(wl, dev)
+    weights = {k: inp[k] for k in ("W_g", "W13", "W2")}
+    layer = MoELayer(D, weights, wl.rho, wl.clamp)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        layer.route(inp["x"], inp["bias"], inp["is_vision"], inp["logit_offset"])
+        if evs is not None:
+            evs[1].record(stream)
+        layer.dispatch(inp["x"])
+        if evs is not None:
+            evs[2].record(stream)
+        layer.expert_gemm1()
+        if evs is not None:
+            evs[3].record(stream)
+        layer.expert_gemm2()
+        if evs is not None:
+            evs[4].record(stream)
+        layer.combine()
+        if evs is not None:
+            evs[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    counts = layer.counts.cpu().numpy()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    names = ["route", "permute", "expert_gemm1", "expert_gemm2", "combine"]
+    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
+           for j, n in enumerate(names)}
+    ms_step = ms / args.steps
+    value = world * D.T / (ms_step / 1e3)
+
+    g1_bytes, g2_bytes = fwd_algorithmic_bytes(D, counts)
+    g1_s = per["expert_gemm1"] / 1e3
+    achieved = g1_bytes / g1_s / 1e9
+    roofline = {"kernel": "expert_gemm1 (grouped GEMM 1 + clamped SwiGLU)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "peak_source": peak_src,
+                "bytes_per_launch": g1_bytes}
+    g1_flops = 4 * D.R * D.d * D.I
+    g2_flops = 2 * D.R * D.I * D.d
+    kernels = {n: {"ms": round(v, 4)} for n, v in per.items()}
+    kernels["expert_gemm1"].update(tflops=round(g1_flops / g1_s / 1e12, 1),
+                                   gbs=round(achieved, 1), hbm_frac=round(achieved / hbm, 4),
+                                   tensor_frac=round(g1_flops / g1_s / 1e12 / bf16, 4))
+    g2_s = per["expert_gemm2"] / 1e3
+    kernels["expert_gemm2"].update(tflops=round(g2_flops / g2_s / 1e12, 1),
+                                   gbs=round(g2_bytes / g2_s / 1e9, 1),
+                                   hbm_frac=round(g2_bytes / g2_s / 1e9 / hbm, 4),
+                                   tensor_frac=round(g2_flops / g2_s / 1e12 / bf16, 4))
+    perm_bytes = D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6
+    kernels["permute"]["gbs"] = round(perm_bytes / (per["permute"] / 1e3) / 1e9, 1)
+    comb_bytes = D.R * D.d * 2 + D.T * D.d * 2 + D.S * 4
+    kernels["combine"]["gbs"] = round(comb_bytes / (per["combine"] / 1e3) / 1e9, 1)
+    route_bytes = D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4 * 2 + D.T * D.k * 12
+    kernels["route"]["gbs"] = round(route_bytes / (per["route"] / 1e3) / 1e9, 1)
+    layer_roof_ms = max(fwd_flops(D) / (bf16 * 1e12),
+                        (g1_bytes + g2_bytes + perm_bytes + comb_bytes + route_bytes) / (hbm * 1e9)) * 1e3
+
+    # ---------------- end to end through the public API with host buffers
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(D.T, D.d, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    for _ in range(args.warmup):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, inp["bias"], inp["is_vision"], inp["logit_offset"])
+        y_host.copy_(layer.y, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, inp["bias"], inp["is_vision"], inp["logit_offset"])
+        y_host.copy_(layer.y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": round(world * D.T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": D.T * D.d * 2, "d2h_bytes_per_step": D.T * D.d * 2,
+           "ms_per_step": round(e2e_ms, 4)}
+    del layer, x_host, y_host, x_dev
+    torch.cuda.empty_cache()
+
+    # ---------------- forward + backward (T=8192 workload, same weights)
+    fb = None
+    if not args.no_bwd:
+        fb = run_fwd_bwd(args, weights, dev, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(inp, wl, args.cpu_tokens)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": {"workload": f"{wl.name}: forward, T={wl.T} d={wl.d} E={wl.E} routed top-{wl.k}"
+                               f" + 1 shared, I={wl.I}, scaling {wl.rho}, clamp {wl.clamp}",
+                   "global_batch": wl.T * world, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (19.3 GB of expert weights streamed per step)"},
+        "roofline": roofline,
+        "layer_roofline_ms": round(layer_roof_ms, 4),
+        "layer_roofline_frac": round(layer_roof_ms / ms_step, 4),
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": FWD_LAUNCHES * args.steps,
+        "clocks": clk,
+        "fwd_bwd": fb,
+    }
+    return line
+
+
+def run_fwd_bwd(args, weights, dev, world):
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+    wl = W.WORKLOADS["fwd_bwd"]
+    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+    inp = layer_inputs(wl, dev, weights=weights)
+    layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        layer.forward(inp["x"], inp["bias"], inp["is_vision"], inp["logit_offset"])
+        if ev is not None:
+            ev.record(stream)
+        layer.backward(inp["dY"])
+
+    steps = max(3, args.steps // 2)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts[0].record(stream)
+    for i in range(steps):
+        step(mids[i])
+        starts[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = starts[0].elapsed_time(starts[-1]) / steps
+    bwd_ms = sum(mids[i].elapsed_time(starts[i + 1]) for i in range(steps)) / steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    out = {"workload": f"{wl.name}: forward+backward, T={wl.T} d={wl.d} E={wl.E} top-{wl.k} "
+                       f"+ shared, I={wl.I}, fp32 weight grads",
+           "value": round(world * D.T / (ms / 1e3), 1), "unit": "tokens/s",
+           "ms_per_step": round(ms, 4), "bwd_ms": round(bwd_ms, 4), "steps": steps,
+           "gpu_launches": (FWD_LAUNCHES + BWD_LAUNCHES) * steps}
+    del layer, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+# -------------------------------------------------------------- oracle
+
+def cpu_baseline(inp, wl, n_tokens):
+    import oracle
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False))
+    oracle.build()
+    t = time.perf_counter()
+    oracle.layer_forward(host["x"], host["W_g"], host["W13"], host["W2"], host["bias"], wl.k,
+                         wl.rho, wl.clamp, is_vision=host["is_vision"],
+                         offset=host["logit_offset"], tok=tok)
+    dt = time.perf_counter() - t
+    return {"value": round(len(tok) / dt, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"forward of {len(tok)} seeded tokens of the {wl.name} workload "
+                      f"({dt:.1f} s, OpenMP over tokens)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample."""
+    import oracle
+    from moe_expert_layer_04_gb300 import workloads as W
+    if rank != 0:
+        return None
+    wl = W.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = layer_inputs(wl, dev)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    del inp
+    oracle.build()
+    n = args.ref_tokens
+    rng = np.random.default_rng(1)
+
+    def step():
+        tok = np.sort(rng.choice(wl.T, size=n, replace=False))
+        oracle.layer_forward(host["x"], host["W_g"], host["W13"], host["W2"], host["bias"], wl.k,
+                             wl.rho, wl.clamp, is_vision=host["is_vision"],
+                             offset=host["logit_offset"], tok=tok)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t) / args.steps
+    value = round(n / dt, 2)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: forward, T={wl.T} d={wl.d} E={wl.E} top-{wl.k} + "
+                               f"shared, I={wl.I}", "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: forward of {n} random tokens of the workload"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="full_fwd")
+    ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=128)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

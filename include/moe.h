@@ -1,0 +1,242 @@
+/*
+ * moe.h -- C ABI of the routed Mixture-of-Experts layer library (libmoe.so).
+ *
+ * One DeepSeek-V4-style MoE layer on one GPU: gate projection and routing,
+ * permutation of token slots into expert-contiguous rows, the two expert
+ * matmuls around a clamped SwiGLU, the weighted combine with the shared
+ * expert, and the backward of all of it.  Sources (page title, section):
+ *
+ *   [HP41] "HyperParallel加速DeepSeek-V4.1多模态1M长序列训练", §2.3 MegaKernel:
+ *          MegaGate (score, bias ranking, top-k, score extraction,
+ *          normalisation and scaling, separate text / vision routing bias,
+ *          fused backward of the normalisation chain; the projection matmul
+ *          is an ordinary GEMM) and MegaMoE (token dispatch, two expert
+ *          matmuls, SwiGLU with the V4.1 clamp, result return).
+ *   [HPF]  "MindSpore HyperParallel一键开箱DeepSeek-V4.1-Flash", §01: each MoE
+ *          layer has 1 shared and 384 routed experts, 6 active per token.
+ *   [TW]   "Twinkle x 昇腾，率先实现Deepseek-V4系列模型高效训练",
+ *          "FSDP2-4D并行引擎适配": TopKRouter returns router logits, routing
+ *          weights and selected experts; HashRouter looks experts up in
+ *          tid2eid[input_ids] and still weights them with the gate logits;
+ *          tokens are dispatched to experts, computed, returned and combined
+ *          by routing weight.
+ *
+ * Conventions for every call
+ *   - All pointers are DEVICE pointers unless marked [host].  The caller owns
+ *     and allocates every buffer, including the workspace; the library never
+ *     allocates and never frees.
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Every matrix is
+ *     row-major and densely packed; base pointers must be 16-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Outputs are overwritten, never accumulated.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failure returns MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED and launches
+ *     nothing.  A CUDA launch error returns MOE_ERR_CUDA.  Errors found on the
+ *     device (an out-of-range table entry, a bounded wait that ran out) are
+ *     recorded in a per-device status word read by moe_last_device_status();
+ *     kernels never trap.
+ *   - Sizes: T tokens, d hidden, E routed experts, k experts per token,
+ *     I expert intermediate size, S = T*k routed slots.  Supported: T >= 1,
+ *     d % 128 == 0, I % 64 == 0, 1 <= k <= min(E, 32), 1 <= E <= 1024,
+ *     (S + T) * max(d, 2I) < 2^31.
+ *
+ * Shared expert and row space.  The shared expert ([HPF] §01) is group E of
+ * the expert weights and runs on every token with weight 1.  Permuted row
+ * buffers have S + T rows: rows [0, S) are the routed slots in expert-major
+ * order, rows [S, S + T) are the tokens themselves in order (the shared
+ * expert's group).  offsets[] therefore has E + 2 entries with
+ * offsets[E] = S and offsets[E + 1] = S + T.
+ *
+ * Expert weights: W13 [E+1, 2I, d] (rows 0..I-1 of each group project to the
+ * gate g, rows I..2I-1 to the up value u), W2 [E+1, d, I], gate W_g [E, d].
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size or mode */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid but outside the supported shapes */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime or launch error */
+    MOE_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up */
+    MOE_ERR_WORKSPACE = 5     /* workspace missing or too small */
+} moe_status;
+
+typedef enum { MOE_ROUTE_TOPK = 0, MOE_ROUTE_HASH = 1 } moe_route_mode;
+
+/* Flags of moe_workspace_size / moe_backward. */
+#define MOE_FLAG_BACKWARD 1   /* size the workspace for moe_backward as well */
+#define MOE_FLAG_RECOMPUTE 2  /* backward rebuilds x_perm and g|u instead of reading them */
+
+/* Bytes of workspace that moe_permute, moe_expert_ffn and (with
+ * MOE_FLAG_BACKWARD) moe_backward need for these sizes.  One buffer of this
+ * size may be reused by every call of one layer; calls on one stream run in
+ * order, so reuse is safe.  Returns 0 for unsupported sizes. */
+size_t moe_workspace_size(int T, int d, int E, int k, int I, int flags);
+
+/* Gate projection and routing ([HP41] §2.3 MegaGate; [TW] TopKRouter and
+ * HashRouter).
+ *   logits[t,e] = sum_i x[t,i] W_g[e,i] + logit_offset[e]    fp32, fp32 accumulate
+ *   s           = sigmoid(logits)                           (score)
+ *   TOPK: key   = fp32(s + bias[m_t, e]), m_t = is_vision[t] ? 1 : 0
+ *         ids   = the k largest keys, descending, equal keys by lower id
+ *   HASH: ids   = tid2eid[input_ids[t]]  (bias unused)
+ *   scores_sel[t,j] = s at ids[t,j]       (unbiased score, fp32 = the sigmoid
+ *                                          evaluated in fp64 and rounded once)
+ *   weights[t,j]    = scaling * scores_sel[t,j] / sum_j scores_sel[t,j]
+ * Arguments
+ *   x [T,d] bf16, W_g [E,d] bf16; logit_offset [E] fp32 or NULL (a fixed
+ *   per-expert shift, no gradient); bias [2,E] fp32 (row 0 text, row 1
+ *   vision); is_vision [T] uint8 or NULL (all text); input_ids [T] int32 and
+ *   tid2eid [vocab,k] int32 for HASH (NULL / ignored for TOPK).
+ *   Outputs: logits [T,E] fp32 (kept for the backward), ids [T,k] int32,
+ *   weights [T,k] fp32, scores_sel [T,k] fp32.
+ *   An input id outside [0,vocab) or a table entry outside [0,E) is replaced
+ *   by 0 and recorded as MOE_ERR_INVALID_ARG in the device status word. */
+moe_status moe_route(const uint16_t *x, const uint16_t *W_g, const float *logit_offset,
+                     const float *bias, const uint8_t *is_vision, const int32_t *input_ids,
+                     const int32_t *tid2eid, int vocab, int T, int d, int E, int k,
+                     float scaling, moe_route_mode mode, float *logits, int32_t *ids,
+                     float *weights, float *scores_sel, void *stream);
+
+/* Routing only, from given logits (the MegaGate pipeline without the
+ * projection, [HP41] §2.3).  Same semantics and outputs as moe_route. */
+moe_status moe_route_logits(const float *logits, const float *bias, const uint8_t *is_vision,
+                            const int32_t *input_ids, const int32_t *tid2eid, int vocab, int T,
+                            int E, int k, float scaling, moe_route_mode mode, int32_t *ids,
+                            float *weights, float *scores_sel, void *stream);
+
+/* Token dispatch on one GPU ([HP41] §2.3 MegaMoE "token dispatch"; [TW]
+ * FSDP2-4D: selected experts become global expert ids of one dispatch).
+ * Stable expert-major permutation of the S = T*k slots (expert, then token,
+ * then slot), plus the shared expert's identity rows:
+ *   counts [E]        slots per routed expert
+ *   offsets [E+2]     first row of each group; offsets[E] = S, offsets[E+1] = S+T
+ *   row_token [S+T]   token of each row (rows >= S: row - S)
+ *   slot_row [S]      row of slot j of token t at index t*k + j
+ *   row_weight [S]    weights[t,j] moved to its row (NULL: not produced; needs
+ *                     weights [T,k] fp32)
+ *   x_perm [S+T, d]   x_perm[row] = x[row_token[row]] (NULL: indices only)
+ * ids [T,k] int32 must lie in [0,E) (out-of-range ids are recorded as
+ * MOE_ERR_INVALID_ARG on the device and their slots are left unwritten).
+ * Needs d % 8 == 0 when x_perm is given.
+ * Workspace: moe_workspace_size(T,d,E,k,I,0) bytes. */
+moe_status moe_permute(const int32_t *ids, const float *weights, const uint16_t *x, int T, int d,
+                       int E, int k, int32_t *counts, int32_t *offsets, int32_t *row_token,
+                       int32_t *slot_row, float *row_weight, uint16_t *x_perm, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* The expert FFN on expert-contiguous rows ([HP41] §2.3 MegaMoE: two expert
+ * matmuls around SwiGLU with clamp; [HPF] §01 shared expert as group E).
+ * For every group g < G and row r in [offsets[g], offsets[g+1]):
+ *   [g | u]  = x_perm[r] W13[g]^T                      (fp32 accumulate)
+ *   h[r]     = bf16( silu(min(g, clamp)) * clamp(u, -clamp, clamp) )
+ *   y[r]     = bf16( row_weight[r] * (h[r] W2[g]^T) )  (row_weight = 1 for r >= S
+ *                                                       or when NULL)
+ * Arguments: x_perm [R,d] bf16 with R = offsets[G]; offsets [G+1] int32
+ * (device; e.g. the E+2 offsets of moe_permute with G = E+1); W13 [G,2I,d],
+ * W2 [G,d,I] bf16; row_weight [S] fp32 or NULL; S = rows carrying a routing
+ * weight.  Outputs h_perm [R,I] bf16, y_perm [R,d] bf16, and gu_save [R,2I]
+ * fp32 (the GEMM-1 accumulators g then u, kept for the backward, which
+ * recomputes h from them bit for bit) when not NULL.  max_rows is an upper
+ * bound of R known on the host (sizes the launch; S + T for a full layer).
+ * Workspace: none is needed (ws may be NULL). */
+moe_status moe_expert_ffn(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                          const uint16_t *W13, const uint16_t *W2, const float *row_weight,
+                          int S, int d, int I, float clamp, float *gu_save,
+                          uint16_t *h_perm, uint16_t *y_perm, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* The two halves of moe_expert_ffn, for callers that schedule them apart.
+ * moe_expert_gemm1 writes h_perm (and gu_save when not NULL);
+ * moe_expert_gemm2 reads h_perm and writes y_perm.  Same arguments, layouts
+ * and rules as moe_expert_ffn. */
+moe_status moe_expert_gemm1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                            const uint16_t *W13, int d, int I, float clamp, float *gu_save,
+                            uint16_t *h_perm, void *stream);
+moe_status moe_expert_gemm2(const uint16_t *h_perm, const int32_t *offsets, int G, int max_rows,
+                            const uint16_t *W2, const float *row_weight, int S, int d, int I,
+                            uint16_t *y_perm, void *stream);
+
+/* Result return and weighted combine ([HP41] §2.3 MegaMoE "result return";
+ * [TW] combine by routing weight).  Gather form, no atomics, fixed order:
+ *   y[t] = bf16( y_perm[S + t] + sum_{j<k} y_perm[slot_row[t*k + j]] )   (fp32 sums)
+ * y_perm [S+T,d] bf16 already carries the routing weights; pass
+ * with_shared = 0 to leave out the shared rows. */
+moe_status moe_combine(const uint16_t *y_perm, const int32_t *slot_row, int T, int d, int k,
+                       int with_shared, uint16_t *y, void *stream);
+
+/* Everything moe_backward reads and writes.  Forward state is what the
+ * forward calls above returned. */
+typedef struct {
+    int T, d, E, k, I;
+    float scaling, clamp;
+    int flags;                    /* MOE_FLAG_RECOMPUTE or 0 */
+    /* forward inputs */
+    const uint16_t *x;            /* [T,d] */
+    const uint16_t *W_g;          /* [E,d] */
+    const uint16_t *W13;          /* [E+1,2I,d] */
+    const uint16_t *W2;           /* [E+1,d,I] */
+    /* saved forward state */
+    const int32_t *ids;           /* [T,k] */
+    const float *weights;         /* [T,k] */
+    const float *scores_sel;      /* [T,k] */
+    const float *row_weight;      /* [S] (moe_permute) */
+    const int32_t *offsets;       /* [E+2] */
+    const int32_t *row_token;     /* [S+T] */
+    const int32_t *slot_row;      /* [S] */
+    const uint16_t *x_perm;       /* [S+T,d]; ignored with MOE_FLAG_RECOMPUTE */
+    const float *gu_save;         /* [S+T,2I] fp32; ignored with MOE_FLAG_RECOMPUTE */
+    /* upstream gradient */
+    const uint16_t *dY;           /* [T,d] */
+    /* outputs (overwritten) */
+    uint16_t *dX;                 /* [T,d] bf16 */
+    float *dW_g;                  /* [E,d] fp32 */
+    float *dW13;                  /* [E+1,2I,d] fp32 */
+    float *dW2;                   /* [E+1,d,I] fp32 */
+    float *dlogits;               /* [T,E] fp32 or NULL (zero off the selection) */
+    float *dweights;              /* [T,k] fp32 or NULL (gradient of the routing weights) */
+    void *ws;                     /* moe_workspace_size(..., MOE_FLAG_BACKWARD | flags) bytes */
+    size_t ws_bytes;
+} moe_bwd_args;
+
+/* Backward of the whole layer (analytic chain rule of the forward above;
+ * [HP41] §2.3 names the fused backward of MegaGate's normalisation chain).
+ *   dY_perm[r] = dY[row_token[r]]
+ *   dA         = dY_perm W2[g]                 dw[r] = <h[r], dA>
+ *   dH = w dA;  dg = dH clamp(u) silu'(min(g,c)) [g <= c];  du = dH silu(min(g,c)) [|u| <= c]
+ *   dW2[g]  = sum_r dY_perm[r]^T (w h)[r]      dW13[g] = sum_r [dg|du][r]^T x_perm[r]
+ *   dX_perm = [dg|du] W13[g]
+ *   ds_j = (scaling/S_t)(dw_j - sum_i dw_i w_i / scaling),  dz_j = ds_j s_j (1 - s_j)
+ *   dX[t] = dX_perm[S+t] + sum_j dX_perm[slot_row[t,j]] + sum_j dz_j W_g[ids_j]
+ *   dW_g  = dz^T x
+ * The bias gets no gradient (it only ranks); hash routing has the same
+ * weight chain.  Clamp gradients pass where the argument equals the bound. */
+moe_status moe_backward(const moe_bwd_args *args, void *stream);
+
+/* Text of a status code (static storage). */
+const char *moe_status_string(moe_status s);
+
+/* Synchronises `stream`, returns the device status word of the current
+ * device (MOE_OK if no kernel recorded an error since the last call) and
+ * resets it. */
+moe_status moe_last_device_status(void *stream);
+
+/* Test hook for the bounded waits: launches one block whose mbarrier wait
+ * can never complete, with a limit of `limit_cycles` SM clock cycles; the
+ * kernel gives up, records MOE_ERR_TIMEOUT in the device status word and
+ * returns.  Nothing traps or hangs.  limit_cycles must be in (0, 2^31). */
+moe_status moe_selftest_wait_timeout(long long limit_cycles, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,277 @@
+"""Build, load and bind libmoe.so -- the C ABI of include/moe.h.
+
+The binding only marshals arguments: every function here takes torch tensors
+(or ints / floats), checks dtype, device and contiguity, and passes raw device
+pointers to the C entry point of the same name.  All arithmetic happens in the
+CUDA kernels behind the ABI; there is no fallback.  A missing or unbuildable
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(HERE, "_build")
+LIB_PATH = os.path.join(BUILD, "libmoe.so")
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
+    MOE_ERR_WORKSPACE = range(6)
+MOE_ROUTE_TOPK, MOE_ROUTE_HASH = 0, 1
+MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE = 1, 2
+
+EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_permute",
+           "moe_expert_ffn", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
+           "moe_last_device_status", "moe_selftest_wait_timeout"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: status {status} ({status_string(status)})")
+
+
+def _sources():
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+
+
+def _headers():
+    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    return hs + [os.path.join(INCLUDE, "moe.h")]
+
+
+def _nvcc():
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a (in parallel) and link libmoe.so."""
+    os.makedirs(BUILD, exist_ok=True)
+    srcs = _sources()
+    newest = max(os.path.getmtime(p) for p in srcs + _headers())
+    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
+        return LIB_PATH
+    nvcc = _nvcc()
+    flags = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+             "-Xptxas", "-v"] if verbose else [ARCH, "-O3", "-lineinfo", "-std=c++17",
+                                                "-Xcompiler", "-fPIC", "-I", INCLUDE]
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        r = subprocess.run([nvcc, *flags, "-c", src, "-o", obj], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        if verbose:
+            print(r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, ARCH, "-shared", "--cudart=static", "-o", tmp, *objs],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+_P, _I, _F, _Z, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, \
+    ctypes.c_longlong
+
+
+class BwdArgs(ctypes.Structure):
+    """Mirror of moe_bwd_args."""
+    _fields_ = [("T", _I), ("d", _I), ("E", _I), ("k", _I), ("I", _I),
+                ("scaling", _F), ("clamp", _F), ("flags", _I),
+                ("x", _P), ("W_g", _P), ("W13", _P), ("W2", _P),
+                ("ids", _P), ("weights", _P), ("scores_sel", _P), ("row_weight", _P),
+                ("offsets", _P), ("row_token", _P), ("slot_row", _P),
+                ("x_perm", _P), ("gu_save", _P), ("dY", _P),
+                ("dX", _P), ("dW_g", _P), ("dW13", _P), ("dW2", _P),
+                ("dlogits", _P), ("dweights", _P), ("ws", _P), ("ws_bytes", _Z)]
+
+
+_SIGS = {
+    "moe_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
+    "moe_route": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P],
+                  _I),
+    "moe_route_logits": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P], _I),
+    "moe_permute": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_expert_ffn": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_expert_gemm1": ([_P, _P, _I, _I, _P, _I, _I, _F, _P, _P, _P], _I),
+    "moe_expert_gemm2": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P], _I),
+    "moe_combine": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "moe_backward": ([ctypes.POINTER(BwdArgs), _P], _I),
+    "moe_status_string": ([_I], ctypes.c_char_p),
+    "moe_last_device_status": ([_P], _I),
+    "moe_selftest_wait_timeout": ([_LL, _P], _I),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) and bind the library."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or build()
+            lib = ctypes.CDLL(p)
+            for name, (args, res) in _SIGS.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def lib_path() -> str:
+    return LIB_PATH
+
+
+# ----------------------------------------------------------- marshalling
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, st):
+    if st != MOE_OK:
+        raise MoeError(fn, st)
+
+
+BF16, F32, I32, U8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def moe_workspace_size(T, d, E, k, I, flags=0) -> int:
+    return int(load().moe_workspace_size(T, d, E, k, I, flags))
+
+
+def moe_route(x, W_g, logit_offset, bias, is_vision, input_ids, tid2eid, T, d, E, k, scaling,
+              mode, logits, ids, weights, scores_sel, stream=None):
+    vocab = 0 if tid2eid is None else int(tid2eid.shape[0])
+    st = load().moe_route(_ptr(x, BF16, "x"), _ptr(W_g, BF16, "W_g"),
+                          _ptr(logit_offset, F32, "logit_offset"), _ptr(bias, F32, "bias"),
+                          _ptr(is_vision, U8, "is_vision"), _ptr(input_ids, I32, "input_ids"),
+                          _ptr(tid2eid, I32, "tid2eid"), vocab, T, d, E, k, float(scaling),
+                          int(mode), _ptr(logits, F32, "logits"), _ptr(ids, I32, "ids"),
+                          _ptr(weights, F32, "weights"), _ptr(scores_sel, F32, "scores_sel"),
+                          _stream(stream))
+    _check("moe_route", st)
+
+
+def moe_route_logits(logits, bias, is_vision, input_ids, tid2eid, T, E, k, scaling, mode, ids,
+                     weights, scores_sel, stream=None):
+    vocab = 0 if tid2eid is None else int(tid2eid.shape[0])
+    st = load().moe_route_logits(_ptr(logits, F32, "logits"), _ptr(bias, F32, "bias"),
+                                 _ptr(is_vision, U8, "is_vision"),
+                                 _ptr(input_ids, I32, "input_ids"), _ptr(tid2eid, I32, "tid2eid"),
+                                 vocab, T, E, k, float(scaling), int(mode),
+                                 _ptr(ids, I32, "ids"), _ptr(weights, F32, "weights"),
+                                 _ptr(scores_sel, F32, "scores_sel"), _stream(stream))
+    _check("moe_route_logits", st)
+
+
+def moe_permute(ids, weights, x, T, d, E, k, counts, offsets, row_token, slot_row, row_weight,
+                x_perm, ws, stream=None):
+    st = load().moe_permute(_ptr(ids, I32, "ids"), _ptr(weights, F32, "weights"),
+                            _ptr(x, BF16, "x"), T, d, E, k, _ptr(counts, I32, "counts"),
+                            _ptr(offsets, I32, "offsets"), _ptr(row_token, I32, "row_token"),
+                            _ptr(slot_row, I32, "slot_row"), _ptr(row_weight, F32, "row_weight"),
+                            _ptr(x_perm, BF16, "x_perm"), _ptr(ws, U8, "ws"),
+                            0 if ws is None else ws.numel(), _stream(stream))
+    _check("moe_permute", st)
+
+
+def moe_expert_ffn(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, gu_save,
+                   h_perm, y_perm, ws=None, stream=None):
+    st = load().moe_expert_ffn(_ptr(x_perm, BF16, "x_perm"), _ptr(offsets, I32, "offsets"), G,
+                               max_rows, _ptr(W13, BF16, "W13"), _ptr(W2, BF16, "W2"),
+                               _ptr(row_weight, F32, "row_weight"), S, d, I, float(clamp),
+                               _ptr(gu_save, F32, "gu_save"), _ptr(h_perm, BF16, "h_perm"),
+                               _ptr(y_perm, BF16, "y_perm"), _ptr(ws, U8, "ws"),
+                               0 if ws is None else ws.numel(), _stream(stream))
+    _check("moe_expert_ffn", st)
+
+
+def moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm,
+                     stream=None):
+    st = load().moe_expert_gemm1(_ptr(x_perm, BF16, "x_perm"), _ptr(offsets, I32, "offsets"), G,
+                                 max_rows, _ptr(W13, BF16, "W13"), d, I, float(clamp),
+                                 _ptr(gu_save, F32, "gu_save"), _ptr(h_perm, BF16, "h_perm"),
+                                 _stream(stream))
+    _check("moe_expert_gemm1", st)
+
+
+def moe_expert_gemm2(h_perm, offsets, G, max_rows, W2, row_weight, S, d, I, y_perm, stream=None):
+    st = load().moe_expert_gemm2(_ptr(h_perm, BF16, "h_perm"), _ptr(offsets, I32, "offsets"), G,
+                                 max_rows, _ptr(W2, BF16, "W2"), _ptr(row_weight, F32, "row_weight"),
+                                 S, d, I, _ptr(y_perm, BF16, "y_perm"), _stream(stream))
+    _check("moe_expert_gemm2", st)
+
+
+def moe_combine(y_perm, slot_row, T, d, k, with_shared, y, stream=None):
+    st = load().moe_combine(_ptr(y_perm, BF16, "y_perm"), _ptr(slot_row, I32, "slot_row"), T, d,
+                            k, int(with_shared), _ptr(y, BF16, "y"), _stream(stream))
+    _check("moe_combine", st)
+
+
+def moe_backward(args: dict, stream=None):
+    """args: the fields of moe_bwd_args (tensors for pointers)."""
+    a = BwdArgs()
+    types = dict(x=BF16, W_g=BF16, W13=BF16, W2=BF16, ids=I32, weights=F32, scores_sel=F32,
+                 row_weight=F32, offsets=I32, row_token=I32, slot_row=I32, x_perm=BF16,
+                 gu_save=F32, dY=BF16, dX=BF16, dW_g=F32, dW13=F32, dW2=F32, dlogits=F32,
+                 dweights=F32, ws=U8)
+    for name, _ in BwdArgs._fields_:
+        if name == "ws_bytes":
+            continue
+        v = args.get(name)
+        if name in types:
+            setattr(a, name, _ptr(v, types[name], name))
+        else:
+            setattr(a, name, v)
+    a.ws_bytes = 0 if args.get("ws") is None else args["ws"].numel()
+    st = load().moe_backward(ctypes.byref(a), _stream(stream))
+    _check("moe_backward", st)
+
+
+def moe_last_device_status(stream=None) -> int:
+    return int(load().moe_last_device_status(_stream(stream)))
+
+
+def moe_selftest_wait_timeout(limit_cycles, stream=None):
+    st = load().moe_selftest_wait_timeout(int(limit_cycles), _stream(stream))
+    _check("moe_selftest_wait_timeout", st)

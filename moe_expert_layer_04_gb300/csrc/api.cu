@@ -1,0 +1,387 @@
+// api.cu -- the C ABI of libmoe (declared in include/moe.h): argument
+// validation, workspace carving, the device status word, tensor-map
+// encoding, and the order of kernel launches of each entry point.
+#include <cstring>
+#include <mutex>
+
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+// implemented in the other translation units
+moe_status route_from_logits(const float *logits, const float *bias, const uint8_t *is_vision,
+                             const int32_t *input_ids, const int32_t *tid2eid, int vocab, int T,
+                             int E, int k, float scaling, moe_route_mode mode, int32_t *ids,
+                             float *weights, float *scores_sel, cudaStream_t st);
+size_t permute_workspace_bytes(int T, int E, int k);
+moe_status launch_permute(const int32_t *ids, const float *weights, const uint16_t *x, int T,
+                          int d, int E, int k, int32_t *counts, int32_t *offsets,
+                          int32_t *row_token, int32_t *slot_row, float *row_weight,
+                          uint16_t *x_perm, void *ws, cudaStream_t st);
+size_t dwg_workspace_bytes(int d, int E);
+moe_status launch_combine(const uint16_t *y_perm, const int32_t *slot_row, int T, int d, int k,
+                          int with_shared, const float *dz, const int32_t *ids,
+                          const uint16_t *Wg, uint16_t *y, cudaStream_t st);
+moe_status launch_router_bwd(const float *dw_part, int n_part, const int32_t *slot_row,
+                             const int32_t *ids, const float *weights, const float *ssel, int T,
+                             int E, int k, float scaling, float *dz_sel, float *dz_row,
+                             float *dlogits, float *dweights, cudaStream_t st);
+moe_status launch_dwg(const uint16_t *x_perm, const float *dz_row, const int32_t *offsets, int d,
+                      int E, float *part, float *dWg, cudaStream_t st);
+
+namespace {
+
+__device__ int g_status;  // the per-device status word
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_status_ptr[kMaxDevices];
+int g_sms[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+__global__ void wait_timeout_kernel(long long limit, int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing ever arrives on `bar`: the wait must give up on its own
+        const WaitCtl wc{&abort_flag, status, limit};
+        mbar_wait(&bar, 0, wc);
+    }
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct BwdWorkspace {
+    uint16_t *dY_perm, *dGU, *hw, *dX_perm, *x_perm;
+    float *gu, *dw_part, *dz_sel, *dz_row, *dwg_part;
+    size_t bytes;
+};
+
+BwdWorkspace carve_bwd(uint8_t *base, int T, int d, int E, int k, int I, int flags) {
+    BwdWorkspace w;
+    std::memset(&w, 0, sizeof w);
+    const size_t R = (size_t)T * k + T;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    w.dY_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
+    w.dGU = reinterpret_cast<uint16_t *>(take(R * 2 * I * 2));
+    w.hw = reinterpret_cast<uint16_t *>(take(R * I * 2));
+    w.dX_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
+    w.dw_part = reinterpret_cast<float *>(take(R * dgrad2_n_tiles(I) * 4));
+    w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
+    w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
+    w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
+    if (flags & MOE_FLAG_RECOMPUTE) {
+        w.x_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
+        w.gu = reinterpret_cast<float *>(take(R * 2 * I * 4));
+    }
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace
+
+int *device_status_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+bool encode_tmap_bf16_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return false;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+    }
+    if (!aligned16(base) || (row_pitch_bytes & 15u) != 0 || inner == 0 || outer == 0) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status check_shapes(int T, int d, int E, int k, int I) {
+    if (T < 1 || d < 1 || E < 1 || k < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+    if (k > E) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
+    if (d % 128 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    const long long R = (long long)T * k + T;
+    const long long wide = d > 2 * I ? d : 2 * I;
+    if (R * wide >= (1LL << 31) || R >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status launch_selftest_timeout(long long limit, cudaStream_t st) {
+    int *status = device_status_ptr();
+    if (!status) return MOE_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, st>>>(limit, status);
+    return cuda_status(cudaGetLastError());
+}
+
+moe_status check_ffn(int G, int max_rows, int d, int I, int S) {
+    if (G < 1 || G > 1025 || max_rows < 1 || d < 1 || I < 1 || S < 0) return MOE_ERR_INVALID_ARG;
+    if (d % 128 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)max_rows * (d > 2 * I ? d : 2 * I) >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(int T, int d, int E, int k, int I, int flags) {
+    if (check_shapes(T, d, E, k, I) != MOE_OK) return 0;
+    size_t b = permute_workspace_bytes(T, E, k);
+    if (flags & MOE_FLAG_BACKWARD) {
+        const size_t bw = carve_bwd(nullptr, T, d, E, k, I, flags).bytes;
+        if (bw > b) b = bw;
+    }
+    return b;
+}
+
+moe_status moe_route_logits(const float *logits, const float *bias, const uint8_t *is_vision,
+                            const int32_t *input_ids, const int32_t *tid2eid, int vocab, int T,
+                            int E, int k, float scaling, moe_route_mode mode, int32_t *ids,
+                            float *weights, float *scores_sel, void *stream) {
+    if (T < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
+    if (!logits || !ids || !weights || !scores_sel) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_ROUTE_TOPK) {
+        if (!bias) return MOE_ERR_INVALID_ARG;
+    } else if (mode == MOE_ROUTE_HASH) {
+        if (!input_ids || !tid2eid || vocab < 1) return MOE_ERR_INVALID_ARG;
+    } else {
+        return MOE_ERR_INVALID_ARG;
+    }
+    return route_from_logits(logits, bias, is_vision, input_ids, tid2eid, vocab, T, E, k,
+                             scaling, mode, ids, weights, scores_sel,
+                             static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route(const uint16_t *x, const uint16_t *W_g, const float *logit_offset,
+                     const float *bias, const uint8_t *is_vision, const int32_t *input_ids,
+                     const int32_t *tid2eid, int vocab, int T, int d, int E, int k,
+                     float scaling, moe_route_mode mode, float *logits, int32_t *ids,
+                     float *weights, float *scores_sel, void *stream) {
+    if (T < 1 || d < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+    if (d % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!x || !W_g || !logits || !aligned16(x) || !aligned16(W_g) || !aligned16(logits))
+        return MOE_ERR_INVALID_ARG;
+    if (mode != MOE_ROUTE_TOPK && mode != MOE_ROUTE_HASH) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_ROUTE_TOPK && !bias) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_ROUTE_HASH && (!input_ids || !tid2eid || vocab < 1)) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
+    if (!ids || !weights || !scores_sel) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    moe_status s = launch_gate_gemm(x, W_g, logit_offset, T, d, E, logits, st);
+    if (s != MOE_OK) return s;
+    return route_from_logits(logits, bias, is_vision, input_ids, tid2eid, vocab, T, E, k,
+                             scaling, mode, ids, weights, scores_sel, st);
+}
+
+moe_status moe_permute(const int32_t *ids, const float *weights, const uint16_t *x, int T, int d,
+                       int E, int k, int32_t *counts, int32_t *offsets, int32_t *row_token,
+                       int32_t *slot_row, float *row_weight, uint16_t *x_perm, void *ws,
+                       size_t ws_bytes, void *stream) {
+    if (T < 1 || E < 1 || k < 1 || k > E || d < 1) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || E > 1024 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)T * k + T >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!ids || !counts || !offsets || !row_token || !slot_row) return MOE_ERR_INVALID_ARG;
+    if (row_weight && !weights) return MOE_ERR_INVALID_ARG;
+    if (x_perm && (!x || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < permute_workspace_bytes(T, E, k)) return MOE_ERR_WORKSPACE;
+    return launch_permute(ids, weights, x, T, d, E, k, counts, offsets, row_token, slot_row,
+                          row_weight, x_perm, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                          const uint16_t *W13, const uint16_t *W2, const float *row_weight,
+                          int S, int d, int I, float clamp, float *gu_save,
+                          uint16_t *h_perm, uint16_t *y_perm, void *ws, size_t ws_bytes,
+                          void *stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!W2 || !y_perm || !aligned16(W2) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+    moe_status s = check_ffn(G, max_rows, d, I, S);
+    if (s != MOE_OK) return s;
+    s = moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm, stream);
+    if (s != MOE_OK) return s;
+    return moe_expert_gemm2(h_perm, offsets, G, max_rows, W2, row_weight, S, d, I, y_perm, stream);
+}
+
+moe_status moe_expert_gemm1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                            const uint16_t *W13, int d, int I, float clamp, float *gu_save,
+                            uint16_t *h_perm, void *stream) {
+    moe_status s = check_ffn(G, max_rows, d, I, 0);
+    if (s != MOE_OK) return s;
+    if (!x_perm || !offsets || !W13 || !h_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(W13) || !aligned16(h_perm) ||
+        (gu_save && !aligned16(gu_save)))
+        return MOE_ERR_INVALID_ARG;
+    if (!(clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    return launch_ffn1(x_perm, offsets, G, max_rows, W13, d, I, clamp, h_perm, gu_save,
+                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_gemm2(const uint16_t *h_perm, const int32_t *offsets, int G, int max_rows,
+                            const uint16_t *W2, const float *row_weight, int S, int d, int I,
+                            uint16_t *y_perm, void *stream) {
+    moe_status s = check_ffn(G, max_rows, d, I, S);
+    if (s != MOE_OK) return s;
+    if (!h_perm || !offsets || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(h_perm) || !aligned16(W2) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+    return launch_ffn2(h_perm, offsets, G, max_rows, W2, row_weight, S, d, I, y_perm,
+                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const uint16_t *y_perm, const int32_t *slot_row, int T, int d, int k,
+                       int with_shared, uint16_t *y, void *stream) {
+    if (T < 1 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!y_perm || !slot_row || !y || !aligned16(y_perm) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    return launch_combine(y_perm, slot_row, T, d, k, with_shared, nullptr, nullptr, nullptr, y,
+                          static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_backward(const moe_bwd_args *a, void *stream) {
+    if (!a) return MOE_ERR_INVALID_ARG;
+    const int T = a->T, d = a->d, E = a->E, k = a->k, I = a->I;
+    moe_status s = check_shapes(T, d, E, k, I);
+    if (s != MOE_OK) return s;
+    const bool rec = (a->flags & MOE_FLAG_RECOMPUTE) != 0;
+    if ((a->flags & ~MOE_FLAG_RECOMPUTE) != 0) return MOE_ERR_INVALID_ARG;
+    if (!a->x || !a->W_g || !a->W13 || !a->W2 || !a->ids || !a->weights || !a->scores_sel ||
+        !a->row_weight || !a->offsets || !a->row_token || !a->slot_row || !a->dY || !a->dX ||
+        !a->dW_g || !a->dW13 || !a->dW2)
+        return MOE_ERR_INVALID_ARG;
+    if (!rec && (!a->x_perm || !a->gu_save)) return MOE_ERR_INVALID_ARG;
+    const void *al[] = {a->x, a->W_g, a->W13, a->W2, a->dY, a->dX, a->dW_g, a->dW13, a->dW2};
+    for (const void *p : al)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!rec && (!aligned16(a->x_perm) || !aligned16(a->gu_save))) return MOE_ERR_INVALID_ARG;
+    if (!(a->clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    const int flags = MOE_FLAG_BACKWARD | (rec ? MOE_FLAG_RECOMPUTE : 0);
+    if (!a->ws || a->ws_bytes < moe_workspace_size(T, d, E, k, I, flags)) return MOE_ERR_WORKSPACE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BwdWorkspace w = carve_bwd(static_cast<uint8_t *>(a->ws), T, d, E, k, I, a->flags);
+    const int S = T * k;
+    const int R = S + T;
+    const int G = E + 1;
+    const uint16_t *x_perm = a->x_perm;
+    const float *gu = a->gu_save;
+    if (rec) {
+        // rebuild the permuted input rows and the expert GEMM-1 outputs
+        if ((s = launch_gather_rows(a->x, a->slot_row, T, d, k, w.x_perm, st)) != MOE_OK) return s;
+        if ((s = launch_ffn1(w.x_perm, a->offsets, G, R, a->W13, d, I, a->clamp, nullptr, w.gu,
+                             st)) != MOE_OK)
+            return s;
+        x_perm = w.x_perm;
+        gu = w.gu;
+    }
+    int n_part = 0;
+    if ((s = launch_gather_rows(a->dY, a->slot_row, T, d, k, w.dY_perm, st)) != MOE_OK) return s;
+    if ((s = launch_dgrad2(w.dY_perm, a->offsets, G, R, a->W2, gu, a->row_weight, S, d, I,
+                           a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
+        return s;
+    if ((s = launch_wgrad(w.dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, st)) != MOE_OK) return s;
+    if ((s = launch_dgrad1(w.dGU, a->offsets, G, R, a->W13, d, I, w.dX_perm, st)) != MOE_OK)
+        return s;
+    if ((s = launch_wgrad(w.dGU, 2 * I, x_perm, d, a->offsets, G, R, a->dW13, st)) != MOE_OK)
+        return s;
+    if ((s = launch_router_bwd(w.dw_part, n_part, a->slot_row, a->ids, a->weights, a->scores_sel,
+                               T, E, k, a->scaling, w.dz_sel, w.dz_row, a->dlogits, a->dweights,
+                               st)) != MOE_OK)
+        return s;
+    if ((s = launch_combine(w.dX_perm, a->slot_row, T, d, k, 1, w.dz_sel, a->ids, a->W_g, a->dX,
+                            st)) != MOE_OK)
+        return s;
+    return launch_dwg(x_perm, w.dz_row, a->offsets, d, E, w.dwg_part, a->dW_g, st);
+}
+
+const char *moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+moe_status moe_last_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    int *p = device_status_ptr();
+    if (!p) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return static_cast<moe_status>(v);
+}
+
+moe_status moe_selftest_wait_timeout(long long limit_cycles, void *stream) {
+    if (limit_cycles <= 0 || limit_cycles >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+    return launch_selftest_timeout(limit_cycles, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// gemm_bwd.cu -- backward matmuls of the expert FFN (chain rule of the two
+// expert matmuls and the clamped SwiGLU of "HyperParallel加速DeepSeek-V4.1
+// 多模态1M长序列训练" §2.3 MegaMoE):
+//   dgrad 2   dA = dY_perm W2[g]; epilogue: dw = <h, dA>, dH = w dA,
+//             dg = dH clamp(u) silu'(min(g,c)) [g <= c], du = dH silu(min(g,c)) [|u| <= c],
+//             w h (the wgrad-2 operand)
+//   dgrad 1   dX_perm = [dg|du] W13[g]
+//   wgrad     dW2[g] = dY_perm_g^T (w h)_g,  dW13[g] = [dg|du]_g^T x_perm_g
+//             (contraction over each expert's own rows)
+#include <cstring>
+
+#include "gemm_launch.cuh"
+
+namespace moe {
+
+int dgrad2_n_tiles(int I) { return (I % 128 == 0) ? I / 128 : I / 64; }
+
+moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G, int max_rows,
+                         const uint16_t *W2, const float *gu, const float *row_w, int S,
+                         int d, int I, float clamp, uint16_t *dGU, uint16_t *hw, float *dw_part,
+                         int *dw_tiles, cudaStream_t st) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    const int BN = (I % 128 == 0) ? 128 : 64;
+    if (!encode_tmap_bf16_2d(&p.tmA, dY_perm, d, max_rows, (uint64_t)d * 2, 64, 128))
+        return MOE_ERR_CUDA;
+    // W2 as [G*d rows (contraction), I columns (output)], MN-major boxes
+    if (!encode_tmap_bf16_2d(&p.tmB, W2, I, (uint64_t)G * d, (uint64_t)I * 2, 64, 64))
+        return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.n_tiles = I / BN;
+    p.k_blocks = d / 64;
+    p.b_rows_per_group = d;
+    p.I = I;
+    p.clamp = clamp;
+    p.out2 = dGU;
+    p.out3 = hw;
+    p.out4 = dw_part;
+    p.row_w = row_w;
+    p.w_rows = S;
+    p.gu_in = gu;
+    if (dw_tiles) *dw_tiles = p.n_tiles;
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return BN == 128 ? launch_gemm<GM_DGRAD2, 128>(p, tiles, st)
+                     : launch_gemm<GM_DGRAD2, 64>(p, tiles, st);
+}
+
+moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int max_rows,
+                         const uint16_t *W13, int d, int I, uint16_t *dX_perm, cudaStream_t st) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    const int BN = (d % 256 == 0) ? 256 : 128;
+    if (!encode_tmap_bf16_2d(&p.tmA, dGU, 2 * I, max_rows, (uint64_t)4 * I, 64, 128))
+        return MOE_ERR_CUDA;
+    // W13 as [G*2I rows (contraction), d columns (output)], MN-major boxes
+    if (!encode_tmap_bf16_2d(&p.tmB, W13, d, (uint64_t)G * 2 * I, (uint64_t)d * 2, 64, 64))
+        return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.n_tiles = d / BN;
+    p.k_blocks = 2 * I / 64;
+    p.N = d;
+    p.b_rows_per_group = 2 * I;
+    p.out = dX_perm;
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return BN == 256 ? launch_gemm<GM_DGRAD1, 256>(p, tiles, st)
+                     : launch_gemm<GM_DGRAD1, 128>(p, tiles, st);
+}
+
+moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, const int32_t *offsets,
+                        int G, int R, float *dW, cudaStream_t st) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    if (M % 128 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    const int BN = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
+    if (!encode_tmap_bf16_2d(&p.tmA, A, M, R, (uint64_t)M * 2, 64, 64)) return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d(&p.tmB, B, N, R, (uint64_t)N * 2, 64, 64)) return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.m_tiles = M / 128;
+    p.n_tiles = N / BN;
+    p.N = N;
+    p.M = M;
+    p.out = dW;
+    const int tiles = G * p.m_tiles * p.n_tiles;
+    switch (BN) {
+        case 256: return launch_gemm<GM_WGRAD, 256>(p, tiles, st);
+        case 128: return launch_gemm<GM_WGRAD, 128>(p, tiles, st);
+        default: return launch_gemm<GM_WGRAD, 64>(p, tiles, st);
+    }
+}
+
+}  // namespace moe

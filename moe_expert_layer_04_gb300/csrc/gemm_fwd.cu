@@ -1,0 +1,80 @@
+// gemm_fwd.cu -- forward matmuls: gate projection and the two expert GEMMs.
+//
+//   gate projection  logits = x W_g^T (+ offset)   ("HyperParallel加速DeepSeek-V4.1
+//                    多模态1M长序列训练" §2.3, MegaGate: the projection stays an
+//                    ordinary matmul ahead of the routing pipeline)
+//   expert GEMM 1    [g|u] = x_perm W13[g]^T, h = silu(min(g,c)) clamp(u,-c,c)
+//   expert GEMM 2    y = w * (h W2[g]^T)          (same page, §2.3 MegaMoE: two
+//                    expert matmuls around SwiGLU with the V4.1 clamp)
+#include <cstring>
+
+#include "gemm_launch.cuh"
+
+namespace moe {
+
+moe_status launch_gate_gemm(const uint16_t *x, const uint16_t *Wg, const float *offset, int T,
+                            int d, int E, float *logits, cudaStream_t st) {
+    constexpr int BN = 64;
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!encode_tmap_bf16_2d(&p.tmA, x, d, T, (uint64_t)d * 2, 64, 128)) return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d(&p.tmB, Wg, d, E, (uint64_t)d * 2, 64, BN)) return MOE_ERR_CUDA;
+    p.G = 1;
+    p.rows = T;
+    p.n_tiles = (E + BN - 1) / BN;
+    p.k_blocks = d / 64;
+    p.N = E;
+    p.out = logits;
+    p.col_add = offset;
+    return launch_gemm<GM_GATE, BN>(p, ((T + 127) / 128) * p.n_tiles, st);
+}
+
+moe_status launch_ffn1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                       const uint16_t *W13, int d, int I, float clamp, uint16_t *h,
+                       float *gu_save, cudaStream_t st) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    const int BN = (I % 128 == 0) ? 256 : 128;
+    if (!encode_tmap_bf16_2d(&p.tmA, x_perm, d, max_rows, (uint64_t)d * 2, 64, 128))
+        return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d(&p.tmB, W13, d, (uint64_t)G * 2 * I, (uint64_t)d * 2, 64, BN / 2))
+        return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.n_tiles = I / (BN / 2);
+    p.k_blocks = d / 64;
+    p.b_rows_per_group = 2 * I;
+    p.I = I;
+    p.clamp = clamp;
+    p.out = h;
+    p.out2 = gu_save;
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return BN == 256 ? launch_gemm<GM_FFN1, 256>(p, tiles, st)
+                     : launch_gemm<GM_FFN1, 128>(p, tiles, st);
+}
+
+moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max_rows,
+                       const uint16_t *W2, const float *row_w, int S, int d, int I, uint16_t *y,
+                       cudaStream_t st) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    const int BN = (d % 256 == 0) ? 256 : 128;
+    if (!encode_tmap_bf16_2d(&p.tmA, h, I, max_rows, (uint64_t)I * 2, 64, 128))
+        return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d(&p.tmB, W2, I, (uint64_t)G * d, (uint64_t)I * 2, 64, BN))
+        return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.n_tiles = d / BN;
+    p.k_blocks = I / 64;
+    p.N = d;
+    p.b_rows_per_group = d;
+    p.out = y;
+    p.row_w = row_w;
+    p.w_rows = S;
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return BN == 256 ? launch_gemm<GM_FFN2, 256>(p, tiles, st)
+                     : launch_gemm<GM_FFN2, 128>(p, tiles, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,525 @@
+// gemm_kernel.cuh -- persistent tcgen05 grouped GEMM for the expert matmuls.
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA producer (one elected thread): A and B tiles of 64 K
+//               elements per stage into 128-byte-swizzled shared memory.
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma (M = 128, N = BN,
+//               K = 16) from shared-memory descriptors into a fp32
+//               accumulator in TMEM; two accumulators so that the epilogue of
+//               one tile overlaps the main loop of the next.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = row),
+//               mode-specific arithmetic, direct global stores.
+//
+// Tiles are 128 rows x BN columns.  Three tile spaces:
+//   dense        (GM_GATE)   rows of A in order;
+//   row-grouped  (FFN1/FFN2/DGRAD2/DGRAD1) rows of A partitioned into groups
+//                by offsets[]; each group's rows are tiled by 128 (the last
+//                tile of a group is ragged and masked at the store), and the
+//                group selects its expert's weights;
+//   K-grouped    (GM_WGRAD) the contraction runs over each group's rows
+//                (ragged K, zero rows -> zero output), output [G, M, N].
+// Tiles are handed out round-robin (tile = blockIdx.x + i * gridDim.x), so
+// the schedule is static and the results are deterministic.
+//
+// Every wait is bounded (moe_ptx.cuh): on a timeout the CTA records
+// MOE_ERR_TIMEOUT, drains its own TMA copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+constexpr int kStageBudget = 192 * 1024;
+constexpr int kGemmThreads = 192;
+
+struct GemmParams {
+    CUtensorMap tmA;
+    CUtensorMap tmB;
+    const int32_t *offsets;  // [G+1] group row offsets (grouped modes)
+    int G;
+    int rows;                // GM_GATE: rows of A
+    int n_tiles;             // column tiles per row tile
+    int m_tiles;             // GM_WGRAD: M / 128
+    int k_blocks;            // fixed-K modes: K / 64
+    int N;                   // output columns (row pitch of the main output)
+    int M;                   // GM_WGRAD: output rows per group
+    int b_rows_per_group;    // rows of the flat weight matrix per group
+    int I;                   // intermediate size (FFN1 / DGRAD2)
+    float clamp;
+    void *out;               // main output
+    void *out2;              // FFN1: fp32 g|u save (nullable); DGRAD2: dGU
+    void *out3;              // DGRAD2: w h
+    float *out4;             // DGRAD2: dw partials [rows, n_tiles]
+    const float *row_w;      // FFN2 / DGRAD2 routing weight of rows < w_rows
+    int w_rows;
+    const float *gu_in;      // DGRAD2: saved fp32 g|u [rows, 2I]
+    const float *col_add;    // GM_GATE: per-column offset (nullable)
+    int *status;
+    long long wait_limit;
+};
+
+template <int MODE>
+struct ModeTraits {
+    static constexpr bool A_MN = (MODE == GM_WGRAD);
+    static constexpr bool B_MN = (MODE == GM_DGRAD2 || MODE == GM_DGRAD1 || MODE == GM_WGRAD);
+    static constexpr bool DENSE = (MODE == GM_GATE);
+    static constexpr bool KGROUP = (MODE == GM_WGRAD);
+    static constexpr bool ROWGROUP = !DENSE && !KGROUP;
+};
+
+template <int BN>
+struct TileShape {
+    static constexpr int A_BYTES = 128 * 64 * 2;
+    static constexpr int B_BYTES = BN * 64 * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = kStageBudget / STAGE_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {64, 128, 256}: a power of two
+};
+
+// Dynamic shared memory of one CTA for G groups.
+template <int BN>
+inline size_t gemm_smem_bytes(int G) {
+    using TS = TileShape<BN>;
+    return 1024 + (size_t)TS::STAGES * TS::STAGE_BYTES + 256 + 8 * (size_t)(G + 2);
+}
+
+struct TileInfo {
+    int g;           // group
+    int row0;        // first output / A row (row modes), 0 otherwise
+    int rows_valid;  // rows of the tile that exist (row modes)
+    int nt;          // column tile
+    int m0;          // GM_WGRAD: first output row inside the group
+    int krow0;       // GM_WGRAD: first contraction row
+    int krows;       // GM_WGRAD: contraction rows
+    int kb;          // k blocks of 64
+};
+
+template <int MODE, int BN>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, const int *mt_start,
+                                                const int *offs) {
+    using MT = ModeTraits<MODE>;
+    TileInfo ti;
+    ti.nt = t % p.n_tiles;
+    const int q = t / p.n_tiles;
+    ti.m0 = 0;
+    ti.krow0 = 0;
+    ti.krows = 0;
+    if constexpr (MT::DENSE) {
+        ti.g = 0;
+        ti.row0 = q * 128;
+        ti.rows_valid = min(128, p.rows - ti.row0);
+        ti.kb = p.k_blocks;
+    } else if constexpr (MT::ROWGROUP) {
+        int lo = 0, hi = p.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (mt_start[mid] <= q) lo = mid; else hi = mid - 1;
+        }
+        ti.g = lo;
+        ti.row0 = offs[lo] + (q - mt_start[lo]) * 128;
+        ti.rows_valid = min(128, offs[lo + 1] - ti.row0);
+        ti.kb = p.k_blocks;
+    } else {
+        ti.g = q / p.m_tiles;
+        ti.m0 = (q % p.m_tiles) * 128;
+        ti.row0 = 0;
+        ti.rows_valid = 128;
+        ti.krow0 = offs[ti.g];
+        ti.krows = max(0, offs[ti.g + 1] - ti.krow0);
+        ti.kb = (ti.krows + 63) >> 6;
+    }
+    return ti;
+}
+
+__device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
+    const float a = fminf(g, c);
+    const float b = fminf(fmaxf(u, -c), c);
+    return a / (1.0f + expf(-a)) * b;
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using MT = ModeTraits<MODE>;
+    using TS = TileShape<BN>;
+    constexpr int STAGES = TS::STAGES;
+    constexpr uint32_t IDESC = idesc_bf16_f32(128, BN, MT::A_MN, MT::B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * TS::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * TS::B_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *done = tempty + 2;
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
+    int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + 256);
+    int *mt_start = offs + (p.G + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(done, 1);
+        *abort_s = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tmA);
+        tma_prefetch_desc(&p.tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_base_s, TS::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if constexpr (!MT::DENSE) {
+        if (warp == 2) {
+            // group offsets and (row modes) the exclusive prefix of 128-row tiles
+            int carry = 0;
+            for (int base = 0; base <= p.G; base += 32) {
+                const int g = base + lane;
+                int o = 0;
+                if (g <= p.G) {
+                    o = p.offsets[g];
+                    offs[g] = o;
+                }
+                int mt = 0;
+                if (g < p.G) {
+                    const int cnt = p.offsets[g + 1] - o;
+                    mt = cnt > 0 ? (cnt + 127) >> 7 : 0;
+                }
+                int incl = mt;
+#pragma unroll
+                for (int sft = 1; sft < 32; sft <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, sft);
+                    if (lane >= sft) incl += v;
+                }
+                if (g <= p.G) mt_start[g] = carry + incl - mt;
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_base_s;
+    const WaitCtl wc{abort_s, p.status, p.wait_limit};
+    int total_tiles;
+    if constexpr (MT::DENSE) {
+        total_tiles = ((p.rows + 127) >> 7) * p.n_tiles;
+    } else if constexpr (MT::ROWGROUP) {
+        total_tiles = mt_start[p.G] * p.n_tiles;
+    } else {
+        total_tiles = p.G * p.m_tiles * p.n_tiles;
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int last_par[STAGES];
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
+            uint32_t s = 0, ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const TileInfo ti = decode_tile<MODE, BN>(p, t, mt_start, offs);
+                for (int kb = 0; kb < ti.kb; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], TS::STAGE_BYTES);
+                    uint8_t *a_dst = sA + s * TS::A_BYTES;
+                    uint8_t *b_dst = sB + s * TS::B_BYTES;
+                    if constexpr (MT::A_MN) {
+                        tma_load_2d(a_dst, &p.tmA, &full[s], ti.m0, ti.krow0 + kb * 64);
+                        tma_load_2d(a_dst + 8192, &p.tmA, &full[s], ti.m0 + 64, ti.krow0 + kb * 64);
+                    } else {
+                        tma_load_2d(a_dst, &p.tmA, &full[s], kb * 64, ti.row0);
+                    }
+                    if constexpr (MODE == GM_GATE) {
+                        tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, ti.nt * BN);
+                    } else if constexpr (MODE == GM_FFN1) {
+                        const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
+                        tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, r);
+                        tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB, &full[s], kb * 64, r + p.I);
+                    } else if constexpr (MODE == GM_FFN2) {
+                        tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64,
+                                    ti.g * p.b_rows_per_group + ti.nt * BN);
+                    } else {
+                        // MN-major B: BN/64 boxes of 64 columns x 64 contraction rows
+                        const int krow = MT::KGROUP ? ti.krow0 + kb * 64
+                                                    : ti.g * p.b_rows_per_group + kb * 64;
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(b_dst + j * 8192, &p.tmB, &full[s], ti.nt * BN + 64 * j,
+                                        krow);
+                    }
+                    last_par[s] = (int)ph;
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // drain the copies still in flight before the CTA exits
+                for (int i = 0; i < STAGES; ++i)
+                    if (last_par[i] >= 0)
+                        mbar_wait_teardown(&full[i], (uint32_t)last_par[i], p.wait_limit);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        uint32_t s = 0, ph = 0;
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile<MODE, BN>(p, t, mt_start, offs);
+            const uint32_t acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait(&tempty[acc], aph ^ 1u, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < ti.kb; ++kb) {
+                if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + s * TS::A_BYTES);
+                const uint32_t b_addr = smem_u32(sB + s * TS::B_BYTES);
+                if constexpr (MT::KGROUP) {
+                    const int valid = ti.krows - kb * 64;
+                    if (valid < 64) {
+                        // rows past the group's end belong to the next group: zero them
+                        const int nbox = 2 + BN / 64;
+                        const int per_box = (64 - valid) * 8;  // 16-byte chunks
+                        for (int i = lane; i < nbox * per_box; i += 32) {
+                            const int box = i / per_box;
+                            const int c = i - box * per_box;
+                            uint8_t *base = box < 2 ? sA + s * TS::A_BYTES + box * 8192
+                                                    : sB + s * TS::B_BYTES + (box - 2) * 8192;
+                            *reinterpret_cast<uint4 *>(base + valid * 128 + c * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = MT::A_MN ? sdesc_sw128(a_addr + kk * 2048, 8192, 1024)
+                                                     : sdesc_sw128(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bd = MT::B_MN ? sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
+                                                     : sdesc_sw128(b_addr + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
+                }
+                __syncwarp();
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&tfull[acc]);
+            __syncwarp();
+        }
+        if (!ok) {
+            // every MMA this thread issued must finish before TMEM is freed
+            if (lane == 0) umma_commit(done);
+            __syncwarp();
+            mbar_wait_teardown(done, 0, p.wait_limit);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;
+        const int r_local = q * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile<MODE, BN>(p, t, mt_start, offs);
+            const uint32_t acc = it & 1;
+            const uint32_t aph = (it >> 1) & 1;
+            if (!mbar_wait(&tfull[acc], aph, wc)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            const bool valid = r_local < ti.rows_valid;
+            const int row = ti.row0 + r_local;
+
+            if constexpr (MODE == GM_GATE) {
+                float *out = static_cast<float *>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c, r);
+                    tmem_wait_ld();
+                    const int col = ti.nt * BN + c;
+                    if (valid && col < p.N) {
+                        float *dst = out + (size_t)row * p.N + col;
+                        if (col + 32 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                float v[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    v[e] = __uint_as_float(r[j + e]) +
+                                           (p.col_add ? p.col_add[col + j + e] : 0.0f);
+                                st_global_v4(dst + j, __float_as_uint(v[0]), __float_as_uint(v[1]),
+                                             __float_as_uint(v[2]), __float_as_uint(v[3]));
+                            }
+                        } else {
+                            for (int j = 0; j < 32 && col + j < p.N; ++j)
+                                dst[j] = __uint_as_float(r[j]) +
+                                         (p.col_add ? p.col_add[col + j] : 0.0f);
+                        }
+                    }
+                }
+            } else if constexpr (MODE == GM_FFN1) {
+                constexpr int BH = BN / 2;
+                uint16_t *h = static_cast<uint16_t *>(p.out);
+                float *gu = static_cast<float *>(p.out2);
+#pragma unroll 1
+                for (int c = 0; c < BH; c += 32) {
+                    uint32_t rg[32], ru[32];
+                    tmem_ld32(tb + c, rg);
+                    tmem_ld32(tb + BH + c, ru);
+                    tmem_wait_ld();
+                    if (valid) {
+                        const int col = ti.nt * BH + c;
+                        uint32_t hp[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            hp[j] = pack_bf16x2(
+                                swiglu_clamped(__uint_as_float(rg[2 * j]), __uint_as_float(ru[2 * j]), p.clamp),
+                                swiglu_clamped(__uint_as_float(rg[2 * j + 1]), __uint_as_float(ru[2 * j + 1]), p.clamp));
+                        if (h) {
+                            uint16_t *dst = h + (size_t)row * p.I + col;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                st_global_v4(dst + 2 * j, hp[j], hp[j + 1], hp[j + 2], hp[j + 3]);
+                        }
+                        if (gu) {
+                            float *gd = gu + (size_t)row * 2 * p.I + col;
+                            float *ud = gd + p.I;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                st_global_v4(gd + j, rg[j], rg[j + 1], rg[j + 2], rg[j + 3]);
+                                st_global_v4(ud + j, ru[j], ru[j + 1], ru[j + 2], ru[j + 3]);
+                            }
+                        }
+                    }
+                }
+            } else if constexpr (MODE == GM_FFN2 || MODE == GM_DGRAD1) {
+                uint16_t *y = static_cast<uint16_t *>(p.out);
+                float w = 1.0f;
+                if constexpr (MODE == GM_FFN2) {
+                    if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c, r);
+                    tmem_wait_ld();
+                    if (valid) {
+                        uint16_t *dst = y + (size_t)row * p.N + ti.nt * BN + c;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8)
+                            st_global_v4(dst + j,
+                                         pack_bf16x2(w * __uint_as_float(r[j]), w * __uint_as_float(r[j + 1])),
+                                         pack_bf16x2(w * __uint_as_float(r[j + 2]), w * __uint_as_float(r[j + 3])),
+                                         pack_bf16x2(w * __uint_as_float(r[j + 4]), w * __uint_as_float(r[j + 5])),
+                                         pack_bf16x2(w * __uint_as_float(r[j + 6]), w * __uint_as_float(r[j + 7])));
+                    }
+                }
+            } else if constexpr (MODE == GM_DGRAD2) {
+                uint16_t *dgu = static_cast<uint16_t *>(p.out2);
+                uint16_t *hw = static_cast<uint16_t *>(p.out3);
+                float w = 1.0f;
+                if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
+                const float cl = p.clamp;
+                float dw = 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c, r);
+                    tmem_wait_ld();
+                    if (valid) {
+                        const int col = ti.nt * BN + c;
+                        const float *gsrc = p.gu_in + (size_t)row * 2 * p.I + col;
+                        const float *usrc = gsrc + p.I;
+                        uint16_t *dgd = dgu + (size_t)row * 2 * p.I + col;
+                        uint16_t *dud = dgd + p.I;
+                        uint16_t *hwd = hw + (size_t)row * p.I + col;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            const float4 g0 = *reinterpret_cast<const float4 *>(gsrc + j);
+                            const float4 g1 = *reinterpret_cast<const float4 *>(gsrc + j + 4);
+                            const float4 u0 = *reinterpret_cast<const float4 *>(usrc + j);
+                            const float4 u1 = *reinterpret_cast<const float4 *>(usrc + j + 4);
+                            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                            uint32_t og[4], ou[4], oh[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float dg2[2], du2[2], hw2[2];
+#pragma unroll
+                                for (int hlf = 0; hlf < 2; ++hlf) {
+                                    const float g = gv[2 * e + hlf];
+                                    const float u = uv[2 * e + hlf];
+                                    const float dA = __uint_as_float(r[j + 2 * e + hlf]);
+                                    const float a = fminf(g, cl);
+                                    const float b = fminf(fmaxf(u, -cl), cl);
+                                    const float sg = 1.0f / (1.0f + expf(-a));
+                                    const float si = a * sg;
+                                    // bit-identical to the forward's h (same fp32 g, u and code)
+                                    const float hv = round_bf16(swiglu_clamped(g, u, cl));
+                                    dw = fmaf(hv, dA, dw);
+                                    const float dH = w * dA;
+                                    dg2[hlf] = g <= cl ? dH * b * (sg + a * sg * (1.0f - sg)) : 0.0f;
+                                    du2[hlf] = (u >= -cl && u <= cl) ? dH * si : 0.0f;
+                                    hw2[hlf] = w * hv;
+                                }
+                                og[e] = pack_bf16x2(dg2[0], dg2[1]);
+                                ou[e] = pack_bf16x2(du2[0], du2[1]);
+                                oh[e] = pack_bf16x2(hw2[0], hw2[1]);
+                            }
+                            st_global_v4(dgd + j, og[0], og[1], og[2], og[3]);
+                            st_global_v4(dud + j, ou[0], ou[1], ou[2], ou[3]);
+                            st_global_v4(hwd + j, oh[0], oh[1], oh[2], oh[3]);
+                        }
+                    }
+                }
+                if (valid) p.out4[(size_t)row * p.n_tiles + ti.nt] = dw;
+            } else {  // GM_WGRAD
+                float *out = static_cast<float *>(p.out);
+                float *dst_row = out + ((size_t)ti.g * p.M + ti.m0 + r_local) * p.N + ti.nt * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    if (ti.kb > 0) {
+                        tmem_ld32(tb + c, r);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        st_global_v4(dst_row + c + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TS::TMEM_COLS);
+}
+
+}  // namespace moe

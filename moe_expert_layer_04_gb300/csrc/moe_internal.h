@@ -1,0 +1,75 @@
+// moe_internal.h -- declarations shared by the translation units of libmoe.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Default limit of every bounded device-side wait, in SM clock cycles
+// (about four seconds at 2 GHz; the longest legitimate wait is one tile).
+constexpr long long kWaitLimitCycles = 1LL << 33;
+
+// Address of this library's status word on the current device.
+int *device_status_ptr();
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Encodes a 2-D bf16 tensor map with 128-byte swizzle: a [outer, inner]
+// row-major matrix with the given row pitch (bytes), copied in boxes of
+// box_inner x box_outer elements.  Out-of-bounds elements read as zero.
+bool encode_tmap_bf16_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Supported-shape check shared by the entry points.
+moe_status check_shapes(int T, int d, int E, int k, int I);
+
+// ------------------------------------------------------------ kernels
+
+// Grouped / dense GEMM modes of the tcgen05 kernel.
+enum GemmMode : int {
+    GM_GATE = 0,    // logits = x W_g^T (+ offset), fp32 out
+    GM_FFN1 = 1,    // [g|u] = x_perm W13[g]^T -> clamped SwiGLU h (bf16), optional g|u save
+    GM_FFN2 = 2,    // y = w * (h W2[g]^T) (bf16)
+    GM_DGRAD2 = 3,  // dA = dY_perm W2[g] -> clamped-SwiGLU backward (dGU, w h, dw partials)
+    GM_DGRAD1 = 4,  // dX_perm = dGU W13[g] (bf16)
+    GM_WGRAD = 5    // dW[g] = A_g^T B_g over the group's rows (fp32)
+};
+
+// Host launchers (gemm_*.cu).  All pointers are device pointers.
+moe_status launch_gate_gemm(const uint16_t *x, const uint16_t *Wg, const float *offset, int T,
+                            int d, int E, float *logits, cudaStream_t st);
+moe_status launch_ffn1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                       const uint16_t *W13, int d, int I, float clamp, uint16_t *h,
+                       float *gu_save, cudaStream_t st);
+moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max_rows,
+                       const uint16_t *W2, const float *row_w, int S, int d, int I, uint16_t *y,
+                       cudaStream_t st);
+moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G, int max_rows,
+                         const uint16_t *W2, const float *gu, const float *row_w, int S,
+                         int d, int I, float clamp, uint16_t *dGU, uint16_t *hw, float *dw_part,
+                         int *dw_tiles, cudaStream_t st);
+int dgrad2_n_tiles(int I);
+moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int max_rows,
+                         const uint16_t *W13, int d, int I, uint16_t *dX_perm, cudaStream_t st);
+// dW[g] (M x N, fp32) = A[rows of g]^T B[rows of g]; A [R, M] and B [R, N] bf16.
+moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, const int32_t *offsets,
+                        int G, int R, float *dW, cudaStream_t st);
+
+// Row gather: dst[row] = src[row_token[row]] for the S routed rows plus the
+// T identity rows, reading each token row once (permute.cu).
+moe_status launch_gather_rows(const uint16_t *src, const int32_t *slot_row, int T, int d, int k,
+                              uint16_t *dst, cudaStream_t st);
+
+moe_status launch_selftest_timeout(long long limit, cudaStream_t st);
+
+}  // namespace moe

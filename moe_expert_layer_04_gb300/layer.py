@@ -1,0 +1,153 @@
+"""The routed MoE layer on one GPU, as a sequence of C-ABI calls.
+
+This module only allocates device memory (through PyTorch) and calls the
+library in order; every step of the layer runs in the library's kernels:
+
+  forward   moe_route -> moe_permute -> moe_expert_ffn -> moe_combine
+  backward  moe_backward
+
+("HyperParallel加速DeepSeek-V4.1多模态1M长序列训练" §2.3: MegaGate routing
+pipeline, then MegaMoE dispatch, two expert matmuls around the clamped
+SwiGLU, and result return; the shared expert of "MindSpore HyperParallel
+一键开箱DeepSeek-V4.1-Flash" §01 runs as expert group E on every token.)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE, MOE_ROUTE_HASH, MOE_ROUTE_TOPK
+
+
+@dataclass(frozen=True)
+class Dims:
+    T: int
+    d: int
+    E: int
+    k: int
+    I: int
+
+    @property
+    def S(self):
+        return self.T * self.k
+
+    @property
+    def R(self):
+        return self.T * self.k + self.T
+
+
+class MoELayer:
+    """Preallocated buffers for one layer shape, reused across calls.
+
+    weights: dict with W_g [E,d], W13 [E+1,2I,d], W2 [E+1,d,I] (bf16, CUDA).
+    """
+
+    def __init__(self, dims: Dims, weights: dict, scaling: float, clamp: float = 7.0,
+                 backward: bool = False, recompute: bool = False, device="cuda"):
+        self.dims = dims
+        self.w = weights
+        self.scaling = float(scaling)
+        self.clamp = float(clamp)
+        self.recompute = recompute
+        self.backward_enabled = backward
+        D = dims
+        dev = torch.device(device)
+        e = dict(device=dev)
+        self.logits = torch.empty(D.T, D.E, dtype=torch.float32, **e)
+        self.ids = torch.empty(D.T, D.k, dtype=torch.int32, **e)
+        self.weights = torch.empty(D.T, D.k, dtype=torch.float32, **e)
+        self.scores_sel = torch.empty(D.T, D.k, dtype=torch.float32, **e)
+        self.counts = torch.empty(D.E, dtype=torch.int32, **e)
+        self.offsets = torch.empty(D.E + 2, dtype=torch.int32, **e)
+        self.row_token = torch.empty(D.R, dtype=torch.int32, **e)
+        self.slot_row = torch.empty(D.S, dtype=torch.int32, **e)
+        self.row_weight = torch.empty(D.S, dtype=torch.float32, **e)
+        self.x_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
+        self.h_perm = torch.empty(D.R, D.I, dtype=torch.bfloat16, **e)
+        self.y_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
+        self.gu_save = (torch.empty(D.R, 2 * D.I, dtype=torch.float32, **e)
+                        if backward and not recompute else None)
+        self.y = torch.empty(D.T, D.d, dtype=torch.bfloat16, **e)
+        flags = (MOE_FLAG_BACKWARD if backward else 0) | (MOE_FLAG_RECOMPUTE if recompute else 0)
+        ws = _lib.moe_workspace_size(D.T, D.d, D.E, D.k, D.I, flags)
+        if ws == 0:
+            raise ValueError(f"unsupported layer shape {D}")
+        self.ws = torch.empty(ws, dtype=torch.uint8, **e)
+        if backward:
+            self.dX = torch.empty(D.T, D.d, dtype=torch.bfloat16, **e)
+            self.dW_g = torch.empty(D.E, D.d, dtype=torch.float32, **e)
+            self.dW13 = torch.empty(D.E + 1, 2 * D.I, D.d, dtype=torch.float32, **e)
+            self.dW2 = torch.empty(D.E + 1, D.d, D.I, dtype=torch.float32, **e)
+            self.dlogits = None
+            self.dweights = None
+
+    # ------------------------------------------------------------ forward
+    def route(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
+              input_ids=None, tid2eid=None, stream=None):
+        D = self.dims
+        _lib.moe_route(x, self.w["W_g"], logit_offset, bias, is_vision, input_ids, tid2eid,
+                       D.T, D.d, D.E, D.k, self.scaling, mode, self.logits, self.ids,
+                       self.weights, self.scores_sel, stream)
+
+    def dispatch(self, x, stream=None):
+        D = self.dims
+        _lib.moe_permute(self.ids, self.weights, x, D.T, D.d, D.E, D.k, self.counts,
+                         self.offsets, self.row_token, self.slot_row, self.row_weight,
+                         self.x_perm, self.ws, stream)
+
+    def experts(self, stream=None):
+        D = self.dims
+        _lib.moe_expert_ffn(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"], self.w["W2"],
+                            self.row_weight, D.S, D.d, D.I, self.clamp, self.gu_save,
+                            self.h_perm, self.y_perm, None, stream)
+
+    def expert_gemm1(self, stream=None):
+        D = self.dims
+        _lib.moe_expert_gemm1(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"], D.d, D.I,
+                              self.clamp, self.gu_save, self.h_perm, stream)
+
+    def expert_gemm2(self, stream=None):
+        D = self.dims
+        _lib.moe_expert_gemm2(self.h_perm, self.offsets, D.E + 1, D.R, self.w["W2"],
+                              self.row_weight, D.S, D.d, D.I, self.y_perm, stream)
+
+    def combine(self, stream=None):
+        D = self.dims
+        _lib.moe_combine(self.y_perm, self.slot_row, D.T, D.d, D.k, 1, self.y, stream)
+
+    def forward(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
+                input_ids=None, tid2eid=None, stream=None):
+        self.x = x
+        self.route(x, bias, is_vision, logit_offset, mode, input_ids, tid2eid, stream)
+        self.dispatch(x, stream)
+        self.experts(stream)
+        self.combine(stream)
+        return self.y
+
+    # ----------------------------------------------------------- backward
+    def backward(self, dY, want_dlogits=False, want_dweights=False, stream=None):
+        D = self.dims
+        if not self.backward_enabled:
+            raise RuntimeError("layer built without backward buffers")
+        if want_dlogits and self.dlogits is None:
+            self.dlogits = torch.empty(D.T, D.E, dtype=torch.float32, device=dY.device)
+        if want_dweights and self.dweights is None:
+            self.dweights = torch.empty(D.T, D.k, dtype=torch.float32, device=dY.device)
+        args = dict(T=D.T, d=D.d, E=D.E, k=D.k, I=D.I, scaling=self.scaling, clamp=self.clamp,
+                    flags=MOE_FLAG_RECOMPUTE if self.recompute else 0,
+                    x=self.x, W_g=self.w["W_g"], W13=self.w["W13"], W2=self.w["W2"],
+                    ids=self.ids, weights=self.weights, scores_sel=self.scores_sel,
+                    row_weight=self.row_weight, offsets=self.offsets, row_token=self.row_token,
+                    slot_row=self.slot_row,
+                    x_perm=None if self.recompute else self.x_perm,
+                    gu_save=None if self.recompute else self.gu_save,
+                    dY=dY, dX=self.dX, dW_g=self.dW_g, dW13=self.dW13, dW2=self.dW2,
+                    dlogits=self.dlogits if want_dlogits else None,
+                    dweights=self.dweights if want_dweights else None, ws=self.ws)
+        _lib.moe_backward(args, stream)
+        return self.dX
+
+
+__all__ = ["Dims", "MoELayer", "MOE_ROUTE_TOPK", "MOE_ROUTE_HASH"]

@@ -1,0 +1,104 @@
+"""The C ABI library on the host: it builds, loads, exports every function that
+include/moe.h declares, its argument struct matches the header, and its
+host-side validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_layer_04_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = open(os.path.join(ROOT, "include", "moe.h")).read()
+
+
+def declared_functions():
+    body = re.sub(r"/\*.*?\*/", "", HEADER, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s+\*?\s*(moe_\w+)\s*\(", body, flags=re.M)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    lib = _lib.load()
+    names = declared_functions()
+    assert "moe_route" in names and "moe_backward" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in moe.h but not exported"
+    assert sorted(_lib.EXPORTS) == names
+
+
+def test_bwd_struct_matches_header():
+    m = re.search(r"typedef struct \{(.*?)\} moe_bwd_args;", HEADER, flags=re.S)
+    body = re.sub(r"/\*.*?\*/", "", m.group(1), flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        names = decl.split()[-1] if "," not in decl else decl
+        # "int T, d, E, k, I" / "float scaling, clamp" / "const float *weights"
+        parts = re.sub(r"^(const\s+)?\w+\s*", "", decl)
+        for p in parts.split(","):
+            fields.append(p.strip().lstrip("*").strip())
+    assert [f for f, _ in _lib.BwdArgs._fields_] == fields
+
+
+def test_workspace_size_host_logic():
+    ws = _lib.moe_workspace_size
+    assert ws(4096, 4096, 384, 6, 2048, 0) > 0
+    assert ws(4096, 4096, 384, 6, 2048, 1) > ws(4096, 4096, 384, 6, 2048, 0)
+    assert ws(4096, 4096, 384, 6, 2048, 3) > ws(4096, 4096, 384, 6, 2048, 1)
+    # backward needs at least the permuted dY, dX, [dg|du] and w h buffers
+    R = 4096 * 7
+    assert ws(4096, 4096, 384, 6, 2048, 1) >= R * (4096 * 2 * 2 + 4096 * 2 + 2048 * 2)
+    # unsupported shapes report 0
+    assert ws(4096, 4000, 384, 6, 2048, 0) == 0      # d % 128
+    assert ws(4096, 4096, 384, 6, 2000, 0) == 0      # I % 64
+    assert ws(4096, 4096, 2048, 6, 2048, 0) == 0     # E > 1024
+    assert ws(4096, 4096, 384, 33, 2048, 0) == 0     # k > 32
+    assert ws(4096, 4096, 4, 6, 2048, 0) == 0        # k > E
+
+
+def test_validation_rejects_before_any_launch():
+    lib = _lib.load()
+    nul = None
+    # moe_route: null x
+    st = lib.moe_route(nul, nul, nul, nul, nul, nul, nul, 0, 8, 128, 4, 2, 1.0, 0, nul, nul, nul,
+                       nul, nul)
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    # bad mode
+    st = lib.moe_route_logits(ctypes.c_void_p(16), ctypes.c_void_p(16), nul, nul, nul, 0, 8, 4, 2,
+                              1.0, 7, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                              ctypes.c_void_p(16), nul)
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    # moe_permute without a workspace
+    p = ctypes.c_void_p(256)
+    st = lib.moe_permute(p, nul, nul, 8, 128, 4, 2, p, p, p, p, nul, nul, nul, 0, nul)
+    assert st == _lib.MOE_ERR_WORKSPACE
+    # moe_expert_ffn: unsupported d
+    st = lib.moe_expert_ffn(p, p, 2, 64, p, p, nul, 0, 96, 64, 7.0, nul, p, p, nul, 0, nul)
+    assert st == _lib.MOE_ERR_UNSUPPORTED
+    # moe_expert_ffn: misaligned pointer
+    q = ctypes.c_void_p(258)
+    st = lib.moe_expert_ffn(q, p, 2, 64, p, p, nul, 0, 128, 64, 7.0, nul, p, p, nul, 0, nul)
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    # moe_backward: null args, and missing saved state without recompute
+    assert lib.moe_backward(None, nul) == _lib.MOE_ERR_INVALID_ARG
+    a = _lib.BwdArgs(T=8, d=128, E=4, k=2, I=64, scaling=1.0, clamp=7.0, flags=0)
+    assert lib.moe_backward(ctypes.byref(a), nul) == _lib.MOE_ERR_INVALID_ARG
+    # non-positive clamp and bad timeout limits
+    assert lib.moe_selftest_wait_timeout(0, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(1 << 40, nul) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings():
+    for s in range(6):
+        assert _lib.status_string(s) and _lib.status_string(s) != "unknown status"
+    assert _lib.status_string(99) == "unknown status"
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        _lib.moe_combine(x, torch.zeros(16, dtype=torch.int32), 8, 128, 2, 1, x)

@@ -1,0 +1,237 @@
+"""GPU path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Index work (expert ids, permutation, counts, offsets) must match bit for bit;
+routing weights within 1e-6 relative; float outputs and gradients within
+relative Frobenius 1e-2 and max-abs 5e-2.  Routing is checked stage-wise: the
+oracle routes the GPU's own fp32 logits, since fp32 GEMM accumulation order
+can move a logit by an ulp and legitimately flip a near-tie.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_layer_04_gb300 import _lib
+from moe_expert_layer_04_gb300 import workloads as W
+from moe_expert_layer_04_gb300.layer import MOE_ROUTE_HASH, MOE_ROUTE_TOPK, Dims, MoELayer
+from tests.helpers import W_RTOL, assert_close, cpu, np64
+
+pytestmark = pytest.mark.gpu
+
+# (name, workload) -- several tiles per group and ragged tails
+CASES = {
+    "tiny": W.WORKLOADS["tiny_fwd"],
+    "mid_I192": W.Workload("mid_I192", 320, 256, 24, 4, 192, 2.5, vision_frac=0.25),
+    "mid_skew": W.Workload("mid_skew", 520, 384, 12, 3, 256, 2.5, zipf_s=1.1),
+}
+
+
+def make_layer(w, backward=False, recompute=False, seed_inputs=None):
+    inp = W.make_inputs(w, device="cuda", with_dy=backward)
+    weights = dict(W_g=inp["W_g"], W13=inp["W13"], W2=inp["W2"])
+    layer = MoELayer(Dims(w.T, w.d, w.E, w.k, w.I), weights, w.rho, w.clamp, backward=backward,
+                     recompute=recompute)
+    return layer, inp
+
+
+def test_gate_logits_and_route_stagewise():
+    for name, w in CASES.items():
+        layer, inp = make_layer(w)
+        vis = inp["is_vision"]
+        layer.route(inp["x"], inp["bias"], vis, inp["logit_offset"])
+        torch.cuda.synchronize()
+        z_ref = oracle.gate_logits(cpu(inp["x"]), cpu(inp["W_g"]),
+                                   offset=None if inp["logit_offset"] is None else cpu(inp["logit_offset"]))
+        z = np64(layer.logits)
+        assert np.max(np.abs(z - z_ref)) < 1e-4 * max(1.0, np.abs(z_ref).max()), name
+        ids, wts, s, _ = oracle.route(z, cpu(inp["bias"]), w.k, w.rho, is_vision=cpu(vis))
+        np.testing.assert_array_equal(cpu(layer.ids).numpy(), ids, err_msg=name)
+        np.testing.assert_array_equal(np64(layer.scores_sel), s, err_msg=name)
+        np.testing.assert_allclose(np64(layer.weights), wts, rtol=W_RTOL, atol=0, err_msg=name)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 4, 4), (200, 40, 6), (97, 384, 6), (33, 1000, 8),
+                                   (64, 16, 1), (50, 32, 32)])
+def test_route_logits_exact(T, E, k):
+    z = W.random_logits(T, E, 2.0, seed=T * 7 + E).cuda()
+    # plant exact ties: equal logits in pairs so equal keys must go to the lower id
+    z[:, 1::2] = z[:, 0::2][:, : z[:, 1::2].shape[1]]
+    g = torch.Generator().manual_seed(E)
+    bias = (torch.rand(2, E, generator=g) * 0.2 - 0.1).cuda()
+    bias[:, 1::2] = bias[:, 0::2][:, : bias[:, 1::2].shape[1]]
+    vis = (torch.arange(T) % 3 == 0).to(torch.uint8).cuda()
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    s = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    _lib.moe_route_logits(z, bias, vis, None, None, T, E, k, 2.5, MOE_ROUTE_TOPK, ids, wt, s)
+    torch.cuda.synchronize()
+    r_ids, r_w, r_s, _ = oracle.route(np64(z), cpu(bias), k, 2.5, is_vision=cpu(vis))
+    np.testing.assert_array_equal(cpu(ids).numpy(), r_ids)
+    np.testing.assert_array_equal(np64(s), r_s)
+    np.testing.assert_allclose(np64(wt), r_w, rtol=W_RTOL, atol=0)
+
+
+def test_route_hash_exact():
+    T, E, k, V = 300, 384, 6, W.VOCAB
+    z = W.random_logits(T, E, 1.5, seed=11).cuda()
+    tab = W.tid2eid_table(V, E, k, 0, "cuda")
+    iid = W.zipf_input_ids(T, V, 1.0, 0, "cuda")
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    s = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    bias = torch.zeros(2, E, device="cuda")
+    _lib.moe_route_logits(z, bias, None, iid, tab, T, E, k, 2.5, MOE_ROUTE_HASH, ids, wt, s)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    r_ids, r_w, r_s, _ = oracle.route(np64(z), cpu(bias), k, 2.5, mode=1, input_ids=cpu(iid),
+                                      tid2eid=cpu(tab))
+    np.testing.assert_array_equal(cpu(ids).numpy(), r_ids)
+    np.testing.assert_array_equal(np64(s), r_s)
+    np.testing.assert_allclose(np64(wt), r_w, rtol=W_RTOL, atol=0)
+
+
+@pytest.mark.parametrize("T,E,k,skew,d", [(64, 16, 2, 0.0, 128), (1, 4, 3, 0.0, 8),
+                                          (2000, 384, 6, 1.1, 64), (700, 50, 5, 2.5, 128),
+                                          (5000, 1000, 8, 0.0, 16)])
+def test_permute_exact(T, E, k, skew, d):
+    ids = W.random_ids(T, E, k, seed=T + E, skew=skew).cuda()
+    wts = torch.rand(T, k, device="cuda")
+    x = W.normal_bf16((T, d), 1.0, 0, "xp", "cuda")
+    S, R = T * k, T * k + T
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 2, dtype=torch.int32, device="cuda")
+    row_token = torch.empty(R, dtype=torch.int32, device="cuda")
+    slot_row = torch.empty(S, dtype=torch.int32, device="cuda")
+    row_w = torch.empty(S, dtype=torch.float32, device="cuda")
+    x_perm = torch.empty(R, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(_lib.moe_workspace_size(T, 128, E, k, 64, 0), dtype=torch.uint8,
+                     device="cuda")
+    _lib.moe_permute(ids, wts, x, T, d, E, k, counts, offsets, row_token, slot_row, row_w,
+                     x_perm, ws)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    c, o, rt, sr = oracle.permute(cpu(ids).numpy(), E)
+    np.testing.assert_array_equal(cpu(counts).numpy(), c)
+    np.testing.assert_array_equal(cpu(offsets).numpy()[: E + 1], o)
+    assert cpu(offsets).numpy()[E + 1] == R
+    np.testing.assert_array_equal(cpu(row_token).numpy()[:S], rt)
+    np.testing.assert_array_equal(cpu(row_token).numpy()[S:], np.arange(T))
+    np.testing.assert_array_equal(cpu(slot_row).numpy(), sr)
+    np.testing.assert_array_equal(cpu(row_w).numpy()[sr], cpu(wts).numpy().ravel())
+    xr = cpu(x).view(torch.int16).numpy()
+    np.testing.assert_array_equal(cpu(x_perm).view(torch.int16).numpy(),
+                                  xr[cpu(row_token).numpy()])
+
+
+def _rows_meta(layer, w):
+    """Per permuted row: token, expert group and routing weight (from the GPU's own routing)."""
+    D = layer.dims
+    offs = cpu(layer.offsets).numpy()
+    rt = cpu(layer.row_token).numpy().astype(np.int64)
+    grp = np.repeat(np.arange(D.E + 1), np.diff(offs)).astype(np.int32)
+    rw = np.ones(D.R)
+    rw[: D.S] = np64(layer.row_weight)
+    return rt, grp, rw
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_layer(name):
+    w = CASES[name]
+    layer, inp = make_layer(w)
+    y = layer.forward(inp["x"], inp["bias"], inp["is_vision"], inp["logit_offset"])
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    x, W13, W2 = cpu(inp["x"]), cpu(inp["W13"]), cpu(inp["W2"])
+    rt, grp, rw = _rows_meta(layer, w)
+    h_ref, y_ref = oracle.expert_rows(x, W13, W2, rt, grp, rw, w.clamp)
+    assert_close(layer.h_perm, h_ref, f"{name} h")
+    assert_close(layer.y_perm, y_ref, f"{name} y_perm")
+    # combine: y[t] = shared row + the token's k routed rows
+    sr = cpu(layer.slot_row).numpy().reshape(w.T, w.k)
+    y_comb = y_ref[w.S + np.arange(w.T)] + y_ref[sr].sum(1)
+    assert_close(y, y_comb, f"{name} y")
+    # end to end against the oracle's own routing, where the routing agrees
+    full = oracle.layer_forward(x, cpu(inp["W_g"]), W13, W2, cpu(inp["bias"]), w.k, w.rho,
+                                w.clamp, is_vision=cpu(inp["is_vision"]),
+                                offset=None if inp["logit_offset"] is None else cpu(inp["logit_offset"]))
+    same = np.all(full["ids"] == cpu(layer.ids).numpy(), axis=1)
+    # a disagreement is only legitimate at a near-tie of the keys
+    assert np.all(same | (full["margin"] < 1e-5)), name
+    assert_close(np64(y)[same], full["y"][same], f"{name} y end-to-end")
+
+
+@pytest.mark.parametrize("name,recompute", [("tiny", False), ("mid_I192", False),
+                                            ("mid_skew", False), ("mid_skew", True)])
+def test_backward_layer(name, recompute):
+    w = CASES[name]
+    layer, inp = make_layer(w, backward=True, recompute=recompute)
+    layer.forward(inp["x"], inp["bias"], inp["is_vision"], inp["logit_offset"])
+    layer.backward(inp["dY"], want_dlogits=True, want_dweights=True)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    x, Wg, W13, W2, dY = (cpu(inp[k]) for k in ("x", "W_g", "W13", "W2", "dY"))
+    off = None if inp["logit_offset"] is None else cpu(inp["logit_offset"])
+    ref = oracle.layer_backward(x, Wg, W13, W2, dY, cpu(inp["bias"]), w.k, w.rho, w.clamp,
+                                is_vision=cpu(inp["is_vision"]), offset=off)
+    fwd = oracle.layer_forward(x, Wg, W13, W2, cpu(inp["bias"]), w.k, w.rho, w.clamp,
+                               is_vision=cpu(inp["is_vision"]), offset=off)
+    np.testing.assert_array_equal(fwd["ids"], cpu(layer.ids).numpy())
+    assert_close(layer.dX, ref["dX"], f"{name} dX")
+    assert_close(layer.dweights, ref["dw"], f"{name} dw", max_abs=5e-2 * max(1, np.abs(ref["dw"]).max() / 10))
+    assert_close(layer.dlogits, ref["dz"], f"{name} dlogits")
+    assert_close(layer.dW_g, ref["dz"].T @ np64(x), f"{name} dW_g")
+    rt, grp, rw = _rows_meta(layer, w)
+    offs = cpu(layer.offsets).numpy()
+    counts = np.diff(offs)
+    experts = sorted({int(np.argmax(counts[:w.E])), int(np.argmin(counts[:w.E])), 0, w.E})
+    for e in experts:
+        rows = np.arange(offs[e], offs[e + 1])
+        g = oracle.expert_wgrad(x, W13, W2, dY, e, rt[rows], rw[rows], w.clamp, store_bf16=True)
+        assert_close(layer.dW13[e], g["dW13"], f"{name} dW13[{e}]")
+        assert_close(layer.dW2[e], g["dW2"], f"{name} dW2[{e}]")
+
+
+def test_empty_expert_gets_zero_grad():
+    w = W.Workload("empty", 96, 128, 8, 2, 64, 1.0)
+    layer, inp = make_layer(w, backward=True)
+    # route every token to experts 0 and 1 only (bias pushes them on top)
+    bias = torch.full((2, w.E), -1.0, device="cuda")
+    bias[:, :2] = 1.0
+    layer.forward(inp["x"], bias)
+    layer.backward(inp["dY"])
+    torch.cuda.synchronize()
+    counts = cpu(layer.counts).numpy()
+    assert counts[2:].sum() == 0
+    assert torch.count_nonzero(layer.dW13[2:w.E]).item() == 0
+    assert torch.count_nonzero(layer.dW2[2:w.E]).item() == 0
+    assert torch.count_nonzero(layer.dW_g[2:]).item() == 0
+
+
+def test_selftest_wait_timeout_reports_status():
+    assert _lib.moe_last_device_status() in (_lib.MOE_OK, _lib.MOE_ERR_TIMEOUT)
+    _lib.moe_selftest_wait_timeout(200_000)
+    assert _lib.moe_last_device_status() == _lib.MOE_ERR_TIMEOUT
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    # the context is still usable
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
+
+
+def test_abi_rejects_bad_arguments_before_launch():
+    T, d, E, k = 8, 128, 4, 2
+    x = torch.zeros(T * d + 8, dtype=torch.bfloat16, device="cuda")
+    Wg = torch.zeros(E, d, dtype=torch.bfloat16, device="cuda")
+    out = [torch.empty(T, E, device="cuda"), torch.empty(T, k, dtype=torch.int32, device="cuda"),
+           torch.empty(T, k, device="cuda"), torch.empty(T, k, device="cuda")]
+    bias = torch.zeros(2, E, device="cuda")
+    with pytest.raises(_lib.MoeError) as ei:   # misaligned x (2-byte offset)
+        _lib.moe_route(x[1:1 + T * d], Wg, None, bias, None, None, None, T, d, E, k, 1.0,
+                       MOE_ROUTE_TOPK, *out)
+    assert ei.value.status == _lib.MOE_ERR_INVALID_ARG
+    with pytest.raises(_lib.MoeError) as ei:   # k > E
+        _lib.moe_route(x[:T * d], Wg, None, bias, None, None, None, T, d, E, E + 1, 1.0,
+                       MOE_ROUTE_TOPK, *out)
+    assert ei.value.status == _lib.MOE_ERR_INVALID_ARG
+    with pytest.raises(_lib.MoeError) as ei:   # d not a multiple of 128 for the expert FFN
+        _lib.moe_expert_ffn(x, out[1], 1, 8, Wg, Wg, None, 0, 96, 64, 7.0, None, x, x)
+    assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
