@@ -120,6 +120,21 @@ def fwd_flops(D):
     return 2 * D.T * D.d * D.E + 6 * D.R * D.d * D.I
 
 
+def workload(args):
+    """The named workload, optionally shrunk (--tokens / --experts) for
+    profiling captures that must stay a few GB."""
+    from moe_expert_layer_04_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    over = {}
+    if args.tokens:
+        over["T"] = args.tokens
+    if args.experts:
+        over["E"] = args.experts
+    if over:
+        wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()), **over)
+    return wl
+
+
 # ------------------------------------------------------------------- ours
 
 def run_ours(args, rank, world, local_rank):
@@ -132,7 +147,7 @@ def run_ours(args, rank, world, local_rank):
     _lib.load()
     hbm, bf16, bf16_sus, peak_src = peaks()
 
-    wl = W.WORKLOADS[args.workload]
+    wl = workload(args)
     D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
     inp = layer_inputs(wl, dev)
     weights = {k: inp[k] for k in ("W_g", "W13", "W2")}
@@ -268,7 +283,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{wl.name}: forward, T={wl.T} d={wl.d} E={wl.E} routed top-{wl.k}"
                                f" + 1 shared, I={wl.I}, scaling {wl.rho}, clamp {wl.clamp}",
                    "global_batch": wl.T * world, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (19.3 GB of expert weights streamed per step)"},
+                   "l2": "inputs larger than L2 (%.1f GB of expert weights streamed per step)"
+                         % (3 * (D.E + 1) * D.d * D.I * 2 / 1e9)},
         "roofline": roofline,
         "layer_roofline_ms": round(layer_roof_ms, 4),
         "layer_roofline_frac": round(layer_roof_ms / ms_step, 4),
@@ -352,7 +368,7 @@ def run_reference(args, rank, world):
     from moe_expert_layer_04_gb300 import workloads as W
     if rank != 0:
         return None
-    wl = W.WORKLOADS[args.workload]
+    wl = workload(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = layer_inputs(wl, dev)
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -400,6 +416,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
