@@ -42,8 +42,10 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
                       pack_bf16x2(a[6], a[7]));
 }
 
-// One warp per token; 16-byte vectors; shared row first, then slots in order.
-// When dz != nullptr the gate term sum_j dz_j W_g[ids_j] is added as well.
+// One thread per (token, 16-byte column chunk): the k + 1 row loads of a
+// chunk are independent, so each thread keeps them all in flight.  Shared row
+// first, then the slots in order.  When dz != nullptr the gate term
+// sum_j dz_j W_g[ids_j] is added as well (the dX assembly of the backward).
 __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ yp,
                                                       const int32_t *__restrict__ slot_row,
                                                       int T, int vecs, int k, int with_shared,
@@ -51,37 +53,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ 
                                                       const int32_t *__restrict__ ids,
                                                       const uint4 *__restrict__ Wg,
                                                       uint4 *__restrict__ y) {
-    const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int nw = gridDim.x * 8;
     const size_t S = (size_t)T * k;
-    for (int t = gw; t < T; t += nw) {
-        int row = 0, eid = 0;
-        float dzv = 0.0f;
-        if (lane < k) {
-            row = slot_row[(size_t)t * k + lane];
-            if (dz) {
-                dzv = dz[(size_t)t * k + lane];
-                eid = ids[(size_t)t * k + lane];
-            }
+    const size_t n = (size_t)T * vecs;
+    for (size_t it = blockIdx.x * (size_t)blockDim.x + threadIdx.x; it < n;
+         it += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(it / vecs);
+        const int c = (int)(it - (size_t)t * vecs);
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (with_shared) add_bf16x8(acc, yp[(S + t) * vecs + c]);
+        const int32_t *sr = slot_row + (size_t)t * k;
+        for (int j = 0; j < k; ++j) add_bf16x8(acc, yp[(size_t)sr[j] * vecs + c]);
+        if (dz) {
+            for (int j = 0; j < k; ++j)
+                fma_bf16x8(acc, dz[(size_t)t * k + j], Wg[(size_t)ids[(size_t)t * k + j] * vecs + c]);
         }
-        for (int c0 = 0; c0 < vecs; c0 += 32) {
-            const int c = c0 + lane;
-            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (with_shared && c < vecs) add_bf16x8(acc, yp[(S + t) * vecs + c]);
-            for (int j = 0; j < k; ++j) {
-                const size_t r = (size_t)__shfl_sync(0xffffffffu, row, j);
-                if (c < vecs) add_bf16x8(acc, yp[r * vecs + c]);
-            }
-            if (dz) {
-                for (int j = 0; j < k; ++j) {
-                    const float a = __shfl_sync(0xffffffffu, dzv, j);
-                    const size_t e = (size_t)__shfl_sync(0xffffffffu, eid, j);
-                    if (c < vecs) fma_bf16x8(acc, a, Wg[e * vecs + c]);
-                }
-            }
-            if (c < vecs) y[(size_t)t * vecs + c] = pack8(acc);
-        }
+        y[it] = pack8(acc);
     }
 }
 
@@ -189,7 +175,10 @@ size_t dwg_workspace_bytes(int d, int E) {
 moe_status launch_combine(const uint16_t *y_perm, const int32_t *slot_row, int T, int d, int k,
                           int with_shared, const float *dz, const int32_t *ids,
                           const uint16_t *Wg, uint16_t *y, cudaStream_t st) {
-    combine_kernel<<<token_blocks(T), 256, 0, st>>>(
+    const size_t n = (size_t)T * (d / 8);
+    const size_t want = (n + 255) / 256;
+    const size_t cap = (size_t)num_sms() * 8;
+    combine_kernel<<<(int)(want < cap ? want : cap), 256, 0, st>>>(
         reinterpret_cast<const uint4 *>(y_perm), slot_row, T, d / 8, k, with_shared, dz, ids,
         reinterpret_cast<const uint4 *>(Wg), reinterpret_cast<uint4 *>(y));
     return cuda_status(cudaGetLastError());

@@ -13,7 +13,9 @@
 
 namespace moe {
 
-int dgrad2_n_tiles(int I) { return (I % 128 == 0) ? I / 128 : I / 64; }
+static int dgrad2_bn(int I) { return (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64; }
+
+int dgrad2_n_tiles(int I) { return I / dgrad2_bn(I); }
 
 moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G, int max_rows,
                          const uint16_t *W2, const float *gu, const float *row_w, int S,
@@ -21,7 +23,7 @@ moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G,
                          int *dw_tiles, cudaStream_t st) {
     GemmParams p;
     std::memset(&p, 0, sizeof p);
-    const int BN = (I % 128 == 0) ? 128 : 64;
+    const int BN = dgrad2_bn(I);
     if (!encode_tmap_bf16_2d(&p.tmA, dY_perm, d, max_rows, (uint64_t)d * 2, 64, 128))
         return MOE_ERR_CUDA;
     // W2 as [G*d rows (contraction), I columns (output)], MN-major boxes
@@ -42,8 +44,11 @@ moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G,
     p.gu_in = gu;
     if (dw_tiles) *dw_tiles = p.n_tiles;
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
-    return BN == 128 ? launch_gemm<GM_DGRAD2, 128>(p, tiles, st)
-                     : launch_gemm<GM_DGRAD2, 64>(p, tiles, st);
+    switch (BN) {
+        case 256: return launch_gemm<GM_DGRAD2, 256>(p, tiles, st);
+        case 128: return launch_gemm<GM_DGRAD2, 128>(p, tiles, st);
+        default: return launch_gemm<GM_DGRAD2, 64>(p, tiles, st);
+    }
 }
 
 moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int max_rows,
@@ -76,6 +81,8 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     const int BN = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
     if (!encode_tmap_bf16_2d(&p.tmA, A, M, R, (uint64_t)M * 2, 64, 64)) return MOE_ERR_CUDA;
     if (!encode_tmap_bf16_2d(&p.tmB, B, N, R, (uint64_t)N * 2, 64, 64)) return MOE_ERR_CUDA;
+    if (!encode_tmap_f32_2d(&p.tmO, dW, N, (uint64_t)G * M, (uint64_t)N * 4, 32, 32))
+        return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
     p.m_tiles = M / 128;

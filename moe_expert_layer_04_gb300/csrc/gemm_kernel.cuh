@@ -35,6 +35,7 @@ constexpr int kGemmThreads = 192;
 struct GemmParams {
     CUtensorMap tmA;
     CUtensorMap tmB;
+    CUtensorMap tmO;         // GM_WGRAD: fp32 output [G*M, N], boxes of 32 x 32
     const int32_t *offsets;  // [G+1] group row offsets (grouped modes)
     int G;
     int rows;                // GM_GATE: rows of A
@@ -67,20 +68,27 @@ struct ModeTraits {
     static constexpr bool ROWGROUP = !DENSE && !KGROUP;
 };
 
-template <int BN>
+// Epilogue staging of the TMA-store path (GM_WGRAD): per epilogue warp two
+// 32 x 32 fp32 blocks (4 KB each, 128-byte swizzled), double buffered.
+constexpr int kEpiStageBytes = 4 * 2 * 4096;
+
+template <int BN, int MODE>
 struct TileShape {
+    static constexpr bool TMA_STORE = (MODE == GM_WGRAD);
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BN * 64 * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = kStageBudget / STAGE_BYTES;
+    static constexpr int EPI_BYTES = TMA_STORE ? kEpiStageBytes : 0;
+    static constexpr int STAGES = (kStageBudget - EPI_BYTES) / STAGE_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {64, 128, 256}: a power of two
 };
 
 // Dynamic shared memory of one CTA for G groups.
-template <int BN>
+template <int BN, int MODE>
 inline size_t gemm_smem_bytes(int G) {
-    using TS = TileShape<BN>;
-    return 1024 + (size_t)TS::STAGES * TS::STAGE_BYTES + 256 + 8 * (size_t)(G + 2);
+    using TS = TileShape<BN, MODE>;
+    return 1024 + (size_t)TS::STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256 +
+           8 * (size_t)(G + 2);
 }
 
 struct TileInfo {
@@ -140,7 +148,7 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
     using MT = ModeTraits<MODE>;
-    using TS = TileShape<BN>;
+    using TS = TileShape<BN, MODE>;
     constexpr int STAGES = TS::STAGES;
     constexpr uint32_t IDESC = idesc_bf16_f32(128, BN, MT::A_MN, MT::B_MN);
 
@@ -149,14 +157,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * TS::A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * TS::B_BYTES);
+    uint8_t *sEpi = smem + STAGES * TS::STAGE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sEpi + TS::EPI_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
-    int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + 256);
+    int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256);
     int *mt_start = offs + (p.G + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -178,6 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
         tma_prefetch_desc(&p.tmB);
+        if constexpr (TS::TMA_STORE) tma_prefetch_desc(&p.tmO);
     }
     if (warp == 1) {
         tmem_alloc(tmem_base_s, TS::TMEM_COLS);
@@ -493,9 +503,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                     }
                 }
                 if (valid) p.out4[(size_t)row * p.n_tiles + ti.nt] = dw;
-            } else {  // GM_WGRAD
-                float *out = static_cast<float *>(p.out);
-                float *dst_row = out + ((size_t)ti.g * p.M + ti.m0 + r_local) * p.N + ti.nt * BN;
+            } else {  // GM_WGRAD: TMA stores of 32 x 32 fp32 blocks through shared memory
+                uint8_t *stg = sEpi + (size_t)(warp - 2) * 8192;
+                const uint32_t sw = (uint32_t)(lane & 7);
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t r[32];
@@ -506,9 +516,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = 0u;
                     }
+                    uint8_t *buf = stg + ((c >> 5) & 1) * 4096;
+                    // the store issued two blocks ago read this buffer: wait for it
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    const uint32_t row_addr = smem_u32(buf) + (uint32_t)lane * 128u;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        st_global_v4(dst_row + c + j, r[j], r[j + 1], r[j + 2], r[j + 3]);
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(row_addr + ((((uint32_t)j) ^ sw) << 4), r[4 * j], r[4 * j + 1],
+                                     r[4 * j + 2], r[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmO, buf, ti.nt * BN + c, ti.g * p.M + ti.m0 + q * 32);
+                        bulk_commit_group();
+                    }
                 }
             }
             tc_fence_before();
@@ -516,6 +538,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
     }
 
+    if constexpr (TS::TMA_STORE) {
+        // the stores must have left shared memory (and landed) before exit
+        if (warp >= 2 && lane == 0) bulk_wait_group_all();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -17,7 +17,7 @@ moe_status launch_gemm(GemmParams &p, int max_tiles, cudaStream_t st) {
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)gemm_smem_bytes<BN>(kMaxGroups));
+                                             (int)gemm_smem_bytes<BN, MODE>(kMaxGroups));
         if (e != cudaSuccess) return MOE_ERR_CUDA;
         attr_set[dev] = true;
     }
@@ -26,7 +26,7 @@ moe_status launch_gemm(GemmParams &p, int max_tiles, cudaStream_t st) {
     p.status = device_status_ptr();
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
-    const size_t smem = gemm_smem_bytes<BN>(ModeTraits<MODE>::DENSE ? 0 : p.G);
+    const size_t smem = gemm_smem_bytes<BN, MODE>(ModeTraits<MODE>::DENSE ? 0 : p.G);
     kern<<<grid, kGemmThreads, smem, st>>>(p);
     return cuda_status(cudaGetLastError());
 }

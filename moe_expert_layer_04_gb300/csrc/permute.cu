@@ -3,13 +3,15 @@
 // selected experts, from top-k or from the hash table, feed one dispatch).
 //
 // The T*k routed slots are ordered expert-major, then by token, then by slot
-// -- a stable order that needs no atomics to be deterministic:
-//   hist     one block per chunk of 4096 slots: per-chunk expert histogram
-//   scan     per expert, exclusive prefix over chunks; exclusive prefix over
-//            experts -> offsets; absolute start of every (chunk, expert)
-//   scatter  inside a chunk, warps take 32 slots at a time in order; equal
-//            experts inside a warp are ranked with __match_any_sync, and warps
-//            advance the per-expert cursors one after the other
+// -- a stable order that needs no atomics to be deterministic.  Every step is
+// parallel over slots:
+//   rank     one block per chunk of 256 slots: each slot's rank among the
+//            chunk's slots of the same expert (warp match + earlier warps'
+//            counts) and the chunk's expert histogram
+//   scan     one block per expert: exclusive prefix of its histogram over the
+//            chunks, and its total count
+//   scatter  one thread per slot: row = offsets[e] + chunk base + rank, with
+//            offsets the exclusive prefix of the counts over experts
 //   gather   one warp per token reads the token's row of x once and writes it
 //            to its k routed rows and to its shared-expert row S + t, in
 //            16-byte vectors
@@ -18,53 +20,63 @@
 namespace moe {
 namespace {
 
-constexpr int kChunk = 4096;
+constexpr int kChunk = 256;   // slots per block of the rank kernel (one per thread)
 constexpr int kPermThreads = 256;
 
-__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t *__restrict__ ids,
+// Block c takes slots [256c, 256c + 256), one per thread.  Equal experts
+// inside a warp are ranked with __match_any_sync; warps before this one add
+// their counts for the same expert.  Writes the slot's rank inside
+// (chunk, expert) into slot_row (the scatter adds the bases later) and the
+// chunk's expert histogram into part[c][e].
+__global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(const int32_t *__restrict__ ids,
                                                                  int S, int E,
                                                                  int32_t *__restrict__ part,
+                                                                 int32_t *__restrict__ local_rank,
                                                                  int *status) {
-    extern __shared__ int hist[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    extern __shared__ int wcnt[];  // [8][E]
+    constexpr int NW = kPermThreads / 32;
+    for (int i = threadIdx.x; i < NW * E; i += blockDim.x) wcnt[i] = 0;
     __syncthreads();
-    const int lo = blockIdx.x * kChunk;
-    const int hi = min(S, lo + kChunk);
-    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-        const int e = ids[i];
-        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-        else record_status(status, MOE_ERR_INVALID_ARG);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kChunk + threadIdx.x;
+    int e = -1;
+    if (i < S) {
+        e = ids[i];
+        if (e < 0 || e >= E) {
+            record_status(status, MOE_ERR_INVALID_ARG);
+            e = -1;
+        }
     }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(same);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) part[(size_t)blockIdx.x * E + e] = hist[e];
+    if (e >= 0) {
+        int r = rank;
+        for (int w = 0; w < warp; ++w) r += wcnt[w * E + e];
+        local_rank[i] = r;
+    }
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) c += wcnt[w * E + x];
+        part[(size_t)blockIdx.x * E + x] = c;
+    }
 }
 
-// One block of 1024 threads; thread e owns expert e.
-__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t *__restrict__ part, int nchunks,
-                                                         int S, int T, int E,
-                                                         int32_t *__restrict__ counts,
-                                                         int32_t *__restrict__ offsets) {
-    __shared__ int wsum[32];
-    const int e = threadIdx.x;
-    int run = 0;
-    if (e < E) {
-        // 8 independent loads in flight per step; the running sum follows
-        for (int b0 = 0; b0 < nchunks; b0 += 8) {
-            int v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = b0 + u < nchunks ? part[(size_t)(b0 + u) * E + e] : 0;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (b0 + u < nchunks) part[(size_t)(b0 + u) * E + e] = run;
-                run += v[u];
-            }
-        }
-        counts[e] = run;
-    }
-    // block-wide exclusive scan of run over experts
-    const int lane = e & 31, wid = e >> 5;
-    int incl = run;
+// Block e: exclusive prefix of part[c][e] over the chunks c, in place, and
+// the expert's total count.
+__global__ void __launch_bounds__(kPermThreads) perm_chunk_scan_kernel(int32_t *__restrict__ part,
+                                                                       int nchunks, int E,
+                                                                       int32_t *__restrict__ counts) {
+    __shared__ int wsum[kPermThreads / 32];
+    const int e = blockIdx.x;
+    const int per = (nchunks + kPermThreads - 1) / kPermThreads;
+    const int c0 = threadIdx.x * per;
+    int local = 0;
+    for (int c = c0; c < c0 + per && c < nchunks; ++c) local += part[(size_t)c * E + e];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -72,60 +84,70 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t *__restrict__ p
     }
     if (lane == 31) wsum[wid] = incl;
     __syncthreads();
-    if (wid == 0) {
-        int v = wsum[lane];
-        int inc = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += u;
-        }
-        wsum[lane] = inc - v;
+    int before = 0;
+    for (int w = 0; w < wid; ++w) before += wsum[w];
+    int run = before + incl - local;
+    for (int c = c0; c < c0 + per && c < nchunks; ++c) {
+        const int v = part[(size_t)c * E + e];
+        part[(size_t)c * E + e] = run;
+        run += v;
     }
-    __syncthreads();
-    const int excl = wsum[wid] + incl - run;
-    if (e < E) {
-        offsets[e] = excl;
-        for (int b = 0; b < nchunks; ++b) part[(size_t)b * E + e] += excl;
-    }
-    if (e == 0) {
-        offsets[E] = S;
-        offsets[E + 1] = S + T;
-    }
+    if (threadIdx.x == kPermThreads - 1) counts[e] = run;
 }
 
+// Exclusive prefix of counts[0..E) into sh[0..E) by one block (E <= 1024).
+__device__ void block_offsets(const int32_t *__restrict__ counts, int E, int *sh) {
+    __shared__ int wsum[kPermThreads / 32];
+    constexpr int PER = 4;  // 256 threads x 4 >= 1024 experts
+    const int e0 = threadIdx.x * PER;
+    int v[PER], local = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        v[u] = e0 + u < E ? counts[e0 + u] : 0;
+        local += v[u];
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < wid; ++w) run += wsum[w];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        if (e0 + u < E) sh[e0 + u] = run;
+        run += v[u];
+    }
+    __syncthreads();
+}
+
+// One thread per slot: row = offsets[e] + chunk base + rank in the chunk.
 __global__ void __launch_bounds__(kPermThreads) perm_scatter_kernel(
     const int32_t *__restrict__ ids, const float *__restrict__ weights,
-    const int32_t *__restrict__ part, int S, int T, int E, int k, int32_t *__restrict__ row_token,
+    const int32_t *__restrict__ part, const int32_t *__restrict__ counts, int S, int T, int E,
+    int k, int32_t *__restrict__ offsets, int32_t *__restrict__ row_token,
     int32_t *__restrict__ slot_row, float *__restrict__ row_weight) {
-    extern __shared__ int cursor[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        cursor[e] = part[(size_t)blockIdx.x * E + e];
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned lt = (1u << lane) - 1u;
-    const int lo = blockIdx.x * kChunk;
-    const int hi = min(S, lo + kChunk);
-    for (int base = lo; base < hi; base += kPermThreads) {
-        const int i = base + threadIdx.x;
-        int e = -1;
-        if (i < hi) {
-            e = ids[i];
-            if (e < 0 || e >= E) e = -1;
+    extern __shared__ int off[];  // [E]
+    block_offsets(counts, E, off);
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = off[e];
+        if (threadIdx.x == 0) {
+            offsets[E] = S;
+            offsets[E + 1] = S + T;
         }
-        const unsigned same = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(same & lt);
-        const int cnt = __popc(same);
-        for (int w = 0; w < kPermThreads / 32; ++w) {
-            if (warp == w && e >= 0) {
-                const int pos = cursor[e] + rank;
-                __syncwarp(same);
-                if (rank == 0) cursor[e] += cnt;
-                row_token[pos] = i / k;
-                slot_row[i] = pos;
-                if (row_weight) row_weight[pos] = weights[i];
-            }
-            __syncthreads();
+    }
+    const int i = blockIdx.x * kChunk + threadIdx.x;
+    if (i < S) {
+        const int e = ids[i];
+        if (e >= 0 && e < E) {
+            const int pos = off[e] + part[(size_t)blockIdx.x * E + e] + slot_row[i];
+            row_token[pos] = i / k;
+            slot_row[i] = pos;
+            if (row_weight) row_weight[pos] = weights[i];
         }
     }
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x)
@@ -193,11 +215,11 @@ moe_status launch_permute(const int32_t *ids, const float *weights, const uint16
     int32_t *part = static_cast<int32_t *>(ws);
     int *status = device_status_ptr();
     if (!status) return MOE_ERR_CUDA;
-    const size_t hsmem = (size_t)E * sizeof(int);
-    perm_hist_kernel<<<nchunks, kPermThreads, hsmem, st>>>(ids, S, E, part, status);
-    perm_scan_kernel<<<1, 1024, 0, st>>>(part, nchunks, S, T, E, counts, offsets);
-    perm_scatter_kernel<<<nchunks, kPermThreads, hsmem, st>>>(ids, weights, part, S, T, E, k,
-                                                              row_token, slot_row, row_weight);
+    perm_rank_kernel<<<nchunks, kPermThreads, (size_t)(kPermThreads / 32) * E * sizeof(int), st>>>(
+        ids, S, E, part, slot_row, status);
+    perm_chunk_scan_kernel<<<E, kPermThreads, 0, st>>>(part, nchunks, E, counts);
+    perm_scatter_kernel<<<nchunks, kPermThreads, (size_t)E * sizeof(int), st>>>(
+        ids, weights, part, counts, S, T, E, k, offsets, row_token, slot_row, row_weight);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     if (x_perm) return launch_gather_rows(x, slot_row, T, d, k, x_perm, st);

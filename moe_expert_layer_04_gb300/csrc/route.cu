@@ -14,7 +14,9 @@
 //      bound of that k-th key (almost always just the k winners) get the
 //      exact key: the sigmoid in fp64 rounded to fp32, plus the bias in one
 //      fp32 add.  The top-k of the exact keys among them is the answer, since
-//      every true winner is inside that window.
+//      every true winner is inside that window.  The window's experts are
+//      packed one per lane first: fp64 runs at a small fraction of the fp32
+//      rate here, and a warp pays for every fp64 sequence any lane needs.
 // Ties go to the lower expert id.  Weights: w_j = scaling * s_j / sum_i s_i
 // with the sum and quotient in fp64, rounded to fp32.
 #include <cfloat>
@@ -62,7 +64,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float *__restrict__ z, const float *__restrict__ bias,
     const uint8_t *__restrict__ is_vision, int T, int E, int k, float scaling,
     int32_t *__restrict__ ids, float *__restrict__ w, float *__restrict__ ssel) {
+    __shared__ int s_e[kRouteWarps][32];
+    __shared__ float s_z[kRouteWarps][32], s_b[kRouteWarps][32];
     const int lane = threadIdx.x & 31;
+    int *lst_e = s_e[threadIdx.x >> 5];
+    float *lst_z = s_z[threadIdx.x >> 5];
+    float *lst_b = s_b[threadIdx.x >> 5];
     const int gw = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
     const int nw = gridDim.x * kRouteWarps;
     for (int t = gw; t < T; t += nw) {
@@ -106,47 +113,98 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
         // few ulp of the score; the two key additions half an ulp of the key each
         const float tol = 4e-6f * fmaxf(1.0f, fabsf(kth));
         const float thr = kth - 2.0f * tol;
-        // pass 2: exact keys inside the window, then the exact top-k
-        float ek[EPL], es[EPL];
+        // pass 2: exact keys inside the window, then the exact top-k.  The
+        // window's experts are first packed one per lane, so that the warp
+        // evaluates the fp64 sigmoid once for all of them.
+        bool cand[EPL];
+        int ncand = 0;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            es[i] = 0.0f;
-            ek[i] = -INFINITY;
-            if (e < E && (key[i] >= thr || !(kth == kth))) {
-                es[i] = sigmoid_exact(zv[i]);
-                const float kk = __fadd_rn(es[i], bv[i]);
-                ek[i] = (kk == kk) ? kk : -FLT_MAX;
-            }
+            cand[i] = e < E && key[i] >= thr;
+            ncand += __popc(__ballot_sync(0xffffffffu, cand[i]));
         }
-        taken = 0;
         int my_id = 0;
         float my_s = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            float bk = -INFINITY;
-            int be = INT_MAX;
+        if (ncand <= 32) {
+            int base = 0;
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !(taken >> i & 1u) && (ek[i] > bk || (ek[i] == bk && e < be))) {
-                    bk = ek[i];
-                    be = e;
+                const unsigned m = __ballot_sync(0xffffffffu, cand[i]);
+                if (cand[i]) {
+                    const int pos = base + __popc(m & ((1u << lane) - 1u));
+                    lst_e[pos] = lane + 32 * i;
+                    lst_z[pos] = zv[i];
+                    lst_b[pos] = bv[i];
+                }
+                base += __popc(m);
+            }
+            __syncwarp();
+            int ce = INT_MAX;
+            float cs = 0.0f, ck = -INFINITY;
+            if (lane < ncand) {
+                ce = lst_e[lane];
+                cs = sigmoid_exact(lst_z[lane]);
+                const float kk = __fadd_rn(cs, lst_b[lane]);
+                ck = (kk == kk) ? kk : -FLT_MAX;
+            }
+            __syncwarp();
+            for (int j = 0; j < k; ++j) {
+                float bk = ck;
+                int be = ce;
+                warp_argmax(bk, be);
+                const unsigned owner = __ballot_sync(0xffffffffu, ce == be && be != INT_MAX);
+                const int ol = owner ? __ffs(owner) - 1 : 0;
+                const float sv = __shfl_sync(0xffffffffu, cs, ol);
+                if (lane == ol) {
+                    ck = -INFINITY;
+                    ce = INT_MAX;
+                }
+                if (lane == j) {
+                    my_id = be == INT_MAX ? 0 : be;
+                    my_s = sv;
                 }
             }
-            warp_argmax(bk, be);
-            float sv = 0.0f;
-            if (be != INT_MAX && (be & 31) == lane) {
-                const int i = be >> 5;
-                taken |= 1u << i;
+        } else {
+            // many exact ties in the window: every lane evaluates its own experts
+            float ek[EPL], es[EPL];
 #pragma unroll
-                for (int ii = 0; ii < EPL; ++ii)
-                    if (ii == i) sv = es[ii];
+            for (int i = 0; i < EPL; ++i) {
+                es[i] = 0.0f;
+                ek[i] = -INFINITY;
+                if (cand[i]) {
+                    es[i] = sigmoid_exact(zv[i]);
+                    const float kk = __fadd_rn(es[i], bv[i]);
+                    ek[i] = (kk == kk) ? kk : -FLT_MAX;
+                }
             }
-            const int owner = be == INT_MAX ? 0 : (be & 31);
-            sv = __shfl_sync(0xffffffffu, sv, owner);
-            if (lane == j) {
-                my_id = be == INT_MAX ? 0 : be;
-                my_s = sv;
+            taken = 0;
+            for (int j = 0; j < k; ++j) {
+                float bk = -INFINITY;
+                int be = INT_MAX;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E && !(taken >> i & 1u) && (ek[i] > bk || (ek[i] == bk && e < be))) {
+                        bk = ek[i];
+                        be = e;
+                    }
+                }
+                warp_argmax(bk, be);
+                float sv = 0.0f;
+                if (be != INT_MAX && (be & 31) == lane) {
+                    const int i = be >> 5;
+                    taken |= 1u << i;
+#pragma unroll
+                    for (int ii = 0; ii < EPL; ++ii)
+                        if (ii == i) sv = es[ii];
+                }
+                const int owner = be == INT_MAX ? 0 : (be & 31);
+                sv = __shfl_sync(0xffffffffu, sv, owner);
+                if (lane == j) {
+                    my_id = be == INT_MAX ? 0 : be;
+                    my_s = sv;
+                }
             }
         }
         write_weights(t, k, lane, my_id, my_s, scaling, ids, w, ssel);

@@ -52,6 +52,7 @@ class Workload:
     vision_frac: float = 0.0
     zipf_s: float = 0.0          # expert-load skew exponent (0 = none)
     hash_variant: bool = False   # also draw tid2eid and Zipf(1.0) input ids
+    bias_amp: float = 0.1        # routing bias ~ U(-bias_amp, bias_amp)
     backward: bool = False
     recompute: bool = False
     seed: int = 0
@@ -62,17 +63,27 @@ class Workload:
         return self.T * self.k
 
 
+# The full-width near-uniform workloads draw the routing bias from
+# U(-0.01, 0.01): with logits of std 1.28 (x ~ N(0,1), W_g ~ N(0,0.02),
+# d = 4096) a selection of 6 of 384 experts sits where a bias of 0.1 is worth
+# about 1.4 logit standard deviations, and U(-0.1, 0.1) leaves ~110 of the 384
+# experts without a token (the hottest gets ~300 rows), which is not the
+# near-uniform ~64 tokens/expert load these workloads stand for.  At 0.01 the
+# load is 43..96 rows per expert.  "full_fwd_bias0.1" keeps the literal range.
 WORKLOADS = {
     "tiny_fwd": Workload("tiny_fwd", 64, 128, 16, 2, 64, 1.0),
-    "full_fwd": Workload("full_fwd", 4096, 4096, 384, 6, 2048, 2.5),
+    "full_fwd": Workload("full_fwd", 4096, 4096, 384, 6, 2048, 2.5, bias_amp=0.01),
+    "full_fwd_bias0.1": Workload("full_fwd_bias0.1", 4096, 4096, 384, 6, 2048, 2.5),
     "skewed_mm_fwd": Workload("skewed_mm_fwd", 8192, 4096, 384, 6, 2048, 2.5,
                               vision_frac=0.25, zipf_s=1.1, hash_variant=True),
-    "fwd_bwd": Workload("fwd_bwd", 8192, 4096, 384, 6, 2048, 2.5, backward=True),
+    "fwd_bwd": Workload("fwd_bwd", 8192, 4096, 384, 6, 2048, 2.5, bias_amp=0.01,
+                        backward=True),
     "long_slice_fwd_bwd": Workload("long_slice_fwd_bwd", 65536, 4096, 384, 6, 2048, 2.5,
                                    vision_frac=0.30, zipf_s=1.1, backward=True,
                                    recompute=True),
 }
 ORDER = ["tiny_fwd", "full_fwd", "skewed_mm_fwd", "fwd_bwd", "long_slice_fwd_bwd"]
+# the full-width workloads with a shared expert-weight draw (same seed, same shapes)
 
 
 def scaled(w: Workload, **kw) -> Workload:
@@ -163,7 +174,7 @@ def make_inputs(w: Workload, device="cpu", with_weights=True, with_dy=None):
     """All inputs of a workload as a dict of tensors on `device`.
 
     x [T,d] bf16 ~ N(0,1); W_g [E,d], W13 [E+1,2I,d], W2 [E+1,d,I] bf16 ~ N(0,0.02)
-    (group E = shared expert); bias [2,E] fp32 ~ U(-0.1,0.1) (row 0 text, row 1
+    (group E = shared expert); bias [2,E] fp32 ~ U(-bias_amp,bias_amp) (row 0 text, row 1
     vision); is_vision [T] uint8; logit_offset [E] fp32 or None; input_ids [T]
     and tid2eid [VOCAB,k] int32 for the hash variant; dY [T,d] bf16 ~ N(0,1)."""
     s = w.seed
@@ -173,7 +184,8 @@ def make_inputs(w: Workload, device="cpu", with_weights=True, with_dy=None):
         out["W13"] = stacked_normal_bf16(w.E + 1, (2 * w.I, w.d), 0.02, s, "W13", device)
         out["W2"] = stacked_normal_bf16(w.E + 1, (w.d, w.I), 0.02, s, "W2", device)
     gb = _gen(s, "bias", device)
-    out["bias"] = (torch.rand((2, w.E), generator=gb, device=device) * 0.2 - 0.1).float()
+    out["bias"] = ((torch.rand((2, w.E), generator=gb, device=device) * 2.0 - 1.0)
+                   * w.bias_amp).float()
     out["is_vision"] = vision_mask(w.T, w.vision_frac, s, device)
     out["logit_offset"] = zipf_offsets(w.E, w.zipf_s, s, device) if w.zipf_s else None
     if w.hash_variant:

@@ -71,6 +71,20 @@ def test_route_logits_exact(T, E, k):
     np.testing.assert_allclose(np64(wt), r_w, rtol=W_RTOL, atol=0)
 
 
+def test_route_all_tied_uses_exact_fallback():
+    # every key equal: more than 32 experts sit in the exact-key window
+    T, E, k = 16, 96, 5
+    z = torch.zeros(T, E, device="cuda")
+    bias = torch.zeros(2, E, device="cuda")
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    s = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    _lib.moe_route_logits(z, bias, None, None, None, T, E, k, 2.5, MOE_ROUTE_TOPK, ids, wt, s)
+    torch.cuda.synchronize()
+    assert cpu(ids).tolist() == [list(range(k))] * T
+    assert np.all(np64(wt) == np.float32(2.5 / k))
+
+
 def test_route_hash_exact():
     T, E, k, V = 300, 384, 6, W.VOCAB
     z = W.random_logits(T, E, 1.5, seed=11).cuda()
