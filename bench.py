@@ -235,6 +235,28 @@ def run_ours(args, rank, world, local_rank):
     layer_roof_ms = max(fwd_flops(D) / (bf16 * 1e12),
                         (g1_bytes + g2_bytes + perm_bytes + comb_bytes + route_bytes) / (hbm * 1e9)) * 1e3
 
+    # ---------------- the same forward with the literal U(-0.1, 0.1) routing bias
+    literal = None
+    if wl.bias_amp != 0.1 and not args.tokens and not args.experts:
+        lw = W.scaled(wl, name=wl.name + "_bias0.1", bias_amp=0.1)
+        lbias = W.make_inputs(lw, device=dev, with_weights=False)["bias"]
+        for _ in range(args.warmup):
+            layer.forward(inp["x"], lbias, inp["is_vision"], inp["logit_offset"])
+        torch.cuda.synchronize()
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        for _ in range(args.steps):
+            layer.forward(inp["x"], lbias, inp["is_vision"], inp["logit_offset"])
+        l1.record(stream)
+        torch.cuda.synchronize()
+        lms = l0.elapsed_time(l1) / args.steps
+        lc = layer.counts.cpu().numpy()
+        literal = {"workload": f"{lw.name}: bias ~ U(-0.1, 0.1)",
+                   "value": round(world * D.T / (lms / 1e3), 1), "unit": "tokens/s",
+                   "ms_per_step": round(lms, 4), "experts_with_tokens": int((lc > 0).sum()),
+                   "max_rows_per_expert": int(lc.max())}
+
     # ---------------- end to end through the public API with host buffers
     x_host = inp["x"].cpu().pin_memory()
     y_host = torch.empty(D.T, D.d, dtype=torch.bfloat16).pin_memory()
@@ -294,6 +316,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": FWD_LAUNCHES * args.steps,
         "clocks": clk,
         "fwd_bwd": fb,
+        "literal_bias": literal,
+        "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
+                        "min_rows": int(counts.min()), "max_rows": int(counts.max())},
     }
     return line
 
