@@ -327,6 +327,9 @@ def run_fwd_bwd(args, weights, dev, world):
     from moe_expert_layer_04_gb300 import workloads as W
     from moe_expert_layer_04_gb300.layer import Dims, MoELayer
     wl = W.WORKLOADS["fwd_bwd"]
+    over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
+    if over:
+        wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()), **over)
     D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
     inp = layer_inputs(wl, dev, weights=weights)
     layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True)

@@ -302,27 +302,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + s * TS::A_BYTES);
                 const uint32_t b_addr = smem_u32(sB + s * TS::B_BYTES);
+                int n_kk = 4;
                 if constexpr (MT::KGROUP) {
+                    // ragged contraction: only the 16-row MMA steps that hold rows of
+                    // this group run; inside the last one, rows past the group's end
+                    // (the next group's rows) are zeroed in A.  B's rows there are
+                    // finite data or TMA zero fill, so they add nothing.
                     const int valid = ti.krows - kb * 64;
                     if (valid < 64) {
-                        // rows past the group's end belong to the next group: zero them
-                        const int nbox = 2 + BN / 64;
-                        const int per_box = (64 - valid) * 8;  // 16-byte chunks
-                        for (int i = lane; i < nbox * per_box; i += 32) {
-                            const int box = i / per_box;
-                            const int c = i - box * per_box;
-                            uint8_t *base = box < 2 ? sA + s * TS::A_BYTES + box * 8192
-                                                    : sB + s * TS::B_BYTES + (box - 2) * 8192;
-                            *reinterpret_cast<uint4 *>(base + valid * 128 + c * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                        n_kk = (valid + 15) >> 4;
+                        const int nrows = n_kk * 16 - valid;  // 0..15
+                        for (int i = lane; i < 2 * nrows * 8; i += 32) {
+                            const int box = i / (nrows * 8);
+                            const int rem = i - box * nrows * 8;
+                            uint8_t *dst = sA + s * TS::A_BYTES + box * 8192 +
+                                           (valid + (rem >> 3)) * 128 + (rem & 7) * 16;
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
                         }
-                        fence_proxy_async_smem();
+                        if (nrows > 0) fence_proxy_async_smem();
                         __syncwarp();
                     }
                 }
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
+                        if (kk >= n_kk) break;
                         const uint64_t ad = MT::A_MN ? sdesc_sw128(a_addr + kk * 2048, 8192, 1024)
                                                      : sdesc_sw128(a_addr + kk * 32, 16, 1024);
                         const uint64_t bd = MT::B_MN ? sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
