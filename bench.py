@@ -48,6 +48,27 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+# ------------------------------------------------------------- multi-rank
+
+def dist_barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def dist_max(value, world, device="cuda"):
+    """Max of a per-rank float over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_rank, max_ms_per_step):
+    """Whole-job tokens/s of N independent replicas timed by the slowest one."""
+    return world * tokens_per_rank / (max_ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -137,6 +158,87 @@ def workload(args):
 
 # ------------------------------------------------------------------- ours
 
+def route_kwargs(inp, mode):
+    from moe_expert_layer_04_gb300.layer import MOE_ROUTE_HASH
+    if mode == MOE_ROUTE_HASH:
+        return dict(logit_offset=None, mode=mode, input_ids=inp["input_ids"],
+                    tid2eid=inp["tid2eid"])
+    return dict(logit_offset=inp["logit_offset"])
+
+
+def forward_breakdown(layer, inp, steps, warmup, mode=0, world=1):
+    """Times `steps` forward passes, with CUDA events on the launching stream
+    around each of the layer's calls.  Returns (per-call ms, ms per step)."""
+    stream = torch.cuda.current_stream()
+    rk = route_kwargs(inp, mode)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        layer.route(inp["x"], inp["bias"], inp["is_vision"], **rk)
+        if evs is not None:
+            evs[1].record(stream)
+        layer.dispatch(inp["x"])
+        if evs is not None:
+            evs[2].record(stream)
+        layer.expert_gemm1()
+        if evs is not None:
+            evs[3].record(stream)
+        layer.expert_gemm2()
+        if evs is not None:
+            evs[4].record(stream)
+        layer.combine()
+        if evs is not None:
+            evs[5].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    ms = dist_max(t0.elapsed_time(t1), world)
+    names = ["route", "permute", "expert_gemm1", "expert_gemm2", "combine"]
+    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+           for j, n in enumerate(names)}
+    return per, ms / steps
+
+
+def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False):
+    """Per-call achieved GB/s (algorithmic bytes) and TFLOP/s with their
+    fractions of the measured peaks."""
+    g1_bytes, g2_bytes = fwd_algorithmic_bytes(D, counts)
+    if save_gu:
+        g1_bytes += D.R * 2 * D.I * 4
+    g1_flops = 4 * D.R * D.d * D.I
+    g2_flops = 2 * D.R * D.I * D.d
+    perm_bytes = D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6
+    comb_bytes = D.R * D.d * 2 + D.T * D.d * 2 + D.S * 4
+    route_bytes = D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4 * 2 + D.T * D.k * 12
+    out = {}
+    for name, by, fl in (("route", route_bytes, 2 * D.T * D.d * D.E), ("permute", perm_bytes, 0),
+                         ("expert_gemm1", g1_bytes, g1_flops), ("expert_gemm2", g2_bytes, g2_flops),
+                         ("combine", comb_bytes, 0)):
+        sec = per[name] / 1e3
+        m = {"ms": round(per[name], 4), "gbs": round(by / sec / 1e9, 1),
+             "hbm_frac": round(by / sec / 1e9 / hbm, 4)}
+        if fl:
+            m["tflops"] = round(fl / sec / 1e12, 1)
+            m["tensor_frac"] = round(fl / sec / 1e12 / bf16, 4)
+        out[name] = m
+    roof_ms = max(fwd_flops(D) / (bf16 * 1e12),
+                  (g1_bytes + g2_bytes + perm_bytes + comb_bytes + route_bytes) / (hbm * 1e9)) * 1e3
+    return out, g1_bytes, roof_ms
+
+
 def run_ours(args, rank, world, local_rank):
     from moe_expert_layer_04_gb300 import _lib
     from moe_expert_layer_04_gb300 import workloads as W
@@ -154,86 +256,21 @@ def run_ours(args, rank, world, local_rank):
     layer = MoELayer(D, weights, wl.rho, wl.clamp)
     stream = torch.cuda.current_stream()
 
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
-        layer.route(inp["x"], inp["bias"], inp["is_vision"], inp["logit_offset"])
-        if evs is not None:
-            evs[1].record(stream)
-        layer.dispatch(inp["x"])
-        if evs is not None:
-            evs[2].record(stream)
-        layer.expert_gemm1()
-        if evs is not None:
-            evs[3].record(stream)
-        layer.expert_gemm2()
-        if evs is not None:
-            evs[4].record(stream)
-        layer.combine()
-        if evs is not None:
-            evs[5].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
+    # warm-up passes (they also give the expert load), then the timed region
+    forward_breakdown(layer, inp, 1, args.warmup)
     counts = layer.counts.cpu().numpy()
     assert _lib.moe_last_device_status() == _lib.MOE_OK
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    names = ["route", "permute", "expert_gemm1", "expert_gemm2", "combine"]
-    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)) / args.steps
-           for j, n in enumerate(names)}
-    ms_step = ms / args.steps
-    value = world * D.T / (ms_step / 1e3)
-
-    g1_bytes, g2_bytes = fwd_algorithmic_bytes(D, counts)
-    g1_s = per["expert_gemm1"] / 1e3
-    achieved = g1_bytes / g1_s / 1e9
+    per, ms_step = forward_breakdown(layer, inp, args.steps, 1, world=world)
+    value = replica_throughput(world, D.T, ms_step)
+    kernels, g1_bytes, layer_roof_ms = kernel_metrics(D, counts, per, hbm, bf16)
+    achieved = kernels["expert_gemm1"]["gbs"]
     roofline = {"kernel": "expert_gemm1 (grouped GEMM 1 + clamped SwiGLU)", "bound": "hbm",
-                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": None,
-                "peak_source": peak_src,
-                "bytes_per_launch": g1_bytes}
-    g1_flops = 4 * D.R * D.d * D.I
-    g2_flops = 2 * D.R * D.I * D.d
-    kernels = {n: {"ms": round(v, 4)} for n, v in per.items()}
-    kernels["expert_gemm1"].update(tflops=round(g1_flops / g1_s / 1e12, 1),
-                                   gbs=round(achieved, 1), hbm_frac=round(achieved / hbm, 4),
-                                   tensor_frac=round(g1_flops / g1_s / 1e12 / bf16, 4))
-    g2_s = per["expert_gemm2"] / 1e3
-    kernels["expert_gemm2"].update(tflops=round(g2_flops / g2_s / 1e12, 1),
-                                   gbs=round(g2_bytes / g2_s / 1e9, 1),
-                                   hbm_frac=round(g2_bytes / g2_s / 1e9 / hbm, 4),
-                                   tensor_frac=round(g2_flops / g2_s / 1e12 / bf16, 4))
-    perm_bytes = D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6
-    kernels["permute"]["gbs"] = round(perm_bytes / (per["permute"] / 1e3) / 1e9, 1)
-    comb_bytes = D.R * D.d * 2 + D.T * D.d * 2 + D.S * 4
-    kernels["combine"]["gbs"] = round(comb_bytes / (per["combine"] / 1e3) / 1e9, 1)
-    route_bytes = D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4 * 2 + D.T * D.k * 12
-    kernels["route"]["gbs"] = round(route_bytes / (per["route"] / 1e3) / 1e9, 1)
-    layer_roof_ms = max(fwd_flops(D) / (bf16 * 1e12),
-                        (g1_bytes + g2_bytes + perm_bytes + comb_bytes + route_bytes) / (hbm * 1e9)) * 1e3
+                "peak_source": peak_src, "bytes_per_launch": g1_bytes}
 
     # ---------------- the same forward with the literal U(-0.1, 0.1) routing bias
     literal = None
@@ -253,7 +290,7 @@ def run_ours(args, rank, world, local_rank):
         lms = l0.elapsed_time(l1) / args.steps
         lc = layer.counts.cpu().numpy()
         literal = {"workload": f"{lw.name}: bias ~ U(-0.1, 0.1)",
-                   "value": round(world * D.T / (lms / 1e3), 1), "unit": "tokens/s",
+                   "value": round(replica_throughput(world, D.T, lms), 1), "unit": "tokens/s",
                    "ms_per_step": round(lms, 4), "experts_with_tokens": int((lc > 0).sum()),
                    "max_rows_per_expert": int(lc.max())}
 
@@ -266,8 +303,7 @@ def run_ours(args, rank, world, local_rank):
         layer.forward(x_dev, inp["bias"], inp["is_vision"], inp["logit_offset"])
         y_host.copy_(layer.y, non_blocking=True)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    dist_barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -277,12 +313,8 @@ def run_ours(args, rank, world, local_rank):
         y_host.copy_(layer.y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": round(world * D.T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+    e2e_ms = dist_max(e0.elapsed_time(e1) / args.steps, world)
+    e2e = {"value": round(replica_throughput(world, D.T, e2e_ms), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": D.T * D.d * 2, "d2h_bytes_per_step": D.T * D.d * 2,
            "ms_per_step": round(e2e_ms, 4)}
     del layer, x_host, y_host, x_dev
@@ -292,6 +324,12 @@ def run_ours(args, rank, world, local_rank):
     fb = None
     if not args.no_bwd:
         fb = run_fwd_bwd(args, weights, dev, world)
+
+    # ---------------- the other full-width workloads (same weights)
+    extra = None
+    if not args.no_extra and not args.tokens and not args.experts:
+        extra = run_extra_workloads(args, weights, dev, world, hbm, bf16)
+    clk = clocks.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -316,6 +354,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": FWD_LAUNCHES * args.steps,
         "clocks": clk,
         "fwd_bwd": fb,
+        "extra_workloads": extra,
         "literal_bias": literal,
         "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
                         "min_rows": int(counts.min()), "max_rows": int(counts.max())},
@@ -323,16 +362,53 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_fwd_bwd(args, weights, dev, world):
+def run_extra_workloads(args, weights, dev, world, hbm, bf16):
+    """Per-call numbers of the skewed multimodal workload (top-k and hash
+    routing) and of the 64K-token slice (forward breakdown, and forward +
+    backward with recompute).  These sizes are where the tensor-core and
+    HBM targets of the routing / dispatch / combine steps apply."""
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import MOE_ROUTE_HASH, Dims, MoELayer
+    steps = max(3, args.steps // 3)
+    out = {}
+    for name, modes in (("skewed_mm_fwd", (0, MOE_ROUTE_HASH)), ("long_slice_fwd_bwd", (0,))):
+        wl = W.WORKLOADS[name]
+        D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+        inp = layer_inputs(wl, dev, weights=weights)
+        layer = MoELayer(D, weights, wl.rho, wl.clamp)
+        for mode in modes:
+            per, ms = forward_breakdown(layer, inp, steps, args.warmup, mode=mode, world=world)
+            counts = layer.counts.cpu().numpy()
+            kern, _, roof = kernel_metrics(D, counts, per, hbm, bf16)
+            key = name + ("_hash" if mode == MOE_ROUTE_HASH else "")
+            out[key] = {"workload": f"{name}: forward, T={wl.T}" +
+                                    (", hash router" if mode == MOE_ROUTE_HASH else ", top-k router"),
+                        "value": round(replica_throughput(world, D.T, ms), 1),
+                        "unit": "tokens/s",
+                        "ms_per_step": round(ms, 4), "layer_roofline_frac": round(roof / ms, 4),
+                        "kernels": kern, "steps": steps,
+                        "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
+                                        "max_rows": int(counts.max())}}
+        del layer
+        torch.cuda.empty_cache()
+        if wl.backward and not args.no_bwd:
+            out[name + "_fwd_bwd"] = run_fwd_bwd(args, weights, dev, world, wl_name=name,
+                                                 inputs=inp)
+        del inp
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_fwd_bwd(args, weights, dev, world, wl_name="fwd_bwd", inputs=None):
     from moe_expert_layer_04_gb300 import workloads as W
     from moe_expert_layer_04_gb300.layer import Dims, MoELayer
-    wl = W.WORKLOADS["fwd_bwd"]
+    wl = W.WORKLOADS[wl_name]
     over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
     if over:
         wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()), **over)
     D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
-    inp = layer_inputs(wl, dev, weights=weights)
-    layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True)
+    inp = inputs if inputs is not None else layer_inputs(wl, dev, weights=weights)
+    layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True, recompute=wl.recompute)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
@@ -347,8 +423,7 @@ def run_fwd_bwd(args, weights, dev, world):
     torch.cuda.synchronize()
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    if world > 1:
-        torch.distributed.barrier()
+    dist_barrier(world)
     torch.cuda.synchronize()
     starts[0].record(stream)
     for i in range(steps):
@@ -357,15 +432,14 @@ def run_fwd_bwd(args, weights, dev, world):
     torch.cuda.synchronize()
     ms = starts[0].elapsed_time(starts[-1]) / steps
     bwd_ms = sum(mids[i].elapsed_time(starts[i + 1]) for i in range(steps)) / steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = dist_max(ms, world)
     out = {"workload": f"{wl.name}: forward+backward, T={wl.T} d={wl.d} E={wl.E} top-{wl.k} "
-                       f"+ shared, I={wl.I}, fp32 weight grads",
-           "value": round(world * D.T / (ms / 1e3), 1), "unit": "tokens/s",
+                       f"+ shared, I={wl.I}, fp32 weight grads"
+                       + (", recompute" if wl.recompute else ""),
+           "value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
            "ms_per_step": round(ms, 4), "bwd_ms": round(bwd_ms, 4), "steps": steps,
-           "gpu_launches": (FWD_LAUNCHES + BWD_LAUNCHES) * steps}
+           "gpu_launches": (FWD_LAUNCHES + BWD_LAUNCHES
+                            + (BWD_RECOMPUTE_EXTRA if wl.recompute else 0)) * steps}
     del layer, inp
     torch.cuda.empty_cache()
     return out
@@ -442,6 +516,8 @@ def main():
     ap.add_argument("--workload", default="full_fwd")
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the skewed and 64K-token workloads")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling)")

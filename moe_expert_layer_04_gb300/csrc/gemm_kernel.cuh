@@ -467,42 +467,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                         uint16_t *dgd = dgu + (size_t)row * 2 * p.I + col;
                         uint16_t *dud = dgd + p.I;
                         uint16_t *hwd = hw + (size_t)row * p.I + col;
+                        // all 16 vector loads of the chunk first: one memory latency per chunk
+                        float4 gv4[8], uv4[8];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            const float4 g0 = *reinterpret_cast<const float4 *>(gsrc + j);
-                            const float4 g1 = *reinterpret_cast<const float4 *>(gsrc + j + 4);
-                            const float4 u0 = *reinterpret_cast<const float4 *>(usrc + j);
-                            const float4 u1 = *reinterpret_cast<const float4 *>(usrc + j + 4);
-                            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                            uint32_t og[4], ou[4], oh[4];
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            gv4[q4] = *reinterpret_cast<const float4 *>(gsrc + 4 * q4);
+                            uv4[q4] = *reinterpret_cast<const float4 *>(usrc + 4 * q4);
+                        }
+                        const float *gv = reinterpret_cast<const float *>(gv4);
+                        const float *uv = reinterpret_cast<const float *>(uv4);
+                        uint32_t og[16], ou[16], oh[16];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                float dg2[2], du2[2], hw2[2];
+                        for (int e = 0; e < 16; ++e) {
+                            float dg2[2], du2[2], hw2[2];
 #pragma unroll
-                                for (int hlf = 0; hlf < 2; ++hlf) {
-                                    const float g = gv[2 * e + hlf];
-                                    const float u = uv[2 * e + hlf];
-                                    const float dA = __uint_as_float(r[j + 2 * e + hlf]);
-                                    const float a = fminf(g, cl);
-                                    const float b = fminf(fmaxf(u, -cl), cl);
-                                    const float sg = 1.0f / (1.0f + expf(-a));
-                                    const float si = a * sg;
-                                    // bit-identical to the forward's h (same fp32 g, u and code)
-                                    const float hv = round_bf16(swiglu_clamped(g, u, cl));
-                                    dw = fmaf(hv, dA, dw);
-                                    const float dH = w * dA;
-                                    dg2[hlf] = g <= cl ? dH * b * (sg + a * sg * (1.0f - sg)) : 0.0f;
-                                    du2[hlf] = (u >= -cl && u <= cl) ? dH * si : 0.0f;
-                                    hw2[hlf] = w * hv;
-                                }
-                                og[e] = pack_bf16x2(dg2[0], dg2[1]);
-                                ou[e] = pack_bf16x2(du2[0], du2[1]);
-                                oh[e] = pack_bf16x2(hw2[0], hw2[1]);
+                            for (int hlf = 0; hlf < 2; ++hlf) {
+                                const float g = gv[2 * e + hlf];
+                                const float u = uv[2 * e + hlf];
+                                const float dA = __uint_as_float(r[2 * e + hlf]);
+                                const float a = fminf(g, cl);
+                                const float b = fminf(fmaxf(u, -cl), cl);
+                                const float sg = 1.0f / (1.0f + expf(-a));
+                                const float si = a * sg;
+                                // bit-identical to the forward's h (same fp32 g, u and code)
+                                const float hv = round_bf16(swiglu_clamped(g, u, cl));
+                                dw = fmaf(hv, dA, dw);
+                                const float dH = w * dA;
+                                dg2[hlf] = g <= cl ? dH * b * (sg + a * sg * (1.0f - sg)) : 0.0f;
+                                du2[hlf] = (u >= -cl && u <= cl) ? dH * si : 0.0f;
+                                hw2[hlf] = w * hv;
                             }
-                            st_global_v4(dgd + j, og[0], og[1], og[2], og[3]);
-                            st_global_v4(dud + j, ou[0], ou[1], ou[2], ou[3]);
-                            st_global_v4(hwd + j, oh[0], oh[1], oh[2], oh[3]);
+                            og[e] = pack_bf16x2(dg2[0], dg2[1]);
+                            ou[e] = pack_bf16x2(du2[0], du2[1]);
+                            oh[e] = pack_bf16x2(hw2[0], hw2[1]);
+                        }
+#pragma unroll
+                        for (int q4 = 0; q4 < 16; q4 += 4) {
+                            st_global_v4(dgd + 2 * q4, og[q4], og[q4 + 1], og[q4 + 2], og[q4 + 3]);
+                            st_global_v4(dud + 2 * q4, ou[q4], ou[q4 + 1], ou[q4 + 2], ou[q4 + 3]);
+                            st_global_v4(hwd + 2 * q4, oh[q4], oh[q4 + 1], oh[q4 + 2], oh[q4 + 3]);
                         }
                     }
                 }
