@@ -133,6 +133,26 @@ moe_status moe_permute(const int32_t *ids, const float *weights, const uint16_t 
                        int32_t *slot_row, float *row_weight, uint16_t *x_perm, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* moe_permute without a workspace argument: the same dispatch with the same
+ * outputs, for callers that cannot allocate device memory -- for instance a
+ * plugin running inside a host program that owns every device allocation, or
+ * a runtime that forbids allocation once it is running so that latency stays
+ * predictable.  The pages have no counterpart of this call; it exists only for
+ * such callers.
+ * Its scratch memory is one fixed array inside the library (4 MiB per GPU that
+ * loads the library, held until the process exits), enough for
+ * ceil(T*k / 256) * E <= 1048576 -- e.g. T = 65536, k = 6, E = 384.  Larger
+ * sizes return MOE_ERR_UNSUPPORTED and launch nothing.  The call itself
+ * allocates nothing.  The first call on a device looks up the array's device
+ * address (a CUDA runtime query, done once per device); make that first call
+ * before any stream capture.  All calls share the one array: two calls whose
+ * kernels overlap on the GPU (different streams, different host threads) race
+ * and give wrong results; calls in order on one stream are safe. */
+moe_status moe_permute_noalloc(const int32_t *ids, const float *weights, const uint16_t *x, int T,
+                               int d, int E, int k, int32_t *counts, int32_t *offsets,
+                               int32_t *row_token, int32_t *slot_row, float *row_weight,
+                               uint16_t *x_perm, void *stream);
+
 /* The expert FFN on expert-contiguous rows ([HP41] §2.3 MegaMoE: two expert
  * matmuls around SwiGLU with clamp; [HPF] §01 shared expert as group E).
  * For every group g < G and row r in [offsets[g], offsets[g+1]):

@@ -30,6 +30,7 @@ MOE_ROUTE_TOPK, MOE_ROUTE_HASH = 0, 1
 MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE = 1, 2
 
 EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_permute",
+           "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout"]
 
@@ -108,6 +109,7 @@ _SIGS = {
                   _I),
     "moe_route_logits": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P], _I),
     "moe_permute": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_permute_noalloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_expert_ffn": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _Z, _P], _I),
     "moe_expert_gemm1": ([_P, _P, _I, _I, _P, _I, _I, _F, _P, _P, _P], _I),
     "moe_expert_gemm2": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -213,6 +215,19 @@ def moe_permute(ids, weights, x, T, d, E, k, counts, offsets, row_token, slot_ro
                             _ptr(x_perm, BF16, "x_perm"), _ptr(ws, U8, "ws"),
                             0 if ws is None else ws.numel(), _stream(stream))
     _check("moe_permute", st)
+
+
+def moe_permute_noalloc(ids, weights, x, T, d, E, k, counts, offsets, row_token, slot_row,
+                        row_weight, x_perm, stream=None):
+    """moe_permute with the library's fixed scratch array instead of a workspace."""
+    st = load().moe_permute_noalloc(_ptr(ids, I32, "ids"), _ptr(weights, F32, "weights"),
+                                    _ptr(x, BF16, "x"), T, d, E, k, _ptr(counts, I32, "counts"),
+                                    _ptr(offsets, I32, "offsets"),
+                                    _ptr(row_token, I32, "row_token"),
+                                    _ptr(slot_row, I32, "slot_row"),
+                                    _ptr(row_weight, F32, "row_weight"),
+                                    _ptr(x_perm, BF16, "x_perm"), _stream(stream))
+    _check("moe_permute_noalloc", st)
 
 
 def moe_expert_ffn(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, gu_save,

@@ -15,6 +15,8 @@
 //   gather   one warp per token reads the token's row of x once and writes it
 //            to its k routed rows and to its shared-expert row S + t, in
 //            16-byte vectors
+#include <mutex>
+
 #include "moe_ptx.cuh"
 
 namespace moe {
@@ -227,3 +229,63 @@ moe_status launch_permute(const int32_t *ids, const float *weights, const uint16
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of moe_permute.
+//
+// The only scratch memory moe_permute needs is the per-(chunk, expert)
+// histogram that the rank / scan / scatter kernels share.  Here it lives in a
+// file-scope device array instead of the caller's workspace, so a caller that
+// cannot allocate device memory can still run the dispatch.  Every GPU that
+// loads this library keeps the array (kNoAllocScratchInts * 4 bytes = 4 MiB)
+// until the process exits.
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchInts = (size_t)1 << 20;
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchInts];
+
+std::mutex g_noalloc_mu;
+int32_t *g_noalloc_ptr[64];
+
+// Device address of the scratch array on the current device.  Host code only
+// sees a host-side stand-in under the array's name, so the real address is
+// asked for once per device (with that device current) and cached.
+int32_t *noalloc_scratch() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        int32_t *p = nullptr;
+        if (cudaGetSymbolAddress((void **)&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const int32_t *ids, const float *weights,
+                                          const uint16_t *x, int T, int d, int E, int k,
+                                          int32_t *counts, int32_t *offsets, int32_t *row_token,
+                                          int32_t *slot_row, float *row_weight, uint16_t *x_perm,
+                                          void *stream) {
+    using namespace moe;
+    if (T < 1 || E < 1 || k < 1 || k > E || d < 1) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || E > 1024 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)T * k + T >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!ids || !counts || !offsets || !row_token || !slot_row) return MOE_ERR_INVALID_ARG;
+    if (row_weight && !weights) return MOE_ERR_INVALID_ARG;
+    if (x_perm && (!x || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+    // the histogram needs ceil(T*k / 256) * E ints of the fixed array
+    if (permute_workspace_bytes(T, E, k) > kNoAllocScratchInts * sizeof(int32_t))
+        return MOE_ERR_UNSUPPORTED;
+    int32_t *scratch = noalloc_scratch();
+    if (!scratch) return MOE_ERR_CUDA;
+    // every histogram entry the scatter reads is written earlier in the same
+    // call, so nothing in the array has to start at zero
+    return launch_permute(ids, weights, x, T, d, E, k, counts, offsets, row_token, slot_row,
+                          row_weight, x_perm, scratch, static_cast<cudaStream_t>(stream));
+}
