@@ -513,16 +513,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             } else {  // GM_WGRAD: TMA stores of 32 x 32 fp32 blocks through shared memory
                 uint8_t *stg = sEpi + (size_t)(warp - 2) * 8192;
                 const uint32_t sw = (uint32_t)(lane & 7);
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    if (ti.kb > 0) {
-                        tmem_ld32(tb + c, r);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = 0u;
-                    }
+                const bool has_k = ti.kb > 0;
+                // stage one 32 x 32 block (this thread's row) and store it with TMA
+                auto store_block = [&](const uint32_t (&v)[32], int c) {
                     uint8_t *buf = stg + ((c >> 5) & 1) * 4096;
                     // the store issued two blocks ago read this buffer: wait for it
                     if (lane == 0) bulk_wait_group_read<1>();
@@ -530,14 +523,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                     const uint32_t row_addr = smem_u32(buf) + (uint32_t)lane * 128u;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        st_shared_v4(row_addr + ((((uint32_t)j) ^ sw) << 4), r[4 * j], r[4 * j + 1],
-                                     r[4 * j + 2], r[4 * j + 3]);
+                        st_shared_v4(row_addr + ((((uint32_t)j) ^ sw) << 4), v[4 * j], v[4 * j + 1],
+                                     v[4 * j + 2], v[4 * j + 3]);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         tma_store_2d(&p.tmO, buf, ti.nt * BN + c, ti.g * p.M + ti.m0 + q * 32);
                         bulk_commit_group();
                     }
+                };
+                // two register sets: the TMEM load of the next block is in flight
+                // while the current one is staged
+                uint32_t ra[32], rb[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    ra[j] = 0u;
+                    rb[j] = 0u;
+                }
+                if (has_k) {
+                    tmem_ld32(tb, ra);
+                    tmem_wait_ld();
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 64) {
+                    if (has_k) tmem_ld32(tb + c + 32, rb);
+                    store_block(ra, c);
+                    if (has_k) tmem_wait_ld();
+                    if (has_k && c + 64 < BN) tmem_ld32(tb + c + 64, ra);
+                    store_block(rb, c + 32);
+                    if (has_k) tmem_wait_ld();
                 }
             }
             tc_fence_before();

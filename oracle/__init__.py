@@ -77,6 +77,7 @@ def _load():
                 "orc_layer_backward": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P,
                                         _I, _I, _P, _I, _I, _I, _I, _D, _D, _I,
                                         _P, _P, _P], None),
+                "orc_rows_dA": ([_P, _P, _I, _I, _P, _P, _I, _I, _P], None),
                 "orc_expert_wgrad": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _D, _I,
                                       _I, _P, _P], None),
                 "orc_expert_wgrad_entries": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I,
@@ -262,6 +263,19 @@ def layer_backward(x, W_g, W13, W2, dY, bias, k, rho, clamp, is_vision=None, mod
                                _ptr(tk), d, E, k, I, float(rho), float(clamp), int(exact),
                                _ptr(dX), _ptr(dz), _ptr(dw))
     return dict(dX=dX, dz=dz, dw=dw)
+
+
+def rows_dA(dY, W2, row_tok, row_exp):
+    """dA[r] = dY[row_tok[r]] W2[row_exp[r]] (length I): the gradient at the
+    SwiGLU output of each listed expert row, before the routing weight."""
+    (dy, w2), bf = _floats(dY, W2)
+    d = dy.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    re = np.ascontiguousarray(_to_np(row_exp), dtype=np.int32)
+    out = np.empty((rt.shape[0], I), np.float64)
+    _load().orc_rows_dA(_ptr(dy), _ptr(w2), bf, rt.shape[0], _ptr(rt), _ptr(re), d, I, _ptr(out))
+    return out
 
 
 def expert_wgrad(x, W13, W2, dY, e, row_tok, row_w, clamp, exact=False, want=("dW13", "dW2"),

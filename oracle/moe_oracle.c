@@ -480,6 +480,26 @@ void orc_layer_backward(const void *x, const void *Wg, const void *W13, const vo
     free(z); free(ids); free(w); free(ssel); free(margin);
 }
 
+/* Gradient reaching the SwiGLU output of one expert row, before the routing
+ * weight (the first product of the expert backward):
+ *   dA[r, i] = sum_m dY[t_r, m] W2[e_r][m, i]          (length I per row)
+ * for rows with token row_tok[r] and expert row_exp[r]. */
+void orc_rows_dA(const void *dY, const void *W2, int bf, int n, const int64_t *row_tok,
+                 const int32_t *row_exp, int d, int I, double *dA)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+        double *out = dA + (size_t)r * I;
+        for (int i = 0; i < I; ++i) out[i] = 0.0;
+        size_t w2 = (size_t)row_exp[r] * d * I;
+        for (int m = 0; m < d; ++m) {
+            double y = ld(dY, (size_t)row_tok[r] * d + m, bf);
+            if (y == 0.0) continue;
+            for (int i = 0; i < I; ++i) out[i] += y * ld(W2, w2 + (size_t)m * I + i, bf);
+        }
+    }
+}
+
 /* Weight gradients of one expert e from the rows routed to it:
  *   dW2[e]  = sum_r dy_r (w_r h_r)^T           [d, I]
  *   dW13[e] = sum_r [dg_r | du_r] x_r^T        [2I, d]

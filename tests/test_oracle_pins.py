@@ -387,3 +387,16 @@ def test_wgrad_entries_match_full_and_bf16_storage():
     for key in ("dW13", "dW2"):
         rel = np.linalg.norm(a[key] - b[key]) / np.linalg.norm(a[key])
         assert 0 < rel < 1e-2
+
+
+def test_rows_dA_is_the_transposed_product():
+    rng = np.random.default_rng(9)
+    T, d, I, G = 7, 24, 10, 3
+    dY = _rand((T, d), 1.0, rng)
+    W2 = _rand((G, d, I), 0.3, rng)
+    rt = np.array([0, 3, 3, 6, 1])
+    re = np.array([2, 0, 1, 2, 0], np.int32)
+    got = oracle.rows_dA(dY, W2, rt, re)
+    ref = np.stack([torch.from_numpy(W2[e]).T.matmul(torch.from_numpy(dY[t])).numpy()
+                    for t, e in zip(rt, re)])
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-13)
