@@ -30,7 +30,6 @@
 namespace moe {
 
 constexpr int kStageBudget = 192 * 1024;
-constexpr int kGemmThreads = 192;
 
 struct GemmParams {
     CUtensorMap tmA;
@@ -61,6 +60,10 @@ struct GemmParams {
 
 template <int MODE>
 struct ModeTraits {
+    // epilogue warps: two per TMEM lane quadrant (each drains half the
+    // columns) for the write-bound weight gradients, one otherwise
+    static constexpr int NEPI = (MODE == GM_WGRAD) ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * NEPI;
     static constexpr bool A_MN = (MODE == GM_WGRAD);
     static constexpr bool B_MN = (MODE == GM_DGRAD2 || MODE == GM_DGRAD1 || MODE == GM_WGRAD);
     static constexpr bool DENSE = (MODE == GM_GATE);
@@ -70,7 +73,9 @@ struct ModeTraits {
 
 // Epilogue staging of the TMA-store path (GM_WGRAD): per epilogue warp two
 // 32 x 32 fp32 blocks (4 KB each, 128-byte swizzled), double buffered.
-constexpr int kEpiStageBytes = 4 * 2 * 4096;
+constexpr int kEpiWarpBytes = 2 * 4096;
+// Operand stages plus staging of the TMA-store path.
+constexpr int kStoreModeBudget = 208 * 1024;
 
 template <int BN, int MODE>
 struct TileShape {
@@ -78,8 +83,9 @@ struct TileShape {
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BN * 64 * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int EPI_BYTES = TMA_STORE ? kEpiStageBytes : 0;
-    static constexpr int STAGES = (kStageBudget - EPI_BYTES) / STAGE_BYTES;
+    static constexpr int EPI_BYTES = TMA_STORE ? ModeTraits<MODE>::NEPI * kEpiWarpBytes : 0;
+    static constexpr int STAGES =
+        ((TMA_STORE ? kStoreModeBudget : kStageBudget) - EPI_BYTES) / STAGE_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {64, 128, 256}: a power of two
 };
 
@@ -146,7 +152,8 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
 }
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmParams p) {
     using MT = ModeTraits<MODE>;
     using TS = TileShape<BN, MODE>;
     constexpr int STAGES = TS::STAGES;
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], 32 * MT::NEPI);
         }
         mbar_init(done, 1);
         *abort_s = 0;
@@ -349,8 +356,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             mbar_wait_teardown(done, 0, p.wait_limit);
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        const int q = warp & 3;
+        // ------------------------------------------------ epilogue (warps 2..)
+        const int q = warp & 3;           // TMEM lane quadrant this warp may read
+        const int ew = warp - 2;          // epilogue warp index
         const int r_local = q * 32 + lane;
         int it = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
@@ -511,9 +519,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                 }
                 if (valid) p.out4[(size_t)row * p.n_tiles + ti.nt] = dw;
             } else {  // GM_WGRAD: TMA stores of 32 x 32 fp32 blocks through shared memory
-                uint8_t *stg = sEpi + (size_t)(warp - 2) * 8192;
+                uint8_t *stg = sEpi + (size_t)ew * kEpiWarpBytes;
                 const uint32_t sw = (uint32_t)(lane & 7);
                 const bool has_k = ti.kb > 0;
+                // this warp's share of the columns
+                constexpr int CW = BN / (MT::NEPI / 4);
+                const int c_lo = (ew >> 2) * CW;
                 // stage one 32 x 32 block (this thread's row) and store it with TMA
                 auto store_block = [&](const uint32_t (&v)[32], int c) {
                     uint8_t *buf = stg + ((c >> 5) & 1) * 4096;
@@ -541,15 +552,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                     rb[j] = 0u;
                 }
                 if (has_k) {
-                    tmem_ld32(tb, ra);
+                    tmem_ld32(tb + c_lo, ra);
                     tmem_wait_ld();
                 }
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 64) {
-                    if (has_k) tmem_ld32(tb + c + 32, rb);
+                for (int c = c_lo; c < c_lo + CW; c += 64) {
+                    const bool more1 = c + 32 < c_lo + CW;
+                    if (has_k && more1) tmem_ld32(tb + c + 32, rb);
                     store_block(ra, c);
+                    if (!more1) break;
                     if (has_k) tmem_wait_ld();
-                    if (has_k && c + 64 < BN) tmem_ld32(tb + c + 64, ra);
+                    if (has_k && c + 64 < c_lo + CW) tmem_ld32(tb + c + 64, ra);
                     store_block(rb, c + 32);
                     if (has_k) tmem_wait_ld();
                 }

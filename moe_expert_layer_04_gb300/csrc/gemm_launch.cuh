@@ -27,7 +27,7 @@ moe_status launch_gemm(GemmParams &p, int max_tiles, cudaStream_t st) {
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
     const size_t smem = gemm_smem_bytes<BN, MODE>(ModeTraits<MODE>::DENSE ? 0 : p.G);
-    kern<<<grid, kGemmThreads, smem, st>>>(p);
+    kern<<<grid, ModeTraits<MODE>::THREADS, smem, st>>>(p);
     return cuda_status(cudaGetLastError());
 }
 

@@ -78,6 +78,8 @@ def _load():
                                         _I, _I, _P, _I, _I, _I, _I, _D, _D, _I,
                                         _P, _P, _P], None),
                 "orc_rows_dA": ([_P, _P, _I, _I, _P, _P, _I, _I, _P], None),
+                "orc_wgrad2_entries_given_h": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P,
+                                                _P], None),
                 "orc_expert_wgrad": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _D, _I,
                                       _I, _P, _P], None),
                 "orc_expert_wgrad_entries": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I,
@@ -275,6 +277,23 @@ def rows_dA(dY, W2, row_tok, row_exp):
     re = np.ascontiguousarray(_to_np(row_exp), dtype=np.int32)
     out = np.empty((rt.shape[0], I), np.float64)
     _load().orc_rows_dA(_ptr(dy), _ptr(w2), bf, rt.shape[0], _ptr(rt), _ptr(re), d, I, _ptr(out))
+    return out
+
+
+def wgrad2_entries_given_h(dY, h_rows, row_tok, row_w, qa, qb, store_bf16=True):
+    """dW2 entries sum_r dY[row_tok[r], qa] * (row_w[r] h_rows[r, qb]) from given
+    intermediate rows (checks the weight-gradient matmul on its own)."""
+    (dy, h), bf = _floats(dY, h_rows)
+    d = dy.shape[1]
+    I = h.shape[1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    rw = np.ascontiguousarray(_to_np(row_w), dtype=np.float64)
+    a = np.ascontiguousarray(qa, dtype=np.int32)
+    b = np.ascontiguousarray(qb, dtype=np.int32)
+    out = np.empty((a.shape[0],), np.float64)
+    _load().orc_wgrad2_entries_given_h(_ptr(dy), _ptr(h), bf, rt.shape[0], _ptr(rt), _ptr(rw), d,
+                                       I, int(store_bf16), a.shape[0], _ptr(a), _ptr(b),
+                                       _ptr(out))
     return out
 
 

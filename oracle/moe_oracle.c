@@ -500,6 +500,27 @@ void orc_rows_dA(const void *dY, const void *W2, int bf, int n, const int64_t *r
     }
 }
 
+/* Entries of the down-projection weight gradient of one expert from given
+ * intermediate rows h (the plain sum, for checking the matmul alone):
+ *   out[q] = sum_r dY[t_r, qa[q]] * w_r h[r, qb[q]]
+ * with w_r h rounded to bf16 when store_bf16 (h is [n_rows, I]). */
+void orc_wgrad2_entries_given_h(const void *dY, const void *h, int bf, int n_rows,
+                                const int64_t *row_tok, const double *row_w, int d, int I,
+                                int store_bf16, int nq, const int32_t *qa, const int32_t *qb,
+                                double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < nq; ++q) {
+        double acc = 0.0;
+        for (int r = 0; r < n_rows; ++r) {
+            double hw = row_w[r] * ld(h, (size_t)r * I + qb[q], bf);
+            if (store_bf16) hw = rbf16(hw);
+            acc += ld(dY, (size_t)row_tok[r] * d + qa[q], bf) * hw;
+        }
+        out[q] = acc;
+    }
+}
+
 /* Weight gradients of one expert e from the rows routed to it:
  *   dW2[e]  = sum_r dy_r (w_r h_r)^T           [d, I]
  *   dW13[e] = sum_r [dg_r | du_r] x_r^T        [2I, d]

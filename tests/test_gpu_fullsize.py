@@ -146,8 +146,17 @@ def _check_backward_sampled(layer, inp, w, weights, counts, n_tok, n_ent):
                                               rw_all[rows], w.clamp, kind, qa, qb, store_bf16=True)
         g2 = layer.dW2[e][torch.from_numpy(qa[:n_ent]).long().cuda(), torch.from_numpy(qb[:n_ent]).long().cuda()]
         g13 = layer.dW13[e][torch.from_numpy(qa[n_ent:]).long().cuda(), torch.from_numpy(qb[n_ent:]).long().cuda()]
-        assert_close(g2, got_ref[:n_ent], f"{w.name} dW2[{e}] entries")
-        assert_close(g13, got_ref[n_ent:], f"{w.name} dW13[{e}] entries")
+        # stage-wise: the weight-gradient matmul on the GPU's own h rows
+        h_rows = layer.h_perm[int(offs[e]):int(offs[e + 1])]
+        stage = oracle.wgrad2_entries_given_h(dY, h_rows.cpu(), rt_all[rows], rw_all[rows],
+                                              qa[:n_ent], qb[:n_ent], store_bf16=True)
+        assert_close(g2, stage, f"{w.name} dW2[{e}] entries (stage-wise)")
+        # end to end: over K rows, one-ulp bf16 flips of h (fp32 vs fp64
+        # accumulators) add up to ~sqrt(K * 3e-4) ulps; the bound scales with
+        # the entries' size above 5e-2
+        tol = max(5e-2, 1e-3 * np.abs(got_ref).max())
+        assert_close(g2, got_ref[:n_ent], f"{w.name} dW2[{e}] entries", max_abs=tol)
+        assert_close(g13, got_ref[n_ent:], f"{w.name} dW13[{e}] entries", max_abs=tol)
 
 
 def test_full_fwd(weights):

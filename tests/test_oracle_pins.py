@@ -400,3 +400,20 @@ def test_rows_dA_is_the_transposed_product():
     ref = np.stack([torch.from_numpy(W2[e]).T.matmul(torch.from_numpy(dY[t])).numpy()
                     for t, e in zip(rt, re)])
     np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_wgrad2_from_given_h_matches_full_wgrad():
+    # with h taken from the oracle's own forward, the two routines agree
+    w = W.scaled(W.WORKLOADS["tiny_fwd"], T=24)
+    inp = W.make_inputs(w, with_dy=True)
+    e = 3
+    rt = np.arange(0, w.T, 2)
+    rw = np.linspace(0.2, 0.9, len(rt))
+    h, _ = oracle.expert_rows(inp["x"], inp["W13"], inp["W2"], rt,
+                              np.full(len(rt), e, np.int32), None, w.clamp)
+    full = oracle.expert_wgrad(inp["x"], inp["W13"], inp["W2"], inp["dY"], e, rt, rw, w.clamp,
+                               want=("dW2",), store_bf16=True)["dW2"]
+    qa = np.array([0, 5, 77, 127], np.int32)
+    qb = np.array([0, 63, 10, 31], np.int32)
+    got = oracle.wgrad2_entries_given_h(inp["dY"], h, rt, rw, qa, qb, store_bf16=True)
+    np.testing.assert_allclose(got, full[qa, qb], rtol=1e-12, atol=1e-12)
