@@ -163,9 +163,12 @@ moe_status moe_permute_noalloc(const int32_t *ids, const float *weights, const u
  * Arguments: x_perm [R,d] bf16 with R = offsets[G]; offsets [G+1] int32
  * (device; e.g. the E+2 offsets of moe_permute with G = E+1); W13 [G,2I,d],
  * W2 [G,d,I] bf16; row_weight [S] fp32 or NULL; S = rows carrying a routing
- * weight.  Outputs h_perm [R,I] bf16, y_perm [R,d] bf16, and gu_save [R,2I]
- * fp32 (the GEMM-1 accumulators g then u, kept for the backward, which
- * recomputes h from them bit for bit) when not NULL.  max_rows is an upper
+ * weight.  Outputs h_perm [R,I] bf16, y_perm [R,d] bf16, and gu_save (when
+ * not NULL): the fp32 GEMM-1 accumulators g (columns 0..I-1) and u (columns
+ * I..2I-1), kept for the backward, which recomputes h from them bit for bit.
+ * gu_save holds ceil(R/32)*32 x 2I floats in blocks of 32 rows: element
+ * (r, c) is at ((r/32)*(I/2) + c/4)*128 + (r%32)*4 + c%4 (row-block
+ * interleaved, so that 32 rows are read and written in contiguous runs).  max_rows is an upper
  * bound of R known on the host (sizes the launch; S + T for a full layer).
  * Workspace: none is needed (ws may be NULL). */
 moe_status moe_expert_ffn(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
@@ -213,7 +216,7 @@ typedef struct {
     const int32_t *row_token;     /* [S+T] */
     const int32_t *slot_row;      /* [S] */
     const uint16_t *x_perm;       /* [S+T,d]; ignored with MOE_FLAG_RECOMPUTE */
-    const float *gu_save;         /* [S+T,2I] fp32; ignored with MOE_FLAG_RECOMPUTE */
+    const float *gu_save;         /* moe_expert_ffn's gu_save; ignored with MOE_FLAG_RECOMPUTE */
     /* upstream gradient */
     const uint16_t *dY;           /* [T,d] */
     /* outputs (overwritten) */

@@ -94,7 +94,7 @@ BwdWorkspace carve_bwd(uint8_t *base, int T, int d, int E, int k, int I, int fla
     w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
     if (flags & MOE_FLAG_RECOMPUTE) {
         w.x_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
-        w.gu = reinterpret_cast<float *>(take(R * 2 * I * 4));
+        w.gu = reinterpret_cast<float *>(take((R + 31) / 32 * 32 * 2 * I * 4));
     }
     w.bytes = off;
     return w;

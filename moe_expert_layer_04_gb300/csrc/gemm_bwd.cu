@@ -15,7 +15,8 @@ namespace moe {
 
 static int dgrad2_bn(int I) { return (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64; }
 
-int dgrad2_n_tiles(int I) { return I / dgrad2_bn(I); }
+// dw partial sums per row: one per column tile and epilogue warp half
+int dgrad2_n_tiles(int I) { return I / dgrad2_bn(I) * 2; }
 
 moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G, int max_rows,
                          const uint16_t *W2, const float *gu, const float *row_w, int S,
@@ -42,7 +43,7 @@ moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G,
     p.row_w = row_w;
     p.w_rows = S;
     p.gu_in = gu;
-    if (dw_tiles) *dw_tiles = p.n_tiles;
+    if (dw_tiles) *dw_tiles = dgrad2_n_tiles(I);
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     switch (BN) {
         case 256: return launch_gemm<GM_DGRAD2, 256>(p, tiles, st);
@@ -78,9 +79,11 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     if (M % 128 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
-    // 128-wide tiles: the output write stream is the bound, and the smaller
-    // tile keeps more operand stages in flight (measured faster than 256)
-    const int BN = (N % 128 == 0) ? 128 : 64;
+    // Short contractions (few rows per group) make the fp32 output stream the
+    // bound: 128-wide tiles keep more operand stages in flight.  Long ones are
+    // tensor-bound: 256-wide tiles halve the operand reads per FLOP.
+    const bool long_k = (long long)R >= 512LL * G;
+    const int BN = (long_k && N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
     if (!encode_tmap_bf16_2d(&p.tmA, A, M, R, (uint64_t)M * 2, 64, 64)) return MOE_ERR_CUDA;
     if (!encode_tmap_bf16_2d(&p.tmB, B, N, R, (uint64_t)N * 2, 64, 64)) return MOE_ERR_CUDA;
     if (!encode_tmap_f32_2d(&p.tmO, dW, N, (uint64_t)G * M, (uint64_t)N * 4, 32, 32))
@@ -93,8 +96,11 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     p.M = M;
     p.out = dW;
     const int tiles = G * p.m_tiles * p.n_tiles;
-    return BN == 128 ? launch_gemm<GM_WGRAD, 128>(p, tiles, st)
-                     : launch_gemm<GM_WGRAD, 64>(p, tiles, st);
+    switch (BN) {
+        case 256: return launch_gemm<GM_WGRAD, 256>(p, tiles, st);
+        case 128: return launch_gemm<GM_WGRAD, 128>(p, tiles, st);
+        default: return launch_gemm<GM_WGRAD, 64>(p, tiles, st);
+    }
 }
 
 }  // namespace moe

@@ -47,12 +47,12 @@ struct GemmParams {
     int I;                   // intermediate size (FFN1 / DGRAD2)
     float clamp;
     void *out;               // main output
-    void *out2;              // FFN1: fp32 g|u save (nullable); DGRAD2: dGU
+    void *out2;              // FFN1: fp32 g|u save, gu_offset layout (nullable); DGRAD2: dGU
     void *out3;              // DGRAD2: w h
-    float *out4;             // DGRAD2: dw partials [rows, n_tiles]
+    float *out4;             // DGRAD2: dw partials [rows, n_tiles * 2]
     const float *row_w;      // FFN2 / DGRAD2 routing weight of rows < w_rows
     int w_rows;
-    const float *gu_in;      // DGRAD2: saved fp32 g|u [rows, 2I]
+    const float *gu_in;      // DGRAD2: saved fp32 g|u (gu_offset layout)
     const float *col_add;    // GM_GATE: per-column offset (nullable)
     int *status;
     long long wait_limit;
@@ -61,8 +61,9 @@ struct GemmParams {
 template <int MODE>
 struct ModeTraits {
     // epilogue warps: two per TMEM lane quadrant (each drains half the
-    // columns) for the write-bound weight gradients, one otherwise
-    static constexpr int NEPI = (MODE == GM_WGRAD) ? 8 : 4;
+    // columns) where the epilogue carries real work -- the weight gradients'
+    // output stream and the SwiGLU backward of dgrad 2 -- one otherwise
+    static constexpr int NEPI = (MODE == GM_WGRAD || MODE == GM_DGRAD2) ? 8 : 4;
     static constexpr int THREADS = 64 + 32 * NEPI;
     static constexpr bool A_MN = (MODE == GM_WGRAD);
     static constexpr bool B_MN = (MODE == GM_DGRAD2 || MODE == GM_DGRAD1 || MODE == GM_WGRAD);
@@ -143,6 +144,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
         ti.kb = (ti.krows + 63) >> 6;
     }
     return ti;
+}
+
+// Offset (in floats) of element (row, col) of the saved fp32 [g | u] buffer.
+// Layout: blocks of 32 rows; inside a block, groups of 4 columns; inside a
+// group, the 32 rows' 4 values back to back.  An epilogue warp owns 32
+// consecutive rows (one per lane), so its 16-byte accesses to a column group
+// cover one or two contiguous 512-byte runs instead of 32 scattered rows.
+__device__ __forceinline__ size_t gu_offset(int row, int col, int I) {
+    return ((size_t)(row >> 5) * (size_t)(I >> 1) + (size_t)(col >> 2)) * 128 +
+           (size_t)(row & 31) * 4 + (size_t)(col & 3);
 }
 
 __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
@@ -424,12 +435,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                                 st_global_v4(dst + 2 * j, hp[j], hp[j + 1], hp[j + 2], hp[j + 3]);
                         }
                         if (gu) {
-                            float *gd = gu + (size_t)row * 2 * p.I + col;
-                            float *ud = gd + p.I;
 #pragma unroll
                             for (int j = 0; j < 32; j += 4) {
-                                st_global_v4(gd + j, rg[j], rg[j + 1], rg[j + 2], rg[j + 3]);
-                                st_global_v4(ud + j, ru[j], ru[j + 1], ru[j + 2], ru[j + 3]);
+                                st_global_v4(gu + gu_offset(row, col + j, p.I), rg[j], rg[j + 1],
+                                             rg[j + 2], rg[j + 3]);
+                                st_global_v4(gu + gu_offset(row, p.I + col + j, p.I), ru[j],
+                                             ru[j + 1], ru[j + 2], ru[j + 3]);
                             }
                         }
                     }
@@ -463,15 +474,15 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
                 const float cl = p.clamp;
                 float dw = 0.0f;
+                constexpr int CW2 = BN / (MT::NEPI / 4);   // this warp's columns
+                const int c_lo2 = (ew >> 2) * CW2;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = c_lo2; c < c_lo2 + CW2; c += 32) {
                     uint32_t r[32];
                     tmem_ld32(tb + c, r);
                     tmem_wait_ld();
                     if (valid) {
                         const int col = ti.nt * BN + c;
-                        const float *gsrc = p.gu_in + (size_t)row * 2 * p.I + col;
-                        const float *usrc = gsrc + p.I;
                         uint16_t *dgd = dgu + (size_t)row * 2 * p.I + col;
                         uint16_t *dud = dgd + p.I;
                         uint16_t *hwd = hw + (size_t)row * p.I + col;
@@ -479,8 +490,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                         float4 gv4[8], uv4[8];
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4) {
-                            gv4[q4] = *reinterpret_cast<const float4 *>(gsrc + 4 * q4);
-                            uv4[q4] = *reinterpret_cast<const float4 *>(usrc + 4 * q4);
+                            gv4[q4] = *reinterpret_cast<const float4 *>(
+                                p.gu_in + gu_offset(row, col + 4 * q4, p.I));
+                            uv4[q4] = *reinterpret_cast<const float4 *>(
+                                p.gu_in + gu_offset(row, p.I + col + 4 * q4, p.I));
                         }
                         const float *gv = reinterpret_cast<const float *>(gv4);
                         const float *uv = reinterpret_cast<const float *>(uv4);
@@ -517,7 +530,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                         }
                     }
                 }
-                if (valid) p.out4[(size_t)row * p.n_tiles + ti.nt] = dw;
+                // one partial of <h, dA> per (row, column tile, warp half)
+                if (valid)
+                    p.out4[((size_t)row * p.n_tiles + ti.nt) * (MT::NEPI / 4) + (ew >> 2)] = dw;
             } else {  // GM_WGRAD: TMA stores of 32 x 32 fp32 blocks through shared memory
                 uint8_t *stg = sEpi + (size_t)ew * kEpiWarpBytes;
                 const uint32_t sw = (uint32_t)(lane & 7);

@@ -67,7 +67,8 @@ class MoELayer:
         self.x_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
         self.h_perm = torch.empty(D.R, D.I, dtype=torch.bfloat16, **e)
         self.y_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
-        self.gu_save = (torch.empty(D.R, 2 * D.I, dtype=torch.float32, **e)
+        # fp32 g|u, row-block interleaved in blocks of 32 rows (see moe.h)
+        self.gu_save = (torch.empty((D.R + 31) // 32 * 32, 2 * D.I, dtype=torch.float32, **e)
                         if backward and not recompute else None)
         self.y = torch.empty(D.T, D.d, dtype=torch.bfloat16, **e)
         flags = (MOE_FLAG_BACKWARD if backward else 0) | (MOE_FLAG_RECOMPUTE if recompute else 0)
