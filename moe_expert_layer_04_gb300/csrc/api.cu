@@ -129,7 +129,8 @@ int num_sms() {
 
 static bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, uint64_t inner,
                       uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner,
-                      uint32_t box_outer) {
+                      uint32_t box_outer,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_encode) {
@@ -148,7 +149,7 @@ static bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, const void *base,
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return g_encode(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -157,6 +158,12 @@ bool encode_tmap_bf16_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint
                          uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
     return encode_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_pitch_bytes,
                      box_inner, box_outer);
+}
+
+bool encode_tmap_bf16_2d_sw64(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+                              uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+    return encode_2d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_pitch_bytes,
+                     box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool encode_tmap_f32_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,

@@ -30,6 +30,10 @@ moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G,
     // W2 as [G*d rows (contraction), I columns (output)], MN-major boxes
     if (!encode_tmap_bf16_2d(&p.tmB, W2, I, (uint64_t)G * d, (uint64_t)I * 2, 64, 64))
         return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d_sw64(&p.tmO, dGU, 2 * I, max_rows, (uint64_t)4 * I, 32, 32))
+        return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d_sw64(&p.tmO2, hw, I, max_rows, (uint64_t)I * 2, 32, 32))
+        return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
     p.n_tiles = I / BN;

@@ -34,7 +34,8 @@ constexpr int kStageBudget = 192 * 1024;
 struct GemmParams {
     CUtensorMap tmA;
     CUtensorMap tmB;
-    CUtensorMap tmO;         // GM_WGRAD: fp32 output [G*M, N], boxes of 32 x 32
+    CUtensorMap tmO;         // GM_WGRAD: fp32 output [G*M, N]; GM_DGRAD2: dGU [rows, 2I] bf16
+    CUtensorMap tmO2;        // GM_DGRAD2: w h [rows, I] bf16 (boxes of 32 x 32)
     const int32_t *offsets;  // [G+1] group row offsets (grouped modes)
     int G;
     int rows;                // GM_GATE: rows of A
@@ -72,19 +73,25 @@ struct ModeTraits {
     static constexpr bool ROWGROUP = !DENSE && !KGROUP;
 };
 
-// Epilogue staging of the TMA-store path (GM_WGRAD): per epilogue warp two
-// 32 x 32 fp32 blocks (4 KB each, 128-byte swizzled), double buffered.
+// Epilogue staging of the TMA-store paths, per epilogue warp:
+//   GM_WGRAD   two 32 x 32 fp32 blocks (4 KB each, 128-byte swizzle), double buffered;
+//   GM_DGRAD2  one 32 x 32 bf16 block for each of dg, du and w h (2 KB each,
+//              64-byte swizzle).
 constexpr int kEpiWarpBytes = 2 * 4096;
+constexpr int kEpiWarpBytesDgrad2 = 3 * 2048;
 // Operand stages plus staging of the TMA-store path.
 constexpr int kStoreModeBudget = 208 * 1024;
 
 template <int BN, int MODE>
 struct TileShape {
-    static constexpr bool TMA_STORE = (MODE == GM_WGRAD);
+    static constexpr bool TMA_STORE = (MODE == GM_WGRAD || MODE == GM_DGRAD2);
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BN * 64 * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int EPI_BYTES = TMA_STORE ? ModeTraits<MODE>::NEPI * kEpiWarpBytes : 0;
+    static constexpr int EPI_BYTES =
+        MODE == GM_WGRAD    ? ModeTraits<MODE>::NEPI * kEpiWarpBytes
+        : MODE == GM_DGRAD2 ? ModeTraits<MODE>::NEPI * kEpiWarpBytesDgrad2
+                            : 0;
     static constexpr int STAGES =
         ((TMA_STORE ? kStoreModeBudget : kStageBudget) - EPI_BYTES) / STAGE_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {64, 128, 256}: a power of two
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         tma_prefetch_desc(&p.tmA);
         tma_prefetch_desc(&p.tmB);
         if constexpr (TS::TMA_STORE) tma_prefetch_desc(&p.tmO);
+        if constexpr (MODE == GM_DGRAD2) tma_prefetch_desc(&p.tmO2);
     }
     if (warp == 1) {
         tmem_alloc(tmem_base_s, TS::TMEM_COLS);
@@ -476,11 +484,16 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 float dw = 0.0f;
                 constexpr int CW2 = BN / (MT::NEPI / 4);   // this warp's columns
                 const int c_lo2 = (ew >> 2) * CW2;
+                // warps whose 32 rows all exist use TMA stores; a ragged warp must not
+                // write past its group (the next rows belong to another tile)
+                const bool warp_full = q * 32 + 32 <= ti.rows_valid;
+                uint8_t *stg2 = sEpi + (size_t)ew * kEpiWarpBytesDgrad2;
 #pragma unroll 1
                 for (int c = c_lo2; c < c_lo2 + CW2; c += 32) {
                     uint32_t r[32];
                     tmem_ld32(tb + c, r);
                     tmem_wait_ld();
+                    uint32_t og[16], ou[16], oh[16];
                     if (valid) {
                         const int col = ti.nt * BN + c;
                         uint16_t *dgd = dgu + (size_t)row * 2 * p.I + col;
@@ -497,7 +510,6 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                         }
                         const float *gv = reinterpret_cast<const float *>(gv4);
                         const float *uv = reinterpret_cast<const float *>(uv4);
-                        uint32_t og[16], ou[16], oh[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             float dg2[2], du2[2], hw2[2];
@@ -522,11 +534,41 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                             ou[e] = pack_bf16x2(du2[0], du2[1]);
                             oh[e] = pack_bf16x2(hw2[0], hw2[1]);
                         }
+                        if (!warp_full) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 16; q4 += 4) {
-                            st_global_v4(dgd + 2 * q4, og[q4], og[q4 + 1], og[q4 + 2], og[q4 + 3]);
-                            st_global_v4(dud + 2 * q4, ou[q4], ou[q4 + 1], ou[q4 + 2], ou[q4 + 3]);
-                            st_global_v4(hwd + 2 * q4, oh[q4], oh[q4 + 1], oh[q4 + 2], oh[q4 + 3]);
+                            for (int q4 = 0; q4 < 16; q4 += 4) {
+                                st_global_v4(dgd + 2 * q4, og[q4], og[q4 + 1], og[q4 + 2], og[q4 + 3]);
+                                st_global_v4(dud + 2 * q4, ou[q4], ou[q4 + 1], ou[q4 + 2], ou[q4 + 3]);
+                                st_global_v4(hwd + 2 * q4, oh[q4], oh[q4 + 1], oh[q4 + 2], oh[q4 + 3]);
+                            }
+                        }
+                    }
+                    if (warp_full) {
+                        // all 32 rows of this warp exist: stage the three 32 x 32 bf16
+                        // blocks (64-byte swizzle) and write them with TMA stores
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                        const uint32_t b0 = smem_u32(stg2);
+                        const uint32_t rowb = (uint32_t)lane * 64u;
+                        const uint32_t sw2 = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t o = rowb + ((((uint32_t)j) ^ sw2) << 4);
+                            st_shared_v4(b0 + o, og[4 * j], og[4 * j + 1], og[4 * j + 2], og[4 * j + 3]);
+                            st_shared_v4(b0 + 2048 + o, ou[4 * j], ou[4 * j + 1], ou[4 * j + 2],
+                                         ou[4 * j + 3]);
+                            st_shared_v4(b0 + 4096 + o, oh[4 * j], oh[4 * j + 1], oh[4 * j + 2],
+                                         oh[4 * j + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int col = ti.nt * BN + c;
+                            const int wrow = ti.row0 + q * 32;
+                            tma_store_2d(&p.tmO, stg2, col, wrow);
+                            tma_store_2d(&p.tmO, stg2 + 2048, p.I + col, wrow);
+                            tma_store_2d(&p.tmO2, stg2 + 4096, col, wrow);
+                            bulk_commit_group();
                         }
                     }
                 }

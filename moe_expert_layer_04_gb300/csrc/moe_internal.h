@@ -26,6 +26,10 @@ int num_sms();
 bool encode_tmap_bf16_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
                          uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// bf16 2-D matrix with 64-byte swizzle (boxes with a 64-byte inner extent).
+bool encode_tmap_bf16_2d_sw64(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+                              uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
+
 // Same for a 2-D fp32 matrix (stores), 128-byte swizzle.
 bool encode_tmap_f32_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
