@@ -62,9 +62,10 @@ struct GemmParams {
 template <int MODE>
 struct ModeTraits {
     // epilogue warps: two per TMEM lane quadrant (each drains half the
-    // columns) where the epilogue carries real work -- the weight gradients'
-    // output stream and the SwiGLU backward of dgrad 2 -- one otherwise
-    static constexpr int NEPI = (MODE == GM_WGRAD || MODE == GM_DGRAD2) ? 8 : 4;
+    // columns) for the heavy SwiGLU-backward epilogue of dgrad 2, one
+    // otherwise (the weight gradients gain more from a fourth operand stage
+    // than from a wider epilogue)
+    static constexpr int NEPI = (MODE == GM_DGRAD2) ? 8 : 4;
     static constexpr int THREADS = 64 + 32 * NEPI;
     static constexpr bool A_MN = (MODE == GM_WGRAD);
     static constexpr bool B_MN = (MODE == GM_DGRAD2 || MODE == GM_DGRAD1 || MODE == GM_WGRAD);
@@ -74,13 +75,14 @@ struct ModeTraits {
 };
 
 // Epilogue staging of the TMA-store paths, per epilogue warp:
-//   GM_WGRAD   two 32 x 32 fp32 blocks (4 KB each, 128-byte swizzle), double buffered;
+//   GM_WGRAD   one 32 x 32 fp32 block (4 KB, 128-byte swizzle);
 //   GM_DGRAD2  one 32 x 32 bf16 block for each of dg, du and w h (2 KB each,
 //              64-byte swizzle).
-constexpr int kEpiWarpBytes = 2 * 4096;
+constexpr int kWgradStageBufs = 1;    // fp32 staging buffers per weight-gradient warp
+constexpr int kEpiWarpBytes = kWgradStageBufs * 4096;
 constexpr int kEpiWarpBytesDgrad2 = 3 * 2048;
 // Operand stages plus staging of the TMA-store path.
-constexpr int kStoreModeBudget = 208 * 1024;
+constexpr int kStoreModeBudget = 216 * 1024;
 
 template <int BN, int MODE>
 struct TileShape {
@@ -584,9 +586,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 const int c_lo = (ew >> 2) * CW;
                 // stage one 32 x 32 block (this thread's row) and store it with TMA
                 auto store_block = [&](const uint32_t (&v)[32], int c) {
-                    uint8_t *buf = stg + ((c >> 5) & 1) * 4096;
-                    // the store issued two blocks ago read this buffer: wait for it
-                    if (lane == 0) bulk_wait_group_read<1>();
+                    uint8_t *buf = stg + (kWgradStageBufs == 2 ? ((c >> 5) & 1) * 4096 : 0);
+                    // the store that last used this buffer must have read it
+                    if (lane == 0) {
+                        if constexpr (kWgradStageBufs == 2) bulk_wait_group_read<1>();
+                        else bulk_wait_group_read<0>();
+                    }
                     __syncwarp();
                     const uint32_t row_addr = smem_u32(buf) + (uint32_t)lane * 128u;
 #pragma unroll
