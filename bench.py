@@ -33,6 +33,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("MoE layer tokens/s (fwd, fwd+bwd) at 1 GB300; grouped-GEMM % of BF16 tensor peak")
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes (read + write) per algorithmic byte of expert GEMM 1, from an ncu
+# capture of the current kernel on a small case of the same workload
+# (T=640, E=64: 2.268 GB measured for 2.236 GB algorithmic); traffic grows in
+# proportion to the experts streamed, so a full launch is this ratio times its
+# algorithmic bytes.
+GEMM1_DRAM_PER_ALGORITHMIC_BYTE = 1.0143
 FALLBACK_BF16_TFLOPS = 1900.0
 FWD_LAUNCHES = 9      # gate GEMM, route, hist, scan, scatter, gather, GEMM1, GEMM2, combine
 BWD_LAUNCHES = 9      # gather dY, dgrad2, wgrad2, dgrad1, wgrad1, router bwd, dX, dW_g (2)
@@ -269,7 +275,9 @@ def run_ours(args, rank, world, local_rank):
     achieved = kernels["expert_gemm1"]["gbs"]
     roofline = {"kernel": "expert_gemm1 (grouped GEMM 1 + clamped SwiGLU)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None,
+                "frac": round(achieved / hbm, 4),
+                "traffic": round(g1_bytes * GEMM1_DRAM_PER_ALGORITHMIC_BYTE),
+                "traffic_source": "ncu dram read+write of a T=640/E=64 launch, scaled by bytes",
                 "peak_source": peak_src, "bytes_per_launch": g1_bytes}
 
     # ---------------- the same forward with the literal U(-0.1, 0.1) routing bias
