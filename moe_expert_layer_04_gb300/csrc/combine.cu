@@ -134,7 +134,19 @@ __global__ void __launch_bounds__(64) dwg_partial_kernel(const uint4 *__restrict
     const int r1 = lo + (int)((long long)n * (sp + 1) / splits);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (c < vecs) {
-        for (int r = r0; r < r1; ++r) fma_bf16x8(acc, dz_row[r], xp[(size_t)r * vecs + c]);
+        int r = r0;
+        // four rows in flight per step, summed in row order
+        for (; r + 4 <= r1; r += 4) {
+            const uint4 v0 = xp[(size_t)r * vecs + c];
+            const uint4 v1 = xp[(size_t)(r + 1) * vecs + c];
+            const uint4 v2 = xp[(size_t)(r + 2) * vecs + c];
+            const uint4 v3 = xp[(size_t)(r + 3) * vecs + c];
+            fma_bf16x8(acc, dz_row[r], v0);
+            fma_bf16x8(acc, dz_row[r + 1], v1);
+            fma_bf16x8(acc, dz_row[r + 2], v2);
+            fma_bf16x8(acc, dz_row[r + 3], v3);
+        }
+        for (; r < r1; ++r) fma_bf16x8(acc, dz_row[r], xp[(size_t)r * vecs + c]);
         float4 *dst = reinterpret_cast<float4 *>(part + (((size_t)sp * E + e) * vecs + c) * 8);
         dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -166,7 +178,9 @@ int token_blocks(int T) {
 
 }  // namespace
 
-constexpr int kDwgSplits = 8;
+// Row splits of each expert's dW_g sum: the hottest expert of a skewed load
+// holds ~40 % of a 64K-token slice's rows, and each split is one block.
+constexpr int kDwgSplits = 32;
 
 size_t dwg_workspace_bytes(int d, int E) {
     return ((size_t)kDwgSplits * E * d * 4 + 255) / 256 * 256;

@@ -100,6 +100,9 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     p.M = M;
     p.out = dW;
     const int tiles = G * p.m_tiles * p.n_tiles;
+    // long contractions: two-CTA clusters share each B tile (measured: the
+    // weight-gradient GEMMs gain, the row-grouped GEMMs do not)
+    if (BN == 256 && p.m_tiles % 2 == 0) return launch_gemm<GM_WGRAD, 256, 2>(p, tiles / 2, st);
     switch (BN) {
         case 256: return launch_gemm<GM_WGRAD, 256>(p, tiles, st);
         case 128: return launch_gemm<GM_WGRAD, 128>(p, tiles, st);

@@ -12,9 +12,9 @@
 
 namespace moe {
 
-moe_status launch_gate_gemm(const uint16_t *x, const uint16_t *Wg, const float *offset, int T,
-                            int d, int E, float *logits, cudaStream_t st) {
-    constexpr int BN = 64;
+template <int BN>
+static moe_status gate_gemm_bn(const uint16_t *x, const uint16_t *Wg, const float *offset, int T,
+                               int d, int E, float *logits, cudaStream_t st) {
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     if (!encode_tmap_bf16_2d(&p.tmA, x, d, T, (uint64_t)d * 2, 64, 128)) return MOE_ERR_CUDA;
@@ -27,6 +27,16 @@ moe_status launch_gate_gemm(const uint16_t *x, const uint16_t *Wg, const float *
     p.out = logits;
     p.col_add = offset;
     return launch_gemm<GM_GATE, BN>(p, ((T + 127) / 128) * p.n_tiles, st);
+}
+
+moe_status launch_gate_gemm(const uint16_t *x, const uint16_t *Wg, const float *offset, int T,
+                            int d, int E, float *logits, cudaStream_t st) {
+    // 128-wide tiles read each x tile half as often; use them when they still
+    // give every SM at least two tiles
+    const long long tiles128 = (long long)((T + 127) / 128) * ((E + 127) / 128);
+    if (tiles128 >= 2LL * num_sms())
+        return gate_gemm_bn<128>(x, Wg, offset, T, d, E, logits, st);
+    return gate_gemm_bn<64>(x, Wg, offset, T, d, E, logits, st);
 }
 
 moe_status launch_ffn1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,

@@ -118,9 +118,13 @@ struct TileInfo {
     int kb;          // k blocks of 64
 };
 
-template <int MODE, int BN>
+// Tile t of the schedule.  With CL = 2 (a two-CTA cluster sharing the B
+// operand) t counts pairs of 128-row tiles of the same group and column tile,
+// and `rank` picks the CTA's tile of the pair; a pair's second tile may lie
+// past the group's rows (rows_valid <= 0: computed, never stored).
+template <int MODE, int BN, int CL>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, const int *mt_start,
-                                                const int *offs) {
+                                                const int *offs, int rank) {
     using MT = ModeTraits<MODE>;
     TileInfo ti;
     ti.nt = t % p.n_tiles;
@@ -130,7 +134,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
     ti.krows = 0;
     if constexpr (MT::DENSE) {
         ti.g = 0;
-        ti.row0 = q * 128;
+        ti.row0 = (q * CL + rank) * 128;
         ti.rows_valid = min(128, p.rows - ti.row0);
         ti.kb = p.k_blocks;
     } else if constexpr (MT::ROWGROUP) {
@@ -140,12 +144,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
             if (mt_start[mid] <= q) lo = mid; else hi = mid - 1;
         }
         ti.g = lo;
-        ti.row0 = offs[lo] + (q - mt_start[lo]) * 128;
+        ti.row0 = offs[lo] + ((q - mt_start[lo]) * CL + rank) * 128;
         ti.rows_valid = min(128, offs[lo + 1] - ti.row0);
         ti.kb = p.k_blocks;
     } else {
-        ti.g = q / p.m_tiles;
-        ti.m0 = (q % p.m_tiles) * 128;
+        const int mp = p.m_tiles / CL;
+        ti.g = q / mp;
+        ti.m0 = ((q % mp) * CL + rank) * 128;
         ti.row0 = 0;
         ti.rows_valid = 128;
         ti.krow0 = offs[ti.g];
@@ -171,10 +176,15 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
     return a / (1.0f + expf(-a)) * b;
 }
 
-template <int MODE, int BN>
+// CL = 1: one CTA per tile.  CL = 2: clusters of two CTAs; the pair computes
+// two 128-row tiles with the same B tile, each CTA loading half of B and
+// multicasting it into both CTAs' shared memory (half the B traffic per CTA).
+template <int MODE, int BN, int CL>
 __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p) {
     using MT = ModeTraits<MODE>;
+    static_assert(CL == 1 || CL == 2, "cluster of one or two CTAs");
+    static_assert(CL == 1 || !MT::B_MN || BN >= 128, "the B boxes split between the pair");
     using TS = TileShape<BN, MODE>;
     constexpr int STAGES = TS::STAGES;
     constexpr uint32_t IDESC = idesc_bf16_f32(128, BN, MT::A_MN, MT::B_MN);
@@ -201,7 +211,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CL);   // released by the MMA of every CTA of the pair
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -236,6 +246,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 if (g < p.G) {
                     const int cnt = p.offsets[g + 1] - o;
                     mt = cnt > 0 ? (cnt + 127) >> 7 : 0;
+                    mt = (mt + CL - 1) / CL;   // tiles, or pairs of tiles
                 }
                 int incl = mt;
 #pragma unroll
@@ -251,16 +262,22 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the peer's multicast copies and commits target our barriers: both CTAs
+    // must have initialised them first
+    if constexpr (CL == 2) cluster_sync_all();
+    const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
+    const int cid = blockIdx.x / CL;          // cluster index
+    const int ncl = gridDim.x / CL;           // clusters in the grid
 
     const uint32_t tmem_base = *tmem_base_s;
     const WaitCtl wc{abort_s, p.status, p.wait_limit};
     int total_tiles;
     if constexpr (MT::DENSE) {
-        total_tiles = ((p.rows + 127) >> 7) * p.n_tiles;
+        total_tiles = ((((p.rows + 127) >> 7) + CL - 1) / CL) * p.n_tiles;
     } else if constexpr (MT::ROWGROUP) {
         total_tiles = mt_start[p.G] * p.n_tiles;
     } else {
-        total_tiles = p.G * p.m_tiles * p.n_tiles;
+        total_tiles = p.G * (p.m_tiles / CL) * p.n_tiles;
     }
 
     if (warp == 0) {
@@ -271,8 +288,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
             for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             uint32_t s = 0, ph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-                const TileInfo ti = decode_tile<MODE, BN>(p, t, mt_start, offs);
+            for (int t = cid; ok && t < total_tiles; t += ncl) {
+                const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
                 for (int kb = 0; kb < ti.kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], TS::STAGE_BYTES);
@@ -284,23 +301,49 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                     } else {
                         tma_load_2d(a_dst, &p.tmA, &full[s], kb * 64, ti.row0);
                     }
-                    if constexpr (MODE == GM_GATE) {
-                        tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, ti.nt * BN);
-                    } else if constexpr (MODE == GM_FFN1) {
-                        const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
-                        tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, r);
-                        tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB, &full[s], kb * 64, r + p.I);
-                    } else if constexpr (MODE == GM_FFN2) {
-                        tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64,
-                                    ti.g * p.b_rows_per_group + ti.nt * BN);
-                    } else {
-                        // MN-major B: BN/64 boxes of 64 columns x 64 contraction rows
-                        const int krow = MT::KGROUP ? ti.krow0 + kb * 64
-                                                    : ti.g * p.b_rows_per_group + kb * 64;
+                    if constexpr (CL == 1) {
+                        if constexpr (MODE == GM_GATE) {
+                            tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, ti.nt * BN);
+                        } else if constexpr (MODE == GM_FFN1) {
+                            const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
+                            tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, r);
+                            tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB, &full[s], kb * 64,
+                                        r + p.I);
+                        } else if constexpr (MODE == GM_FFN2) {
+                            tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64,
+                                        ti.g * p.b_rows_per_group + ti.nt * BN);
+                        } else {
+                            // MN-major B: BN/64 boxes of 64 columns x 64 contraction rows
+                            const int krow = MT::KGROUP ? ti.krow0 + kb * 64
+                                                        : ti.g * p.b_rows_per_group + kb * 64;
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(b_dst + j * 8192, &p.tmB, &full[s], ti.nt * BN + 64 * j,
-                                        krow);
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_2d(b_dst + j * 8192, &p.tmB, &full[s],
+                                            ti.nt * BN + 64 * j, krow);
+                        }
+                    } else {
+                        // the pair shares B: this CTA loads its half and multicasts it
+                        constexpr uint16_t kPair = 0x3;
+                        if constexpr (MODE == GM_GATE) {
+                            tma_load_2d_mc(b_dst + rank * (BN / 2) * 128, &p.tmB, &full[s],
+                                           kb * 64, ti.nt * BN + rank * (BN / 2), kPair);
+                        } else if constexpr (MODE == GM_FFN1) {
+                            const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
+                            tma_load_2d_mc(b_dst + rank * (BN / 2) * 128, &p.tmB, &full[s],
+                                           kb * 64, r + rank * p.I, kPair);
+                        } else if constexpr (MODE == GM_FFN2) {
+                            tma_load_2d_mc(b_dst + rank * (BN / 2) * 128, &p.tmB, &full[s],
+                                           kb * 64,
+                                           ti.g * p.b_rows_per_group + ti.nt * BN + rank * (BN / 2),
+                                           kPair);
+                        } else {
+                            const int krow = MT::KGROUP ? ti.krow0 + kb * 64
+                                                        : ti.g * p.b_rows_per_group + kb * 64;
+#pragma unroll
+                            for (int j = rank; j < BN / 64; j += 2)
+                                tma_load_2d_mc(b_dst + j * 8192, &p.tmB, &full[s],
+                                               ti.nt * BN + 64 * j, krow, kPair);
+                        }
                     }
                     last_par[s] = (int)ph;
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -311,6 +354,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 for (int i = 0; i < STAGES; ++i)
                     if (last_par[i] >= 0)
                         mbar_wait_teardown(&full[i], (uint32_t)last_par[i], p.wait_limit);
+            } else if constexpr (CL == 2) {
+                // every release of a stage (ours and the peer's commit) must have
+                // landed in our barriers before the CTA may exit
+                for (int i = 0; i < STAGES; ++i)
+                    if (last_par[i] >= 0)
+                        mbar_wait_teardown(&empty[i], (uint32_t)last_par[i], p.wait_limit);
             }
         }
     } else if (warp == 1) {
@@ -318,8 +367,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         uint32_t s = 0, ph = 0;
         int it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile<MODE, BN>(p, t, mt_start, offs);
+        for (int t = cid; ok && t < total_tiles; t += ncl, ++it) {
+            const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             if (!mbar_wait(&tempty[acc], aph ^ 1u, wc)) { ok = false; break; }
@@ -361,7 +410,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                                                      : sdesc_sw128(b_addr + kk * 32, 16, 1024);
                         umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    umma_commit(&empty[s]);
+                    if constexpr (CL == 2) umma_commit_mc(&empty[s], 0x3);
+                    else umma_commit(&empty[s]);
                 }
                 __syncwarp();
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -382,8 +432,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         const int ew = warp - 2;          // epilogue warp index
         const int r_local = q * 32 + lane;
         int it = 0;
-        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile<MODE, BN>(p, t, mt_start, offs);
+        for (int t = cid; t < total_tiles; t += ncl, ++it) {
+            const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
             if (!mbar_wait(&tfull[acc], aph, wc)) break;
@@ -642,6 +692,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TS::TMEM_COLS);
+    // neither CTA of a pair leaves while the other may still signal it
+    if constexpr (CL == 2) cluster_sync_all();
 }
 
 }  // namespace moe

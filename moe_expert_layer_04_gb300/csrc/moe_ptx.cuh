@@ -106,6 +106,30 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *t
         : "memory");
 }
 
+// 2-D tiled copy global -> shared of every CTA in `mask` of the cluster (same
+// shared-memory offset and mbarrier offset in each); each destination CTA's
+// mbarrier receives the transaction bytes of its own copy.
+__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const CUtensorMap *tm,
+                                               uint64_t *bar, int c0, int c1, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Same with an L2 eviction-priority hint (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *tm,
                                                  uint64_t *bar, int c0, int c1, uint64_t policy) {
@@ -210,6 +234,15 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// Arrives once on the mbarrier at the same offset in every CTA of `mask`
+// when every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }
 

@@ -23,6 +23,8 @@ CASES = {
     "tiny": W.WORKLOADS["tiny_fwd"],
     "mid_I192": W.Workload("mid_I192", 320, 256, 24, 4, 192, 2.5, vision_frac=0.25),
     "mid_skew": W.Workload("mid_skew", 520, 384, 12, 3, 256, 2.5, zipf_s=1.1),
+    # many rows per expert: the weight gradients run as two-CTA clusters sharing B
+    "paired": W.Workload("paired", 2048, 256, 6, 2, 256, 2.5, vision_frac=0.3),
 }
 
 
@@ -175,7 +177,8 @@ def test_forward_layer(name):
 
 
 @pytest.mark.parametrize("name,recompute", [("tiny", False), ("mid_I192", False),
-                                            ("mid_skew", False), ("mid_skew", True)])
+                                            ("mid_skew", False), ("mid_skew", True),
+                                            ("paired", False)])
 def test_backward_layer(name, recompute):
     w = CASES[name]
     layer, inp = make_layer(w, backward=True, recompute=recompute)
