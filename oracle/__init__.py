@@ -69,6 +69,7 @@ def _load():
                 "orc_route": ([_P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _I, _D, _I,
                                _P, _P, _P, _P], None),
                 "orc_permute": ([_P, _I, _I, _I, _P, _P, _P, _P], None),
+                "orc_modality_counts": ([_P, _P, _I, _I, _I, _P], None),
                 "orc_expert_rows": ([_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _D, _I,
                                      _P, _P], None),
                 "orc_layer_forward": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _P, _I,
@@ -199,6 +200,17 @@ def permute(ids, E):
     _load().orc_permute(_ptr(idn), T, E, k, _ptr(counts), _ptr(offsets), _ptr(row_token),
                         _ptr(slot_row))
     return counts, offsets, row_token, slot_row
+
+
+def modality_counts(ids, is_vision, E):
+    """Slots per (modality, expert): [2, E], row 0 text, row 1 vision."""
+    idn = np.ascontiguousarray(_to_np(ids), dtype=np.int32)
+    T, k = idn.shape
+    vis = None if is_vision is None else np.ascontiguousarray(_to_np(is_vision), dtype=np.uint8)
+    counts = np.empty((2, E), np.int32)
+    _load().orc_modality_counts(_ptr(idn), None if vis is None else _ptr(vis), T, E, k,
+                                _ptr(counts))
+    return counts
 
 
 def expert_rows(x, W13, W2, row_tok, row_exp, row_w, clamp, exact=False):

@@ -264,6 +264,21 @@ void orc_permute(const int32_t *ids, int T, int E, int k, int32_t *counts,
                 }
 }
 
+/* Expert load per modality ([HP41] §01 item 5, native multimodal MoE: the
+ * text and the vision load of the experts are balanced separately).
+ *   counts[m*E + e] = number of slots (t, j) with ids[t*k + j] = e whose token
+ *                     has modality m = is_vision[t] (0 text, 1 vision;
+ *                     is_vision NULL = all text) */
+void orc_modality_counts(const int32_t *ids, const uint8_t *is_vision, int T, int E, int k,
+                         int32_t *counts)
+{
+    for (int i = 0; i < 2 * E; ++i) counts[i] = 0;
+    for (int t = 0; t < T; ++t) {
+        const int m = (is_vision && is_vision[t]) ? 1 : 0;
+        for (int j = 0; j < k; ++j) counts[m * E + ids[(size_t)t * k + j]]++;
+    }
+}
+
 /* ------------------------------------------------------ expert FFN (F4/F5) */
 
 /* One expert on one input row ([HP41] §2.3 MegaMoE: two expert matmuls around

@@ -160,6 +160,26 @@ def test_permute_invariants(T, E, k, skew):
         np.testing.assert_array_equal(back[:, j], x)
 
 
+@pytest.mark.parametrize("T,E,k,skew,frac", [(64, 16, 2, 0.0, 0.0), (257, 40, 6, 1.1, 0.3),
+                                             (300, 64, 3, 2.0, 1.0), (1, 4, 4, 0.0, 1.0)])
+def test_modality_counts_split_the_expert_histogram(T, E, k, skew, frac):
+    ids = W.random_ids(T, E, k, seed=T + 2 * E, skew=skew).numpy()
+    vis = (np.random.default_rng(T).random(T) < frac).astype(np.uint8)
+    c = oracle.modality_counts(ids, vis, E)
+    # the two rows add up to the permutation's histogram
+    np.testing.assert_array_equal(c.sum(0), oracle.permute(ids, E)[0])
+    # each row is the histogram of that modality's tokens alone
+    for m in (0, 1):
+        sub = ids[vis == m]
+        want = oracle.permute(sub, E)[0] if len(sub) else np.zeros(E, np.int32)
+        np.testing.assert_array_equal(c[m], want)
+        assert c[m].sum() == k * int((vis == m).sum())
+    # no modality flags: everything is text
+    c0 = oracle.modality_counts(ids, None, E)
+    np.testing.assert_array_equal(c0[1], 0)
+    np.testing.assert_array_equal(c0[0], c.sum(0))
+
+
 # --------------------------------------------------------------- expert FFN
 
 def _rand(shape, std, rng):
