@@ -113,6 +113,25 @@ moe_status moe_route_logits(const float *logits, const float *bias, const uint8_
                             int E, int k, float scaling, moe_route_mode mode, int32_t *ids,
                             float *weights, float *scores_sel, void *stream);
 
+/* Gate projection and routing in one kernel, with the expert load of each
+ * modality ([HP41] §2.3 MegaGate; [HP41] §01 item 5, native multimodal MoE:
+ * text and vision load are balanced separately).  Same semantics and outputs
+ * as moe_route, plus
+ *   modality_counts [2,E] int32 or NULL: modality_counts[m,e] = number of
+ *   slots (t,j) with ids[t,j] = e and m = is_vision[t] ? 1 : 0 (row 0 text,
+ *   row 1 vision); rows sum to T*k.  Overwritten (zeroed on `stream` first).
+ * Each 128-token block keeps its logits for all E experts in tensor memory
+ * and routes them there, so the logits are written once and never re-read.
+ * Supported: d % 64 == 0, E % 32 == 0, 32 <= E <= 512, 1 <= k <= min(8, E);
+ * other sizes return MOE_ERR_UNSUPPORTED (use moe_route).  Needs logits 16-
+ * byte aligned; ids, weights, scores_sel and modality_counts 4-byte aligned. */
+moe_status moe_gate_route(const uint16_t *x, const uint16_t *W_g, const float *logit_offset,
+                          const float *bias, const uint8_t *is_vision, const int32_t *input_ids,
+                          const int32_t *tid2eid, int vocab, int T, int d, int E, int k,
+                          float scaling, moe_route_mode mode, float *logits, int32_t *ids,
+                          float *weights, float *scores_sel, int32_t *modality_counts,
+                          void *stream);
+
 /* Token dispatch on one GPU ([HP41] §2.3 MegaMoE "token dispatch"; [TW]
  * FSDP2-4D: selected experts become global expert ids of one dispatch).
  * Stable expert-major permutation of the S = T*k slots (expert, then token,

@@ -29,7 +29,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT,
 MOE_ROUTE_TOPK, MOE_ROUTE_HASH = 0, 1
 MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE = 1, 2
 
-EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_permute",
+EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_route", "moe_permute",
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout"]
@@ -108,6 +108,8 @@ _SIGS = {
     "moe_route": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P],
                   _I),
     "moe_route_logits": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P], _I),
+    "moe_gate_route": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P,
+                        _P, _P], _I),
     "moe_permute": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_permute_noalloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_expert_ffn": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _Z, _P], _I),
@@ -204,6 +206,20 @@ def moe_route_logits(logits, bias, is_vision, input_ids, tid2eid, T, E, k, scali
                                  _ptr(ids, I32, "ids"), _ptr(weights, F32, "weights"),
                                  _ptr(scores_sel, F32, "scores_sel"), _stream(stream))
     _check("moe_route_logits", st)
+
+
+def moe_gate_route(x, W_g, logit_offset, bias, is_vision, input_ids, tid2eid, T, d, E, k,
+                   scaling, mode, logits, ids, weights, scores_sel, modality_counts=None,
+                   stream=None):
+    vocab = 0 if tid2eid is None else int(tid2eid.shape[0])
+    st = load().moe_gate_route(_ptr(x, BF16, "x"), _ptr(W_g, BF16, "W_g"),
+                               _ptr(logit_offset, F32, "logit_offset"), _ptr(bias, F32, "bias"),
+                               _ptr(is_vision, U8, "is_vision"), _ptr(input_ids, I32, "input_ids"),
+                               _ptr(tid2eid, I32, "tid2eid"), vocab, T, d, E, k, float(scaling),
+                               int(mode), _ptr(logits, F32, "logits"), _ptr(ids, I32, "ids"),
+                               _ptr(weights, F32, "weights"), _ptr(scores_sel, F32, "scores_sel"),
+                               _ptr(modality_counts, I32, "modality_counts"), _stream(stream))
+    _check("moe_gate_route", st)
 
 
 def moe_permute(ids, weights, x, T, d, E, k, counts, offsets, row_token, slot_row, row_weight,

@@ -13,6 +13,13 @@ moe_status route_from_logits(const float *logits, const float *bias, const uint8
                              const int32_t *input_ids, const int32_t *tid2eid, int vocab, int T,
                              int E, int k, float scaling, moe_route_mode mode, int32_t *ids,
                              float *weights, float *scores_sel, cudaStream_t st);
+bool gate_route_supported(int T, int d, int E, int k);
+moe_status launch_gate_route(const uint16_t *x, const uint16_t *Wg, const float *offset,
+                             const float *bias, const uint8_t *is_vision,
+                             const int32_t *input_ids, const int32_t *tid2eid, int vocab, int T,
+                             int d, int E, int k, float scaling, moe_route_mode mode,
+                             float *logits, int32_t *ids, float *weights, float *ssel,
+                             int32_t *counts, cudaStream_t st);
 size_t permute_workspace_bytes(int T, int E, int k);
 moe_status launch_permute(const int32_t *ids, const float *weights, const uint16_t *x, int T,
                           int d, int E, int k, int32_t *counts, int32_t *offsets,
@@ -251,6 +258,25 @@ moe_status moe_route(const uint16_t *x, const uint16_t *W_g, const float *logit_
     if (s != MOE_OK) return s;
     return route_from_logits(logits, bias, is_vision, input_ids, tid2eid, vocab, T, E, k,
                              scaling, mode, ids, weights, scores_sel, st);
+}
+
+moe_status moe_gate_route(const uint16_t *x, const uint16_t *W_g, const float *logit_offset,
+                          const float *bias, const uint8_t *is_vision, const int32_t *input_ids,
+                          const int32_t *tid2eid, int vocab, int T, int d, int E, int k,
+                          float scaling, moe_route_mode mode, float *logits, int32_t *ids,
+                          float *weights, float *scores_sel, int32_t *modality_counts,
+                          void *stream) {
+    if (T < 1 || d < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+    if (mode != MOE_ROUTE_TOPK && mode != MOE_ROUTE_HASH) return MOE_ERR_INVALID_ARG;
+    if (!x || !W_g || !logits || !aligned16(x) || !aligned16(W_g) || !aligned16(logits))
+        return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_ROUTE_TOPK && !bias) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_ROUTE_HASH && (!input_ids || !tid2eid || vocab < 1)) return MOE_ERR_INVALID_ARG;
+    if (!ids || !weights || !scores_sel) return MOE_ERR_INVALID_ARG;
+    if (!gate_route_supported(T, d, E, k)) return MOE_ERR_UNSUPPORTED;
+    return launch_gate_route(x, W_g, logit_offset, bias, is_vision, input_ids, tid2eid, vocab, T,
+                             d, E, k, scaling, mode, logits, ids, weights, scores_sel,
+                             modality_counts, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_permute(const int32_t *ids, const float *weights, const uint16_t *x, int T, int d,

@@ -130,6 +130,62 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ------------------------------------------- distributed shared memory
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Arrives once on an mbarrier of another CTA of the cluster (address from
+// dsmem_map), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with acquire at cluster scope: the arrivals came from another
+// CTA of the cluster and released writes this thread is about to read.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  const WaitCtl &w) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        if (*w.abort) return false;
+        if (clock64() - t0 > w.limit) {
+            *w.abort = 1;
+            atomicExch(w.status, (int)MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Orders this thread's completed async-proxy (TMA) writes to global memory
+// before its later generic-proxy accesses and releases.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Same with an L2 eviction-priority hint (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *tm,
                                                  uint64_t *bar, int c0, int c1, uint64_t policy) {

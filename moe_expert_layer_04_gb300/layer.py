@@ -3,7 +3,8 @@
 This module only allocates device memory (through PyTorch) and calls the
 library in order; every step of the layer runs in the library's kernels:
 
-  forward   moe_route -> moe_permute -> moe_expert_ffn -> moe_combine
+  forward   moe_gate_route (or moe_route) -> moe_permute -> moe_expert_ffn
+            -> moe_combine
   backward  moe_backward
 
 ("HyperParallel加速DeepSeek-V4.1多模态1M长序列训练" §2.3: MegaGate routing
@@ -19,6 +20,12 @@ import torch
 
 from . import _lib
 from ._lib import MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE, MOE_ROUTE_HASH, MOE_ROUTE_TOPK
+
+
+def gate_route_supported(d: int, E: int, k: int) -> bool:
+    """Shapes the one-kernel gate projection + routing (moe_gate_route) takes:
+    the logits of 128 tokens for all E experts must fit in tensor memory."""
+    return d % 64 == 0 and E % 32 == 0 and 32 <= E <= 512 and 1 <= k <= min(8, E)
 
 
 @dataclass(frozen=True)
@@ -42,11 +49,18 @@ class MoELayer:
     """Preallocated buffers for one layer shape, reused across calls.
 
     weights: dict with W_g [E,d], W13 [E+1,2I,d], W2 [E+1,d,I] (bf16, CUDA).
+    fused_route: route with the one-kernel gate projection + routing, which
+    also counts the expert load per modality (None: whenever the shape allows).
     """
 
     def __init__(self, dims: Dims, weights: dict, scaling: float, clamp: float = 7.0,
-                 backward: bool = False, recompute: bool = False, device="cuda"):
+                 backward: bool = False, recompute: bool = False, device="cuda",
+                 fused_route: bool | None = None):
         self.dims = dims
+        ok = gate_route_supported(dims.d, dims.E, dims.k)
+        if fused_route and not ok:
+            raise ValueError(f"moe_gate_route does not take the shape {dims}")
+        self.fused_route = ok if fused_route is None else bool(fused_route)
         self.w = weights
         self.scaling = float(scaling)
         self.clamp = float(clamp)
@@ -60,6 +74,9 @@ class MoELayer:
         self.weights = torch.empty(D.T, D.k, dtype=torch.float32, **e)
         self.scores_sel = torch.empty(D.T, D.k, dtype=torch.float32, **e)
         self.counts = torch.empty(D.E, dtype=torch.int32, **e)
+        # slots per (modality, expert), row 0 text, row 1 vision (fused routing)
+        self.modality_counts = (torch.empty(2, D.E, dtype=torch.int32, **e)
+                                if self.fused_route else None)
         self.offsets = torch.empty(D.E + 2, dtype=torch.int32, **e)
         self.row_token = torch.empty(D.R, dtype=torch.int32, **e)
         self.slot_row = torch.empty(D.S, dtype=torch.int32, **e)
@@ -88,9 +105,15 @@ class MoELayer:
     def route(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
               input_ids=None, tid2eid=None, stream=None):
         D = self.dims
-        _lib.moe_route(x, self.w["W_g"], logit_offset, bias, is_vision, input_ids, tid2eid,
-                       D.T, D.d, D.E, D.k, self.scaling, mode, self.logits, self.ids,
-                       self.weights, self.scores_sel, stream)
+        if self.fused_route:
+            _lib.moe_gate_route(x, self.w["W_g"], logit_offset, bias, is_vision, input_ids,
+                                tid2eid, D.T, D.d, D.E, D.k, self.scaling, mode, self.logits,
+                                self.ids, self.weights, self.scores_sel, self.modality_counts,
+                                stream)
+        else:
+            _lib.moe_route(x, self.w["W_g"], logit_offset, bias, is_vision, input_ids, tid2eid,
+                           D.T, D.d, D.E, D.k, self.scaling, mode, self.logits, self.ids,
+                           self.weights, self.scores_sel, stream)
 
     def dispatch(self, x, stream=None):
         D = self.dims

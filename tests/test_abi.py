@@ -71,6 +71,17 @@ def test_validation_rejects_before_any_launch():
                               1.0, 7, ctypes.c_void_p(16), ctypes.c_void_p(16),
                               ctypes.c_void_p(16), nul)
     assert st == _lib.MOE_ERR_INVALID_ARG
+    # moe_gate_route: shapes whose logits tile does not fit in tensor memory,
+    # or k above 8, are unsupported (moe_route takes them)
+    a = ctypes.c_void_p(4096)
+    for (d, E, k) in [(128, 16, 2), (128, 1024, 6), (128, 384, 9), (96, 384, 6), (128, 100, 4)]:
+        st = lib.moe_gate_route(a, a, nul, a, nul, nul, nul, 0, 256, d, E, k, 1.0, 0, a, a, a,
+                                a, nul, nul)
+        assert st == _lib.MOE_ERR_UNSUPPORTED, (d, E, k)
+    # ... and a misaligned logits pointer is an invalid argument
+    st = lib.moe_gate_route(a, a, nul, a, nul, nul, nul, 0, 256, 128, 64, 4, 1.0, 0,
+                            ctypes.c_void_p(4100), a, a, a, nul, nul)
+    assert st == _lib.MOE_ERR_INVALID_ARG
     # moe_permute without a workspace
     p = ctypes.c_void_p(256)
     st = lib.moe_permute(p, nul, nul, 8, 128, 4, 2, p, p, p, p, nul, nul, nul, 0, nul)

@@ -67,6 +67,9 @@ def _check_indices(layer, inp, w, mode):
     np.testing.assert_allclose(np64(layer.weights), wts, rtol=W_RTOL, atol=0)
     c, o, rt, sr = oracle.permute(g_ids, w.E)
     np.testing.assert_array_equal(cpu(layer.counts).numpy(), c)
+    if layer.modality_counts is not None:
+        np.testing.assert_array_equal(cpu(layer.modality_counts).numpy(),
+                                      oracle.modality_counts(g_ids, cpu(inp["is_vision"]), w.E))
     np.testing.assert_array_equal(cpu(layer.offsets).numpy()[: w.E + 1], o)
     np.testing.assert_array_equal(cpu(layer.row_token).numpy()[: w.S], rt)
     np.testing.assert_array_equal(cpu(layer.slot_row).numpy(), sr)
