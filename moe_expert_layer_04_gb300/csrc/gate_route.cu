@@ -72,13 +72,14 @@ struct GateRouteParams {
     long long wait_limit;
 };
 
-// Dynamic shared memory: operand stages, 4 x 4 KB logits staging, 256 B of
+// Dynamic shared memory: operand stages, 4 x 4 KB logits staging, 4 x 4 KB
+// approximate-key staging (one 32 x 32 block per epilogue warp each), 256 B of
 // barriers, the merge buffer (2 quadrants x 3 fields x L x 32 floats), then
 // offset [E], text bias [E], 4 floats of padding (the two bias rows fall in
 // different banks), vision bias [E], counts [2, E].
 size_t gr_smem_bytes(int E, int CS, int L, int stages) {
     const size_t stage = kGrABytes + (size_t)(E / CS) * 128;
-    return 1024 + (size_t)stages * stage + 4 * 4096 + 256 + (size_t)2 * 3 * L * 32 * 4 +
+    return 1024 + (size_t)stages * stage + 8 * 4096 + 256 + (size_t)2 * 3 * L * 32 * 4 +
            (size_t)(3 * E + 4) * 4 + (size_t)2 * E * 4;
 }
 
@@ -107,13 +108,13 @@ __device__ __forceinline__ float exact_key(float se, float b) {
     return (kk == kk) ? kk : -FLT_MAX;
 }
 
-// Inserts (key, id, z) into the descending list; the slot comes after every
-// entry not below the key (independent compares), then the tail shifts.
+// Inserts (key, id, z) into the descending list when it beats the smallest
+// entry, without branches: the slot comes after every entry not below the key
+// (independent compares), then the tail shifts.
 template <int L>
 __device__ __forceinline__ void list_insert(float (&kv)[L], int (&iv)[L], float (&zv)[L],
                                             float key, int id, float z) {
-    if (!(key > kv[L - 1])) return;
-    int pos = 0;
+    int pos = key > kv[L - 1] ? 0 : L;   // L: no slot, nothing moves
 #pragma unroll
     for (int q = 0; q < L - 1; ++q) pos += kv[q] >= key ? 1 : 0;
 #pragma unroll
@@ -123,11 +124,10 @@ __device__ __forceinline__ void list_insert(float (&kv)[L], int (&iv)[L], float 
         iv[q] = sh ? iv[q - 1] : (put ? id : iv[q]);
         zv[q] = sh ? zv[q - 1] : (put ? z : zv[q]);
     }
-    if (pos == 0) {
-        kv[0] = key;
-        iv[0] = id;
-        zv[0] = z;
-    }
+    const bool put0 = pos == 0;
+    kv[0] = put0 ? key : kv[0];
+    iv[0] = put0 ? id : iv[0];
+    zv[0] = put0 ? z : zv[0];
 }
 
 // L: approximate candidates kept per token (more than k); CS: CTAs per tile.
@@ -147,11 +147,13 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     const int cid = blockIdx.x / CS, ncl = gridDim.x / CS;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // aligned to 1024 B by pointer arithmetic on the shared array itself, so
+    // that the compiler keeps every access derived from it in the shared
+    // state space (LDS/STS, shared atomics) instead of generic addressing
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *stages = smem;
     uint8_t *stg_all = smem + (size_t)STAGES * STAGE;
-    uint64_t *full = reinterpret_cast<uint64_t *>(stg_all + 4 * 4096);
+    uint64_t *full = reinterpret_cast<uint64_t *>(stg_all + 8 * 4096);
     uint64_t *empty = full + kGrMaxStages;
     uint64_t *tfull = empty + kGrMaxStages;
     uint64_t *tempty = tfull + 2;
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     uint64_t *done = lempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
-    float *mrg = reinterpret_cast<float *>(stg_all + 4 * 4096 + 256);
+    float *mrg = reinterpret_cast<float *>(stg_all + 8 * 4096 + 256);
     float *s_off = mrg + 2 * 3 * L * 32;
     float *s_bias = s_off + E;   // text row at [0, E), vision row at [E + 4, 2E + 4)
     int *cnt = reinterpret_cast<int *>(s_bias + 2 * E + 4);
@@ -300,6 +302,8 @@ __global__ void __launch_bounds__(kGrThreads, 1)
         uint8_t *stg = stg_all + (size_t)(warp - 2) * 4096;
         const uint32_t stg_row = smem_u32(stg) + (uint32_t)lane * 128u;
         const uint8_t *row_s = stg + lane * 128;
+        // this lane's row of approximate keys, laid out like its logits row
+        uint8_t *krow = stg_all + 4 * 4096 + (size_t)(warp - 2) * 4096 + lane * 128;
         const uint32_t sw = (uint32_t)(lane & 7);
         float *my_mrg = mrg + qq * 3 * L * 32;   // entry i, field f at [(f * L + i) * 32 + lane]
         int it = 0;
@@ -383,41 +387,65 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                     }
                 }
                 if (cc + 32 < NE) tmem_ld32(tb + cc + 32, rb);
-                if (valid) {
-                    if (topk) {
-                        // candidates: keys above the list's smallest at the chunk's
-                        // start, as a bit mask; each lane then inserts only its own,
-                        // in increasing expert order, reading z back from the
-                        // staging row it wrote
-                        const float thr0 = kv[L - 1];
-                        uint32_t m = 0;
+                if (topk) {
+                    {
+                        // (every lane: the insertion loop below is warp-wide; rows
+                        // past T get no candidates)
+                        float kc[32];
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
                             const float4 b4 = *reinterpret_cast<const float4 *>(bt + c + j);
-                            m |= (approx_key(__uint_as_float(ra[j]), b4.x) > thr0 ? 1u : 0u) << j;
-                            m |= (approx_key(__uint_as_float(ra[j + 1]), b4.y) > thr0 ? 1u : 0u)
-                                 << (j + 1);
-                            m |= (approx_key(__uint_as_float(ra[j + 2]), b4.z) > thr0 ? 1u : 0u)
-                                 << (j + 2);
-                            m |= (approx_key(__uint_as_float(ra[j + 3]), b4.w) > thr0 ? 1u : 0u)
-                                 << (j + 3);
+                            kc[j] = approx_key(__uint_as_float(ra[j]), b4.x);
+                            kc[j + 1] = approx_key(__uint_as_float(ra[j + 1]), b4.y);
+                            kc[j + 2] = approx_key(__uint_as_float(ra[j + 2]), b4.z);
+                            kc[j + 3] = approx_key(__uint_as_float(ra[j + 3]), b4.w);
                         }
-                        while (m) {
-                            const int j = __ffs(m) - 1;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(krow + ((((uint32_t)j) ^ sw) << 4)) =
+                                make_float4(kc[4 * j], kc[4 * j + 1], kc[4 * j + 2], kc[4 * j + 3]);
+                        // candidates: keys above the list's smallest so far and, for
+                        // L = 8, not below the smallest of the chunk's 8 group-of-4
+                        // maxima (those are 8 distinct keys at least that large, so
+                        // nothing below it can be among the 8 largest), as a bit
+                        // mask.  Each lane then inserts only its own, in increasing
+                        // expert order, reading key and z back from its rows.
+                        const float thr0 = kv[L - 1];
+                        float gmin = -INFINITY;
+                        if constexpr (L == 8) {
+                            gmin = INFINITY;
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                gmin = fminf(gmin, fmaxf(fmaxf(kc[4 * g], kc[4 * g + 1]),
+                                                         fmaxf(kc[4 * g + 2], kc[4 * g + 3])));
+                        }
+                        uint32_t m = 0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            m |= (kc[j] > thr0 && kc[j] >= gmin ? 1u : 0u) << j;
+                        if (!valid) m = 0;
+                        // a converged loop: every lane runs the warp's largest count,
+                        // lanes out of candidates insert nothing (a divergent loop
+                        // costs several times more per trip here)
+                        const int trips = __reduce_max_sync(0xffffffffu, __popc(m));
+                        for (int r = 0; r < trips; ++r) {
+                            const bool act = m != 0u;
+                            const int j = act ? __ffs(m) - 1 : 0;
                             m &= m - 1u;
-                            const float zz = *reinterpret_cast<const float *>(
-                                row_s + ((((uint32_t)(j >> 2)) ^ sw) << 4) + (j & 3) * 4);
-                            list_insert<L>(kv, iv, zv, approx_key(zz, bt[c + j]), c + j, zz);
+                            const uint32_t off = ((((uint32_t)(j >> 2)) ^ sw) << 4) + (j & 3) * 4;
+                            const float zz = *reinterpret_cast<const float *>(row_s + off);
+                            const float key = *reinterpret_cast<const float *>(krow + off);
+                            list_insert<L>(kv, iv, zv, act ? key : -INFINITY, c + j, zz);
                         }
-                    } else {
+                    }
+                } else if (valid) {
 #pragma unroll
-                        for (int j = 0; j < kGrKmax; ++j) {
-                            const int e = hid[j] - c;
-                            if (j < k && e >= 0 && e < 32) {
+                    for (int j = 0; j < kGrKmax; ++j) {
+                        const int e = hid[j] - c;
+                        if (j < k && e >= 0 && e < 32) {
 #pragma unroll
-                                for (int jj = 0; jj < 32; ++jj)
-                                    if (jj == e) hz[j] = __uint_as_float(ra[jj]);
-                            }
+                            for (int jj = 0; jj < 32; ++jj)
+                                if (jj == e) hz[j] = __uint_as_float(ra[jj]);
                         }
                     }
                 }

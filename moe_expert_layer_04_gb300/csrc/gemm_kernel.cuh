@@ -190,8 +190,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     constexpr uint32_t IDESC = idesc_bf16_f32(128, BN, MT::A_MN, MT::B_MN);
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // aligned to 1024 B by pointer arithmetic on the shared array itself, so
+    // that the compiler keeps every access derived from it in the shared
+    // state space (LDS/STS, shared atomics) instead of generic addressing
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * TS::A_BYTES;
     uint8_t *sEpi = smem + STAGES * TS::STAGE_BYTES;
