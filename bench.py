@@ -35,12 +35,18 @@ METRIC = ("MoE layer tokens/s (fwd, fwd+bwd) at 1 GB300; grouped-GEMM % of BF16 
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per algorithmic byte of expert GEMM 1, from an ncu
 # capture of the current kernel on a small case of the same workload
-# (T=640, E=64: 2.268 GB measured for 2.236 GB algorithmic); traffic grows in
+# (T=640, E=64: 2.270 GB measured for 2.236 GB algorithmic); traffic grows in
 # proportion to the experts streamed, so a full launch is this ratio times its
 # algorithmic bytes.
-GEMM1_DRAM_PER_ALGORITHMIC_BYTE = 1.0143
+GEMM1_DRAM_PER_ALGORITHMIC_BYTE = 1.0154
 FALLBACK_BF16_TFLOPS = 1900.0
-FWD_LAUNCHES = 9      # gate GEMM, route, hist, scan, scatter, gather, GEMM1, GEMM2, combine
+# library kernels of one forward: routing (one fused gate + route kernel, or the
+# gate GEMM and the routing kernel), rank, scan, scatter, gather, GEMM1, GEMM2,
+# combine
+def fwd_launches(fused_route):
+    return 8 if fused_route else 9
+
+
 BWD_LAUNCHES = 9      # gather dY, dgrad2, wgrad2, dgrad1, wgrad1, router bwd, dX, dW_g (2)
 BWD_RECOMPUTE_EXTRA = 2
 
@@ -218,9 +224,11 @@ def forward_breakdown(layer, inp, steps, warmup, mode=0, world=1):
     return per, ms / steps
 
 
-def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False):
+def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False, fused_route=True):
     """Per-call achieved GB/s (algorithmic bytes) and TFLOP/s with their
-    fractions of the measured peaks."""
+    fractions of the measured peaks.  Routing reads x and W_g and writes the
+    logits (the two-kernel path reads them back once more), ids, weights and
+    selected scores."""
     g1_bytes, g2_bytes = fwd_algorithmic_bytes(D, counts)
     if save_gu:
         g1_bytes += D.R * 2 * D.I * 4
@@ -228,7 +236,8 @@ def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False):
     g2_flops = 2 * D.R * D.I * D.d
     perm_bytes = D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6
     comb_bytes = D.R * D.d * 2 + D.T * D.d * 2 + D.S * 4
-    route_bytes = D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4 * 2 + D.T * D.k * 12
+    route_bytes = (D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4 * (1 if fused_route else 2)
+                   + D.T * D.k * 12)
     out = {}
     for name, by, fl in (("route", route_bytes, 2 * D.T * D.d * D.E), ("permute", perm_bytes, 0),
                          ("expert_gemm1", g1_bytes, g1_flops), ("expert_gemm2", g2_bytes, g2_flops),
@@ -271,7 +280,9 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)
     per, ms_step = forward_breakdown(layer, inp, args.steps, 1, world=world)
     value = replica_throughput(world, D.T, ms_step)
-    kernels, g1_bytes, layer_roof_ms = kernel_metrics(D, counts, per, hbm, bf16)
+    kernels, g1_bytes, layer_roof_ms = kernel_metrics(D, counts, per, hbm, bf16,
+                                                      fused_route=layer.fused_route)
+    fused = layer.fused_route
     achieved = kernels["expert_gemm1"]["gbs"]
     roofline = {"kernel": "expert_gemm1 (grouped GEMM 1 + clamped SwiGLU)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -359,7 +370,9 @@ def run_ours(args, rank, world, local_rank):
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": FWD_LAUNCHES * args.steps,
+        "gpu_launches": fwd_launches(fused) * args.steps,
+        "routing": ("one kernel: gate projection + top-k + per-modality load (moe_gate_route)"
+                    if fused else "gate GEMM, then the routing kernel (moe_route)"),
         "clocks": clk,
         "fwd_bwd": fb,
         "extra_workloads": extra,
@@ -387,16 +400,22 @@ def run_extra_workloads(args, weights, dev, world, hbm, bf16):
         for mode in modes:
             per, ms = forward_breakdown(layer, inp, steps, args.warmup, mode=mode, world=world)
             counts = layer.counts.cpu().numpy()
-            kern, _, roof = kernel_metrics(D, counts, per, hbm, bf16)
+            kern, _, roof = kernel_metrics(D, counts, per, hbm, bf16,
+                                           fused_route=layer.fused_route)
             key = name + ("_hash" if mode == MOE_ROUTE_HASH else "")
+            load = {"experts_with_tokens": int((counts > 0).sum()), "max_rows": int(counts.max())}
+            if layer.modality_counts is not None:
+                mc = layer.modality_counts.cpu().numpy()
+                # text and vision slots per expert, from the routing kernel's counters
+                load["by_modality"] = {m: {"slots": int(mc[i].sum()), "max_rows": int(mc[i].max()),
+                                           "experts_with_tokens": int((mc[i] > 0).sum())}
+                                       for i, m in enumerate(("text", "vision"))}
             out[key] = {"workload": f"{name}: forward, T={wl.T}" +
                                     (", hash router" if mode == MOE_ROUTE_HASH else ", top-k router"),
                         "value": round(replica_throughput(world, D.T, ms), 1),
                         "unit": "tokens/s",
                         "ms_per_step": round(ms, 4), "layer_roofline_frac": round(roof / ms, 4),
-                        "kernels": kern, "steps": steps,
-                        "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
-                                        "max_rows": int(counts.max())}}
+                        "kernels": kern, "steps": steps, "expert_load": load}
         del layer
         torch.cuda.empty_cache()
         if wl.backward and not args.no_bwd:
@@ -446,11 +465,62 @@ def run_fwd_bwd(args, weights, dev, world, wl_name="fwd_bwd", inputs=None):
                        + (", recompute" if wl.recompute else ""),
            "value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
            "ms_per_step": round(ms, 4), "bwd_ms": round(bwd_ms, 4), "steps": steps,
-           "gpu_launches": (FWD_LAUNCHES + BWD_LAUNCHES
+           "gpu_launches": (fwd_launches(layer.fused_route) + BWD_LAUNCHES
                             + (BWD_RECOMPUTE_EXTRA if wl.recompute else 0)) * steps}
     del layer, inp
     torch.cuda.empty_cache()
     return out
+
+
+# ------------------------------------------------------ routing alone
+
+def run_route_only(args):
+    """Times the routing step alone (gate projection + routing) on the
+    workload's routing inputs: the one-kernel path (moe_gate_route, with the
+    per-modality counters) and the two-kernel path (moe_route), CUDA events
+    around each call, L2 flushed before each.  Used to profile the routing
+    kernels without the expert weights on the device."""
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import gate_route_supported
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = workload(args)
+    inp = W.make_inputs(wl, device=dev, with_weights=False)
+    Wg = W.normal_bf16((wl.E, wl.d), 0.02, wl.seed, "W_g", dev)
+    T, E, k = wl.T, wl.E, wl.k
+    z = torch.empty(T, E, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, k, device=dev)
+    ssel = torch.empty(T, k, device=dev)
+    cnt = torch.empty(2, E, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    args_r = (inp["x"], Wg, inp["logit_offset"], inp["bias"], inp["is_vision"], None, None, T,
+              wl.d, E, k, wl.rho, 0, z, ids, wts, ssel)
+    paths = [("two_kernels", lambda: _lib.moe_route(*args_r))]
+    if gate_route_supported(wl.d, E, k):
+        paths.insert(0, ("fused", lambda: _lib.moe_gate_route(*args_r, cnt)))
+    out = {}
+    for name, call in paths:
+        for _ in range(args.warmup):
+            call()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        assert _lib.moe_last_device_status() == _lib.MOE_OK
+        out[name] = {"ms": round(statistics.median(ts), 4),
+                     "tflops": round(2 * T * wl.d * E / (statistics.median(ts) / 1e3) / 1e12, 1)}
+    return {"metric": "routing step ms (gate projection + top-k routing)",
+            "config": {"workload": f"{wl.name}: T={T} d={wl.d} E={E} top-{k}"},
+            "steps": args.steps, "warmup": args.warmup, "l2": "flushed before each call",
+            **out}
 
 
 # -------------------------------------------------------------- oracle
@@ -530,6 +600,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling)")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time only the routing step of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -537,6 +609,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.route_only:
+        print(json.dumps(run_route_only(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
