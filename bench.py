@@ -257,7 +257,7 @@ def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False, fused_route=True):
 def run_ours(args, rank, world, local_rank):
     from moe_expert_layer_04_gb300 import _lib
     from moe_expert_layer_04_gb300 import workloads as W
-    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer, ffn_fused_supported
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -290,6 +290,27 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": round(g1_bytes * GEMM1_DRAM_PER_ALGORITHMIC_BYTE),
                 "traffic_source": "ncu dram read+write of a T=640/E=64 launch, scaled by bytes",
                 "peak_source": peak_src, "bytes_per_launch": g1_bytes}
+
+    # ---------------- both expert matmuls: two launches vs one persistent launch
+    ffn_launch = None
+    if ffn_fused_supported(D.d, D.I):
+        ffn_launch = {}
+        for fused in (False, True):
+            layer.fused_ffn = fused
+            for _ in range(args.warmup):
+                layer.experts()
+            torch.cuda.synchronize()
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(args.steps):
+                layer.experts()
+            f1.record(stream)
+            torch.cuda.synchronize()
+            ffn_launch["one_launch_ms" if fused else "two_launches_ms"] = round(
+                f0.elapsed_time(f1) / args.steps, 4)
+        layer.fused_ffn = False
+        assert _lib.moe_last_device_status() == _lib.MOE_OK
 
     # ---------------- the same forward with the literal U(-0.1, 0.1) routing bias
     literal = None
@@ -377,6 +398,7 @@ def run_ours(args, rank, world, local_rank):
         "fwd_bwd": fb,
         "extra_workloads": extra,
         "literal_bias": literal,
+        "expert_ffn_launches": ffn_launch,
         "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
                         "min_rows": int(counts.min()), "max_rows": int(counts.max())},
     }

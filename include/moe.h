@@ -75,7 +75,7 @@ typedef enum { MOE_ROUTE_TOPK = 0, MOE_ROUTE_HASH = 1 } moe_route_mode;
 #define MOE_FLAG_BACKWARD 1   /* size the workspace for moe_backward as well */
 #define MOE_FLAG_RECOMPUTE 2  /* backward rebuilds x_perm and g|u instead of reading them */
 
-/* Bytes of workspace that moe_permute, moe_expert_ffn and (with
+/* Bytes of workspace that moe_permute, moe_expert_ffn_fused and (with
  * MOE_FLAG_BACKWARD) moe_backward need for these sizes.  One buffer of this
  * size may be reused by every call of one layer; calls on one stream run in
  * order, so reuse is safe.  Returns 0 for unsupported sizes. */
@@ -120,8 +120,9 @@ moe_status moe_route_logits(const float *logits, const float *bias, const uint8_
  *   modality_counts [2,E] int32 or NULL: modality_counts[m,e] = number of
  *   slots (t,j) with ids[t,j] = e and m = is_vision[t] ? 1 : 0 (row 0 text,
  *   row 1 vision); rows sum to T*k.  Overwritten (zeroed on `stream` first).
- * Each 128-token block keeps its logits for all E experts in tensor memory
- * and routes them there, so the logits are written once and never re-read.
+ * The logits of each 128-token block stay in tensor memory (of one CTA, or
+ * split by experts over a pair of CTAs when E % 64 == 0) and are routed
+ * there, so they are written once and never read back.
  * Supported: d % 64 == 0, E % 32 == 0, 32 <= E <= 512, 1 <= k <= min(8, E);
  * other sizes return MOE_ERR_UNSUPPORTED (use moe_route).  Needs logits 16-
  * byte aligned; ids, weights, scores_sel and modality_counts 4-byte aligned. */
@@ -195,6 +196,27 @@ moe_status moe_expert_ffn(const uint16_t *x_perm, const int32_t *offsets, int G,
                           int S, int d, int I, float clamp, float *gu_save,
                           uint16_t *h_perm, uint16_t *y_perm, void *ws, size_t ws_bytes,
                           void *stream);
+
+/* The same two expert matmuls as moe_expert_ffn in ONE persistent launch
+ * ([HP41] §2.3 MegaMoE: the two expert matmuls and the SwiGLU with the V4.1
+ * clamp organised as one fused chain, linked by tile-level dependencies).
+ * The tiles of the first matmul come first in a static schedule over all
+ * SMs; a tile of the second matmul waits, in the kernel, until every tile of
+ * the first that writes its 128 rows of h has finished (per-row-tile
+ * counters in `ws`), so the second matmul starts on early row tiles while the
+ * first is still finishing the last ones, without a second launch.
+ * Arguments and outputs as moe_expert_ffn; h_perm is required (it carries h
+ * between the two matmuls).  ws: at least 4 * (ceil(max_rows/128) + G) bytes,
+ * 4-byte aligned (moe_workspace_size covers it), zeroed by the call itself.
+ * Supported: I % 128 == 0 and d % 256 == 0, else MOE_ERR_UNSUPPORTED.  The
+ * waits assume the whole grid is resident (one CTA per SM, nothing else
+ * running on the GPU's SMs); a wait that runs out ends the kernel and
+ * records MOE_ERR_TIMEOUT in the device status word. */
+moe_status moe_expert_ffn_fused(const uint16_t *x_perm, const int32_t *offsets, int G,
+                                int max_rows, const uint16_t *W13, const uint16_t *W2,
+                                const float *row_weight, int S, int d, int I, float clamp,
+                                float *gu_save, uint16_t *h_perm, uint16_t *y_perm, void *ws,
+                                size_t ws_bytes, void *stream);
 
 /* The two halves of moe_expert_ffn, for callers that schedule them apart.
  * moe_expert_gemm1 writes h_perm (and gu_save when not NULL);

@@ -31,7 +31,7 @@ MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE = 1, 2
 
 EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_route", "moe_permute",
            "moe_permute_noalloc",
-           "moe_expert_ffn", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
+           "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout"]
 
 
@@ -113,6 +113,8 @@ _SIGS = {
     "moe_permute": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_permute_noalloc": ([_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_expert_ffn": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_expert_ffn_fused": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _Z, _P],
+                             _I),
     "moe_expert_gemm1": ([_P, _P, _I, _I, _P, _I, _I, _F, _P, _P, _P], _I),
     "moe_expert_gemm2": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_combine": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
@@ -255,6 +257,17 @@ def moe_expert_ffn(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, c
                                _ptr(y_perm, BF16, "y_perm"), _ptr(ws, U8, "ws"),
                                0 if ws is None else ws.numel(), _stream(stream))
     _check("moe_expert_ffn", st)
+
+
+def moe_expert_ffn_fused(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp,
+                         gu_save, h_perm, y_perm, ws, stream=None):
+    st = load().moe_expert_ffn_fused(_ptr(x_perm, BF16, "x_perm"), _ptr(offsets, I32, "offsets"),
+                                     G, max_rows, _ptr(W13, BF16, "W13"), _ptr(W2, BF16, "W2"),
+                                     _ptr(row_weight, F32, "row_weight"), S, d, I, float(clamp),
+                                     _ptr(gu_save, F32, "gu_save"), _ptr(h_perm, BF16, "h_perm"),
+                                     _ptr(y_perm, BF16, "y_perm"), _ptr(ws, U8, "ws"),
+                                     0 if ws is None else ws.numel(), _stream(stream))
+    _check("moe_expert_ffn_fused", st)
 
 
 def moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm,

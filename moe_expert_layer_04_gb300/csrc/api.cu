@@ -213,6 +213,10 @@ extern "C" {
 size_t moe_workspace_size(int T, int d, int E, int k, int I, int flags) {
     if (check_shapes(T, d, E, k, I) != MOE_OK) return 0;
     size_t b = permute_workspace_bytes(T, E, k);
+    // moe_expert_ffn_fused's readiness counters (the calls run one after the
+    // other on a stream, so they share the buffer)
+    const size_t fc = (size_t)ffn_fused_counters(T * k + T, E + 1) * sizeof(int);
+    if (fc > b) b = fc;
     if (flags & MOE_FLAG_BACKWARD) {
         const size_t bw = carve_bwd(nullptr, T, d, E, k, I, flags).bytes;
         if (bw > b) b = bw;
@@ -307,6 +311,26 @@ moe_status moe_expert_ffn(const uint16_t *x_perm, const int32_t *offsets, int G,
     s = moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm, stream);
     if (s != MOE_OK) return s;
     return moe_expert_gemm2(h_perm, offsets, G, max_rows, W2, row_weight, S, d, I, y_perm, stream);
+}
+
+moe_status moe_expert_ffn_fused(const uint16_t *x_perm, const int32_t *offsets, int G,
+                                int max_rows, const uint16_t *W13, const uint16_t *W2,
+                                const float *row_weight, int S, int d, int I, float clamp,
+                                float *gu_save, uint16_t *h_perm, uint16_t *y_perm, void *ws,
+                                size_t ws_bytes, void *stream) {
+    moe_status s = check_ffn(G, max_rows, d, I, S);
+    if (s != MOE_OK) return s;
+    if (I % 128 != 0 || d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!x_perm || !offsets || !W13 || !W2 || !h_perm || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(W13) || !aligned16(W2) || !aligned16(h_perm) ||
+        !aligned16(y_perm) || (gu_save && !aligned16(gu_save)))
+        return MOE_ERR_INVALID_ARG;
+    if (!(clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < (size_t)ffn_fused_counters(max_rows, G) * sizeof(int) ||
+        (reinterpret_cast<uintptr_t>(ws) & 3u) != 0)
+        return MOE_ERR_WORKSPACE;
+    return launch_ffn12(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, h_perm,
+                        gu_save, y_perm, static_cast<int *>(ws), static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_expert_gemm1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,

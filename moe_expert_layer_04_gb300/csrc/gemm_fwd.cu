@@ -88,3 +88,52 @@ moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// One readiness counter per 128-row tile of the grouped row space.
+int ffn_fused_counters(int max_rows, int G) { return row_tile_bound(max_rows, G); }
+
+moe_status launch_ffn12(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                        const uint16_t *W13, const uint16_t *W2, const float *row_w, int S, int d,
+                        int I, float clamp, uint16_t *h, float *gu_save, uint16_t *y, int *ready,
+                        cudaStream_t st) {
+    if (I % 128 != 0 || d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    constexpr int BN = 256;
+    // GEMM 1: [g|u] = x_perm W13[g]^T, 128 h columns (gate and up halves) per tile
+    if (!encode_tmap_bf16_2d(&p.tmA, x_perm, d, max_rows, (uint64_t)d * 2, 64, 128))
+        return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d(&p.tmB, W13, d, (uint64_t)G * 2 * I, (uint64_t)d * 2, 64, BN / 2))
+        return MOE_ERR_CUDA;
+    // GEMM 2: y = w (h W2[g]^T), 256 output columns per tile
+    if (!encode_tmap_bf16_2d(&p.tmO, h, I, max_rows, (uint64_t)I * 2, 64, 128))
+        return MOE_ERR_CUDA;
+    if (!encode_tmap_bf16_2d(&p.tmO2, W2, I, (uint64_t)G * d, (uint64_t)I * 2, 64, BN))
+        return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.n_tiles = I / (BN / 2);
+    p.k_blocks = d / 64;
+    p.b_rows_per_group = 2 * I;
+    p.I = I;
+    p.clamp = clamp;
+    p.out = h;
+    p.out2 = gu_save;
+    p.out3 = y;
+    p.N = d;
+    p.n_tiles2 = d / BN;
+    p.k_blocks2 = I / 64;
+    p.b_rows2 = d;
+    p.row_w = row_w;
+    p.w_rows = S;
+    p.ready = ready;
+    p.ready_target = p.n_tiles * ModeTraits<GM_FFN12>::NEPI;
+    const int rt = ffn_fused_counters(max_rows, G);
+    if (cudaMemsetAsync(ready, 0, (size_t)rt * sizeof(int), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return launch_gemm<GM_FFN12, BN>(p, rt * (p.n_tiles + p.n_tiles2), st);
+}
+
+}  // namespace moe

@@ -18,6 +18,10 @@
 //                group selects its expert's weights;
 //   K-grouped    (GM_WGRAD) the contraction runs over each group's rows
 //                (ragged K, zero rows -> zero output), output [G, M, N].
+// GM_FFN12 runs the row-grouped tiles of expert GEMM 1 and then those of
+// expert GEMM 2 in one launch: a GEMM-2 row tile's producer waits (bounded)
+// until every epilogue warp of the GEMM-1 tiles of that row tile has
+// released its h rows through a counter.
 // Tiles are handed out round-robin (tile = blockIdx.x + i * gridDim.x), so
 // the schedule is static and the results are deterministic.
 //
@@ -55,6 +59,11 @@ struct GemmParams {
     int w_rows;
     const float *gu_in;      // DGRAD2: saved fp32 g|u (gu_offset layout)
     const float *col_add;    // GM_GATE: per-column offset (nullable)
+    // GM_FFN12: the GEMM-2 phase (A = h through tmO, B = W2 through tmO2,
+    // y to out3) and the per-row-tile counters of finished GEMM-1 warps
+    int n_tiles2, k_blocks2, b_rows2;
+    int *ready;
+    int ready_target;
     int *status;
     long long wait_limit;
 };
@@ -116,6 +125,8 @@ struct TileInfo {
     int krow0;       // GM_WGRAD: first contraction row
     int krows;       // GM_WGRAD: contraction rows
     int kb;          // k blocks of 64
+    int phase;       // GM_FFN12: 0 = GEMM 1, 1 = GEMM 2
+    int rt;          // row modes: index of the row tile (over all groups)
 };
 
 // Tile t of the schedule.  With CL = 2 (a two-CTA cluster sharing the B
@@ -127,8 +138,19 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
                                                 const int *offs, int rank) {
     using MT = ModeTraits<MODE>;
     TileInfo ti;
-    ti.nt = t % p.n_tiles;
-    const int q = t / p.n_tiles;
+    int tt = t, ntc = p.n_tiles;
+    ti.phase = 0;
+    if constexpr (MODE == GM_FFN12) {
+        const int t1 = mt_start[p.G] * p.n_tiles;   // tiles of GEMM 1
+        if (t >= t1) {
+            tt = t - t1;
+            ntc = p.n_tiles2;
+            ti.phase = 1;
+        }
+    }
+    ti.nt = tt % ntc;
+    const int q = tt / ntc;
+    ti.rt = q;
     ti.m0 = 0;
     ti.krow0 = 0;
     ti.krows = 0;
@@ -146,7 +168,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
         ti.g = lo;
         ti.row0 = offs[lo] + ((q - mt_start[lo]) * CL + rank) * 128;
         ti.rows_valid = min(128, offs[lo + 1] - ti.row0);
-        ti.kb = p.k_blocks;
+        ti.kb = ti.phase ? p.k_blocks2 : p.k_blocks;
     } else {
         const int mp = p.m_tiles / CL;
         ti.g = q / mp;
@@ -174,6 +196,72 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
     const float a = fminf(g, c);
     const float b = fminf(fmaxf(u, -c), c);
     return a / (1.0f + expf(-a)) * b;
+}
+
+// Epilogue of expert GEMM 1 (one thread = one row of the tile): the clamped
+// SwiGLU of the accumulator's gate half (columns [0, BN/2)) and up half ->
+// h (bf16), plus the fp32 g|u when it is saved for the backward.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(const GemmParams &p, const TileInfo &ti, uint32_t tb,
+                                           bool valid, int row) {
+    constexpr int BH = BN / 2;
+    uint16_t *h = static_cast<uint16_t *>(p.out);
+    float *gu = static_cast<float *>(p.out2);
+#pragma unroll 1
+    for (int c = 0; c < BH; c += 32) {
+        uint32_t rg[32], ru[32];
+        tmem_ld32(tb + c, rg);
+        tmem_ld32(tb + BH + c, ru);
+        tmem_wait_ld();
+        if (valid) {
+            const int col = ti.nt * BH + c;
+            uint32_t hp[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                hp[j] = pack_bf16x2(
+                    swiglu_clamped(__uint_as_float(rg[2 * j]), __uint_as_float(ru[2 * j]), p.clamp),
+                    swiglu_clamped(__uint_as_float(rg[2 * j + 1]), __uint_as_float(ru[2 * j + 1]),
+                                   p.clamp));
+            if (h) {
+                uint16_t *dst = h + (size_t)row * p.I + col;
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    st_global_v4(dst + 2 * j, hp[j], hp[j + 1], hp[j + 2], hp[j + 3]);
+            }
+            if (gu) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    st_global_v4(gu + gu_offset(row, col + j, p.I), rg[j], rg[j + 1], rg[j + 2],
+                                 rg[j + 3]);
+                    st_global_v4(gu + gu_offset(row, p.I + col + j, p.I), ru[j], ru[j + 1],
+                                 ru[j + 2], ru[j + 3]);
+                }
+            }
+        }
+    }
+}
+
+// Epilogue of expert GEMM 2 and dgrad 1: the accumulator times w -> bf16
+// columns [nt BN, (nt + 1) BN) of this thread's row of y (row pitch N).
+template <int BN>
+__device__ __forceinline__ void epi_bf16_scaled(uint16_t *y, int N, const TileInfo &ti, uint32_t tb,
+                                                bool valid, int row, float w) {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tb + c, r);
+        tmem_wait_ld();
+        if (valid) {
+            uint16_t *dst = y + (size_t)row * N + ti.nt * BN + c;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8)
+                st_global_v4(dst + j,
+                             pack_bf16x2(w * __uint_as_float(r[j]), w * __uint_as_float(r[j + 1])),
+                             pack_bf16x2(w * __uint_as_float(r[j + 2]), w * __uint_as_float(r[j + 3])),
+                             pack_bf16x2(w * __uint_as_float(r[j + 4]), w * __uint_as_float(r[j + 5])),
+                             pack_bf16x2(w * __uint_as_float(r[j + 6]), w * __uint_as_float(r[j + 7])));
+        }
+    }
 }
 
 // CL = 1: one CTA per tile.  CL = 2: clusters of two CTAs; the pair computes
@@ -226,7 +314,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
         tma_prefetch_desc(&p.tmB);
-        if constexpr (TS::TMA_STORE) tma_prefetch_desc(&p.tmO);
+        if constexpr (TS::TMA_STORE || MODE == GM_FFN12) tma_prefetch_desc(&p.tmO);
+        if constexpr (MODE == GM_FFN12) tma_prefetch_desc(&p.tmO2);
         if constexpr (MODE == GM_DGRAD2) tma_prefetch_desc(&p.tmO2);
     }
     if (warp == 1) {
@@ -277,7 +366,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     if constexpr (MT::DENSE) {
         total_tiles = ((((p.rows + 127) >> 7) + CL - 1) / CL) * p.n_tiles;
     } else if constexpr (MT::ROWGROUP) {
-        total_tiles = mt_start[p.G] * p.n_tiles;
+        total_tiles = mt_start[p.G] * (MODE == GM_FFN12 ? p.n_tiles + p.n_tiles2 : p.n_tiles);
     } else {
         total_tiles = p.G * (p.m_tiles / CL) * p.n_tiles;
     }
@@ -292,6 +381,19 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
             bool ok = true;
             for (int t = cid; ok && t < total_tiles; t += ncl) {
                 const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
+                if constexpr (MODE == GM_FFN12) {
+                    if (ti.phase == 1) {
+                        // the h rows of this row tile: every epilogue warp of its
+                        // GEMM-1 tiles has released them (earlier tiles of the
+                        // static order, all on resident CTAs).  The writers
+                        // fenced their stores into the async proxy before the
+                        // release, so the copies below may read them at once.
+                        if (!wait_count_geq(p.ready + ti.rt, p.ready_target, wc)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
                 for (int kb = 0; kb < ti.kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], TS::STAGE_BYTES);
@@ -300,11 +402,23 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                     if constexpr (MT::A_MN) {
                         tma_load_2d(a_dst, &p.tmA, &full[s], ti.m0, ti.krow0 + kb * 64);
                         tma_load_2d(a_dst + 8192, &p.tmA, &full[s], ti.m0 + 64, ti.krow0 + kb * 64);
+                    } else if (MODE == GM_FFN12 && ti.phase == 1) {
+                        tma_load_2d(a_dst, &p.tmO, &full[s], kb * 64, ti.row0);
                     } else {
                         tma_load_2d(a_dst, &p.tmA, &full[s], kb * 64, ti.row0);
                     }
                     if constexpr (CL == 1) {
-                        if constexpr (MODE == GM_GATE) {
+                        if constexpr (MODE == GM_FFN12) {
+                            if (ti.phase == 0) {
+                                const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
+                                tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, r);
+                                tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB, &full[s], kb * 64,
+                                            r + p.I);
+                            } else {
+                                tma_load_2d(b_dst, &p.tmO2, &full[s], kb * 64,
+                                            ti.g * p.b_rows2 + ti.nt * BN);
+                            }
+                        } else if constexpr (MODE == GM_GATE) {
                             tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, ti.nt * BN);
                         } else if constexpr (MODE == GM_FFN1) {
                             const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
@@ -473,62 +587,28 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                     }
                 }
             } else if constexpr (MODE == GM_FFN1) {
-                constexpr int BH = BN / 2;
-                uint16_t *h = static_cast<uint16_t *>(p.out);
-                float *gu = static_cast<float *>(p.out2);
-#pragma unroll 1
-                for (int c = 0; c < BH; c += 32) {
-                    uint32_t rg[32], ru[32];
-                    tmem_ld32(tb + c, rg);
-                    tmem_ld32(tb + BH + c, ru);
-                    tmem_wait_ld();
-                    if (valid) {
-                        const int col = ti.nt * BH + c;
-                        uint32_t hp[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            hp[j] = pack_bf16x2(
-                                swiglu_clamped(__uint_as_float(rg[2 * j]), __uint_as_float(ru[2 * j]), p.clamp),
-                                swiglu_clamped(__uint_as_float(rg[2 * j + 1]), __uint_as_float(ru[2 * j + 1]), p.clamp));
-                        if (h) {
-                            uint16_t *dst = h + (size_t)row * p.I + col;
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                st_global_v4(dst + 2 * j, hp[j], hp[j + 1], hp[j + 2], hp[j + 3]);
-                        }
-                        if (gu) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                st_global_v4(gu + gu_offset(row, col + j, p.I), rg[j], rg[j + 1],
-                                             rg[j + 2], rg[j + 3]);
-                                st_global_v4(gu + gu_offset(row, p.I + col + j, p.I), ru[j],
-                                             ru[j + 1], ru[j + 2], ru[j + 3]);
-                            }
-                        }
-                    }
+                epi_swiglu<BN>(p, ti, tb, valid, row);
+            } else if constexpr (MODE == GM_FFN12) {
+                if (ti.phase == 0) {
+                    epi_swiglu<BN>(p, ti, tb, valid, row);
+                    // release this warp's h rows of the tile to the GEMM-2 producers,
+                    // which read them with TMA: each lane orders its stores before
+                    // later async-proxy accesses, then one release increment
+                    __threadfence();
+                    fence_proxy_async_global();
+                    __syncwarp();
+                    if (lane == 0) red_release_gpu_add(p.ready + ti.rt, 1);
+                } else {
+                    float w = 1.0f;
+                    if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
+                    epi_bf16_scaled<BN>(static_cast<uint16_t *>(p.out3), p.N, ti, tb, valid, row, w);
                 }
             } else if constexpr (MODE == GM_FFN2 || MODE == GM_DGRAD1) {
-                uint16_t *y = static_cast<uint16_t *>(p.out);
                 float w = 1.0f;
                 if constexpr (MODE == GM_FFN2) {
                     if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
                 }
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tb + c, r);
-                    tmem_wait_ld();
-                    if (valid) {
-                        uint16_t *dst = y + (size_t)row * p.N + ti.nt * BN + c;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8)
-                            st_global_v4(dst + j,
-                                         pack_bf16x2(w * __uint_as_float(r[j]), w * __uint_as_float(r[j + 1])),
-                                         pack_bf16x2(w * __uint_as_float(r[j + 2]), w * __uint_as_float(r[j + 3])),
-                                         pack_bf16x2(w * __uint_as_float(r[j + 4]), w * __uint_as_float(r[j + 5])),
-                                         pack_bf16x2(w * __uint_as_float(r[j + 6]), w * __uint_as_float(r[j + 7])));
-                    }
-                }
+                epi_bf16_scaled<BN>(static_cast<uint16_t *>(p.out), p.N, ti, tb, valid, row, w);
             } else if constexpr (MODE == GM_DGRAD2) {
                 uint16_t *dgu = static_cast<uint16_t *>(p.out2);
                 uint16_t *hw = static_cast<uint16_t *>(p.out3);

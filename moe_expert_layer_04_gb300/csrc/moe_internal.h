@@ -50,7 +50,9 @@ enum GemmMode : int {
     GM_FFN2 = 2,    // y = w * (h W2[g]^T) (bf16)
     GM_DGRAD2 = 3,  // dA = dY_perm W2[g] -> clamped-SwiGLU backward (dGU, w h, dw partials)
     GM_DGRAD1 = 4,  // dX_perm = dGU W13[g] (bf16)
-    GM_WGRAD = 5    // dW[g] = A_g^T B_g over the group's rows (fp32)
+    GM_WGRAD = 5,   // dW[g] = A_g^T B_g over the group's rows (fp32)
+    GM_FFN12 = 6    // GM_FFN1 then GM_FFN2 in one persistent launch, each GEMM-2 row
+                    // tile waiting for the GEMM-1 tiles that produce its h rows
 };
 
 // Host launchers (gemm_*.cu).  All pointers are device pointers.
@@ -59,6 +61,13 @@ moe_status launch_gate_gemm(const uint16_t *x, const uint16_t *Wg, const float *
 moe_status launch_ffn1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
                        const uint16_t *W13, int d, int I, float clamp, uint16_t *h,
                        float *gu_save, cudaStream_t st);
+// Both expert GEMMs in one launch (needs I % 128 == 0 and d % 256 == 0);
+// `ready` holds ffn_fused_counters(max_rows, G) ints of the caller's workspace.
+int ffn_fused_counters(int max_rows, int G);
+moe_status launch_ffn12(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                        const uint16_t *W13, const uint16_t *W2, const float *row_w, int S, int d,
+                        int I, float clamp, uint16_t *h, float *gu_save, uint16_t *y, int *ready,
+                        cudaStream_t st);
 moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max_rows,
                        const uint16_t *W2, const float *row_w, int S, int d, int I, uint16_t *y,
                        cudaStream_t st);

@@ -180,6 +180,35 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
+// -------------------------------------------- counters between CTAs
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *p >= target (written by other CTAs with release semantics).
+// Bounded like mbar_wait: false once the CTA has aborted or the limit ran out.
+__device__ __forceinline__ bool wait_count_geq(const int *p, int target, const WaitCtl &w) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const long long t0 = clock64();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (*w.abort) return false;
+        if (clock64() - t0 > w.limit) {
+            *w.abort = 1;
+            atomicExch(w.status, (int)MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Orders this thread's completed async-proxy (TMA) writes to global memory
 // before its later generic-proxy accesses and releases.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -4,7 +4,7 @@ This module only allocates device memory (through PyTorch) and calls the
 library in order; every step of the layer runs in the library's kernels:
 
   forward   moe_gate_route (or moe_route) -> moe_permute -> moe_expert_ffn
-            -> moe_combine
+            (or the one-launch moe_expert_ffn_fused) -> moe_combine
   backward  moe_backward
 
 ("HyperParallel加速DeepSeek-V4.1多模态1M长序列训练" §2.3: MegaGate routing
@@ -26,6 +26,12 @@ def gate_route_supported(d: int, E: int, k: int) -> bool:
     """Shapes the one-kernel gate projection + routing (moe_gate_route) takes:
     the logits of 128 tokens for all E experts must fit in tensor memory."""
     return d % 64 == 0 and E % 32 == 0 and 32 <= E <= 512 and 1 <= k <= min(8, E)
+
+
+def ffn_fused_supported(d: int, I: int) -> bool:
+    """Shapes the one-launch expert FFN (moe_expert_ffn_fused) takes: 256-wide
+    tiles in both matmuls."""
+    return I % 128 == 0 and d % 256 == 0
 
 
 @dataclass(frozen=True)
@@ -51,16 +57,23 @@ class MoELayer:
     weights: dict with W_g [E,d], W13 [E+1,2I,d], W2 [E+1,d,I] (bf16, CUDA).
     fused_route: route with the one-kernel gate projection + routing, which
     also counts the expert load per modality (None: whenever the shape allows).
+    fused_ffn: run both expert matmuls in one persistent launch
+    (moe_expert_ffn_fused).  Off by default: it is bit-identical to the two
+    launches and measures the same on one GPU, and its waits assume that no
+    other work shares the GPU's SMs.
     """
 
     def __init__(self, dims: Dims, weights: dict, scaling: float, clamp: float = 7.0,
                  backward: bool = False, recompute: bool = False, device="cuda",
-                 fused_route: bool | None = None):
+                 fused_route: bool | None = None, fused_ffn: bool = False):
         self.dims = dims
         ok = gate_route_supported(dims.d, dims.E, dims.k)
         if fused_route and not ok:
             raise ValueError(f"moe_gate_route does not take the shape {dims}")
         self.fused_route = ok if fused_route is None else bool(fused_route)
+        if fused_ffn and not ffn_fused_supported(dims.d, dims.I):
+            raise ValueError(f"moe_expert_ffn_fused does not take the shape {dims}")
+        self.fused_ffn = bool(fused_ffn)
         self.w = weights
         self.scaling = float(scaling)
         self.clamp = float(clamp)
@@ -123,6 +136,11 @@ class MoELayer:
 
     def experts(self, stream=None):
         D = self.dims
+        if self.fused_ffn:
+            _lib.moe_expert_ffn_fused(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"],
+                                      self.w["W2"], self.row_weight, D.S, D.d, D.I, self.clamp,
+                                      self.gu_save, self.h_perm, self.y_perm, self.ws, stream)
+            return
         _lib.moe_expert_ffn(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"], self.w["W2"],
                             self.row_weight, D.S, D.d, D.I, self.clamp, self.gu_save,
                             self.h_perm, self.y_perm, None, stream)

@@ -93,6 +93,17 @@ def test_validation_rejects_before_any_launch():
     q = ctypes.c_void_p(258)
     st = lib.moe_expert_ffn(q, p, 2, 64, p, p, nul, 0, 128, 64, 7.0, nul, p, p, nul, 0, nul)
     assert st == _lib.MOE_ERR_INVALID_ARG
+    # moe_expert_ffn_fused: tiles must be 256 wide in both matmuls, and the
+    # readiness counters need a workspace of 4 * (ceil(max_rows/128) + G) bytes
+    big = 1 << 20
+    assert lib.moe_expert_ffn_fused(p, p, 2, 64, p, p, nul, 0, 384, 128, 7.0, nul, p, p, p, big,
+                                    nul) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_fused(p, p, 2, 64, p, p, nul, 0, 256, 192, 7.0, nul, p, p, p, big,
+                                    nul) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_fused(p, p, 2, 64, p, p, nul, 0, 256, 128, 7.0, nul, p, p, nul, 0,
+                                    nul) == _lib.MOE_ERR_WORKSPACE
+    assert lib.moe_expert_ffn_fused(p, p, 2, 300, p, p, nul, 0, 256, 128, 7.0, nul, p, p, p, 16,
+                                    nul) == _lib.MOE_ERR_WORKSPACE
     # moe_backward: null args, and missing saved state without recompute
     assert lib.moe_backward(None, nul) == _lib.MOE_ERR_INVALID_ARG
     a = _lib.BwdArgs(T=8, d=128, E=4, k=2, I=64, scaling=1.0, clamp=7.0, flags=0)
