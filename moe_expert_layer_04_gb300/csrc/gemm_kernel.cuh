@@ -85,11 +85,13 @@ struct ModeTraits {
 
 // Epilogue staging of the TMA-store paths, per epilogue warp:
 //   GM_WGRAD   one 32 x 32 fp32 block (4 KB, 128-byte swizzle);
-//   GM_DGRAD2  one 32 x 32 bf16 block for each of dg, du and w h (2 KB each,
-//              64-byte swizzle).
+//   GM_DGRAD2  one 32 x 32 bf16 block (2 KB, 64-byte swizzle) that dg, du and
+//              w h pass through in turn: the smaller staging leaves room for a
+//              fourth operand stage, which the contraction over d = 4096 needs
+//              more than the epilogue needs three blocks in flight.
 constexpr int kWgradStageBufs = 1;    // fp32 staging buffers per weight-gradient warp
 constexpr int kEpiWarpBytes = kWgradStageBufs * 4096;
-constexpr int kEpiWarpBytesDgrad2 = 3 * 2048;
+constexpr int kEpiWarpBytesDgrad2 = 2048;
 // Operand stages plus staging of the TMA-store path.
 constexpr int kStoreModeBudget = 216 * 1024;
 
@@ -679,30 +681,30 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                     }
                     if (warp_full) {
                         // all 32 rows of this warp exist: stage the three 32 x 32 bf16
-                        // blocks (64-byte swizzle) and write them with TMA stores
-                        if (lane == 0) bulk_wait_group_read<0>();
-                        __syncwarp();
+                        // blocks (64-byte swizzle) one after the other in the
+                        // warp's buffer and write each with a TMA store
                         const uint32_t b0 = smem_u32(stg2);
                         const uint32_t rowb = (uint32_t)lane * 64u;
                         const uint32_t sw2 = (uint32_t)((lane >> 1) & 3);
+                        const int col = ti.nt * BN + c;
+                        const int wrow = ti.row0 + q * 32;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t o = rowb + ((((uint32_t)j) ^ sw2) << 4);
-                            st_shared_v4(b0 + o, og[4 * j], og[4 * j + 1], og[4 * j + 2], og[4 * j + 3]);
-                            st_shared_v4(b0 + 2048 + o, ou[4 * j], ou[4 * j + 1], ou[4 * j + 2],
-                                         ou[4 * j + 3]);
-                            st_shared_v4(b0 + 4096 + o, oh[4 * j], oh[4 * j + 1], oh[4 * j + 2],
-                                         oh[4 * j + 3]);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int col = ti.nt * BN + c;
-                            const int wrow = ti.row0 + q * 32;
-                            tma_store_2d(&p.tmO, stg2, col, wrow);
-                            tma_store_2d(&p.tmO, stg2 + 2048, p.I + col, wrow);
-                            tma_store_2d(&p.tmO2, stg2 + 4096, col, wrow);
-                            bulk_commit_group();
+                        for (int which = 0; which < 3; ++which) {
+                            const uint32_t *src = which == 0 ? og : (which == 1 ? ou : oh);
+                            if (lane == 0) bulk_wait_group_read<0>();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_shared_v4(b0 + rowb + ((((uint32_t)j) ^ sw2) << 4), src[4 * j],
+                                             src[4 * j + 1], src[4 * j + 2], src[4 * j + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (which == 0) tma_store_2d(&p.tmO, stg2, col, wrow);
+                                else if (which == 1) tma_store_2d(&p.tmO, stg2, p.I + col, wrow);
+                                else tma_store_2d(&p.tmO2, stg2, col, wrow);
+                                bulk_commit_group();
+                            }
                         }
                     }
                 }
