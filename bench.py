@@ -448,13 +448,15 @@ def run_extra_workloads(args, weights, dev, world, hbm, bf16):
     return out
 
 
-def run_fwd_bwd(args, weights, dev, world, wl_name="fwd_bwd", inputs=None):
+def run_fwd_bwd(args, weights, dev, world, wl_name="fwd_bwd", inputs=None, wl=None):
     from moe_expert_layer_04_gb300 import workloads as W
     from moe_expert_layer_04_gb300.layer import Dims, MoELayer
-    wl = W.WORKLOADS[wl_name]
-    over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
-    if over:
-        wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()), **over)
+    if wl is None:
+        wl = W.WORKLOADS[wl_name]
+        over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
+        if over:
+            wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()),
+                          **over)
     D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
     inp = inputs if inputs is not None else layer_inputs(wl, dev, weights=weights)
     layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True, recompute=wl.recompute)
@@ -491,6 +493,24 @@ def run_fwd_bwd(args, weights, dev, world, wl_name="fwd_bwd", inputs=None):
                             + (BWD_RECOMPUTE_EXTRA if wl.recompute else 0)) * steps}
     del layer, inp
     torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------- forward + backward alone
+
+def run_fwd_bwd_only(args):
+    """Forward + backward of the named workload alone (its own weights at its
+    own sizes), e.g. to capture a launch list of the 64K-token slice."""
+    from moe_expert_layer_04_gb300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    wl = workload(args)
+    inp = layer_inputs(wl, dev)
+    weights = {k: inp[k] for k in ("W_g", "W13", "W2")}
+    args.tokens = args.experts = 0          # already applied by workload()
+    out = run_fwd_bwd(args, weights, dev, 1, wl_name=args.workload, inputs=inp, wl=wl)
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
     return out
 
 
@@ -624,6 +644,8 @@ def main():
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling)")
     ap.add_argument("--route-only", action="store_true",
                     help="time only the routing step of the workload (profiling)")
+    ap.add_argument("--fwd-bwd-only", action="store_true",
+                    help="time only forward + backward of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -633,6 +655,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.route_only:
         print(json.dumps(run_route_only(args)), flush=True)
+        return
+    if args.fwd_bwd_only:
+        print(json.dumps(run_fwd_bwd_only(args)), flush=True)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
