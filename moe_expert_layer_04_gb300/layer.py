@@ -155,18 +155,21 @@ class MoELayer:
         _lib.moe_expert_gemm2(self.h_perm, self.offsets, D.E + 1, D.R, self.w["W2"],
                               self.row_weight, D.S, D.d, D.I, self.y_perm, stream)
 
-    def combine(self, stream=None):
+    def combine(self, stream=None, y=None):
         D = self.dims
-        _lib.moe_combine(self.y_perm, self.slot_row, D.T, D.d, D.k, 1, self.y, stream)
+        _lib.moe_combine(self.y_perm, self.slot_row, D.T, D.d, D.k, 1,
+                         self.y if y is None else y, stream)
 
     def forward(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
-                input_ids=None, tid2eid=None, stream=None):
+                input_ids=None, tid2eid=None, stream=None, y=None):
+        """One forward pass; the output goes to self.y, or to `y` ([T, d] bf16)
+        when given."""
         self.x = x
         self.route(x, bias, is_vision, logit_offset, mode, input_ids, tid2eid, stream)
         self.dispatch(x, stream)
         self.experts(stream)
-        self.combine(stream)
-        return self.y
+        self.combine(stream, y)
+        return self.y if y is None else y
 
     # ----------------------------------------------------------- backward
     def backward(self, dY, want_dlogits=False, want_dweights=False, stream=None):
@@ -193,3 +196,61 @@ class MoELayer:
 
 
 __all__ = ["Dims", "MoELayer", "MOE_ROUTE_TOPK", "MOE_ROUTE_HASH"]
+
+
+class HostPipeline:
+    """Forward passes over batches that live in pinned host memory.
+
+    Each batch is copied to the device, run through the layer, and its output
+    copied back.  Two device buffers each way and one copy stream per
+    direction let batch i+1's host-to-device copy and batch i-1's
+    device-to-host copy run while the layer computes batch i, so a sequence
+    of batches costs about the compute alone; every batch still makes both
+    copies.  Batches run in order on the caller's current stream, which
+    afterwards also waits for the last copy back.
+    """
+
+    def __init__(self, layer: MoELayer):
+        D = layer.dims
+        dev = layer.y.device
+        self.layer = layer
+        self.x_dev = [torch.empty(D.T, D.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.y_dev = [torch.empty(D.T, D.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.x_ready = [torch.cuda.Event() for _ in range(2)]
+        self.x_free = [torch.cuda.Event() for _ in range(2)]
+        self.y_ready = [torch.cuda.Event() for _ in range(2)]
+        self.y_free = [torch.cuda.Event() for _ in range(2)]
+
+    def _copy_in(self, i, x_host):
+        b = i % 2
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.x_free[b])      # batch i-2 no longer reads x_dev[b]
+            self.x_dev[b].copy_(x_host, non_blocking=True)
+            self.x_ready[b].record(self.h2d)
+
+    def run(self, xs_host, ys_host, bias, is_vision=None, logit_offset=None, **route_kw):
+        """xs_host[i] ([T, d] bf16, pinned) -> layer -> ys_host[i] (pinned)."""
+        comp = torch.cuda.current_stream(self.layer.y.device)
+        # the copies start after everything the caller queued before
+        self.h2d.wait_stream(comp)
+        self.d2h.wait_stream(comp)
+        n = len(xs_host)
+        if n:
+            self._copy_in(0, xs_host[0])
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                self._copy_in(i + 1, xs_host[i + 1])
+            comp.wait_event(self.x_ready[b])
+            comp.wait_event(self.y_free[b])          # batch i-2's output has left y_dev[b]
+            self.layer.forward(self.x_dev[b], bias, is_vision, logit_offset, y=self.y_dev[b],
+                               **route_kw)
+            self.x_free[b].record(comp)
+            self.y_ready[b].record(comp)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.y_ready[b])
+                ys_host[i].copy_(self.y_dev[b], non_blocking=True)
+                self.y_free[b].record(self.d2h)
+        comp.wait_stream(self.d2h)
