@@ -42,10 +42,14 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
                       pack_bf16x2(a[6], a[7]));
 }
 
-// One thread per (token, 16-byte column chunk): the k + 1 row loads of a
-// chunk are independent, so each thread keeps them all in flight.  Shared row
-// first, then the slots in order.  When dz != nullptr the gate term
-// sum_j dz_j W_g[ids_j] is added as well (the dX assembly of the backward).
+// One thread per (token, 16-byte column chunk).  KM >= k is a compile-time
+// bound: the slot indices and then all k + 1 row loads of the chunk are issued
+// before the first add, so a thread waits for one memory latency, not k + 1
+// in a row.  The sum is fp32 in a fixed order: shared row first, then the
+// slots in order.  KM = 0 is the generic form for any k (one row at a time).
+// When dz != nullptr the gate term sum_j dz_j W_g[ids_j] is added as well (the
+// dX assembly of the backward).
+template <int KM>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ yp,
                                                       const int32_t *__restrict__ slot_row,
                                                       int T, int vecs, int k, int with_shared,
@@ -60,12 +64,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ 
         const int t = (int)(it / vecs);
         const int c = (int)(it - (size_t)t * vecs);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (with_shared) add_bf16x8(acc, yp[(S + t) * vecs + c]);
         const int32_t *sr = slot_row + (size_t)t * k;
-        for (int j = 0; j < k; ++j) add_bf16x8(acc, yp[(size_t)sr[j] * vecs + c]);
-        if (dz) {
-            for (int j = 0; j < k; ++j)
-                fma_bf16x8(acc, dz[(size_t)t * k + j], Wg[(size_t)ids[(size_t)t * k + j] * vecs + c]);
+        if constexpr (KM == 0) {
+            if (with_shared) add_bf16x8(acc, yp[(S + t) * vecs + c]);
+            for (int j = 0; j < k; ++j) add_bf16x8(acc, yp[(size_t)sr[j] * vecs + c]);
+            if (dz) {
+                for (int j = 0; j < k; ++j)
+                    fma_bf16x8(acc, dz[(size_t)t * k + j],
+                               Wg[(size_t)ids[(size_t)t * k + j] * vecs + c]);
+            }
+        } else {
+            int rows[KM];
+#pragma unroll
+            for (int j = 0; j < KM; ++j) rows[j] = j < k ? sr[j] : 0;
+            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 vs = with_shared ? yp[(S + t) * vecs + c] : zero;
+            uint4 v[KM];
+#pragma unroll
+            for (int j = 0; j < KM; ++j) v[j] = j < k ? yp[(size_t)rows[j] * vecs + c] : zero;
+            if (with_shared) add_bf16x8(acc, vs);
+#pragma unroll
+            for (int j = 0; j < KM; ++j)
+                if (j < k) add_bf16x8(acc, v[j]);
+            if (dz) {
+                float a[KM];
+#pragma unroll
+                for (int j = 0; j < KM; ++j) {
+                    a[j] = j < k ? dz[(size_t)t * k + j] : 0.0f;
+                    rows[j] = j < k ? ids[(size_t)t * k + j] : 0;
+                }
+#pragma unroll
+                for (int j = 0; j < KM; ++j) v[j] = j < k ? Wg[(size_t)rows[j] * vecs + c] : zero;
+#pragma unroll
+                for (int j = 0; j < KM; ++j)
+                    if (j < k) fma_bf16x8(acc, a[j], v[j]);
+            }
         }
         y[it] = pack8(acc);
     }
@@ -192,9 +225,16 @@ moe_status launch_combine(const uint16_t *y_perm, const int32_t *slot_row, int T
     const size_t n = (size_t)T * (d / 8);
     const size_t want = (n + 255) / 256;
     const size_t cap = (size_t)num_sms() * 8;
-    combine_kernel<<<(int)(want < cap ? want : cap), 256, 0, st>>>(
-        reinterpret_cast<const uint4 *>(y_perm), slot_row, T, d / 8, k, with_shared, dz, ids,
-        reinterpret_cast<const uint4 *>(Wg), reinterpret_cast<uint4 *>(y));
+    const int grid = (int)(want < cap ? want : cap);
+    const uint4 *yp = reinterpret_cast<const uint4 *>(y_perm);
+    const uint4 *wg = reinterpret_cast<const uint4 *>(Wg);
+    uint4 *yo = reinterpret_cast<uint4 *>(y);
+    if (k <= 8)
+        combine_kernel<8><<<grid, 256, 0, st>>>(yp, slot_row, T, d / 8, k, with_shared, dz, ids,
+                                                wg, yo);
+    else
+        combine_kernel<0><<<grid, 256, 0, st>>>(yp, slot_row, T, d / 8, k, with_shared, dz, ids,
+                                                wg, yo);
     return cuda_status(cudaGetLastError());
 }
 
