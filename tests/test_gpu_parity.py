@@ -25,6 +25,10 @@ CASES = {
     "mid_skew": W.Workload("mid_skew", 520, 384, 12, 3, 256, 2.5, zipf_s=1.1),
     # many rows per expert: the weight gradients run as two-CTA clusters sharing B
     "paired": W.Workload("paired", 2048, 256, 6, 2, 256, 2.5, vision_frac=0.3),
+    # the largest expert count: 1025 GEMM groups, most with 0..4 rows
+    "max_groups": W.Workload("max_groups", 300, 128, 1024, 8, 64, 2.5, vision_frac=0.3),
+    # one token routed to every expert (k = E)
+    "one_token_all_experts": W.Workload("one_token_all_experts", 1, 128, 4, 4, 64, 1.0),
 }
 
 
@@ -178,7 +182,9 @@ def test_forward_layer(name):
 
 @pytest.mark.parametrize("name,recompute", [("tiny", False), ("mid_I192", False),
                                             ("mid_skew", False), ("mid_skew", True),
-                                            ("paired", False)])
+                                            ("paired", False), ("max_groups", False),
+                                            ("max_groups", True),
+                                            ("one_token_all_experts", False)])
 def test_backward_layer(name, recompute):
     w = CASES[name]
     layer, inp = make_layer(w, backward=True, recompute=recompute)
