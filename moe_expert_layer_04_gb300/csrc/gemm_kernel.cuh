@@ -277,6 +277,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     static_assert(CL == 1 || !MT::B_MN || BN >= 128, "the B boxes split between the pair");
     using TS = TileShape<BN, MODE>;
     constexpr int STAGES = TS::STAGES;
+    // the barrier block (full/empty per stage, two tfull, two tempty, done, the
+    // TMEM base and the abort flag) must fit the 256 bytes the layout reserves
+    static_assert((2 * STAGES + 5) * 8 + 8 <= 256, "too many operand stages for the barrier block");
     constexpr uint32_t IDESC = idesc_bf16_f32(128, BN, MT::A_MN, MT::B_MN);
 
     extern __shared__ uint8_t smem_raw[];
