@@ -85,6 +85,11 @@ def _load():
                                       _I, _P, _P], None),
                 "orc_expert_wgrad_entries": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I,
                                               _D, _I, _I, _I, _P, _P, _P, _P], None),
+                "orc_mx_quantize": ([_P, _I, _I, _I, _I, _P, _P], None),
+                "orc_mx_dequantize": ([_P, _P, _I, _I, _I, _P], None),
+                "orc_e4m3_decode_all": ([_P], None),
+                "orc_e4m3_encode": ([_P, _I, _P], None),
+                "orc_expert_rows_mx": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _D, _P, _P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -349,3 +354,64 @@ def expert_wgrad_entries(x, W13, W2, dY, e, row_tok, row_w, clamp, kind, qa, qb,
                                      int(exact), int(store_bf16), kd.shape[0], _ptr(kd),
                                      _ptr(a), _ptr(b), _ptr(out))
     return out
+
+
+# ------------------------------------------------------------------ MXFP8
+# OCP Microscaling (MX) v1.0 with E4M3 elements: blocks of 32 along the
+# contraction, one E8M0 scale per block (see moe_oracle.c for the reading).
+
+def e4m3_decode_all():
+    """Value of every E4M3 code 0..255 (NaN for 0x7F and 0xFF)."""
+    out = np.empty(256, np.float64)
+    _load().orc_e4m3_decode_all(_ptr(out))
+    return out
+
+
+def e4m3_encode(y):
+    """Nearest E4M3 code of each value (ties to even, saturating at 448)."""
+    yv = np.ascontiguousarray(np.asarray(y, dtype=np.float64).reshape(-1))
+    out = np.empty(yv.shape[0], np.uint8)
+    _load().orc_e4m3_encode(_ptr(yv), int(yv.shape[0]), _ptr(out))
+    return out.reshape(np.shape(y))
+
+
+def mx_quantize(src, sf_pitch=None):
+    """MX quantisation of a [rows, K] matrix (torch bf16 or float64, K % 32 ==
+    0) along K.  Returns (q uint8 [rows, K], sf uint8 [rows, sf_pitch]);
+    sf_pitch defaults to K // 32 (padding bytes are zero)."""
+    (a,), bf = _floats(src)
+    rows, K = a.shape
+    assert K % 32 == 0
+    pitch = K // 32 if sf_pitch is None else int(sf_pitch)
+    q = np.empty((rows, K), np.uint8)
+    sf = np.zeros((rows, pitch), np.uint8)
+    _load().orc_mx_quantize(_ptr(a), bf, rows, K, pitch, _ptr(q), _ptr(sf))
+    return q, sf
+
+
+def mx_dequantize(q, sf, K=None):
+    """Values (float64 [rows, K]) of a quantised matrix."""
+    qn = np.ascontiguousarray(_to_np(q), dtype=np.uint8)
+    sn = np.ascontiguousarray(_to_np(sf), dtype=np.uint8)
+    rows, K = qn.shape
+    out = np.empty((rows, K), np.float64)
+    _load().orc_mx_dequantize(_ptr(qn), _ptr(sn), rows, K, int(sn.shape[1]), _ptr(out))
+    return out
+
+
+def expert_rows_mx(x, W13, W2, row_tok, row_exp, row_w, clamp):
+    """MXFP8 expert FFN per row (x, W13, W2 bf16): returns (h, y) with h the
+    dequantised MX h [n, I] and y = row_w * W2~[e] h [n, d]."""
+    (xn, w13, w2), bf = _floats(x, W13, W2)
+    assert bf == 1, "the MX oracle takes bf16 inputs"
+    d = xn.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    re = np.ascontiguousarray(_to_np(row_exp), dtype=np.int32)
+    rw = _opt(row_w, np.float64)
+    n = rt.shape[0]
+    h = np.empty((n, I), np.float64)
+    y = np.empty((n, d), np.float64)
+    _load().orc_expert_rows_mx(_ptr(xn), _ptr(w13), _ptr(w2), n, _ptr(rt), _ptr(re), _ptr(rw),
+                               d, I, float(clamp), _ptr(h), _ptr(y))
+    return h, y

@@ -638,3 +638,196 @@ void orc_expert_wgrad_entries(const void *x, const void *W13, const void *W2, co
         out[q] = acc;
     }
 }
+
+/* ------------------------------------------------------------- MXFP8 */
+/*
+ * MXFP8 expert matmuls, the low-precision variant.  The page "DeepSeek-V4昇腾
+ * 训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse 极简训练优化实践",
+ * 性能结果与未来展望 (outlook), names FP8 training on MxFP8 compute as the
+ * next step and defines no format, so the format is the published OCP
+ * Microscaling Formats (MX) specification v1.0:
+ *   - a block is 32 consecutive elements along the contraction dimension;
+ *   - the block's shared scale is E8M0: code c stands for 2^(c - 127);
+ *   - elements are OCP FP8 E4M3: sign, 4 exponent bits (bias 7), 3 mantissa
+ *     bits, no infinities; largest finite 448 = 1.75 * 2^8, smallest normal
+ *     2^-6, subnormal quantum 2^-9; code 0x7F / 0xFF is NaN.
+ * Quantisation of one block (the spec's conversion section):
+ *   e  = floor(log2(max_i |v_i|)),
+ *   X  = 2^(e - 8)       (8 = exponent of E4M3's largest normal), with the
+ *                         exponent clamped to the E8M0 range [-127, 127],
+ *   p_i = v_i / X rounded to the nearest E4M3 value (ties to even), a
+ *         magnitude above 448 saturated to 448; the sign of p_i is that of
+ *         v_i (a negative value that rounds to zero gives -0).
+ * A block of zeros gets scale code 0 and zero elements.  Readings: the
+ * scale is taken from the block's own values (no global amax), elements
+ * saturate rather than becoming NaN, and in the expert FFN the intermediate
+ * h goes from the SwiGLU straight to MXFP8 (no bf16 step in between).
+ *
+ * Layouts: a quantised [rows, K] matrix is q [rows, K] (one E4M3 code per
+ * byte, row-major) plus sf [rows, sf_pitch] (E8M0 code of block b of row r
+ * at sf[r * sf_pitch + b]; sf_pitch >= K / 32).
+ */
+
+/* Value of an E4M3 code, from the format's definition. */
+static double e4m3_value(uint8_t c)
+{
+    int s = c >> 7, E = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (E == 15 && m == 7) return NAN;
+    if (E == 0) v = ldexp((double)m, -9);                   /* m/8 * 2^-6 */
+    else v = ldexp(1.0 + m / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 code of y (ties to even), magnitude saturated at 448. */
+static uint8_t e4m3_code(double y)
+{
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs(y);
+    if (a == 0.0) return sign;
+    /* spacing of the E4M3 values around a: 2^-9 below the smallest normal,
+     * else 2^(exponent - 3) (3 mantissa bits) */
+    int ex;
+    frexp(a, &ex);                      /* a = f * 2^ex, 0.5 <= f < 1 */
+    int e = ex - 1;                     /* floor(log2 a) */
+    double quantum = e < -6 ? ldexp(1.0, -9) : ldexp(1.0, e - 3);
+    double r = nearbyint(a / quantum) * quantum;   /* ties to even */
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -6)) return sign | (uint8_t)(r / ldexp(1.0, -9));
+    frexp(r, &ex);
+    e = ex - 1;
+    int mant = (int)((r / ldexp(1.0, e) - 1.0) * 8.0);
+    return sign | (uint8_t)(((e + 7) << 3) | mant);
+}
+
+/* E8M0 code of the shared scale of a block of n values. */
+static uint8_t e8m0_block_code(const double *v, int n)
+{
+    double amax = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    if (amax == 0.0) return 0;
+    int ex;
+    frexp(amax, &ex);
+    int se = (ex - 1) - 8;
+    if (se < -127) se = -127;
+    if (se > 127) se = 127;
+    return (uint8_t)(se + 127);
+}
+
+static double e8m0_value(uint8_t c) { return ldexp(1.0, (int)c - 127); }
+
+/* Quantise one row of K values (K % 32 == 0) into codes q[K] and scale codes
+ * sf[K/32]; dq (nullable) receives the dequantised values. */
+static void mx_quantize_row(const double *v, int K, uint8_t *q, uint8_t *sf, double *dq)
+{
+    for (int b = 0; b < K / 32; ++b) {
+        const double *vb = v + 32 * b;
+        uint8_t c = e8m0_block_code(vb, 32);
+        double X = e8m0_value(c);
+        sf[b] = c;
+        for (int i = 0; i < 32; ++i) {
+            uint8_t p = e4m3_code(vb[i] / X);
+            q[32 * b + i] = p;
+            if (dq) dq[32 * b + i] = e4m3_value(p) * X;
+        }
+    }
+}
+
+/* MX quantisation of a [rows, K] matrix (bf16 bit patterns when bf = 1, else
+ * doubles) into q [rows, K] and sf [rows, sf_pitch]; padding bytes of sf are
+ * left untouched. */
+void orc_mx_quantize(const void *src, int bf, int rows, int K, int sf_pitch, uint8_t *q,
+                     uint8_t *sf)
+{
+#pragma omp parallel
+    {
+        double *row = (double *)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(static)
+        for (int r = 0; r < rows; ++r) {
+            for (int i = 0; i < K; ++i) row[i] = ld(src, (size_t)r * K + i, bf);
+            mx_quantize_row(row, K, q + (size_t)r * K, sf + (size_t)r * sf_pitch, NULL);
+        }
+        free(row);
+    }
+}
+
+/* Values of a quantised [rows, K] matrix. */
+void orc_mx_dequantize(const uint8_t *q, const uint8_t *sf, int rows, int K, int sf_pitch,
+                       double *out)
+{
+    for (int r = 0; r < rows; ++r)
+        for (int i = 0; i < K; ++i)
+            out[(size_t)r * K + i] =
+                e4m3_value(q[(size_t)r * K + i]) * e8m0_value(sf[(size_t)r * sf_pitch + i / 32]);
+}
+
+/* Value tables for the pins: E4M3 code -> value (256 entries) and the code
+ * of each y[i]. */
+void orc_e4m3_decode_all(double *out)
+{
+    for (int c = 0; c < 256; ++c) out[c] = e4m3_value((uint8_t)c);
+}
+
+void orc_e4m3_encode(const double *y, int n, uint8_t *out)
+{
+    for (int i = 0; i < n; ++i) out[i] = e4m3_code(y[i]);
+}
+
+/* MXFP8 expert FFN over a list of rows (the MX form of orc_expert_rows):
+ *   x~ = MX(x[row_tok[r]]) along d,  W13~[e] and W2~[e] = MX of each weight
+ *   row along its contraction (d for W13, I for W2),
+ *   g = W13~[e, 0:I] x~,  u = W13~[e, I:2I] x~   (fp64 sums of exact products)
+ *   h = MX(silu(min(g, c)) * clamp(u, -c, c))     along I
+ *   y[r] = row_w[r] * W2~[e] h
+ * h[r] (length I) returns the dequantised MX h; x and the weights are bf16
+ * bit patterns.  Each weight row is quantised on the fly, so the cost is
+ * that of the plain FFN plus one quantisation pass per weight row used. */
+void orc_expert_rows_mx(const uint16_t *x, const uint16_t *W13, const uint16_t *W2, int n,
+                        const int64_t *row_tok, const int32_t *row_exp, const double *row_w,
+                        int d, int I, double c, double *h, double *y)
+{
+#pragma omp parallel
+    {
+        double *xr = (double *)malloc(sizeof(double) * (size_t)d);
+        double *xq = (double *)malloc(sizeof(double) * (size_t)d);
+        double *wr = (double *)malloc(sizeof(double) * (size_t)(d > I ? d : I));
+        double *wq = (double *)malloc(sizeof(double) * (size_t)(d > I ? d : I));
+        double *hv = (double *)malloc(sizeof(double) * (size_t)I);
+        uint8_t *qb = (uint8_t *)malloc((size_t)(d > I ? d : I));
+        uint8_t *sb = (uint8_t *)malloc((size_t)(d > I ? d : I) / 32);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n; ++r) {
+            const int e = row_exp[r];
+            for (int i = 0; i < d; ++i) xr[i] = bf16_to_f64(x[(size_t)row_tok[r] * d + i]);
+            mx_quantize_row(xr, d, qb, sb, xq);
+            for (int i = 0; i < I; ++i) {
+                double gu[2];
+                for (int half = 0; half < 2; ++half) {
+                    const uint16_t *w = W13 + ((size_t)e * 2 * I + (size_t)half * I + i) * d;
+                    for (int k = 0; k < d; ++k) wr[k] = bf16_to_f64(w[k]);
+                    mx_quantize_row(wr, d, qb, sb, wq);
+                    double s = 0.0;
+                    for (int k = 0; k < d; ++k) s += xq[k] * wq[k];
+                    gu[half] = s;
+                }
+                double a = gu[0] < c ? gu[0] : c;
+                double b = gu[1] < -c ? -c : (gu[1] > c ? c : gu[1]);
+                hv[i] = silu(a) * b;
+            }
+            double *hq = h + (size_t)r * I;
+            mx_quantize_row(hv, I, qb, sb, hq);
+            const double w = row_w ? row_w[r] : 1.0;
+            for (int m = 0; m < d; ++m) {
+                const uint16_t *w2 = W2 + ((size_t)e * d + m) * I;
+                for (int i = 0; i < I; ++i) wr[i] = bf16_to_f64(w2[i]);
+                mx_quantize_row(wr, I, qb, sb, wq);
+                double s = 0.0;
+                for (int i = 0; i < I; ++i) s += hq[i] * wq[i];
+                y[(size_t)r * d + m] = w * s;
+            }
+        }
+        free(xr); free(xq); free(wr); free(wq); free(hv); free(qb); free(sb);
+    }
+}

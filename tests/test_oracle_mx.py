@@ -1,0 +1,167 @@
+"""Pins of the MXFP8 part of the oracle (OCP MX v1.0 with E4M3 elements).
+
+The pages name MxFP8 as the next low-precision step and define no format, so
+the pins come from the format's published definition (values in
+tests/golden/ocp_mx_e4m3.txt), from a library routine (PyTorch's float8_e4m3fn
+cast, round-to-nearest-even), from closed forms of the scale selection, from
+the quantisation error bound, and from the reduction of the MX expert FFN to
+the plain expert FFN oracle (itself pinned in test_oracle_pins.py) on
+dequantised inputs."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ocp_mx_e4m3.txt")
+
+
+def _golden():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            kind, code, val = line.split()
+            rows.append((kind, int(code, 16), float(val)))
+    return rows
+
+
+def _same(a, b):
+    return (math.isnan(a) and math.isnan(b)) or (a == b and math.copysign(1, a) == math.copysign(1, b))
+
+
+def test_e4m3_values_from_spec():
+    tab = oracle.e4m3_decode_all()
+    for kind, code, val in _golden():
+        if kind == "e4m3":
+            assert _same(tab[code], val), (hex(code), tab[code], val)
+
+
+def test_e4m3_table_matches_torch():
+    tab = oracle.e4m3_decode_all()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    for c in range(256):
+        assert _same(tab[c], ref[c]), hex(c)
+    # strictly increasing over the finite non-negative codes
+    assert np.all(np.diff(tab[:0x7F]) > 0)
+
+
+def _torch_codes(y):
+    return torch.tensor(y, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    tab = oracle.e4m3_decode_all()
+    grid = tab[:0x7F]                        # 0 .. 448
+    mids = (grid[:-1] + grid[1:]) / 2        # every tie between neighbours
+    rng = np.random.default_rng(0)
+    rand = rng.uniform(-448, 448, 20000)
+    small = rng.uniform(-0.03, 0.03, 20000)  # subnormal and smallest normals
+    y = np.concatenate([grid, -grid, mids, -mids, rand, small]).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(y.astype(np.float64)), _torch_codes(y))
+
+
+def test_e4m3_encode_saturates():
+    codes = oracle.e4m3_encode(np.array([448.0, 449.0, 464.0, 480.0, 511.0, 1e6, -470.0, -1e30]))
+    assert list(codes) == [0x7E] * 6 + [0xFE, 0xFE]
+
+
+def test_e4m3_encode_signed_zero():
+    codes = oracle.e4m3_encode(np.array([0.0, -0.0, 1e-9, -1e-9, 2.0 ** -10, -(2.0 ** -10)]))
+    # 2^-10 is the tie between 0 and the smallest subnormal: ties to even -> 0
+    assert list(codes) == [0x00, 0x80, 0x00, 0x80, 0x00, 0x80]
+
+
+def _block(vals):
+    v = np.zeros((1, 32))
+    v[0, :len(vals)] = vals
+    return v
+
+
+def test_mx_scale_closed_forms():
+    for p in range(-30, 31):
+        q, sf = oracle.mx_quantize(_block([2.0 ** p, 0.5 * 2.0 ** p, -(2.0 ** p)]))
+        assert sf[0, 0] == p - 8 + 127
+        assert list(q[0, :3]) == [0x78, 0x70, 0xF8]       # 256, 128, -256 after scaling
+        q, sf = oracle.mx_quantize(_block([1.75 * 2.0 ** p]))
+        assert sf[0, 0] == p - 8 + 127 and q[0, 0] == 0x7E
+        q, sf = oracle.mx_quantize(_block([1.9 * 2.0 ** p]))   # 486.4 -> saturates to 448
+        assert sf[0, 0] == p - 8 + 127 and q[0, 0] == 0x7E
+    q, sf = oracle.mx_quantize(np.zeros((2, 64)))
+    assert not q.any() and not sf.any()
+    q, sf = oracle.mx_quantize(_block([2.0 ** -130]))        # scale exponent clamps at -127
+    assert sf[0, 0] == 0 and q[0, 0] == 0x20                 # 2^-130 / 2^-127 = 2^-3
+    q, sf = oracle.mx_quantize(_block([2.0 ** 140]))         # clamps at +127, element saturates
+    assert sf[0, 0] == 254 and q[0, 0] == 0x7E
+
+
+def test_mx_roundtrip_on_grid():
+    rng = np.random.default_rng(1)
+    tab = oracle.e4m3_decode_all()
+    rows, K = 16, 256
+    codes = rng.integers(0, 0x7F, size=(rows, K)) | (rng.integers(0, 2, size=(rows, K)) << 7)
+    codes = codes.astype(np.uint8)
+    codes[:, ::32] = rng.integers(0x78, 0x7F, size=(rows, K // 32))  # block max in the top binade
+    se = rng.integers(-40, 40, size=(rows, K // 32))
+    v = tab[codes] * np.repeat(2.0 ** se, 32, axis=1)
+    q, sf = oracle.mx_quantize(v)
+    assert np.array_equal(sf.astype(np.int64) - 127, se)
+    assert np.array_equal(q, codes)
+    assert np.array_equal(oracle.mx_dequantize(q, sf), v)
+
+
+def test_mx_error_bound_and_bf16_path():
+    g = torch.Generator().manual_seed(2)
+    x = torch.randn(64, 512, generator=g, dtype=torch.float64)
+    x[:, 64:96] *= 1e-3                         # blocks of very different magnitude
+    x[3, 100] = 40.0                            # an outlier inside a block
+    xb = x.to(torch.bfloat16)
+    q, sf = oracle.mx_quantize(xb)
+    q2, sf2 = oracle.mx_quantize(xb.double().numpy())
+    assert np.array_equal(q, q2) and np.array_equal(sf, sf2)
+    v = xb.double().numpy()
+    dq = oracle.mx_dequantize(q, sf)
+    X = np.repeat(2.0 ** (sf.astype(np.float64) - 127), 32, axis=1)
+    # half a quantum (2^-4 relative in the normal range, 2^-10 X below it), or
+    # the saturation of a scaled magnitude in (448, 512) to 448
+    bound = np.maximum(np.maximum(np.abs(v) * 2.0 ** -4, X * 2.0 ** -10), np.abs(v) - 448 * X)
+    assert np.all(np.abs(dq - v) <= bound)
+    # the block maximum lands in E4M3's top binade [256, 448]
+    bmax = np.abs(v).reshape(64, 16, 32).max(axis=2)
+    r = bmax / 2.0 ** (sf.astype(np.float64) - 127)
+    assert np.all((r >= 256) & (r < 512))
+
+
+def _bf16(a):
+    t = torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+    assert np.array_equal(t.double().numpy(), a)   # MX values are exact in bf16
+    return t
+
+
+def test_expert_rows_mx_reduces_to_plain_oracle():
+    d, I, G = 128, 64, 3
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(6, d, generator=g).to(torch.bfloat16)
+    W13 = (torch.randn(G, 2 * I, d, generator=g) * 0.05).to(torch.bfloat16)
+    W2 = (torch.randn(G, d, I, generator=g) * 0.05).to(torch.bfloat16)
+    tok = np.array([0, 1, 2, 3, 4, 5, 1, 0])
+    exp_ = np.array([0, 2, 1, 1, 0, 2, 0, 1], np.int32)
+    rw = np.linspace(0.2, 1.4, 8)
+    clamp = 0.8                              # some g and u clamp
+    h_mx, y_mx = oracle.expert_rows_mx(x, W13, W2, tok, exp_, rw, clamp)
+    # the same FFN on the dequantised operands, exactly, through the plain oracle
+    xd = _bf16(oracle.mx_dequantize(*oracle.mx_quantize(x)))
+    w13d = _bf16(oracle.mx_dequantize(*oracle.mx_quantize(W13.reshape(-1, d))).reshape(G, 2 * I, d))
+    w2d = _bf16(oracle.mx_dequantize(*oracle.mx_quantize(W2.reshape(-1, I))).reshape(G, d, I))
+    h_ex, _ = oracle.expert_rows(xd, w13d, w2d, tok, exp_, rw, clamp, exact=True)
+    assert np.array_equal(h_mx, oracle.mx_dequantize(*oracle.mx_quantize(h_ex)))
+    y_lib = np.stack([rw[r] * (w2d[exp_[r]].double().numpy() @ h_mx[r]) for r in range(8)])
+    assert np.allclose(y_mx, y_lib, rtol=1e-12, atol=1e-15)
+    # MXFP8 is a few percent away from the bf16 FFN, never identical to it
+    _, y_bf = oracle.expert_rows(x, W13, W2, tok, exp_, rw, clamp, exact=True)
+    rel = np.linalg.norm(y_mx - y_bf) / np.linalg.norm(y_bf)
+    assert 1e-3 < rel < 0.1, rel
