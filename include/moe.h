@@ -20,6 +20,9 @@
  *          tid2eid[input_ids] and still weights them with the gate logits;
  *          tokens are dispatched to experts, computed, returned and combined
  *          by routing weight.
+ *   [TTN]  "DeepSeek-V4昇腾训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse
+ *          极简训练优化实践", 性能结果与未来展望: FP8 training on MxFP8
+ *          low-precision compute as the next step (the MXFP8 calls below).
  *
  * Conventions for every call
  *   - All pointers are DEVICE pointers unless marked [host].  The caller owns
@@ -284,6 +287,64 @@ typedef struct {
  * The bias gets no gradient (it only ranks); hash routing has the same
  * weight chain.  Clamp gradients pass where the argument equals the bound. */
 moe_status moe_backward(const moe_bwd_args *args, void *stream);
+
+/* ---------------------------------------------------------------- MXFP8
+ * Low-precision expert matmuls ([TTN] outlook: FP8 training on MxFP8
+ * compute).  The pages fix no format; these calls use the OCP Microscaling
+ * Formats (MX) v1.0 specification with FP8 E4M3 elements:
+ *   - a block is 32 consecutive elements along the contraction dimension
+ *     (a row of a K-major matrix), with one E8M0 scale code c: X = 2^(c-127);
+ *   - element codes are OCP E4M3 (bias 7, no infinities, largest 448);
+ *   - quantisation: X = 2^(floor(log2 max|v|) - 8), exponent clamped to
+ *     [-127, 127] (code 0 for an all-zero block); element = v / X rounded to
+ *     the nearest E4M3 value, ties to even, saturated at +-448, the sign kept
+ *     for values that round to zero.
+ * A quantised [rows, K] matrix is a pair of byte arrays:
+ *   q  [rows, K]                 E4M3 codes, row-major (pitch K bytes)
+ *   sf [rows, moe_mx_sf_pitch(K)] E8M0 codes, block b of row r at
+ *                                sf[r * pitch + b]; the padding bytes of a row
+ *                                are neither read for results nor written.
+ * Both must be 16-byte aligned; K % 32 == 0.  The MX expert matmuls compute
+ * with the exact values of the operands (an E4M3 value times its scale is
+ * exact in bf16; products accumulate in fp32), so they differ from a
+ * block-scaled MMA only in the order of the fp32 additions.  Operand blocks
+ * with scales below 2^-117 are outside that exactness. */
+
+/* Bytes per row of the scale array for a contraction of K elements: K/32
+ * rounded up to a multiple of 16. */
+int moe_mx_sf_pitch(int K);
+
+/* MX quantisation of a bf16 [rows, K] matrix along its rows (weights once at
+ * load time: W13 as [G*2I, d], W2 as [G*d, I]).  Needs K % 32 == 0, rows >= 0;
+ * src, q and sf 16-byte aligned, else MOE_ERR_INVALID_ARG. */
+moe_status moe_mx_quantize(const uint16_t *src, long long rows, int K, uint8_t *q, uint8_t *sf,
+                           void *stream);
+
+/* Dispatch gather into MX rows ([HP41] §2.3 MegaMoE token dispatch): each
+ * token row x[t] (bf16 [T, d]) is quantised once and written to rows
+ * slot_row[t*k + j] (j < k) and S + t of x_perm_q [S+T, d] / x_perm_sf
+ * [S+T, moe_mx_sf_pitch(d)], S = T*k; slot_row comes from moe_permute (which
+ * is called with x = NULL for the indices alone).  Needs d % 32 == 0. */
+moe_status moe_mx_gather(const uint16_t *x, const int32_t *slot_row, int T, int d, int k,
+                         uint8_t *x_perm_q, uint8_t *x_perm_sf, void *stream);
+
+/* MXFP8 expert FFN on expert-contiguous rows: the computation of
+ * moe_expert_ffn with MX operands.  For every group g < G and row r in
+ * [offsets[g], offsets[g+1]):
+ *   [g | u] = x~[r] W13~[g]^T                  (exact products, fp32 sums)
+ *   h~[r]   = MX( silu(min(g, clamp)) * clamp(u, -clamp, clamp) )  along I
+ *   y[r]    = bf16( row_weight[r] * (h~[r] W2~[g]^T) )
+ * x~ = (x_perm_q, x_perm_sf) [R, d]; W13~ = (W13_q, W13_sf) [G*2I, d];
+ * W2~ = (W2_q, W2_sf) [G*d, I]; row_weight [S] fp32 or NULL (1 for rows >= S).
+ * Outputs: h_q [R, I] and h_sf [R, moe_mx_sf_pitch(I)] (the MX h), y_perm
+ * [R, d] bf16.  max_rows bounds R = offsets[G] (sizes the launch).  Needs
+ * d % 256 == 0 and I % 128 == 0 (else MOE_ERR_UNSUPPORTED), clamp > 0 and
+ * 16-byte aligned arrays (else MOE_ERR_INVALID_ARG).  No workspace. */
+moe_status moe_expert_ffn_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
+                             const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
+                             const uint8_t *W13_sf, const uint8_t *W2_q, const uint8_t *W2_sf,
+                             const float *row_weight, int S, int d, int I, float clamp,
+                             uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm, void *stream);
 
 /* Text of a status code (static storage). */
 const char *moe_status_string(moe_status s);

@@ -32,7 +32,8 @@ MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE = 1, 2
 EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_route", "moe_permute",
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
-           "moe_last_device_status", "moe_selftest_wait_timeout"]
+           "moe_last_device_status", "moe_selftest_wait_timeout",
+           "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx"]
 
 
 class MoeError(RuntimeError):
@@ -122,6 +123,11 @@ _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_last_device_status": ([_P], _I),
     "moe_selftest_wait_timeout": ([_LL, _P], _I),
+    "moe_mx_sf_pitch": ([_I], _I),
+    "moe_mx_quantize": ([_P, _LL, _I, _P, _P, _P], _I),
+    "moe_mx_gather": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_expert_ffn_mx": ([_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P,
+                           _P], _I),
 }
 
 _lock = threading.Lock()
@@ -268,6 +274,35 @@ def moe_expert_ffn_fused(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d
                                      _ptr(y_perm, BF16, "y_perm"), _ptr(ws, U8, "ws"),
                                      0 if ws is None else ws.numel(), _stream(stream))
     _check("moe_expert_ffn_fused", st)
+
+
+def moe_mx_sf_pitch(K):
+    return load().moe_mx_sf_pitch(int(K))
+
+
+def moe_mx_quantize(src, rows, K, q, sf, stream=None):
+    st = load().moe_mx_quantize(_ptr(src, BF16, "src"), int(rows), int(K), _ptr(q, U8, "q"),
+                                _ptr(sf, U8, "sf"), _stream(stream))
+    _check("moe_mx_quantize", st)
+
+
+def moe_mx_gather(x, slot_row, T, d, k, x_perm_q, x_perm_sf, stream=None):
+    st = load().moe_mx_gather(_ptr(x, BF16, "x"), _ptr(slot_row, I32, "slot_row"), T, d, k,
+                              _ptr(x_perm_q, U8, "x_perm_q"), _ptr(x_perm_sf, U8, "x_perm_sf"),
+                              _stream(stream))
+    _check("moe_mx_gather", st)
+
+
+def moe_expert_ffn_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, W2_q, W2_sf,
+                      row_weight, S, d, I, clamp, h_q, h_sf, y_perm, stream=None):
+    st = load().moe_expert_ffn_mx(_ptr(x_perm_q, U8, "x_perm_q"), _ptr(x_perm_sf, U8, "x_perm_sf"),
+                                  _ptr(offsets, I32, "offsets"), G, max_rows,
+                                  _ptr(W13_q, U8, "W13_q"), _ptr(W13_sf, U8, "W13_sf"),
+                                  _ptr(W2_q, U8, "W2_q"), _ptr(W2_sf, U8, "W2_sf"),
+                                  _ptr(row_weight, F32, "row_weight"), S, d, I, float(clamp),
+                                  _ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"),
+                                  _ptr(y_perm, BF16, "y_perm"), _stream(stream))
+    _check("moe_expert_ffn_mx", st)
 
 
 def moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm,

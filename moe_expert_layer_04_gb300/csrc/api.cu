@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "moe_ptx.cuh"
+#include "mx_common.cuh"
 
 namespace moe {
 
@@ -179,6 +180,14 @@ bool encode_tmap_f32_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint6
                      box_inner, box_outer);
 }
 
+bool encode_tmap_u8_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+                       bool swizzle64) {
+    return encode_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, outer, row_pitch_bytes,
+                     box_inner, box_outer,
+                     swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 moe_status check_shapes(int T, int d, int E, int k, int I) {
     if (T < 1 || d < 1 || E < 1 || k < 1 || I < 1) return MOE_ERR_INVALID_ARG;
     if (k > E) return MOE_ERR_INVALID_ARG;
@@ -331,6 +340,48 @@ moe_status moe_expert_ffn_fused(const uint16_t *x_perm, const int32_t *offsets, 
         return MOE_ERR_WORKSPACE;
     return launch_ffn12(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, h_perm,
                         gu_save, y_perm, static_cast<int *>(ws), static_cast<cudaStream_t>(stream));
+}
+
+int moe_mx_sf_pitch(int K) { return K > 0 ? mx_sf_pitch(K) : 0; }
+
+moe_status moe_mx_quantize(const uint16_t *src, long long rows, int K, uint8_t *q, uint8_t *sf,
+                           void *stream) {
+    if (rows < 0 || K < 32 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!src || !q || !sf || !aligned16(src) || !aligned16(q) || !aligned16(sf))
+        return MOE_ERR_INVALID_ARG;
+    return launch_mx_quantize(src, rows, K, q, sf, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_mx_gather(const uint16_t *x, const int32_t *slot_row, int T, int d, int k,
+                         uint8_t *x_perm_q, uint8_t *x_perm_sf, void *stream) {
+    if (T < 1 || d < 32 || d % 32 != 0 || k < 1 || k > 32) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * (k + 1) * d >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+    if (!x || !slot_row || !x_perm_q || !x_perm_sf || !aligned16(x) || !aligned16(x_perm_q) ||
+        !aligned16(x_perm_sf))
+        return MOE_ERR_INVALID_ARG;
+    return launch_mx_gather(x, slot_row, T, d, k, x_perm_q, x_perm_sf,
+                            static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
+                             const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
+                             const uint8_t *W13_sf, const uint8_t *W2_q, const uint8_t *W2_sf,
+                             const float *row_weight, int S, int d, int I, float clamp,
+                             uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm, void *stream) {
+    moe_status s = check_ffn(G, max_rows, d, I, S);
+    if (s != MOE_OK) return s;
+    if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {x_perm_q, x_perm_sf, W13_q, W13_sf, W2_q, W2_sf, h_q, h_sf, y_perm};
+    for (const void *ptr : ptrs)
+        if (!ptr || !aligned16(ptr)) return MOE_ERR_INVALID_ARG;
+    if (!offsets || !(clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = launch_mx_ffn1(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp, h_q,
+                       h_sf, st);
+    if (s != MOE_OK) return s;
+    return launch_mx_ffn2(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight, S, d, I,
+                          y_perm, st);
 }
 
 moe_status moe_expert_gemm1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,

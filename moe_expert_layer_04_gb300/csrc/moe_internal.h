@@ -34,6 +34,11 @@ bool encode_tmap_bf16_2d_sw64(CUtensorMap *tm, const void *base, uint64_t inner,
 bool encode_tmap_f32_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// 2-D byte matrix (MXFP8 codes or scale codes), 64-byte swizzle or none.
+bool encode_tmap_u8_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+                       bool swizzle64);
+
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -86,6 +91,19 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
 // T identity rows, reading each token row once (permute.cu).
 moe_status launch_gather_rows(const uint16_t *src, const int32_t *slot_row, int T, int d, int k,
                               uint16_t *dst, cudaStream_t st);
+
+// MXFP8 (mx.cu, gemm_mx.cu): quantisation of bf16 rows, the quantising
+// dispatch gather, and the two MX expert GEMMs (d % 256 == 0, I % 128 == 0).
+moe_status launch_mx_quantize(const uint16_t *src, long long rows, int K, uint8_t *q, uint8_t *sf,
+                              cudaStream_t st);
+moe_status launch_mx_gather(const uint16_t *x, const int32_t *slot_row, int T, int d, int k,
+                            uint8_t *q, uint8_t *sf, cudaStream_t st);
+moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *offsets, int G,
+                          int max_rows, const uint8_t *W13q, const uint8_t *W13sf, int d, int I,
+                          float clamp, uint8_t *hq, uint8_t *hsf, cudaStream_t st);
+moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *offsets, int G,
+                          int max_rows, const uint8_t *W2q, const uint8_t *W2sf,
+                          const float *row_w, int S, int d, int I, uint16_t *y, cudaStream_t st);
 
 moe_status launch_selftest_timeout(long long limit, cudaStream_t st);
 

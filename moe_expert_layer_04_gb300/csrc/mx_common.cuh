@@ -1,0 +1,108 @@
+// mx_common.cuh -- MXFP8 helpers shared by the quantiser and the MX GEMMs.
+//
+// Format: OCP Microscaling Formats (MX) v1.0 with FP8 E4M3 elements.  A
+// block is 32 consecutive elements along the contraction; its E8M0 scale code
+// c stands for X = 2^(c - 127).  E4M3 (OCP FP8): sign, 4 exponent bits with
+// bias 7, 3 mantissa bits, no infinities, largest finite 448, subnormal
+// quantum 2^-9.  A block is quantised with X = 2^(floor(log2 amax) - 8)
+// (8 = exponent of E4M3's largest normal, clamped to [-127, 127]) and
+// elements v / X rounded to the nearest E4M3 value, ties to even, saturating
+// at 448.  ("DeepSeek-V4昇腾训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse
+// 极简训练优化实践", 性能结果与未来展望: FP8 training on MxFP8 compute.)
+#pragma once
+
+#include <cstdint>
+
+namespace moe {
+
+// Bytes per row of an MX scale matrix for a contraction of K elements: K / 32
+// codes, padded to a multiple of 16 bytes (TMA rows).
+__host__ __device__ inline int mx_sf_pitch(int K) { return ((K / 32) + 15) / 16 * 16; }
+
+// floor(log2(a)) of a finite fp32 a > 0 (normal or subnormal), from its bits.
+__device__ __forceinline__ int floor_log2_f32(float a) {
+    const uint32_t b = __float_as_uint(a);
+    const int e = (int)(b >> 23);
+    if (e > 0) return e - 127;
+    return (31 - __clz(b & 0x7FFFFFu)) - 149;
+}
+
+// E8M0 code of the scale of a block whose largest magnitude is amax.
+__device__ __forceinline__ uint32_t mx_scale_code(float amax) {
+    if (!(amax > 0.0f)) return 0u;
+    int se = floor_log2_f32(amax) - 8;
+    se = se < -127 ? -127 : (se > 127 ? 127 : se);
+    return (uint32_t)(se + 127);
+}
+
+// 2^p for p in [-127, 127] (2^-127 is an fp32 subnormal).
+__device__ __forceinline__ float exp2_int(int p) {
+    return p >= -126 ? __uint_as_float((uint32_t)(p + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// X = 2^(code - 127) and 1 / X.
+__device__ __forceinline__ float mx_scale(uint32_t code) { return exp2_int((int)code - 127); }
+__device__ __forceinline__ float mx_inv_scale(uint32_t code) { return exp2_int(127 - (int)code); }
+
+// E4M3 code nearest to y (ties to even), magnitude saturated at 448; the sign
+// is kept for values that round to zero.  Integer arithmetic on y's bits.
+__device__ __forceinline__ uint32_t e4m3_rne(float y) {
+    const uint32_t b = __float_as_uint(y);
+    const uint32_t sign = (b >> 24) & 0x80u;
+    const uint32_t mag = b & 0x7FFFFFFFu;
+    if (mag >= 0x44000000u) return sign | 0x7Eu;         // |y| >= 512 (or not finite)
+    const int e = (int)(mag >> 23) - 127;                  // floor(log2 |y|) for normal y
+    if (e < -10) return sign;                              // |y| < 2^-10: rounds to zero
+    const uint32_t m = (mag & 0x7FFFFFu) | 0x800000u;      // 24-bit significand
+    // units of the target spacing: 2^(e-3) for E4M3 normals, 2^-9 below 2^-6
+    const int shift = e >= -6 ? 20 : 14 - e;               // 20 .. 24
+    uint32_t q = m >> shift;
+    const uint32_t rem = m & ((1u << shift) - 1u);
+    const uint32_t half = 1u << (shift - 1);
+    q += (rem > half || (rem == half && (q & 1u))) ? 1u : 0u;
+    uint32_t code;
+    if (e >= -6) {
+        int ee = e;
+        if (q == 16u) {                                    // rounded up into the next binade
+            q = 8u;
+            ++ee;
+        }
+        code = ((uint32_t)(ee + 7) << 3) | (q - 8u);
+        if (code > 0x7Eu) code = 0x7Eu;                    // 480 and above saturate to 448
+    } else {
+        code = q;                                          // subnormal; q = 8 is 2^-6
+    }
+    return sign | code;
+}
+
+// Quantises 32 fp32 values (one block) into 8 words of E4M3 codes (element i
+// in byte i % 4 of word i / 4) and returns the block's E8M0 scale code.
+__device__ __forceinline__ uint32_t mx_quantize_block(const float (&v)[32], uint32_t (&w)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t code = mx_scale_code(amax);
+    const float inv = mx_inv_scale(code);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        w[j] = e4m3_rne(v[4 * j] * inv) | (e4m3_rne(v[4 * j + 1] * inv) << 8) |
+               (e4m3_rne(v[4 * j + 2] * inv) << 16) | (e4m3_rne(v[4 * j + 3] * inv) << 24);
+    return code;
+}
+
+// Two E4M3 codes (bits 0-7: first, 8-15: second) -> their values times the
+// scale X, packed as bf16x2 (first in the low half).  Exact: an E4M3 value
+// has 4 significant bits, and the product is a normal bf16 for block scales
+// down to 2^-117.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two, float X) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+    float lo, hi;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h2 & 0xFFFFu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h2 >> 16)));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi * X), "f"(lo * X));
+    return r;
+}
+
+}  // namespace moe

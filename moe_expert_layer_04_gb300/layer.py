@@ -28,6 +28,11 @@ def gate_route_supported(d: int, E: int, k: int) -> bool:
     return d % 64 == 0 and E % 32 == 0 and 32 <= E <= 512 and 1 <= k <= min(8, E)
 
 
+def mx_supported(d: int, I: int) -> bool:
+    """Shapes the MXFP8 expert matmuls (moe_expert_ffn_mx) take."""
+    return d % 256 == 0 and I % 128 == 0
+
+
 def ffn_fused_supported(d: int, I: int) -> bool:
     """Shapes the one-launch expert FFN (moe_expert_ffn_fused) takes: 256-wide
     tiles in both matmuls."""
@@ -61,12 +66,20 @@ class MoELayer:
     (moe_expert_ffn_fused).  Off by default: it is bit-identical to the two
     launches and measures the same on one GPU, and its waits assume that no
     other work shares the GPU's SMs.
+    mx: the low-precision variant -- the expert weights are quantised to MXFP8
+    once here (moe_mx_quantize), each step's token rows are quantised in the
+    dispatch (moe_mx_gather) and both expert matmuls take MXFP8 operands
+    (moe_expert_ffn_mx); h between them is MXFP8 too.  Forward only.
     """
 
     def __init__(self, dims: Dims, weights: dict, scaling: float, clamp: float = 7.0,
                  backward: bool = False, recompute: bool = False, device="cuda",
-                 fused_route: bool | None = None, fused_ffn: bool = False):
+                 fused_route: bool | None = None, fused_ffn: bool = False, mx: bool = False):
         self.dims = dims
+        if mx and (backward or fused_ffn or not mx_supported(dims.d, dims.I)):
+            raise ValueError(f"the MXFP8 layer is forward-only with two launches and needs "
+                             f"d % 256 == 0, I % 128 == 0 (got {dims})")
+        self.mx = bool(mx)
         ok = gate_route_supported(dims.d, dims.E, dims.k)
         if fused_route and not ok:
             raise ValueError(f"moe_gate_route does not take the shape {dims}")
@@ -94,8 +107,11 @@ class MoELayer:
         self.row_token = torch.empty(D.R, dtype=torch.int32, **e)
         self.slot_row = torch.empty(D.S, dtype=torch.int32, **e)
         self.row_weight = torch.empty(D.S, dtype=torch.float32, **e)
-        self.x_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
-        self.h_perm = torch.empty(D.R, D.I, dtype=torch.bfloat16, **e)
+        if self.mx:
+            self._init_mx(weights, e)
+        else:
+            self.x_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
+            self.h_perm = torch.empty(D.R, D.I, dtype=torch.bfloat16, **e)
         self.y_perm = torch.empty(D.R, D.d, dtype=torch.bfloat16, **e)
         # fp32 g|u, row-block interleaved in blocks of 32 rows (see moe.h)
         self.gu_save = (torch.empty((D.R + 31) // 32 * 32, 2 * D.I, dtype=torch.float32, **e)
@@ -114,6 +130,22 @@ class MoELayer:
             self.dlogits = None
             self.dweights = None
 
+    def _init_mx(self, weights, e):
+        D = self.dims
+        u8 = dict(dtype=torch.uint8, **e)
+        pd, pi = _lib.moe_mx_sf_pitch(D.d), _lib.moe_mx_sf_pitch(D.I)
+        G = D.E + 1
+        self.W13_q = torch.empty(G * 2 * D.I, D.d, **u8)
+        self.W13_sf = torch.empty(G * 2 * D.I, pd, **u8)
+        self.W2_q = torch.empty(G * D.d, D.I, **u8)
+        self.W2_sf = torch.empty(G * D.d, pi, **u8)
+        _lib.moe_mx_quantize(weights["W13"], G * 2 * D.I, D.d, self.W13_q, self.W13_sf)
+        _lib.moe_mx_quantize(weights["W2"], G * D.d, D.I, self.W2_q, self.W2_sf)
+        self.x_perm_q = torch.empty(D.R, D.d, **u8)
+        self.x_perm_sf = torch.empty(D.R, pd, **u8)
+        self.h_q = torch.empty(D.R, D.I, **u8)
+        self.h_sf = torch.empty(D.R, pi, **u8)
+
     # ------------------------------------------------------------ forward
     def route(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
               input_ids=None, tid2eid=None, stream=None):
@@ -130,12 +162,21 @@ class MoELayer:
 
     def dispatch(self, x, stream=None):
         D = self.dims
-        _lib.moe_permute(self.ids, self.weights, x, D.T, D.d, D.E, D.k, self.counts,
-                         self.offsets, self.row_token, self.slot_row, self.row_weight,
-                         self.x_perm, self.ws, stream)
+        _lib.moe_permute(self.ids, self.weights, None if self.mx else x, D.T, D.d, D.E, D.k,
+                         self.counts, self.offsets, self.row_token, self.slot_row,
+                         self.row_weight, None if self.mx else self.x_perm, self.ws, stream)
+        if self.mx:
+            _lib.moe_mx_gather(x, self.slot_row, D.T, D.d, D.k, self.x_perm_q, self.x_perm_sf,
+                               stream)
 
     def experts(self, stream=None):
         D = self.dims
+        if self.mx:
+            _lib.moe_expert_ffn_mx(self.x_perm_q, self.x_perm_sf, self.offsets, D.E + 1, D.R,
+                                   self.W13_q, self.W13_sf, self.W2_q, self.W2_sf,
+                                   self.row_weight, D.S, D.d, D.I, self.clamp, self.h_q,
+                                   self.h_sf, self.y_perm, stream)
+            return
         if self.fused_ffn:
             _lib.moe_expert_ffn_fused(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"],
                                       self.w["W2"], self.row_weight, D.S, D.d, D.I, self.clamp,

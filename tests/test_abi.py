@@ -113,6 +113,31 @@ def test_validation_rejects_before_any_launch():
     assert lib.moe_selftest_wait_timeout(1 << 40, nul) == _lib.MOE_ERR_INVALID_ARG
 
 
+def test_mx_calls_host_logic():
+    lib = _lib.load()
+    # scale rows: K/32 codes padded to 16 bytes
+    assert [lib.moe_mx_sf_pitch(K) for K in (32, 64, 512, 544, 2048, 4096)] == [16, 16, 16, 32,
+                                                                                 64, 128]
+    nul = None
+    p = ctypes.c_void_p(256)
+    q = ctypes.c_void_p(264)                       # 8-byte aligned only
+    # moe_mx_quantize: K a multiple of 32, aligned arrays; zero rows launch nothing
+    assert lib.moe_mx_quantize(p, 4, 48, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_quantize(p, 4, 64, q, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_quantize(nul, 4, 64, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_quantize(p, 0, 64, p, p, nul) == _lib.MOE_OK
+    # moe_mx_gather
+    assert lib.moe_mx_gather(p, p, 8, 48, 2, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_gather(p, nul, 8, 64, 2, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    # moe_expert_ffn_mx: 256-wide tiles in both matmuls, aligned arrays, clamp > 0
+    args = lambda d, I, clamp=7.0, hq=p: (p, p, p, 2, 64, p, p, p, p, nul, 0, d, I, clamp, hq, p,
+                                          p, nul)
+    assert lib.moe_expert_ffn_mx(*args(128, 128)) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_mx(*args(256, 64)) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_expert_ffn_mx(*args(256, 128, hq=q)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_expert_ffn_mx(*args(256, 128, clamp=0.0)) == _lib.MOE_ERR_INVALID_ARG
+
+
 def test_status_strings():
     for s in range(6):
         assert _lib.status_string(s) and _lib.status_string(s) != "unknown status"
