@@ -149,6 +149,18 @@ def fwd_algorithmic_bytes(D, counts):
     return g1, g2
 
 
+def mx_fwd_bytes(D, counts):
+    """The same minimum bytes for the MXFP8 forward: one byte per operand
+    element plus one scale byte per 32 (weights, x_perm, h); y_perm stays
+    bf16.  Returns (GEMM 1, GEMM 2, dispatch)."""
+    used = int((counts > 0).sum()) + 1
+    c = 1 + 1 / 32
+    g1 = used * 2 * D.I * D.d * c + D.R * D.d * c + D.R * D.I * c
+    g2 = used * D.d * D.I * c + D.R * D.I * c + D.R * D.d * 2
+    perm = D.T * D.d * 2 + D.R * D.d * c + D.S * 4 * 6
+    return int(g1), int(g2), int(perm)
+
+
 def fwd_flops(D):
     return 2 * D.T * D.d * D.E + 6 * D.R * D.d * D.I
 
@@ -224,17 +236,20 @@ def forward_breakdown(layer, inp, steps, warmup, mode=0, world=1):
     return per, ms / steps
 
 
-def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False, fused_route=True):
+def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False, fused_route=True, mx=False):
     """Per-call achieved GB/s (algorithmic bytes) and TFLOP/s with their
     fractions of the measured peaks.  Routing reads x and W_g and writes the
     logits (the two-kernel path reads them back once more), ids, weights and
-    selected scores."""
+    selected scores.  mx: the MXFP8 forward's bytes (its matmuls run on the
+    bf16 tensor path, so the tensor peak stays the bf16 one)."""
     g1_bytes, g2_bytes = fwd_algorithmic_bytes(D, counts)
+    perm_bytes = D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6
+    if mx:
+        g1_bytes, g2_bytes, perm_bytes = mx_fwd_bytes(D, counts)
     if save_gu:
         g1_bytes += D.R * 2 * D.I * 4
     g1_flops = 4 * D.R * D.d * D.I
     g2_flops = 2 * D.R * D.I * D.d
-    perm_bytes = D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6
     comb_bytes = D.R * D.d * 2 + D.T * D.d * 2 + D.S * 4
     route_bytes = (D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4 * (1 if fused_route else 2)
                    + D.T * D.k * 12)
@@ -367,6 +382,13 @@ def run_ours(args, rank, world, local_rank):
     extra = None
     if not args.no_extra and not args.tokens and not args.experts:
         extra = run_extra_workloads(args, weights, dev, world, hbm, bf16)
+    # ---------------- the MXFP8 forward (same weights, quantised once)
+    mx = None
+    if not args.no_mx and not args.tokens and not args.experts:
+        names = ["full_fwd"] + ([] if args.no_extra else ["long_slice_fwd_bwd"])
+        mx = run_mx(args, weights, dev, world, hbm, bf16, names)
+        if "full_fwd" in mx:
+            mx["full_fwd"]["speedup_vs_bf16"] = round(ms_step / mx["full_fwd"]["ms_per_step"], 3)
     clk = clocks.stop()
 
     cpu = None
@@ -396,11 +418,65 @@ def run_ours(args, rank, world, local_rank):
         "fwd_bwd": fb,
         "extra_workloads": extra,
         "literal_bias": literal,
+        "mx_fwd": mx,
         "expert_ffn_launches": ffn_launch,
         "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
                         "min_rows": int(counts.min()), "max_rows": int(counts.max())},
     }
     return line
+
+
+def run_mx(args, weights, dev, world, hbm, bf16, names):
+    """The MXFP8 forward (weights quantised once, token rows quantised in the
+    dispatch, both expert matmuls on MXFP8 operands) on the named workloads,
+    with the same per-call breakdown as the bf16 forward."""
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+    out = {}
+    for name in names:
+        wl = W.WORKLOADS[name]
+        D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+        inp = layer_inputs(wl, dev, weights=weights)
+        layer = MoELayer(D, weights, wl.rho, wl.clamp, mx=True)
+        steps = args.steps if name == "full_fwd" else max(3, args.steps // 3)
+        forward_breakdown(layer, inp, 1, args.warmup, world=world)
+        counts = layer.counts.cpu().numpy()
+        per, ms = forward_breakdown(layer, inp, steps, 1, world=world)
+        assert _lib.moe_last_device_status() == _lib.MOE_OK
+        kern, _, roof = kernel_metrics(D, counts, per, hbm, bf16,
+                                       fused_route=layer.fused_route, mx=True)
+        out[name] = {"workload": f"{name}: forward, MXFP8 expert matmuls, T={wl.T}",
+                     "value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
+                     "ms_per_step": round(ms, 4), "layer_roofline_ms": round(roof, 4),
+                     "layer_roofline_frac": round(roof / ms, 4), "kernels": kern,
+                     "steps": steps, "dtype": "mxfp8 operands (e4m3 + e8m0 per 32), fp32 accumulate"}
+        del layer, inp
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_mx_only(args):
+    """Only the MXFP8 forward of the workload (profiling captures)."""
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    hbm, bf16, _, _ = peaks()
+    wl = workload(args)
+    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+    inp = layer_inputs(wl, dev)
+    layer = MoELayer(D, {k: inp[k] for k in ("W_g", "W13", "W2")}, wl.rho, wl.clamp, mx=True)
+    forward_breakdown(layer, inp, 1, args.warmup)
+    counts = layer.counts.cpu().numpy()
+    per, ms = forward_breakdown(layer, inp, args.steps, 1)
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    kern, _, roof = kernel_metrics(D, counts, per, hbm, bf16, fused_route=layer.fused_route,
+                                   mx=True)
+    return {"workload": f"{wl.name}: forward, MXFP8 expert matmuls", "ms_per_step": round(ms, 4),
+            "value": round(D.T / ms * 1e3, 1), "unit": "tokens/s",
+            "layer_roofline_frac": round(roof / ms, 4), "kernels": kern}
 
 
 def run_extra_workloads(args, weights, dev, world, hbm, bf16):
@@ -644,6 +720,9 @@ def main():
                     help="time only the routing step of the workload (profiling)")
     ap.add_argument("--fwd-bwd-only", action="store_true",
                     help="time only forward + backward of the workload (profiling)")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward")
+    ap.add_argument("--mx-only", action="store_true",
+                    help="time only the MXFP8 forward of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -656,6 +735,9 @@ def main():
         return
     if args.fwd_bwd_only:
         print(json.dumps(run_fwd_bwd_only(args)), flush=True)
+        return
+    if args.mx_only:
+        print(json.dumps(run_mx_only(args)), flush=True)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)

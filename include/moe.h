@@ -346,6 +346,17 @@ moe_status moe_expert_ffn_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
                              const float *row_weight, int S, int d, int I, float clamp,
                              uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm, void *stream);
 
+/* The two matmuls of moe_expert_ffn_mx as separate calls (same arguments
+ * and checks; GEMM 1 writes h_q / h_sf, GEMM 2 reads them). */
+moe_status moe_expert_gemm1_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
+                               const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
+                               const uint8_t *W13_sf, int d, int I, float clamp, uint8_t *h_q,
+                               uint8_t *h_sf, void *stream);
+moe_status moe_expert_gemm2_mx(const uint8_t *h_q, const uint8_t *h_sf, const int32_t *offsets,
+                               int G, int max_rows, const uint8_t *W2_q, const uint8_t *W2_sf,
+                               const float *row_weight, int S, int d, int I, uint16_t *y_perm,
+                               void *stream);
+
 /* Text of a status code (static storage). */
 const char *moe_status_string(moe_status s);
 

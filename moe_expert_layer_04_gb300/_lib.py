@@ -33,7 +33,8 @@ EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_rout
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout",
-           "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx"]
+           "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
+           "moe_expert_gemm1_mx", "moe_expert_gemm2_mx"]
 
 
 class MoeError(RuntimeError):
@@ -128,6 +129,8 @@ _SIGS = {
     "moe_mx_gather": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
     "moe_expert_ffn_mx": ([_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P,
                            _P], _I),
+    "moe_expert_gemm1_mx": ([_P, _P, _P, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P], _I),
+    "moe_expert_gemm2_mx": ([_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P], _I),
 }
 
 _lock = threading.Lock()
@@ -303,6 +306,27 @@ def moe_expert_ffn_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, 
                                   _ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"),
                                   _ptr(y_perm, BF16, "y_perm"), _stream(stream))
     _check("moe_expert_ffn_mx", st)
+
+
+def moe_expert_gemm1_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp,
+                        h_q, h_sf, stream=None):
+    st = load().moe_expert_gemm1_mx(_ptr(x_perm_q, U8, "x_perm_q"),
+                                    _ptr(x_perm_sf, U8, "x_perm_sf"),
+                                    _ptr(offsets, I32, "offsets"), G, max_rows,
+                                    _ptr(W13_q, U8, "W13_q"), _ptr(W13_sf, U8, "W13_sf"), d, I,
+                                    float(clamp), _ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"),
+                                    _stream(stream))
+    _check("moe_expert_gemm1_mx", st)
+
+
+def moe_expert_gemm2_mx(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight, S, d, I,
+                        y_perm, stream=None):
+    st = load().moe_expert_gemm2_mx(_ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"),
+                                    _ptr(offsets, I32, "offsets"), G, max_rows,
+                                    _ptr(W2_q, U8, "W2_q"), _ptr(W2_sf, U8, "W2_sf"),
+                                    _ptr(row_weight, F32, "row_weight"), S, d, I,
+                                    _ptr(y_perm, BF16, "y_perm"), _stream(stream))
+    _check("moe_expert_gemm2_mx", st)
 
 
 def moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm,

@@ -2,6 +2,7 @@
 // validation, workspace carving, the device status word, tensor-map
 // encoding, and the order of kernel launches of each entry point.
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "moe_ptx.cuh"
@@ -182,10 +183,12 @@ bool encode_tmap_f32_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint6
 
 bool encode_tmap_u8_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
                        uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,
-                       bool swizzle64) {
+                       int swizzle_bytes) {
+    const CUtensorMapSwizzle swz = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
     return encode_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, outer, row_pitch_bytes,
-                     box_inner, box_outer,
-                     swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
+                     box_inner, box_outer, swz);
 }
 
 moe_status check_shapes(int T, int d, int E, int k, int I) {
@@ -364,24 +367,53 @@ moe_status moe_mx_gather(const uint16_t *x, const int32_t *slot_row, int T, int 
                             static_cast<cudaStream_t>(stream));
 }
 
+static moe_status check_ffn_mx(int G, int max_rows, int d, int I, int S, float clamp,
+                               std::initializer_list<const void *> ptrs, const int32_t *offsets) {
+    moe_status s = check_ffn(G, max_rows, d, I, S);
+    if (s != MOE_OK) return s;
+    if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    for (const void *ptr : ptrs)
+        if (!ptr || !aligned16(ptr)) return MOE_ERR_INVALID_ARG;
+    if (!offsets || !(clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_expert_gemm1_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
+                               const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
+                               const uint8_t *W13_sf, int d, int I, float clamp, uint8_t *h_q,
+                               uint8_t *h_sf, void *stream) {
+    moe_status s = check_ffn_mx(G, max_rows, d, I, 0, clamp,
+                                {x_perm_q, x_perm_sf, W13_q, W13_sf, h_q, h_sf}, offsets);
+    if (s != MOE_OK) return s;
+    return launch_mx_ffn1(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp,
+                          h_q, h_sf, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_gemm2_mx(const uint8_t *h_q, const uint8_t *h_sf, const int32_t *offsets,
+                               int G, int max_rows, const uint8_t *W2_q, const uint8_t *W2_sf,
+                               const float *row_weight, int S, int d, int I, uint16_t *y_perm,
+                               void *stream) {
+    moe_status s = check_ffn_mx(G, max_rows, d, I, S, 1.0f, {h_q, h_sf, W2_q, W2_sf, y_perm},
+                                offsets);
+    if (s != MOE_OK) return s;
+    return launch_mx_ffn2(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight, S, d, I, y_perm,
+                          static_cast<cudaStream_t>(stream));
+}
+
 moe_status moe_expert_ffn_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
                              const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
                              const uint8_t *W13_sf, const uint8_t *W2_q, const uint8_t *W2_sf,
                              const float *row_weight, int S, int d, int I, float clamp,
                              uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm, void *stream) {
-    moe_status s = check_ffn(G, max_rows, d, I, S);
+    moe_status s = check_ffn_mx(G, max_rows, d, I, S, clamp,
+                                {x_perm_q, x_perm_sf, W13_q, W13_sf, W2_q, W2_sf, h_q, h_sf,
+                                 y_perm}, offsets);
     if (s != MOE_OK) return s;
-    if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
-    const void *ptrs[] = {x_perm_q, x_perm_sf, W13_q, W13_sf, W2_q, W2_sf, h_q, h_sf, y_perm};
-    for (const void *ptr : ptrs)
-        if (!ptr || !aligned16(ptr)) return MOE_ERR_INVALID_ARG;
-    if (!offsets || !(clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = launch_mx_ffn1(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp, h_q,
-                       h_sf, st);
+    s = moe_expert_gemm1_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp,
+                            h_q, h_sf, stream);
     if (s != MOE_OK) return s;
-    return launch_mx_ffn2(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight, S, d, I,
-                          y_perm, st);
+    return moe_expert_gemm2_mx(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight, S, d, I,
+                               y_perm, stream);
 }
 
 moe_status moe_expert_gemm1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,

@@ -16,7 +16,7 @@
 // one scale byte per 32, half the bytes of bf16, which is what bounds these
 // GEMMs at tens of rows per expert.
 //
-// One CTA per SM, 10 warps:
+// One CTA per SM, 18 warps:
 //   warp 0      TMA producer: code tiles (A 128 x 64, B 256 x 64 bytes, 64-byte
 //               swizzle) into a 4-stage ring; every 8 k-steps the scale codes
 //               of the tile's rows for those 8 steps (16 bytes a row) into a
@@ -26,9 +26,10 @@
 //   warps 2-5   epilogue, thread = row: GEMM 1 the clamped SwiGLU and h
 //               quantised to MXFP8 per 32 columns; GEMM 2 the routing-weight
 //               scale to bf16.
-//   warps 6-9   converters: thread c expands A row c and B rows c and c + 128
-//               of a code stage into a 128-byte-swizzled bf16 stage (2
-//               stages), then releases both.
+//   warps 6-17  converters, three per scheduler: thread c expands row c of a
+//               code stage (rows 0-127 A, 128-383 B) into a 128-byte-swizzled
+//               bf16 stage (2 stages), then releases both.  Fewer warps leave
+//               the schedulers idle on the conversion's dependency chains.
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and exits.
 #include <cstring>
@@ -60,6 +61,7 @@ struct MxParams {
     uint16_t *y;           // GEMM 2: [rows, d] bf16
     const float *row_w;    // GEMM 2: weight of rows < w_rows (others 1)
     int w_rows;
+    uint32_t k16;          // 16 (see e4m3x4_to_bf16x2x2)
     int *status;
     long long wait_limit;
 };
@@ -68,7 +70,7 @@ constexpr int kMxRaw = 4;           // code stages
 constexpr int kMxBf = 2;            // bf16 operand stages
 constexpr int kMxSfSlots = 2;       // scale slots (8 k-steps each)
 constexpr int kMxEpiWarps = 4;
-constexpr int kMxConvWarps = 4;
+constexpr int kMxConvWarps = 12;    // one A or B row per thread
 constexpr int kMxThreads = 64 + 32 * (kMxEpiWarps + kMxConvWarps);
 constexpr int kMxRawA = 128 * 64;
 constexpr int kMxRawStage = kMxRawA + 256 * 64;
@@ -107,26 +109,24 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
 // (128 bytes, 128-byte swizzle); elements 0-31 scaled by 2^(sf[0] - 127),
 // 32-63 by 2^(sf[1] - 127).
 __device__ __forceinline__ void mx_expand_row(const uint8_t *codes, const uint8_t *sf,
-                                              uint8_t *dst, int r) {
-    const float X0 = mx_scale(sf[0]);
-    const float X1 = mx_scale(sf[1]);
+                                              uint8_t *dst, int r, uint32_t k16) {
+    const MxBf16Factors f0 = mx_bf16_factors(sf[0]);
+    const MxBf16Factors f1 = mx_bf16_factors(sf[1]);
     const uint32_t sw_in = (uint32_t)(r >> 1) & 3u;
-    const uint32_t sw_out = (uint32_t)r & 7u;
+    const uint32_t sw = (uint32_t)r & 7u;
     const uint8_t *src = codes + r * 64;
     const uint32_t out = smem_u32(dst + r * 128);
 #pragma unroll
     for (uint32_t c = 0; c < 4; ++c) {
         const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ sw_in) << 4));
-        const float X = c < 2 ? X0 : X1;
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const MxBf16Factors &f = c < 2 ? f0 : f1;
         uint32_t o[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2_scaled(w[e] & 0xFFFFu, X);
-            o[2 * e + 1] = e4m3x2_to_bf16x2_scaled(w[e] >> 16, X);
-        }
-        st_shared_v4(out + (((2 * c) ^ sw_out) << 4), o[0], o[1], o[2], o[3]);
-        st_shared_v4(out + (((2 * c + 1) ^ sw_out) << 4), o[4], o[5], o[6], o[7]);
+        e4m3x4_to_bf16x2x2(v.x, f, k16, o[0], o[1]);
+        e4m3x4_to_bf16x2x2(v.y, f, k16, o[2], o[3]);
+        e4m3x4_to_bf16x2x2(v.z, f, k16, o[4], o[5]);
+        e4m3x4_to_bf16x2x2(v.w, f, k16, o[6], o[7]);
+        st_shared_v4(out + (((2 * c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+        st_shared_v4(out + (((2 * c + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -305,7 +305,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
         }
     } else if (warp >= 2 + kMxEpiWarps) {
         // ------------------------------------------------ converters
-        const int ct = (warp - 2 - kMxEpiWarps) * 32 + lane;   // 0..127
+        // rows 0..127: A, 128..383: B; warps hold one kind of row each
+        const int ct = (warp - 2 - kMxEpiWarps) * 32 + lane;   // 0..383
+        const bool is_a = ct < 128;
+        const int r = is_a ? ct : ct - 128;
         uint32_t s = 0, ph = 0, sb = 0, phb = 0, js = 0, phs = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
@@ -317,9 +320,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                 const uint8_t *raw = sRaw + s * kMxRawStage;
                 const uint8_t *sf = sSf + js * kMxSfSlot + (kb & 7) * 2;
                 uint8_t *bf = sBf + sb * kMxBfStage;
-                mx_expand_row(raw, sf + ct * 16, bf, ct);
-                mx_expand_row(raw + kMxRawA, sf + kMxSfA + ct * 16, bf + kMxBfA, ct);
-                mx_expand_row(raw + kMxRawA, sf + kMxSfA + (ct + 128) * 16, bf + kMxBfA, ct + 128);
+                if (is_a) mx_expand_row(raw, sf + r * 16, bf, r, p.k16);
+                else mx_expand_row(raw + kMxRawA, sf + kMxSfA + r * 16, bf + kMxBfA, r, p.k16);
                 // the tensor cores read the stage through the async proxy
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -404,6 +406,7 @@ moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
     p.status = device_status_ptr();
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
+    p.k16 = 16u;
     const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
     kern<<<grid, kMxThreads, mx_smem_bytes(p.G), st>>>(p);
     return cuda_status(cudaGetLastError());
@@ -419,10 +422,10 @@ moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *
     std::memset(&p, 0, sizeof p);
     const int sfd = mx_sf_pitch(d);
     const uint64_t brows = (uint64_t)G * 2 * I;
-    if (!encode_tmap_u8_2d(&p.tmA, xq, d, max_rows, d, 64, 128, true) ||
-        !encode_tmap_u8_2d(&p.tmB, W13q, d, brows, d, 64, 128, true) ||
-        !encode_tmap_u8_2d(&p.tmSA, xsf, sfd, max_rows, sfd, 16, 128, false) ||
-        !encode_tmap_u8_2d(&p.tmSB, W13sf, sfd, brows, sfd, 16, 128, false))
+    if (!encode_tmap_u8_2d(&p.tmA, xq, d, max_rows, d, 64, 128, 64) ||
+        !encode_tmap_u8_2d(&p.tmB, W13q, d, brows, d, 64, 128, 64) ||
+        !encode_tmap_u8_2d(&p.tmSA, xsf, sfd, max_rows, sfd, 16, 128, 0) ||
+        !encode_tmap_u8_2d(&p.tmSB, W13sf, sfd, brows, sfd, 16, 128, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
@@ -445,10 +448,10 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
     std::memset(&p, 0, sizeof p);
     const int sfi = mx_sf_pitch(I);
     const uint64_t brows = (uint64_t)G * d;
-    if (!encode_tmap_u8_2d(&p.tmA, hq, I, max_rows, I, 64, 128, true) ||
-        !encode_tmap_u8_2d(&p.tmB, W2q, I, brows, I, 64, 128, true) ||
-        !encode_tmap_u8_2d(&p.tmSA, hsf, sfi, max_rows, sfi, 16, 128, false) ||
-        !encode_tmap_u8_2d(&p.tmSB, W2sf, sfi, brows, sfi, 16, 128, false))
+    if (!encode_tmap_u8_2d(&p.tmA, hq, I, max_rows, I, 64, 128, 64) ||
+        !encode_tmap_u8_2d(&p.tmB, W2q, I, brows, I, 64, 128, 64) ||
+        !encode_tmap_u8_2d(&p.tmSA, hsf, sfi, max_rows, sfi, 16, 128, 0) ||
+        !encode_tmap_u8_2d(&p.tmSB, W2sf, sfi, brows, sfi, 16, 128, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;

@@ -34,10 +34,11 @@ bool encode_tmap_bf16_2d_sw64(CUtensorMap *tm, const void *base, uint64_t inner,
 bool encode_tmap_f32_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
                         uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer);
 
-// 2-D byte matrix (MXFP8 codes or scale codes), 64-byte swizzle or none.
+// 2-D byte matrix (MXFP8 codes or scale codes); swizzle_bytes 128, 64 or 0
+// (none).
 bool encode_tmap_u8_2d(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
                        uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,
-                       bool swizzle64);
+                       int swizzle_bytes);
 
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 

@@ -90,19 +90,57 @@ __device__ __forceinline__ uint32_t mx_quantize_block(const float (&v)[32], uint
     return code;
 }
 
-// Two E4M3 codes (bits 0-7: first, 8-15: second) -> their values times the
-// scale X, packed as bf16x2 (first in the low half).  Exact: an E4M3 value
-// has 4 significant bits, and the product is a normal bf16 for block scales
-// down to 2^-117.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two, float X) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
-    float lo, hi;
-    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h2 & 0xFFFFu)));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h2 >> 16)));
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi * X), "f"(lo * X));
-    return r;
+// E4M3 -> bf16 without conversion instructions.  Placing a code's bits 6..0
+// at bf16 bits 10..4 and its sign at bit 15 gives a bf16 whose value is the
+// code's value times 2^-120, for normal codes ((1 + m/8) 2^(E-7) against
+// (1 + m/8) 2^(E-127)) and subnormal ones (m/8 2^-6 against the bf16
+// subnormal m/8 2^-126) alike; one bf16x2 multiply by 2^(120 + se) then gives
+// the code's value times the block scale 2^se, exactly while the product is a
+// normal bf16 (block scales down to 2^-117).
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The factors for a block with scale code c (se = c - 127): f1 = 2^(120 + se)
+// as bf16x2, and f2 = 1 unless 120 + se passes bf16's largest exponent 127,
+// where f1 = 2^127 and f2 = 2^(se - 7).
+struct MxBf16Factors {
+    uint32_t f1, f2;
+    bool two;
+};
+
+__device__ __forceinline__ MxBf16Factors mx_bf16_factors(uint32_t code) {
+    MxBf16Factors f;
+    f.two = code > 134u;
+    const uint32_t e1 = f.two ? 254u : code + 120u;   // biased bf16 exponent of f1
+    const uint32_t e2 = f.two ? code - 7u : 127u;
+    f.f1 = (e1 << 7) | (e1 << 23);
+    f.f2 = (e2 << 7) | (e2 << 23);
+    return f;
+}
+
+// Four E4M3 codes (byte i of w = element i) -> two bf16x2 words (elements 0,1
+// in lo, 2,3 in hi, first element in the low half) times the block scale.
+// k16 is 16, passed at run time so that the magnitude shift and the join with
+// the sign bits stay one integer multiply-add (FMA pipe; the byte permutes
+// and masks already fill the ALU pipe).
+__device__ __forceinline__ void e4m3x4_to_bf16x2x2(uint32_t w, const MxBf16Factors &f,
+                                                   uint32_t k16, uint32_t &lo, uint32_t &hi) {
+    const uint32_t mag = w & 0x7F7F7F7Fu;
+    const uint32_t sgn = w ^ mag;
+    const uint32_t t0 = __byte_perm(mag, 0u, 0x4140);   // bytes: mag 0, 0, mag 1, 0
+    const uint32_t t1 = __byte_perm(mag, 0u, 0x4342);   // bytes: mag 2, 0, mag 3, 0
+    const uint32_t s0 = __byte_perm(sgn, 0u, 0x1404);   // sign 0 -> bit 15, sign 1 -> bit 31
+    const uint32_t s1 = __byte_perm(sgn, 0u, 0x3424);
+    lo = mul_bf16x2(t0 * k16 + s0, f.f1);                // disjoint bits: the add is an OR
+    hi = mul_bf16x2(t1 * k16 + s1, f.f1);
+    if (f.two) {
+        lo = mul_bf16x2(lo, f.f2);
+        hi = mul_bf16x2(hi, f.f2);
+    }
 }
 
 }  // namespace moe

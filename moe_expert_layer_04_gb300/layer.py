@@ -188,11 +188,21 @@ class MoELayer:
 
     def expert_gemm1(self, stream=None):
         D = self.dims
+        if self.mx:
+            _lib.moe_expert_gemm1_mx(self.x_perm_q, self.x_perm_sf, self.offsets, D.E + 1, D.R,
+                                     self.W13_q, self.W13_sf, D.d, D.I, self.clamp, self.h_q,
+                                     self.h_sf, stream)
+            return
         _lib.moe_expert_gemm1(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"], D.d, D.I,
                               self.clamp, self.gu_save, self.h_perm, stream)
 
     def expert_gemm2(self, stream=None):
         D = self.dims
+        if self.mx:
+            _lib.moe_expert_gemm2_mx(self.h_q, self.h_sf, self.offsets, D.E + 1, D.R, self.W2_q,
+                                     self.W2_sf, self.row_weight, D.S, D.d, D.I, self.y_perm,
+                                     stream)
+            return
         _lib.moe_expert_gemm2(self.h_perm, self.offsets, D.E + 1, D.R, self.w["W2"],
                               self.row_weight, D.S, D.d, D.I, self.y_perm, stream)
 
