@@ -108,10 +108,10 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
 // Row r of a code tile (64 bytes, 64-byte swizzle) -> row r of a bf16 tile
 // (128 bytes, 128-byte swizzle); elements 0-31 scaled by 2^(sf[0] - 127),
 // 32-63 by 2^(sf[1] - 127).
-__device__ __forceinline__ void mx_expand_row(const uint8_t *codes, const uint8_t *sf,
-                                              uint8_t *dst, int r, uint32_t k16) {
-    const MxBf16Factors f0 = mx_bf16_factors(sf[0]);
-    const MxBf16Factors f1 = mx_bf16_factors(sf[1]);
+template <bool TWO>
+__device__ __forceinline__ void mx_expand_row_t(const uint8_t *codes, const MxBf16Factors &f0,
+                                                const MxBf16Factors &f1, uint8_t *dst, int r,
+                                                uint32_t k16) {
     const uint32_t sw_in = (uint32_t)(r >> 1) & 3u;
     const uint32_t sw = (uint32_t)r & 7u;
     const uint8_t *src = codes + r * 64;
@@ -121,13 +121,23 @@ __device__ __forceinline__ void mx_expand_row(const uint8_t *codes, const uint8_
         const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ sw_in) << 4));
         const MxBf16Factors &f = c < 2 ? f0 : f1;
         uint32_t o[8];
-        e4m3x4_to_bf16x2x2(v.x, f, k16, o[0], o[1]);
-        e4m3x4_to_bf16x2x2(v.y, f, k16, o[2], o[3]);
-        e4m3x4_to_bf16x2x2(v.z, f, k16, o[4], o[5]);
-        e4m3x4_to_bf16x2x2(v.w, f, k16, o[6], o[7]);
+        e4m3x4_to_bf16x2x2<TWO>(v.x, f, k16, o[0], o[1]);
+        e4m3x4_to_bf16x2x2<TWO>(v.y, f, k16, o[2], o[3]);
+        e4m3x4_to_bf16x2x2<TWO>(v.z, f, k16, o[4], o[5]);
+        e4m3x4_to_bf16x2x2<TWO>(v.w, f, k16, o[6], o[7]);
         st_shared_v4(out + (((2 * c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
         st_shared_v4(out + (((2 * c + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
     }
+}
+
+// One decision per row and k-step: the second multiply only where a block's
+// scale exceeds 2^7 (rare), so the common path carries no per-word test.
+__device__ __forceinline__ void mx_expand_row(const uint8_t *codes, const uint8_t *sf,
+                                              uint8_t *dst, int r, uint32_t k16) {
+    const MxBf16Factors f0 = mx_bf16_factors(sf[0]);
+    const MxBf16Factors f1 = mx_bf16_factors(sf[1]);
+    if (f0.two || f1.two) mx_expand_row_t<true>(codes, f0, f1, dst, r, k16);
+    else mx_expand_row_t<false>(codes, f0, f1, dst, r, k16);
 }
 
 template <int MODE>

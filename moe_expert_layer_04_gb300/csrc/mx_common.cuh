@@ -123,10 +123,12 @@ __device__ __forceinline__ MxBf16Factors mx_bf16_factors(uint32_t code) {
 }
 
 // Four E4M3 codes (byte i of w = element i) -> two bf16x2 words (elements 0,1
-// in lo, 2,3 in hi, first element in the low half) times the block scale.
+// in lo, 2,3 in hi, first element in the low half) times the block scale;
+// TWO applies f2 as well (needed only when the scale exceeds 2^7).
 // k16 is 16, passed at run time so that the magnitude shift and the join with
 // the sign bits stay one integer multiply-add (FMA pipe; the byte permutes
 // and masks already fill the ALU pipe).
+template <bool TWO>
 __device__ __forceinline__ void e4m3x4_to_bf16x2x2(uint32_t w, const MxBf16Factors &f,
                                                    uint32_t k16, uint32_t &lo, uint32_t &hi) {
     const uint32_t mag = w & 0x7F7F7F7Fu;
@@ -137,7 +139,7 @@ __device__ __forceinline__ void e4m3x4_to_bf16x2x2(uint32_t w, const MxBf16Facto
     const uint32_t s1 = __byte_perm(sgn, 0u, 0x3424);
     lo = mul_bf16x2(t0 * k16 + s0, f.f1);                // disjoint bits: the add is an OR
     hi = mul_bf16x2(t1 * k16 + s1, f.f1);
-    if (f.two) {
+    if constexpr (TWO) {   // f2 == 1 unless the block's scale exceeds 2^7
         lo = mul_bf16x2(lo, f.f2);
         hi = mul_bf16x2(hi, f.f2);
     }

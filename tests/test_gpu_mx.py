@@ -20,7 +20,7 @@ import oracle
 from moe_expert_layer_04_gb300 import _lib
 from moe_expert_layer_04_gb300 import workloads as W
 from moe_expert_layer_04_gb300.layer import Dims, MoELayer
-from tests.helpers import assert_close, cpu, np64
+from tests.helpers import MAX_ABS, assert_close, cpu, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -76,11 +76,16 @@ def test_mx_quantize_bit_exact(rows, K):
     assert np.all(sf[:, K // 32:] == PAD)
 
 
-def _mx_layer(name, T, d, E, k, I, n_empty=0):
+def _mx_layer(name, T, d, E, k, I, n_empty=0, big=False):
     w = W.Workload(name, T, d, E, k, I, 2.5, vision_frac=0.3)
     inp = W.make_inputs(w, device="cuda")
     if n_empty:
         inp["bias"][:, :n_empty] = -10.0   # these experts get no slot
+    if big:
+        # block scales above 2^7 (the expansion's second multiply): x and one
+        # expert's W13 rows times 2^16; the clamp keeps h, and so y, bounded
+        inp["x"] *= 2.0 ** 16
+        inp["W13"][1] *= 2.0 ** 16
     weights = dict(W_g=inp["W_g"], W13=inp["W13"], W2=inp["W2"])
     layer = MoELayer(Dims(T, d, E, k, I), weights, w.rho, w.clamp, mx=True)
     layer.h_sf.fill_(PAD)
@@ -96,8 +101,11 @@ def _row_groups(layer, rows):
     return (np.searchsorted(offs, rows, side="right") - 1).astype(np.int32)
 
 
-def _check_rows(w, inp, layer, rows):
-    """y_perm and the MX h of the given rows against the oracle's MX FFN."""
+def _check_rows(w, inp, layer, rows, scale_abs=False):
+    """y_perm and the MX h of the given rows against the oracle's MX FFN.
+    scale_abs: the max-abs bound is relative to the largest |value| (outputs
+    far from unit magnitude, where one h code step moves y by more than the
+    absolute bound)."""
     rt = cpu(layer.row_token).numpy()[rows].astype(np.int64)
     grp = _row_groups(layer, rows)
     rw = np.ones(len(rows))
@@ -109,12 +117,14 @@ def _check_rows(w, inp, layer, rows):
     h_ref, y_ref = oracle.expert_rows_mx(cpu(inp["x"]), cpu(inp["W13"][sel]), cpu(inp["W2"][sel]),
                                          rt, inv.astype(np.int32), rw, w.clamp)
     ridx = torch.from_numpy(rows).cuda()
-    assert_close(layer.y_perm[ridx], y_ref, f"{w.name} MX y_perm rows")
+    ay = MAX_ABS * max(1.0, float(np.abs(y_ref).max())) if scale_abs else MAX_ABS
+    assert_close(layer.y_perm[ridx], y_ref, f"{w.name} MX y_perm rows", max_abs=ay)
     hq = cpu(layer.h_q[ridx]).numpy()
     hsf = cpu(layer.h_sf[ridx]).numpy()
     assert np.all(hsf[:, w.I // 32:] == PAD)
     h_gpu = oracle.mx_dequantize(hq, hsf[:, : w.I // 32])
-    assert_close(h_gpu, h_ref, f"{w.name} MX h rows")
+    ah = MAX_ABS * max(1.0, float(np.abs(h_ref).max())) if scale_abs else MAX_ABS
+    assert_close(h_gpu, h_ref, f"{w.name} MX h rows", max_abs=ah)
     # codes: the oracle's MX h re-encoded from its values
     q_ref, sf_ref = oracle.mx_quantize(h_ref)
     assert np.array_equal(oracle.mx_dequantize(q_ref, sf_ref), h_ref)
@@ -123,19 +133,23 @@ def _check_rows(w, inp, layer, rows):
     return rt
 
 
-# name, T, d, E, k, I, experts forced empty, rows checked (None: all)
+# name, T, d, E, k, I, experts forced empty, rows checked (None: all), large scales
 CASES = [
-    ("ragged", 300, 256, 6, 2, 128, 0, None),
-    ("two_scale_chunks", 700, 1024, 5, 2, 256, 0, None),
-    ("empty_experts", 500, 512, 16, 4, 128, 5, None),
-    ("many_row_tiles", 12000, 256, 4, 2, 128, 0, 384),
+    ("ragged", 300, 256, 6, 2, 128, 0, None, False),
+    ("two_scale_chunks", 700, 1024, 5, 2, 256, 0, None, False),
+    ("empty_experts", 500, 512, 16, 4, 128, 5, None, False),
+    ("many_row_tiles", 12000, 256, 4, 2, 128, 0, 384, False),
+    ("scales_above_2e7", 400, 256, 4, 2, 128, 0, None, True),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_mx_ffn_parity(case):
-    name, T, d, E, k, I, n_empty, n_rows = case
-    w, inp, layer = _mx_layer(name, T, d, E, k, I, n_empty)
+    name, T, d, E, k, I, n_empty, n_rows, big = case
+    w, inp, layer = _mx_layer(name, T, d, E, k, I, n_empty, big)
+    if big:
+        sf = cpu(layer.x_perm_sf).numpy()[:, : d // 32]
+        assert (sf.astype(int) - 127 > 7).all()            # every x block takes the second multiply
     if n_empty:
         assert int(cpu(layer.counts)[:n_empty].sum()) == 0
     R = w.S + w.T
@@ -152,13 +166,17 @@ def test_mx_ffn_parity(case):
     assert np.array_equal(cpu(layer.W13_sf).numpy()[:, : d // 32], sf13)
     rows = (np.arange(R) if n_rows is None else
             np.sort(np.random.default_rng(11).choice(R, size=n_rows, replace=False)))
-    _check_rows(w, inp, layer, rows.astype(np.int64))
+    # with x and W13 times 2^16, g is a sum of ~1e3-sized terms whose fp32
+    # rounding (~1e-2) can move an unclamped h across an E4M3 boundary; one h
+    # code step then moves y by ~0.2 on outputs of magnitude ~10
+    _check_rows(w, inp, layer, rows.astype(np.int64), scale_abs=big)
     # the combine of the MX rows: y of sampled tokens
     toks = np.sort(np.random.default_rng(12).choice(T, size=min(T, 48), replace=False))
     slot_row = cpu(layer.slot_row).numpy().reshape(T, k)
     yp = np64(layer.y_perm)
     y_ref = yp[w.S + toks] + yp[slot_row[toks]].sum(axis=1)
-    assert_close(layer.y[torch.from_numpy(toks).cuda()], y_ref, f"{name} MX y")
+    ay = MAX_ABS * max(1.0, float(np.abs(y_ref).max())) if big else MAX_ABS
+    assert_close(layer.y[torch.from_numpy(toks).cuda()], y_ref, f"{name} MX y", max_abs=ay)
 
 
 @pytest.mark.slow
