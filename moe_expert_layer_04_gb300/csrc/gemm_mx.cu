@@ -330,8 +330,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                 const uint8_t *raw = sRaw + s * kMxRawStage;
                 const uint8_t *sf = sSf + js * kMxSfSlot + (kb & 7) * 2;
                 uint8_t *bf = sBf + sb * kMxBfStage;
-                if (is_a) mx_expand_row(raw, sf + r * 16, bf, r, p.k16);
-                else mx_expand_row(raw + kMxRawA, sf + kMxSfA + r * 16, bf + kMxBfA, r, p.k16);
+                // A rows past the group's end feed only accumulator rows that are
+                // never stored (MMA rows are independent), so they are not expanded
+                if (!is_a) mx_expand_row(raw + kMxRawA, sf + kMxSfA + r * 16, bf + kMxBfA, r, p.k16);
+                else if (r < ti.rows_valid) mx_expand_row(raw, sf + r * 16, bf, r, p.k16);
                 // the tensor cores read the stage through the async proxy
                 fence_proxy_async_smem();
                 __syncwarp();
