@@ -13,8 +13,10 @@
 // both MX operands to bf16 in shared memory and running the bf16
 // tcgen05.mma gives the sums of a block-scaled MXFP8 MMA up to the order of
 // the fp32 additions.  The operands cross HBM at one byte per element plus
-// one scale byte per 32, half the bytes of bf16, which is what bounds these
-// GEMMs at tens of rows per expert.
+// one scale byte per 32, half the bytes of bf16; what bounds these GEMMs is
+// the expansion itself (its instructions and its shared-memory traffic: per
+// k-step 24 KB of codes read back and 48 KB of bf16 written, beside the
+// tensor cores' 48 KB of operand reads).
 //
 // One CTA per SM, 18 warps:
 //   warp 0      TMA producer: code tiles (A 128 x 64, B 256 x 64 bytes, 64-byte
