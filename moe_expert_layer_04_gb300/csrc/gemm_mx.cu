@@ -63,7 +63,6 @@ struct MxParams {
     uint16_t *y;           // GEMM 2: [rows, d] bf16
     const float *row_w;    // GEMM 2: weight of rows < w_rows (others 1)
     int w_rows;
-    uint32_t k16;          // 16 (see e4m3x4_to_bf16x2x2)
     int *status;
     long long wait_limit;
 };
@@ -108,12 +107,12 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
 }
 
 // Row r of a code tile (64 bytes, 64-byte swizzle) -> row r of a bf16 tile
-// (128 bytes, 128-byte swizzle); elements 0-31 scaled by 2^(sf[0] - 127),
-// 32-63 by 2^(sf[1] - 127).
+// (128 bytes, 128-byte swizzle; inside each group of four contraction
+// elements the order 0, 2, 1, 3, the same for A and B rows); elements 0-31
+// scaled by 2^(sf[0] - 127), 32-63 by 2^(sf[1] - 127).
 template <bool TWO>
 __device__ __forceinline__ void mx_expand_row_t(const uint8_t *codes, const MxBf16Factors &f0,
-                                                const MxBf16Factors &f1, uint8_t *dst, int r,
-                                                uint32_t k16) {
+                                                const MxBf16Factors &f1, uint8_t *dst, int r) {
     const uint32_t sw_in = (uint32_t)(r >> 1) & 3u;
     const uint32_t sw = (uint32_t)r & 7u;
     const uint8_t *src = codes + r * 64;
@@ -123,10 +122,10 @@ __device__ __forceinline__ void mx_expand_row_t(const uint8_t *codes, const MxBf
         const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ sw_in) << 4));
         const MxBf16Factors &f = c < 2 ? f0 : f1;
         uint32_t o[8];
-        e4m3x4_to_bf16x2x2<TWO>(v.x, f, k16, o[0], o[1]);
-        e4m3x4_to_bf16x2x2<TWO>(v.y, f, k16, o[2], o[3]);
-        e4m3x4_to_bf16x2x2<TWO>(v.z, f, k16, o[4], o[5]);
-        e4m3x4_to_bf16x2x2<TWO>(v.w, f, k16, o[6], o[7]);
+        e4m3x4_to_bf16x2x2<TWO>(v.x, f, o[0], o[1]);
+        e4m3x4_to_bf16x2x2<TWO>(v.y, f, o[2], o[3]);
+        e4m3x4_to_bf16x2x2<TWO>(v.z, f, o[4], o[5]);
+        e4m3x4_to_bf16x2x2<TWO>(v.w, f, o[6], o[7]);
         st_shared_v4(out + (((2 * c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
         st_shared_v4(out + (((2 * c + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
     }
@@ -135,11 +134,11 @@ __device__ __forceinline__ void mx_expand_row_t(const uint8_t *codes, const MxBf
 // One decision per row and k-step: the second multiply only where a block's
 // scale exceeds 2^7 (rare), so the common path carries no per-word test.
 __device__ __forceinline__ void mx_expand_row(const uint8_t *codes, const uint8_t *sf,
-                                              uint8_t *dst, int r, uint32_t k16) {
+                                              uint8_t *dst, int r) {
     const MxBf16Factors f0 = mx_bf16_factors(sf[0]);
     const MxBf16Factors f1 = mx_bf16_factors(sf[1]);
-    if (f0.two || f1.two) mx_expand_row_t<true>(codes, f0, f1, dst, r, k16);
-    else mx_expand_row_t<false>(codes, f0, f1, dst, r, k16);
+    if (f0.two || f1.two) mx_expand_row_t<true>(codes, f0, f1, dst, r);
+    else mx_expand_row_t<false>(codes, f0, f1, dst, r);
 }
 
 template <int MODE>
@@ -334,8 +333,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                 uint8_t *bf = sBf + sb * kMxBfStage;
                 // A rows past the group's end feed only accumulator rows that are
                 // never stored (MMA rows are independent), so they are not expanded
-                if (!is_a) mx_expand_row(raw + kMxRawA, sf + kMxSfA + r * 16, bf + kMxBfA, r, p.k16);
-                else if (r < ti.rows_valid) mx_expand_row(raw, sf + r * 16, bf, r, p.k16);
+                if (!is_a) mx_expand_row(raw + kMxRawA, sf + kMxSfA + r * 16, bf + kMxBfA, r);
+                else if (r < ti.rows_valid) mx_expand_row(raw, sf + r * 16, bf, r);
                 // the tensor cores read the stage through the async proxy
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -420,7 +419,6 @@ moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
     p.status = device_status_ptr();
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
-    p.k16 = 16u;
     const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
     kern<<<grid, kMxThreads, mx_smem_bytes(p.G), st>>>(p);
     return cuda_status(cudaGetLastError());

@@ -122,23 +122,18 @@ __device__ __forceinline__ MxBf16Factors mx_bf16_factors(uint32_t code) {
     return f;
 }
 
-// Four E4M3 codes (byte i of w = element i) -> two bf16x2 words (elements 0,1
-// in lo, 2,3 in hi, first element in the low half) times the block scale;
+// Four E4M3 codes (byte i of w = element i) -> two bf16x2 words times the
+// block scale: lo holds elements 0 (low half) and 2, hi elements 1 and 3.
+// Shifts and masks of w alone place every code (no byte permutes), at the
+// price of the order 0, 2, 1, 3 inside each group of four; A and B rows go
+// through the same expansion, so both operands of the matmul carry the same
+// permutation of the contraction index and every dot product is unchanged.
 // TWO applies f2 as well (needed only when the scale exceeds 2^7).
-// k16 is 16, passed at run time so that the magnitude shift and the join with
-// the sign bits stay one integer multiply-add (FMA pipe; the byte permutes
-// and masks already fill the ALU pipe).
 template <bool TWO>
 __device__ __forceinline__ void e4m3x4_to_bf16x2x2(uint32_t w, const MxBf16Factors &f,
-                                                   uint32_t k16, uint32_t &lo, uint32_t &hi) {
-    const uint32_t mag = w & 0x7F7F7F7Fu;
-    const uint32_t sgn = w ^ mag;
-    const uint32_t t0 = __byte_perm(mag, 0u, 0x4140);   // bytes: mag 0, 0, mag 1, 0
-    const uint32_t t1 = __byte_perm(mag, 0u, 0x4342);   // bytes: mag 2, 0, mag 3, 0
-    const uint32_t s0 = __byte_perm(sgn, 0u, 0x1404);   // sign 0 -> bit 15, sign 1 -> bit 31
-    const uint32_t s1 = __byte_perm(sgn, 0u, 0x3424);
-    lo = mul_bf16x2(t0 * k16 + s0, f.f1);                // disjoint bits: the add is an OR
-    hi = mul_bf16x2(t1 * k16 + s1, f.f1);
+                                                   uint32_t &lo, uint32_t &hi) {
+    lo = mul_bf16x2(((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u), f.f1);
+    hi = mul_bf16x2(((w >> 4) & 0x07F007F0u) | (w & 0x80008000u), f.f1);
     if constexpr (TWO) {   // f2 == 1 unless the block's scale exceeds 2^7
         lo = mul_bf16x2(lo, f.f2);
         hi = mul_bf16x2(hi, f.f2);
