@@ -26,8 +26,8 @@
 //   warp 1      TMEM owner and MMA issuer (bf16, M = 128, N = 256, K = 16;
 //               two accumulators).
 //   warps 2-5   epilogue, thread = row: GEMM 1 the clamped SwiGLU and h
-//               quantised to MXFP8 per 32 columns; GEMM 2 the routing-weight
-//               scale to bf16.
+//               quantised to MXFP8 per 32 columns (hardware conversion);
+//               GEMM 2 the routing-weight scale to bf16.
 //   warps 6-17  converters, three per scheduler: thread c expands row c of a
 //               code stage (rows 0-127 A, 128-383 B) into a 128-byte-swizzled
 //               bf16 stage (2 stages), then releases both.  Fewer warps leave
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                             hv[j] = swiglu_clamped(__uint_as_float(rg[j]), __uint_as_float(ru[j]),
                                                    p.clamp);
                         uint32_t w[8];
-                        const uint32_t code = mx_quantize_block(hv, w);
+                        const uint32_t code = mx_quantize_block_hw(hv, w);
                         const int col = ti.nt * 128 + c;
                         uint8_t *dst = p.hq + (size_t)row * p.I + col;
                         st_global_v4(dst, w[0], w[1], w[2], w[3]);

@@ -90,6 +90,28 @@ __device__ __forceinline__ uint32_t mx_quantize_block(const float (&v)[32], uint
     return code;
 }
 
+// The same quantisation of one block with the hardware conversion
+// (cvt.rn.satfinite: nearest-even, saturating at 448), for the expert GEMM's
+// epilogue, where it takes a fraction of the issue slots of e4m3_rne and
+// leaves them to the converter warps.  The quantiser kernel keeps e4m3_rne.
+__device__ __forceinline__ uint32_t mx_quantize_block_hw(const float (&v)[32], uint32_t (&w)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t code = mx_scale_code(amax);
+    const float inv = mx_inv_scale(code);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint16_t a, b;   // first operand -> high byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+            : "=h"(a) : "f"(v[4 * j + 1] * inv), "f"(v[4 * j] * inv));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+            : "=h"(b) : "f"(v[4 * j + 3] * inv), "f"(v[4 * j + 2] * inv));
+        w[j] = (uint32_t)a | ((uint32_t)b << 16);
+    }
+    return code;
+}
+
 // E4M3 -> bf16 without conversion instructions.  Placing a code's bits 6..0
 // at bf16 bits 10..4 and its sign at bit 15 gives a bf16 whose value is the
 // code's value times 2^-120, for normal codes ((1 + m/8) 2^(E-7) against
