@@ -723,7 +723,13 @@ def main():
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward")
     ap.add_argument("--mx-only", action="store_true",
                     help="time only the MXFP8 forward of the workload (profiling)")
+    ap.add_argument("--pairs", type=int, default=None,
+                    help="MOE_PAIR_* mask of the matmuls that may run as 2-SM pairs "
+                         "(default: the library's)")
     args = ap.parse_args()
+    if args.pairs is not None:
+        from moe_expert_layer_04_gb300 import _lib
+        _lib.moe_set_gemm_pairs(args.pairs)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 

@@ -167,8 +167,11 @@ moe_status moe_permute(const int32_t *ids, const float *weights, const uint16_t 
  * ceil(T*k / 256) * E <= 1048576 -- e.g. T = 65536, k = 6, E = 384.  Larger
  * sizes return MOE_ERR_UNSUPPORTED and launch nothing.  The call itself
  * allocates nothing.  The first call on a device looks up the array's device
- * address (a CUDA runtime query, done once per device); make that first call
- * before any stream capture.  All calls share the one array: two calls whose
+ * address (a CUDA runtime query, done once per device); under lazy module
+ * loading (the CUDA default) that first query may also load the library's
+ * module on that device and so reserve the array's 4 MiB at that moment.
+ * Make that first call during set-up, before any stream capture and before
+ * the point from which the program forbids allocation.  All calls share the one array: two calls whose
  * kernels overlap on the GPU (different streams, different host threads) race
  * and give wrong results; calls in order on one stream are safe. */
 moe_status moe_permute_noalloc(const int32_t *ids, const float *weights, const uint16_t *x, int T,
@@ -272,7 +275,28 @@ typedef struct {
     float *dweights;              /* [T,k] fp32 or NULL (gradient of the routing weights) */
     void *ws;                     /* moe_workspace_size(..., MOE_FLAG_BACKWARD | flags) bytes */
     size_t ws_bytes;
+    /* [host] profiling hook, or NULL: MOE_BWD_STAGES + 1 cudaEvent_t handles
+     * (created by the caller); event i is recorded on `stream` before stage i
+     * and the last one after the last stage, so the caller can time each stage
+     * with cudaEventElapsedTime.  A NULL entry is skipped. */
+    void *const *stage_events;
 } moe_bwd_args;
+
+/* Stages of moe_backward, in launch order (the two recompute stages are
+ * empty without MOE_FLAG_RECOMPUTE). */
+enum {
+    MOE_BWD_RECOMPUTE_GATHER = 0,  /* x_perm rebuilt from x */
+    MOE_BWD_RECOMPUTE_GEMM1 = 1,   /* g|u rebuilt (expert GEMM 1) */
+    MOE_BWD_GATHER_DY = 2,         /* dY_perm */
+    MOE_BWD_DGRAD2 = 3,            /* dA = dY_perm W2, SwiGLU backward, dw */
+    MOE_BWD_WGRAD2 = 4,            /* dW2 */
+    MOE_BWD_DGRAD1 = 5,            /* dX_perm = [dg|du] W13 */
+    MOE_BWD_WGRAD1 = 6,            /* dW13 */
+    MOE_BWD_ROUTER = 7,            /* routing-weight chain -> dz */
+    MOE_BWD_DX = 8,                /* dX assembly with the gate term */
+    MOE_BWD_DWG = 9,               /* dW_g */
+    MOE_BWD_STAGES = 10
+};
 
 /* Backward of the whole layer (analytic chain rule of the forward above;
  * [HP41] §2.3 names the fused backward of MegaGate's normalisation chain).
@@ -281,7 +305,7 @@ typedef struct {
  *   dH = w dA;  dg = dH clamp(u) silu'(min(g,c)) [g <= c];  du = dH silu(min(g,c)) [|u| <= c]
  *   dW2[g]  = sum_r dY_perm[r]^T (w h)[r]      dW13[g] = sum_r [dg|du][r]^T x_perm[r]
  *   dX_perm = [dg|du] W13[g]
- *   ds_j = (scaling/S_t)(dw_j - sum_i dw_i w_i / scaling),  dz_j = ds_j s_j (1 - s_j)
+ *   ds_j = (scaling dw_j - sum_i dw_i w_i) / S_t,  dz_j = ds_j s_j (1 - s_j)
  *   dX[t] = dX_perm[S+t] + sum_j dX_perm[slot_row[t,j]] + sum_j dz_j W_g[ids_j]
  *   dW_g  = dz^T x
  * The bias gets no gradient (it only ranks); hash routing has the same
@@ -364,6 +388,20 @@ const char *moe_status_string(moe_status s);
  * device (MOE_OK if no kernel recorded an error since the last call) and
  * resets it. */
 moe_status moe_last_device_status(void *stream);
+
+/* Tuning: which grouped matmuls may run as 2-SM pairs (two CTAs on two SMs
+ * sharing one tcgen05 MMA of 256 rows, each CTA loading half of the weight
+ * tile).  `mask` is an OR of the MOE_PAIR_* bits; a paired matmul is used only
+ * where the shape suits it (256-wide tiles; for the row-grouped matmuls, on
+ * average at least 1024 rows per group).  Results are those of the
+ * single-SM form up to the order of fp32 additions inside the tensor core.
+ * Process-wide; takes effect at the next call.  Returns the previous mask. */
+#define MOE_PAIR_EXPERT_GEMM1 (1 << 1)
+#define MOE_PAIR_EXPERT_GEMM2 (1 << 2)
+#define MOE_PAIR_DGRAD2 (1 << 3)        /* backward of expert GEMM 2 (+ SwiGLU backward) */
+#define MOE_PAIR_DGRAD1 (1 << 4)        /* backward of expert GEMM 1 w.r.t. its input */
+#define MOE_PAIR_WGRAD (1 << 5)         /* both weight-gradient matmuls */
+int moe_set_gemm_pairs(int mask);
 
 /* Test hook for the bounded waits: launches one block whose mbarrier wait
  * can never complete, with a limit of `limit_cycles` SM clock cycles; the

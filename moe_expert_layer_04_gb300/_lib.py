@@ -28,12 +28,16 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT,
     MOE_ERR_WORKSPACE = range(6)
 MOE_ROUTE_TOPK, MOE_ROUTE_HASH = 0, 1
 MOE_FLAG_BACKWARD, MOE_FLAG_RECOMPUTE = 1, 2
+MOE_PAIR_EXPERT_GEMM1, MOE_PAIR_EXPERT_GEMM2, MOE_PAIR_DGRAD2, MOE_PAIR_DGRAD1, MOE_PAIR_WGRAD = \
+    1 << 1, 1 << 2, 1 << 3, 1 << 4, 1 << 5
+MOE_PAIR_ALL = (MOE_PAIR_EXPERT_GEMM1 | MOE_PAIR_EXPERT_GEMM2 | MOE_PAIR_DGRAD2 | MOE_PAIR_DGRAD1
+                | MOE_PAIR_WGRAD)
 
 EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_route", "moe_permute",
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout",
-           "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
+           "moe_set_gemm_pairs", "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
            "moe_expert_gemm1_mx", "moe_expert_gemm2_mx"]
 
 
@@ -102,7 +106,13 @@ class BwdArgs(ctypes.Structure):
                 ("offsets", _P), ("row_token", _P), ("slot_row", _P),
                 ("x_perm", _P), ("gu_save", _P), ("dY", _P),
                 ("dX", _P), ("dW_g", _P), ("dW13", _P), ("dW2", _P),
-                ("dlogits", _P), ("dweights", _P), ("ws", _P), ("ws_bytes", _Z)]
+                ("dlogits", _P), ("dweights", _P), ("ws", _P), ("ws_bytes", _Z),
+                ("stage_events", ctypes.POINTER(_P))]
+
+
+MOE_BWD_STAGE_NAMES = ["recompute_gather", "recompute_gemm1", "gather_dY", "dgrad2", "wgrad2",
+                       "dgrad1", "wgrad1", "router_bwd", "dX", "dW_g"]
+MOE_BWD_STAGES = len(MOE_BWD_STAGE_NAMES)
 
 
 _SIGS = {
@@ -124,6 +134,7 @@ _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_last_device_status": ([_P], _I),
     "moe_selftest_wait_timeout": ([_LL, _P], _I),
+    "moe_set_gemm_pairs": ([_I], _I),
     "moe_mx_sf_pitch": ([_I], _I),
     "moe_mx_quantize": ([_P, _LL, _I, _P, _P, _P], _I),
     "moe_mx_gather": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
@@ -359,7 +370,7 @@ def moe_backward(args: dict, stream=None):
                  gu_save=F32, dY=BF16, dX=BF16, dW_g=F32, dW13=F32, dW2=F32, dlogits=F32,
                  dweights=F32, ws=U8)
     for name, _ in BwdArgs._fields_:
-        if name == "ws_bytes":
+        if name in ("ws_bytes", "stage_events"):
             continue
         v = args.get(name)
         if name in types:
@@ -367,6 +378,14 @@ def moe_backward(args: dict, stream=None):
         else:
             setattr(a, name, v)
     a.ws_bytes = 0 if args.get("ws") is None else args["ws"].numel()
+    ev = args.get("stage_events")
+    if ev is not None:
+        # torch.cuda.Event objects (recorded at least once, so that their CUDA
+        # events exist) or None entries
+        if len(ev) != MOE_BWD_STAGES + 1:
+            raise ValueError(f"stage_events: {MOE_BWD_STAGES + 1} entries expected")
+        handles = (_P * len(ev))(*[None if e is None else e.cuda_event for e in ev])
+        a.stage_events = ctypes.cast(handles, ctypes.POINTER(_P))
     st = load().moe_backward(ctypes.byref(a), _stream(stream))
     _check("moe_backward", st)
 
@@ -378,3 +397,9 @@ def moe_last_device_status(stream=None) -> int:
 def moe_selftest_wait_timeout(limit_cycles, stream=None):
     st = load().moe_selftest_wait_timeout(int(limit_cycles), _stream(stream))
     _check("moe_selftest_wait_timeout", st)
+
+
+def moe_set_gemm_pairs(mask: int) -> int:
+    """Which grouped matmuls may run as 2-SM pairs (MOE_PAIR_* bits); returns
+    the previous mask."""
+    return int(load().moe_set_gemm_pairs(int(mask)))

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libmoe (declared in include/moe.h): argument
 // validation, workspace carving, the device status word, tensor-map
 // encoding, and the order of kernel launches of each entry point.
+#include <atomic>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -208,6 +209,12 @@ moe_status launch_selftest_timeout(long long limit, cudaStream_t st) {
     wait_timeout_kernel<<<1, 32, 0, st>>>(limit, status);
     return cuda_status(cudaGetLastError());
 }
+
+namespace {
+std::atomic<int> g_pair_modes{MOE_PAIR_DGRAD2 | MOE_PAIR_WGRAD};
+}
+
+int gemm_pair_modes() { return g_pair_modes.load(std::memory_order_relaxed); }
 
 moe_status check_ffn(int G, int max_rows, int d, int I, int S) {
     if (G < 1 || G > 1025 || max_rows < 1 || d < 1 || I < 1 || S < 0) return MOE_ERR_INVALID_ARG;
@@ -472,15 +479,24 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
     if (!a->ws || a->ws_bytes < moe_workspace_size(T, d, E, k, I, flags)) return MOE_ERR_WORKSPACE;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // profiling hook: an event before each stage and after the last
+    auto mark = [&](int i) -> bool {
+        if (!a->stage_events || !a->stage_events[i]) return true;
+        return cudaEventRecord(static_cast<cudaEvent_t>(a->stage_events[i]), st) == cudaSuccess;
+    };
     BwdWorkspace w = carve_bwd(static_cast<uint8_t *>(a->ws), T, d, E, k, I, a->flags);
     const int S = T * k;
     const int R = S + T;
     const int G = E + 1;
     const uint16_t *x_perm = a->x_perm;
     const float *gu = a->gu_save;
+    if (!mark(MOE_BWD_RECOMPUTE_GATHER)) return MOE_ERR_CUDA;
     if (rec) {
         // rebuild the permuted input rows and the expert GEMM-1 outputs
         if ((s = launch_gather_rows(a->x, a->slot_row, T, d, k, w.x_perm, st)) != MOE_OK) return s;
+    }
+    if (!mark(MOE_BWD_RECOMPUTE_GEMM1)) return MOE_ERR_CUDA;
+    if (rec) {
         if ((s = launch_ffn1(w.x_perm, a->offsets, G, R, a->W13, d, I, a->clamp, nullptr, w.gu,
                              st)) != MOE_OK)
             return s;
@@ -488,23 +504,33 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
         gu = w.gu;
     }
     int n_part = 0;
+    if (!mark(MOE_BWD_GATHER_DY)) return MOE_ERR_CUDA;
     if ((s = launch_gather_rows(a->dY, a->slot_row, T, d, k, w.dY_perm, st)) != MOE_OK) return s;
+    if (!mark(MOE_BWD_DGRAD2)) return MOE_ERR_CUDA;
     if ((s = launch_dgrad2(w.dY_perm, a->offsets, G, R, a->W2, gu, a->row_weight, S, d, I,
                            a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
         return s;
+    if (!mark(MOE_BWD_WGRAD2)) return MOE_ERR_CUDA;
     if ((s = launch_wgrad(w.dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, st)) != MOE_OK) return s;
+    if (!mark(MOE_BWD_DGRAD1)) return MOE_ERR_CUDA;
     if ((s = launch_dgrad1(w.dGU, a->offsets, G, R, a->W13, d, I, w.dX_perm, st)) != MOE_OK)
         return s;
+    if (!mark(MOE_BWD_WGRAD1)) return MOE_ERR_CUDA;
     if ((s = launch_wgrad(w.dGU, 2 * I, x_perm, d, a->offsets, G, R, a->dW13, st)) != MOE_OK)
         return s;
+    if (!mark(MOE_BWD_ROUTER)) return MOE_ERR_CUDA;
     if ((s = launch_router_bwd(w.dw_part, n_part, a->slot_row, a->ids, a->weights, a->scores_sel,
                                T, E, k, a->scaling, w.dz_sel, w.dz_row, a->dlogits, a->dweights,
                                st)) != MOE_OK)
         return s;
+    if (!mark(MOE_BWD_DX)) return MOE_ERR_CUDA;
     if ((s = launch_combine(w.dX_perm, a->slot_row, T, d, k, 1, w.dz_sel, a->ids, a->W_g, a->dX,
                             st)) != MOE_OK)
         return s;
-    return launch_dwg(x_perm, w.dz_row, a->offsets, d, E, w.dwg_part, a->dW_g, st);
+    if (!mark(MOE_BWD_DWG)) return MOE_ERR_CUDA;
+    if ((s = launch_dwg(x_perm, w.dz_row, a->offsets, d, E, w.dwg_part, a->dW_g, st)) != MOE_OK)
+        return s;
+    return mark(MOE_BWD_STAGES) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 const char *moe_status_string(moe_status s) {
@@ -530,6 +556,12 @@ moe_status moe_last_device_status(void *stream) {
     if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
         return MOE_ERR_CUDA;
     return static_cast<moe_status>(v);
+}
+
+int moe_set_gemm_pairs(int mask) {
+    const int valid = MOE_PAIR_EXPERT_GEMM1 | MOE_PAIR_EXPERT_GEMM2 | MOE_PAIR_DGRAD2 |
+                      MOE_PAIR_DGRAD1 | MOE_PAIR_WGRAD;
+    return g_pair_modes.exchange(mask & valid);
 }
 
 moe_status moe_selftest_wait_timeout(long long limit_cycles, void *stream) {

@@ -130,10 +130,11 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
             Ssum += __shfl_sync(0xffffffffu, s, j);
             dot += __shfl_sync(0xffffffffu, dw, j) * __shfl_sync(0xffffffffu, wt, j);
         }
-        // w_j = scaling s_j / S  =>  ds_j = (scaling / S) (dw_j - sum_i dw_i w_i / scaling)
+        // w_j = scaling s_j / S  =>  ds_j = (scaling dw_j - sum_i dw_i w_i) / S
+        // (no division by the scaling: scaling 0 gives zero gradients)
         float dzv = 0.0f;
         if (Ssum > 0.0f) {
-            const float ds = (scaling / Ssum) * (dw - dot / scaling);
+            const float ds = (scaling * dw - dot) / Ssum;
             dzv = ds * s * (1.0f - s);
         }
         if (dlogits) {

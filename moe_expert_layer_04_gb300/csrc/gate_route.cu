@@ -7,8 +7,8 @@
 //
 // Work split.  A tile is 128 tokens.  With CS = 2 a cluster of two CTAs takes
 // a tile and splits the experts: CTA r accumulates the logits of experts
-// [r E/2, (r+1) E/2) in TMEM (tcgen05.mma, M = 128, N = E/2), both CTAs
-// reading the tile of x that each loads half of and multicasts to the pair.
+// [r E/2, (r+1) E/2) in TMEM (tcgen05.mma, M = 128, N = E/2); each CTA loads
+// the whole x tile itself (the pair's two reads of it meet in L2).
 // With CS = 1 (E not a multiple of 64) one CTA takes all E columns.  TMEM
 // holds two accumulators when a CTA's columns fit in 256, so the epilogue of
 // one tile overlaps the MMAs of the next.
@@ -53,7 +53,7 @@ constexpr int kGrABytes = 128 * 64 * 2;
 constexpr size_t kGrSmemLimit = 227 * 1024;
 
 struct GateRouteParams {
-    CUtensorMap tmX;  // x [T, d] bf16, boxes 64 x (128 / CS)
+    CUtensorMap tmX;  // x [T, d] bf16, boxes 64 x 128
     CUtensorMap tmW;  // W_g [E, d] bf16, boxes 64 x (columns of one MMA)
     CUtensorMap tmZ;  // logits [T, E] fp32, boxes 32 x 32 (stores)
     const float *offset;  // [E] or null
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CS);   // released by the MMA of every CTA of the pair
+            mbar_init(&empty[s], 1);    // released by this CTA's MMAs
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(kGrThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the peer's multicast copies, commits and list arrivals target our
-    // barriers: both CTAs must have initialised them first
+    // the peer's list arrivals target our barriers: both CTAs must have
+    // initialised them first
     if constexpr (CS == 2) cluster_sync_all();
     const uint32_t tmem_base = *tmem_base_s;
     const WaitCtl wc{abort_s, p.status, p.wait_limit};
@@ -225,13 +225,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                     mbar_arrive_expect_tx(&full[s], STAGE);
                     uint8_t *a = stages + (size_t)s * STAGE;
                     uint8_t *b = a + kGrABytes;
-                    if constexpr (CS == 2) {
-                        // our half of the x tile, into both CTAs of the pair
-                        tma_load_2d_mc(a + rank * 8192, &p.tmX, &full[s], kb * 64,
-                                       t * 128 + rank * 64, 0x3);
-                    } else {
-                        tma_load_2d(a, &p.tmX, &full[s], kb * 64, t * 128);
-                    }
+                    tma_load_2d(a, &p.tmX, &full[s], kb * 64, t * 128);
                     for (int h = 0; h < nmma; ++h)
                         tma_load_2d(b + h * NM * 128, &p.tmW, &full[s], kb * 64, col0 + h * NM);
                     last_par[s] = (int)ph;
@@ -242,12 +236,6 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                 for (int i = 0; i < STAGES; ++i)
                     if (last_par[i] >= 0)
                         mbar_wait_teardown(&full[i], (uint32_t)last_par[i], p.wait_limit);
-            } else if constexpr (CS == 2) {
-                // both MMAs' releases of every stage (the peer read our multicast
-                // half) must have landed before the CTA may exit
-                for (int i = 0; i < STAGES; ++i)
-                    if (last_par[i] >= 0)
-                        mbar_wait_teardown(&empty[i], (uint32_t)last_par[i], p.wait_limit);
             }
         }
     } else if (warp == 1) {
@@ -276,8 +264,7 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                             umma_bf16(d_tmem + h * NM, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                         }
                     }
-                    if constexpr (CS == 2) umma_commit_mc(&empty[s], 0x3);
-                    else umma_commit(&empty[s]);
+                    umma_commit(&empty[s]);
                 }
                 __syncwarp();
                 if (++s == (uint32_t)STAGES) { s = 0; ph ^= 1u; }
@@ -732,7 +719,7 @@ moe_status launch_gate_route(const uint16_t *x, const uint16_t *Wg, const float 
     std::memset(&p, 0, sizeof p);
     const int NE = E / CS;
     const int NM = NE > 256 ? NE / 2 : NE;
-    if (!encode_tmap_bf16_2d(&p.tmX, x, d, T, (uint64_t)d * 2, 64, 128 / CS))
+    if (!encode_tmap_bf16_2d(&p.tmX, x, d, T, (uint64_t)d * 2, 64, 128))
         return MOE_ERR_CUDA;
     if (!encode_tmap_bf16_2d(&p.tmW, Wg, d, E, (uint64_t)d * 2, 64, NM)) return MOE_ERR_CUDA;
     if (!encode_tmap_f32_2d(&p.tmZ, logits, E, T, (uint64_t)E * 4, 32, 32)) return MOE_ERR_CUDA;

@@ -48,6 +48,8 @@ moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G,
     p.w_rows = S;
     p.gu_in = gu;
     if (dw_tiles) *dw_tiles = dgrad2_n_tiles(I);
+    if (BN == 256 && rows_pair(GM_DGRAD2, max_rows, G))
+        return launch_gemm<GM_DGRAD2, 256, 2>(p, row_pair_bound(max_rows, G) * p.n_tiles, st);
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     switch (BN) {
         case 256: return launch_gemm<GM_DGRAD2, 256>(p, tiles, st);
@@ -73,6 +75,8 @@ moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int
     p.N = d;
     p.b_rows_per_group = 2 * I;
     p.out = dX_perm;
+    if (BN == 256 && rows_pair(GM_DGRAD1, max_rows, G))
+        return launch_gemm<GM_DGRAD1, 256, 2>(p, row_pair_bound(max_rows, G) * p.n_tiles, st);
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     return BN == 256 ? launch_gemm<GM_DGRAD1, 256>(p, tiles, st)
                      : launch_gemm<GM_DGRAD1, 128>(p, tiles, st);
@@ -100,9 +104,10 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     p.M = M;
     p.out = dW;
     const int tiles = G * p.m_tiles * p.n_tiles;
-    // long contractions: two-CTA clusters share each B tile (measured: the
-    // weight-gradient GEMMs gain, the row-grouped GEMMs do not)
-    if (BN == 256 && p.m_tiles % 2 == 0) return launch_gemm<GM_WGRAD, 256, 2>(p, tiles / 2, st);
+    // long contractions: 2-SM pairs, two 128-row output tiles sharing one B
+    // tile, each CTA loading half of it
+    if (BN == 256 && p.m_tiles % 2 == 0 && (gemm_pair_modes() >> GM_WGRAD & 1))
+        return launch_gemm<GM_WGRAD, 256, 2>(p, tiles / 2, st);
     switch (BN) {
         case 256: return launch_gemm<GM_WGRAD, 256>(p, tiles, st);
         case 128: return launch_gemm<GM_WGRAD, 128>(p, tiles, st);

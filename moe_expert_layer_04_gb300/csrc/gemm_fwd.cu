@@ -58,6 +58,8 @@ moe_status launch_ffn1(const uint16_t *x_perm, const int32_t *offsets, int G, in
     p.clamp = clamp;
     p.out = h;
     p.out2 = gu_save;
+    if (BN == 256 && rows_pair(GM_FFN1, max_rows, G))
+        return launch_gemm<GM_FFN1, 256, 2>(p, row_pair_bound(max_rows, G) * p.n_tiles, st);
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     return BN == 256 ? launch_gemm<GM_FFN1, 256>(p, tiles, st)
                      : launch_gemm<GM_FFN1, 128>(p, tiles, st);
@@ -69,9 +71,12 @@ moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     const int BN = (d % 256 == 0) ? 256 : 128;
+    const bool pair = BN == 256 && rows_pair(GM_FFN2, max_rows, G);
     if (!encode_tmap_bf16_2d(&p.tmA, h, I, max_rows, (uint64_t)I * 2, 64, 128))
         return MOE_ERR_CUDA;
-    if (!encode_tmap_bf16_2d(&p.tmB, W2, I, (uint64_t)G * d, (uint64_t)I * 2, 64, BN))
+    // a pair's CTAs each load half of the B tile's rows
+    if (!encode_tmap_bf16_2d(&p.tmB, W2, I, (uint64_t)G * d, (uint64_t)I * 2, 64,
+                             pair ? BN / 2 : BN))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
@@ -82,6 +87,7 @@ moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max
     p.out = y;
     p.row_w = row_w;
     p.w_rows = S;
+    if (pair) return launch_gemm<GM_FFN2, 256, 2>(p, row_pair_bound(max_rows, G) * p.n_tiles, st);
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     return BN == 256 ? launch_gemm<GM_FFN2, 256>(p, tiles, st)
                      : launch_gemm<GM_FFN2, 128>(p, tiles, st);

@@ -25,6 +25,17 @@
 // Tiles are handed out round-robin (tile = blockIdx.x + i * gridDim.x), so
 // the schedule is static and the results are deterministic.
 //
+// CL = 2 (row-grouped and K-grouped modes): clusters of two CTAs run 2-SM
+// MMAs (tcgen05.mma.cta_group::2, M = 256).  The pair computes two 128-row
+// tiles of the same group and column tile; CTA r loads its own 128 rows of A
+// and half of the B tile (columns [r BN/2, (r+1) BN/2)) with plain TMA
+// copies, so each CTA reads half the B bytes per MMA that a lone CTA does and
+// more operand stages fit.  The even CTA issues the MMAs once both CTAs'
+// stages are full (the odd CTA's MMA warp forwards its stage's completion
+// through a cluster-scope arrive) and releases stages and accumulators to
+// both CTAs with one commit; every epilogue warp of the pair hands its drained
+// accumulator back to the even CTA.
+//
 // Every wait is bounded (moe_ptx.cuh): on a timeout the CTA records
 // MOE_ERR_TIMEOUT, drains its own TMA copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -95,11 +106,11 @@ constexpr int kEpiWarpBytesDgrad2 = 2048;
 // Operand stages plus staging of the TMA-store path.
 constexpr int kStoreModeBudget = 216 * 1024;
 
-template <int BN, int MODE>
+template <int BN, int MODE, int CL = 1>
 struct TileShape {
     static constexpr bool TMA_STORE = (MODE == GM_WGRAD || MODE == GM_DGRAD2);
     static constexpr int A_BYTES = 128 * 64 * 2;
-    static constexpr int B_BYTES = BN * 64 * 2;
+    static constexpr int B_BYTES = (BN / CL) * 64 * 2;   // this CTA's share of the B tile
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int EPI_BYTES =
         MODE == GM_WGRAD    ? ModeTraits<MODE>::NEPI * kEpiWarpBytes
@@ -111,9 +122,9 @@ struct TileShape {
 };
 
 // Dynamic shared memory of one CTA for G groups.
-template <int BN, int MODE>
+template <int BN, int MODE, int CL = 1>
 inline size_t gemm_smem_bytes(int G) {
-    using TS = TileShape<BN, MODE>;
+    using TS = TileShape<BN, MODE, CL>;
     return 1024 + (size_t)TS::STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256 +
            8 * (size_t)(G + 2);
 }
@@ -131,10 +142,10 @@ struct TileInfo {
     int rt;          // row modes: index of the row tile (over all groups)
 };
 
-// Tile t of the schedule.  With CL = 2 (a two-CTA cluster sharing the B
-// operand) t counts pairs of 128-row tiles of the same group and column tile,
-// and `rank` picks the CTA's tile of the pair; a pair's second tile may lie
-// past the group's rows (rows_valid <= 0: computed, never stored).
+// Tile t of the schedule.  With CL = 2 (a 2-SM pair) t counts pairs of
+// 128-row tiles of the same group and column tile, and `rank` picks the CTA's
+// tile of the pair; a pair's second tile may lie past the group's rows
+// (rows_valid <= 0: computed, never stored).
 template <int MODE, int BN, int CL>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, const int *mt_start,
                                                 const int *offs, int rank) {
@@ -266,21 +277,21 @@ __device__ __forceinline__ void epi_bf16_scaled(uint16_t *y, int N, const TileIn
     }
 }
 
-// CL = 1: one CTA per tile.  CL = 2: clusters of two CTAs; the pair computes
-// two 128-row tiles with the same B tile, each CTA loading half of B and
-// multicasting it into both CTAs' shared memory (half the B traffic per CTA).
+// CL = 1: one CTA per tile.  CL = 2: a 2-SM pair per two tiles (see above).
 template <int MODE, int BN, int CL>
 __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p) {
     using MT = ModeTraits<MODE>;
-    static_assert(CL == 1 || CL == 2, "cluster of one or two CTAs");
-    static_assert(CL == 1 || !MT::B_MN || BN >= 128, "the B boxes split between the pair");
-    using TS = TileShape<BN, MODE>;
+    static_assert(CL == 1 || CL == 2, "one CTA or a 2-SM pair");
+    static_assert(CL == 1 || (BN >= 128 && !MT::DENSE && MODE != GM_FFN12),
+                  "the pair form: row- or K-grouped modes, 64-column B boxes per CTA");
+    using TS = TileShape<BN, MODE, CL>;
     constexpr int STAGES = TS::STAGES;
-    // the barrier block (full/empty per stage, two tfull, two tempty, done, the
-    // TMEM base and the abort flag) must fit the 256 bytes the layout reserves
-    static_assert((2 * STAGES + 5) * 8 + 8 <= 256, "too many operand stages for the barrier block");
-    constexpr uint32_t IDESC = idesc_bf16_f32(128, BN, MT::A_MN, MT::B_MN);
+    // the barrier block (full/empty/pfull per stage, two tfull, two tempty,
+    // done, the TMEM base and the abort flag) must fit the 256 bytes the
+    // layout reserves
+    static_assert((3 * STAGES + 5) * 8 + 8 <= 256, "too many operand stages for the barrier block");
+    constexpr uint32_t IDESC = idesc_bf16_f32(128 * CL, BN, MT::A_MN, MT::B_MN);
 
     extern __shared__ uint8_t smem_raw[];
     // aligned to 1024 B by pointer arithmetic on the shared array itself, so
@@ -295,7 +306,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
-    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *pfull = done + 1;   // CL = 2, even CTA: the odd CTA's stage is full
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(pfull + STAGES);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
     int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256);
     int *mt_start = offs + (p.G + 1);
@@ -306,11 +318,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CL);   // released by the MMA of every CTA of the pair
+            mbar_init(&empty[s], 1);
+            mbar_init(&pfull[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 32 * MT::NEPI);
+            // CL = 2: one arrival per epilogue warp of either CTA
+            mbar_init(&tempty[a], CL == 1 ? 32 * MT::NEPI : 2 * MT::NEPI);
         }
         mbar_init(done, 1);
         *abort_s = 0;
@@ -324,8 +338,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         if constexpr (MODE == GM_DGRAD2) tma_prefetch_desc(&p.tmO2);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_base_s, TS::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (CL == 2) {
+            tmem_alloc_pair(tmem_base_s, TS::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_base_s, TS::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if constexpr (!MT::DENSE) {
         if (warp == 2) {
@@ -358,8 +377,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the peer's multicast copies and commits target our barriers: both CTAs
-    // must have initialised them first
+    // the pair's commits and forwarded arrivals target both CTAs' barriers:
+    // both must have initialised them first
     if constexpr (CL == 2) cluster_sync_all();
     const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
     const int cid = blockIdx.x / CL;          // cluster index
@@ -401,37 +420,52 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 }
                 for (int kb = 0; kb < ti.kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], TS::STAGE_BYTES);
+                    // CL = 2: the even CTA's barrier takes both CTAs' halves of a
+                    // stage, except a ragged-contraction tail stage, whose halves
+                    // each CTA completes on its own barrier (each zeroes its rows
+                    // past the group's end before the pair's MMA reads them)
+                    const bool tail = MT::KGROUP && ti.krows - kb * 64 < 64;
+                    const bool to_even = CL == 2 && rank == 1 && !tail;
+                    uint32_t bar_even = 0;
+                    if (to_even)
+                        bar_even = dsmem_map(&full[s], 0);
+                    else
+                        mbar_arrive_expect_tx(
+                            &full[s], (CL == 2 && !tail ? 2 : 1) * (uint32_t)TS::STAGE_BYTES);
+                    auto load = [&](void *dst, const CUtensorMap *tm, int c0, int c1) {
+                        if (to_even) tma_load_2d_pairbar(dst, tm, bar_even, c0, c1);
+                        else tma_load_2d(dst, tm, &full[s], c0, c1);
+                    };
                     uint8_t *a_dst = sA + s * TS::A_BYTES;
                     uint8_t *b_dst = sB + s * TS::B_BYTES;
                     if constexpr (MT::A_MN) {
-                        tma_load_2d(a_dst, &p.tmA, &full[s], ti.m0, ti.krow0 + kb * 64);
-                        tma_load_2d(a_dst + 8192, &p.tmA, &full[s], ti.m0 + 64, ti.krow0 + kb * 64);
+                        load(a_dst, &p.tmA, ti.m0, ti.krow0 + kb * 64);
+                        load(a_dst + 8192, &p.tmA, ti.m0 + 64, ti.krow0 + kb * 64);
                     } else if (MODE == GM_FFN12 && ti.phase == 1) {
-                        tma_load_2d(a_dst, &p.tmO, &full[s], kb * 64, ti.row0);
+                        load(a_dst, &p.tmO, kb * 64, ti.row0);
                     } else {
-                        tma_load_2d(a_dst, &p.tmA, &full[s], kb * 64, ti.row0);
+                        load(a_dst, &p.tmA, kb * 64, ti.row0);
                     }
                     if constexpr (CL == 1) {
                         if constexpr (MODE == GM_FFN12) {
                             if (ti.phase == 0) {
                                 const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
-                                tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, r);
-                                tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB, &full[s], kb * 64,
+                                load(b_dst, &p.tmB, kb * 64, r);
+                                load(b_dst + (BN / 2) * 128, &p.tmB, kb * 64,
                                             r + p.I);
                             } else {
-                                tma_load_2d(b_dst, &p.tmO2, &full[s], kb * 64,
+                                load(b_dst, &p.tmO2, kb * 64,
                                             ti.g * p.b_rows2 + ti.nt * BN);
                             }
                         } else if constexpr (MODE == GM_GATE) {
-                            tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, ti.nt * BN);
+                            load(b_dst, &p.tmB, kb * 64, ti.nt * BN);
                         } else if constexpr (MODE == GM_FFN1) {
                             const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
-                            tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64, r);
-                            tma_load_2d(b_dst + (BN / 2) * 128, &p.tmB, &full[s], kb * 64,
+                            load(b_dst, &p.tmB, kb * 64, r);
+                            load(b_dst + (BN / 2) * 128, &p.tmB, kb * 64,
                                         r + p.I);
                         } else if constexpr (MODE == GM_FFN2) {
-                            tma_load_2d(b_dst, &p.tmB, &full[s], kb * 64,
+                            load(b_dst, &p.tmB, kb * 64,
                                         ti.g * p.b_rows_per_group + ti.nt * BN);
                         } else {
                             // MN-major B: BN/64 boxes of 64 columns x 64 contraction rows
@@ -439,44 +473,43 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                                                         : ti.g * p.b_rows_per_group + kb * 64;
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
-                                tma_load_2d(b_dst + j * 8192, &p.tmB, &full[s],
-                                            ti.nt * BN + 64 * j, krow);
+                                load(b_dst + j * 8192, &p.tmB, ti.nt * BN + 64 * j, krow);
                         }
                     } else {
-                        // the pair shares B: this CTA loads its half and multicasts it
-                        constexpr uint16_t kPair = 0x3;
-                        if constexpr (MODE == GM_GATE) {
-                            tma_load_2d_mc(b_dst + rank * (BN / 2) * 128, &p.tmB, &full[s],
-                                           kb * 64, ti.nt * BN + rank * (BN / 2), kPair);
-                        } else if constexpr (MODE == GM_FFN1) {
+                        // 2-SM pair: this CTA's half of the B tile, into its own stage
+                        if constexpr (MODE == GM_FFN1) {
+                            // rank 0: the gate rows, rank 1: the matching up rows
                             const int r = ti.g * p.b_rows_per_group + ti.nt * (BN / 2);
-                            tma_load_2d_mc(b_dst + rank * (BN / 2) * 128, &p.tmB, &full[s],
-                                           kb * 64, r + rank * p.I, kPair);
+                            load(b_dst, &p.tmB, kb * 64, r + rank * p.I);
                         } else if constexpr (MODE == GM_FFN2) {
-                            tma_load_2d_mc(b_dst + rank * (BN / 2) * 128, &p.tmB, &full[s],
-                                           kb * 64,
-                                           ti.g * p.b_rows_per_group + ti.nt * BN + rank * (BN / 2),
-                                           kPair);
+                            load(b_dst, &p.tmB, kb * 64,
+                                        ti.g * p.b_rows_per_group + ti.nt * BN + rank * (BN / 2));
                         } else {
+                            // MN-major B: BN/128 boxes of 64 columns x 64 contraction rows
                             const int krow = MT::KGROUP ? ti.krow0 + kb * 64
                                                         : ti.g * p.b_rows_per_group + kb * 64;
 #pragma unroll
-                            for (int j = rank; j < BN / 64; j += 2)
-                                tma_load_2d_mc(b_dst + j * 8192, &p.tmB, &full[s],
-                                               ti.nt * BN + 64 * j, krow, kPair);
+                            for (int j = 0; j < BN / 128; ++j)
+                                load(b_dst + j * 8192, &p.tmB, ti.nt * BN + rank * (BN / 2) + 64 * j, krow);
                         }
                     }
                     last_par[s] = (int)ph;
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok) {
+            if (!ok && CL == 2 && rank == 1) {
+                // this CTA's copies complete on the even CTA's barriers, which it
+                // cannot wait on: give those still in flight time to land (a
+                // copy takes microseconds; this waits about a millisecond)
+                const long long t0 = clock64();
+                while (clock64() - t0 < (1LL << 21)) __nanosleep(1000);
+            } else if (!ok) {
                 // drain the copies still in flight before the CTA exits
                 for (int i = 0; i < STAGES; ++i)
                     if (last_par[i] >= 0)
                         mbar_wait_teardown(&full[i], (uint32_t)last_par[i], p.wait_limit);
             } else if constexpr (CL == 2) {
-                // every release of a stage (ours and the peer's commit) must have
+                // every release of a stage (the even CTA's commits) must have
                 // landed in our barriers before the CTA may exit
                 for (int i = 0; i < STAGES; ++i)
                     if (last_par[i] >= 0)
@@ -485,40 +518,80 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // CL = 2: the even CTA issues the pair's MMAs.  The odd CTA's warp only
+        // takes part in the ragged-contraction tail stages: it zeroes its own A
+        // rows past the group's end and then tells the even CTA (pfull).
+        const bool issuer = CL == 1 || rank == 0;
         uint32_t s = 0, ph = 0;
+        uint32_t tail_ph = 0;   // bit s: parity of stage s's next tail handshake
         int it = 0;
         bool ok = true;
+        bool issued = false;
+        // ragged contraction: only the 16-row MMA steps that hold rows of this
+        // group run; inside the last one, rows past the group's end (the next
+        // group's rows) are zeroed in A.  B's rows there are finite data or TMA
+        // zero fill, so they add nothing.  In a pair each CTA zeroes its own A
+        // rows, which are the only A rows its output rows read.  Returns the
+        // number of 16-row steps.
+        auto zero_tail = [&](int valid) {
+            const int n_kk = (valid + 15) >> 4;
+            const int nrows = n_kk * 16 - valid;  // 0..15
+            for (int i = lane; i < 2 * nrows * 8; i += 32) {
+                const int box = i / (nrows * 8);
+                const int rem = i - box * nrows * 8;
+                uint8_t *dst = sA + s * TS::A_BYTES + box * 8192 + (valid + (rem >> 3)) * 128 +
+                               (rem & 7) * 16;
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (nrows > 0) fence_proxy_async_smem();
+            __syncwarp();
+            return n_kk;
+        };
         for (int t = cid; ok && t < total_tiles; t += ncl, ++it) {
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
-            if (!mbar_wait(&tempty[acc], aph ^ 1u, wc)) { ok = false; break; }
-            tc_fence_after();
+            if (issuer) {
+                const bool got = CL == 2 ? mbar_wait_cluster(&tempty[acc], aph ^ 1u, wc)
+                                         : mbar_wait(&tempty[acc], aph ^ 1u, wc);
+                if (!got) { ok = false; break; }
+                tc_fence_after();
+            }
             const uint32_t d_tmem = tmem_base + acc * BN;
             for (int kb = 0; kb < ti.kb; ++kb) {
+                const int valid = MT::KGROUP ? ti.krows - kb * 64 : 64;
+                const bool tail = valid < 64;
+                if constexpr (CL == 2) {
+                    if (rank == 1) {
+                        if (tail) {
+                            // this CTA's half of the tail stage landed on its own barrier
+                            if (!mbar_wait(&full[s], (tail_ph >> s) & 1u, wc)) { ok = false; break; }
+                            zero_tail(valid);
+                            if (lane == 0) mbar_arrive_remote(dsmem_map(&pfull[s], 0));
+                            __syncwarp();
+                            tail_ph ^= 1u << s;
+                        }
+                        if (++s == STAGES) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
+                }
                 if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + s * TS::A_BYTES);
                 const uint32_t b_addr = smem_u32(sB + s * TS::B_BYTES);
                 int n_kk = 4;
                 if constexpr (MT::KGROUP) {
-                    // ragged contraction: only the 16-row MMA steps that hold rows of
-                    // this group run; inside the last one, rows past the group's end
-                    // (the next group's rows) are zeroed in A.  B's rows there are
-                    // finite data or TMA zero fill, so they add nothing.
-                    const int valid = ti.krows - kb * 64;
-                    if (valid < 64) {
-                        n_kk = (valid + 15) >> 4;
-                        const int nrows = n_kk * 16 - valid;  // 0..15
-                        for (int i = lane; i < 2 * nrows * 8; i += 32) {
-                            const int box = i / (nrows * 8);
-                            const int rem = i - box * nrows * 8;
-                            uint8_t *dst = sA + s * TS::A_BYTES + box * 8192 +
-                                           (valid + (rem >> 3)) * 128 + (rem & 7) * 16;
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                    if (tail) n_kk = zero_tail(valid);
+                }
+                if constexpr (CL == 2) {
+                    if (tail) {
+                        // the odd CTA has zeroed its rows of the tail stage too
+                        if (!mbar_wait_cluster(&pfull[s], (tail_ph >> s) & 1u, wc)) {
+                            ok = false;
+                            break;
                         }
-                        if (nrows > 0) fence_proxy_async_smem();
-                        __syncwarp();
+                        tail_ph ^= 1u << s;
+                        tc_fence_after();
                     }
                 }
                 if (lane == 0) {
@@ -529,21 +602,34 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                                                      : sdesc_sw128(a_addr + kk * 32, 16, 1024);
                         const uint64_t bd = MT::B_MN ? sdesc_sw128(b_addr + kk * 2048, 8192, 1024)
                                                      : sdesc_sw128(b_addr + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        if constexpr (CL == 2)
+                            umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if constexpr (CL == 2) umma_commit_mc(&empty[s], 0x3);
+                    if constexpr (CL == 2) umma_commit_pair(&empty[s], 0x3);
                     else umma_commit(&empty[s]);
                 }
+                issued = true;
                 __syncwarp();
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
             if (!ok) break;
-            if (lane == 0) umma_commit(&tfull[acc]);
-            __syncwarp();
+            if (issuer) {
+                if (lane == 0) {
+                    if constexpr (CL == 2) umma_commit_pair(&tfull[acc], 0x3);
+                    else umma_commit(&tfull[acc]);
+                }
+                __syncwarp();
+            }
         }
-        if (!ok) {
-            // every MMA this thread issued must finish before TMEM is freed
-            if (lane == 0) umma_commit(done);
+        if (issuer && (CL == 2 ? issued : !ok)) {
+            // every MMA this thread issued must finish before TMEM is freed (and,
+            // for a pair, before either CTA's operand stages go away)
+            if (lane == 0) {
+                if constexpr (CL == 2) umma_commit_pair(done, 0x1);
+                else umma_commit(done);
+            }
             __syncwarp();
             mbar_wait_teardown(done, 0, p.wait_limit);
         }
@@ -767,7 +853,16 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            if constexpr (CL == 2) {
+                // one arrival per warp on the even CTA's accumulator barrier
+                __syncwarp();
+                if (lane == 0) {
+                    if (rank == 0) mbar_arrive(&tempty[acc]);
+                    else mbar_arrive_remote(dsmem_map(&tempty[acc], 0));
+                }
+            } else {
+                mbar_arrive(&tempty[acc]);
+            }
         }
     }
 
@@ -778,9 +873,15 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TS::TMEM_COLS);
-    // neither CTA of a pair leaves while the other may still signal it
-    if constexpr (CL == 2) cluster_sync_all();
+    if constexpr (CL == 2) {
+        // both CTAs are past their last TMEM read and the pair's MMAs have
+        // completed; neither leaves while the other may still signal it
+        cluster_sync_all();
+        if (warp == 1) tmem_dealloc_pair(tmem_base, TS::TMEM_COLS);
+        cluster_sync_all();
+    } else {
+        if (warp == 1) tmem_dealloc(tmem_base, TS::TMEM_COLS);
+    }
 }
 
 }  // namespace moe

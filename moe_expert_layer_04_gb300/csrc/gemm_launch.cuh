@@ -20,7 +20,7 @@ moe_status launch_gemm(GemmParams &p, int max_tiles, cudaStream_t st) {
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
     const int threads = ModeTraits<MODE>::THREADS;
     if (!attr_set[dev]) {
-        const int smem_max = (int)gemm_smem_bytes<BN, MODE>(kMaxGroups);
+        const int smem_max = (int)gemm_smem_bytes<BN, MODE, CL>(kMaxGroups);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem_max);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -48,7 +48,7 @@ moe_status launch_gemm(GemmParams &p, int max_tiles, cudaStream_t st) {
     p.status = device_status_ptr();
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
-    const size_t smem = gemm_smem_bytes<BN, MODE>(ModeTraits<MODE>::DENSE ? 0 : p.G);
+    const size_t smem = gemm_smem_bytes<BN, MODE, CL>(ModeTraits<MODE>::DENSE ? 0 : p.G);
     if constexpr (CL == 1) {
         const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
         kern<<<grid, threads, smem, st>>>(p);
@@ -74,5 +74,17 @@ moe_status launch_gemm(GemmParams &p, int max_tiles, cudaStream_t st) {
 
 // Upper bound of the 128-row tiles of R rows split into G groups.
 inline int row_tile_bound(int max_rows, int G) { return (max_rows + 127) / 128 + G; }
+
+// The same for pairs of 128-row tiles (2-SM MMAs).
+inline int row_pair_bound(int max_rows, int G) { return (max_rows + 255) / 256 + G; }
+
+// Which grouped GEMMs may run as 2-SM pairs (bit GM_x; moe_set_gemm_pairs).
+int gemm_pair_modes();
+
+// Row-grouped GEMMs pair their tiles when groups hold many row tiles: a
+// group with an odd tile count leaves half of its last pair idle.
+inline bool rows_pair(int mode, int max_rows, int G) {
+    return (gemm_pair_modes() >> mode & 1) && (long long)max_rows >= 1024LL * G;
+}
 
 }  // namespace moe

@@ -109,3 +109,11 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
 moe_status launch_selftest_timeout(long long limit, cudaStream_t st);
 
 }  // namespace moe
+
+namespace moe {
+// the MOE_PAIR_* bits of moe.h are the GemmMode values
+static_assert(MOE_PAIR_EXPERT_GEMM1 == 1 << GM_FFN1 && MOE_PAIR_EXPERT_GEMM2 == 1 << GM_FFN2 &&
+                  MOE_PAIR_DGRAD2 == 1 << GM_DGRAD2 && MOE_PAIR_DGRAD1 == 1 << GM_DGRAD1 &&
+                  MOE_PAIR_WGRAD == 1 << GM_WGRAD,
+              "pair bits follow the matmul modes");
+}  // namespace moe

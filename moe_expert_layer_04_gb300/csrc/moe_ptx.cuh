@@ -106,15 +106,16 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *t
         : "memory");
 }
 
-// 2-D tiled copy global -> shared of every CTA in `mask` of the cluster (same
-// shared-memory offset and mbarrier offset in each); each destination CTA's
-// mbarrier receives the transaction bytes of its own copy.
-__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const CUtensorMap *tm,
-                                               uint64_t *bar, int c0, int c1, uint16_t mask) {
+// The same copy into this CTA's shared memory, with its completion signalled
+// on an mbarrier of the even CTA of a 2-SM pair (`bar`: a shared::cluster
+// address from dsmem_map).  The pair's MMA issuer then waits on one barrier
+// for both CTAs' operand halves.
+__device__ __forceinline__ void tma_load_2d_pairbar(void *smem_dst, const CUtensorMap *tm,
+                                                    uint32_t bar, int c0, int c1) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
 
@@ -322,11 +323,49 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
         : "memory");
 }
 
-// Arrives once on the mbarrier at the same offset in every CTA of `mask`
-// when every tcgen05 operation this thread issued before has completed.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
+// ------------------------------------------- tcgen05, CTA pairs (2-SM MMA)
+//
+// With .cta_group::2 the two CTAs of a cluster pair share one MMA of M = 256:
+// CTA r holds rows [128 r, 128 r + 128) of A and half of the N columns of B
+// in its own shared memory (same offsets in both CTAs), and receives its 128
+// rows of D, all N columns, in its own TMEM.  The even CTA issues the MMA.
+// Every tcgen05 instruction of a kernel that uses the pair form carries
+// .cta_group::2: the allocation is made by one warp of each CTA together and
+// gives both the same TMEM columns.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T, M = 256.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on the mbarrier at the same offset in each CTA of `mask` (bit
+// r = CTA r of the pair) when every pair MMA this thread issued before has
+// completed.  This is a completion signal to barriers, not a data copy.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }

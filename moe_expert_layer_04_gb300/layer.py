@@ -223,7 +223,11 @@ class MoELayer:
         return self.y if y is None else y
 
     # ----------------------------------------------------------- backward
-    def backward(self, dY, want_dlogits=False, want_dweights=False, stream=None):
+    def backward(self, dY, want_dlogits=False, want_dweights=False, stream=None,
+                 stage_events=None):
+        """Backward of the last forward; returns dX.  stage_events: optional
+        list of MOE_BWD_STAGES + 1 torch.cuda.Event (recorded once before) that
+        the library records around each of its stages."""
         D = self.dims
         if not self.backward_enabled:
             raise RuntimeError("layer built without backward buffers")
@@ -241,7 +245,8 @@ class MoELayer:
                     gu_save=None if self.recompute else self.gu_save,
                     dY=dY, dX=self.dX, dW_g=self.dW_g, dW13=self.dW13, dW2=self.dW2,
                     dlogits=self.dlogits if want_dlogits else None,
-                    dweights=self.dweights if want_dweights else None, ws=self.ws)
+                    dweights=self.dweights if want_dweights else None, ws=self.ws,
+                    stage_events=stage_events)
         _lib.moe_backward(args, stream)
         return self.dX
 
