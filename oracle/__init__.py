@@ -79,6 +79,7 @@ def _load():
                                         _I, _I, _P, _I, _I, _I, _I, _D, _D, _I,
                                         _P, _P, _P], None),
                 "orc_rows_dA": ([_P, _P, _I, _I, _P, _P, _I, _I, _P], None),
+                "orc_gate_wgrad_rows": ([_P, _I, _P, _I, _P, _I, _I, _I, _P, _P], None),
                 "orc_wgrad2_entries_given_h": ([_P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _P, _P,
                                                 _P], None),
                 "orc_expert_wgrad": ([_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _D, _I,
@@ -282,6 +283,21 @@ def layer_backward(x, W_g, W13, W2, dY, bias, k, rho, clamp, is_vision=None, mod
                                _ptr(tk), d, E, k, I, float(rho), float(clamp), int(exact),
                                _ptr(dX), _ptr(dz), _ptr(dw))
     return dict(dX=dX, dz=dz, dw=dw)
+
+
+def gate_wgrad_rows(x, dz, rows, tok=None):
+    """Rows of the gate weight gradient, dW_g[e] = sum_t dz[t, e] x[t] for each
+    expert e in `rows`, over the tokens of dz [n, E] (x rows tok, or 0..n-1)."""
+    (xn,), bf = _floats(x)
+    d = xn.shape[1]
+    dzn = np.ascontiguousarray(_to_np(dz), dtype=np.float64)
+    n, E = dzn.shape
+    tk, _ = _tok(tok, n)
+    rr = np.ascontiguousarray(rows, dtype=np.int32)
+    out = np.empty((rr.shape[0], d), np.float64)
+    _load().orc_gate_wgrad_rows(_ptr(xn), bf, _ptr(dzn), n, _ptr(tk), d, E, rr.shape[0], _ptr(rr),
+                                _ptr(out))
+    return out
 
 
 def rows_dA(dY, W2, row_tok, row_exp):

@@ -495,6 +495,28 @@ void orc_layer_backward(const void *x, const void *Wg, const void *W13, const vo
     free(z); free(ids); free(w); free(ssel); free(margin);
 }
 
+/* Rows of the gate weight gradient.  The gate projection z = x W_g^T (+ a
+ * constant offset) is an ordinary matmul ([HP41] §2.3 MegaGate), so by the
+ * chain rule
+ *   dW_g[e, i] = sum_t dz[t, e] x[t, i]
+ * over every token t.  Here for the experts rows[0..n_rows) and the n listed
+ * tokens (x row tok[r], NULL = tokens 0..n-1), with dz[n, E] given.  One
+ * fp64 sum per entry, tokens in order. */
+void orc_gate_wgrad_rows(const void *x, int bf, const double *dz, int n, const int64_t *tok,
+                         int d, int E, int n_rows, const int32_t *rows, double *out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int j = 0; j < n_rows; ++j)
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int r = 0; r < n; ++r) {
+                size_t t = tok ? (size_t)tok[r] : (size_t)r;
+                acc += dz[(size_t)r * E + rows[j]] * ld(x, t * d + i, bf);
+            }
+            out[(size_t)j * d + i] = acc;
+        }
+}
+
 /* Gradient reaching the SwiGLU output of one expert row, before the routing
  * weight (the first product of the expert backward):
  *   dA[r, i] = sum_m dY[t_r, m] W2[e_r][m, i]          (length I per row)

@@ -34,3 +34,29 @@ def assert_close(got, ref, what, rel_fro=REL_FRO, max_abs=MAX_ABS):
 
 def cpu(t):
     return t.detach().cpu()
+
+
+def bf16_ulp(v):
+    """Spacing of bf16 values at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np64(v)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def assert_close_rounded(got, ref, what, rel_fro=REL_FRO, max_abs=MAX_ABS, max_flip_frac=1e-3):
+    """A bf16 intermediate that both sides round from sums taken in a different
+    order (fp32 on the GPU, fp64 in the oracle): where the two sums straddle a
+    rounding boundary the values sit one bf16 step apart, which for values of
+    magnitude 8 or more exceeds the 5e-2 bound.  Each element must lie within
+    max(max_abs, one bf16 step of the reference); at most max_flip_frac of the
+    elements may exceed max_abs at all; relative Frobenius as usual."""
+    g, r = np64(got), np64(ref)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    diff = np.abs(g - r)
+    rel = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
+    bound = np.maximum(max_abs, bf16_ulp(r) * (1 + 1e-6))
+    worst = float(np.max(diff / bound)) if diff.size else 0.0
+    flips = float(np.mean(diff > max_abs)) if diff.size else 0.0
+    assert rel <= rel_fro and worst <= 1.0 and flips <= max_flip_frac, \
+        (f"{what}: rel Frobenius {rel:.3e} (<= {rel_fro}), worst |diff| / max({max_abs}, one "
+         f"bf16 step) {worst:.3f} (<= 1), elements beyond {max_abs}: {flips:.2e}")
+    return rel, float(diff.max()) if diff.size else 0.0

@@ -14,7 +14,7 @@ import oracle
 from moe_expert_layer_04_gb300 import _lib
 from moe_expert_layer_04_gb300 import workloads as W
 from moe_expert_layer_04_gb300.layer import MOE_ROUTE_HASH, MOE_ROUTE_TOPK, Dims, MoELayer
-from tests.helpers import W_RTOL, assert_close, cpu, np64
+from tests.helpers import W_RTOL, assert_close, assert_close_rounded, cpu, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -164,8 +164,8 @@ def test_forward_layer(name):
     x, W13, W2 = cpu(inp["x"]), cpu(inp["W13"]), cpu(inp["W2"])
     rt, grp, rw = _rows_meta(layer, w)
     h_ref, y_ref = oracle.expert_rows(x, W13, W2, rt, grp, rw, w.clamp)
-    assert_close(layer.h_perm, h_ref, f"{name} h")
-    assert_close(layer.y_perm, y_ref, f"{name} y_perm")
+    assert_close_rounded(layer.h_perm, h_ref, f"{name} h")
+    assert_close_rounded(layer.y_perm, y_ref, f"{name} y_perm")
     # combine: y[t] = shared row + the token's k routed rows
     sr = cpu(layer.slot_row).numpy().reshape(w.T, w.k)
     y_comb = y_ref[w.S + np.arange(w.T)] + y_ref[sr].sum(1)
@@ -202,7 +202,7 @@ def test_backward_layer(name, recompute):
     assert_close(layer.dX, ref["dX"], f"{name} dX")
     assert_close(layer.dweights, ref["dw"], f"{name} dw", max_abs=5e-2 * max(1, np.abs(ref["dw"]).max() / 10))
     assert_close(layer.dlogits, ref["dz"], f"{name} dlogits")
-    assert_close(layer.dW_g, ref["dz"].T @ np64(x), f"{name} dW_g")
+    assert_close(layer.dW_g, oracle.gate_wgrad_rows(x, ref["dz"], np.arange(w.E)), f"{name} dW_g")
     rt, grp, rw = _rows_meta(layer, w)
     offs = cpu(layer.offsets).numpy()
     counts = np.diff(offs)
@@ -212,6 +212,58 @@ def test_backward_layer(name, recompute):
         g = oracle.expert_wgrad(x, W13, W2, dY, e, rt[rows], rw[rows], w.clamp, store_bf16=True)
         assert_close(layer.dW13[e], g["dW13"], f"{name} dW13[{e}]")
         assert_close(layer.dW2[e], g["dW2"], f"{name} dW2[{e}]")
+
+
+@pytest.mark.parametrize("recompute", [False, True])
+def test_backward_layer_hash_router(recompute):
+    # the backward of the hash router: experts from tid2eid[input_ids], weights
+    # from the sigmoid of the gate logits at those experts (bias unused)
+    w = W.Workload("mid_hash", 400, 256, 24, 4, 192, 2.5, vision_frac=0.25, hash_variant=True)
+    layer, inp = make_layer(w, backward=True, recompute=recompute)
+    layer.forward(inp["x"], inp["bias"], inp["is_vision"], None, mode=MOE_ROUTE_HASH,
+                  input_ids=inp["input_ids"], tid2eid=inp["tid2eid"])
+    layer.backward(inp["dY"], want_dlogits=True, want_dweights=True)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    x, Wg, W13, W2, dY = (cpu(inp[k]) for k in ("x", "W_g", "W13", "W2", "dY"))
+    hk = dict(is_vision=cpu(inp["is_vision"]), mode=1, input_ids=cpu(inp["input_ids"]),
+              tid2eid=cpu(inp["tid2eid"]))
+    fwd = oracle.layer_forward(x, Wg, W13, W2, cpu(inp["bias"]), w.k, w.rho, w.clamp, **hk)
+    np.testing.assert_array_equal(fwd["ids"], cpu(layer.ids).numpy())
+    np.testing.assert_array_equal(fwd["ids"], cpu(inp["tid2eid"]).numpy()[cpu(inp["input_ids"]).numpy()])
+    ref = oracle.layer_backward(x, Wg, W13, W2, dY, cpu(inp["bias"]), w.k, w.rho, w.clamp, **hk)
+    assert_close(layer.dX, ref["dX"], "hash dX")
+    assert_close(layer.dweights, ref["dw"], "hash dw",
+                 max_abs=5e-2 * max(1, np.abs(ref["dw"]).max() / 10))
+    assert_close(layer.dlogits, ref["dz"], "hash dlogits")
+    assert_close(layer.dW_g, oracle.gate_wgrad_rows(x, ref["dz"], np.arange(w.E)), "hash dW_g")
+    rt, grp, rw = _rows_meta(layer, w)
+    offs = cpu(layer.offsets).numpy()
+    counts = np.diff(offs)
+    for e in sorted({int(np.argmax(counts[:w.E])), int(np.argmin(counts[:w.E])), w.E}):
+        rows = np.arange(offs[e], offs[e + 1])
+        g = oracle.expert_wgrad(x, W13, W2, dY, e, rt[rows], rw[rows], w.clamp, store_bf16=True)
+        assert_close(layer.dW13[e], g["dW13"], f"hash dW13[{e}]")
+        assert_close(layer.dW2[e], g["dW2"], f"hash dW2[{e}]")
+
+
+def test_zero_routed_scaling_gives_zero_routing_gradients():
+    # with scaling 0 every routing weight is 0: y is the shared expert alone,
+    # and the routing chain passes no gradient (and no NaN) to the logits
+    w = W.scaled(CASES["mid_I192"], name="rho0", rho=0.0)
+    layer, inp = make_layer(w, backward=True)
+    layer.forward(inp["x"], inp["bias"], inp["is_vision"], inp["logit_offset"])
+    layer.backward(inp["dY"], want_dlogits=True, want_dweights=True)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    assert torch.count_nonzero(layer.weights).item() == 0
+    assert torch.count_nonzero(layer.dlogits).item() == 0
+    assert torch.count_nonzero(layer.dW_g).item() == 0
+    assert bool(torch.isfinite(layer.dX).all()) and bool(torch.isfinite(layer.dweights).all())
+    x, Wg, W13, W2, dY = (cpu(inp[k]) for k in ("x", "W_g", "W13", "W2", "dY"))
+    ref = oracle.layer_backward(x, Wg, W13, W2, dY, cpu(inp["bias"]), w.k, w.rho, w.clamp,
+                                is_vision=cpu(inp["is_vision"]))
+    assert_close(layer.dX, ref["dX"], "rho0 dX")
 
 
 def test_empty_expert_gets_zero_grad():

@@ -353,7 +353,8 @@ def test_backward_finite_differences(clamp, mode):
     for _ in range(6):
         idx = (rng.integers(T), rng.integers(d))
         np.testing.assert_allclose(bwd["dX"][idx], _fd(c, "x", idx), **tol)
-    dWg = bwd["dz"].T @ c["x"]
+    # the gate weight gradient from the oracle's own reduction routine
+    dWg = oracle.gate_wgrad_rows(c["x"], bwd["dz"], np.arange(c["E"]))
     for _ in range(6):
         idx = (rng.integers(c["E"]), rng.integers(d))
         np.testing.assert_allclose(dWg[idx], _fd(c, "Wg", idx), **tol)
@@ -378,6 +379,26 @@ def test_backward_finite_differences(clamp, mode):
                                exact=True)
     ref = (yj.reshape(T, c["k"], d) * c["dY"][:, None, :]).sum(-1)
     np.testing.assert_allclose(bwd["dw"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gate_wgrad_rows_is_the_transposed_product():
+    # dW_g rows = dz^T x (a library matmul), for all tokens and for a listed
+    # subset whose dz rows are given in the listed order; bf16 x bits and
+    # fp64 x give the same sums
+    rng = np.random.default_rng(12)
+    T, d, E = 37, 20, 9
+    x = torch.randn(T, d, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    xd = x.double()
+    dz = rng.standard_normal((T, E)) * (rng.random((T, E)) < 0.4)
+    rows = np.array([8, 0, 3, 3], np.int32)
+    ref = torch.from_numpy(dz).T.matmul(xd).numpy()[rows]
+    np.testing.assert_allclose(oracle.gate_wgrad_rows(x, dz, rows), ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle.gate_wgrad_rows(xd.numpy(), dz, rows), ref, rtol=1e-13,
+                               atol=1e-13)
+    tok = np.array([30, 2, 11, 5])
+    sub = torch.from_numpy(dz[:4]).T.matmul(xd[torch.from_numpy(tok)]).numpy()[rows]
+    np.testing.assert_allclose(oracle.gate_wgrad_rows(x, dz[:4], rows, tok=tok), sub,
+                               rtol=1e-13, atol=1e-13)
 
 
 def test_wgrad_entries_match_full_and_bf16_storage():

@@ -60,3 +60,25 @@ def test_noalloc_rejects_sizes_beyond_its_array():
         _lib.moe_permute_noalloc(small, None, None, 70000, 128, 1024, 8, small, small, small,
                                  small, None, None)
     assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_at_its_size_limit():
+    # ceil(32768 * 8 / 256) * 1024 = 2^20 histogram entries: exactly the whole
+    # array; one more token is one chunk too many
+    T, E, k, d = 32768, 1024, 8, 8
+    ids = W.random_ids(T, E, k, seed=5).cuda()
+    wts = torch.rand(T, k, device="cuda")
+    x = W.normal_bf16((T, d), 1.0, 0, "noalloc_limit", "cuda")
+    got = _dispatch(True, ids, wts, x, T, d, E, k)
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    ref = _dispatch(False, ids, wts, x, T, d, E, k)
+    for name in ref:
+        a, b = got[name], ref[name]
+        if a.dtype == torch.bfloat16:
+            a, b = a.view(torch.int16), b.view(torch.int16)
+        assert torch.equal(a, b), f"{name} differs at the size limit"
+    ids1 = torch.zeros(T + 1, k, dtype=torch.int32, device="cuda")
+    with pytest.raises(_lib.MoeError) as ei:
+        _lib.moe_permute_noalloc(ids1, None, None, T + 1, d, E, k, *[torch.zeros(
+            16, dtype=torch.int32, device="cuda") for _ in range(4)], None, None)
+    assert ei.value.status == _lib.MOE_ERR_UNSUPPORTED
