@@ -2,14 +2,18 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-A step is one forward pass of the whole layer (gate projection + routing,
-dispatch, the two grouped expert GEMMs with the shared expert, combine) over
-one batch of the full-width workload (T=4096 tokens, d=4096, 384 routed
-experts top-6 + 1 shared, I=2048, bf16).  Inputs are seeded synthetic tensors
-made on the device; they are resident in HBM when the timed region starts.
-The forward+backward of the T=8192 workload is measured as well and reported
-under "fwd_bwd".  N > 1 runs N independent replicas (one per GPU), since the
-single-GPU layer has no exchange step: value = all ranks' tokens / max time.
+The headline step is one forward + backward pass of the whole layer over the
+largest single-GPU workload: a 64K-token slice of a 1M-token sequence (T =
+65536, d = 4096, 384 routed experts top-6 + 1 shared, I = 2048, bf16 with
+fp32 accumulation and fp32 weight gradients, 30 % vision tokens with their
+own routing bias, Zipf(1.1) expert load, g|u recomputed in the backward).
+Inputs are seeded synthetic tensors made on the device; they are resident in
+HBM when the timed region starts.  The line also carries the same step end to
+end from host memory (moe_layer_step_host), the full-width T = 4096 forward,
+the T = 8192 forward + backward, the skewed multimodal forward (top-k and
+hash routers) and the MXFP8 forward.  N > 1 runs N independent replicas (one
+per GPU), since the single-GPU layer has no exchange step: value = all
+ranks' tokens / max time.
 
 --impl reference times the CPU oracle (the plain fp64 implementation the
 tests compare against) on the host cores, on a bounded sample of tokens of
@@ -272,32 +276,104 @@ def kernel_metrics(D, counts, per, hbm, bf16, save_gu=False, fused_route=True, m
 def run_ours(args, rank, world, local_rank):
     from moe_expert_layer_04_gb300 import _lib
     from moe_expert_layer_04_gb300 import workloads as W
-    from moe_expert_layer_04_gb300.layer import Dims, HostPipeline, MoELayer, ffn_fused_supported
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     _lib.load()
     hbm, bf16, bf16_sus, peak_src = peaks()
+    # the full-width expert weights (same seed and shapes for every full-width
+    # workload)
+    weights = {k: v for k, v in layer_inputs(W.WORKLOADS["full_fwd"], dev).items()
+               if k in ("W_g", "W13", "W2")}
 
-    wl = workload(args)
-    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
-    inp = layer_inputs(wl, dev)
-    weights = {k: inp[k] for k in ("W_g", "W13", "W2")}
-    layer = MoELayer(D, weights, wl.rho, wl.clamp)
-    stream = torch.cuda.current_stream()
-
-    # warm-up passes (they also give the expert load), then the timed region
-    forward_breakdown(layer, inp, 1, args.warmup)
-    counts = layer.counts.cpu().numpy()
-    assert _lib.moe_last_device_status() == _lib.MOE_OK
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    per, ms_step = forward_breakdown(layer, inp, args.steps, 1, world=world)
+    h = run_headline(args, weights, dev, world, hbm, bf16_sus)
+    e2e = run_headline_e2e(args, h, world)
+    wl, D = h["wl"], h["D"]
+    ms_step = h["ms_step"]
     value = replica_throughput(world, D.T, ms_step)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline_fwd_bwd(h["inp"], wl, args.cpu_tokens, args.cpu_rows)
+    counts = h["counts"]
+    kernels, roofline = h["kernels"], h["roofline"]
+    layer_roof_ms, alg_flops, launches = h["layer_roof_ms"], h["alg_flops"], h["launches"]
+    del h
+    torch.cuda.empty_cache()
+
+    full = fb = extra = mx = None
+    if not args.no_extra and not args.tokens and not args.experts:
+        full = run_full_fwd(args, weights, dev, world, hbm, bf16, peak_src)
+        if not args.no_bwd:
+            fb = run_fwd_bwd(args, weights, dev, world)
+        extra = run_extra_workloads(args, weights, dev, world, hbm, bf16)
+        if not args.no_mx:
+            mx = run_mx(args, weights, dev, world, hbm, bf16, ["full_fwd", HEADLINE])
+            if full is not None and "full_fwd" in mx:
+                mx["full_fwd"]["speedup_vs_bf16"] = round(
+                    full["ms_per_step"] / mx["full_fwd"]["ms_per_step"], 3)
+    clk = clocks.stop()
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": {"workload": workload_string(wl),
+                   "global_batch": wl.T * world, "seq_len": wl.T,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.1f GB of expert weights, %.1f GB of fp32 "
+                         "weight gradients per step)" % (3 * (D.E + 1) * D.d * D.I * 2 / 1e9,
+                                                         3 * (D.E + 1) * D.d * D.I * 4 / 1e9)},
+        "roofline": roofline,
+        "layer_roofline_ms": round(layer_roof_ms, 4),
+        "layer_roofline_frac": round(layer_roof_ms / ms_step, 4),
+        "layer_roofline_basis": "algorithmic FLOPs of forward + backward (%.1f TFLOP, the "
+                                "recompute not counted) at the sustained bf16 peak" % (
+                                    alg_flops / 1e12),
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+        "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
+                        "min_rows": int(counts.min()), "max_rows": int(counts.max())},
+        "full_fwd": full,
+        "fwd_bwd": fb,
+        "extra_workloads": extra,
+        "mx_fwd": mx,
+    }
+    return line
+
+
+def workload_string(wl):
+    return (f"{wl.name}: forward+backward, T={wl.T} d={wl.d} E={wl.E} routed top-{wl.k} + 1 "
+            f"shared, I={wl.I}, scaling {wl.rho}, clamp {wl.clamp}, "
+            f"{round(100 * wl.vision_frac)}% vision tokens, Zipf({wl.zipf_s}) expert load, "
+            f"fp32 weight gradients" + (", g|u recomputed in the backward" if wl.recompute else ""))
+
+
+def run_full_fwd(args, weights, dev, world, hbm, bf16, peak_src):
+    """The full-width forward (T = 4096, near-uniform load): per-call
+    breakdown, the weight-streaming roofline of expert GEMM 1, the forward
+    through HostPipeline, the literal-bias variant and one launch vs two for
+    the expert matmuls."""
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import Dims, HostPipeline, MoELayer, ffn_fused_supported
+    wl = W.WORKLOADS["full_fwd"]
+    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+    inp = layer_inputs(wl, dev, weights=weights)
+    layer = MoELayer(D, weights, wl.rho, wl.clamp)
+    stream = torch.cuda.current_stream()
+    forward_breakdown(layer, inp, 1, args.warmup)
+    counts = layer.counts.cpu().numpy()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    per, ms_step = forward_breakdown(layer, inp, args.steps, 1, world=world)
     kernels, g1_bytes, layer_roof_ms = kernel_metrics(D, counts, per, hbm, bf16,
                                                       fused_route=layer.fused_route)
-    fused = layer.fused_route
     achieved = kernels["expert_gemm1"]["gbs"]
     roofline = {"kernel": "expert_gemm1 (grouped GEMM 1 + clamped SwiGLU)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -305,8 +381,6 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": round(g1_bytes * GEMM1_DRAM_PER_ALGORITHMIC_BYTE),
                 "traffic_source": "ncu dram read+write of a T=640/E=64 launch, scaled by bytes",
                 "peak_source": peak_src, "bytes_per_launch": g1_bytes}
-
-    # ---------------- both expert matmuls: two launches vs one persistent launch
     ffn_launch = None
     if ffn_fused_supported(D.d, D.I):
         ffn_launch = {}
@@ -326,104 +400,56 @@ def run_ours(args, rank, world, local_rank):
                 f0.elapsed_time(f1) / args.steps, 4)
         layer.fused_ffn = False
         assert _lib.moe_last_device_status() == _lib.MOE_OK
-
-    # ---------------- the same forward with the literal U(-0.1, 0.1) routing bias
-    literal = None
-    if wl.bias_amp != 0.1 and not args.tokens and not args.experts:
-        lw = W.scaled(wl, name=wl.name + "_bias0.1", bias_amp=0.1)
-        lbias = W.make_inputs(lw, device=dev, with_weights=False)["bias"]
-        for _ in range(args.warmup):
-            layer.forward(inp["x"], lbias, inp["is_vision"], inp["logit_offset"])
-        torch.cuda.synchronize()
-        l0 = torch.cuda.Event(enable_timing=True)
-        l1 = torch.cuda.Event(enable_timing=True)
-        l0.record(stream)
-        for _ in range(args.steps):
-            layer.forward(inp["x"], lbias, inp["is_vision"], inp["logit_offset"])
-        l1.record(stream)
-        torch.cuda.synchronize()
-        lms = l0.elapsed_time(l1) / args.steps
-        lc = layer.counts.cpu().numpy()
-        literal = {"workload": f"{lw.name}: bias ~ U(-0.1, 0.1)",
-                   "value": round(replica_throughput(world, D.T, lms), 1), "unit": "tokens/s",
-                   "ms_per_step": round(lms, 4), "experts_with_tokens": int((lc > 0).sum()),
-                   "max_rows_per_expert": int(lc.max())}
-
-    # ---------------- end to end through the public API with host buffers: every
-    # step copies its input batch in from pinned host memory and its output out;
-    # HostPipeline overlaps those copies with the neighbouring steps' compute
+    # the same forward with the literal U(-0.1, 0.1) routing bias
+    lw = W.scaled(wl, name=wl.name + "_bias0.1", bias_amp=0.1)
+    lbias = W.make_inputs(lw, device=dev, with_weights=False)["bias"]
+    for _ in range(args.warmup):
+        layer.forward(inp["x"], lbias, inp["is_vision"], inp["logit_offset"])
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(args.steps):
+        layer.forward(inp["x"], lbias, inp["is_vision"], inp["logit_offset"])
+    l1.record(stream)
+    torch.cuda.synchronize()
+    lms = l0.elapsed_time(l1) / args.steps
+    lc = layer.counts.cpu().numpy()
+    literal = {"workload": f"{lw.name}: bias ~ U(-0.1, 0.1)",
+               "value": round(replica_throughput(world, D.T, lms), 1), "unit": "tokens/s",
+               "ms_per_step": round(lms, 4), "experts_with_tokens": int((lc > 0).sum()),
+               "max_rows_per_expert": int(lc.max())}
+    # forward passes over host batches: HostPipeline overlaps each batch's
+    # copies with the neighbouring batches' compute
     x_host = inp["x"].cpu().pin_memory()
     y_host = [torch.empty(D.T, D.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     pipe = HostPipeline(layer)
     route_args = (inp["bias"], inp["is_vision"], inp["logit_offset"])
     pipe.run([x_host] * args.warmup, [y_host[i % 2] for i in range(args.warmup)], *route_args)
     torch.cuda.synchronize()
-    dist_barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     pipe.run([x_host] * args.steps, [y_host[i % 2] for i in range(args.steps)], *route_args)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = dist_max(e0.elapsed_time(e1) / args.steps, world)
-    e2e = {"value": round(replica_throughput(world, D.T, e2e_ms), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": D.T * D.d * 2, "d2h_bytes_per_step": D.T * D.d * 2,
-           "ms_per_step": round(e2e_ms, 4),
-           "copies": "overlapped with the neighbouring steps (two copy streams, double buffers)"}
-    del layer, x_host, y_host, pipe
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    out = {"workload": f"{wl.name}: forward, T={wl.T} d={wl.d} E={wl.E} routed top-{wl.k} + 1 "
+                       f"shared, I={wl.I}, bias U(-0.01, 0.01)",
+           "value": round(replica_throughput(world, D.T, ms_step), 1), "unit": "tokens/s",
+           "ms_per_step": round(ms_step, 4), "roofline": roofline,
+           "layer_roofline_ms": round(layer_roof_ms, 4),
+           "layer_roofline_frac": round(layer_roof_ms / ms_step, 4), "kernels": kernels,
+           "host_pipeline": {"value": round(replica_throughput(world, D.T, e2e_ms), 1),
+                             "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
+                             "h2d_bytes_per_step": D.T * D.d * 2,
+                             "d2h_bytes_per_step": D.T * D.d * 2},
+           "literal_bias": literal, "expert_ffn_launches": ffn_launch,
+           "routing": ("one kernel: gate projection + top-k + per-modality load (moe_gate_route)"
+                       if layer.fused_route else "gate GEMM, then the routing kernel (moe_route)"),
+           "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
+                           "min_rows": int(counts.min()), "max_rows": int(counts.max())}}
+    del layer, pipe, x_host, y_host, inp
     torch.cuda.empty_cache()
-
-    # ---------------- forward + backward (T=8192 workload, same weights)
-    fb = None
-    if not args.no_bwd:
-        fb = run_fwd_bwd(args, weights, dev, world)
-
-    # ---------------- the other full-width workloads (same weights)
-    extra = None
-    if not args.no_extra and not args.tokens and not args.experts:
-        extra = run_extra_workloads(args, weights, dev, world, hbm, bf16)
-    # ---------------- the MXFP8 forward (same weights, quantised once)
-    mx = None
-    if not args.no_mx and not args.tokens and not args.experts:
-        names = ["full_fwd"] + ([] if args.no_extra else ["long_slice_fwd_bwd"])
-        mx = run_mx(args, weights, dev, world, hbm, bf16, names)
-        if "full_fwd" in mx:
-            mx["full_fwd"]["speedup_vs_bf16"] = round(ms_step / mx["full_fwd"]["ms_per_step"], 3)
-    clk = clocks.stop()
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(inp, wl, args.cpu_tokens)
-
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
-        "config": {"workload": f"{wl.name}: forward, T={wl.T} d={wl.d} E={wl.E} routed top-{wl.k}"
-                               f" + 1 shared, I={wl.I}, scaling {wl.rho}, clamp {wl.clamp}",
-                   "global_batch": wl.T * world, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (%.1f GB of expert weights streamed per step)"
-                         % (3 * (D.E + 1) * D.d * D.I * 2 / 1e9)},
-        "roofline": roofline,
-        "layer_roofline_ms": round(layer_roof_ms, 4),
-        "layer_roofline_frac": round(layer_roof_ms / ms_step, 4),
-        "kernels": kernels,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": fwd_launches(fused) * args.steps,
-        "routing": ("one kernel: gate projection + top-k + per-modality load (moe_gate_route)"
-                    if fused else "gate GEMM, then the routing kernel (moe_route)"),
-        "clocks": clk,
-        "fwd_bwd": fb,
-        "extra_workloads": extra,
-        "literal_bias": literal,
-        "mx_fwd": mx,
-        "expert_ffn_launches": ffn_launch,
-        "expert_load": {"experts_with_tokens": int((counts > 0).sum()),
-                        "min_rows": int(counts.min()), "max_rows": int(counts.max())},
-    }
-    return line
+    return out
 
 
 def run_mx(args, weights, dev, world, hbm, bf16, names):
@@ -480,15 +506,14 @@ def run_mx_only(args):
 
 
 def run_extra_workloads(args, weights, dev, world, hbm, bf16):
-    """Per-call numbers of the skewed multimodal workload (top-k and hash
-    routing) and of the 64K-token slice (forward breakdown, and forward +
-    backward with recompute).  These sizes are where the tensor-core and
-    HBM targets of the routing / dispatch / combine steps apply."""
+    """Per-call numbers of the skewed multimodal forward (top-k and hash
+    routing), one of the sizes where the HBM targets of the routing /
+    dispatch / combine steps apply."""
     from moe_expert_layer_04_gb300 import workloads as W
     from moe_expert_layer_04_gb300.layer import MOE_ROUTE_HASH, Dims, MoELayer
     steps = max(3, args.steps // 3)
     out = {}
-    for name, modes in (("skewed_mm_fwd", (0, MOE_ROUTE_HASH)), ("long_slice_fwd_bwd", (0,))):
+    for name, modes in (("skewed_mm_fwd", (0, MOE_ROUTE_HASH)),):
         wl = W.WORKLOADS[name]
         D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
         inp = layer_inputs(wl, dev, weights=weights)
@@ -570,6 +595,239 @@ def run_fwd_bwd(args, weights, dev, world, wl_name="fwd_bwd", inputs=None, wl=No
     return out
 
 
+# ------------------------------------------------ the headline step
+
+HEADLINE = "long_slice_fwd_bwd"
+FWD_CALLS = ["route", "permute", "expert_gemm1", "expert_gemm2", "combine"]
+
+
+def bwd_stage_work(D, counts):
+    """Algorithmic FLOPs and minimum HBM bytes of each moe_backward stage:
+    weights of every expert with rows read once, fp32 weight gradients
+    written once, each permuted activation read or written once."""
+    from moe_expert_layer_04_gb300 import _lib
+    used = int((counts > 0).sum()) + 1
+    R, S, T, d, I, E = D.R, D.S, D.T, D.d, D.I, D.E
+    w13, w2 = used * 2 * I * d * 2, used * d * I * 2
+    work = {
+        "recompute_gather": (0, T * d * 2 + R * d * 2),
+        "recompute_gemm1": (4 * R * d * I, w13 + R * d * 2 + R * 2 * I * 4),
+        "gather_dY": (0, T * d * 2 + R * d * 2),
+        "dgrad2": (2 * R * d * I, w2 + R * d * 2 + R * 2 * I * 4 + R * 2 * I * 2 + R * I * 2),
+        "wgrad2": (2 * R * d * I, (E + 1) * d * I * 4 + R * d * 2 + R * I * 2),
+        "dgrad1": (4 * R * I * d, w13 + R * 2 * I * 2 + R * d * 2),
+        "wgrad1": (4 * R * I * d, (E + 1) * 2 * I * d * 4 + R * 2 * I * 2 + R * d * 2),
+        "router_bwd": (0, S * 4 * 6 + T * E * 4),
+        "dX": (2 * S * d, R * d * 2 + T * d * 2 + S * 8),
+        "dW_g": (2 * S * d, S * d * 2 + E * d * 4),
+    }
+    assert list(work) == _lib.MOE_BWD_STAGE_NAMES
+    return work
+
+
+def stage_metrics(ms, flops, nbytes, hbm, tflops_peak):
+    sec = ms / 1e3
+    m = {"ms": round(ms, 4), "gbs": round(nbytes / sec / 1e9, 1),
+         "hbm_frac": round(nbytes / sec / 1e9 / hbm, 4)}
+    if flops:
+        m["tflops"] = round(flops / sec / 1e12, 1)
+        m["tensor_frac"] = round(flops / sec / 1e12 / tflops_peak, 4)
+    return m
+
+
+def oracle_fwd_bwd_sample(host, wl, n_tok, n_rows, rng):
+    """The oracle on a bounded sample of a forward + backward step: the
+    forward and the token-local backward (dX, logit and routing-weight
+    gradients) of n_tok seeded tokens, and the weight gradients of the shared
+    expert over n_rows seeded token rows (one output of each weight gradient,
+    as a full step writes it once per expert).  A token's share of a step is
+    its forward and local backward plus k + 1 weight-gradient rows (its k
+    routed experts and the shared one).  Returns (seconds of CPU work,
+    seconds per token)."""
+    import oracle
+    tok = np.sort(rng.choice(wl.T, size=min(n_tok, wl.T), replace=False))
+    rows = np.sort(rng.choice(wl.T, size=min(n_rows, wl.T), replace=False))
+    kw = dict(is_vision=host["is_vision"], offset=host["logit_offset"])
+    t0 = time.perf_counter()
+    oracle.layer_forward(host["x"], host["W_g"], host["W13"], host["W2"], host["bias"], wl.k,
+                         wl.rho, wl.clamp, tok=tok, **kw)
+    oracle.layer_backward(host["x"], host["W_g"], host["W13"], host["W2"], host["dY"],
+                          host["bias"], wl.k, wl.rho, wl.clamp, tok=tok, **kw)
+    t1 = time.perf_counter()
+    oracle.expert_wgrad(host["x"], host["W13"], host["W2"], host["dY"], wl.E, rows,
+                        np.ones(len(rows)), wl.clamp)
+    t2 = time.perf_counter()
+    per_tok = (t1 - t0) / len(tok) + (wl.k + 1) * (t2 - t1) / len(rows)
+    return t2 - t0, per_tok
+
+
+def cpu_baseline_fwd_bwd(inp, wl, n_tok, n_rows):
+    import oracle
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    oracle.build()
+    sec, per_tok = oracle_fwd_bwd_sample(host, wl, n_tok, n_rows, np.random.default_rng(0))
+    return {"value": round(1.0 / per_tok, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"forward + token-local backward of {n_tok} seeded tokens and the weight "
+                      f"gradients of the shared expert over {n_rows} seeded token rows of the "
+                      f"{wl.name} workload; a token costs its forward and local backward plus "
+                      f"k + 1 = {wl.k + 1} weight-gradient rows ({sec:.1f} s of CPU work, "
+                      f"OpenMP over tokens / output entries)"}
+
+
+def run_headline(args, weights, dev, world, hbm, bf16_sus):
+    """The headline: forward + backward of the 64K-token slice, with CUDA
+    events around each forward call and each backward stage."""
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+    wl = W.WORKLOADS[HEADLINE]
+    over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
+    if over:
+        wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()), **over)
+    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+    inp = layer_inputs(wl, dev, weights=weights)
+    layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True, recompute=wl.recompute)
+    stream = torch.cuda.current_stream()
+    nb = _lib.MOE_BWD_STAGES
+    off = inp["logit_offset"]
+
+    def events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)      # creates the CUDA event behind each
+        return evs
+
+    def step(fev=None, bev=None):
+        def mark(i):
+            if fev is not None:
+                fev[i].record(stream)
+        mark(0)
+        layer.route(inp["x"], inp["bias"], inp["is_vision"], off)
+        mark(1)
+        layer.dispatch(inp["x"])
+        mark(2)
+        layer.expert_gemm1()
+        mark(3)
+        layer.expert_gemm2()
+        mark(4)
+        layer.combine()
+        mark(5)
+        layer.backward(inp["dY"], stage_events=bev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    counts = layer.counts.cpu().numpy()
+    K = args.steps
+    fevs = [events(6) for _ in range(K)]
+    bevs = [events(nb + 1) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(fevs[i], bevs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    ms_step = dist_max(t0.elapsed_time(t1) / K, world)
+    fwd_ms = {n: sum(fevs[i][j].elapsed_time(fevs[i][j + 1]) for i in range(K)) / K
+              for j, n in enumerate(FWD_CALLS)}
+    bwd_ms = {n: sum(bevs[i][j].elapsed_time(bevs[i][j + 1]) for i in range(K)) / K
+              for j, n in enumerate(_lib.MOE_BWD_STAGE_NAMES)}
+
+    # per call / stage: algorithmic work against the sustained peaks (the
+    # kernels run inside a step of tens of milliseconds)
+    g1b, g2b = fwd_algorithmic_bytes(D, counts)
+    fwd_work = {"route": (2 * D.T * D.d * D.E, D.T * D.d * 2 + D.E * D.d * 2 + D.T * D.E * 4
+                          + D.T * D.k * 12),
+                "permute": (0, D.T * D.d * 2 + D.R * D.d * 2 + D.S * 4 * 6),
+                "expert_gemm1": (4 * D.R * D.d * D.I, g1b),
+                "expert_gemm2": (2 * D.R * D.I * D.d, g2b),
+                "combine": (0, D.R * D.d * 2 + D.T * D.d * 2 + D.S * 4)}
+    bwd_work = bwd_stage_work(D, counts)
+    kernels = {n: stage_metrics(fwd_ms[n], *fwd_work[n], hbm, bf16_sus) for n in FWD_CALLS}
+    kernels.update({"bwd_" + n: stage_metrics(bwd_ms[n], *bwd_work[n], hbm, bf16_sus)
+                    for n in _lib.MOE_BWD_STAGE_NAMES if bwd_ms[n] > 0})
+
+    # the dominant kernel: the grouped-GEMM kernel (template instance) with the
+    # largest share of the step
+    groups = {
+        "expert GEMM 1 (moe_gemm_kernel<GM_FFN1>: forward and the backward's recompute)":
+            (("fwd", "expert_gemm1"), ("bwd", "recompute_gemm1")),
+        "weight gradients (moe_gemm_kernel<GM_WGRAD>: dW2 and dW13)":
+            (("bwd", "wgrad2"), ("bwd", "wgrad1")),
+        "dgrad 1 (moe_gemm_kernel<GM_DGRAD1>)": (("bwd", "dgrad1"),),
+        "dgrad 2 + SwiGLU backward (moe_gemm_kernel<GM_DGRAD2>)": (("bwd", "dgrad2"),),
+        "expert GEMM 2 (moe_gemm_kernel<GM_FFN2>)": (("fwd", "expert_gemm2"),),
+    }
+    def tot(parts, what):
+        out = 0.0
+        for side, n in parts:
+            if side == "fwd":
+                out += fwd_ms[n] if what == "ms" else fwd_work[n][0]
+            else:
+                out += bwd_ms[n] if what == "ms" else bwd_work[n][0]
+        return out
+    name = max(groups, key=lambda g: tot(groups[g], "ms"))
+    g_ms, g_fl, n_launch = tot(groups[name], "ms"), tot(groups[name], "flops"), len(groups[name])
+    achieved = g_fl / (g_ms / 1e3) / 1e12
+    roofline = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": bf16_sus, "unit": "TFLOP/s", "frac": round(achieved / bf16_sus, 4),
+                "traffic": None, "launches_per_step": n_launch,
+                "flops_per_launch": int(g_fl / n_launch),
+                "ms_per_launch": round(g_ms / n_launch, 4),
+                "peak_source": "measured sustained bf16 (cuBLAS loop under the power cap)"}
+    alg_flops = (sum(fwd_work[n][0] for n in FWD_CALLS) +
+                 sum(f for n, (f, _) in bwd_work.items() if n != "recompute_gemm1"))
+    layer_roof_ms = alg_flops / (bf16_sus * 1e12) * 1e3
+    out = dict(wl=wl, D=D, inp=inp, layer=layer, ms_step=ms_step, kernels=kernels,
+               roofline=roofline, counts=counts, layer_roof_ms=layer_roof_ms,
+               alg_flops=alg_flops,
+               launches=fwd_launches(layer.fused_route) + BWD_LAUNCHES +
+               (BWD_RECOMPUTE_EXTRA if wl.recompute else 0))
+    return out
+
+
+def run_headline_e2e(args, h, world):
+    """The headline step end to end through moe_layer_step_host: x and dY
+    copied in from pinned host memory and y and dX copied back every step
+    (dY's upload overlaps the forward and y's download the backward)."""
+    layer, inp, D = h["layer"], h["inp"], h["D"]
+    stream = torch.cuda.current_stream()
+    x_h = inp["x"].cpu().pin_memory()
+    dY_h = inp["dY"].cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dX_h = torch.empty_like(x_h).pin_memory()
+    cs = torch.cuda.Stream()
+    route = (inp["bias"], inp["is_vision"], inp["logit_offset"])
+
+    def step():
+        layer.step_host(x_h, y_h, dY_h, dX_h, *route, copy_stream=cs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist_max(e0.elapsed_time(e1) / args.steps, world)
+    nb = D.T * D.d * 2
+    return {"value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": 2 * nb, "d2h_bytes_per_step": 2 * nb,
+            "ms_per_step": round(ms, 4),
+            "path": "moe_layer_step_host (C ABI, host x and dY in, host y and dX out every "
+                    "step; dY's upload overlaps the forward, y's download the backward)"}
+
+
 # --------------------------------------------- forward + backward alone
 
 def run_fwd_bwd_only(args):
@@ -641,61 +899,48 @@ def run_route_only(args):
 
 # -------------------------------------------------------------- oracle
 
-def cpu_baseline(inp, wl, n_tokens):
-    import oracle
-    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    rng = np.random.default_rng(0)
-    tok = np.sort(rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False))
-    oracle.build()
-    t = time.perf_counter()
-    oracle.layer_forward(host["x"], host["W_g"], host["W13"], host["W2"], host["bias"], wl.k,
-                         wl.rho, wl.clamp, is_vision=host["is_vision"],
-                         offset=host["logit_offset"], tok=tok)
-    dt = time.perf_counter() - t
-    return {"value": round(len(tok) / dt, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"forward of {len(tok)} seeded tokens of the {wl.name} workload "
-                      f"({dt:.1f} s, OpenMP over tokens)"}
-
-
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is a bounded sample."""
+    """The oracle as the reference arm: each step is a bounded sample of the
+    headline forward + backward (oracle_fwd_bwd_sample), its tokens/s the
+    sample's tokens over the CPU time they cost."""
     import oracle
     from moe_expert_layer_04_gb300 import workloads as W
     if rank != 0:
         return None
-    wl = workload(args)
+    wl = W.WORKLOADS[HEADLINE]
+    over = {k: v for k, v in (("T", args.tokens), ("E", args.experts)) if v}
+    if over:
+        wl = W.scaled(wl, name=wl.name + "-" + "-".join(f"{k}{v}" for k, v in over.items()), **over)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = layer_inputs(wl, dev)
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     del inp
+    if dev == "cuda":
+        torch.cuda.empty_cache()
     oracle.build()
-    n = args.ref_tokens
     rng = np.random.default_rng(1)
-
-    def step():
-        tok = np.sort(rng.choice(wl.T, size=n, replace=False))
-        oracle.layer_forward(host["x"], host["W_g"], host["W13"], host["W2"], host["bias"], wl.k,
-                             wl.rho, wl.clamp, is_vision=host["is_vision"],
-                             offset=host["logit_offset"], tok=tok)
-
+    n_tok, n_rows = args.ref_tokens, args.ref_rows
     for _ in range(args.warmup):
-        step()
-    t = time.perf_counter()
+        oracle_fwd_bwd_sample(host, wl, n_tok, n_rows, rng)
+    secs, per_tok = [], []
     for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t) / args.steps
-    value = round(n / dt, 2)
+        sec, pt = oracle_fwd_bwd_sample(host, wl, n_tok, n_rows, rng)
+        secs.append(sec)
+        per_tok.append(pt)
+    value = round(1.0 / statistics.mean(per_tok), 3)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: forward, T={wl.T} d={wl.d} E={wl.E} top-{wl.k} + "
-                               f"shared, I={wl.I}", "parallelism": "host cores"},
+        "ms_per_step": round(statistics.mean(secs) * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_string(wl), "global_batch": wl.T * world,
+                   "seq_len": wl.T, "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"each step: forward of {n} random tokens of the workload"},
+                         "sample": f"each step: forward + token-local backward of {n_tok} random "
+                                   f"tokens and the shared expert's weight gradients over "
+                                   f"{n_rows} random token rows; a token costs its forward and "
+                                   f"local backward plus k + 1 weight-gradient rows"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -707,13 +952,19 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="full_fwd")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="workload of the profiling modes (--route-only, --fwd-bwd-only, "
+                         "--mx-only)")
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the skewed and 64K-token workloads")
-    ap.add_argument("--cpu-tokens", type=int, default=1024)
-    ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--cpu-tokens", type=int, default=64,
+                    help="oracle baseline: tokens of the forward + local backward sample")
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="oracle baseline: shared-expert rows of the weight-gradient sample")
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling)")
     ap.add_argument("--route-only", action="store_true",

@@ -312,6 +312,61 @@ enum {
  * weight chain.  Clamp gradients pass where the argument equals the bound. */
 moe_status moe_backward(const moe_bwd_args *args, void *stream);
 
+/* ------------------------------------------------- whole layer from host
+ * One layer as everything a training step touches: its sizes and options,
+ * its weights and routing inputs, and every device buffer of the calls above
+ * (all allocated by the caller, as for those calls). */
+typedef struct {
+    int T, d, E, k, I;
+    float scaling, clamp;
+    int flags;                    /* MOE_FLAG_RECOMPUTE or 0 */
+    int mode;                     /* moe_route_mode */
+    const uint16_t *W_g;          /* [E,d] */
+    const uint16_t *W13;          /* [E+1,2I,d] */
+    const uint16_t *W2;           /* [E+1,d,I] */
+    const float *logit_offset;    /* [E] or NULL */
+    const float *bias;            /* [2,E] (top-k mode; row 0 text, row 1 vision) */
+    const uint8_t *is_vision;     /* [T] or NULL */
+    const int32_t *input_ids;     /* [T] (hash mode) */
+    const int32_t *tid2eid;       /* [vocab,k] (hash mode) */
+    int vocab;
+    /* device copies of the step's host input and output rows, [T,d] bf16 each */
+    uint16_t *x, *y, *dY, *dX;    /* dY and dX may be NULL for forward-only steps */
+    /* forward state (moe_gate_route / moe_route, moe_permute, moe_expert_ffn) */
+    float *logits;                /* [T,E] */
+    int32_t *ids;                 /* [T,k] */
+    float *weights, *scores_sel;  /* [T,k] */
+    int32_t *modality_counts;     /* [2,E]: route with moe_gate_route; NULL: with moe_route */
+    int32_t *counts;              /* [E] */
+    int32_t *offsets;             /* [E+2] */
+    int32_t *row_token;           /* [S+T] */
+    int32_t *slot_row;            /* [S] */
+    float *row_weight;            /* [S] */
+    uint16_t *x_perm, *h_perm, *y_perm; /* [S+T,d], [S+T,I], [S+T,d] */
+    float *gu_save;               /* as for moe_expert_ffn; NULL with MOE_FLAG_RECOMPUTE */
+    /* gradients (training steps) */
+    float *dW_g, *dW13, *dW2;
+    void *ws;                     /* moe_workspace_size(T,d,E,k,I, MOE_FLAG_BACKWARD | flags) */
+    size_t ws_bytes;
+} moe_layer_buffers;
+
+/* One step of the layer from and to HOST memory: x_host is copied to L->x,
+ * the forward runs (routing, dispatch, both expert matmuls, combine into
+ * L->y) and L->y is copied to y_host; with dY_host, dY_host is copied to
+ * L->dY, the backward runs (moe_backward into L->dX and the weight
+ * gradients) and L->dX is copied to dX_host.  All four host arrays are
+ * [host] [T,d] bf16; dY_host and dX_host are both NULL (forward only) or
+ * both given.  Copies are cudaMemcpyAsync: host memory should be page-locked
+ * for them to run asynchronously.  With copy_stream (a second cudaStream_t)
+ * the upload of dY overlaps the forward and the download of y overlaps the
+ * backward; the call still leaves `stream` waiting for every copy, so work
+ * queued on `stream` afterwards sees the step complete (the call creates and
+ * releases a few CUDA events; it allocates no memory).  Returns the first
+ * failing call's status. */
+moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_host,
+                               const uint16_t *dY_host, uint16_t *y_host, uint16_t *dX_host,
+                               void *stream, void *copy_stream);
+
 /* ---------------------------------------------------------------- MXFP8
  * Low-precision expert matmuls ([TTN] outlook: FP8 training on MxFP8
  * compute).  The pages fix no format; these calls use the OCP Microscaling
@@ -388,6 +443,21 @@ const char *moe_status_string(moe_status s);
  * device (MOE_OK if no kernel recorded an error since the last call) and
  * resets it. */
 moe_status moe_last_device_status(void *stream);
+
+/* Test hook for the bounded wait of moe_expert_ffn_fused: the same call
+ * (gu_save = NULL), except that the expert GEMM-2 tiles of the 128-row tile
+ * `stall_row_tile` (counted over the groups' row tiles in order) wait for one
+ * more GEMM-1 release than will ever come.  Their waits give up after
+ * `limit_cycles` SM clock cycles, record MOE_ERR_TIMEOUT in the device status
+ * word, and their CTAs drain their copies and MMAs, free their tensor memory
+ * and return; the other tiles finish normally.  Nothing traps or hangs, and
+ * the context stays usable.  limit_cycles must be in (0, 2^31). */
+moe_status moe_selftest_ffn_fused_stall(const uint16_t *x_perm, const int32_t *offsets, int G,
+                                        int max_rows, const uint16_t *W13, const uint16_t *W2,
+                                        const float *row_weight, int S, int d, int I, float clamp,
+                                        uint16_t *h_perm, uint16_t *y_perm, void *ws,
+                                        size_t ws_bytes, int stall_row_tile,
+                                        long long limit_cycles, void *stream);
 
 /* Tuning: which grouped matmuls may run as 2-SM pairs (two CTAs on two SMs
  * sharing one tcgen05 MMA of 256 rows, each CTA loading half of the weight

@@ -36,7 +36,8 @@ MOE_PAIR_ALL = (MOE_PAIR_EXPERT_GEMM1 | MOE_PAIR_EXPERT_GEMM2 | MOE_PAIR_DGRAD2 
 EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_route", "moe_permute",
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
-           "moe_last_device_status", "moe_selftest_wait_timeout",
+           "moe_last_device_status", "moe_selftest_wait_timeout", "moe_selftest_ffn_fused_stall",
+           "moe_layer_step_host",
            "moe_set_gemm_pairs", "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
            "moe_expert_gemm1_mx", "moe_expert_gemm2_mx"]
 
@@ -110,6 +111,21 @@ class BwdArgs(ctypes.Structure):
                 ("stage_events", ctypes.POINTER(_P))]
 
 
+class LayerBuffers(ctypes.Structure):
+    """Mirror of moe_layer_buffers."""
+    _fields_ = [("T", _I), ("d", _I), ("E", _I), ("k", _I), ("I", _I),
+                ("scaling", _F), ("clamp", _F), ("flags", _I), ("mode", _I),
+                ("W_g", _P), ("W13", _P), ("W2", _P),
+                ("logit_offset", _P), ("bias", _P), ("is_vision", _P), ("input_ids", _P),
+                ("tid2eid", _P), ("vocab", _I),
+                ("x", _P), ("y", _P), ("dY", _P), ("dX", _P),
+                ("logits", _P), ("ids", _P), ("weights", _P), ("scores_sel", _P),
+                ("modality_counts", _P), ("counts", _P), ("offsets", _P), ("row_token", _P),
+                ("slot_row", _P), ("row_weight", _P), ("x_perm", _P), ("h_perm", _P),
+                ("y_perm", _P), ("gu_save", _P), ("dW_g", _P), ("dW13", _P), ("dW2", _P),
+                ("ws", _P), ("ws_bytes", _Z)]
+
+
 MOE_BWD_STAGE_NAMES = ["recompute_gather", "recompute_gemm1", "gather_dY", "dgrad2", "wgrad2",
                        "dgrad1", "wgrad1", "router_bwd", "dX", "dW_g"]
 MOE_BWD_STAGES = len(MOE_BWD_STAGE_NAMES)
@@ -135,6 +151,9 @@ _SIGS = {
     "moe_last_device_status": ([_P], _I),
     "moe_selftest_wait_timeout": ([_LL, _P], _I),
     "moe_set_gemm_pairs": ([_I], _I),
+    "moe_layer_step_host": ([ctypes.POINTER(LayerBuffers), _P, _P, _P, _P, _P, _P], _I),
+    "moe_selftest_ffn_fused_stall": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _Z,
+                                      _I, _LL, _P], _I),
     "moe_mx_sf_pitch": ([_I], _I),
     "moe_mx_quantize": ([_P, _LL, _I, _P, _P, _P], _I),
     "moe_mx_gather": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
@@ -403,3 +422,59 @@ def moe_set_gemm_pairs(mask: int) -> int:
     """Which grouped matmuls may run as 2-SM pairs (MOE_PAIR_* bits); returns
     the previous mask."""
     return int(load().moe_set_gemm_pairs(int(mask)))
+
+
+def moe_selftest_ffn_fused_stall(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I,
+                                 clamp, h_perm, y_perm, ws, stall_row_tile, limit_cycles,
+                                 stream=None):
+    """moe_expert_ffn_fused with one row tile's GEMM-2 wait made unreachable
+    (test hook of the bounded wait)."""
+    st = load().moe_selftest_ffn_fused_stall(
+        _ptr(x_perm, BF16, "x_perm"), _ptr(offsets, I32, "offsets"), G, max_rows,
+        _ptr(W13, BF16, "W13"), _ptr(W2, BF16, "W2"), _ptr(row_weight, F32, "row_weight"), S, d,
+        I, clamp, _ptr(h_perm, BF16, "h_perm"), _ptr(y_perm, BF16, "y_perm"), _ptr(ws, U8, "ws"),
+        0 if ws is None else ws.numel(), int(stall_row_tile), int(limit_cycles), _stream(stream))
+    _check("moe_selftest_ffn_fused_stall", st)
+
+
+_LAYER_TYPES = dict(W_g=BF16, W13=BF16, W2=BF16, logit_offset=F32, bias=F32, is_vision=U8,
+                    input_ids=I32, tid2eid=I32, x=BF16, y=BF16, dY=BF16, dX=BF16, logits=F32,
+                    ids=I32, weights=F32, scores_sel=F32, modality_counts=I32, counts=I32,
+                    offsets=I32, row_token=I32, slot_row=I32, row_weight=F32, x_perm=BF16,
+                    h_perm=BF16, y_perm=BF16, gu_save=F32, dW_g=F32, dW13=F32, dW2=F32, ws=U8)
+
+
+def layer_buffers(fields: dict) -> LayerBuffers:
+    """A moe_layer_buffers from a dict of ints / floats / CUDA tensors (None
+    for NULL).  The caller keeps the tensors alive while the struct is used."""
+    L = LayerBuffers()
+    for name, _ in LayerBuffers._fields_:
+        if name == "ws_bytes":
+            continue
+        v = fields.get(name)
+        if name in _LAYER_TYPES:
+            setattr(L, name, _ptr(v, _LAYER_TYPES[name], name))
+        else:
+            setattr(L, name, 0 if v is None else v)
+    L.ws_bytes = 0 if fields.get("ws") is None else fields["ws"].numel()
+    return L
+
+
+def _host_ptr(t, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CPU tensor")
+    if t.dtype != BF16:
+        raise TypeError(f"{name}: expected {BF16}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def moe_layer_step_host(L: LayerBuffers, x_host, dY_host, y_host, dX_host, stream=None,
+                        copy_stream=None):
+    """One layer step from and to host memory (pinned CPU tensors, [T,d] bf16)."""
+    cs = None if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    st = load().moe_layer_step_host(ctypes.byref(L), _host_ptr(x_host, "x_host"),
+                                    _host_ptr(dY_host, "dY_host"), _host_ptr(y_host, "y_host"),
+                                    _host_ptr(dX_host, "dX_host"), _stream(stream), cs)
+    _check("moe_layer_step_host", st)

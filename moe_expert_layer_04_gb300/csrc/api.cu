@@ -332,11 +332,11 @@ moe_status moe_expert_ffn(const uint16_t *x_perm, const int32_t *offsets, int G,
     return moe_expert_gemm2(h_perm, offsets, G, max_rows, W2, row_weight, S, d, I, y_perm, stream);
 }
 
-moe_status moe_expert_ffn_fused(const uint16_t *x_perm, const int32_t *offsets, int G,
-                                int max_rows, const uint16_t *W13, const uint16_t *W2,
-                                const float *row_weight, int S, int d, int I, float clamp,
-                                float *gu_save, uint16_t *h_perm, uint16_t *y_perm, void *ws,
-                                size_t ws_bytes, void *stream) {
+static moe_status ffn_fused(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
+                            const uint16_t *W13, const uint16_t *W2, const float *row_weight,
+                            int S, int d, int I, float clamp, float *gu_save, uint16_t *h_perm,
+                            uint16_t *y_perm, void *ws, size_t ws_bytes, void *stream,
+                            int stall_rt, long long wait_limit) {
     moe_status s = check_ffn(G, max_rows, d, I, S);
     if (s != MOE_OK) return s;
     if (I % 128 != 0 || d % 256 != 0) return MOE_ERR_UNSUPPORTED;
@@ -349,7 +349,29 @@ moe_status moe_expert_ffn_fused(const uint16_t *x_perm, const int32_t *offsets, 
         (reinterpret_cast<uintptr_t>(ws) & 3u) != 0)
         return MOE_ERR_WORKSPACE;
     return launch_ffn12(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, h_perm,
-                        gu_save, y_perm, static_cast<int *>(ws), static_cast<cudaStream_t>(stream));
+                        gu_save, y_perm, static_cast<int *>(ws), static_cast<cudaStream_t>(stream),
+                        stall_rt, wait_limit);
+}
+
+moe_status moe_expert_ffn_fused(const uint16_t *x_perm, const int32_t *offsets, int G,
+                                int max_rows, const uint16_t *W13, const uint16_t *W2,
+                                const float *row_weight, int S, int d, int I, float clamp,
+                                float *gu_save, uint16_t *h_perm, uint16_t *y_perm, void *ws,
+                                size_t ws_bytes, void *stream) {
+    return ffn_fused(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, gu_save,
+                     h_perm, y_perm, ws, ws_bytes, stream, -1, 0);
+}
+
+moe_status moe_selftest_ffn_fused_stall(const uint16_t *x_perm, const int32_t *offsets, int G,
+                                        int max_rows, const uint16_t *W13, const uint16_t *W2,
+                                        const float *row_weight, int S, int d, int I, float clamp,
+                                        uint16_t *h_perm, uint16_t *y_perm, void *ws,
+                                        size_t ws_bytes, int stall_row_tile,
+                                        long long limit_cycles, void *stream) {
+    if (stall_row_tile < 0 || limit_cycles <= 0 || limit_cycles >= (1LL << 31))
+        return MOE_ERR_INVALID_ARG;
+    return ffn_fused(x_perm, offsets, G, max_rows, W13, W2, row_weight, S, d, I, clamp, nullptr,
+                     h_perm, y_perm, ws, ws_bytes, stream, stall_row_tile, limit_cycles);
 }
 
 int moe_mx_sf_pitch(int K) { return K > 0 ? mx_sf_pitch(K) : 0; }
@@ -531,6 +553,99 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
     if ((s = launch_dwg(x_perm, w.dz_row, a->offsets, d, E, w.dwg_part, a->dW_g, st)) != MOE_OK)
         return s;
     return mark(MOE_BWD_STAGES) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_host,
+                               const uint16_t *dY_host, uint16_t *y_host, uint16_t *dX_host,
+                               void *stream, void *copy_stream) {
+    if (!L || !x_host || !y_host || !L->x || !L->y) return MOE_ERR_INVALID_ARG;
+    const bool train = dY_host != nullptr;
+    if (train != (dX_host != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (train && (!L->dY || !L->dX)) return MOE_ERR_INVALID_ARG;
+    moe_status s = check_shapes(L->T, L->d, L->E, L->k, L->I);
+    if (s != MOE_OK) return s;
+    const int T = L->T, d = L->d, E = L->E, k = L->k, I = L->I;
+    const size_t row_bytes = (size_t)T * d * sizeof(uint16_t);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+    const bool overlap = train && cs != nullptr && cs != st;
+    // events of this call: the call's start on `stream`, dY uploaded, forward
+    // done, y downloaded
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    auto cleanup = [&](moe_status r) {
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);
+        return r;
+    };
+    if (overlap)
+        for (cudaEvent_t &e : ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                return cleanup(MOE_ERR_CUDA);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!ok(cudaMemcpyAsync(L->x, x_host, row_bytes, cudaMemcpyHostToDevice, st)))
+        return cleanup(MOE_ERR_CUDA);
+    if (overlap) {
+        // the upload of dY waits for whatever `stream` ran before this call
+        if (!ok(cudaEventRecord(ev[0], st)) || !ok(cudaStreamWaitEvent(cs, ev[0], 0)) ||
+            !ok(cudaMemcpyAsync(L->dY, dY_host, row_bytes, cudaMemcpyHostToDevice, cs)) ||
+            !ok(cudaEventRecord(ev[1], cs)))
+            return cleanup(MOE_ERR_CUDA);
+    }
+    // forward
+    if (L->modality_counts)
+        s = moe_gate_route(L->x, L->W_g, L->logit_offset, L->bias, L->is_vision, L->input_ids,
+                           L->tid2eid, L->vocab, T, d, E, k, L->scaling,
+                           static_cast<moe_route_mode>(L->mode), L->logits, L->ids, L->weights,
+                           L->scores_sel, L->modality_counts, stream);
+    else
+        s = moe_route(L->x, L->W_g, L->logit_offset, L->bias, L->is_vision, L->input_ids,
+                      L->tid2eid, L->vocab, T, d, E, k, L->scaling,
+                      static_cast<moe_route_mode>(L->mode), L->logits, L->ids, L->weights,
+                      L->scores_sel, stream);
+    if (s != MOE_OK) return cleanup(s);
+    s = moe_permute(L->ids, L->weights, L->x, T, d, E, k, L->counts, L->offsets, L->row_token,
+                    L->slot_row, L->row_weight, L->x_perm, L->ws, L->ws_bytes, stream);
+    if (s != MOE_OK) return cleanup(s);
+    const int R = T * k + T;
+    s = moe_expert_ffn(L->x_perm, L->offsets, E + 1, R, L->W13, L->W2, L->row_weight, T * k, d,
+                       I, L->clamp, (L->flags & MOE_FLAG_RECOMPUTE) ? nullptr : L->gu_save,
+                       L->h_perm, L->y_perm, nullptr, 0, stream);
+    if (s != MOE_OK) return cleanup(s);
+    s = moe_combine(L->y_perm, L->slot_row, T, d, k, 1, L->y, stream);
+    if (s != MOE_OK) return cleanup(s);
+    if (overlap) {
+        if (!ok(cudaEventRecord(ev[2], st)) || !ok(cudaStreamWaitEvent(cs, ev[2], 0)) ||
+            !ok(cudaMemcpyAsync(y_host, L->y, row_bytes, cudaMemcpyDeviceToHost, cs)) ||
+            !ok(cudaEventRecord(ev[3], cs)) || !ok(cudaStreamWaitEvent(st, ev[1], 0)))
+            return cleanup(MOE_ERR_CUDA);
+    } else {
+        if (!ok(cudaMemcpyAsync(y_host, L->y, row_bytes, cudaMemcpyDeviceToHost, st)))
+            return cleanup(MOE_ERR_CUDA);
+        if (train &&
+            !ok(cudaMemcpyAsync(L->dY, dY_host, row_bytes, cudaMemcpyHostToDevice, st)))
+            return cleanup(MOE_ERR_CUDA);
+    }
+    if (train) {
+        moe_bwd_args a;
+        std::memset(&a, 0, sizeof a);
+        a.T = T; a.d = d; a.E = E; a.k = k; a.I = I;
+        a.scaling = L->scaling;
+        a.clamp = L->clamp;
+        a.flags = L->flags & MOE_FLAG_RECOMPUTE;
+        a.x = L->x; a.W_g = L->W_g; a.W13 = L->W13; a.W2 = L->W2;
+        a.ids = L->ids; a.weights = L->weights; a.scores_sel = L->scores_sel;
+        a.row_weight = L->row_weight; a.offsets = L->offsets; a.row_token = L->row_token;
+        a.slot_row = L->slot_row; a.x_perm = L->x_perm; a.gu_save = L->gu_save;
+        a.dY = L->dY; a.dX = L->dX; a.dW_g = L->dW_g; a.dW13 = L->dW13; a.dW2 = L->dW2;
+        a.ws = L->ws; a.ws_bytes = L->ws_bytes;
+        s = moe_backward(&a, stream);
+        if (s != MOE_OK) return cleanup(s);
+        if (!ok(cudaMemcpyAsync(dX_host, L->dX, row_bytes, cudaMemcpyDeviceToHost, st)))
+            return cleanup(MOE_ERR_CUDA);
+    }
+    // `stream` ends after every copy of the step
+    if (overlap && !ok(cudaStreamWaitEvent(st, ev[3], 0))) return cleanup(MOE_ERR_CUDA);
+    return cleanup(MOE_OK);
 }
 
 const char *moe_status_string(moe_status s) {

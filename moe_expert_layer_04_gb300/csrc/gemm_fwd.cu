@@ -103,7 +103,7 @@ int ffn_fused_counters(int max_rows, int G) { return row_tile_bound(max_rows, G)
 moe_status launch_ffn12(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
                         const uint16_t *W13, const uint16_t *W2, const float *row_w, int S, int d,
                         int I, float clamp, uint16_t *h, float *gu_save, uint16_t *y, int *ready,
-                        cudaStream_t st) {
+                        cudaStream_t st, int stall_rt, long long wait_limit) {
     if (I % 128 != 0 || d % 256 != 0) return MOE_ERR_UNSUPPORTED;
     GemmParams p;
     std::memset(&p, 0, sizeof p);
@@ -136,6 +136,8 @@ moe_status launch_ffn12(const uint16_t *x_perm, const int32_t *offsets, int G, i
     p.w_rows = S;
     p.ready = ready;
     p.ready_target = p.n_tiles * ModeTraits<GM_FFN12>::NEPI;
+    p.stall_rt = stall_rt;
+    p.wait_limit = wait_limit;
     const int rt = ffn_fused_counters(max_rows, G);
     if (cudaMemsetAsync(ready, 0, (size_t)rt * sizeof(int), st) != cudaSuccess)
         return MOE_ERR_CUDA;

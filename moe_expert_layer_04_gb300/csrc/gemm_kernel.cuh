@@ -75,6 +75,7 @@ struct GemmParams {
     int n_tiles2, k_blocks2, b_rows2;
     int *ready;
     int ready_target;
+    int stall_rt;            // GM_FFN12 test hook: this row tile never becomes ready (-1: none)
     int *status;
     long long wait_limit;
 };
@@ -412,7 +413,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                         // static order, all on resident CTAs).  The writers
                         // fenced their stores into the async proxy before the
                         // release, so the copies below may read them at once.
-                        if (!wait_count_geq(p.ready + ti.rt, p.ready_target, wc)) {
+                        const int target = p.ready_target + (ti.rt == p.stall_rt ? 1 : 0);
+                        if (!wait_count_geq(p.ready + ti.rt, target, wc)) {
                             ok = false;
                             break;
                         }

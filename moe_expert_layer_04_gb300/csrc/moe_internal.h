@@ -73,7 +73,7 @@ int ffn_fused_counters(int max_rows, int G);
 moe_status launch_ffn12(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,
                         const uint16_t *W13, const uint16_t *W2, const float *row_w, int S, int d,
                         int I, float clamp, uint16_t *h, float *gu_save, uint16_t *y, int *ready,
-                        cudaStream_t st);
+                        cudaStream_t st, int stall_rt = -1, long long wait_limit = 0);
 moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max_rows,
                        const uint16_t *W2, const float *row_w, int S, int d, int I, uint16_t *y,
                        cudaStream_t st);

@@ -150,6 +150,7 @@ class MoELayer:
     def route(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
               input_ids=None, tid2eid=None, stream=None):
         D = self.dims
+        self.x = x       # the backward reads the forward's input
         if self.fused_route:
             _lib.moe_gate_route(x, self.w["W_g"], logit_offset, bias, is_vision, input_ids,
                                 tid2eid, D.T, D.d, D.E, D.k, self.scaling, mode, self.logits,
@@ -249,6 +250,50 @@ class MoELayer:
                     stage_events=stage_events)
         _lib.moe_backward(args, stream)
         return self.dX
+
+
+    # ------------------------------------------------- steps from host memory
+    def step_host(self, x_host, y_host, dY_host=None, dX_host=None, bias=None, is_vision=None,
+                  logit_offset=None, mode=MOE_ROUTE_TOPK, input_ids=None, tid2eid=None,
+                  stream=None, copy_stream=None):
+        """One step from and to host memory through moe_layer_step_host: x_host
+        ([T,d] bf16, pinned CPU) in, y_host out; with dY_host / dX_host also the
+        backward (dX out, weight gradients in self.dW13 / dW2 / dW_g).  The
+        routing inputs are device tensors as for forward()."""
+        D = self.dims
+        if self.mx:
+            raise RuntimeError("moe_layer_step_host runs the bf16 layer")
+        train = dY_host is not None
+        if train and not self.backward_enabled:
+            raise RuntimeError("layer built without backward buffers")
+        key = (id(bias), id(is_vision), id(logit_offset), mode, id(input_ids), id(tid2eid))
+        if getattr(self, "_host_key", None) != key:
+            dev = self.y.device
+            if getattr(self, "x_dev", None) is None:
+                self.x_dev = torch.empty(D.T, D.d, dtype=torch.bfloat16, device=dev)
+            if self.backward_enabled and getattr(self, "dY_dev", None) is None:
+                self.dY_dev = torch.empty(D.T, D.d, dtype=torch.bfloat16, device=dev)
+            self._host_refs = (bias, is_vision, logit_offset, input_ids, tid2eid)
+            self._host_struct = _lib.layer_buffers(dict(
+                T=D.T, d=D.d, E=D.E, k=D.k, I=D.I, scaling=self.scaling, clamp=self.clamp,
+                flags=MOE_FLAG_RECOMPUTE if self.recompute else 0, mode=int(mode),
+                W_g=self.w["W_g"], W13=self.w["W13"], W2=self.w["W2"],
+                logit_offset=logit_offset, bias=bias, is_vision=is_vision, input_ids=input_ids,
+                tid2eid=tid2eid, vocab=0 if tid2eid is None else int(tid2eid.shape[0]),
+                x=self.x_dev, y=self.y,
+                dY=self.dY_dev if self.backward_enabled else None,
+                dX=self.dX if self.backward_enabled else None,
+                logits=self.logits, ids=self.ids, weights=self.weights,
+                scores_sel=self.scores_sel, modality_counts=self.modality_counts,
+                counts=self.counts, offsets=self.offsets, row_token=self.row_token,
+                slot_row=self.slot_row, row_weight=self.row_weight, x_perm=self.x_perm,
+                h_perm=self.h_perm, y_perm=self.y_perm, gu_save=self.gu_save,
+                dW_g=getattr(self, "dW_g", None), dW13=getattr(self, "dW13", None),
+                dW2=getattr(self, "dW2", None), ws=self.ws))
+            self._host_key = key
+        self.x = self.x_dev
+        _lib.moe_layer_step_host(self._host_struct, x_host, dY_host, y_host, dX_host, stream,
+                                 copy_stream)
 
 
 __all__ = ["Dims", "MoELayer", "MOE_ROUTE_TOPK", "MOE_ROUTE_HASH"]

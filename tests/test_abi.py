@@ -27,8 +27,11 @@ def test_library_builds_and_exports_every_declared_symbol():
     assert sorted(_lib.EXPORTS) == names
 
 
-def test_bwd_struct_matches_header():
-    m = re.search(r"typedef struct \{(.*?)\} moe_bwd_args;", HEADER, flags=re.S)
+@pytest.mark.parametrize("struct,mirror", [("moe_bwd_args", _lib.BwdArgs),
+                                           ("moe_layer_buffers", _lib.LayerBuffers)])
+def test_structs_match_header(struct, mirror):
+    m = re.search(r"typedef struct \{((?:(?!typedef struct).)*?)\} " + struct + ";", HEADER,
+                  flags=re.S)
     body = re.sub(r"/\*.*?\*/", "", m.group(1), flags=re.S)
     fields = []
     for decl in body.split(";"):
@@ -39,8 +42,8 @@ def test_bwd_struct_matches_header():
         # "int T, d, E, k, I" / "float scaling, clamp" / "const float *weights"
         parts = re.sub(r"^(const\s+)?\w+\s*", "", decl)
         for p in parts.split(","):
-            fields.append(p.strip().lstrip("*").strip())
-    assert [f for f, _ in _lib.BwdArgs._fields_] == fields
+            fields.append(re.findall(r"\w+", p)[-1])    # the declarator's name
+    assert [f for f, _ in mirror._fields_] == fields
 
 
 def test_workspace_size_host_logic():

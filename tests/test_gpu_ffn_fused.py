@@ -86,3 +86,28 @@ def test_fused_ffn_saves_the_same_gu_for_the_backward():
     assert _lib.moe_last_device_status() == _lib.MOE_OK
     assert torch.equal(lf.dX.view(torch.int16), lu.dX.view(torch.int16))
     assert torch.equal(lf.dW13, lu.dW13)
+
+
+@pytest.mark.parametrize("stall", [0, 5])
+def test_fused_ffn_wait_times_out_and_context_stays_usable(stall):
+    # the GEMM-2 tiles of one row tile wait for a GEMM-1 release that never
+    # comes: their bounded waits give up, the call reports MOE_ERR_TIMEOUT,
+    # and the next calls on the same context give the usual results
+    w, inp, (lf, lu) = _layers("stall", 1000, 256, 6, 2, 256, 0)
+    D = lf.dims
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    h = torch.zeros_like(lf.h_perm)
+    y = torch.zeros_like(lf.y_perm)
+    _lib.moe_selftest_ffn_fused_stall(lf.x_perm, lf.offsets, D.E + 1, D.R, inp["W13"], inp["W2"],
+                                      lf.row_weight, D.S, D.d, D.I, lf.clamp, h, y, lf.ws, stall,
+                                      1 << 20)
+    assert _lib.moe_last_device_status() == _lib.MOE_ERR_TIMEOUT
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    # every GEMM-1 tile ran: h is complete
+    assert torch.equal(h.view(torch.int16), lu.h_perm.view(torch.int16))
+    # the context is usable: the one-launch call again, bit-identical to the
+    # two launches
+    lf.experts()
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    assert torch.equal(lf.y_perm.view(torch.int16), lu.y_perm.view(torch.int16))

@@ -174,7 +174,10 @@ def _check_backward_sampled(layer, inp, w, weights, counts, n_tok, n_ent):
         h_rows = layer.h_perm[int(offs[e]):int(offs[e + 1])]
         stage = oracle.wgrad2_entries_given_h(dY, h_rows.cpu(), rt_all[rows], rw_all[rows],
                                               qa[:n_ent], qb[:n_ent], store_bf16=True)
-        assert_close(g2, stage, f"{w.name} dW2[{e}] entries (stage-wise)")
+        # the tensor cores' fp32 accumulation over up to 2^16 rows (the shared
+        # expert of the 64K-token slice) leaves ~1e-4 of the entries' size
+        assert_close(g2, stage, f"{w.name} dW2[{e}] entries (stage-wise)",
+                     max_abs=max(5e-2, 2e-4 * np.abs(stage).max()))
         # end to end: over K rows, one-ulp bf16 flips of h (fp32 vs fp64
         # accumulators) add up to ~sqrt(K * 3e-4) ulps; the bound scales with
         # the entries' size above 5e-2
