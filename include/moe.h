@@ -312,6 +312,71 @@ enum {
  * weight chain.  Clamp gradients pass where the argument equals the bound. */
 moe_status moe_backward(const moe_bwd_args *args, void *stream);
 
+/* ------------------------------------------- expert parallelism pieces
+ * With the experts split over GPUs ("Twinkle x 昇腾…", FSDP2-4D: dispatch to
+ * the expert's owner, local expert compute, all-to-all back, combine by
+ * routing weight), the caller's collective moves permuted rows between ranks
+ * and the calls below do each rank's share: moe_gather_rows regroups rows
+ * around an exchange, moe_expert_ffn (forward) and moe_expert_ffn_backward
+ * run on the rows a rank's experts received, and moe_router_backward
+ * finishes the backward on the rank that routed the tokens. */
+
+/* dst row i = src row idx[i] for i < n (rows of row_bytes bytes, a multiple
+ * of 4; 16-byte rows with 16-byte aligned src and dst move as vectors).  A
+ * negative idx[i] writes a zero row; idx[i] >= n_src is recorded as
+ * MOE_ERR_INVALID_ARG in the device status word and leaves row i unwritten.
+ * src [n_src rows], idx int32 [n], dst [n rows]; 4-byte aligned. */
+moe_status moe_gather_rows(const void *src, const int32_t *idx, long long n, long long n_src,
+                           int row_bytes, void *dst, void *stream);
+
+/* Backward of moe_expert_ffn on its rows (the same four matmuls and clamped
+ * SwiGLU backward as in moe_backward, without the routing or combine):
+ *   dA = dY_perm[r] W2[g];  dw_rows[r] = <h[r], dA>  (r < S)
+ *   dH = w dA;  [dg|du] as in moe_backward;  dX_perm[r] = [dg|du] W13[g]
+ *   dW2[g] = sum_r dY_perm[r]^T (w h)[r];  dW13[g] = sum_r [dg|du][r]^T x_perm[r]
+ * for every group g < G and row r in [offsets[g], offsets[g+1]), w = row_weight[r]
+ * for r < S (rows >= S carry weight 1, e.g. the shared expert's).  gu_save:
+ * moe_expert_ffn's saved g|u of these rows, or NULL to recompute it from
+ * x_perm into the workspace.  Outputs are overwritten.  Workspace:
+ * moe_expert_bwd_workspace_size(max_rows, d, I, gu_save == NULL). */
+typedef struct {
+    int G, max_rows, S, d, I;
+    float clamp;
+    const int32_t *offsets;       /* [G+1] */
+    const uint16_t *x_perm;       /* [R,d] the rows' GEMM-1 input */
+    const uint16_t *W13;          /* [G,2I,d] */
+    const uint16_t *W2;           /* [G,d,I] */
+    const float *row_weight;      /* [S] or NULL (weight 1) */
+    const float *gu_save;         /* or NULL: recompute */
+    const uint16_t *dY_perm;      /* [R,d] gradient at the rows' outputs */
+    uint16_t *dX_perm;            /* [R,d] out */
+    float *dw_rows;               /* [S] out or NULL */
+    float *dW13;                  /* [G,2I,d] fp32 out */
+    float *dW2;                   /* [G,d,I] fp32 out */
+    void *ws;
+    size_t ws_bytes;
+} moe_expert_bwd_args;
+size_t moe_expert_bwd_workspace_size(int max_rows, int d, int I, int recompute);
+moe_status moe_expert_ffn_backward(const moe_expert_bwd_args *args, void *stream);
+
+/* The routing and combine part of moe_backward, on the rank that routed the
+ * tokens: from the routing-weight gradient of each routed row (dw_rows [S],
+ * indexed by permuted row) and the input gradient of every permuted row
+ * (dX_perm [S+T,d], the routed rows in this rank's permuted order, then the
+ * shared expert's), the normalisation-chain backward (dz, as in
+ * moe_backward), dX = dX_perm[S+t] + sum_j dX_perm[slot_row[t,j]] + dz W_g,
+ * and dW_g = dz^T x (from this rank's x_perm and offsets).  dlogits /
+ * dweights as in moe_backward (nullable).  Workspace:
+ * moe_router_bwd_workspace_size(T,d,E,k). */
+size_t moe_router_bwd_workspace_size(int T, int d, int E, int k);
+moe_status moe_router_backward(const float *dw_rows, const uint16_t *dX_perm,
+                               const uint16_t *x_perm, const int32_t *offsets, const int32_t *ids,
+                               const float *weights, const float *scores_sel,
+                               const int32_t *slot_row, const uint16_t *W_g, int T, int d, int E,
+                               int k, float scaling, uint16_t *dX, float *dlogits,
+                               float *dweights, float *dW_g, void *ws, size_t ws_bytes,
+                               void *stream);
+
 /* ------------------------------------------------- whole layer from host
  * One layer as everything a training step touches: its sizes and options,
  * its weights and routing inputs, and every device buffer of the calls above

@@ -37,7 +37,8 @@ EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_rout
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout", "moe_selftest_ffn_fused_stall",
-           "moe_layer_step_host",
+           "moe_layer_step_host", "moe_gather_rows", "moe_expert_bwd_workspace_size",
+           "moe_expert_ffn_backward", "moe_router_bwd_workspace_size", "moe_router_backward",
            "moe_set_gemm_pairs", "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
            "moe_expert_gemm1_mx", "moe_expert_gemm2_mx"]
 
@@ -111,6 +112,14 @@ class BwdArgs(ctypes.Structure):
                 ("stage_events", ctypes.POINTER(_P))]
 
 
+class ExpertBwdArgs(ctypes.Structure):
+    """Mirror of moe_expert_bwd_args."""
+    _fields_ = [("G", _I), ("max_rows", _I), ("S", _I), ("d", _I), ("I", _I), ("clamp", _F),
+                ("offsets", _P), ("x_perm", _P), ("W13", _P), ("W2", _P), ("row_weight", _P),
+                ("gu_save", _P), ("dY_perm", _P), ("dX_perm", _P), ("dw_rows", _P),
+                ("dW13", _P), ("dW2", _P), ("ws", _P), ("ws_bytes", _Z)]
+
+
 class LayerBuffers(ctypes.Structure):
     """Mirror of moe_layer_buffers."""
     _fields_ = [("T", _I), ("d", _I), ("E", _I), ("k", _I), ("I", _I),
@@ -151,6 +160,12 @@ _SIGS = {
     "moe_last_device_status": ([_P], _I),
     "moe_selftest_wait_timeout": ([_LL, _P], _I),
     "moe_set_gemm_pairs": ([_I], _I),
+    "moe_gather_rows": ([_P, _P, _LL, _LL, _I, _P, _P], _I),
+    "moe_expert_bwd_workspace_size": ([_I, _I, _I, _I], _Z),
+    "moe_expert_ffn_backward": ([ctypes.POINTER(ExpertBwdArgs), _P], _I),
+    "moe_router_bwd_workspace_size": ([_I, _I, _I, _I], _Z),
+    "moe_router_backward": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P,
+                             _P, _P, _Z, _P], _I),
     "moe_layer_step_host": ([ctypes.POINTER(LayerBuffers), _P, _P, _P, _P, _P, _P], _I),
     "moe_selftest_ffn_fused_stall": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _Z,
                                       _I, _LL, _P], _I),
@@ -478,3 +493,54 @@ def moe_layer_step_host(L: LayerBuffers, x_host, dY_host, y_host, dX_host, strea
                                     _host_ptr(dY_host, "dY_host"), _host_ptr(y_host, "y_host"),
                                     _host_ptr(dX_host, "dX_host"), _stream(stream), cs)
     _check("moe_layer_step_host", st)
+
+
+def moe_gather_rows(src, idx, dst, stream=None):
+    """dst[i] = src[idx[i]] row by row (negative index: zero row).  src and dst
+    CUDA tensors with equal row sizes (any dtype, rows a multiple of 4 bytes)."""
+    if src.dim() == 1:
+        src, dst = src.view(-1, 1), dst.view(-1, 1)
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else \
+        dst[0].numel() * dst.element_size()
+    n = int(idx.numel())
+    if dst.shape[0] != n:
+        raise ValueError("dst rows must equal the index count")
+    st = load().moe_gather_rows(_ptr(src, None, "src") if src.shape[0] else None,
+                                _ptr(idx, I32, "idx"), n, int(src.shape[0]), int(row_bytes),
+                                _ptr(dst, None, "dst"), _stream(stream))
+    _check("moe_gather_rows", st)
+
+
+def moe_expert_bwd_workspace_size(max_rows, d, I, recompute) -> int:
+    return int(load().moe_expert_bwd_workspace_size(max_rows, d, I, int(bool(recompute))))
+
+
+def moe_expert_ffn_backward(args: dict, stream=None):
+    """args: the fields of moe_expert_bwd_args (tensors for pointers)."""
+    a = ExpertBwdArgs()
+    types = dict(offsets=I32, x_perm=BF16, W13=BF16, W2=BF16, row_weight=F32, gu_save=F32,
+                 dY_perm=BF16, dX_perm=BF16, dw_rows=F32, dW13=F32, dW2=F32, ws=U8)
+    for name, _ in ExpertBwdArgs._fields_:
+        if name == "ws_bytes":
+            continue
+        v = args.get(name)
+        setattr(a, name, _ptr(v, types[name], name) if name in types else v)
+    a.ws_bytes = 0 if args.get("ws") is None else args["ws"].numel()
+    st = load().moe_expert_ffn_backward(ctypes.byref(a), _stream(stream))
+    _check("moe_expert_ffn_backward", st)
+
+
+def moe_router_bwd_workspace_size(T, d, E, k) -> int:
+    return int(load().moe_router_bwd_workspace_size(T, d, E, k))
+
+
+def moe_router_backward(dw_rows, dX_perm, x_perm, offsets, ids, weights, scores_sel, slot_row,
+                        W_g, T, d, E, k, scaling, dX, dlogits, dweights, dW_g, ws, stream=None):
+    st = load().moe_router_backward(
+        _ptr(dw_rows, F32, "dw_rows"), _ptr(dX_perm, BF16, "dX_perm"), _ptr(x_perm, BF16, "x_perm"),
+        _ptr(offsets, I32, "offsets"), _ptr(ids, I32, "ids"), _ptr(weights, F32, "weights"),
+        _ptr(scores_sel, F32, "scores_sel"), _ptr(slot_row, I32, "slot_row"),
+        _ptr(W_g, BF16, "W_g"), T, d, E, k, scaling, _ptr(dX, BF16, "dX"),
+        _ptr(dlogits, F32, "dlogits"), _ptr(dweights, F32, "dweights"), _ptr(dW_g, F32, "dW_g"),
+        _ptr(ws, U8, "ws"), 0 if ws is None else ws.numel(), _stream(stream))
+    _check("moe_router_backward", st)

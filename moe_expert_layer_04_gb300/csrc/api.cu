@@ -78,6 +78,54 @@ __global__ void wait_timeout_kernel(long long limit, int *status) {
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
+// Workspace of moe_expert_ffn_backward: [dg|du] and w h (the weight-gradient
+// operands), the dw partial sums, and with recompute the g|u of GEMM 1.
+struct ExpertBwdWorkspace {
+    uint16_t *dGU, *hw;
+    float *dw_part, *gu;
+    size_t bytes;
+};
+
+ExpertBwdWorkspace carve_expert_bwd(uint8_t *base, int R, int d, int I, bool recompute) {
+    ExpertBwdWorkspace w;
+    std::memset(&w, 0, sizeof w);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    w.dGU = reinterpret_cast<uint16_t *>(take((size_t)R * 2 * I * 2));
+    w.hw = reinterpret_cast<uint16_t *>(take((size_t)R * I * 2));
+    w.dw_part = reinterpret_cast<float *>(take((size_t)R * dgrad2_n_tiles(I) * 4));
+    if (recompute) w.gu = reinterpret_cast<float *>(take(((size_t)R + 31) / 32 * 32 * 2 * I * 4));
+    w.bytes = off;
+    (void)d;
+    return w;
+}
+
+// Workspace of moe_router_backward: dz per slot and per row, dW_g partials.
+struct RouterBwdWorkspace {
+    float *dz_sel, *dz_row, *dwg_part;
+    size_t bytes;
+};
+
+RouterBwdWorkspace carve_router_bwd(uint8_t *base, int T, int d, int E, int k) {
+    RouterBwdWorkspace w;
+    std::memset(&w, 0, sizeof w);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
+    w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
+    w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
+    w.bytes = off;
+    return w;
+}
+
 struct BwdWorkspace {
     uint16_t *dY_perm, *dGU, *hw, *dX_perm, *x_perm;
     float *gu, *dw_part, *dz_sel, *dz_row, *dwg_part;
@@ -553,6 +601,96 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
     if ((s = launch_dwg(x_perm, w.dz_row, a->offsets, d, E, w.dwg_part, a->dW_g, st)) != MOE_OK)
         return s;
     return mark(MOE_BWD_STAGES) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_gather_rows(const void *src, const int32_t *idx, long long n, long long n_src,
+                           int row_bytes, void *dst, void *stream) {
+    if (n < 0 || n_src < 0 || row_bytes < 4 || row_bytes % 4 != 0) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!idx || !dst || (n_src > 0 && !src)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 3u)
+        return MOE_ERR_INVALID_ARG;
+    return launch_index_gather(src, idx, n, n_src, row_bytes, dst,
+                               static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_expert_bwd_workspace_size(int max_rows, int d, int I, int recompute) {
+    if (max_rows < 1 || d < 1 || I < 1 || I % 64 != 0) return 0;
+    return carve_expert_bwd(nullptr, max_rows, d, I, recompute != 0).bytes;
+}
+
+moe_status moe_expert_ffn_backward(const moe_expert_bwd_args *a, void *stream) {
+    if (!a) return MOE_ERR_INVALID_ARG;
+    moe_status s = check_ffn(a->G, a->max_rows, a->d, a->I, a->S);
+    if (s != MOE_OK) return s;
+    if (a->S > a->max_rows) return MOE_ERR_INVALID_ARG;
+    if (!a->offsets || !a->x_perm || !a->W13 || !a->W2 || !a->dY_perm || !a->dX_perm ||
+        !a->dW13 || !a->dW2)
+        return MOE_ERR_INVALID_ARG;
+    if (a->S > 0 && a->dw_rows && !a->row_weight) return MOE_ERR_INVALID_ARG;
+    const void *al[] = {a->x_perm, a->W13, a->W2, a->dY_perm, a->dX_perm, a->dW13, a->dW2};
+    for (const void *p : al)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (a->gu_save && !aligned16(a->gu_save)) return MOE_ERR_INVALID_ARG;
+    if (!(a->clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    const bool rec = a->gu_save == nullptr;
+    const int R = a->max_rows, d = a->d, I = a->I, G = a->G;
+    if (!a->ws || a->ws_bytes < moe_expert_bwd_workspace_size(R, d, I, rec ? 1 : 0))
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ExpertBwdWorkspace w = carve_expert_bwd(static_cast<uint8_t *>(a->ws), R, d, I, rec);
+    const float *gu = a->gu_save;
+    if (rec) {
+        if ((s = launch_ffn1(a->x_perm, a->offsets, G, R, a->W13, d, I, a->clamp, nullptr, w.gu,
+                             st)) != MOE_OK)
+            return s;
+        gu = w.gu;
+    }
+    int n_part = 0;
+    if ((s = launch_dgrad2(a->dY_perm, a->offsets, G, R, a->W2, gu, a->row_weight, a->S, d, I,
+                           a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
+        return s;
+    if ((s = launch_wgrad(a->dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, st)) != MOE_OK)
+        return s;
+    if ((s = launch_dgrad1(w.dGU, a->offsets, G, R, a->W13, d, I, a->dX_perm, st)) != MOE_OK)
+        return s;
+    if ((s = launch_wgrad(w.dGU, 2 * I, a->x_perm, d, a->offsets, G, R, a->dW13, st)) != MOE_OK)
+        return s;
+    if (a->dw_rows && a->S > 0)
+        return launch_row_sum(w.dw_part, a->S, n_part, a->dw_rows, st);
+    return MOE_OK;
+}
+
+size_t moe_router_bwd_workspace_size(int T, int d, int E, int k) {
+    if (T < 1 || d < 1 || E < 1 || k < 1 || k > E) return 0;
+    return carve_router_bwd(nullptr, T, d, E, k).bytes;
+}
+
+moe_status moe_router_backward(const float *dw_rows, const uint16_t *dX_perm,
+                               const uint16_t *x_perm, const int32_t *offsets, const int32_t *ids,
+                               const float *weights, const float *scores_sel,
+                               const int32_t *slot_row, const uint16_t *W_g, int T, int d, int E,
+                               int k, float scaling, uint16_t *dX, float *dlogits,
+                               float *dweights, float *dW_g, void *ws, size_t ws_bytes,
+                               void *stream) {
+    if (T < 1 || d < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+    if (k > 32 || E > 1024 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!dw_rows || !dX_perm || !x_perm || !offsets || !ids || !weights || !scores_sel ||
+        !slot_row || !W_g || !dX || !dW_g)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dX_perm) || !aligned16(x_perm) || !aligned16(W_g) || !aligned16(dX) ||
+        !aligned16(dW_g))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < moe_router_bwd_workspace_size(T, d, E, k)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    RouterBwdWorkspace w = carve_router_bwd(static_cast<uint8_t *>(ws), T, d, E, k);
+    moe_status s;
+    if ((s = launch_router_bwd(dw_rows, 1, slot_row, ids, weights, scores_sel, T, E, k, scaling,
+                               w.dz_sel, w.dz_row, dlogits, dweights, st)) != MOE_OK)
+        return s;
+    if ((s = launch_combine(dX_perm, slot_row, T, d, k, 1, w.dz_sel, ids, W_g, dX, st)) != MOE_OK)
+        return s;
+    return launch_dwg(x_perm, w.dz_row, offsets, d, E, w.dwg_part, dW_g, st);
 }
 
 moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_host,

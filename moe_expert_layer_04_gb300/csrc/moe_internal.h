@@ -108,6 +108,12 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
 
 moe_status launch_selftest_timeout(long long limit, cudaStream_t st);
 
+// Row movement around an exchange between GPUs (exchange.cu).
+moe_status launch_index_gather(const void *src, const int32_t *idx, long long n, long long n_src,
+                               int row_bytes, void *dst, cudaStream_t st);
+moe_status launch_row_sum(const float *part, long long n, int n_part, float *out,
+                          cudaStream_t st);
+
 }  // namespace moe
 
 namespace moe {

@@ -28,7 +28,8 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 
 @pytest.mark.parametrize("struct,mirror", [("moe_bwd_args", _lib.BwdArgs),
-                                           ("moe_layer_buffers", _lib.LayerBuffers)])
+                                           ("moe_layer_buffers", _lib.LayerBuffers),
+                                           ("moe_expert_bwd_args", _lib.ExpertBwdArgs)])
 def test_structs_match_header(struct, mirror):
     m = re.search(r"typedef struct \{((?:(?!typedef struct).)*?)\} " + struct + ";", HEADER,
                   flags=re.S)
