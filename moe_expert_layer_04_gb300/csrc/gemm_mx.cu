@@ -1,37 +1,43 @@
 // gemm_mx.cu -- MXFP8 expert GEMMs: E4M3 operands with E8M0 scales per block
-// of 32 along the contraction (OCP MX v1.0), on the bf16 tensor-core path.
+// of 32 along the contraction (OCP MX v1.0), on the block-scaled tensor-core
+// MMA (tcgen05.mma kind::mxf8f6f4).
 //
 //   MX GEMM 1   [g|u] = x~ W13~[g]^T,  h~ = MX(silu(min(g,c)) clamp(u,-c,c))
 //   MX GEMM 2   y = w * (h~ W2~[g]^T)                               (bf16)
-// ("DeepSeek-V4昇腾训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse
-// 极简训练优化实践", 性能结果与未来展望: FP8 training on MxFP8 compute; the
-// expert matmuls themselves: "HyperParallel加速DeepSeek-V4.1多模态1M长序列
-// 训练" §2.3 MegaMoE.)
+// ("DeepSeek-V4昇腾训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse 极简训练优化
+// 实践", 性能结果与未来展望: FP8 training on MxFP8 compute; the expert matmuls
+// themselves: "HyperParallel加速DeepSeek-V4.1多模态1M长序列训练" §2.3 MegaMoE.)
 //
-// An E4M3 value times a power-of-two scale is an exact bf16 value, and the
-// products of bf16 values are exact in the fp32 accumulator, so expanding
-// both MX operands to bf16 in shared memory and running the bf16
-// tcgen05.mma gives the sums of a block-scaled MXFP8 MMA up to the order of
-// the fp32 additions.  The operands cross HBM at one byte per element plus
-// one scale byte per 32, half the bytes of bf16; what bounds these GEMMs is
-// the expansion itself (its instructions and its shared-memory traffic: per
-// k-step 24 KB of codes read back and 48 KB of bf16 written, beside the
-// tensor cores' 48 KB of operand reads).
+// The tensor cores read the E4M3 codes straight from shared memory and apply
+// each block's scale from tensor memory, so every product is exact and the
+// sums are fp32: the results are those of the MX definition up to the order
+// of the fp32 additions.  The operands cross HBM at one byte an element plus
+// one scale byte per 32.
 //
-// One CTA per SM, 18 warps:
-//   warp 0      TMA producer: code tiles (A 128 x 64, B 256 x 64 bytes, 64-byte
-//               swizzle) into a 4-stage ring; every 8 k-steps the scale codes
-//               of the tile's rows for those 8 steps (16 bytes a row) into a
-//               2-slot ring.
-//   warp 1      TMEM owner and MMA issuer (bf16, M = 128, N = 256, K = 16;
-//               two accumulators).
+// Tiles are 128 rows x 128 columns (GEMM 1: 64 gate and the matching 64 up
+// columns, i.e. 64 h columns; GEMM 2: 128 output columns), 128 contraction
+// elements per stage.  Tensor memory holds two fp32 accumulators (128 columns
+// each, so one tile's epilogue overlaps the next tile's MMAs) and, per stage,
+// four columns of A scales and four of B scales.  Each of the four lane
+// quadrants computes its 32 rows of D against every column, so it reads the
+// scales of all of B, and of A, from its own lanes: in every quadrant q, lane
+// 32q + j at column (first + c) holds the word of row 32c + j; the
+// instruction descriptor picks its byte -- byte j for the j-th block of 32 of
+// the stage.
+//
+// One CTA per SM, 10 warps:
+//   warp 0      TMA producer: per stage the A and B code tiles (128-byte rows,
+//               128-byte swizzle) and the 16-byte scale rows of A and B that
+//               hold the stage's four scale codes.
+//   warp 1      TMEM owner and MMA issuer (block-scaled MMA, M = 128, N = 128,
+//               K = 32, four per stage).
 //   warps 2-5   epilogue, thread = row: GEMM 1 the clamped SwiGLU and h
 //               quantised to MXFP8 per 32 columns (hardware conversion);
 //               GEMM 2 the routing-weight scale to bf16.
-//   warps 6-17  converters, three per scheduler: thread c expands row c of a
-//               code stage (rows 0-127 A, 128-383 B) into a 128-byte-swizzled
-//               bf16 stage (2 stages), then releases both.  Fewer warps leave
-//               the schedulers idle on the conversion's dependency chains.
+//   warps 6-9   scale writers, one per TMEM lane quadrant, thread = row: the
+//               stage's four A scale codes and four B scale codes of its row
+//               into tensor memory (tcgen05.st), then release the stage to the
+//               MMA issuer.
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and exits.
 #include <cstring>
@@ -45,14 +51,14 @@ namespace {
 enum MxMode : int { MX_FFN1 = 0, MX_FFN2 = 1 };
 
 struct MxParams {
-    CUtensorMap tmA;   // A codes [rows, K] u8, boxes 64 x 128, 64-byte swizzle
-    CUtensorMap tmB;   // B codes [G * b_rows_per_group, K] u8, same boxes
+    CUtensorMap tmA;   // A codes [rows, K] u8, boxes 128 x 128, 128-byte swizzle
+    CUtensorMap tmB;   // B codes [G * b_rows_per_group, K] u8, boxes 128 x 64 (GEMM 1) / 128 x 128
     CUtensorMap tmSA;  // A scale codes [rows, pitch] u8, boxes 16 x 128
-    CUtensorMap tmSB;  // B scale codes [G * b_rows_per_group, pitch] u8
+    CUtensorMap tmSB;  // B scale codes, boxes 16 x 64 (GEMM 1) / 16 x 128
     const int32_t *offsets;
     int G;
     int n_tiles;           // column tiles per row tile
-    int k_blocks;          // K / 64
+    int k_blocks;          // K / 128
     int b_rows_per_group;  // 2I (GEMM 1) or d (GEMM 2)
     int I;
     int N;                 // GEMM 2: output columns (d)
@@ -67,25 +73,25 @@ struct MxParams {
     long long wait_limit;
 };
 
-constexpr int kMxRaw = 4;           // code stages
-constexpr int kMxBf = 2;            // bf16 operand stages
-constexpr int kMxSfSlots = 2;       // scale slots (8 k-steps each)
+constexpr int kMxStages = 5;
+constexpr int kMxCodeA = 128 * 128;   // A codes of a stage
+constexpr int kMxCodeB = 128 * 128;   // B codes
+constexpr int kMxSfRow = 16;          // bytes of a scale row in a stage (4 stages' codes)
+constexpr int kMxSfA = 128 * kMxSfRow;
+constexpr int kMxSfB = 128 * kMxSfRow;
+constexpr int kMxStage = kMxCodeA + kMxCodeB + kMxSfA + kMxSfB;
 constexpr int kMxEpiWarps = 4;
-constexpr int kMxConvWarps = 12;    // one A or B row per thread
-constexpr int kMxThreads = 64 + 32 * (kMxEpiWarps + kMxConvWarps);
-constexpr int kMxRawA = 128 * 64;
-constexpr int kMxRawStage = kMxRawA + 256 * 64;
-constexpr int kMxBfA = 128 * 128;
-constexpr int kMxBfStage = kMxBfA + 256 * 128;
-constexpr int kMxSfA = 128 * 16;
-constexpr int kMxSfSlot = kMxSfA + 256 * 16;
+constexpr int kMxSfWarps = 4;
+constexpr int kMxThreads = 64 + 32 * (kMxEpiWarps + kMxSfWarps);
 constexpr int kMxBarBytes = 256;
-constexpr int kMxFixedSmem = kMxBf * kMxBfStage + kMxRaw * kMxRawStage + kMxSfSlots * kMxSfSlot;
-static_assert((2 * kMxRaw + 2 * kMxBf + 2 * kMxSfSlots + 5) * 8 + 8 <= kMxBarBytes,
-              "barrier block");
+constexpr uint32_t kMxAccCols = 128;
+constexpr uint32_t kMxSfCol0 = 2 * kMxAccCols;   // scale columns after the accumulators
+constexpr uint32_t kMxTmemCols = 512;
+static_assert(kMxSfCol0 + 8 * kMxStages <= kMxTmemCols, "tensor memory columns");
+static_assert((3 * kMxStages + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
 
 inline size_t mx_smem_bytes(int G) {
-    return 1024 + (size_t)kMxFixedSmem + kMxBarBytes + 8 * (size_t)(G + 2);
+    return 1024 + (size_t)kMxStages * kMxStage + kMxBarBytes + 8 * (size_t)(G + 2);
 }
 
 __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int *mt_start,
@@ -106,78 +112,29 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
     return ti;
 }
 
-// Row r of a code tile (64 bytes, 64-byte swizzle) -> row r of a bf16 tile
-// (128 bytes, 128-byte swizzle; inside each group of four contraction
-// elements the order 0, 2, 1, 3, the same for A and B rows); elements 0-31
-// scaled by 2^(sf[0] - 127), 32-63 by 2^(sf[1] - 127).
-template <bool TWO>
-__device__ __forceinline__ void mx_expand_row_t(const uint8_t *codes, const MxBf16Factors &f0,
-                                                const MxBf16Factors &f1, uint8_t *dst, int r) {
-    const uint32_t sw_in = (uint32_t)(r >> 1) & 3u;
-    const uint32_t sw = (uint32_t)r & 7u;
-    const uint8_t *src = codes + r * 64;
-    const uint32_t out = smem_u32(dst + r * 128);
-#pragma unroll
-    for (uint32_t c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ sw_in) << 4));
-        const MxBf16Factors &f = c < 2 ? f0 : f1;
-        uint32_t o[8];
-        e4m3x4_to_bf16x2x2<TWO>(v.x, f, o[0], o[1]);
-        e4m3x4_to_bf16x2x2<TWO>(v.y, f, o[2], o[3]);
-        e4m3x4_to_bf16x2x2<TWO>(v.z, f, o[4], o[5]);
-        e4m3x4_to_bf16x2x2<TWO>(v.w, f, o[6], o[7]);
-        st_shared_v4(out + (((2 * c) ^ sw) << 4), o[0], o[1], o[2], o[3]);
-        st_shared_v4(out + (((2 * c + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
-    }
-}
-
-// One decision per row and k-step: the second multiply only where a block's
-// scale exceeds 2^7 (rare), so the common path carries no per-word test.
-__device__ __forceinline__ void mx_expand_row(const uint8_t *codes, const uint8_t *sf,
-                                              uint8_t *dst, int r) {
-    const MxBf16Factors f0 = mx_bf16_factors(sf[0]);
-    const MxBf16Factors f1 = mx_bf16_factors(sf[1]);
-    if (f0.two || f1.two) mx_expand_row_t<true>(codes, f0, f1, dst, r);
-    else mx_expand_row_t<false>(codes, f0, f1, dst, r);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid_constant__ MxParams p) {
-    constexpr uint32_t IDESC = idesc_bf16_f32(128, 256, false, false);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sBf = smem;
-    uint8_t *sRaw = smem + kMxBf * kMxBfStage;
-    uint8_t *sSf = sRaw + kMxRaw * kMxRawStage;
-    uint64_t *rfull = reinterpret_cast<uint64_t *>(smem + kMxFixedSmem);
-    uint64_t *rempty = rfull + kMxRaw;
-    uint64_t *bfull = rempty + kMxRaw;
-    uint64_t *bempty = bfull + kMxBf;
-    uint64_t *sfull = bempty + kMxBf;
-    uint64_t *sempty = sfull + kMxSfSlots;
-    uint64_t *tfull = sempty + kMxSfSlots;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kMxStages * kMxStage);
+    uint64_t *sfready = full + kMxStages;   // the stage's scales are in tensor memory
+    uint64_t *empty = sfready + kMxStages;
+    uint64_t *tfull = empty + kMxStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
-    int *offs = reinterpret_cast<int *>(smem + kMxFixedSmem + kMxBarBytes);
+    int *offs = reinterpret_cast<int *>(smem + kMxStages * kMxStage + kMxBarBytes);
     int *mt_start = offs + (p.G + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kMxRaw; ++s) {
-            mbar_init(&rfull[s], 1);
-            mbar_init(&rempty[s], kMxConvWarps);
-        }
-        for (int s = 0; s < kMxBf; ++s) {
-            mbar_init(&bfull[s], kMxConvWarps);
-            mbar_init(&bempty[s], 1);
-        }
-        for (int s = 0; s < kMxSfSlots; ++s) {
-            mbar_init(&sfull[s], 1);
-            mbar_init(&sempty[s], kMxConvWarps);
+        for (int s = 0; s < kMxStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&sfready[s], kMxSfWarps);
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -194,7 +151,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
         tma_prefetch_desc(&p.tmSB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_base_s, 512);
+        tmem_alloc(tmem_base_s, kMxTmemCols);
         tmem_relinquish();
     }
     if (warp == 2) {
@@ -233,52 +190,49 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int last_r[kMxRaw], last_s[kMxSfSlots];
+            int last_par[kMxStages];
 #pragma unroll
-            for (int i = 0; i < kMxRaw; ++i) last_r[i] = -1;
-#pragma unroll
-            for (int i = 0; i < kMxSfSlots; ++i) last_s[i] = -1;
-            uint32_t s = 0, ph = 0, js = 0, phs = 0;
+            for (int i = 0; i < kMxStages; ++i) last_par[i] = -1;
+            uint32_t s = 0, ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
                 const TileInfo ti = mx_tile(p, t, mt_start, offs);
-                // B rows of the tile: GEMM 1 the gate rows and the up rows of
-                // its 128 h columns, GEMM 2 256 consecutive output rows
-                const int brow = ti.g * p.b_rows_per_group + ti.nt * (MODE == MX_FFN1 ? 128 : 256);
-                const int brow2 = MODE == MX_FFN1 ? brow + p.I : brow + 128;
+                // B rows of the tile: GEMM 1 the gate rows and the up rows of its
+                // 64 h columns, GEMM 2 128 consecutive output rows
+                const int brow = ti.g * p.b_rows_per_group + ti.nt * (MODE == MX_FFN1 ? 64 : 128);
                 for (int kb = 0; kb < ti.kb; ++kb) {
-                    if ((kb & 7) == 0) {
-                        if (!mbar_wait(&sempty[js], phs ^ 1u, wc)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&sfull[js], kMxSfSlot);
-                        uint8_t *d = sSf + js * kMxSfSlot;
-                        const int x = (kb >> 3) * 16;
-                        tma_load_2d(d, &p.tmSA, &sfull[js], x, ti.row0);
-                        tma_load_2d(d + kMxSfA, &p.tmSB, &sfull[js], x, brow);
-                        tma_load_2d(d + kMxSfA + 128 * 16, &p.tmSB, &sfull[js], x, brow2);
-                        last_s[js] = (int)phs;
-                        if (++js == kMxSfSlots) { js = 0; phs ^= 1u; }
+                    if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], kMxStage);
+                    uint8_t *a = smem + s * kMxStage;
+                    uint8_t *b = a + kMxCodeA;
+                    uint8_t *sa = b + kMxCodeB;
+                    uint8_t *sb = sa + kMxSfA;
+                    const int x = (kb >> 2) * kMxSfRow;   // the 16 scale bytes holding this stage's 4
+                    tma_load_2d(a, &p.tmA, &full[s], kb * 128, ti.row0);
+                    tma_load_2d(sa, &p.tmSA, &full[s], x, ti.row0);
+                    if constexpr (MODE == MX_FFN1) {
+                        tma_load_2d(b, &p.tmB, &full[s], kb * 128, brow);
+                        tma_load_2d(b + 64 * 128, &p.tmB, &full[s], kb * 128, brow + p.I);
+                        tma_load_2d(sb, &p.tmSB, &full[s], x, brow);
+                        tma_load_2d(sb + 64 * kMxSfRow, &p.tmSB, &full[s], x, brow + p.I);
+                    } else {
+                        tma_load_2d(b, &p.tmB, &full[s], kb * 128, brow);
+                        tma_load_2d(sb, &p.tmSB, &full[s], x, brow);
                     }
-                    if (!mbar_wait(&rempty[s], ph ^ 1u, wc)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&rfull[s], kMxRawStage);
-                    uint8_t *a = sRaw + s * kMxRawStage;
-                    tma_load_2d(a, &p.tmA, &rfull[s], kb * 64, ti.row0);
-                    tma_load_2d(a + kMxRawA, &p.tmB, &rfull[s], kb * 64, brow);
-                    tma_load_2d(a + kMxRawA + 128 * 64, &p.tmB, &rfull[s], kb * 64, brow2);
-                    last_r[s] = (int)ph;
-                    if (++s == kMxRaw) { s = 0; ph ^= 1u; }
+                    last_par[s] = (int)ph;
+                    if (++s == kMxStages) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // drain the copies still in flight before the CTA exits
-                for (int i = 0; i < kMxRaw; ++i)
-                    if (last_r[i] >= 0) mbar_wait_teardown(&rfull[i], (uint32_t)last_r[i], p.wait_limit);
-                for (int i = 0; i < kMxSfSlots; ++i)
-                    if (last_s[i] >= 0) mbar_wait_teardown(&sfull[i], (uint32_t)last_s[i], p.wait_limit);
+                for (int i = 0; i < kMxStages; ++i)
+                    if (last_par[i] >= 0)
+                        mbar_wait_teardown(&full[i], (uint32_t)last_par[i], p.wait_limit);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        uint32_t sb = 0, phb = 0;
+        uint32_t s = 0, ph = 0;
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
@@ -287,22 +241,25 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
             const uint32_t aph = (it >> 1) & 1;
             if (!mbar_wait(&tempty[acc], aph ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * 256;
+            const uint32_t d_tmem = tmem_base + acc * kMxAccCols;
             for (int kb = 0; kb < ti.kb; ++kb) {
-                if (!mbar_wait(&bfull[sb], phb, wc)) { ok = false; break; }
+                // the scale writers waited for the stage's copies first
+                if (!mbar_wait(&sfready[s], ph, wc)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t a_addr = smem_u32(sBf + sb * kMxBfStage);
-                    const uint32_t b_addr = a_addr + kMxBfA;
+                    const uint32_t a_addr = smem_u32(smem + s * kMxStage);
+                    const uint32_t b_addr = a_addr + kMxCodeA;
+                    const uint32_t sfa = tmem_base + kMxSfCol0 + 8u * s;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d_tmem, sdesc_sw128(a_addr + kk * 32, 16, 1024),
-                                  sdesc_sw128(b_addr + kk * 32, 16, 1024), IDESC,
+                        umma_mxf8(d_tmem, sdesc_sw128(a_addr + kk * 32, 16, 1024),
+                                  sdesc_sw128(b_addr + kk * 32, 16, 1024),
+                                  idesc_mxf8_f32(128, 128, (uint32_t)kk), sfa, sfa + 4,
                                   (kb | kk) != 0 ? 1u : 0u);
-                    umma_commit(&bempty[sb]);
+                    umma_commit(&empty[s]);
                 }
                 __syncwarp();
-                if (++sb == kMxBf) { sb = 0; phb ^= 1u; }
+                if (++s == kMxStages) { s = 0; ph ^= 1u; }
             }
             if (!ok) break;
             if (lane == 0) umma_commit(&tfull[acc]);
@@ -315,39 +272,38 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
             mbar_wait_teardown(done, 0, p.wait_limit);
         }
     } else if (warp >= 2 + kMxEpiWarps) {
-        // ------------------------------------------------ converters
-        // rows 0..127: A, 128..383: B; warps hold one kind of row each
-        const int ct = (warp - 2 - kMxEpiWarps) * 32 + lane;   // 0..383
-        const bool is_a = ct < 128;
-        const int r = is_a ? ct : ct - 128;
-        uint32_t s = 0, ph = 0, sb = 0, phb = 0, js = 0, phs = 0;
+        // ------------------------------------------------ scale writers
+        // per stage, the word of the stage's four scale codes of every A and B
+        // row, in the layout the tensor cores read: each lane quadrant holds
+        // all 128 rows of A and of B, lane 32q + j at column (first + c)
+        // holding row 32c + j (A at the stage's first four scale columns, B at
+        // the next four)
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+        uint32_t s = 0, ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
             const TileInfo ti = mx_tile(p, t, mt_start, offs);
             for (int kb = 0; kb < ti.kb; ++kb) {
-                if ((kb & 7) == 0 && !mbar_wait(&sfull[js], phs, wc)) { ok = false; break; }
-                if (!mbar_wait(&rfull[s], ph, wc)) { ok = false; break; }
-                if (!mbar_wait(&bempty[sb], phb ^ 1u, wc)) { ok = false; break; }
-                const uint8_t *raw = sRaw + s * kMxRawStage;
-                const uint8_t *sf = sSf + js * kMxSfSlot + (kb & 7) * 2;
-                uint8_t *bf = sBf + sb * kMxBfStage;
-                // A rows past the group's end feed only accumulator rows that are
-                // never stored (MMA rows are independent), so they are not expanded
-                if (!is_a) mx_expand_row(raw + kMxRawA, sf + kMxSfA + r * 16, bf + kMxBfA, r);
-                else if (r < ti.rows_valid) mx_expand_row(raw, sf + r * 16, bf, r);
-                // the tensor cores read the stage through the async proxy
-                fence_proxy_async_smem();
+                if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
+                const uint8_t *sa = smem + s * kMxStage + kMxCodeA + kMxCodeB;
+                const uint8_t *sb = sa + kMxSfA;
+                const uint32_t koff = (uint32_t)(kb & 3) * 4u;
+                uint32_t wa[4], wb[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t off = (uint32_t)(32 * c + lane) * kMxSfRow + koff;
+                    wa[c] = *reinterpret_cast<const uint32_t *>(sa + off);
+                    wb[c] = *reinterpret_cast<const uint32_t *>(sb + off);
+                }
+                const uint32_t col = kMxSfCol0 + 8u * s;
+                tmem_st4(lane_base + col, wa[0], wa[1], wa[2], wa[3]);
+                tmem_st4(lane_base + col + 4u, wb[0], wb[1], wb[2], wb[3]);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bfull[sb]);
-                    mbar_arrive(&rempty[s]);
-                }
-                if (++s == kMxRaw) { s = 0; ph ^= 1u; }
-                if (++sb == kMxBf) { sb = 0; phb ^= 1u; }
-                if ((kb & 7) == 7 || kb == ti.kb - 1) {
-                    if (lane == 0) mbar_arrive(&sempty[js]);
-                    if (++js == kMxSfSlots) { js = 0; phs ^= 1u; }
-                }
+                if (lane == 0) mbar_arrive(&sfready[s]);
+                if (++s == kMxStages) { s = 0; ph ^= 1u; }
             }
         }
     } else {
@@ -361,15 +317,15 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
             const uint32_t aph = (it >> 1) & 1;
             if (!mbar_wait(&tfull[acc], aph, wc)) break;
             tc_fence_after();
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kMxAccCols;
             const bool valid = r_local < ti.rows_valid;
             const int row = ti.row0 + r_local;
             if constexpr (MODE == MX_FFN1) {
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
+                for (int c = 0; c < 64; c += 32) {
                     uint32_t rg[32], ru[32];
                     tmem_ld32(tb + c, rg);
-                    tmem_ld32(tb + 128 + c, ru);
+                    tmem_ld32(tb + 64 + c, ru);
                     tmem_wait_ld();
                     if (valid) {
                         float hv[32];
@@ -379,7 +335,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                                                    p.clamp);
                         uint32_t w[8];
                         const uint32_t code = mx_quantize_block_hw(hv, w);
-                        const int col = ti.nt * 128 + c;
+                        const int col = ti.nt * 64 + c;
                         uint8_t *dst = p.hq + (size_t)row * p.I + col;
                         st_global_v4(dst, w[0], w[1], w[2], w[3]);
                         st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
@@ -389,7 +345,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
             } else {
                 float w = 1.0f;
                 if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
-                epi_bf16_scaled<256>(p.y, p.N, ti, tb, valid, row, w);
+                epi_bf16_scaled<128>(p.y, p.N, ti, tb, valid, row, w);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -399,7 +355,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, 512);
+    if (warp == 1) tmem_dealloc(tmem_base, kMxTmemCols);
 }
 
 template <int MODE>
@@ -434,15 +390,15 @@ moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *
     std::memset(&p, 0, sizeof p);
     const int sfd = mx_sf_pitch(d);
     const uint64_t brows = (uint64_t)G * 2 * I;
-    if (!encode_tmap_u8_2d(&p.tmA, xq, d, max_rows, d, 64, 128, 64) ||
-        !encode_tmap_u8_2d(&p.tmB, W13q, d, brows, d, 64, 128, 64) ||
+    if (!encode_tmap_u8_2d(&p.tmA, xq, d, max_rows, d, 128, 128, 128) ||
+        !encode_tmap_u8_2d(&p.tmB, W13q, d, brows, d, 128, 64, 128) ||
         !encode_tmap_u8_2d(&p.tmSA, xsf, sfd, max_rows, sfd, 16, 128, 0) ||
-        !encode_tmap_u8_2d(&p.tmSB, W13sf, sfd, brows, sfd, 16, 128, 0))
+        !encode_tmap_u8_2d(&p.tmSB, W13sf, sfd, brows, sfd, 16, 64, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
-    p.n_tiles = I / 128;
-    p.k_blocks = d / 64;
+    p.n_tiles = I / 64;
+    p.k_blocks = d / 128;
     p.b_rows_per_group = 2 * I;
     p.I = I;
     p.clamp = clamp;
@@ -460,15 +416,15 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
     std::memset(&p, 0, sizeof p);
     const int sfi = mx_sf_pitch(I);
     const uint64_t brows = (uint64_t)G * d;
-    if (!encode_tmap_u8_2d(&p.tmA, hq, I, max_rows, I, 64, 128, 64) ||
-        !encode_tmap_u8_2d(&p.tmB, W2q, I, brows, I, 64, 128, 64) ||
+    if (!encode_tmap_u8_2d(&p.tmA, hq, I, max_rows, I, 128, 128, 128) ||
+        !encode_tmap_u8_2d(&p.tmB, W2q, I, brows, I, 128, 128, 128) ||
         !encode_tmap_u8_2d(&p.tmSA, hsf, sfi, max_rows, sfi, 16, 128, 0) ||
         !encode_tmap_u8_2d(&p.tmSB, W2sf, sfi, brows, sfi, 16, 128, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
-    p.n_tiles = d / 256;
-    p.k_blocks = I / 64;
+    p.n_tiles = d / 128;
+    p.k_blocks = I / 128;
     p.b_rows_per_group = d;
     p.I = I;
     p.N = d;

@@ -314,6 +314,52 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= (A[smem] * SFA) (B[smem] * SFB)^T: E4M3 operands (one byte an
+// element, K = 32 per instruction), E8M0 scale per block of 32 along K read
+// from TMEM (block-scaled MMA, kind::mxf8f6f4, one scale per 32 elements),
+// fp32 accumulator.  The instruction descriptor picks which byte of each
+// scale word applies (idesc_mxf8_f32).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of the block-scaled MMA with E4M3 A and B, E8M0
+// scales and an fp32 D: B scale byte [4,6); A / B format [7,10) / [10,13) = 0
+// (E4M3); K-major A and B; N >> 3 at [17,23); scale format [23] = 1 (E8M0);
+// M >> 4 at [24,29); A scale byte [29,31).
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, uint32_t sf_byte) {
+    return (sf_byte << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | (sf_byte << 29);
+}
+
+// Stores one 32-bit word per thread into TMEM (32x32b shape: warp w writes
+// lanes 32*(w%4) .. +31 at column taddr & 0xFFFF).  tmem_wait_st() before the
+// words may be read by an MMA.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+                 : "memory");
+}
+
+// Four consecutive TMEM columns of this thread's lane (32x32b.x4).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
+                                         uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {

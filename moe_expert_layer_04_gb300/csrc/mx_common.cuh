@@ -92,8 +92,8 @@ __device__ __forceinline__ uint32_t mx_quantize_block(const float (&v)[32], uint
 
 // The same quantisation of one block with the hardware conversion
 // (cvt.rn.satfinite: nearest-even, saturating at 448), for the expert GEMM's
-// epilogue, where it takes a fraction of the issue slots of e4m3_rne and
-// leaves them to the converter warps.  The quantiser kernel keeps e4m3_rne.
+// epilogue, where it takes a fraction of the issue slots of e4m3_rne.  The
+// quantiser kernel keeps e4m3_rne.
 __device__ __forceinline__ uint32_t mx_quantize_block_hw(const float (&v)[32], uint32_t (&w)[8]) {
     float amax = 0.0f;
 #pragma unroll
@@ -110,56 +110,6 @@ __device__ __forceinline__ uint32_t mx_quantize_block_hw(const float (&v)[32], u
         w[j] = (uint32_t)a | ((uint32_t)b << 16);
     }
     return code;
-}
-
-// E4M3 -> bf16 without conversion instructions.  Placing a code's bits 6..0
-// at bf16 bits 10..4 and its sign at bit 15 gives a bf16 whose value is the
-// code's value times 2^-120, for normal codes ((1 + m/8) 2^(E-7) against
-// (1 + m/8) 2^(E-127)) and subnormal ones (m/8 2^-6 against the bf16
-// subnormal m/8 2^-126) alike; one bf16x2 multiply by 2^(120 + se) then gives
-// the code's value times the block scale 2^se, exactly while the product is a
-// normal bf16 (block scales down to 2^-117).
-
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// The factors for a block with scale code c (se = c - 127): f1 = 2^(120 + se)
-// as bf16x2, and f2 = 1 unless 120 + se passes bf16's largest exponent 127,
-// where f1 = 2^127 and f2 = 2^(se - 7).
-struct MxBf16Factors {
-    uint32_t f1, f2;
-    bool two;
-};
-
-__device__ __forceinline__ MxBf16Factors mx_bf16_factors(uint32_t code) {
-    MxBf16Factors f;
-    f.two = code > 134u;
-    const uint32_t e1 = f.two ? 254u : code + 120u;   // biased bf16 exponent of f1
-    const uint32_t e2 = f.two ? code - 7u : 127u;
-    f.f1 = (e1 << 7) | (e1 << 23);
-    f.f2 = (e2 << 7) | (e2 << 23);
-    return f;
-}
-
-// Four E4M3 codes (byte i of w = element i) -> two bf16x2 words times the
-// block scale: lo holds elements 0 (low half) and 2, hi elements 1 and 3.
-// Shifts and masks of w alone place every code (no byte permutes), at the
-// price of the order 0, 2, 1, 3 inside each group of four; A and B rows go
-// through the same expansion, so both operands of the matmul carry the same
-// permutation of the contraction index and every dot product is unchanged.
-// TWO applies f2 as well (needed only when the scale exceeds 2^7).
-template <bool TWO>
-__device__ __forceinline__ void e4m3x4_to_bf16x2x2(uint32_t w, const MxBf16Factors &f,
-                                                   uint32_t &lo, uint32_t &hi) {
-    lo = mul_bf16x2(((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u), f.f1);
-    hi = mul_bf16x2(((w >> 4) & 0x07F007F0u) | (w & 0x80008000u), f.f1);
-    if constexpr (TWO) {   // f2 == 1 unless the block's scale exceeds 2^7
-        lo = mul_bf16x2(lo, f.f2);
-        hi = mul_bf16x2(hi, f.f2);
-    }
 }
 
 }  // namespace moe
