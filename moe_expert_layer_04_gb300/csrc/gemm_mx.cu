@@ -14,11 +14,15 @@
 // of the fp32 additions.  The operands cross HBM at one byte an element plus
 // one scale byte per 32.
 //
-// Tiles are 128 rows x 128 columns (GEMM 1: 64 gate and the matching 64 up
-// columns, i.e. 64 h columns; GEMM 2: 128 output columns), 128 contraction
-// elements per stage.  Tensor memory holds two fp32 accumulators (128 columns
-// each, so one tile's epilogue overlaps the next tile's MMAs) and, per stage,
-// four columns of A scales and four of B scales.  Each of the four lane
+// Tiles are 128 rows x BN columns (GEMM 1: BN/2 gate and the matching BN/2
+// up columns, i.e. BN/2 h columns; GEMM 2: BN output columns), 128
+// contraction elements per stage.  BN = 128: two fp32 accumulators (one
+// tile's epilogue overlaps the next tile's MMAs), for few rows per expert,
+// where the weights stream from HBM.  BN = 256: one accumulator (512 tensor
+// memory columns would leave none for the scales), half the operand bytes per
+// MMA from L2, for many rows per expert, where the MMAs set the pace.  Per
+// stage tensor memory also holds four columns of A scales and BN/32 of B
+// scales.  Each of the four lane
 // quadrants computes its 32 rows of D against every column, so it reads the
 // scales of all of B, and of A, from its own lanes: in every quadrant q, lane
 // 32q + j at column (first + c) holds the word of row 32c + j; the
@@ -73,25 +77,33 @@ struct MxParams {
     long long wait_limit;
 };
 
-constexpr int kMxStages = 5;
+constexpr int kMxSfRow = 16;          // bytes of a scale row in a slot (4 stages' codes)
 constexpr int kMxCodeA = 128 * 128;   // A codes of a stage
-constexpr int kMxCodeB = 128 * 128;   // B codes
-constexpr int kMxSfRow = 16;          // bytes of a scale row in a stage (4 stages' codes)
 constexpr int kMxSfA = 128 * kMxSfRow;
-constexpr int kMxSfB = 128 * kMxSfRow;
-constexpr int kMxStage = kMxCodeA + kMxCodeB + kMxSfA + kMxSfB;
-constexpr int kMxEpiWarps = 4;
 constexpr int kMxSfWarps = 4;
-constexpr int kMxThreads = 64 + 32 * (kMxEpiWarps + kMxSfWarps);
+constexpr int kMxSfSlots = 2;         // scale slots, 4 stages each
 constexpr int kMxBarBytes = 256;
-constexpr uint32_t kMxAccCols = 128;
-constexpr uint32_t kMxSfCol0 = 2 * kMxAccCols;   // scale columns after the accumulators
 constexpr uint32_t kMxTmemCols = 512;
-static_assert(kMxSfCol0 + 8 * kMxStages <= kMxTmemCols, "tensor memory columns");
-static_assert((3 * kMxStages + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
 
+template <int BN>
+struct MxShape {
+    static constexpr int CODE_B = BN * 128;
+    static constexpr int STAGE = kMxCodeA + CODE_B;              // codes of a stage
+    static constexpr int SF_SLOT = kMxSfA + BN * kMxSfRow;        // scales of 4 stages
+    static constexpr int STAGES = 4;
+    static constexpr int NACC = BN == 256 ? 1 : 2;                // accumulators
+    static constexpr int NEPI = BN == 256 ? 8 : 4;                // epilogue warps
+    static constexpr int THREADS = 64 + 32 * (NEPI + kMxSfWarps);
+    static constexpr uint32_t SF_COL0 = NACC * BN;                // scale columns after them
+    static constexpr uint32_t SF_COLS = 4 + BN / 32;              // per stage: A, then B
+    static constexpr int FIXED = STAGES * STAGE + kMxSfSlots * SF_SLOT;
+    static_assert(SF_COL0 + SF_COLS * STAGES <= kMxTmemCols, "tensor memory columns");
+    static_assert((4 * STAGES + 2 * kMxSfSlots + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
+};
+
+template <int BN>
 inline size_t mx_smem_bytes(int G) {
-    return 1024 + (size_t)kMxStages * kMxStage + kMxBarBytes + 8 * (size_t)(G + 2);
+    return 1024 + (size_t)MxShape<BN>::FIXED + kMxBarBytes + 8 * (size_t)(G + 2);
 }
 
 __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int *mt_start,
@@ -112,33 +124,48 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
     return ti;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid_constant__ MxParams p) {
+template <int MODE, int BN>
+__global__ void __launch_bounds__(MxShape<BN>::THREADS, 1)
+    moe_mx_gemm_kernel(const __grid_constant__ MxParams p) {
+    using SH = MxShape<BN>;
+    constexpr int STAGES = SH::STAGES;
+    constexpr int NACC = SH::NACC;
+    constexpr int NEPI = SH::NEPI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kMxStages * kMxStage);
-    uint64_t *sfready = full + kMxStages;   // the stage's scales are in tensor memory
-    uint64_t *empty = sfready + kMxStages;
-    uint64_t *tfull = empty + kMxStages;
+    uint8_t *sCodes = smem;                                   // STAGES x (A | B codes)
+    uint8_t *sSf = smem + STAGES * SH::STAGE;                 // kMxSfSlots x (A | B scales)
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SH::FIXED);
+    uint64_t *empty = full + STAGES;      // the stage's MMAs are done (codes and scales free)
+    uint64_t *sfready = empty + STAGES;   // the stage's scales are in tensor memory
+    uint64_t *spare = sfready + STAGES;   // (unused; keeps the block layout simple)
+    uint64_t *sffull = spare + STAGES;    // a scale slot landed
+    uint64_t *sfempty = sffull + kMxSfSlots;   // the scale writers are done with a slot
+    uint64_t *tfull = sfempty + kMxSfSlots;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
-    int *offs = reinterpret_cast<int *>(smem + kMxStages * kMxStage + kMxBarBytes);
+    int *offs = reinterpret_cast<int *>(smem + SH::FIXED + kMxBarBytes);
     int *mt_start = offs + (p.G + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kMxStages; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&sfready[s], kMxSfWarps);
             mbar_init(&empty[s], 1);
+            mbar_init(&sfready[s], kMxSfWarps);
+            mbar_init(&spare[s], 1);
+        }
+        for (int j = 0; j < kMxSfSlots; ++j) {
+            mbar_init(&sffull[j], 1);
+            mbar_init(&sfempty[j], kMxSfWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 32 * kMxEpiWarps);
+            mbar_init(&tempty[a], 32 * NEPI);
         }
         mbar_init(done, 1);
         *abort_s = 0;
@@ -190,44 +217,60 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int last_par[kMxStages];
+            int last_par[STAGES], last_sf[kMxSfSlots];
 #pragma unroll
-            for (int i = 0; i < kMxStages; ++i) last_par[i] = -1;
-            uint32_t s = 0, ph = 0;
+            for (int i = 0; i < STAGES; ++i) last_par[i] = -1;
+#pragma unroll
+            for (int i = 0; i < kMxSfSlots; ++i) last_sf[i] = -1;
+            uint32_t s = 0, ph = 0, js = 0, phs = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
                 const TileInfo ti = mx_tile(p, t, mt_start, offs);
                 // B rows of the tile: GEMM 1 the gate rows and the up rows of its
-                // 64 h columns, GEMM 2 128 consecutive output rows
-                const int brow = ti.g * p.b_rows_per_group + ti.nt * (MODE == MX_FFN1 ? 64 : 128);
+                // BN/2 h columns, GEMM 2 BN consecutive output rows
+                const int brow = ti.g * p.b_rows_per_group + ti.nt * (MODE == MX_FFN1 ? BN / 2 : BN);
                 for (int kb = 0; kb < ti.kb; ++kb) {
+                    if ((kb & 3) == 0) {
+                        // the scale codes of this and the next three stages (16 bytes a row)
+                        if (!mbar_wait(&sfempty[js], phs ^ 1u, wc)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&sffull[js], SH::SF_SLOT);
+                        uint8_t *sa = sSf + js * SH::SF_SLOT;
+                        uint8_t *sb = sa + kMxSfA;
+                        const int x = (kb >> 2) * kMxSfRow;
+                        tma_load_2d(sa, &p.tmSA, &sffull[js], x, ti.row0);
+                        if constexpr (MODE == MX_FFN1) {
+                            tma_load_2d(sb, &p.tmSB, &sffull[js], x, brow);
+                            tma_load_2d(sb + (BN / 2) * kMxSfRow, &p.tmSB, &sffull[js], x,
+                                        brow + p.I);
+                        } else {
+                            tma_load_2d(sb, &p.tmSB, &sffull[js], x, brow);
+                        }
+                        last_sf[js] = (int)phs;
+                        if (++js == kMxSfSlots) { js = 0; phs ^= 1u; }
+                    }
                     if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], kMxStage);
-                    uint8_t *a = smem + s * kMxStage;
+                    mbar_arrive_expect_tx(&full[s], SH::STAGE);
+                    uint8_t *a = sCodes + s * SH::STAGE;
                     uint8_t *b = a + kMxCodeA;
-                    uint8_t *sa = b + kMxCodeB;
-                    uint8_t *sb = sa + kMxSfA;
-                    const int x = (kb >> 2) * kMxSfRow;   // the 16 scale bytes holding this stage's 4
                     tma_load_2d(a, &p.tmA, &full[s], kb * 128, ti.row0);
-                    tma_load_2d(sa, &p.tmSA, &full[s], x, ti.row0);
                     if constexpr (MODE == MX_FFN1) {
                         tma_load_2d(b, &p.tmB, &full[s], kb * 128, brow);
-                        tma_load_2d(b + 64 * 128, &p.tmB, &full[s], kb * 128, brow + p.I);
-                        tma_load_2d(sb, &p.tmSB, &full[s], x, brow);
-                        tma_load_2d(sb + 64 * kMxSfRow, &p.tmSB, &full[s], x, brow + p.I);
+                        tma_load_2d(b + (BN / 2) * 128, &p.tmB, &full[s], kb * 128, brow + p.I);
                     } else {
                         tma_load_2d(b, &p.tmB, &full[s], kb * 128, brow);
-                        tma_load_2d(sb, &p.tmSB, &full[s], x, brow);
                     }
                     last_par[s] = (int)ph;
-                    if (++s == kMxStages) { s = 0; ph ^= 1u; }
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // drain the copies still in flight before the CTA exits
-                for (int i = 0; i < kMxStages; ++i)
+                for (int i = 0; i < STAGES; ++i)
                     if (last_par[i] >= 0)
                         mbar_wait_teardown(&full[i], (uint32_t)last_par[i], p.wait_limit);
+                for (int i = 0; i < kMxSfSlots; ++i)
+                    if (last_sf[i] >= 0)
+                        mbar_wait_teardown(&sffull[i], (uint32_t)last_sf[i], p.wait_limit);
             }
         }
     } else if (warp == 1) {
@@ -237,29 +280,29 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
             const TileInfo ti = mx_tile(p, t, mt_start, offs);
-            const uint32_t acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            const uint32_t acc = NACC == 2 ? (it & 1) : 0;
+            const uint32_t aph = NACC == 2 ? ((it >> 1) & 1) : (it & 1);
             if (!mbar_wait(&tempty[acc], aph ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * kMxAccCols;
+            const uint32_t d_tmem = tmem_base + acc * BN;
             for (int kb = 0; kb < ti.kb; ++kb) {
-                // the scale writers waited for the stage's copies first
+                if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
                 if (!mbar_wait(&sfready[s], ph, wc)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t a_addr = smem_u32(smem + s * kMxStage);
+                    const uint32_t a_addr = smem_u32(sCodes + s * SH::STAGE);
                     const uint32_t b_addr = a_addr + kMxCodeA;
-                    const uint32_t sfa = tmem_base + kMxSfCol0 + 8u * s;
+                    const uint32_t sfa = tmem_base + SH::SF_COL0 + SH::SF_COLS * s;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_mxf8(d_tmem, sdesc_sw128(a_addr + kk * 32, 16, 1024),
                                   sdesc_sw128(b_addr + kk * 32, 16, 1024),
-                                  idesc_mxf8_f32(128, 128, (uint32_t)kk), sfa, sfa + 4,
+                                  idesc_mxf8_f32(128, BN, (uint32_t)kk), sfa, sfa + 4,
                                   (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(&empty[s]);
                 }
                 __syncwarp();
-                if (++s == kMxStages) { s = 0; ph ^= 1u; }
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
             if (!ok) break;
             if (lane == 0) umma_commit(&tfull[acc]);
@@ -271,61 +314,77 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
             __syncwarp();
             mbar_wait_teardown(done, 0, p.wait_limit);
         }
-    } else if (warp >= 2 + kMxEpiWarps) {
+    } else if (warp >= 2 + NEPI) {
         // ------------------------------------------------ scale writers
         // per stage, the word of the stage's four scale codes of every A and B
         // row, in the layout the tensor cores read: each lane quadrant holds
-        // all 128 rows of A and of B, lane 32q + j at column (first + c)
-        // holding row 32c + j (A at the stage's first four scale columns, B at
-        // the next four)
+        // all 128 rows of A and all BN rows of B, lane 32q + j at column
+        // (first + c) holding row 32c + j (A at the stage's first four scale
+        // columns, B at the next BN/32).  A stage's columns are rewritten once
+        // its previous MMAs are done (empty), ahead of its codes.
         const int q = warp & 3;
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-        uint32_t s = 0, ph = 0;
+        uint32_t s = 0, ph = 0, js = 0, phs = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
             const TileInfo ti = mx_tile(p, t, mt_start, offs);
             for (int kb = 0; kb < ti.kb; ++kb) {
-                if (!mbar_wait(&full[s], ph, wc)) { ok = false; break; }
-                const uint8_t *sa = smem + s * kMxStage + kMxCodeA + kMxCodeB;
+                if ((kb & 3) == 0 && !mbar_wait(&sffull[js], phs, wc)) { ok = false; break; }
+                if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
+                tc_fence_after();
+                const uint8_t *sa = sSf + js * SH::SF_SLOT;
                 const uint8_t *sb = sa + kMxSfA;
                 const uint32_t koff = (uint32_t)(kb & 3) * 4u;
-                uint32_t wa[4], wb[4];
+                uint32_t wa[4], wb[BN / 32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t off = (uint32_t)(32 * c + lane) * kMxSfRow + koff;
-                    wa[c] = *reinterpret_cast<const uint32_t *>(sa + off);
-                    wb[c] = *reinterpret_cast<const uint32_t *>(sb + off);
-                }
-                const uint32_t col = kMxSfCol0 + 8u * s;
+                for (int c = 0; c < 4; ++c)
+                    wa[c] = *reinterpret_cast<const uint32_t *>(
+                        sa + (uint32_t)(32 * c + lane) * kMxSfRow + koff);
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    wb[c] = *reinterpret_cast<const uint32_t *>(
+                        sb + (uint32_t)(32 * c + lane) * kMxSfRow + koff);
+                const uint32_t col = SH::SF_COL0 + SH::SF_COLS * s;
                 tmem_st4(lane_base + col, wa[0], wa[1], wa[2], wa[3]);
-                tmem_st4(lane_base + col + 4u, wb[0], wb[1], wb[2], wb[3]);
+#pragma unroll
+                for (int c = 0; c < BN / 32; c += 4)
+                    tmem_st4(lane_base + col + 4u + c, wb[c], wb[c + 1], wb[c + 2], wb[c + 3]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sfready[s]);
-                if (++s == kMxStages) { s = 0; ph ^= 1u; }
+                if ((kb & 3) == 3 || kb == ti.kb - 1) {
+                    if (lane == 0) mbar_arrive(&sfempty[js]);
+                    if (++js == kMxSfSlots) { js = 0; phs ^= 1u; }
+                }
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2-5)
+        // ------------------------------------------------ epilogue (warps 2..)
+        // NEPI / 4 warps per TMEM lane quadrant, each taking an equal share of
+        // the tile's columns
         const int q = warp & 3;   // TMEM lane quadrant this warp may read
+        const int part = (warp - 2) >> 2;
+        constexpr int NPART = NEPI / 4;
         const int r_local = q * 32 + lane;
         int it = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
             const TileInfo ti = mx_tile(p, t, mt_start, offs);
-            const uint32_t acc = it & 1;
-            const uint32_t aph = (it >> 1) & 1;
+            const uint32_t acc = NACC == 2 ? (it & 1) : 0;
+            const uint32_t aph = NACC == 2 ? ((it >> 1) & 1) : (it & 1);
             if (!mbar_wait(&tfull[acc], aph, wc)) break;
             tc_fence_after();
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kMxAccCols;
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             const bool valid = r_local < ti.rows_valid;
             const int row = ti.row0 + r_local;
             if constexpr (MODE == MX_FFN1) {
+                constexpr int HC = BN / 2 / NPART;   // h columns of this warp
 #pragma unroll 1
-                for (int c = 0; c < 64; c += 32) {
+                for (int c = part * HC; c < (part + 1) * HC; c += 32) {
                     uint32_t rg[32], ru[32];
                     tmem_ld32(tb + c, rg);
-                    tmem_ld32(tb + 64 + c, ru);
+                    tmem_ld32(tb + BN / 2 + c, ru);
                     tmem_wait_ld();
                     if (valid) {
                         float hv[32];
@@ -335,7 +394,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                                                    p.clamp);
                         uint32_t w[8];
                         const uint32_t code = mx_quantize_block_hw(hv, w);
-                        const int col = ti.nt * 64 + c;
+                        const int col = ti.nt * (BN / 2) + c;
                         uint8_t *dst = p.hq + (size_t)row * p.I + col;
                         st_global_v4(dst, w[0], w[1], w[2], w[3]);
                         st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
@@ -343,9 +402,29 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
                     }
                 }
             } else {
+                constexpr int YC = BN / NPART;       // output columns of this warp
                 float w = 1.0f;
                 if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
-                epi_bf16_scaled<128>(p.y, p.N, ti, tb, valid, row, w);
+#pragma unroll 1
+                for (int c = part * YC; c < (part + 1) * YC; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c, r);
+                    tmem_wait_ld();
+                    if (valid) {
+                        uint16_t *dst = p.y + (size_t)row * p.N + ti.nt * BN + c;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8)
+                            st_global_v4(dst + j,
+                                         pack_bf16x2(w * __uint_as_float(r[j]),
+                                                     w * __uint_as_float(r[j + 1])),
+                                         pack_bf16x2(w * __uint_as_float(r[j + 2]),
+                                                     w * __uint_as_float(r[j + 3])),
+                                         pack_bf16x2(w * __uint_as_float(r[j + 4]),
+                                                     w * __uint_as_float(r[j + 5])),
+                                         pack_bf16x2(w * __uint_as_float(r[j + 6]),
+                                                     w * __uint_as_float(r[j + 7])));
+                    }
+                }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -358,16 +437,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) moe_mx_gemm_kernel(const __grid
     if (warp == 1) tmem_dealloc(tmem_base, kMxTmemCols);
 }
 
-template <int MODE>
+template <int MODE, int BN>
 moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
-    auto kern = moe_mx_gemm_kernel<MODE>;
+    auto kern = moe_mx_gemm_kernel<MODE, BN>;
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)mx_smem_bytes(kMaxGroups)) != cudaSuccess)
+                                 (int)mx_smem_bytes<BN>(kMaxGroups)) != cudaSuccess)
             return MOE_ERR_CUDA;
         attr_set[dev] = true;
     }
@@ -376,11 +455,15 @@ moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
     const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
-    kern<<<grid, kMxThreads, mx_smem_bytes(p.G), st>>>(p);
+    kern<<<grid, MxShape<BN>::THREADS, mx_smem_bytes<BN>(p.G), st>>>(p);
     return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
+
+// 256-wide tiles (one accumulator) when the groups hold many rows, where the
+// MMAs set the pace; 128-wide ones (two accumulators) otherwise.
+static int mx_bn(int max_rows, int G) { return (long long)max_rows >= 1024LL * G ? 256 : 128; }
 
 moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *offsets, int G,
                           int max_rows, const uint8_t *W13q, const uint8_t *W13sf, int d, int I,
@@ -388,16 +471,17 @@ moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *
     if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     MxParams p;
     std::memset(&p, 0, sizeof p);
+    const int BN = mx_bn(max_rows, G);
     const int sfd = mx_sf_pitch(d);
     const uint64_t brows = (uint64_t)G * 2 * I;
     if (!encode_tmap_u8_2d(&p.tmA, xq, d, max_rows, d, 128, 128, 128) ||
-        !encode_tmap_u8_2d(&p.tmB, W13q, d, brows, d, 128, 64, 128) ||
+        !encode_tmap_u8_2d(&p.tmB, W13q, d, brows, d, 128, BN / 2, 128) ||
         !encode_tmap_u8_2d(&p.tmSA, xsf, sfd, max_rows, sfd, 16, 128, 0) ||
-        !encode_tmap_u8_2d(&p.tmSB, W13sf, sfd, brows, sfd, 16, 64, 0))
+        !encode_tmap_u8_2d(&p.tmSB, W13sf, sfd, brows, sfd, 16, BN / 2, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
-    p.n_tiles = I / 64;
+    p.n_tiles = I / (BN / 2);
     p.k_blocks = d / 128;
     p.b_rows_per_group = 2 * I;
     p.I = I;
@@ -405,7 +489,8 @@ moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *
     p.hq = hq;
     p.hsf = hsf;
     p.h_pitch = mx_sf_pitch(I);
-    return launch_mx<MX_FFN1>(p, row_tile_bound(max_rows, G) * p.n_tiles, st);
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return BN == 256 ? launch_mx<MX_FFN1, 256>(p, tiles, st) : launch_mx<MX_FFN1, 128>(p, tiles, st);
 }
 
 moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *offsets, int G,
@@ -414,16 +499,17 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
     if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     MxParams p;
     std::memset(&p, 0, sizeof p);
+    const int BN = mx_bn(max_rows, G);
     const int sfi = mx_sf_pitch(I);
     const uint64_t brows = (uint64_t)G * d;
     if (!encode_tmap_u8_2d(&p.tmA, hq, I, max_rows, I, 128, 128, 128) ||
-        !encode_tmap_u8_2d(&p.tmB, W2q, I, brows, I, 128, 128, 128) ||
+        !encode_tmap_u8_2d(&p.tmB, W2q, I, brows, I, 128, BN, 128) ||
         !encode_tmap_u8_2d(&p.tmSA, hsf, sfi, max_rows, sfi, 16, 128, 0) ||
-        !encode_tmap_u8_2d(&p.tmSB, W2sf, sfi, brows, sfi, 16, 128, 0))
+        !encode_tmap_u8_2d(&p.tmSB, W2sf, sfi, brows, sfi, 16, BN, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
-    p.n_tiles = d / 128;
+    p.n_tiles = d / BN;
     p.k_blocks = I / 128;
     p.b_rows_per_group = d;
     p.I = I;
@@ -431,7 +517,8 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
     p.y = y;
     p.row_w = row_w;
     p.w_rows = S;
-    return launch_mx<MX_FFN2>(p, row_tile_bound(max_rows, G) * p.n_tiles, st);
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return BN == 256 ? launch_mx<MX_FFN2, 256>(p, tiles, st) : launch_mx<MX_FFN2, 128>(p, tiles, st);
 }
 
 }  // namespace moe

@@ -139,6 +139,8 @@ CASES = [
     ("two_scale_chunks", 700, 1024, 5, 2, 256, 0, None, False),
     ("empty_experts", 500, 512, 16, 4, 128, 5, None, False),
     ("many_row_tiles", 12000, 256, 4, 2, 128, 0, 384, False),
+    # many rows per expert: the 256-wide tiles, several column tiles each way
+    ("wide_tiles", 6000, 512, 4, 2, 256, 0, 384, False),
     ("scales_above_2e7", 400, 256, 4, 2, 128, 0, None, True),
 ]
 
