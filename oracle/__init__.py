@@ -91,6 +91,8 @@ def _load():
                 "orc_e4m3_decode_all": ([_P], None),
                 "orc_e4m3_encode": ([_P, _I, _P], None),
                 "orc_expert_rows_mx": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _D, _P, _P], None),
+                "orc_expert_rows_mx_backward": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _D,
+                                                 _P, _P, _P, _P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -431,3 +433,25 @@ def expert_rows_mx(x, W13, W2, row_tok, row_exp, row_w, clamp):
     _load().orc_expert_rows_mx(_ptr(xn), _ptr(w13), _ptr(w2), n, _ptr(rt), _ptr(re), _ptr(rw),
                                d, I, float(clamp), _ptr(h), _ptr(y))
     return h, y
+
+
+def expert_rows_mx_backward(x, W13, W2, dY, row_tok, row_exp, row_w, clamp):
+    """Backward of the MXFP8 expert FFN per row (training form: each matmul's
+    operands MX along its own contraction).  Returns dict(dw [n], dgu [n, 2I]
+    (before quantisation), h [n, I] (the forward's MX h), dx [n, d])."""
+    (xn, w13, w2, dy), bf = _floats(x, W13, W2, dY)
+    assert bf == 1, "the MX oracle takes bf16 inputs"
+    d = xn.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    re = np.ascontiguousarray(_to_np(row_exp), dtype=np.int32)
+    rw = _opt(row_w, np.float64)
+    n = rt.shape[0]
+    dw = np.empty((n,), np.float64)
+    dgu = np.empty((n, 2 * I), np.float64)
+    h = np.empty((n, I), np.float64)
+    dx = np.empty((n, d), np.float64)
+    _load().orc_expert_rows_mx_backward(_ptr(xn), _ptr(w13), _ptr(w2), _ptr(dy), n, _ptr(rt),
+                                        _ptr(re), _ptr(rw), d, I, float(clamp), _ptr(dw),
+                                        _ptr(dgu), _ptr(h), _ptr(dx))
+    return dict(dw=dw, dgu=dgu, h=h, dx=dx)

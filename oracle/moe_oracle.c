@@ -853,3 +853,127 @@ void orc_expert_rows_mx(const uint16_t *x, const uint16_t *W13, const uint16_t *
         free(xr); free(xq); free(wr); free(wq); free(hv); free(qb); free(sb);
     }
 }
+
+/* Backward of the MXFP8 expert FFN over a list of rows, in the training form
+ * where every matmul takes MXFP8 operands quantised along its own contraction
+ * (the forward quantises x and W13 along d and h and W2 along I; the
+ * backward's two data-gradient matmuls contract over d and over 2I):
+ *   forward, as orc_expert_rows_mx:  g, u from x~ and W13~;  h~ = MX_I(h)
+ *   dY~  = MX_d(dY[row_tok[r]])
+ *   W2^  = W2[e] quantised along d (each of its I columns as a row of d)
+ *   dA   = W2^ dY~                                  (length I)
+ *   dw   = <h~, dA>                                 (routing-weight gradient)
+ *   dH   = w dA;  dg = dH clamp(u) silu'(min(g,c)) [g <= c];
+ *                 du = dH silu(min(g,c)) [-c <= u <= c]
+ *   dGU~ = MX_2I([dg | du])
+ *   W13^ = W13[e] quantised along 2I (each of its d columns as a row of 2I)
+ *   dX   = W13^ dGU~                                (length d)
+ * Outputs per row: dw[r], dgu[r] (the [dg | du] before quantisation, length
+ * 2I), hq[r] (h~, length I) and dx[r] (length d), all fp64.  The rows are
+ * taken expert by expert so that each expert's transposed weights are
+ * quantised once.  x, dY and the weights are bf16 bit patterns. */
+void orc_expert_rows_mx_backward(const uint16_t *x, const uint16_t *W13, const uint16_t *W2,
+                                 const uint16_t *dY, int n, const int64_t *row_tok,
+                                 const int32_t *row_exp, const double *row_w, int d, int I,
+                                 double c, double *dw, double *dgu, double *hq, double *dx)
+{
+    int emax = -1;
+    for (int r = 0; r < n; ++r) if (row_exp[r] > emax) emax = row_exp[r];
+    const int K2 = 2 * I;
+    double *w2t = (double *)malloc(sizeof(double) * (size_t)I * d);    /* [I][d] */
+    double *w13t = (double *)malloc(sizeof(double) * (size_t)d * K2);  /* [d][2I] */
+    for (int e = 0; e <= emax; ++e) {
+        int any = 0;
+        for (int r = 0; r < n && !any; ++r) any = row_exp[r] == e;
+        if (!any) continue;
+#pragma omp parallel
+        {
+            double *col = (double *)malloc(sizeof(double) * (size_t)(d > K2 ? d : K2));
+            uint8_t *qb = (uint8_t *)malloc((size_t)(d > K2 ? d : K2));
+            uint8_t *sb = (uint8_t *)malloc((size_t)(d > K2 ? d : K2) / 32);
+#pragma omp for schedule(static)
+            for (int i = 0; i < I; ++i) {
+                for (int m = 0; m < d; ++m)
+                    col[m] = bf16_to_f64(W2[((size_t)e * d + m) * I + i]);
+                mx_quantize_row(col, d, qb, sb, w2t + (size_t)i * d);
+            }
+#pragma omp for schedule(static)
+            for (int m = 0; m < d; ++m) {
+                for (int j = 0; j < K2; ++j)
+                    col[j] = bf16_to_f64(W13[((size_t)e * K2 + j) * d + m]);
+                mx_quantize_row(col, K2, qb, sb, w13t + (size_t)m * K2);
+            }
+            free(col); free(qb); free(sb);
+        }
+#pragma omp parallel
+        {
+            double *xr = (double *)malloc(sizeof(double) * (size_t)d);
+            double *xq = (double *)malloc(sizeof(double) * (size_t)d);
+            double *wr = (double *)malloc(sizeof(double) * (size_t)d);
+            double *wq = (double *)malloc(sizeof(double) * (size_t)d);
+            double *g = (double *)malloc(sizeof(double) * (size_t)I);
+            double *u = (double *)malloc(sizeof(double) * (size_t)I);
+            double *hv = (double *)malloc(sizeof(double) * (size_t)I);
+            double *dA = (double *)malloc(sizeof(double) * (size_t)I);
+            double *dyq = (double *)malloc(sizeof(double) * (size_t)d);
+            double *gq = (double *)malloc(sizeof(double) * (size_t)K2);
+            uint8_t *qb = (uint8_t *)malloc((size_t)(d > K2 ? d : K2));
+            uint8_t *sb = (uint8_t *)malloc((size_t)(d > K2 ? d : K2) / 32);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = 0; r < n; ++r) {
+                if (row_exp[r] != e) continue;
+                const size_t t = (size_t)row_tok[r];
+                const double w = row_w ? row_w[r] : 1.0;
+                /* forward: g, u from the MX operands, h~ */
+                for (int k = 0; k < d; ++k) xr[k] = bf16_to_f64(x[t * d + k]);
+                mx_quantize_row(xr, d, qb, sb, xq);
+                for (int i = 0; i < I; ++i) {
+                    for (int half = 0; half < 2; ++half) {
+                        const uint16_t *wrow = W13 + ((size_t)e * K2 + (size_t)half * I + i) * d;
+                        for (int k = 0; k < d; ++k) wr[k] = bf16_to_f64(wrow[k]);
+                        mx_quantize_row(wr, d, qb, sb, wq);
+                        double s = 0.0;
+                        for (int k = 0; k < d; ++k) s += xq[k] * wq[k];
+                        if (half == 0) g[i] = s; else u[i] = s;
+                    }
+                    double a = g[i] < c ? g[i] : c;
+                    double b = u[i] < -c ? -c : (u[i] > c ? c : u[i]);
+                    hv[i] = silu(a) * b;
+                }
+                double *hr = hq + (size_t)r * I;
+                mx_quantize_row(hv, I, qb, sb, hr);
+                /* dA = W2^ dY~ */
+                for (int k = 0; k < d; ++k) xr[k] = bf16_to_f64(dY[t * d + k]);
+                mx_quantize_row(xr, d, qb, sb, dyq);
+                for (int i = 0; i < I; ++i) {
+                    double s = 0.0;
+                    for (int k = 0; k < d; ++k) s += w2t[(size_t)i * d + k] * dyq[k];
+                    dA[i] = s;
+                }
+                double acc = 0.0;
+                for (int i = 0; i < I; ++i) acc += hr[i] * dA[i];
+                dw[r] = acc;
+                /* SwiGLU-clamp backward, then dX = W13^ dGU~ */
+                double *gr = dgu + (size_t)r * K2;
+                for (int i = 0; i < I; ++i) {
+                    const double dH = w * dA[i];
+                    const double a = g[i] < c ? g[i] : c;
+                    const double b = u[i] < -c ? -c : (u[i] > c ? c : u[i]);
+                    gr[i] = g[i] <= c ? dH * b * dsilu(a) : 0.0;
+                    gr[I + i] = (u[i] >= -c && u[i] <= c) ? dH * silu(a) : 0.0;
+                }
+                mx_quantize_row(gr, K2, qb, sb, gq);
+                double *xo = dx + (size_t)r * d;
+                for (int m = 0; m < d; ++m) {
+                    double s = 0.0;
+                    for (int j = 0; j < K2; ++j) s += w13t[(size_t)m * K2 + j] * gq[j];
+                    xo[m] = s;
+                }
+            }
+            free(xr); free(xq); free(wr); free(wq); free(g); free(u); free(hv); free(dA);
+            free(dyq); free(gq); free(qb); free(sb);
+        }
+    }
+    free(w2t);
+    free(w13t);
+}

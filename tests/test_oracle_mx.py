@@ -165,3 +165,113 @@ def test_expert_rows_mx_reduces_to_plain_oracle():
     _, y_bf = oracle.expert_rows(x, W13, W2, tok, exp_, rw, clamp, exact=True)
     rel = np.linalg.norm(y_mx - y_bf) / np.linalg.norm(y_bf)
     assert 1e-3 < rel < 0.1, rel
+
+
+# ------------------------------------------------------- the MX backward
+
+
+def _deq(q, sf):
+    return oracle.mx_dequantize(q, sf)
+
+
+def _mx(a):
+    """Values of a [rows, K] matrix after MX quantisation along K (the
+    quantiser itself is pinned above)."""
+    q, sf = oracle.mx_quantize(np.ascontiguousarray(a, dtype=np.float64))
+    return _deq(q, sf)
+
+
+def _bwd_case(grid, seed=5):
+    rng = np.random.default_rng(seed)
+    n, d, I, E = 10, 64, 64, 3
+    if grid:
+        # powers of two in [1/2, 2] (and zeros): every block of 32 along any
+        # axis is exactly on the MX grid, so every quantisation of an input
+        # operand is the identity
+        def pick(shape):
+            v = rng.choice([0.0, 0.5, 1.0, 2.0, -0.5, -1.0, -2.0], size=shape)
+            return torch.from_numpy(v).to(torch.bfloat16)
+        x, dY = pick((n, d)), pick((n, d))
+        W13 = torch.from_numpy(rng.choice([0.0, 0.5, -0.5, 1.0 / 64, -1.0 / 64],
+                                          size=(E, 2 * I, d))).to(torch.bfloat16)
+        W2 = torch.from_numpy(rng.choice([0.0, 0.5, -0.5, 1.0 / 64, -1.0 / 64],
+                                         size=(E, d, I))).to(torch.bfloat16)
+    else:
+        x = torch.randn(n, d, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+        dY = torch.randn(n, d, generator=torch.Generator().manual_seed(seed + 1)).to(torch.bfloat16)
+        W13 = (torch.randn(E, 2 * I, d, generator=torch.Generator().manual_seed(seed + 2)) *
+               0.1).to(torch.bfloat16)
+        W2 = (torch.randn(E, d, I, generator=torch.Generator().manual_seed(seed + 3)) *
+              0.1).to(torch.bfloat16)
+    rt = np.arange(n, dtype=np.int64)
+    re = (np.arange(n) % E).astype(np.int32)
+    rw = np.linspace(0.3, 1.7, n)
+    return x, dY, W13, W2, rt, re, rw
+
+
+@pytest.mark.parametrize("clamp", [7.0, 1.5])
+def test_mx_backward_on_grid_inputs_is_the_autograd_chain(clamp):
+    # inputs on the MX grid along every axis: the only quantisations left are
+    # those of h (the forward's GEMM-2 input) and of [dg | du] (dgrad 1's
+    # input); everything else must be the exact chain rule, which torch's
+    # autograd differentiates independently of the oracle's formulas
+    x, dY, W13, W2, rt, re, rw = _bwd_case(grid=True)
+    out = oracle.expert_rows_mx_backward(x, W13, W2, dY, rt, re, rw, clamp)
+    xd, dyd = x.double(), dY.double()
+    I = W2.shape[-1]
+    for r in range(len(rt)):
+        e = int(re[r])
+        w13, w2 = W13[e].double(), W2[e].double()
+        gu = (w13 @ xd[r]).clone().requires_grad_(True)
+        g, u = gu[:I], gu[I:]
+        h = torch.nn.functional.silu(torch.clamp(g, max=clamp)) * torch.clamp(u, -clamp, clamp)
+        hq = torch.from_numpy(_mx(h.detach().numpy()[None])[0])
+        np.testing.assert_array_equal(out["h"][r], hq.numpy())
+        dA = w2.T @ dyd[r]
+        np.testing.assert_allclose(out["dw"][r], float(hq @ dA), rtol=1e-12, atol=1e-12)
+        (h * (rw[r] * dA)).sum().backward()
+        np.testing.assert_allclose(out["dgu"][r], gu.grad.numpy(), rtol=1e-12, atol=1e-12)
+        dgq = torch.from_numpy(_mx(gu.grad.numpy()[None])[0])
+        np.testing.assert_allclose(out["dx"][r], (w13.T @ dgq).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mx_backward_quantises_each_matmul_along_its_contraction():
+    # general inputs: dA uses W2 quantised along d (its columns) and dY along
+    # d; dX uses W13 quantised along 2I (its columns) and [dg | du] along 2I
+    x, dY, W13, W2, rt, re, rw = _bwd_case(grid=False)
+    out = oracle.expert_rows_mx_backward(x, W13, W2, dY, rt, re, rw, 7.0)
+    dyq = _mx(dY.double().numpy())
+    for r in range(len(rt)):
+        e = int(re[r])
+        w2t = _mx(W2[e].double().numpy().T)          # [I, d]: along d
+        w13t = _mx(W13[e].double().numpy().T)        # [d, 2I]: along 2I
+        dA = w2t @ dyq[r]
+        np.testing.assert_allclose(out["dw"][r], out["h"][r] @ dA, rtol=1e-12, atol=1e-12)
+        dgq = _mx(out["dgu"][r][None])[0]
+        np.testing.assert_allclose(out["dx"][r], w13t @ dgq, rtol=1e-12, atol=1e-12)
+        # quantising W2 along I instead (a plausible mistake) changes dw
+        wrong = _mx(W2[e].double().numpy()).T @ dyq[r]
+        assert abs(out["h"][r] @ wrong - out["dw"][r]) > 1e-9 * max(1.0, abs(out["dw"][r]))
+    # and the MX h is the forward's (orc_expert_rows_mx)
+    h_fwd, _ = oracle.expert_rows_mx(x, W13, W2, rt, re, rw, 7.0)
+    np.testing.assert_array_equal(out["h"], h_fwd)
+
+
+def test_mx_backward_stays_near_the_exact_backward():
+    # the MX chain approximates the exact gradients: against the plain
+    # per-row forward's h and the exact dA (fp64 on the bf16 operands), the
+    # MX dw and [dg | du] differ by no more than the E4M3 rounding allows
+    x, dY, W13, W2, rt, re, rw = _bwd_case(grid=False, seed=9)
+    out = oracle.expert_rows_mx_backward(x, W13, W2, dY, rt, re, rw, 7.0)
+    h_plain, _ = oracle.expert_rows(x, W13, W2, rt, re, rw, 7.0, exact=True)
+    dA = oracle.rows_dA(dY, W2, rt, re)
+    dw_exact = (h_plain * dA).sum(1)
+    # each product carries at most a few E4M3 steps (2^-3 relative at most per
+    # factor), so the error is bounded by a fraction of the sum of |products|
+    mag = np.abs(h_plain * dA).sum(1)
+    assert np.all(np.abs(out["dw"] - dw_exact) <= 0.15 * mag), \
+        np.max(np.abs(out["dw"] - dw_exact) / mag)
+    # over the rows the MX dw follows the exact one; a sign slip would not
+    nrm = np.linalg.norm(dw_exact)
+    assert np.linalg.norm(out["dw"] - dw_exact) < 0.2 * nrm
+    assert np.linalg.norm(-out["dw"] - dw_exact) > 1.5 * nrm
