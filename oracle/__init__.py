@@ -93,6 +93,8 @@ def _load():
                 "orc_expert_rows_mx": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _D, _P, _P], None),
                 "orc_expert_rows_mx_backward": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _D,
                                                  _P, _P, _P, _P], None),
+                "orc_layer_backward_mx": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
+                                           _I, _P, _I, _I, _I, _I, _D, _D, _P, _P, _P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -455,3 +457,24 @@ def expert_rows_mx_backward(x, W13, W2, dY, row_tok, row_exp, row_w, clamp):
                                         _ptr(re), _ptr(rw), d, I, float(clamp), _ptr(dw),
                                         _ptr(dgu), _ptr(h), _ptr(dx))
     return dict(dw=dw, dgu=dgu, h=h, dx=dx)
+
+
+def layer_backward_mx(x, W_g, W13, W2, dY, bias, k, rho, clamp, is_vision=None, mode=0,
+                      input_ids=None, tid2eid=None, offset=None, tok=None):
+    """Token-local backward of the layer with the MXFP8 expert matmuls for the
+    listed tokens (bf16 inputs): dict(dX [n,d], dz [n,E], dw [n,k])."""
+    (xn, wg, w13, w2, dy), bf = _floats(x, W_g, W13, W2, dY)
+    assert bf == 1, "the MX oracle takes bf16 inputs"
+    E, d = wg.shape
+    I = w2.shape[-1]
+    b, vis, ii, tab, vocab, off = _route_args(bias, E, is_vision, input_ids, tid2eid, offset)
+    tk, n = _tok(tok, xn.shape[0])
+    dX = np.empty((n, d), np.float64)
+    dz = np.empty((n, E), np.float64)
+    dw = np.empty((n, k), np.float64)
+    _load().orc_layer_backward_mx(_ptr(xn), _ptr(wg), _ptr(w13), _ptr(w2), _ptr(dy), _ptr(off),
+                                  _ptr(b), _ptr(vis), int(mode), _ptr(ii), _ptr(tab), vocab, n,
+                                  _ptr(tk), d, E, k, I, float(rho), float(clamp), _ptr(dX),
+                                  _ptr(dz), _ptr(dw))
+    return dict(dX=dX, dz=dz, dw=dw)
+

@@ -977,3 +977,69 @@ void orc_expert_rows_mx_backward(const uint16_t *x, const uint16_t *W13, const u
     free(w2t);
     free(w13t);
 }
+
+/* Token-local backward of the layer with the MXFP8 expert matmuls, for the
+ * listed tokens: the routing and its backward chain are those of
+ * orc_layer_backward (interface rounding on, exact = 0), the expert rows those
+ * of orc_expert_rows_mx_backward.  Per listed token t with routed experts
+ * ids_j and weights w_j:
+ *   rows    (t, shared expert, 1) and (t, ids_j, w_j)
+ *   dw[j]   = the row (t, ids_j)'s <h~, dA>
+ *   dz      = route_backward(dw)            (zero off the selection)
+ *   dX[t]   = sum over the token's k + 1 rows of their dx + sum_e dz_e W_g[e]
+ * bf16 inputs only (uint16 bit patterns). */
+void orc_layer_backward_mx(const uint16_t *x, const uint16_t *Wg, const uint16_t *W13,
+                           const uint16_t *W2, const uint16_t *dY, const float *offset,
+                           const float *bias, const uint8_t *is_vision, int mode,
+                           const int32_t *input_ids, const int32_t *tid2eid, int vocab, int n,
+                           const int64_t *tok, int d, int E, int k, int I, double rho, double c,
+                           double *dX, double *dz, double *dw)
+{
+    double *z = (double *)malloc(sizeof(double) * (size_t)n * E);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)n * k);
+    double *w = (double *)malloc(sizeof(double) * (size_t)n * k);
+    double *ssel = (double *)malloc(sizeof(double) * (size_t)n * k);
+    double *margin = (double *)malloc(sizeof(double) * (size_t)n);
+    orc_gate_logits(x, Wg, 1, offset, n, tok, d, E, 0, z);
+    orc_route(z, bias, is_vision, mode, input_ids, tid2eid, vocab, n, tok, E, k, rho, 0, ids, w,
+              ssel, margin);
+    /* the token's rows: slot 0 the shared expert, slots 1..k the routed ones */
+    const int nr = n * (k + 1);
+    int64_t *rt = (int64_t *)malloc(sizeof(int64_t) * (size_t)nr);
+    int32_t *re = (int32_t *)malloc(sizeof(int32_t) * (size_t)nr);
+    double *rw = (double *)malloc(sizeof(double) * (size_t)nr);
+    for (int r = 0; r < n; ++r) {
+        const int64_t t = tok ? tok[r] : r;
+        for (int j = 0; j <= k; ++j) {
+            const size_t i = (size_t)r * (k + 1) + j;
+            rt[i] = t;
+            re[i] = j == 0 ? E : ids[(size_t)r * k + j - 1];
+            rw[i] = j == 0 ? 1.0 : w[(size_t)r * k + j - 1];
+        }
+    }
+    double *dwr = (double *)malloc(sizeof(double) * (size_t)nr);
+    double *dgu = (double *)malloc(sizeof(double) * (size_t)nr * 2 * I);
+    double *hq = (double *)malloc(sizeof(double) * (size_t)nr * I);
+    double *dxr = (double *)malloc(sizeof(double) * (size_t)nr * d);
+    orc_expert_rows_mx_backward(x, W13, W2, dY, nr, rt, re, rw, d, I, c, dwr, dgu, hq, dxr);
+    for (int r = 0; r < n; ++r) {
+        double *dxt = dX + (size_t)r * d;
+        for (int m = 0; m < d; ++m) dxt[m] = 0.0;
+        for (int j = 0; j <= k; ++j) {
+            const double *src = dxr + ((size_t)r * (k + 1) + j) * d;
+            for (int m = 0; m < d; ++m) dxt[m] += src[m];
+        }
+        for (int j = 0; j < k; ++j) dw[(size_t)r * k + j] = dwr[(size_t)r * (k + 1) + j + 1];
+        double dzs[64];
+        route_backward(z + (size_t)r * E, ids + (size_t)r * k, dw + (size_t)r * k, k, rho, dzs);
+        double *dzt = dz + (size_t)r * E;
+        for (int e = 0; e < E; ++e) dzt[e] = 0.0;
+        for (int j = 0; j < k; ++j) dzt[ids[(size_t)r * k + j]] += dzs[j];
+        for (int e = 0; e < E; ++e) {
+            if (dzt[e] == 0.0) continue;
+            for (int m = 0; m < d; ++m) dxt[m] += dzt[e] * bf16_to_f64(Wg[(size_t)e * d + m]);
+        }
+    }
+    free(z); free(ids); free(w); free(ssel); free(margin);
+    free(rt); free(re); free(rw); free(dwr); free(dgu); free(hq); free(dxr);
+}

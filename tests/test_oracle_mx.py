@@ -275,3 +275,64 @@ def test_mx_backward_stays_near_the_exact_backward():
     nrm = np.linalg.norm(dw_exact)
     assert np.linalg.norm(out["dw"] - dw_exact) < 0.2 * nrm
     assert np.linalg.norm(-out["dw"] - dw_exact) > 1.5 * nrm
+
+
+# ----------------------------------------------- the MX layer backward
+
+
+def _layer_case(seed=21):
+    g = torch.Generator().manual_seed(seed)
+    T, d, E, k, I = 12, 64, 5, 2, 64
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    dY = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    W_g = (torch.randn(E, d, generator=g) * 0.2).to(torch.bfloat16)
+    W13 = (torch.randn(E + 1, 2 * I, d, generator=g) * 0.1).to(torch.bfloat16)
+    W2 = (torch.randn(E + 1, d, I, generator=g) * 0.1).to(torch.bfloat16)
+    bias = torch.zeros(E)
+    is_vision = (torch.arange(T) % 3 == 0).to(torch.uint8)
+    return T, d, E, k, I, x, dY, W_g, W13, W2, bias, is_vision
+
+
+def test_mx_layer_backward_assembles_the_token_rows():
+    # dw is the routed rows' <h~, dA>, and dX is the sum of the token's k + 1
+    # MX rows (shared expert included) plus the gate term dz W_g
+    T, d, E, k, I, x, dY, W_g, W13, W2, bias, vis = _layer_case()
+    rho, clamp = 2.5, 7.0
+    out = oracle.layer_backward_mx(x, W_g, W13, W2, dY, bias, k, rho, clamp, is_vision=vis)
+    fwd = oracle.layer_forward(x, W_g, W13, W2, bias, k, rho, clamp, is_vision=vis)
+    rt = np.repeat(np.arange(T), k + 1).astype(np.int64)
+    re = np.concatenate([np.full((T, 1), E, np.int32), fwd["ids"]], axis=1).reshape(-1)
+    rw = np.concatenate([np.ones((T, 1)), fwd["w"]], axis=1).reshape(-1)
+    rows = oracle.expert_rows_mx_backward(x, W13, W2, dY, rt, re.astype(np.int32), rw, clamp)
+    np.testing.assert_allclose(out["dw"], rows["dw"].reshape(T, k + 1)[:, 1:], rtol=1e-12,
+                               atol=1e-14)
+    dx_rows = rows["dx"].reshape(T, k + 1, d).sum(1)
+    gate = out["dz"] @ W_g.double().numpy()
+    np.testing.assert_allclose(out["dX"], dx_rows + gate, rtol=1e-10, atol=1e-12)
+    # dz lives on the selection only, and the gate term is not negligible
+    sel = np.zeros((T, E), bool)
+    np.put_along_axis(sel, fwd["ids"].astype(np.int64), True, axis=1)
+    assert np.all(out["dz"][~sel] == 0.0) and np.abs(out["dz"][sel]).min() > 0.0
+    assert np.linalg.norm(gate) > 1e-3 * np.linalg.norm(out["dX"])
+
+
+def test_mx_layer_backward_logit_gradient_by_finite_differences():
+    # dz is the derivative of sum_j dw_j w_j(z) at the fp32 logits the layer
+    # routes with, with dw held fixed: central differences of the oracle's
+    # own forward routing (exact weights, fixed selection)
+    T, d, E, k, I, x, dY, W_g, W13, W2, bias, vis = _layer_case(seed=22)
+    rho = 2.5
+    out = oracle.layer_backward_mx(x, W_g, W13, W2, dY, bias, k, rho, 7.0, is_vision=vis)
+    z = oracle.gate_logits(x, W_g)
+    ids0, _, _, margin = oracle.route(z, bias, k, rho, is_vision=vis, exact=True)
+    assert margin.min() > 1e-3
+    eps = 1e-6
+    for m in range(E):
+        zp, zm = z.copy(), z.copy()
+        zp[:, m] += eps
+        zm[:, m] -= eps
+        idp, wp, _, _ = oracle.route(zp, bias, k, rho, is_vision=vis, exact=True)
+        idm, wm, _, _ = oracle.route(zm, bias, k, rho, is_vision=vis, exact=True)
+        assert np.array_equal(idp, ids0) and np.array_equal(idm, ids0)
+        fd = ((wp - wm) / (2 * eps) * out["dw"]).sum(1)
+        np.testing.assert_allclose(out["dz"][:, m], fd, rtol=1e-5, atol=1e-8)
