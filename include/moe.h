@@ -488,18 +488,119 @@ moe_status moe_expert_ffn_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
                              const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
                              const uint8_t *W13_sf, const uint8_t *W2_q, const uint8_t *W2_sf,
                              const float *row_weight, int S, int d, int I, float clamp,
-                             uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm, void *stream);
+                             float *gu_save, uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm,
+                             void *stream);
 
 /* The two matmuls of moe_expert_ffn_mx as separate calls (same arguments
- * and checks; GEMM 1 writes h_q / h_sf, GEMM 2 reads them). */
+ * and checks; GEMM 1 writes h_q / h_sf, GEMM 2 reads them).  gu_save (both
+ * calls that take it): NULL, or the fp32 GEMM-1 accumulators g|u kept for
+ * moe_expert_ffn_backward_mx, in moe_expert_ffn's gu_save layout
+ * (ceil(max_rows/32)*32 x 2I floats). */
 moe_status moe_expert_gemm1_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
                                const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
-                               const uint8_t *W13_sf, int d, int I, float clamp, uint8_t *h_q,
-                               uint8_t *h_sf, void *stream);
+                               const uint8_t *W13_sf, int d, int I, float clamp, float *gu_save,
+                               uint8_t *h_q, uint8_t *h_sf, void *stream);
 moe_status moe_expert_gemm2_mx(const uint8_t *h_q, const uint8_t *h_sf, const int32_t *offsets,
                                int G, int max_rows, const uint8_t *W2_q, const uint8_t *W2_sf,
                                const float *row_weight, int S, int d, int I, uint16_t *y_perm,
                                void *stream);
+
+/* MX quantisation along the rows of a stack of matrices, written transposed:
+ * src [G, R, C] bf16; output row g*C + c is column c of matrix g (R values)
+ * quantised in blocks of 32 along R: q [G*C, R], sf [G*C, moe_mx_sf_pitch(R)].
+ * The backward's weight copies: W2 [G, d, I] -> W2^T [G*I, d] quantised along
+ * d, W13 [G, 2I, d] -> W13^T [G*d, 2I] quantised along 2I.  Needs R % 32 == 0,
+ * G, C >= 1; 16-byte aligned arrays. */
+moe_status moe_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
+                             void *stream);
+
+/* Backward of moe_expert_ffn_mx on its rows, in the MX training form: each
+ * matmul takes its two operands quantised along its own contraction.
+ *   dA[r]   = dY~[r] (W2^T)~[g]^T     dY along d, W2 along d  (fp32 sums)
+ *   dw_rows[r] = <h~[r], dA[r]>       h~ the forward's MX h   (r < S)
+ *   dH = w dA;  [dg|du][r] = clamped-SwiGLU backward as in moe_backward, from
+ *                                     the forward's fp32 g|u
+ *   dX_perm[r] = bf16( MX([dg|du][r]) (W13^T)~[g]^T )   along 2I
+ *   dW2[g]  = sum_r dY_perm[r]^T bf16(w h~[r])            (bf16 operands,
+ *   dW13[g] = sum_r bf16([dg|du][r])^T x_perm[r]           fp32 sums)
+ * The weight gradients are bf16 matmuls of the same rows (the MX recipe
+ * leaves them open; these keep the bf16 layer's weight-gradient arithmetic).
+ * gu_save = NULL recomputes g|u and h~ with MX GEMM 1 into the workspace
+ * (then x_perm_q/sf and W13_q/sf are read, h_q/h_sf are not); otherwise the
+ * forward's gu_save and h_q/h_sf are read.  Needs d % 256 == 0 and
+ * I % 128 == 0 (else MOE_ERR_UNSUPPORTED).  Workspace:
+ * moe_expert_bwd_mx_workspace_size(max_rows, d, I, gu_save == NULL). */
+typedef struct {
+    int G, max_rows, S, d, I;
+    float clamp;
+    const int32_t *offsets;       /* [G+1] */
+    const uint16_t *x_perm;       /* [R,d] bf16 rows of the forward (dW13) */
+    const uint8_t *x_perm_q;      /* [R,d] their MX codes (recompute only) */
+    const uint8_t *x_perm_sf;     /* [R,pitch(d)] */
+    const uint8_t *W13_q;         /* [G*2I,d] forward W13~ (recompute only) */
+    const uint8_t *W13_sf;
+    const float *gu_save;         /* forward's g|u, or NULL: recompute */
+    const uint8_t *h_q;           /* [R,I] forward's h~ (with gu_save) */
+    const uint8_t *h_sf;          /* [R,pitch(I)] */
+    const uint8_t *W2t_q;         /* [G*I,d] W2 along d (moe_mx_quantize_t) */
+    const uint8_t *W2t_sf;        /* [G*I,pitch(d)] */
+    const uint8_t *W13t_q;        /* [G*d,2I] W13 along 2I (moe_mx_quantize_t) */
+    const uint8_t *W13t_sf;       /* [G*d,pitch(2I)] */
+    const float *row_weight;      /* [S] or NULL (weight 1) */
+    const uint16_t *dY_perm;      /* [R,d] bf16 gradient at the rows' outputs */
+    const uint8_t *dY_perm_q;     /* [R,d] the same rows MX along d */
+    const uint8_t *dY_perm_sf;    /* [R,pitch(d)] */
+    uint16_t *dX_perm;            /* [R,d] bf16 out */
+    float *dw_rows;               /* [S] out or NULL */
+    float *dW13;                  /* [G,2I,d] fp32 out */
+    float *dW2;                   /* [G,d,I] fp32 out */
+    void *ws;
+    size_t ws_bytes;
+} moe_expert_bwd_mx_args;
+size_t moe_expert_bwd_mx_workspace_size(int max_rows, int d, int I, int recompute);
+moe_status moe_expert_ffn_backward_mx(const moe_expert_bwd_mx_args *args, void *stream);
+
+/* Backward of the whole layer with the MX expert matmuls: moe_backward with
+ * the expert part of moe_expert_ffn_backward_mx (dY gathered twice: bf16 for
+ * dW2, MX along d for dgrad 2) and the same routing and combine chain.  The
+ * bf16 x_perm (dW13, dW_g) is gathered from x; the stages and their events
+ * are those of moe_backward.  Workspace:
+ * moe_backward_mx_workspace_size(T, d, E, k, I, gu_save == NULL). */
+typedef struct {
+    int T, d, E, k, I;
+    float scaling, clamp;
+    const uint16_t *x;            /* [T,d] */
+    const uint16_t *W_g;          /* [E,d] */
+    const uint8_t *W13_q;         /* forward W13~ [(E+1)*2I,d] (recompute only) */
+    const uint8_t *W13_sf;
+    const uint8_t *W2t_q;         /* [(E+1)*I,d] */
+    const uint8_t *W2t_sf;
+    const uint8_t *W13t_q;        /* [(E+1)*d,2I] */
+    const uint8_t *W13t_sf;
+    const int32_t *ids;           /* [T,k] */
+    const float *weights;         /* [T,k] */
+    const float *scores_sel;      /* [T,k] */
+    const float *row_weight;      /* [S] */
+    const int32_t *offsets;       /* [E+2] */
+    const int32_t *slot_row;      /* [S] */
+    const uint8_t *x_perm_q;      /* [S+T,d] (moe_mx_gather; recompute only) */
+    const uint8_t *x_perm_sf;
+    const float *gu_save;         /* forward's g|u or NULL: recompute */
+    const uint8_t *h_q;           /* forward's h~ (with gu_save) */
+    const uint8_t *h_sf;
+    const uint16_t *dY;           /* [T,d] */
+    uint16_t *dX;                 /* [T,d] bf16 out */
+    float *dW_g;                  /* [E,d] */
+    float *dW13;                  /* [E+1,2I,d] */
+    float *dW2;                   /* [E+1,d,I] */
+    float *dlogits;               /* [T,E] or NULL */
+    float *dweights;              /* [T,k] or NULL */
+    void *ws;
+    size_t ws_bytes;
+    void *const *stage_events;    /* as in moe_bwd_args, or NULL */
+} moe_bwd_mx_args;
+size_t moe_backward_mx_workspace_size(int T, int d, int E, int k, int I, int recompute);
+moe_status moe_backward_mx(const moe_bwd_mx_args *args, void *stream);
 
 /* Text of a status code (static storage). */
 const char *moe_status_string(moe_status s);

@@ -40,7 +40,9 @@ EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_rout
            "moe_layer_step_host", "moe_gather_rows", "moe_expert_bwd_workspace_size",
            "moe_expert_ffn_backward", "moe_router_bwd_workspace_size", "moe_router_backward",
            "moe_set_gemm_pairs", "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
-           "moe_expert_gemm1_mx", "moe_expert_gemm2_mx"]
+           "moe_expert_gemm1_mx", "moe_expert_gemm2_mx", "moe_mx_quantize_t",
+           "moe_expert_bwd_mx_workspace_size", "moe_expert_ffn_backward_mx",
+           "moe_backward_mx_workspace_size", "moe_backward_mx"]
 
 
 class MoeError(RuntimeError):
@@ -135,6 +137,31 @@ class LayerBuffers(ctypes.Structure):
                 ("ws", _P), ("ws_bytes", _Z)]
 
 
+class ExpertBwdMxArgs(ctypes.Structure):
+    """Mirror of moe_expert_bwd_mx_args."""
+    _fields_ = [("G", _I), ("max_rows", _I), ("S", _I), ("d", _I), ("I", _I), ("clamp", _F),
+                ("offsets", _P), ("x_perm", _P), ("x_perm_q", _P), ("x_perm_sf", _P),
+                ("W13_q", _P), ("W13_sf", _P), ("gu_save", _P), ("h_q", _P), ("h_sf", _P),
+                ("W2t_q", _P), ("W2t_sf", _P), ("W13t_q", _P), ("W13t_sf", _P),
+                ("row_weight", _P), ("dY_perm", _P), ("dY_perm_q", _P), ("dY_perm_sf", _P),
+                ("dX_perm", _P), ("dw_rows", _P), ("dW13", _P), ("dW2", _P),
+                ("ws", _P), ("ws_bytes", _Z)]
+
+
+class BwdMxArgs(ctypes.Structure):
+    """Mirror of moe_bwd_mx_args."""
+    _fields_ = [("T", _I), ("d", _I), ("E", _I), ("k", _I), ("I", _I),
+                ("scaling", _F), ("clamp", _F),
+                ("x", _P), ("W_g", _P), ("W13_q", _P), ("W13_sf", _P), ("W2t_q", _P),
+                ("W2t_sf", _P), ("W13t_q", _P), ("W13t_sf", _P),
+                ("ids", _P), ("weights", _P), ("scores_sel", _P), ("row_weight", _P),
+                ("offsets", _P), ("slot_row", _P), ("x_perm_q", _P), ("x_perm_sf", _P),
+                ("gu_save", _P), ("h_q", _P), ("h_sf", _P), ("dY", _P),
+                ("dX", _P), ("dW_g", _P), ("dW13", _P), ("dW2", _P),
+                ("dlogits", _P), ("dweights", _P), ("ws", _P), ("ws_bytes", _Z),
+                ("stage_events", ctypes.POINTER(_P))]
+
+
 MOE_BWD_STAGE_NAMES = ["recompute_gather", "recompute_gemm1", "gather_dY", "dgrad2", "wgrad2",
                        "dgrad1", "wgrad1", "router_bwd", "dX", "dW_g"]
 MOE_BWD_STAGES = len(MOE_BWD_STAGE_NAMES)
@@ -173,8 +200,13 @@ _SIGS = {
     "moe_mx_quantize": ([_P, _LL, _I, _P, _P, _P], _I),
     "moe_mx_gather": ([_P, _P, _I, _I, _I, _P, _P, _P], _I),
     "moe_expert_ffn_mx": ([_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P,
-                           _P], _I),
-    "moe_expert_gemm1_mx": ([_P, _P, _P, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P], _I),
+                           _P, _P], _I),
+    "moe_expert_gemm1_mx": ([_P, _P, _P, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P, _P], _I),
+    "moe_mx_quantize_t": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_expert_bwd_mx_workspace_size": ([_I, _I, _I, _I], _Z),
+    "moe_expert_ffn_backward_mx": ([ctypes.POINTER(ExpertBwdMxArgs), _P], _I),
+    "moe_backward_mx_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
+    "moe_backward_mx": ([ctypes.POINTER(BwdMxArgs), _P], _I),
     "moe_expert_gemm2_mx": ([_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P], _I),
 }
 
@@ -342,25 +374,26 @@ def moe_mx_gather(x, slot_row, T, d, k, x_perm_q, x_perm_sf, stream=None):
 
 
 def moe_expert_ffn_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, W2_q, W2_sf,
-                      row_weight, S, d, I, clamp, h_q, h_sf, y_perm, stream=None):
+                      row_weight, S, d, I, clamp, h_q, h_sf, y_perm, gu_save=None, stream=None):
     st = load().moe_expert_ffn_mx(_ptr(x_perm_q, U8, "x_perm_q"), _ptr(x_perm_sf, U8, "x_perm_sf"),
                                   _ptr(offsets, I32, "offsets"), G, max_rows,
                                   _ptr(W13_q, U8, "W13_q"), _ptr(W13_sf, U8, "W13_sf"),
                                   _ptr(W2_q, U8, "W2_q"), _ptr(W2_sf, U8, "W2_sf"),
                                   _ptr(row_weight, F32, "row_weight"), S, d, I, float(clamp),
-                                  _ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"),
-                                  _ptr(y_perm, BF16, "y_perm"), _stream(stream))
+                                  _ptr(gu_save, F32, "gu_save"), _ptr(h_q, U8, "h_q"),
+                                  _ptr(h_sf, U8, "h_sf"), _ptr(y_perm, BF16, "y_perm"),
+                                  _stream(stream))
     _check("moe_expert_ffn_mx", st)
 
 
 def moe_expert_gemm1_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp,
-                        h_q, h_sf, stream=None):
+                        h_q, h_sf, gu_save=None, stream=None):
     st = load().moe_expert_gemm1_mx(_ptr(x_perm_q, U8, "x_perm_q"),
                                     _ptr(x_perm_sf, U8, "x_perm_sf"),
                                     _ptr(offsets, I32, "offsets"), G, max_rows,
                                     _ptr(W13_q, U8, "W13_q"), _ptr(W13_sf, U8, "W13_sf"), d, I,
-                                    float(clamp), _ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"),
-                                    _stream(stream))
+                                    float(clamp), _ptr(gu_save, F32, "gu_save"),
+                                    _ptr(h_q, U8, "h_q"), _ptr(h_sf, U8, "h_sf"), _stream(stream))
     _check("moe_expert_gemm1_mx", st)
 
 
@@ -372,6 +405,54 @@ def moe_expert_gemm2_mx(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight
                                     _ptr(row_weight, F32, "row_weight"), S, d, I,
                                     _ptr(y_perm, BF16, "y_perm"), _stream(stream))
     _check("moe_expert_gemm2_mx", st)
+
+
+def moe_mx_quantize_t(src, G, R, C, q, sf, stream=None):
+    st = load().moe_mx_quantize_t(_ptr(src, BF16, "src"), int(G), int(R), int(C),
+                                  _ptr(q, U8, "q"), _ptr(sf, U8, "sf"), _stream(stream))
+    _check("moe_mx_quantize_t", st)
+
+
+def moe_expert_bwd_mx_workspace_size(max_rows, d, I, recompute) -> int:
+    return int(load().moe_expert_bwd_mx_workspace_size(max_rows, d, I, int(bool(recompute))))
+
+
+def moe_backward_mx_workspace_size(T, d, E, k, I, recompute) -> int:
+    return int(load().moe_backward_mx_workspace_size(T, d, E, k, I, int(bool(recompute))))
+
+
+_MX_BWD_TYPES = dict(offsets=I32, x_perm=BF16, x_perm_q=U8, x_perm_sf=U8, W13_q=U8, W13_sf=U8,
+                     gu_save=F32, h_q=U8, h_sf=U8, W2t_q=U8, W2t_sf=U8, W13t_q=U8, W13t_sf=U8,
+                     row_weight=F32, dY_perm=BF16, dY_perm_q=U8, dY_perm_sf=U8, dX_perm=BF16,
+                     dw_rows=F32, dW13=F32, dW2=F32, ws=U8, x=BF16, W_g=BF16, ids=I32,
+                     weights=F32, scores_sel=F32, slot_row=I32, dY=BF16, dX=BF16, dW_g=F32,
+                     dlogits=F32, dweights=F32)
+
+
+def _fill_args(a, args: dict):
+    for name, _ in a._fields_:
+        if name in ("ws_bytes", "stage_events"):
+            continue
+        v = args.get(name)
+        setattr(a, name, _ptr(v, _MX_BWD_TYPES[name], name) if name in _MX_BWD_TYPES else v)
+    a.ws_bytes = 0 if args.get("ws") is None else args["ws"].numel()
+
+
+def moe_expert_ffn_backward_mx(args: dict, stream=None):
+    """args: the fields of moe_expert_bwd_mx_args (tensors for pointers)."""
+    a = ExpertBwdMxArgs()
+    _fill_args(a, args)
+    st = load().moe_expert_ffn_backward_mx(ctypes.byref(a), _stream(stream))
+    _check("moe_expert_ffn_backward_mx", st)
+
+
+def moe_backward_mx(args: dict, stream=None):
+    """args: the fields of moe_bwd_mx_args (tensors for pointers)."""
+    a = BwdMxArgs()
+    _fill_args(a, args)
+    a.stage_events = _stage_events(args.get("stage_events"))
+    st = load().moe_backward_mx(ctypes.byref(a), _stream(stream))
+    _check("moe_backward_mx", st)
 
 
 def moe_expert_gemm1(x_perm, offsets, G, max_rows, W13, d, I, clamp, gu_save, h_perm,
@@ -396,6 +477,18 @@ def moe_combine(y_perm, slot_row, T, d, k, with_shared, y, stream=None):
     _check("moe_combine", st)
 
 
+def _stage_events(ev):
+    """torch.cuda.Event objects (recorded at least once, so that their CUDA
+    events exist) or None entries -> a C array of cudaEvent_t (or NULL)."""
+    if ev is None:
+        return None
+    if len(ev) != MOE_BWD_STAGES + 1:
+        raise ValueError(f"stage_events: {MOE_BWD_STAGES + 1} entries expected")
+    handles = (_P * len(ev))(*[None if e is None else e.cuda_event for e in ev])
+    _stage_events.keep = handles   # alive until the call returns
+    return ctypes.cast(handles, ctypes.POINTER(_P))
+
+
 def moe_backward(args: dict, stream=None):
     """args: the fields of moe_bwd_args (tensors for pointers)."""
     a = BwdArgs()
@@ -412,14 +505,7 @@ def moe_backward(args: dict, stream=None):
         else:
             setattr(a, name, v)
     a.ws_bytes = 0 if args.get("ws") is None else args["ws"].numel()
-    ev = args.get("stage_events")
-    if ev is not None:
-        # torch.cuda.Event objects (recorded at least once, so that their CUDA
-        # events exist) or None entries
-        if len(ev) != MOE_BWD_STAGES + 1:
-            raise ValueError(f"stage_events: {MOE_BWD_STAGES + 1} entries expected")
-        handles = (_P * len(ev))(*[None if e is None else e.cuda_event for e in ev])
-        a.stage_events = ctypes.cast(handles, ctypes.POINTER(_P))
+    a.stage_events = _stage_events(args.get("stage_events"))
     st = load().moe_backward(ctypes.byref(a), _stream(stream))
     _check("moe_backward", st)
 

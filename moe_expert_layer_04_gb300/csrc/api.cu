@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstring>
 #include <initializer_list>
+#include <functional>
 #include <mutex>
 
 #include "moe_ptx.cuh"
@@ -122,6 +123,55 @@ RouterBwdWorkspace carve_router_bwd(uint8_t *base, int T, int d, int E, int k) {
     w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
+    w.bytes = off;
+    return w;
+}
+
+// Workspace of the MX expert backward: [dg|du] in bf16 (dW13) and MX along
+// 2I (dgrad 1), w h~ (dW2), the dw partials; with recompute g|u and h~; in
+// the layer-level call also x_perm and dY_perm in bf16, dY_perm in MX, dX_perm
+// and the router's scratch.
+struct MxBwdWorkspace {
+    uint16_t *dGU, *hw;
+    uint8_t *dGUq, *dGUsf;
+    float *dw_part, *gu;
+    uint8_t *hq, *hsf;
+    uint16_t *x_perm, *dY_perm, *dX_perm;
+    uint8_t *dYq, *dYsf;
+    RouterBwdWorkspace router;
+    size_t bytes;
+};
+
+MxBwdWorkspace carve_mx_bwd(uint8_t *base, int R, int d, int I, bool recompute, bool layer, int T,
+                            int E, int k) {
+    MxBwdWorkspace w;
+    std::memset(&w, 0, sizeof w);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + off : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    const size_t r = (size_t)R;
+    w.dGU = reinterpret_cast<uint16_t *>(take(r * 2 * I * 2));
+    w.hw = reinterpret_cast<uint16_t *>(take(r * I * 2));
+    w.dGUq = take(r * 2 * I);
+    w.dGUsf = take(r * mx_sf_pitch(2 * I));
+    w.dw_part = reinterpret_cast<float *>(take(r * mx_dgrad2_n_part(I) * 4));
+    if (recompute) {
+        w.gu = reinterpret_cast<float *>(take((r + 31) / 32 * 32 * 2 * I * 4));
+        w.hq = take(r * I);
+        w.hsf = take(r * mx_sf_pitch(I));
+    }
+    if (layer) {
+        w.x_perm = reinterpret_cast<uint16_t *>(take(r * d * 2));
+        w.dY_perm = reinterpret_cast<uint16_t *>(take(r * d * 2));
+        w.dX_perm = reinterpret_cast<uint16_t *>(take(r * d * 2));
+        w.dYq = take(r * d);
+        w.dYsf = take(r * mx_sf_pitch(d));
+        const RouterBwdWorkspace rw = carve_router_bwd(nullptr, T, d, E, k);
+        w.router = carve_router_bwd(take(rw.bytes), T, d, E, k);
+    }
     w.bytes = off;
     return w;
 }
@@ -457,13 +507,14 @@ static moe_status check_ffn_mx(int G, int max_rows, int d, int I, int S, float c
 
 moe_status moe_expert_gemm1_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
                                const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
-                               const uint8_t *W13_sf, int d, int I, float clamp, uint8_t *h_q,
-                               uint8_t *h_sf, void *stream) {
+                               const uint8_t *W13_sf, int d, int I, float clamp, float *gu_save,
+                               uint8_t *h_q, uint8_t *h_sf, void *stream) {
     moe_status s = check_ffn_mx(G, max_rows, d, I, 0, clamp,
                                 {x_perm_q, x_perm_sf, W13_q, W13_sf, h_q, h_sf}, offsets);
     if (s != MOE_OK) return s;
+    if (gu_save && !aligned16(gu_save)) return MOE_ERR_INVALID_ARG;
     return launch_mx_ffn1(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp,
-                          h_q, h_sf, static_cast<cudaStream_t>(stream));
+                          h_q, h_sf, gu_save, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_expert_gemm2_mx(const uint8_t *h_q, const uint8_t *h_sf, const int32_t *offsets,
@@ -481,16 +532,194 @@ moe_status moe_expert_ffn_mx(const uint8_t *x_perm_q, const uint8_t *x_perm_sf,
                              const int32_t *offsets, int G, int max_rows, const uint8_t *W13_q,
                              const uint8_t *W13_sf, const uint8_t *W2_q, const uint8_t *W2_sf,
                              const float *row_weight, int S, int d, int I, float clamp,
-                             uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm, void *stream) {
+                             float *gu_save, uint8_t *h_q, uint8_t *h_sf, uint16_t *y_perm,
+                             void *stream) {
     moe_status s = check_ffn_mx(G, max_rows, d, I, S, clamp,
                                 {x_perm_q, x_perm_sf, W13_q, W13_sf, W2_q, W2_sf, h_q, h_sf,
                                  y_perm}, offsets);
     if (s != MOE_OK) return s;
     s = moe_expert_gemm1_mx(x_perm_q, x_perm_sf, offsets, G, max_rows, W13_q, W13_sf, d, I, clamp,
-                            h_q, h_sf, stream);
+                            gu_save, h_q, h_sf, stream);
     if (s != MOE_OK) return s;
     return moe_expert_gemm2_mx(h_q, h_sf, offsets, G, max_rows, W2_q, W2_sf, row_weight, S, d, I,
                                y_perm, stream);
+}
+
+moe_status moe_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
+                             void *stream) {
+    if (G < 1 || C < 1 || R < 32 || R % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if ((long long)G * R * C >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+    if (!src || !q || !sf || !aligned16(src) || !aligned16(q) || !aligned16(sf))
+        return MOE_ERR_INVALID_ARG;
+    return launch_mx_quantize_t(src, G, R, C, q, sf, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+// The expert part of the MX backward on expert-contiguous rows (shared by the
+// expert-level and the layer-level call; arguments already checked).
+struct MxExpertBwd {
+    int G, R, S, d, I;
+    float clamp;
+    const int32_t *offsets;
+    const uint16_t *x_perm;
+    const uint8_t *x_perm_q, *x_perm_sf, *W13_q, *W13_sf;
+    const float *gu_save;
+    const uint8_t *h_q, *h_sf, *W2t_q, *W2t_sf, *W13t_q, *W13t_sf;
+    const float *row_weight;
+    const uint16_t *dY_perm;
+    const uint8_t *dY_perm_q, *dY_perm_sf;
+    uint16_t *dX_perm;
+    float *dW13, *dW2;
+};
+
+moe_status run_mx_expert_bwd(const MxExpertBwd &a, const MxBwdWorkspace &w, int *n_part,
+                             const std::function<bool(int)> &mark, cudaStream_t st) {
+    moe_status s;
+    const float *gu = a.gu_save;
+    const uint8_t *hq = a.h_q, *hsf = a.h_sf;
+    if (!mark(MOE_BWD_RECOMPUTE_GEMM1)) return MOE_ERR_CUDA;
+    if (!gu) {
+        if ((s = launch_mx_ffn1(a.x_perm_q, a.x_perm_sf, a.offsets, a.G, a.R, a.W13_q, a.W13_sf,
+                                a.d, a.I, a.clamp, w.hq, w.hsf, w.gu, st)) != MOE_OK)
+            return s;
+        gu = w.gu;
+        hq = w.hq;
+        hsf = w.hsf;
+    }
+    if (!mark(MOE_BWD_DGRAD2)) return MOE_ERR_CUDA;
+    if ((s = launch_mx_dgrad2(a.dY_perm_q, a.dY_perm_sf, a.offsets, a.G, a.R, a.W2t_q, a.W2t_sf,
+                              gu, hq, hsf, a.row_weight, a.S, a.d, a.I, a.clamp, w.dGU, w.dGUq,
+                              w.dGUsf, w.hw, w.dw_part, n_part, st)) != MOE_OK)
+        return s;
+    if (!mark(MOE_BWD_WGRAD2)) return MOE_ERR_CUDA;
+    if ((s = launch_wgrad(a.dY_perm, a.d, w.hw, a.I, a.offsets, a.G, a.R, a.dW2, st)) != MOE_OK)
+        return s;
+    if (!mark(MOE_BWD_DGRAD1)) return MOE_ERR_CUDA;
+    // dgrad 1 is MX GEMM 2 with the contraction over 2I and no row weight
+    if ((s = launch_mx_ffn2(w.dGUq, w.dGUsf, a.offsets, a.G, a.R, a.W13t_q, a.W13t_sf, nullptr, 0,
+                            a.d, 2 * a.I, a.dX_perm, st)) != MOE_OK)
+        return s;
+    if (!mark(MOE_BWD_WGRAD1)) return MOE_ERR_CUDA;
+    return launch_wgrad(w.dGU, 2 * a.I, a.x_perm, a.d, a.offsets, a.G, a.R, a.dW13, st);
+}
+
+}  // namespace
+
+size_t moe_expert_bwd_mx_workspace_size(int max_rows, int d, int I, int recompute) {
+    if (max_rows < 1 || d < 32 || I < 128 || I % 128 != 0 || d % 32 != 0) return 0;
+    return carve_mx_bwd(nullptr, max_rows, d, I, recompute != 0, false, 0, 0, 0).bytes;
+}
+
+moe_status moe_expert_ffn_backward_mx(const moe_expert_bwd_mx_args *a, void *stream) {
+    if (!a) return MOE_ERR_INVALID_ARG;
+    moe_status s = check_ffn_mx(a->G, a->max_rows, a->d, a->I, a->S, a->clamp,
+                                {a->x_perm, a->W2t_q, a->W2t_sf, a->W13t_q,
+                                 a->W13t_sf, a->dY_perm, a->dY_perm_q, a->dY_perm_sf, a->dX_perm,
+                                 a->dW13, a->dW2},
+                                a->offsets);
+    if (s != MOE_OK) return s;
+    if (a->S > a->max_rows) return MOE_ERR_INVALID_ARG;
+    if (a->S > 0 && a->dw_rows && !a->row_weight) return MOE_ERR_INVALID_ARG;
+    const bool rec = a->gu_save == nullptr;
+    const void *need[] = {a->x_perm_q, a->x_perm_sf, a->W13_q, a->W13_sf};
+    const void *need_saved[] = {a->gu_save, a->h_q, a->h_sf};
+    for (const void *p : need)
+        if (rec && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
+    for (const void *p : need_saved)
+        if (!rec && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
+    if (!a->ws || a->ws_bytes < moe_expert_bwd_mx_workspace_size(a->max_rows, a->d, a->I, rec))
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const MxBwdWorkspace w =
+        carve_mx_bwd(static_cast<uint8_t *>(a->ws), a->max_rows, a->d, a->I, rec, false, 0, 0, 0);
+    const MxExpertBwd e{a->G, a->max_rows, a->S, a->d, a->I, a->clamp, a->offsets, a->x_perm,
+                        a->x_perm_q, a->x_perm_sf, a->W13_q, a->W13_sf, a->gu_save, a->h_q,
+                        a->h_sf, a->W2t_q, a->W2t_sf, a->W13t_q, a->W13t_sf, a->row_weight,
+                        a->dY_perm, a->dY_perm_q, a->dY_perm_sf, a->dX_perm, a->dW13, a->dW2};
+    int n_part = 0;
+    if ((s = run_mx_expert_bwd(e, w, &n_part, [](int) { return true; }, st)) != MOE_OK) return s;
+    if (a->dw_rows && a->S > 0) return launch_row_sum(w.dw_part, a->S, n_part, a->dw_rows, st);
+    return MOE_OK;
+}
+
+size_t moe_backward_mx_workspace_size(int T, int d, int E, int k, int I, int recompute) {
+    if (check_shapes(T, d, E, k, I) != MOE_OK || d % 256 != 0 || I % 128 != 0) return 0;
+    const int R = T * k + T;
+    return carve_mx_bwd(nullptr, R, d, I, recompute != 0, true, T, E, k).bytes;
+}
+
+moe_status moe_backward_mx(const moe_bwd_mx_args *a, void *stream) {
+    if (!a) return MOE_ERR_INVALID_ARG;
+    const int T = a->T, d = a->d, E = a->E, k = a->k, I = a->I;
+    moe_status s = check_shapes(T, d, E, k, I);
+    if (s != MOE_OK) return s;
+    if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    const bool rec = a->gu_save == nullptr;
+    const void *need[] = {a->x,        a->W_g,    a->W2t_q,  a->W2t_sf, a->W13t_q, a->W13t_sf,
+                          a->ids,      a->weights, a->scores_sel, a->row_weight, a->offsets,
+                          a->slot_row, a->dY,     a->dX,     a->dW_g,   a->dW13,   a->dW2};
+    for (const void *p : need)
+        if (!p) return MOE_ERR_INVALID_ARG;
+    const void *al[] = {a->x,      a->W_g,    a->W2t_q, a->W2t_sf, a->W13t_q, a->W13t_sf,
+                        a->dY,     a->dX,     a->dW_g,  a->dW13,   a->dW2};
+    for (const void *p : al)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const void *need_rec[] = {a->x_perm_q, a->x_perm_sf, a->W13_q, a->W13_sf};
+    const void *need_saved[] = {a->gu_save, a->h_q, a->h_sf};
+    for (const void *p : need_rec)
+        if (rec && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
+    for (const void *p : need_saved)
+        if (!rec && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
+    if (!(a->clamp > 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (!a->ws || a->ws_bytes < moe_backward_mx_workspace_size(T, d, E, k, I, rec))
+        return MOE_ERR_WORKSPACE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const std::function<bool(int)> mark = [&](int i) -> bool {
+        if (!a->stage_events || !a->stage_events[i]) return true;
+        return cudaEventRecord(static_cast<cudaEvent_t>(a->stage_events[i]), st) == cudaSuccess;
+    };
+    const int S = T * k;
+    const int R = S + T;
+    const int G = E + 1;
+    const MxBwdWorkspace w =
+        carve_mx_bwd(static_cast<uint8_t *>(a->ws), R, d, I, rec, true, T, E, k);
+    // the bf16 rows of x (dW13 and dW_g), and of dY (dW2) and its MX rows (dgrad 2)
+    if (!mark(MOE_BWD_RECOMPUTE_GATHER)) return MOE_ERR_CUDA;
+    if ((s = launch_gather_rows(a->x, a->slot_row, T, d, k, w.x_perm, st)) != MOE_OK) return s;
+    const MxExpertBwd e{G, R, S, d, I, a->clamp, a->offsets, w.x_perm, a->x_perm_q, a->x_perm_sf,
+                        a->W13_q, a->W13_sf, a->gu_save, a->h_q, a->h_sf, a->W2t_q, a->W2t_sf,
+                        a->W13t_q, a->W13t_sf, a->row_weight, w.dY_perm, w.dYq, w.dYsf,
+                        w.dX_perm, a->dW13, a->dW2};
+    // the expert stages mark their own starts; the dY gathers sit between the
+    // GEMM-1 recompute and dgrad 2
+    const std::function<bool(int)> mark_expert = [&](int i) -> bool {
+        if (i == MOE_BWD_DGRAD2) {
+            if (!mark(MOE_BWD_GATHER_DY)) return false;
+            if (launch_gather_rows(a->dY, a->slot_row, T, d, k, w.dY_perm, st) != MOE_OK)
+                return false;
+            if (launch_mx_gather(a->dY, a->slot_row, T, d, k, w.dYq, w.dYsf, st) != MOE_OK)
+                return false;
+        }
+        return mark(i);
+    };
+    int n_part = 0;
+    if ((s = run_mx_expert_bwd(e, w, &n_part, mark_expert, st)) != MOE_OK) return s;
+    if (!mark(MOE_BWD_ROUTER)) return MOE_ERR_CUDA;
+    if ((s = launch_router_bwd(w.dw_part, n_part, a->slot_row, a->ids, a->weights, a->scores_sel,
+                               T, E, k, a->scaling, w.router.dz_sel, w.router.dz_row, a->dlogits,
+                               a->dweights, st)) != MOE_OK)
+        return s;
+    if (!mark(MOE_BWD_DX)) return MOE_ERR_CUDA;
+    if ((s = launch_combine(w.dX_perm, a->slot_row, T, d, k, 1, w.router.dz_sel, a->ids, a->W_g,
+                            a->dX, st)) != MOE_OK)
+        return s;
+    if (!mark(MOE_BWD_DWG)) return MOE_ERR_CUDA;
+    if ((s = launch_dwg(w.x_perm, w.router.dz_row, a->offsets, d, E, w.router.dwg_part, a->dW_g,
+                        st)) != MOE_OK)
+        return s;
+    return mark(MOE_BWD_STAGES) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_expert_gemm1(const uint16_t *x_perm, const int32_t *offsets, int G, int max_rows,

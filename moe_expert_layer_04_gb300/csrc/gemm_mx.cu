@@ -3,7 +3,14 @@
 // MMA (tcgen05.mma kind::mxf8f6f4).
 //
 //   MX GEMM 1   [g|u] = x~ W13~[g]^T,  h~ = MX(silu(min(g,c)) clamp(u,-c,c))
+//               (and the fp32 g|u for the backward, when it is saved)
 //   MX GEMM 2   y = w * (h~ W2~[g]^T)                               (bf16)
+//   MX dgrad 2  dA = dY~ (W2^T)~[g]^T, with W2 quantised along d; epilogue:
+//               the partial <h~, dA> per tile, dH = w dA through the clamped
+//               SwiGLU's derivative -> dG|dU (bf16, and MX along 2I), w h~
+//               (bf16)
+//   MX dgrad 1  dX = dGU~ (W13^T)~[g]^T, with W13 quantised along 2I: GEMM 2
+//               with K = 2I and no row weight
 // ("DeepSeek-V4昇腾训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse 极简训练优化
 // 实践", 性能结果与未来展望: FP8 training on MxFP8 compute; the expert matmuls
 // themselves: "HyperParallel加速DeepSeek-V4.1多模态1M长序列训练" §2.3 MegaMoE.)
@@ -52,7 +59,7 @@
 namespace moe {
 namespace {
 
-enum MxMode : int { MX_FFN1 = 0, MX_FFN2 = 1 };
+enum MxMode : int { MX_FFN1 = 0, MX_FFN2 = 1, MX_DGRAD2 = 2 };
 
 struct MxParams {
     CUtensorMap tmA;   // A codes [rows, K] u8, boxes 128 x 128, 128-byte swizzle
@@ -70,9 +77,19 @@ struct MxParams {
     uint8_t *hq;           // GEMM 1: h codes [rows, I]
     uint8_t *hsf;          // GEMM 1: h scale codes [rows, h_pitch]
     int h_pitch;
+    float *gu_out;         // GEMM 1: fp32 g|u (gu_offset layout) or null
     uint16_t *y;           // GEMM 2: [rows, d] bf16
-    const float *row_w;    // GEMM 2: weight of rows < w_rows (others 1)
+    const float *row_w;    // GEMM 2, dgrad 2: weight of rows < w_rows (others 1)
     int w_rows;
+    const float *gu_in;    // dgrad 2: the forward's fp32 g|u (gu_offset layout)
+    const uint8_t *hq_in;  // dgrad 2: the forward's h~ codes [rows, I] ...
+    const uint8_t *hsf_in; //          ... and scale codes [rows, h_pitch]
+    uint16_t *dgu;         // dgrad 2: dG|dU [rows, 2I] bf16
+    uint8_t *dguq;         //          dG|dU MX along 2I: codes [rows, 2I] ...
+    uint8_t *dgusf;        //          ... and scale codes [rows, dgu_pitch]
+    int dgu_pitch;
+    uint16_t *hw;          // dgrad 2: w h~ [rows, I] bf16
+    float *dw_part;        // dgrad 2: [rows, n_tiles * NEPI / 4] partials of <h~, dA>
     int *status;
     long long wait_limit;
 };
@@ -85,14 +102,16 @@ constexpr int kMxSfSlots = 2;         // scale slots, 4 stages each
 constexpr int kMxBarBytes = 256;
 constexpr uint32_t kMxTmemCols = 512;
 
-template <int BN>
+template <int MODE, int BN>
 struct MxShape {
     static constexpr int CODE_B = BN * 128;
     static constexpr int STAGE = kMxCodeA + CODE_B;              // codes of a stage
     static constexpr int SF_SLOT = kMxSfA + BN * kMxSfRow;        // scales of 4 stages
     static constexpr int STAGES = 4;
     static constexpr int NACC = BN == 256 ? 1 : 2;                // accumulators
-    static constexpr int NEPI = BN == 256 ? 8 : 4;                // epilogue warps
+    // epilogue warps: two per lane quadrant for the wide tiles and for the
+    // heavy epilogue of dgrad 2
+    static constexpr int NEPI = (BN == 256 || MODE == MX_DGRAD2) ? 8 : 4;
     static constexpr int THREADS = 64 + 32 * (NEPI + kMxSfWarps);
     static constexpr uint32_t SF_COL0 = NACC * BN;                // scale columns after them
     static constexpr uint32_t SF_COLS = 4 + BN / 32;              // per stage: A, then B
@@ -101,9 +120,18 @@ struct MxShape {
     static_assert((4 * STAGES + 2 * kMxSfSlots + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
 };
 
-template <int BN>
+template <int MODE, int BN>
 inline size_t mx_smem_bytes(int G) {
-    return 1024 + (size_t)MxShape<BN>::FIXED + kMxBarBytes + 8 * (size_t)(G + 2);
+    return 1024 + (size_t)MxShape<MODE, BN>::FIXED + kMxBarBytes + 8 * (size_t)(G + 2);
+}
+
+// The value of an E4M3 code (OCP FP8: bias 7, subnormal quantum 2^-9), exact.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t sign = (c & 0x80u) << 24;
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    const float mag = e != 0u ? __uint_as_float(((e + 120u) << 23) | (m << 20))
+                              : (float)m * 0.001953125f;
+    return __uint_as_float(__float_as_uint(mag) | sign);
 }
 
 __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int *mt_start,
@@ -125,9 +153,9 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
 }
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(MxShape<BN>::THREADS, 1)
+__global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
     moe_mx_gemm_kernel(const __grid_constant__ MxParams p) {
-    using SH = MxShape<BN>;
+    using SH = MxShape<MODE, BN>;
     constexpr int STAGES = SH::STAGES;
     constexpr int NACC = SH::NACC;
     constexpr int NEPI = SH::NEPI;
@@ -399,8 +427,99 @@ __global__ void __launch_bounds__(MxShape<BN>::THREADS, 1)
                         st_global_v4(dst, w[0], w[1], w[2], w[3]);
                         st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
                         p.hsf[(size_t)row * p.h_pitch + col / 32] = (uint8_t)code;
+                        if (p.gu_out) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                st_global_v4(p.gu_out + gu_offset(row, col + j, p.I), rg[j],
+                                             rg[j + 1], rg[j + 2], rg[j + 3]);
+                                st_global_v4(p.gu_out + gu_offset(row, p.I + col + j, p.I), ru[j],
+                                             ru[j + 1], ru[j + 2], ru[j + 3]);
+                            }
+                        }
                     }
                 }
+            } else if constexpr (MODE == MX_DGRAD2) {
+                constexpr int DC = BN / NPART;       // columns of dA of this warp
+                float w = 1.0f;
+                if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
+                const float cl = p.clamp;
+                float dw = 0.0f;
+#pragma unroll 1
+                for (int c = part * DC; c < (part + 1) * DC; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c, r);
+                    tmem_wait_ld();
+                    if (valid) {
+                        const int col = ti.nt * BN + c;
+                        // the forward's fp32 g, u and MX h~ of these 32 columns
+                        float4 gv4[8], uv4[8];
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4) {
+                            gv4[q4] = *reinterpret_cast<const float4 *>(
+                                p.gu_in + gu_offset(row, col + 4 * q4, p.I));
+                            uv4[q4] = *reinterpret_cast<const float4 *>(
+                                p.gu_in + gu_offset(row, p.I + col + 4 * q4, p.I));
+                        }
+                        const uint4 *hp =
+                            reinterpret_cast<const uint4 *>(p.hq_in + (size_t)row * p.I + col);
+                        const uint4 h0 = hp[0], h1 = hp[1];
+                        const uint32_t hc[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                        const float hs = mx_scale(p.hsf_in[(size_t)row * p.h_pitch + col / 32]);
+                        float *dg = reinterpret_cast<float *>(gv4);
+                        float *du = reinterpret_cast<float *>(uv4);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float g = dg[j], u = du[j];
+                            const float dA = __uint_as_float(r[j]);
+                            const float ht = e4m3_value((hc[j >> 2] >> (8 * (j & 3))) & 0xFFu) * hs;
+                            const float a = fminf(g, cl);
+                            const float b = fminf(fmaxf(u, -cl), cl);
+                            const float sg = 1.0f / (1.0f + expf(-a));
+                            const float dH = w * dA;
+                            dw = fmaf(ht, dA, dw);
+                            dg[j] = g <= cl ? dH * b * (sg + a * sg * (1.0f - sg)) : 0.0f;
+                            du[j] = (u >= -cl && u <= cl) ? dH * (a * sg) : 0.0f;
+                            r[j] = __float_as_uint(w * ht);
+                        }
+                        uint16_t *dgd = p.dgu + (size_t)row * 2 * p.I + col;
+                        uint16_t *hwd = p.hw + (size_t)row * p.I + col;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            st_global_v4(dgd + j, pack_bf16x2(dg[j], dg[j + 1]),
+                                         pack_bf16x2(dg[j + 2], dg[j + 3]),
+                                         pack_bf16x2(dg[j + 4], dg[j + 5]),
+                                         pack_bf16x2(dg[j + 6], dg[j + 7]));
+                            st_global_v4(dgd + p.I + j, pack_bf16x2(du[j], du[j + 1]),
+                                         pack_bf16x2(du[j + 2], du[j + 3]),
+                                         pack_bf16x2(du[j + 4], du[j + 5]),
+                                         pack_bf16x2(du[j + 6], du[j + 7]));
+                            st_global_v4(hwd + j,
+                                         pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                         pack_bf16x2(__uint_as_float(r[j + 2]),
+                                                     __uint_as_float(r[j + 3])),
+                                         pack_bf16x2(__uint_as_float(r[j + 4]),
+                                                     __uint_as_float(r[j + 5])),
+                                         pack_bf16x2(__uint_as_float(r[j + 6]),
+                                                     __uint_as_float(r[j + 7])));
+                        }
+                        // dG and dU quantised along 2I: each 32 columns are one block
+                        uint8_t *qd = p.dguq + (size_t)row * 2 * p.I + col;
+                        uint8_t *sd = p.dgusf + (size_t)row * p.dgu_pitch;
+                        uint32_t wq[8];
+                        const uint32_t cg =
+                            mx_quantize_block_hw(*reinterpret_cast<const float(*)[32]>(dg), wq);
+                        st_global_v4(qd, wq[0], wq[1], wq[2], wq[3]);
+                        st_global_v4(qd + 16, wq[4], wq[5], wq[6], wq[7]);
+                        sd[col / 32] = (uint8_t)cg;
+                        const uint32_t cu =
+                            mx_quantize_block_hw(*reinterpret_cast<const float(*)[32]>(du), wq);
+                        st_global_v4(qd + p.I, wq[0], wq[1], wq[2], wq[3]);
+                        st_global_v4(qd + p.I + 16, wq[4], wq[5], wq[6], wq[7]);
+                        sd[(p.I + col) / 32] = (uint8_t)cu;
+                    }
+                }
+                // one partial of <h~, dA> per (row, column tile, warp part)
+                if (valid) p.dw_part[((size_t)row * p.n_tiles + ti.nt) * NPART + part] = dw;
             } else {
                 constexpr int YC = BN / NPART;       // output columns of this warp
                 float w = 1.0f;
@@ -439,6 +558,7 @@ __global__ void __launch_bounds__(MxShape<BN>::THREADS, 1)
 
 template <int MODE, int BN>
 moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
+    using SH = MxShape<MODE, BN>;
     auto kern = moe_mx_gemm_kernel<MODE, BN>;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -446,7 +566,7 @@ moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
     if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)mx_smem_bytes<BN>(kMaxGroups)) != cudaSuccess)
+                                 (int)mx_smem_bytes<MODE, BN>(kMaxGroups)) != cudaSuccess)
             return MOE_ERR_CUDA;
         attr_set[dev] = true;
     }
@@ -455,7 +575,7 @@ moe_status launch_mx(MxParams &p, int max_tiles, cudaStream_t st) {
     if (!p.status) return MOE_ERR_CUDA;
     if (p.wait_limit <= 0) p.wait_limit = kWaitLimitCycles;
     const int grid = max_tiles < num_sms() ? max_tiles : num_sms();
-    kern<<<grid, MxShape<BN>::THREADS, mx_smem_bytes<BN>(p.G), st>>>(p);
+    kern<<<grid, SH::THREADS, mx_smem_bytes<MODE, BN>(p.G), st>>>(p);
     return cuda_status(cudaGetLastError());
 }
 
@@ -467,7 +587,8 @@ static int mx_bn(int max_rows, int G) { return (long long)max_rows >= 1024LL * G
 
 moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *offsets, int G,
                           int max_rows, const uint8_t *W13q, const uint8_t *W13sf, int d, int I,
-                          float clamp, uint8_t *hq, uint8_t *hsf, cudaStream_t st) {
+                          float clamp, uint8_t *hq, uint8_t *hsf, float *gu_save,
+                          cudaStream_t st) {
     if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     MxParams p;
     std::memset(&p, 0, sizeof p);
@@ -489,6 +610,7 @@ moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *
     p.hq = hq;
     p.hsf = hsf;
     p.h_pitch = mx_sf_pitch(I);
+    p.gu_out = gu_save;
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     return BN == 256 ? launch_mx<MX_FFN1, 256>(p, tiles, st) : launch_mx<MX_FFN1, 128>(p, tiles, st);
 }
@@ -520,5 +642,48 @@ moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     return BN == 256 ? launch_mx<MX_FFN2, 256>(p, tiles, st) : launch_mx<MX_FFN2, 128>(p, tiles, st);
 }
+
+moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32_t *offsets, int G,
+                            int max_rows, const uint8_t *W2tq, const uint8_t *W2tsf,
+                            const float *gu, const uint8_t *hq, const uint8_t *hsf,
+                            const float *row_w, int S, int d, int I, float clamp, uint16_t *dGU,
+                            uint8_t *dGUq, uint8_t *dGUsf, uint16_t *hw, float *dw_part,
+                            int *n_part, cudaStream_t st) {
+    if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    constexpr int BN = 128;   // two accumulators: a tile's epilogue overlaps the next's MMAs
+    MxParams p;
+    std::memset(&p, 0, sizeof p);
+    const int sfd = mx_sf_pitch(d);
+    const uint64_t brows = (uint64_t)G * I;
+    if (!encode_tmap_u8_2d(&p.tmA, dYq, d, max_rows, d, 128, 128, 128) ||
+        !encode_tmap_u8_2d(&p.tmB, W2tq, d, brows, d, 128, BN, 128) ||
+        !encode_tmap_u8_2d(&p.tmSA, dYsf, sfd, max_rows, sfd, 16, 128, 0) ||
+        !encode_tmap_u8_2d(&p.tmSB, W2tsf, sfd, brows, sfd, 16, BN, 0))
+        return MOE_ERR_CUDA;
+    p.offsets = offsets;
+    p.G = G;
+    p.n_tiles = I / BN;
+    p.k_blocks = d / 128;
+    p.b_rows_per_group = I;
+    p.I = I;
+    p.clamp = clamp;
+    p.row_w = row_w;
+    p.w_rows = S;
+    p.gu_in = gu;
+    p.hq_in = hq;
+    p.hsf_in = hsf;
+    p.h_pitch = mx_sf_pitch(I);
+    p.dgu = dGU;
+    p.dguq = dGUq;
+    p.dgusf = dGUsf;
+    p.dgu_pitch = mx_sf_pitch(2 * I);
+    p.hw = hw;
+    p.dw_part = dw_part;
+    if (n_part) *n_part = mx_dgrad2_n_part(I);
+    const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
+    return launch_mx<MX_DGRAD2, BN>(p, tiles, st);
+}
+
+int mx_dgrad2_n_part(int I) { return I / 128 * (MxShape<MX_DGRAD2, 128>::NEPI / 4); }
 
 }  // namespace moe

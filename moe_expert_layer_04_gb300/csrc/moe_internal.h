@@ -93,18 +93,31 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
 moe_status launch_gather_rows(const uint16_t *src, const int32_t *slot_row, int T, int d, int k,
                               uint16_t *dst, cudaStream_t st);
 
-// MXFP8 (mx.cu, gemm_mx.cu): quantisation of bf16 rows, the quantising
-// dispatch gather, and the two MX expert GEMMs (d % 256 == 0, I % 128 == 0).
+// MXFP8 (mx.cu, gemm_mx.cu): quantisation of bf16 rows (along the rows of a
+// stack of matrices, written transposed: src [G, R, C] -> q [G*C, R]), the
+// quantising dispatch gather, the two MX expert GEMMs and the MX dgrad 2
+// (d % 256 == 0, I % 128 == 0); MX dgrad 1 is launch_mx_ffn2 with K = 2I.
 moe_status launch_mx_quantize(const uint16_t *src, long long rows, int K, uint8_t *q, uint8_t *sf,
                               cudaStream_t st);
+moe_status launch_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
+                                cudaStream_t st);
 moe_status launch_mx_gather(const uint16_t *x, const int32_t *slot_row, int T, int d, int k,
                             uint8_t *q, uint8_t *sf, cudaStream_t st);
 moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *offsets, int G,
                           int max_rows, const uint8_t *W13q, const uint8_t *W13sf, int d, int I,
-                          float clamp, uint8_t *hq, uint8_t *hsf, cudaStream_t st);
+                          float clamp, uint8_t *hq, uint8_t *hsf, float *gu_save,
+                          cudaStream_t st);
 moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *offsets, int G,
                           int max_rows, const uint8_t *W2q, const uint8_t *W2sf,
                           const float *row_w, int S, int d, int I, uint16_t *y, cudaStream_t st);
+// Partials of <h~, dA> per row written by launch_mx_dgrad2.
+int mx_dgrad2_n_part(int I);
+moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32_t *offsets, int G,
+                            int max_rows, const uint8_t *W2tq, const uint8_t *W2tsf,
+                            const float *gu, const uint8_t *hq, const uint8_t *hsf,
+                            const float *row_w, int S, int d, int I, float clamp, uint16_t *dGU,
+                            uint8_t *dGUq, uint8_t *dGUsf, uint16_t *hw, float *dw_part,
+                            int *n_part, cudaStream_t st);
 
 moe_status launch_selftest_timeout(long long limit, cudaStream_t st);
 

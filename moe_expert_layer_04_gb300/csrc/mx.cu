@@ -93,7 +93,44 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Quantisation along the rows of a stack of matrices, written transposed:
+// for src [G, R, C] bf16, output row g*C + c is column c of matrix g (R
+// values) quantised in blocks of 32 along R.  One thread per output block;
+// consecutive threads take consecutive columns, so each of the 32 loads of a
+// warp reads 64 contiguous bytes.
+__global__ void __launch_bounds__(256)
+    mx_quantize_t_kernel(const uint16_t *__restrict__ src, int G, int R, int C, int sfp,
+                         uint8_t *__restrict__ q, uint8_t *__restrict__ sf) {
+    const long long nb = (long long)G * (R / 32) * C;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride) {
+        const int c = (int)(i % C);
+        const long long gb = i / C;
+        const int b = (int)(gb % (R / 32));
+        const int g = (int)(gb / (R / 32));
+        const uint16_t *col = src + ((size_t)g * R + (size_t)b * 32) * C + c;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float((uint32_t)__ldg(col + (size_t)j * C) << 16);
+        uint32_t w[8];
+        const uint32_t code = mx_quantize_block(v, w);
+        const size_t orow = (size_t)g * C + c;
+        store_block(q + orow * R + (size_t)b * 32, w);
+        sf[orow * sfp + b] = (uint8_t)code;
+    }
+}
+
 }  // namespace
+
+moe_status launch_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
+                                cudaStream_t st) {
+    const long long nb = (long long)G * (R / 32) * C;
+    if (nb == 0) return MOE_OK;
+    const long long want = (nb + 255) / 256;
+    const int blocks = (int)(want < (long long)num_sms() * 16 ? want : (long long)num_sms() * 16);
+    mx_quantize_t_kernel<<<blocks, 256, 0, st>>>(src, G, R, C, mx_sf_pitch(R), q, sf);
+    return cuda_status(cudaGetLastError());
+}
 
 moe_status launch_mx_quantize(const uint16_t *src, long long rows, int K, uint8_t *q, uint8_t *sf,
                               cudaStream_t st) {

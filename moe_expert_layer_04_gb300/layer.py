@@ -67,17 +67,20 @@ class MoELayer:
     launches and measures the same on one GPU, and its waits assume that no
     other work shares the GPU's SMs.
     mx: the low-precision variant -- the expert weights are quantised to MXFP8
-    once here (moe_mx_quantize), each step's token rows are quantised in the
-    dispatch (moe_mx_gather) and both expert matmuls take MXFP8 operands
-    (moe_expert_ffn_mx); h between them is MXFP8 too.  Forward only.
+    here (moe_mx_quantize; again with quantize_weights() after they change),
+    each step's token rows are quantised in the dispatch (moe_mx_gather) and
+    both expert matmuls take MXFP8 operands (moe_expert_ffn_mx); h between them
+    is MXFP8 too.  With backward, the weights also get copies quantised along
+    their other axis (moe_mx_quantize_t) and the backward runs the MX dgrad
+    matmuls (moe_backward_mx).  Two launches (not fused_ffn).
     """
 
     def __init__(self, dims: Dims, weights: dict, scaling: float, clamp: float = 7.0,
                  backward: bool = False, recompute: bool = False, device="cuda",
                  fused_route: bool | None = None, fused_ffn: bool = False, mx: bool = False):
         self.dims = dims
-        if mx and (backward or fused_ffn or not mx_supported(dims.d, dims.I)):
-            raise ValueError(f"the MXFP8 layer is forward-only with two launches and needs "
+        if mx and (fused_ffn or not mx_supported(dims.d, dims.I)):
+            raise ValueError(f"the MXFP8 layer runs two launches and needs "
                              f"d % 256 == 0, I % 128 == 0 (got {dims})")
         self.mx = bool(mx)
         ok = gate_route_supported(dims.d, dims.E, dims.k)
@@ -118,10 +121,16 @@ class MoELayer:
                         if backward and not recompute else None)
         self.y = torch.empty(D.T, D.d, dtype=torch.bfloat16, **e)
         flags = (MOE_FLAG_BACKWARD if backward else 0) | (MOE_FLAG_RECOMPUTE if recompute else 0)
-        ws = _lib.moe_workspace_size(D.T, D.d, D.E, D.k, D.I, flags)
+        # the MX backward has a workspace of its own
+        ws = _lib.moe_workspace_size(D.T, D.d, D.E, D.k, D.I, 0 if self.mx else flags)
         if ws == 0:
             raise ValueError(f"unsupported layer shape {D}")
         self.ws = torch.empty(ws, dtype=torch.uint8, **e)
+        if self.mx and backward:
+            wsb = _lib.moe_backward_mx_workspace_size(D.T, D.d, D.E, D.k, D.I, recompute)
+            if wsb == 0:
+                raise ValueError(f"unsupported layer shape {D}")
+            self.ws_bwd = torch.empty(wsb, dtype=torch.uint8, **e)
         if backward:
             self.dX = torch.empty(D.T, D.d, dtype=torch.bfloat16, **e)
             self.dW_g = torch.empty(D.E, D.d, dtype=torch.float32, **e)
@@ -139,12 +148,30 @@ class MoELayer:
         self.W13_sf = torch.empty(G * 2 * D.I, pd, **u8)
         self.W2_q = torch.empty(G * D.d, D.I, **u8)
         self.W2_sf = torch.empty(G * D.d, pi, **u8)
-        _lib.moe_mx_quantize(weights["W13"], G * 2 * D.I, D.d, self.W13_q, self.W13_sf)
-        _lib.moe_mx_quantize(weights["W2"], G * D.d, D.I, self.W2_q, self.W2_sf)
+        if self.backward_enabled:
+            # the dgrad matmuls contract over d (W2) and 2I (W13)
+            self.W2t_q = torch.empty(G * D.I, D.d, **u8)
+            self.W2t_sf = torch.empty(G * D.I, pd, **u8)
+            self.W13t_q = torch.empty(G * D.d, 2 * D.I, **u8)
+            self.W13t_sf = torch.empty(G * D.d, _lib.moe_mx_sf_pitch(2 * D.I), **u8)
+        self.quantize_weights()
         self.x_perm_q = torch.empty(D.R, D.d, **u8)
         self.x_perm_sf = torch.empty(D.R, pd, **u8)
         self.h_q = torch.empty(D.R, D.I, **u8)
         self.h_sf = torch.empty(D.R, pi, **u8)
+
+    def quantize_weights(self, stream=None):
+        """(MX layer) Quantise the expert weights from self.w into the MX
+        copies the matmuls read: along d and I for the forward, and with
+        backward also along d (W2) and 2I (W13) for the dgrad matmuls."""
+        D = self.dims
+        G = D.E + 1
+        W13, W2 = self.w["W13"], self.w["W2"]
+        _lib.moe_mx_quantize(W13, G * 2 * D.I, D.d, self.W13_q, self.W13_sf, stream)
+        _lib.moe_mx_quantize(W2, G * D.d, D.I, self.W2_q, self.W2_sf, stream)
+        if self.backward_enabled:
+            _lib.moe_mx_quantize_t(W2, G, D.d, D.I, self.W2t_q, self.W2t_sf, stream)
+            _lib.moe_mx_quantize_t(W13, G, 2 * D.I, D.d, self.W13t_q, self.W13t_sf, stream)
 
     # ------------------------------------------------------------ forward
     def route(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,
@@ -176,7 +203,7 @@ class MoELayer:
             _lib.moe_expert_ffn_mx(self.x_perm_q, self.x_perm_sf, self.offsets, D.E + 1, D.R,
                                    self.W13_q, self.W13_sf, self.W2_q, self.W2_sf,
                                    self.row_weight, D.S, D.d, D.I, self.clamp, self.h_q,
-                                   self.h_sf, self.y_perm, stream)
+                                   self.h_sf, self.y_perm, self.gu_save, stream)
             return
         if self.fused_ffn:
             _lib.moe_expert_ffn_fused(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"],
@@ -192,7 +219,7 @@ class MoELayer:
         if self.mx:
             _lib.moe_expert_gemm1_mx(self.x_perm_q, self.x_perm_sf, self.offsets, D.E + 1, D.R,
                                      self.W13_q, self.W13_sf, D.d, D.I, self.clamp, self.h_q,
-                                     self.h_sf, stream)
+                                     self.h_sf, self.gu_save, stream)
             return
         _lib.moe_expert_gemm1(self.x_perm, self.offsets, D.E + 1, D.R, self.w["W13"], D.d, D.I,
                               self.clamp, self.gu_save, self.h_perm, stream)
@@ -236,6 +263,21 @@ class MoELayer:
             self.dlogits = torch.empty(D.T, D.E, dtype=torch.float32, device=dY.device)
         if want_dweights and self.dweights is None:
             self.dweights = torch.empty(D.T, D.k, dtype=torch.float32, device=dY.device)
+        if self.mx:
+            _lib.moe_backward_mx(dict(
+                T=D.T, d=D.d, E=D.E, k=D.k, I=D.I, scaling=self.scaling, clamp=self.clamp,
+                x=self.x, W_g=self.w["W_g"], W13_q=self.W13_q, W13_sf=self.W13_sf,
+                W2t_q=self.W2t_q, W2t_sf=self.W2t_sf, W13t_q=self.W13t_q, W13t_sf=self.W13t_sf,
+                ids=self.ids, weights=self.weights, scores_sel=self.scores_sel,
+                row_weight=self.row_weight, offsets=self.offsets, slot_row=self.slot_row,
+                x_perm_q=self.x_perm_q, x_perm_sf=self.x_perm_sf, gu_save=self.gu_save,
+                h_q=None if self.recompute else self.h_q,
+                h_sf=None if self.recompute else self.h_sf,
+                dY=dY, dX=self.dX, dW_g=self.dW_g, dW13=self.dW13, dW2=self.dW2,
+                dlogits=self.dlogits if want_dlogits else None,
+                dweights=self.dweights if want_dweights else None, ws=self.ws_bwd,
+                stage_events=stage_events), stream)
+            return self.dX
         args = dict(T=D.T, d=D.d, E=D.E, k=D.k, I=D.I, scaling=self.scaling, clamp=self.clamp,
                     flags=MOE_FLAG_RECOMPUTE if self.recompute else 0,
                     x=self.x, W_g=self.w["W_g"], W13=self.w["W13"], W2=self.w["W2"],

@@ -29,7 +29,9 @@ def test_library_builds_and_exports_every_declared_symbol():
 
 @pytest.mark.parametrize("struct,mirror", [("moe_bwd_args", _lib.BwdArgs),
                                            ("moe_layer_buffers", _lib.LayerBuffers),
-                                           ("moe_expert_bwd_args", _lib.ExpertBwdArgs)])
+                                           ("moe_expert_bwd_args", _lib.ExpertBwdArgs),
+                                           ("moe_expert_bwd_mx_args", _lib.ExpertBwdMxArgs),
+                                           ("moe_bwd_mx_args", _lib.BwdMxArgs)])
 def test_structs_match_header(struct, mirror):
     m = re.search(r"typedef struct \{((?:(?!typedef struct).)*?)\} " + struct + ";", HEADER,
                   flags=re.S)
@@ -134,12 +136,48 @@ def test_mx_calls_host_logic():
     assert lib.moe_mx_gather(p, p, 8, 48, 2, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_mx_gather(p, nul, 8, 64, 2, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
     # moe_expert_ffn_mx: 256-wide tiles in both matmuls, aligned arrays, clamp > 0
-    args = lambda d, I, clamp=7.0, hq=p: (p, p, p, 2, 64, p, p, p, p, nul, 0, d, I, clamp, hq, p,
-                                          p, nul)
+    args = lambda d, I, clamp=7.0, hq=p: (p, p, p, 2, 64, p, p, p, p, nul, 0, d, I, clamp, nul,
+                                          hq, p, p, nul)
     assert lib.moe_expert_ffn_mx(*args(128, 128)) == _lib.MOE_ERR_UNSUPPORTED
     assert lib.moe_expert_ffn_mx(*args(256, 64)) == _lib.MOE_ERR_UNSUPPORTED
     assert lib.moe_expert_ffn_mx(*args(256, 128, hq=q)) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_expert_ffn_mx(*args(256, 128, clamp=0.0)) == _lib.MOE_ERR_INVALID_ARG
+    # moe_mx_quantize_t: R a multiple of 32, G and C at least 1, aligned arrays
+    assert lib.moe_mx_quantize_t(p, 2, 48, 8, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_quantize_t(p, 0, 64, 8, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_mx_quantize_t(p, 2, 64, 8, q, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    # the MX backward: shapes, workspace sizes, missing saved state
+    assert lib.moe_backward_mx_workspace_size(64, 128, 8, 2, 128, 0) == 0    # d % 256
+    assert lib.moe_backward_mx_workspace_size(64, 256, 8, 2, 64, 0) == 0     # I % 128
+    ws0 = lib.moe_backward_mx_workspace_size(64, 256, 8, 2, 128, 0)
+    ws1 = lib.moe_backward_mx_workspace_size(64, 256, 8, 2, 128, 1)
+    assert 0 < ws0 < ws1
+    assert 0 < lib.moe_expert_bwd_mx_workspace_size(300, 256, 128, 0) < \
+        lib.moe_expert_bwd_mx_workspace_size(300, 256, 128, 1)
+    a = _lib.BwdMxArgs()
+    a.T, a.d, a.E, a.k, a.I, a.scaling, a.clamp = 64, 256, 8, 2, 128, 2.5, 7.0
+    for name, _ in _lib.BwdMxArgs._fields_[7:]:
+        if name not in ("ws_bytes", "stage_events", "dlogits", "dweights"):
+            setattr(a, name, 256)
+    a.ws_bytes = ws0
+    a.gu_save = None                                  # recompute: needs ws1 bytes
+    assert lib.moe_backward_mx(ctypes.byref(a), nul) == _lib.MOE_ERR_WORKSPACE
+    a.x_perm_q = None                                 # ... and the forward's MX rows
+    a.ws_bytes = ws1
+    assert lib.moe_backward_mx(ctypes.byref(a), nul) == _lib.MOE_ERR_INVALID_ARG
+    a.x_perm_q, a.gu_save, a.h_q = 256, 256, None     # saved g|u without the MX h
+    assert lib.moe_backward_mx(ctypes.byref(a), nul) == _lib.MOE_ERR_INVALID_ARG
+    a.I = 64
+    assert lib.moe_backward_mx(ctypes.byref(a), nul) == _lib.MOE_ERR_UNSUPPORTED
+    e = _lib.ExpertBwdMxArgs()
+    e.G, e.max_rows, e.S, e.d, e.I, e.clamp = 3, 300, 200, 256, 128, 7.0
+    for name, _ in _lib.ExpertBwdMxArgs._fields_[6:]:
+        if name not in ("ws_bytes", "dw_rows"):
+            setattr(e, name, 256)
+    e.ws_bytes = lib.moe_expert_bwd_mx_workspace_size(300, 256, 128, 0) - 1
+    assert lib.moe_expert_ffn_backward_mx(ctypes.byref(e), nul) == _lib.MOE_ERR_WORKSPACE
+    e.dY_perm_q = 264                                 # 8-byte aligned only
+    assert lib.moe_expert_ffn_backward_mx(ctypes.byref(e), nul) == _lib.MOE_ERR_INVALID_ARG
 
 
 def test_status_strings():
