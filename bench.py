@@ -310,7 +310,7 @@ def run_ours(args, rank, world, local_rank):
     del h
     torch.cuda.empty_cache()
 
-    full = fb = extra = mx = None
+    full = fb = extra = mx = mxs = None
     if not args.no_extra and not args.tokens and not args.experts:
         full = run_full_fwd(args, weights, dev, world, hbm, bf16, peak_src)
         if not args.no_bwd:
@@ -321,6 +321,9 @@ def run_ours(args, rank, world, local_rank):
             if full is not None and "full_fwd" in mx:
                 mx["full_fwd"]["speedup_vs_bf16"] = round(
                     full["ms_per_step"] / mx["full_fwd"]["ms_per_step"], 3)
+            if not args.no_bwd:
+                mxs = run_mx_fwd_bwd(args, weights, dev, world, hbm, bf16_sus)
+                mxs["speedup_vs_bf16"] = round(ms_step / mxs["ms_per_step"], 3)
     clk = clocks.stop()
 
     line = {
@@ -351,6 +354,7 @@ def run_ours(args, rank, world, local_rank):
         "fwd_bwd": fb,
         "extra_workloads": extra,
         "mx_fwd": mx,
+        "mx_fwd_bwd": mxs,
     }
     return line
 
@@ -510,6 +514,145 @@ def run_mx_only(args):
     return {"workload": f"{wl.name}: forward, MXFP8 expert matmuls", "ms_per_step": round(ms, 4),
             "value": round(D.T / ms * 1e3, 1), "unit": "tokens/s",
             "layer_roofline_frac": round(roof / ms, 4), "kernels": kern}
+
+
+MX_STEP_CALLS = ["quantize_weights", "route", "dispatch", "expert_gemm1", "expert_gemm2",
+                 "combine"]
+MX_MATMUL_STAGES = {"expert_gemm1", "expert_gemm2", "bwd_recompute_gemm1", "bwd_dgrad2",
+                    "bwd_dgrad1"}
+
+
+def mx_step_work(D, counts):
+    """Algorithmic FLOPs and minimum HBM bytes of each call of the MXFP8
+    training step (codes one byte an element, scales one byte per 32)."""
+    used = int((counts > 0).sum()) + 1
+    R, S, T, d, I, E, G = D.R, D.S, D.T, D.d, D.I, D.E, D.E + 1
+    nw = 3 * G * d * I                               # weight elements
+    sc = lambda n: n // 32                           # scale bytes of n elements
+    fwd = {
+        "quantize_weights": (0, nw * 2 + 2 * (nw + sc(nw))),   # one read, both copies
+        "route": (2 * T * d * E, T * d * 2 + E * d * 2 + T * E * 4 + T * D.k * 12),
+        "dispatch": (0, T * d * 2 + R * d + sc(R * d) + S * 4 * 6),
+        "expert_gemm1": (4 * R * d * I, used * 2 * I * d + R * d + sc(R * d) + R * I + sc(R * I)),
+        "expert_gemm2": (2 * R * I * d, used * d * I + R * I + sc(R * I) + R * d * 2),
+        "combine": (0, R * d * 2 + T * d * 2 + S * 4),
+    }
+    bwd = {
+        "recompute_gather": (0, T * d * 2 + R * d * 2),
+        "recompute_gemm1": (4 * R * d * I, used * 2 * I * d + R * d + R * 2 * I * 4 + R * I),
+        "gather_dY": (0, 2 * T * d * 2 + R * d * 2 + R * d + sc(R * d)),
+        "dgrad2": (2 * R * d * I, used * d * I + R * d + R * 2 * I * 4 + R * I
+                   + R * 2 * I * 2 + R * 2 * I + R * I * 2),
+        "wgrad2": (2 * R * d * I, G * d * I * 4 + R * d * 2 + R * I * 2),
+        "dgrad1": (4 * R * I * d, used * 2 * I * d + R * 2 * I + R * d * 2),
+        "wgrad1": (4 * R * I * d, G * 2 * I * d * 4 + R * 2 * I * 2 + R * d * 2),
+        "router_bwd": (0, S * 4 * 6 + T * E * 4),
+        "dX": (2 * S * d, R * d * 2 + T * d * 2 + S * 8),
+        "dW_g": (2 * S * d, S * d * 2 + E * d * 4),
+    }
+    return fwd, bwd
+
+
+def run_mx_fwd_bwd(args, weights, dev, world, hbm, bf16_sus, wl=None):
+    """One MXFP8 training step of the workload (the headline's by default):
+    the expert weights quantised from bf16 (both orientations, as after an
+    optimizer update), the forward with MX expert matmuls and the MX backward
+    (dgrad matmuls on MX operands, bf16 weight gradients), CUDA events around
+    each call and backward stage."""
+    from moe_expert_layer_04_gb300 import _lib
+    from moe_expert_layer_04_gb300 import workloads as W
+    from moe_expert_layer_04_gb300.layer import Dims, MoELayer
+    wl = wl or W.WORKLOADS[HEADLINE]
+    D = Dims(wl.T, wl.d, wl.E, wl.k, wl.I)
+    inp = layer_inputs(wl, dev, weights=weights)
+    if weights is None:
+        weights = {k: inp[k] for k in ("W_g", "W13", "W2")}
+    layer = MoELayer(D, weights, wl.rho, wl.clamp, backward=True, recompute=wl.recompute,
+                     mx=True)
+    stream = torch.cuda.current_stream()
+    nb = _lib.MOE_BWD_STAGES
+    off = inp["logit_offset"]
+
+    def events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def step(fev=None, bev=None):
+        def mark(i):
+            if fev is not None:
+                fev[i].record(stream)
+        mark(0)
+        layer.quantize_weights()
+        mark(1)
+        layer.route(inp["x"], inp["bias"], inp["is_vision"], off)
+        mark(2)
+        layer.dispatch(inp["x"])
+        mark(3)
+        layer.expert_gemm1()
+        mark(4)
+        layer.expert_gemm2()
+        mark(5)
+        layer.combine()
+        mark(6)
+        layer.backward(inp["dY"], stage_events=bev)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    counts = layer.counts.cpu().numpy()
+    K = max(3, args.steps // 2)
+    fevs = [events(len(MX_STEP_CALLS) + 1) for _ in range(K)]
+    bevs = [events(nb + 1) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(fevs[i], bevs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    ms = dist_max(t0.elapsed_time(t1) / K, world)
+    fwd_ms = {n: sum(fevs[i][j].elapsed_time(fevs[i][j + 1]) for i in range(K)) / K
+              for j, n in enumerate(MX_STEP_CALLS)}
+    bwd_ms = {n: sum(bevs[i][j].elapsed_time(bevs[i][j + 1]) for i in range(K)) / K
+              for j, n in enumerate(_lib.MOE_BWD_STAGE_NAMES)}
+    fwd_work, bwd_work = mx_step_work(D, counts)
+    kernels = {}
+    for n in MX_STEP_CALLS:
+        peak = 2 * bf16_sus if n in MX_MATMUL_STAGES else bf16_sus
+        kernels[n] = stage_metrics(fwd_ms[n], *fwd_work[n], hbm, peak)
+    for n in _lib.MOE_BWD_STAGE_NAMES:
+        if bwd_ms[n] > 0:
+            key = "bwd_" + n
+            peak = 2 * bf16_sus if key in MX_MATMUL_STAGES else bf16_sus
+            kernels[key] = stage_metrics(bwd_ms[n], *bwd_work[n], hbm, peak)
+    out = {"workload": f"{wl.name}: MXFP8 training step (weights quantised, forward, "
+                       f"backward), T={wl.T} d={wl.d} E={wl.E} top-{wl.k} + shared, I={wl.I}"
+                       + (", recompute" if wl.recompute else ""),
+           "value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
+           "ms_per_step": round(ms, 4), "steps": K,
+           "dtype": "mxfp8 matmul operands (e4m3 + e8m0 per 32) in the forward and both dgrad "
+                    "matmuls, bf16 weight gradients, fp32 accumulate",
+           "peak_note": "MX matmul stages against 2x the measured sustained bf16 peak",
+           "kernels": kernels}
+    del layer, inp
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_mx_fwd_bwd_only(args):
+    """Only the MXFP8 training step of the workload (profiling captures)."""
+    from moe_expert_layer_04_gb300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    hbm, _, bf16_sus, _ = peaks()
+    wl = workload(args)
+    return run_mx_fwd_bwd(args, None, dev, 1, hbm, bf16_sus, wl=wl)
 
 
 def run_extra_workloads(args, weights, dev, world, hbm, bf16):
@@ -981,6 +1124,8 @@ def main():
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP8 forward")
     ap.add_argument("--mx-only", action="store_true",
                     help="time only the MXFP8 forward of the workload (profiling)")
+    ap.add_argument("--mx-fwd-bwd-only", action="store_true",
+                    help="time only the MXFP8 training step of the workload (profiling)")
     ap.add_argument("--pairs", type=int, default=None,
                     help="MOE_PAIR_* mask of the matmuls that may run as 2-SM pairs "
                          "(default: the library's)")
@@ -1002,6 +1147,9 @@ def main():
         return
     if args.mx_only:
         print(json.dumps(run_mx_only(args)), flush=True)
+        return
+    if args.mx_fwd_bwd_only:
+        print(json.dumps(run_mx_fwd_bwd_only(args)), flush=True)
         return
     if args.impl == "reference":
         line = run_reference(args, rank, world)

@@ -514,6 +514,16 @@ moe_status moe_expert_gemm2_mx(const uint8_t *h_q, const uint8_t *h_sf, const in
 moe_status moe_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
                              void *stream);
 
+/* Both quantisations of a stack of matrices in one pass over src [G, R, C]
+ * bf16: q [G*R, C] / sf [G*R, moe_mx_sf_pitch(C)] along the rows (as
+ * moe_mx_quantize of src viewed as [G*R, C]) and qt [G*C, R] / sft [G*C,
+ * moe_mx_sf_pitch(R)] along the columns (as moe_mx_quantize_t) -- the
+ * forward's and the backward's copies of a weight after each update, for
+ * half the HBM reads of the two calls.  Needs R % 128 == 0 and C % 128 == 0
+ * (else MOE_ERR_UNSUPPORTED), G >= 1, 16-byte aligned arrays. */
+moe_status moe_mx_quantize_both(const uint16_t *src, int G, int R, int C, uint8_t *q,
+                                uint8_t *sf, uint8_t *qt, uint8_t *sft, void *stream);
+
 /* Backward of moe_expert_ffn_mx on its rows, in the MX training form: each
  * matmul takes its two operands quantised along its own contraction.
  *   dA[r]   = dY~[r] (W2^T)~[g]^T     dY along d, W2 along d  (fp32 sums)

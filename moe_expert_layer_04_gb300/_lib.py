@@ -42,7 +42,7 @@ EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_rout
            "moe_set_gemm_pairs", "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
            "moe_expert_gemm1_mx", "moe_expert_gemm2_mx", "moe_mx_quantize_t",
            "moe_expert_bwd_mx_workspace_size", "moe_expert_ffn_backward_mx",
-           "moe_backward_mx_workspace_size", "moe_backward_mx"]
+           "moe_backward_mx_workspace_size", "moe_backward_mx", "moe_mx_quantize_both"]
 
 
 class MoeError(RuntimeError):
@@ -203,6 +203,7 @@ _SIGS = {
                            _P, _P], _I),
     "moe_expert_gemm1_mx": ([_P, _P, _P, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P, _P], _I),
     "moe_mx_quantize_t": ([_P, _I, _I, _I, _P, _P, _P], _I),
+    "moe_mx_quantize_both": ([_P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "moe_expert_bwd_mx_workspace_size": ([_I, _I, _I, _I], _Z),
     "moe_expert_ffn_backward_mx": ([ctypes.POINTER(ExpertBwdMxArgs), _P], _I),
     "moe_backward_mx_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
@@ -411,6 +412,13 @@ def moe_mx_quantize_t(src, G, R, C, q, sf, stream=None):
     st = load().moe_mx_quantize_t(_ptr(src, BF16, "src"), int(G), int(R), int(C),
                                   _ptr(q, U8, "q"), _ptr(sf, U8, "sf"), _stream(stream))
     _check("moe_mx_quantize_t", st)
+
+
+def moe_mx_quantize_both(src, G, R, C, q, sf, qt, sft, stream=None):
+    st = load().moe_mx_quantize_both(_ptr(src, BF16, "src"), int(G), int(R), int(C),
+                                     _ptr(q, U8, "q"), _ptr(sf, U8, "sf"), _ptr(qt, U8, "qt"),
+                                     _ptr(sft, U8, "sft"), _stream(stream))
+    _check("moe_mx_quantize_both", st)
 
 
 def moe_expert_bwd_mx_workspace_size(max_rows, d, I, recompute) -> int:

@@ -554,6 +554,18 @@ moe_status moe_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *
     return launch_mx_quantize_t(src, G, R, C, q, sf, static_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_mx_quantize_both(const uint16_t *src, int G, int R, int C, uint8_t *q,
+                                uint8_t *sf, uint8_t *qt, uint8_t *sft, void *stream) {
+    if (G < 1 || R < 1 || C < 1) return MOE_ERR_INVALID_ARG;
+    if (R % 128 != 0 || C % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)G * R * C >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+    for (const void *p : {static_cast<const void *>(src), static_cast<const void *>(q),
+                          static_cast<const void *>(sf), static_cast<const void *>(qt),
+                          static_cast<const void *>(sft)})
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    return launch_mx_quantize_both(src, G, R, C, q, sf, qt, sft, static_cast<cudaStream_t>(stream));
+}
+
 namespace {
 
 // The expert part of the MX backward on expert-contiguous rows (shared by the

@@ -36,22 +36,28 @@
 // instruction descriptor picks its byte -- byte j for the j-th block of 32 of
 // the stage.
 //
-// One CTA per SM, 10 warps:
+// One CTA per SM, 10 warps (14 with two epilogue warps per lane quadrant:
+// the 256-wide tiles and dgrad 2):
 //   warp 0      TMA producer: per stage the A and B code tiles (128-byte rows,
-//               128-byte swizzle) and the 16-byte scale rows of A and B that
-//               hold the stage's four scale codes.
-//   warp 1      TMEM owner and MMA issuer (block-scaled MMA, M = 128, N = 128,
-//               K = 32, four per stage).
-//   warps 2-5   epilogue, thread = row: GEMM 1 the clamped SwiGLU and h
+//               128-byte swizzle), per four stages the 16-byte scale rows of
+//               A and B that hold their scale codes.
+//   warp 1      TMEM owner and MMA issuer (block-scaled MMA, M = 128,
+//               N = BN, K = 32, four per stage).
+//   warps 2-    epilogue, thread = row: GEMM 1 the clamped SwiGLU and h
 //               quantised to MXFP8 per 32 columns (hardware conversion);
-//               GEMM 2 the routing-weight scale to bf16.
-//   warps 6-9   scale writers, one per TMEM lane quadrant, thread = row: the
-//               stage's four A scale codes and four B scale codes of its row
-//               into tensor memory (tcgen05.st), then release the stage to the
-//               MMA issuer.
+//               GEMM 2 the routing-weight scale to bf16; dgrad 2 the SwiGLU
+//               backward and its four outputs.
+//   last 4      scale writers, one per TMEM lane quadrant, thread = row: per
+//               stage the four A scale codes and the B scale codes of its
+//               rows into tensor memory (tcgen05.st), then the stage is
+//               released to the MMA issuer.  (Loading a slot's 16-byte rows
+//               once into registers and releasing the slot early measured
+//               slower for the forward GEMMs and dgrad 1.)
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and exits.
 #include <cstring>
+
+#include <cuda_fp16.h>
 
 #include "gemm_launch.cuh"
 #include "mx_common.cuh"
@@ -125,13 +131,31 @@ inline size_t mx_smem_bytes(int G) {
     return 1024 + (size_t)MxShape<MODE, BN>::FIXED + kMxBarBytes + 8 * (size_t)(G + 2);
 }
 
-// The value of an E4M3 code (OCP FP8: bias 7, subnormal quantum 2^-9), exact.
-__device__ __forceinline__ float e4m3_value(uint32_t c) {
-    const uint32_t sign = (c & 0x80u) << 24;
-    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-    const float mag = e != 0u ? __uint_as_float(((e + 120u) << 23) | (m << 20))
-                              : (float)m * 0.001953125f;
-    return __uint_as_float(__float_as_uint(mag) | sign);
+// Values of four E4M3 codes (one 32-bit word, element i in byte i), exact:
+// the hardware conversion to f16 pairs (every E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_values(uint32_t w, float (&v)[4]) {
+    uint32_t lo, hi;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((uint16_t)(w & 0xFFFFu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((uint16_t)(w >> 16)));
+    const __half2 l = *reinterpret_cast<const __half2 *>(&lo);
+    const __half2 h = *reinterpret_cast<const __half2 *>(&hi);
+    v[0] = __low2float(l);
+    v[1] = __high2float(l);
+    v[2] = __low2float(h);
+    v[3] = __high2float(h);
+}
+
+// sigmoid(a) with the fast exponential and division (a few ulp): the MX
+// epilogues quantise what they compute from it to E4M3 (or use it in a
+// gradient), far coarser than this error.
+__device__ __forceinline__ float sigmoid_fast(float a) {
+    return __fdividef(1.0f, 1.0f + __expf(-a));
+}
+
+__device__ __forceinline__ float swiglu_clamped_fast(float g, float u, float c) {
+    const float a = fminf(g, c);
+    const float b = fminf(fmaxf(u, -c), c);
+    return a * sigmoid_fast(a) * b;
 }
 
 __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int *mt_start,
@@ -418,8 +442,8 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                         float hv[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            hv[j] = swiglu_clamped(__uint_as_float(rg[j]), __uint_as_float(ru[j]),
-                                                   p.clamp);
+                            hv[j] = swiglu_clamped_fast(__uint_as_float(rg[j]),
+                                                        __uint_as_float(ru[j]), p.clamp);
                         uint32_t w[8];
                         const uint32_t code = mx_quantize_block_hw(hv, w);
                         const int col = ti.nt * (BN / 2) + c;
@@ -469,12 +493,14 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                         float *du = reinterpret_cast<float *>(uv4);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
+                            float h4[4];
+                            e4m3x4_values(hc[j >> 2], h4);
                             const float g = dg[j], u = du[j];
                             const float dA = __uint_as_float(r[j]);
-                            const float ht = e4m3_value((hc[j >> 2] >> (8 * (j & 3))) & 0xFFu) * hs;
+                            const float ht = h4[j & 3] * hs;
                             const float a = fminf(g, cl);
                             const float b = fminf(fmaxf(u, -cl), cl);
-                            const float sg = 1.0f / (1.0f + expf(-a));
+                            const float sg = sigmoid_fast(a);
                             const float dH = w * dA;
                             dw = fmaf(ht, dA, dw);
                             dg[j] = g <= cl ? dH * b * (sg + a * sg * (1.0f - sg)) : 0.0f;

@@ -101,6 +101,8 @@ moe_status launch_mx_quantize(const uint16_t *src, long long rows, int K, uint8_
                               cudaStream_t st);
 moe_status launch_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
                                 cudaStream_t st);
+moe_status launch_mx_quantize_both(const uint16_t *src, int G, int R, int C, uint8_t *q,
+                                   uint8_t *sf, uint8_t *qt, uint8_t *sft, cudaStream_t st);
 moe_status launch_mx_gather(const uint16_t *x, const int32_t *slot_row, int T, int d, int k,
                             uint8_t *q, uint8_t *sf, cudaStream_t st);
 moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *offsets, int G,

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256)
         float v[32];
         load_block_bf16(src + (size_t)r * K + (size_t)b * 32, v);
         uint32_t w[8];
-        const uint32_t code = mx_quantize_block(v, w);
+        const uint32_t code = mx_quantize_block_hw(v, w);
         store_block(q + (size_t)r * K + (size_t)b * 32, w);
         sf[(size_t)r * sfp + b] = (uint8_t)code;
     }
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256)
                 if (b < nb) {
                     float v[32];
                     load_block_bf16(x + (size_t)t * d + (size_t)b * 32, v);
-                    code[u] = mx_quantize_block(v, w[u]);
+                    code[u] = mx_quantize_block_hw(v, w[u]);
                 }
             }
             for (int j = 0; j <= k; ++j) {
@@ -113,14 +113,152 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float((uint32_t)__ldg(col + (size_t)j * C) << 16);
         uint32_t w[8];
-        const uint32_t code = mx_quantize_block(v, w);
+        const uint32_t code = mx_quantize_block_hw(v, w);
         const size_t orow = (size_t)g * C + c;
         store_block(q + orow * R + (size_t)b * 32, w);
         sf[orow * sfp + b] = (uint8_t)code;
     }
 }
 
+// Both orientations of a stack of matrices in one pass: for src [G, R, C]
+// bf16 (R, C multiples of 128), q [G*R, C] quantised along C (rows) and qt
+// [G*C, R] quantised along R (columns, written transposed).  A CTA takes
+// 128 x 128 tiles: its 256 threads stage the tile in shared memory, then
+// threads 0-127 quantise one row each (4 blocks) while threads 128-255
+// quantise one column each (4 blocks along R); both write their codes to
+// staging tiles in shared memory and their four scale codes as one 32-bit
+// word, and all threads then copy the two code tiles out with coalesced
+// 16-byte stores (eight threads per 128-byte row).  Row pitches padded by
+// 16 bytes keep every shared-memory pass free of bank conflicts.  The next
+// tile's loads are in flight during the quantisation.
+constexpr int kQT = 128;                  // tile edge
+constexpr int kQTPitch = kQT * 2 + 16;    // bytes per staged bf16 row
+constexpr int kQCPitch = kQT + 16;        // bytes per staged code row
+constexpr int kQSmem = kQT * kQTPitch + 2 * kQT * kQCPitch;
+
+__global__ void __launch_bounds__(256)
+    mx_quantize_both_kernel(const uint16_t *__restrict__ src, int G, int R, int C, int sfpC,
+                            int sfpR, uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
+                            uint8_t *__restrict__ qt, uint8_t *__restrict__ sft) {
+    extern __shared__ __align__(16) uint8_t qsm[];
+    uint8_t *tile = qsm;                              // [128][kQTPitch] bf16 rows
+    uint8_t *cq = qsm + kQT * kQTPitch;               // [128 rows][kQCPitch] codes along C
+    uint8_t *cqt = cq + kQT * kQCPitch;               // [128 cols][kQCPitch] codes along R
+    const int tr = R / kQT, tc = C / kQT;
+    const long long n_tiles = (long long)G * tr * tc;
+    const int t = threadIdx.x;
+    // column tiles fastest: the scale words of a row fill their 32-byte
+    // sectors within a few consecutive tiles
+    auto origin = [&](long long i, int &g, int &r0, int &c0) {
+        c0 = (int)(i % tc) * kQT;
+        const long long rest = i / tc;
+        r0 = (int)(rest % tr) * kQT;
+        g = (int)(rest / tr);
+    };
+    // the tile's 16-byte chunks of this thread (16 per row), loaded into
+    // registers one tile ahead
+    uint4 v[8];
+    auto load = [&](long long i) {
+        int g, r0, c0;
+        origin(i, g, r0, c0);
+        const uint16_t *base = src + ((size_t)g * R + r0) * C + c0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int chunk = t + 256 * j;
+            v[j] = __ldg(reinterpret_cast<const uint4 *>(base + (size_t)(chunk >> 4) * C) +
+                         (chunk & 15));
+        }
+    };
+    if ((long long)blockIdx.x < n_tiles) load(blockIdx.x);
+    for (long long i = blockIdx.x; i < n_tiles; i += gridDim.x) {
+        int g, r0, c0;
+        origin(i, g, r0, c0);
+        __syncthreads();   // the previous tile's readers and copiers are done
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int chunk = t + 256 * j;
+            *reinterpret_cast<uint4 *>(tile + (chunk >> 4) * kQTPitch + (chunk & 15) * 16) = v[j];
+        }
+        __syncthreads();
+        if (i + gridDim.x < n_tiles) load(i + gridDim.x);
+        uint32_t codes = 0;
+        if (t < kQT) {
+            // row r0 + t: four blocks along C
+            const uint8_t *rowp = tile + t * kQTPitch;
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(rowp + b * 64 + j * 16);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        f[8 * j + 2 * e] = __uint_as_float(w[e] << 16);
+                        f[8 * j + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                    }
+                }
+                uint32_t w[8];
+                codes |= mx_quantize_block_hw(f, w) << (8 * b);
+                store_block(cq + t * kQCPitch + b * 32, w);
+            }
+            *reinterpret_cast<uint32_t *>(sf + ((size_t)g * R + r0 + t) * sfpC + c0 / 32) = codes;
+        } else {
+            // column c0 + (t - 128): four blocks along R
+            const int c = t - kQT;
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    f[j] = __uint_as_float(
+                        (uint32_t)*reinterpret_cast<const uint16_t *>(tile + (b * 32 + j) * kQTPitch +
+                                                                      c * 2)
+                        << 16);
+                uint32_t w[8];
+                codes |= mx_quantize_block_hw(f, w) << (8 * b);
+                store_block(cqt + c * kQCPitch + b * 32, w);
+            }
+            *reinterpret_cast<uint32_t *>(sft + ((size_t)g * C + c0 + c) * sfpR + r0 / 32) = codes;
+        }
+        __syncthreads();
+        // both code tiles out: 8 chunks of 16 bytes per 128-byte row
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int chunk = t + 256 * j;
+            const int row = chunk >> 3, c16 = (chunk & 7) * 16;
+            *reinterpret_cast<uint4 *>(q + ((size_t)g * R + r0 + row) * C + c0 + c16) =
+                *reinterpret_cast<const uint4 *>(cq + row * kQCPitch + c16);
+            *reinterpret_cast<uint4 *>(qt + ((size_t)g * C + c0 + row) * R + r0 + c16) =
+                *reinterpret_cast<const uint4 *>(cqt + row * kQCPitch + c16);
+        }
+    }
+}
+
 }  // namespace
+
+moe_status launch_mx_quantize_both(const uint16_t *src, int G, int R, int C, uint8_t *q,
+                                   uint8_t *sf, uint8_t *qt, uint8_t *sft, cudaStream_t st) {
+    if (R % kQT != 0 || C % kQT != 0) return MOE_ERR_UNSUPPORTED;
+    const long long n_tiles = (long long)G * (R / kQT) * (C / kQT);
+    if (n_tiles == 0) return MOE_OK;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(mx_quantize_both_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const long long cap = (long long)num_sms() * 3;
+    const int blocks = (int)(n_tiles < cap ? n_tiles : cap);
+    mx_quantize_both_kernel<<<blocks, 256, kQSmem, st>>>(src, G, R, C, mx_sf_pitch(C),
+                                                         mx_sf_pitch(R), q, sf, qt, sft);
+    return cuda_status(cudaGetLastError());
+}
 
 moe_status launch_mx_quantize_t(const uint16_t *src, int G, int R, int C, uint8_t *q, uint8_t *sf,
                                 cudaStream_t st) {

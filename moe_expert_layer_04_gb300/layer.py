@@ -167,11 +167,15 @@ class MoELayer:
         D = self.dims
         G = D.E + 1
         W13, W2 = self.w["W13"], self.w["W2"]
+        if self.backward_enabled:
+            # one pass over each weight for both copies
+            _lib.moe_mx_quantize_both(W13, G, 2 * D.I, D.d, self.W13_q, self.W13_sf,
+                                      self.W13t_q, self.W13t_sf, stream)
+            _lib.moe_mx_quantize_both(W2, G, D.d, D.I, self.W2_q, self.W2_sf, self.W2t_q,
+                                      self.W2t_sf, stream)
+            return
         _lib.moe_mx_quantize(W13, G * 2 * D.I, D.d, self.W13_q, self.W13_sf, stream)
         _lib.moe_mx_quantize(W2, G * D.d, D.I, self.W2_q, self.W2_sf, stream)
-        if self.backward_enabled:
-            _lib.moe_mx_quantize_t(W2, G, D.d, D.I, self.W2t_q, self.W2t_sf, stream)
-            _lib.moe_mx_quantize_t(W13, G, 2 * D.I, D.d, self.W13t_q, self.W13t_sf, stream)
 
     # ------------------------------------------------------------ forward
     def route(self, x, bias, is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK,

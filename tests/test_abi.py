@@ -146,6 +146,9 @@ def test_mx_calls_host_logic():
     assert lib.moe_mx_quantize_t(p, 2, 48, 8, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_mx_quantize_t(p, 0, 64, 8, p, p, nul) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_mx_quantize_t(p, 2, 64, 8, q, p, nul) == _lib.MOE_ERR_INVALID_ARG
+    # moe_mx_quantize_both: 128 x 128 tiles
+    assert lib.moe_mx_quantize_both(p, 1, 96, 128, p, p, p, p, nul) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_mx_quantize_both(p, 1, 128, 128, p, p, q, p, nul) == _lib.MOE_ERR_INVALID_ARG
     # the MX backward: shapes, workspace sizes, missing saved state
     assert lib.moe_backward_mx_workspace_size(64, 128, 8, 2, 128, 0) == 0    # d % 256
     assert lib.moe_backward_mx_workspace_size(64, 256, 8, 2, 64, 0) == 0     # I % 128

@@ -50,6 +50,36 @@ def test_mx_quantize_t_bit_exact(G, R, C):
     assert np.all(sf[:, R // 32:] == PAD)
 
 
+@pytest.mark.parametrize("G,R,C", [(1, 128, 128), (2, 256, 384)])
+def test_mx_quantize_both_bit_exact(G, R, C):
+    """Both orientations in one pass: each equal, bit for bit, to the
+    oracle's quantisation of the rows and of the columns."""
+    g = torch.Generator().manual_seed(G * 977 + R + C)
+    x = torch.randn(G, R, C, generator=g, dtype=torch.float64)
+    x *= torch.exp(torch.randn(G, R, 1, generator=g, dtype=torch.float64) * 2)
+    x *= torch.exp(torch.randn(G, 1, C, generator=g, dtype=torch.float64) * 2)
+    x[0, :32, :32] = 0.0                                # zero blocks both ways
+    x[0, 32:64, 0:32] = 2.0 ** -131                     # scales clamp at 2^-127
+    x[0, 64, 64:96] = 1.9 * 2.0 ** 3                    # a row block that saturates
+    xb = x.to(torch.bfloat16)
+    dev = dict(dtype=torch.uint8, device="cuda")
+    q = torch.empty(G * R, C, **dev)
+    sf = torch.full((G * R, _lib.moe_mx_sf_pitch(C)), PAD, **dev)
+    qt = torch.empty(G * C, R, **dev)
+    sft = torch.full((G * C, _lib.moe_mx_sf_pitch(R)), PAD, **dev)
+    _lib.moe_mx_quantize_both(xb.cuda(), G, R, C, q, sf, qt, sft)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    q_ref, sf_ref = oracle.mx_quantize(xb.reshape(G * R, C))
+    assert np.array_equal(cpu(q).numpy(), q_ref)
+    assert np.array_equal(cpu(sf).numpy()[:, : C // 32], sf_ref)
+    qt_ref, sft_ref = oracle.mx_quantize(xb.transpose(1, 2).reshape(G * C, R))
+    assert np.array_equal(cpu(qt).numpy(), qt_ref)
+    assert np.array_equal(cpu(sft).numpy()[:, : R // 32], sft_ref)
+    assert np.all(cpu(sf).numpy()[:, C // 32:] == PAD)
+    assert np.all(cpu(sft).numpy()[:, R // 32:] == PAD)
+
+
 def _run(name, T, d, E, k, I, n_empty=0, recompute=False):
     w = W.Workload(name, T, d, E, k, I, 2.5, vision_frac=0.3)
     inp = W.make_inputs(w, device="cuda", with_dy=True)
