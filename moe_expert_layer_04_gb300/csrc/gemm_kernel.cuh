@@ -206,10 +206,19 @@ __device__ __forceinline__ size_t gu_offset(int row, int col, int I) {
            (size_t)(row & 31) * 4 + (size_t)(col & 3);
 }
 
+// sigmoid(a) with the fast exponential and division (a few ulp of fp32, far
+// below the bf16 or E4M3 rounding of everything computed from it).
+__device__ __forceinline__ float sigmoid_fast(float a) {
+    return __fdividef(1.0f, 1.0f + __expf(-a));
+}
+
+// h = silu(min(g, c)) * clamp(u, -c, c).  The forward's epilogues and dgrad 2's
+// recompute of h call this one function on the same fp32 g and u, so the two
+// agree bit for bit.
 __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
     const float a = fminf(g, c);
     const float b = fminf(fmaxf(u, -c), c);
-    return a / (1.0f + expf(-a)) * b;
+    return a * sigmoid_fast(a) * b;
 }
 
 // Epilogue of expert GEMM 1 (one thread = one row of the tile): the clamped
@@ -747,7 +756,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                                 const float dA = __uint_as_float(r[2 * e + hlf]);
                                 const float a = fminf(g, cl);
                                 const float b = fminf(fmaxf(u, -cl), cl);
-                                const float sg = 1.0f / (1.0f + expf(-a));
+                                const float sg = sigmoid_fast(a);
                                 const float si = a * sg;
                                 // bit-identical to the forward's h (same fp32 g, u and code)
                                 const float hv = round_bf16(swiglu_clamped(g, u, cl));

@@ -145,19 +145,6 @@ __device__ __forceinline__ void e4m3x4_values(uint32_t w, float (&v)[4]) {
     v[3] = __high2float(h);
 }
 
-// sigmoid(a) with the fast exponential and division (a few ulp): the MX
-// epilogues quantise what they compute from it to E4M3 (or use it in a
-// gradient), far coarser than this error.
-__device__ __forceinline__ float sigmoid_fast(float a) {
-    return __fdividef(1.0f, 1.0f + __expf(-a));
-}
-
-__device__ __forceinline__ float swiglu_clamped_fast(float g, float u, float c) {
-    const float a = fminf(g, c);
-    const float b = fminf(fmaxf(u, -c), c);
-    return a * sigmoid_fast(a) * b;
-}
-
 __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int *mt_start,
                                             const int *offs) {
     TileInfo ti{};
@@ -442,10 +429,10 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                         float hv[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            hv[j] = swiglu_clamped_fast(__uint_as_float(rg[j]),
+                            hv[j] = swiglu_clamped(__uint_as_float(rg[j]),
                                                         __uint_as_float(ru[j]), p.clamp);
                         uint32_t w[8];
-                        const uint32_t code = mx_quantize_block_hw(hv, w);
+                        const uint32_t code = mx_quantize_block(hv, w);
                         const int col = ti.nt * (BN / 2) + c;
                         uint8_t *dst = p.hq + (size_t)row * p.I + col;
                         st_global_v4(dst, w[0], w[1], w[2], w[3]);
@@ -533,12 +520,12 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                         uint8_t *sd = p.dgusf + (size_t)row * p.dgu_pitch;
                         uint32_t wq[8];
                         const uint32_t cg =
-                            mx_quantize_block_hw(*reinterpret_cast<const float(*)[32]>(dg), wq);
+                            mx_quantize_block(*reinterpret_cast<const float(*)[32]>(dg), wq);
                         st_global_v4(qd, wq[0], wq[1], wq[2], wq[3]);
                         st_global_v4(qd + 16, wq[4], wq[5], wq[6], wq[7]);
                         sd[col / 32] = (uint8_t)cg;
                         const uint32_t cu =
-                            mx_quantize_block_hw(*reinterpret_cast<const float(*)[32]>(du), wq);
+                            mx_quantize_block(*reinterpret_cast<const float(*)[32]>(du), wq);
                         st_global_v4(qd + p.I, wq[0], wq[1], wq[2], wq[3]);
                         st_global_v4(qd + p.I + 16, wq[4], wq[5], wq[6], wq[7]);
                         sd[(p.I + col) / 32] = (uint8_t)cu;

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256)
         float v[32];
         load_block_bf16(src + (size_t)r * K + (size_t)b * 32, v);
         uint32_t w[8];
-        const uint32_t code = mx_quantize_block_hw(v, w);
+        const uint32_t code = mx_quantize_block(v, w);
         store_block(q + (size_t)r * K + (size_t)b * 32, w);
         sf[(size_t)r * sfp + b] = (uint8_t)code;
     }
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256)
                 if (b < nb) {
                     float v[32];
                     load_block_bf16(x + (size_t)t * d + (size_t)b * 32, v);
-                    code[u] = mx_quantize_block_hw(v, w[u]);
+                    code[u] = mx_quantize_block(v, w[u]);
                 }
             }
             for (int j = 0; j <= k; ++j) {
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float((uint32_t)__ldg(col + (size_t)j * C) << 16);
         uint32_t w[8];
-        const uint32_t code = mx_quantize_block_hw(v, w);
+        const uint32_t code = mx_quantize_block(v, w);
         const size_t orow = (size_t)g * C + c;
         store_block(q + orow * R + (size_t)b * 32, w);
         sf[orow * sfp + b] = (uint8_t)code;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(256)
                     }
                 }
                 uint32_t w[8];
-                codes |= mx_quantize_block_hw(f, w) << (8 * b);
+                codes |= mx_quantize_block(f, w) << (8 * b);
                 store_block(cq + t * kQCPitch + b * 32, w);
             }
             *reinterpret_cast<uint32_t *>(sf + ((size_t)g * R + r0 + t) * sfpC + c0 / 32) = codes;
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(256)
                                                                       c * 2)
                         << 16);
                 uint32_t w[8];
-                codes |= mx_quantize_block_hw(f, w) << (8 * b);
+                codes |= mx_quantize_block(f, w) << (8 * b);
                 store_block(cqt + c * kQCPitch + b * 32, w);
             }
             *reinterpret_cast<uint32_t *>(sft + ((size_t)g * C + c0 + c) * sfpR + r0 / 32) = codes;

@@ -44,57 +44,12 @@ __device__ __forceinline__ float exp2_int(int p) {
 __device__ __forceinline__ float mx_scale(uint32_t code) { return exp2_int((int)code - 127); }
 __device__ __forceinline__ float mx_inv_scale(uint32_t code) { return exp2_int(127 - (int)code); }
 
-// E4M3 code nearest to y (ties to even), magnitude saturated at 448; the sign
-// is kept for values that round to zero.  Integer arithmetic on y's bits.
-__device__ __forceinline__ uint32_t e4m3_rne(float y) {
-    const uint32_t b = __float_as_uint(y);
-    const uint32_t sign = (b >> 24) & 0x80u;
-    const uint32_t mag = b & 0x7FFFFFFFu;
-    if (mag >= 0x44000000u) return sign | 0x7Eu;         // |y| >= 512 (or not finite)
-    const int e = (int)(mag >> 23) - 127;                  // floor(log2 |y|) for normal y
-    if (e < -10) return sign;                              // |y| < 2^-10: rounds to zero
-    const uint32_t m = (mag & 0x7FFFFFu) | 0x800000u;      // 24-bit significand
-    // units of the target spacing: 2^(e-3) for E4M3 normals, 2^-9 below 2^-6
-    const int shift = e >= -6 ? 20 : 14 - e;               // 20 .. 24
-    uint32_t q = m >> shift;
-    const uint32_t rem = m & ((1u << shift) - 1u);
-    const uint32_t half = 1u << (shift - 1);
-    q += (rem > half || (rem == half && (q & 1u))) ? 1u : 0u;
-    uint32_t code;
-    if (e >= -6) {
-        int ee = e;
-        if (q == 16u) {                                    // rounded up into the next binade
-            q = 8u;
-            ++ee;
-        }
-        code = ((uint32_t)(ee + 7) << 3) | (q - 8u);
-        if (code > 0x7Eu) code = 0x7Eu;                    // 480 and above saturate to 448
-    } else {
-        code = q;                                          // subnormal; q = 8 is 2^-6
-    }
-    return sign | code;
-}
-
 // Quantises 32 fp32 values (one block) into 8 words of E4M3 codes (element i
-// in byte i % 4 of word i / 4) and returns the block's E8M0 scale code.
+// in byte i % 4 of word i / 4) and returns the block's E8M0 scale code.  The
+// element codes come from the hardware conversion (cvt.rn.satfinite: nearest
+// value, ties to even, magnitudes saturating at 448, the sign kept for values
+// that round to zero), which is the rounding rule above.
 __device__ __forceinline__ uint32_t mx_quantize_block(const float (&v)[32], uint32_t (&w)[8]) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const uint32_t code = mx_scale_code(amax);
-    const float inv = mx_inv_scale(code);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        w[j] = e4m3_rne(v[4 * j] * inv) | (e4m3_rne(v[4 * j + 1] * inv) << 8) |
-               (e4m3_rne(v[4 * j + 2] * inv) << 16) | (e4m3_rne(v[4 * j + 3] * inv) << 24);
-    return code;
-}
-
-// The same quantisation of one block with the hardware conversion
-// (cvt.rn.satfinite: nearest-even, saturating at 448), for the expert GEMM's
-// epilogue, where it takes a fraction of the issue slots of e4m3_rne.  The
-// quantiser kernel keeps e4m3_rne.
-__device__ __forceinline__ uint32_t mx_quantize_block_hw(const float (&v)[32], uint32_t (&w)[8]) {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
