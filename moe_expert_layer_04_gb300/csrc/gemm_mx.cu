@@ -69,6 +69,9 @@ enum MxMode : int { MX_FFN1 = 0, MX_FFN2 = 1, MX_DGRAD2 = 2 };
 
 struct MxParams {
     CUtensorMap tmA;   // A codes [rows, K] u8, boxes 128 x 128, 128-byte swizzle
+    CUtensorMap tmO;   // dgrad 2: dG|dU [rows, 2I] bf16, boxes 32 x 32, 64-byte swizzle
+    CUtensorMap tmO2;  // dgrad 2: w h~ [rows, I] bf16, boxes 32 x 32, 64-byte swizzle
+    CUtensorMap tmOQ;  // dgrad 2: dG|dU codes [rows, 2I] u8, boxes 32 x 32
     CUtensorMap tmB;   // B codes [G * b_rows_per_group, K] u8, boxes 128 x 64 (GEMM 1) / 128 x 128
     CUtensorMap tmSA;  // A scale codes [rows, pitch] u8, boxes 16 x 128
     CUtensorMap tmSB;  // B scale codes, boxes 16 x 64 (GEMM 1) / 16 x 128
@@ -121,7 +124,11 @@ struct MxShape {
     static constexpr int THREADS = 64 + 32 * (NEPI + kMxSfWarps);
     static constexpr uint32_t SF_COL0 = NACC * BN;                // scale columns after them
     static constexpr uint32_t SF_COLS = 4 + BN / 32;              // per stage: A, then B
-    static constexpr int FIXED = STAGES * STAGE + kMxSfSlots * SF_SLOT;
+    // dgrad 2: per epilogue warp one staging block for each of its five
+    // outputs of 32 rows x 32 columns (dg, du, w h~ in bf16; dg, du codes)
+    static constexpr int EPI_WARP = 3 * 2048 + 2 * 1024;
+    static constexpr int EPI = MODE == MX_DGRAD2 ? NEPI * EPI_WARP : 0;
+    static constexpr int FIXED = STAGES * STAGE + kMxSfSlots * SF_SLOT + EPI;
     static_assert(SF_COL0 + SF_COLS * STAGES <= kMxTmemCols, "tensor memory columns");
     static_assert((4 * STAGES + 2 * kMxSfSlots + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
 };
@@ -174,6 +181,7 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sCodes = smem;                                   // STAGES x (A | B codes)
     uint8_t *sSf = smem + STAGES * SH::STAGE;                 // kMxSfSlots x (A | B scales)
+    uint8_t *sEpi = sSf + kMxSfSlots * SH::SF_SLOT;           // dgrad 2 staging (1 KB aligned)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SH::FIXED);
     uint64_t *empty = full + STAGES;      // the stage's MMAs are done (codes and scales free)
     uint64_t *sfready = empty + STAGES;   // the stage's scales are in tensor memory
@@ -215,6 +223,11 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         tma_prefetch_desc(&p.tmB);
         tma_prefetch_desc(&p.tmSA);
         tma_prefetch_desc(&p.tmSB);
+        if constexpr (MODE == MX_DGRAD2) {
+            tma_prefetch_desc(&p.tmO);
+            tma_prefetch_desc(&p.tmO2);
+            tma_prefetch_desc(&p.tmOQ);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_base_s, kMxTmemCols);
@@ -451,6 +464,9 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                 }
             } else if constexpr (MODE == MX_DGRAD2) {
                 constexpr int DC = BN / NPART;       // columns of dA of this warp
+                // warps whose 32 rows all exist use TMA stores; the others direct ones
+                const bool warp_full = q * 32 + 32 <= ti.rows_valid;
+                uint8_t *stg = sEpi + (size_t)(warp - 2) * SH::EPI_WARP;
                 float w = 1.0f;
                 if (valid && p.row_w && row < p.w_rows) w = p.row_w[row];
                 const float cl = p.clamp;
@@ -494,41 +510,68 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                             du[j] = (u >= -cl && u <= cl) ? dH * (a * sg) : 0.0f;
                             r[j] = __float_as_uint(w * ht);
                         }
-                        uint16_t *dgd = p.dgu + (size_t)row * 2 * p.I + col;
-                        uint16_t *hwd = p.hw + (size_t)row * p.I + col;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            st_global_v4(dgd + j, pack_bf16x2(dg[j], dg[j + 1]),
-                                         pack_bf16x2(dg[j + 2], dg[j + 3]),
-                                         pack_bf16x2(dg[j + 4], dg[j + 5]),
-                                         pack_bf16x2(dg[j + 6], dg[j + 7]));
-                            st_global_v4(dgd + p.I + j, pack_bf16x2(du[j], du[j + 1]),
-                                         pack_bf16x2(du[j + 2], du[j + 3]),
-                                         pack_bf16x2(du[j + 4], du[j + 5]),
-                                         pack_bf16x2(du[j + 6], du[j + 7]));
-                            st_global_v4(hwd + j,
-                                         pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                         pack_bf16x2(__uint_as_float(r[j + 2]),
-                                                     __uint_as_float(r[j + 3])),
-                                         pack_bf16x2(__uint_as_float(r[j + 4]),
-                                                     __uint_as_float(r[j + 5])),
-                                         pack_bf16x2(__uint_as_float(r[j + 6]),
-                                                     __uint_as_float(r[j + 7])));
+                        // five 32-column outputs of this thread's row, one at a time
+                        // (few live registers): dg and du quantised along 2I (each 32
+                        // columns one block), dg, du and w h~ in bf16.  A warp whose
+                        // 32 rows all exist stages each as a 32 x 32 block in shared
+                        // memory and writes it with one TMA store; a ragged warp must
+                        // not write past its group's rows and stores directly.
+                        const uint32_t b0 = smem_u32(stg);
+                        if (warp_full) {
+                            if (lane == 0) bulk_wait_group_read<0>();   // staging free again
+                            __syncwarp();
                         }
-                        // dG and dU quantised along 2I: each 32 columns are one block
-                        uint8_t *qd = p.dguq + (size_t)row * 2 * p.I + col;
                         uint8_t *sd = p.dgusf + (size_t)row * p.dgu_pitch;
-                        uint32_t wq[8];
-                        const uint32_t cg =
-                            mx_quantize_block(*reinterpret_cast<const float(*)[32]>(dg), wq);
-                        st_global_v4(qd, wq[0], wq[1], wq[2], wq[3]);
-                        st_global_v4(qd + 16, wq[4], wq[5], wq[6], wq[7]);
-                        sd[col / 32] = (uint8_t)cg;
-                        const uint32_t cu =
-                            mx_quantize_block(*reinterpret_cast<const float(*)[32]>(du), wq);
-                        st_global_v4(qd + p.I, wq[0], wq[1], wq[2], wq[3]);
-                        st_global_v4(qd + p.I + 16, wq[4], wq[5], wq[6], wq[7]);
-                        sd[(p.I + col) / 32] = (uint8_t)cu;
+                        auto emit_codes = [&](const float *v, int c, uint32_t soff) {
+                            uint32_t wq[8];
+                            sd[c / 32] = (uint8_t)mx_quantize_block(
+                                *reinterpret_cast<const float(*)[32]>(v), wq);
+                            if (warp_full) {
+                                const uint32_t a = b0 + soff + (uint32_t)lane * 32u;
+                                st_shared_v4(a, wq[0], wq[1], wq[2], wq[3]);
+                                st_shared_v4(a + 16u, wq[4], wq[5], wq[6], wq[7]);
+                            } else {
+                                uint8_t *qd = p.dguq + (size_t)row * 2 * p.I + c;
+                                st_global_v4(qd, wq[0], wq[1], wq[2], wq[3]);
+                                st_global_v4(qd + 16, wq[4], wq[5], wq[6], wq[7]);
+                            }
+                        };
+                        auto emit_bf16 = [&](const float *v, uint16_t *gdst, uint32_t soff) {
+                            const uint32_t sw2 = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                const uint32_t x0 = pack_bf16x2(v[8 * jj], v[8 * jj + 1]);
+                                const uint32_t x1 = pack_bf16x2(v[8 * jj + 2], v[8 * jj + 3]);
+                                const uint32_t x2 = pack_bf16x2(v[8 * jj + 4], v[8 * jj + 5]);
+                                const uint32_t x3 = pack_bf16x2(v[8 * jj + 6], v[8 * jj + 7]);
+                                if (warp_full)
+                                    st_shared_v4(b0 + soff + (uint32_t)lane * 64u +
+                                                     ((((uint32_t)jj) ^ sw2) << 4),
+                                                 x0, x1, x2, x3);
+                                else
+                                    st_global_v4(gdst + 8 * jj, x0, x1, x2, x3);
+                            }
+                        };
+                        emit_codes(dg, col, 6144u);
+                        emit_codes(du, p.I + col, 7168u);
+                        uint16_t *dgd = p.dgu + (size_t)row * 2 * p.I + col;
+                        emit_bf16(dg, dgd, 0u);
+                        emit_bf16(du, dgd + p.I, 2048u);
+                        emit_bf16(reinterpret_cast<const float *>(r), p.hw + (size_t)row * p.I + col,
+                                  4096u);
+                        if (warp_full) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int wrow = ti.row0 + q * 32;
+                                tma_store_2d(&p.tmO, stg, col, wrow);
+                                tma_store_2d(&p.tmO, stg + 2048, p.I + col, wrow);
+                                tma_store_2d(&p.tmO2, stg + 4096, col, wrow);
+                                tma_store_2d(&p.tmOQ, stg + 6144, col, wrow);
+                                tma_store_2d(&p.tmOQ, stg + 7168, p.I + col, wrow);
+                                bulk_commit_group();
+                            }
+                        }
                     }
                 }
                 // one partial of <h~, dA> per (row, column tile, warp part)
@@ -561,6 +604,8 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
         }
+        // the TMA stores must have left shared memory (and landed) before exit
+        if (MODE == MX_DGRAD2 && lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -671,7 +716,10 @@ moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32
     if (!encode_tmap_u8_2d(&p.tmA, dYq, d, max_rows, d, 128, 128, 128) ||
         !encode_tmap_u8_2d(&p.tmB, W2tq, d, brows, d, 128, BN, 128) ||
         !encode_tmap_u8_2d(&p.tmSA, dYsf, sfd, max_rows, sfd, 16, 128, 0) ||
-        !encode_tmap_u8_2d(&p.tmSB, W2tsf, sfd, brows, sfd, 16, BN, 0))
+        !encode_tmap_u8_2d(&p.tmSB, W2tsf, sfd, brows, sfd, 16, BN, 0) ||
+        !encode_tmap_bf16_2d_sw64(&p.tmO, dGU, 2 * I, max_rows, (uint64_t)4 * I, 32, 32) ||
+        !encode_tmap_bf16_2d_sw64(&p.tmO2, hw, I, max_rows, (uint64_t)2 * I, 32, 32) ||
+        !encode_tmap_u8_2d(&p.tmOQ, dGUq, 2 * I, max_rows, 2 * I, 32, 32, 0))
         return MOE_ERR_CUDA;
     p.offsets = offsets;
     p.G = G;
