@@ -60,3 +60,19 @@ def assert_close_rounded(got, ref, what, rel_fro=REL_FRO, max_abs=MAX_ABS, max_f
         (f"{what}: rel Frobenius {rel:.3e} (<= {rel_fro}), worst |diff| / max({max_abs}, one "
          f"bf16 step) {worst:.3f} (<= 1), elements beyond {max_abs}: {flips:.2e}")
     return rel, float(diff.max()) if diff.size else 0.0
+
+
+def assert_wgrad_bf16_bound(got, a, b, what):
+    """got ~ a^T b, where the GPU rounded b (w h~, or [dg | du]) to bf16 and
+    summed in fp32: each entry within 2^-8 sum_r |a_r b_r| of the fp64 sum
+    (round to nearest moves each term by at most 2^-9 of itself; the rest
+    covers the fp32 sums).  An entry may exceed it only where a clamp
+    decision sits within fp32 rounding of the bound (a few in 10^4)."""
+    want = a.T @ b
+    bound = 2.0 ** -8 * (np.abs(a).T @ np.abs(b)) + 1e-6 * float(np.abs(want).max())
+    g = np64(got)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    over = np.abs(g - want) > bound
+    rel = np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30)
+    assert rel <= 1e-2 and over.mean() <= 1e-4, \
+        f"{what}: rel Frobenius {rel:.3e}, entries beyond the rounding bound {over.mean():.2e}"

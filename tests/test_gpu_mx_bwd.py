@@ -22,7 +22,7 @@ import oracle
 from moe_expert_layer_04_gb300 import _lib
 from moe_expert_layer_04_gb300 import workloads as W
 from moe_expert_layer_04_gb300.layer import Dims, MoELayer
-from tests.helpers import MAX_ABS, assert_close, cpu, np64
+from tests.helpers import assert_close, assert_wgrad_bf16_bound, cpu, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -104,22 +104,6 @@ def _rows_meta(layer, w):
     return offs, rt, grp, rw
 
 
-def _assert_wgrad(got, a, b, what):
-    """got ~ a^T b, where the GPU rounded b (w h~, or [dg | du]) to bf16 and
-    summed in fp32: each entry within 2^-8 sum_r |a_r b_r| of the fp64 sum
-    (round to nearest moves each term by at most 2^-9 of itself; the rest
-    covers the fp32 sums).  An entry may exceed it only where a clamp
-    decision sits within fp32 rounding of the bound (a few in 10^4)."""
-    want = a.T @ b
-    bound = 2.0 ** -8 * (np.abs(a).T @ np.abs(b)) + 1e-6 * float(np.abs(want).max())
-    g = np64(got)
-    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
-    over = np.abs(g - want) > bound
-    rel = np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30)
-    assert rel <= 1e-2 and over.mean() <= 1e-4, \
-        f"{what}: rel Frobenius {rel:.3e}, entries beyond the rounding bound {over.mean():.2e}"
-
-
 def _check_expert_wgrads(w, inp, layer, experts):
     """dW2[e] against fp64 sums over the GPU's own MX h (its codes are checked
     against the oracle in the forward tests), dW13[e] against the oracle's
@@ -142,8 +126,8 @@ def _check_expert_wgrads(w, inp, layer, experts):
         h_gpu = oracle.mx_dequantize(cpu(layer.h_q[ridx]).numpy(),
                                      cpu(layer.h_sf[ridx]).numpy()[:, : w.I // 32])
         assert np.mean(np.abs(h_gpu - ref["h"]) > 0) <= 2e-3
-        _assert_wgrad(layer.dW2[e], dyr, rw[rows, None] * h_gpu, f"{w.name} dW2[{e}]")
-        _assert_wgrad(layer.dW13[e].t(), xr, ref["dgu"], f"{w.name} dW13[{e}]")
+        assert_wgrad_bf16_bound(layer.dW2[e], dyr, rw[rows, None] * h_gpu, f"{w.name} dW2[{e}]")
+        assert_wgrad_bf16_bound(layer.dW13[e].t(), xr, ref["dgu"], f"{w.name} dW13[{e}]")
 
 
 # name, T, d, E, k, I, experts forced empty, recompute, tokens checked (None: all)
