@@ -30,11 +30,13 @@
 // tiles of the same group and column tile; CTA r loads its own 128 rows of A
 // and half of the B tile (columns [r BN/2, (r+1) BN/2)) with plain TMA
 // copies, so each CTA reads half the B bytes per MMA that a lone CTA does and
-// more operand stages fit.  The even CTA issues the MMAs once both CTAs'
-// stages are full (the odd CTA's MMA warp forwards its stage's completion
-// through a cluster-scope arrive) and releases stages and accumulators to
+// more operand stages fit.  The odd CTA's copies complete on the even CTA's
+// barrier of the stage (cta_group::2 TMA), so the even CTA issues the MMAs
+// once both CTAs' halves have landed, and releases stages and accumulators to
 // both CTAs with one commit; every epilogue warp of the pair hands its drained
-// accumulator back to the even CTA.
+// accumulator back to the even CTA.  In a ragged contraction's last stage the
+// even CTA also zeroes the rows past the group's end in the odd CTA's A,
+// through distributed shared memory, before its MMAs.
 //
 // Every wait is bounded (moe_ptx.cuh): on a timeout the CTA records
 // MOE_ERR_TIMEOUT, drains its own TMA copies and MMAs, frees TMEM and exits.
@@ -297,10 +299,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                   "the pair form: row- or K-grouped modes, 64-column B boxes per CTA");
     using TS = TileShape<BN, MODE, CL>;
     constexpr int STAGES = TS::STAGES;
-    // the barrier block (full/empty/pfull per stage, two tfull, two tempty,
-    // done, the TMEM base and the abort flag) must fit the 256 bytes the
-    // layout reserves
-    static_assert((3 * STAGES + 5) * 8 + 8 <= 256, "too many operand stages for the barrier block");
+    // the barrier block (full/empty per stage, two tfull, two tempty, done,
+    // the TMEM base and the abort flag) must fit the 256 bytes the layout
+    // reserves
+    static_assert((2 * STAGES + 5) * 8 + 8 <= 256, "too many operand stages for the barrier block");
     constexpr uint32_t IDESC = idesc_bf16_f32(128 * CL, BN, MT::A_MN, MT::B_MN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -316,8 +318,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
-    uint64_t *pfull = done + 1;   // CL = 2, even CTA: the odd CTA's stage is full
-    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(pfull + STAGES);
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
     int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256);
     int *mt_start = offs + (p.G + 1);
@@ -329,7 +330,6 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&pfull[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -431,18 +431,15 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 }
                 for (int kb = 0; kb < ti.kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
-                    // CL = 2: the even CTA's barrier takes both CTAs' halves of a
-                    // stage, except a ragged-contraction tail stage, whose halves
-                    // each CTA completes on its own barrier (each zeroes its rows
-                    // past the group's end before the pair's MMA reads them)
-                    const bool tail = MT::KGROUP && ti.krows - kb * 64 < 64;
-                    const bool to_even = CL == 2 && rank == 1 && !tail;
+                    // CL = 2: the even CTA's barrier takes both CTAs' halves of
+                    // every stage (the even CTA zeroes the rows of a ragged
+                    // contraction's tail stage in both CTAs before its MMAs)
+                    const bool to_even = CL == 2 && rank == 1;
                     uint32_t bar_even = 0;
                     if (to_even)
                         bar_even = dsmem_map(&full[s], 0);
                     else
-                        mbar_arrive_expect_tx(
-                            &full[s], (CL == 2 && !tail ? 2 : 1) * (uint32_t)TS::STAGE_BYTES);
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(CL * TS::STAGE_BYTES));
                     auto load = [&](void *dst, const CUtensorMap *tm, int c0, int c1) {
                         if (to_even) tma_load_2d_pairbar(dst, tm, bar_even, c0, c1);
                         else tma_load_2d(dst, tm, &full[s], c0, c1);
@@ -529,21 +526,21 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        // CL = 2: the even CTA issues the pair's MMAs.  The odd CTA's warp only
-        // takes part in the ragged-contraction tail stages: it zeroes its own A
-        // rows past the group's end and then tells the even CTA (pfull).
+        // CL = 2: the even CTA issues the pair's MMAs (the odd CTA's warp only
+        // keeps its stage count).
         const bool issuer = CL == 1 || rank == 0;
         uint32_t s = 0, ph = 0;
-        uint32_t tail_ph = 0;   // bit s: parity of stage s's next tail handshake
         int it = 0;
         bool ok = true;
         bool issued = false;
         // ragged contraction: only the 16-row MMA steps that hold rows of this
         // group run; inside the last one, rows past the group's end (the next
         // group's rows) are zeroed in A.  B's rows there are finite data or TMA
-        // zero fill, so they add nothing.  In a pair each CTA zeroes its own A
-        // rows, which are the only A rows its output rows read.  Returns the
-        // number of 16-row steps.
+        // zero fill, so they add nothing.  In a pair the even CTA zeroes them in
+        // both CTAs' A (each CTA's output rows read only its own A).  A first
+        // form had each CTA zero its own rows and the odd CTA signal the even
+        // one through a barrier: about 2000 cycles per tail stage, most of it
+        // in that handshake.  Returns the number of 16-row steps.
         auto zero_tail = [&](int valid) {
             const int n_kk = (valid + 15) >> 4;
             const int nrows = n_kk * 16 - valid;  // 0..15
@@ -553,8 +550,14 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 uint8_t *dst = sA + s * TS::A_BYTES + box * 8192 + (valid + (rem >> 3)) * 128 +
                                (rem & 7) * 16;
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                // a pair's odd CTA: the same rows of its own A, through
+                // distributed shared memory
+                if constexpr (CL == 2) st_cluster_v4(dsmem_map(dst, 1), 0u, 0u, 0u, 0u);
             }
-            if (nrows > 0) fence_proxy_async_smem();
+            if (nrows > 0) {
+                if constexpr (CL == 2) fence_proxy_async_cluster();
+                else fence_proxy_async_smem();
+            }
             __syncwarp();
             return n_kk;
         };
@@ -574,14 +577,6 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 const bool tail = valid < 64;
                 if constexpr (CL == 2) {
                     if (rank == 1) {
-                        if (tail) {
-                            // this CTA's half of the tail stage landed on its own barrier
-                            if (!mbar_wait(&full[s], (tail_ph >> s) & 1u, wc)) { ok = false; break; }
-                            zero_tail(valid);
-                            if (lane == 0) mbar_arrive_remote(dsmem_map(&pfull[s], 0));
-                            __syncwarp();
-                            tail_ph ^= 1u << s;
-                        }
                         if (++s == STAGES) { s = 0; ph ^= 1u; }
                         continue;
                     }
@@ -594,17 +589,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 if constexpr (MT::KGROUP) {
                     if (tail) n_kk = zero_tail(valid);
                 }
-                if constexpr (CL == 2) {
-                    if (tail) {
-                        // the odd CTA has zeroed its rows of the tail stage too
-                        if (!mbar_wait_cluster(&pfull[s], (tail_ph >> s) & 1u, wc)) {
-                            ok = false;
-                            break;
-                        }
-                        tail_ph ^= 1u << s;
-                        tc_fence_after();
-                    }
-                }
+
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
