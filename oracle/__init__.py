@@ -93,6 +93,8 @@ def _load():
                 "orc_expert_rows_mx": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _D, _P, _P], None),
                 "orc_expert_rows_mx_backward": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _D,
                                                  _P, _P, _P, _P], None),
+                "orc_mx_rows_matmul": ([_P, _P, _I, _I, _I, _P], None),
+                "orc_expert_wgrad_mx": ([_P, _P, _P, _P, _I, _P, _P, _I, _I, _D, _P, _P], None),
                 "orc_layer_backward_mx": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
                                            _I, _P, _I, _I, _I, _I, _D, _D, _P, _P, _P], None),
             }
@@ -477,4 +479,36 @@ def layer_backward_mx(x, W_g, W13, W2, dY, bias, k, rho, clamp, is_vision=None, 
                                   _ptr(tk), d, E, k, I, float(rho), float(clamp), _ptr(dX),
                                   _ptr(dz), _ptr(dw))
     return dict(dX=dX, dz=dz, dw=dw)
+
+
+def mx_rows_matmul(A, B):
+    """A^T B (A [K, M], B [K, N], float64) with both operands MX-quantised
+    along their rows in blocks of 32 from row 0 (the last block zero-padded):
+    float64 [M, N]."""
+    a = np.ascontiguousarray(np.asarray(A, dtype=np.float64))
+    b = np.ascontiguousarray(np.asarray(B, dtype=np.float64))
+    K, M = a.shape
+    assert b.shape[0] == K
+    N = b.shape[1]
+    out = np.empty((M, N), np.float64)
+    _load().orc_mx_rows_matmul(_ptr(a), _ptr(b), K, M, N, _ptr(out))
+    return out
+
+
+def expert_wgrad_mx(x, W13e, W2e, dY, row_tok, row_w, clamp):
+    """Weight gradients of one expert in the MX training form over its rows in
+    the given order (bf16 inputs; W13e [2I, d], W2e [d, I] that expert's
+    weights): dict(dW13 [2I, d], dW2 [d, I])."""
+    (xn, w13, w2, dy), bf = _floats(x, W13e, W2e, dY)
+    assert bf == 1, "the MX oracle takes bf16 inputs"
+    d = xn.shape[1]
+    I = w2.shape[-1]
+    rt = np.ascontiguousarray(_to_np(row_tok), dtype=np.int64)
+    rw = _opt(row_w, np.float64)
+    n = rt.shape[0]
+    dW13 = np.empty((2 * I, d), np.float64)
+    dW2 = np.empty((d, I), np.float64)
+    _load().orc_expert_wgrad_mx(_ptr(xn), _ptr(w13), _ptr(w2), _ptr(dy), n, _ptr(rt), _ptr(rw),
+                                d, I, float(clamp), _ptr(dW13), _ptr(dW2))
+    return dict(dW13=dW13, dW2=dW2)
 

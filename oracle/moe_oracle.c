@@ -1043,3 +1043,89 @@ void orc_layer_backward_mx(const uint16_t *x, const uint16_t *Wg, const uint16_t
     free(z); free(ids); free(w); free(ssel); free(margin);
     free(rt); free(re); free(rw); free(dwr); free(dgu); free(hq); free(dxr);
 }
+
+/* A^T B with both operands MX-quantised along their rows (the contraction):
+ * A [K, M] and B [K, N] (doubles, row-major); rows are taken in blocks of 32
+ * from row 0, the last block zero-padded; every column of a block is one MX
+ * block (one scale), in A and in B alike.  out [M, N] = sum over blocks of
+ * q(A_block)^T q(B_block), accumulated in fp64.  This is the weight-gradient
+ * matmul of the MX training form, where the contraction runs over an
+ * expert's token rows. */
+void orc_mx_rows_matmul(const double *A, const double *B, int K, int M, int N, double *out)
+{
+    for (size_t i = 0; i < (size_t)M * N; ++i) out[i] = 0.0;
+    const int nb = (K + 31) / 32;
+    double *qa = (double *)malloc(sizeof(double) * (size_t)32 * M);
+    double *qb = (double *)malloc(sizeof(double) * (size_t)32 * N);
+    for (int b = 0; b < nb; ++b) {
+#pragma omp parallel
+        {
+            double col[32], dq[32];
+            uint8_t q[32], sf[1];
+#pragma omp for schedule(static)
+            for (int m = 0; m < M; ++m) {
+                for (int j = 0; j < 32; ++j) {
+                    const int r = 32 * b + j;
+                    col[j] = r < K ? A[(size_t)r * M + m] : 0.0;
+                }
+                mx_quantize_row(col, 32, q, sf, dq);
+                for (int j = 0; j < 32; ++j) qa[(size_t)j * M + m] = dq[j];
+            }
+#pragma omp for schedule(static)
+            for (int n = 0; n < N; ++n) {
+                for (int j = 0; j < 32; ++j) {
+                    const int r = 32 * b + j;
+                    col[j] = r < K ? B[(size_t)r * N + n] : 0.0;
+                }
+                mx_quantize_row(col, 32, q, sf, dq);
+                for (int j = 0; j < 32; ++j) qb[(size_t)j * N + n] = dq[j];
+            }
+#pragma omp for schedule(static)
+            for (int m = 0; m < M; ++m) {
+                double *o = out + (size_t)m * N;
+                for (int j = 0; j < 32; ++j) {
+                    const double a = qa[(size_t)j * M + m];
+                    if (a == 0.0) continue;
+                    const double *bq = qb + (size_t)j * N;
+                    for (int n = 0; n < N; ++n) o[n] += a * bq[n];
+                }
+            }
+        }
+    }
+    free(qa);
+    free(qb);
+}
+
+/* Weight gradients of one expert in the MX training form, over its rows in
+ * the given order (the permuted order of its group): with h~, [dg|du] and
+ * the routing weights w of orc_expert_rows_mx_backward,
+ *   dW2  [d, I]  = mx_rows_matmul(dY rows, w h~)
+ *   dW13 [2I, d] = mx_rows_matmul([dg|du], x rows)
+ * W13 [2I, d] and W2 [d, I] are the expert's weights (bf16). */
+void orc_expert_wgrad_mx(const uint16_t *x, const uint16_t *W13, const uint16_t *W2,
+                         const uint16_t *dY, int n, const int64_t *row_tok, const double *row_w,
+                         int d, int I, double c, double *dW13, double *dW2)
+{
+    const int K2 = 2 * I;
+    int32_t *re = (int32_t *)calloc((size_t)(n > 0 ? n : 1), sizeof(int32_t));
+    double *dw = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double *dgu = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * K2);
+    double *h = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * I);
+    double *dx = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    double *xr = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    double *dyr = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    if (n > 0)
+        orc_expert_rows_mx_backward(x, W13, W2, dY, n, row_tok, re, row_w, d, I, c, dw, dgu, h,
+                                    dx);
+    for (int r = 0; r < n; ++r) {
+        const double w = row_w ? row_w[r] : 1.0;
+        for (int i = 0; i < I; ++i) h[(size_t)r * I + i] *= w;   /* w h~ */
+        for (int m = 0; m < d; ++m) {
+            xr[(size_t)r * d + m] = bf16_to_f64(x[(size_t)row_tok[r] * d + m]);
+            dyr[(size_t)r * d + m] = bf16_to_f64(dY[(size_t)row_tok[r] * d + m]);
+        }
+    }
+    orc_mx_rows_matmul(dyr, h, n, d, I, dW2);
+    orc_mx_rows_matmul(dgu, xr, n, K2, d, dW13);
+    free(re); free(dw); free(dgu); free(h); free(dx); free(xr); free(dyr);
+}

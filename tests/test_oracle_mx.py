@@ -336,3 +336,72 @@ def test_mx_layer_backward_logit_gradient_by_finite_differences():
         assert np.array_equal(idp, ids0) and np.array_equal(idm, ids0)
         fd = ((wp - wm) / (2 * eps) * out["dw"]).sum(1)
         np.testing.assert_allclose(out["dz"][:, m], fd, rtol=1e-5, atol=1e-8)
+
+
+# ----------------------------------------- MX weight gradients (rows)
+
+
+def _grid(rng, shape):
+    # powers of two in [1/2, 2] and zeros: every block of 32, along any axis,
+    # is on the MX grid, so its quantisation is the identity
+    return rng.choice([0.0, 0.5, 1.0, 2.0, -0.5, -1.0, -2.0], size=shape)
+
+
+@pytest.mark.parametrize("K", [32, 70, 5])
+def test_mx_rows_matmul_on_grid_is_the_matmul(K):
+    rng = np.random.default_rng(K)
+    A, B = _grid(rng, (K, 40)), _grid(rng, (K, 24))
+    np.testing.assert_array_equal(oracle.mx_rows_matmul(A, B), A.T @ B)
+
+
+def test_mx_rows_matmul_error_bound():
+    # each operand element moves by at most 2^-4 of itself (E4M3 rounding of
+    # a normal value) plus half the subnormal quantum of its block, 2^-10 X
+    # with X <= 2^-8 of the block's largest magnitude
+    rng = np.random.default_rng(7)
+    K, M, N = 100, 48, 40
+    A = rng.standard_normal((K, M)) * np.exp(rng.standard_normal((K, 1)))
+    B = rng.standard_normal((K, N)) * np.exp(rng.standard_normal((1, N)))
+    out = oracle.mx_rows_matmul(A, B)
+    exact = A.T @ B
+    ea = 2.0 ** -4 * np.abs(A) + 2.0 ** -18 * np.abs(A).max()
+    eb = 2.0 ** -4 * np.abs(B) + 2.0 ** -18 * np.abs(B).max()
+    bound = ea.T @ np.abs(B) + np.abs(A).T @ eb + ea.T @ eb
+    assert np.all(np.abs(out - exact) <= bound * (1 + 1e-12))
+    assert np.linalg.norm(out - exact) < 0.05 * np.linalg.norm(exact)
+    # quantising along the columns instead (a plausible mistake) differs
+    qa = oracle.mx_dequantize(*oracle.mx_quantize(A[:, :32].copy()))
+    qb = oracle.mx_dequantize(*oracle.mx_quantize(B[:, :32].copy()))
+    assert np.abs(qa.T @ qb - out[:32, :32]).max() > 1e-6 * np.abs(out).max()
+
+
+def test_mx_rows_matmul_blocks_start_at_row_zero():
+    rng = np.random.default_rng(9)
+    A, B = rng.standard_normal((96, 16)), rng.standard_normal((96, 8))
+    # independent blocks of 32 rows from row 0
+    parts = sum(oracle.mx_rows_matmul(A[i:i + 32], B[i:i + 32]) for i in (0, 32, 64))
+    np.testing.assert_allclose(oracle.mx_rows_matmul(A, B), parts, rtol=1e-12, atol=1e-12)
+    # moving the rows across block boundaries (a plausible alignment mistake:
+    # blocks counted from a global row, not the group's first) changes it
+    Z = np.zeros((5, 16)), np.zeros((5, 8))
+    shifted = oracle.mx_rows_matmul(np.vstack([Z[0], A]), np.vstack([Z[1], B]))
+    assert np.abs(shifted - oracle.mx_rows_matmul(A, B)).max() > 1e-6
+
+
+def test_expert_wgrad_mx_assembles_the_rows():
+    # dW2 = rows-MX(dY rows, w h~) and dW13 = rows-MX([dg|du], x rows), with
+    # h~ and [dg|du] the MX backward's, and both near the exact gradients
+    x, dY, W13, W2, rt, re, rw = _bwd_case(grid=False, seed=13)
+    e = 1
+    sel = re == e
+    rt_e, rw_e = rt[sel], rw[sel]
+    out = oracle.expert_wgrad_mx(x, W13[e], W2[e], dY, rt_e, rw_e, 7.0)
+    rows = oracle.expert_rows_mx_backward(x, W13[e:e + 1], W2[e:e + 1], dY, rt_e,
+                                          np.zeros(len(rt_e), np.int32), rw_e, 7.0)
+    xr, dyr = x.double().numpy()[rt_e], dY.double().numpy()[rt_e]
+    np.testing.assert_array_equal(out["dW2"], oracle.mx_rows_matmul(dyr, rw_e[:, None] * rows["h"]))
+    np.testing.assert_array_equal(out["dW13"], oracle.mx_rows_matmul(rows["dgu"], xr))
+    ex = oracle.expert_wgrad(x, W13, W2, dY, e, rt_e, rw_e, 7.0, exact=True)
+    for k in ("dW2", "dW13"):
+        rel = np.linalg.norm(out[k] - ex[k]) / np.linalg.norm(ex[k])
+        assert 1e-3 < rel < 0.15, (k, rel)
