@@ -1099,9 +1099,12 @@ void orc_mx_rows_matmul(const double *A, const double *B, int K, int M, int N, d
 /* Weight gradients of one expert in the MX training form, over its rows in
  * the given order (the permuted order of its group): with h~, [dg|du] and
  * the routing weights w of orc_expert_rows_mx_backward,
- *   dW2  [d, I]  = mx_rows_matmul(dY rows, w h~)
- *   dW13 [2I, d] = mx_rows_matmul([dg|du], x rows)
- * W13 [2I, d] and W2 [d, I] are the expert's weights (bf16). */
+ *   dW2  [d, I]  = mx_rows_matmul(dY rows, bf16(w h~))
+ *   dW13 [2I, d] = mx_rows_matmul(bf16([dg|du]), x rows)
+ * w h~ and [dg|du] are stored in bf16 before their quantisation, the
+ * interface rounding point of the layer's weight-gradient operands (as in
+ * orc_expert_wgrad's store_bf16 mode).  W13 [2I, d] and W2 [d, I] are the
+ * expert's weights (bf16). */
 void orc_expert_wgrad_mx(const uint16_t *x, const uint16_t *W13, const uint16_t *W2,
                          const uint16_t *dY, int n, const int64_t *row_tok, const double *row_w,
                          int d, int I, double c, double *dW13, double *dW2)
@@ -1119,7 +1122,8 @@ void orc_expert_wgrad_mx(const uint16_t *x, const uint16_t *W13, const uint16_t 
                                     dx);
     for (int r = 0; r < n; ++r) {
         const double w = row_w ? row_w[r] : 1.0;
-        for (int i = 0; i < I; ++i) h[(size_t)r * I + i] *= w;   /* w h~ */
+        for (int i = 0; i < I; ++i) h[(size_t)r * I + i] = rbf16(w * h[(size_t)r * I + i]);
+        for (int j = 0; j < K2; ++j) dgu[(size_t)r * K2 + j] = rbf16(dgu[(size_t)r * K2 + j]);
         for (int m = 0; m < d; ++m) {
             xr[(size_t)r * d + m] = bf16_to_f64(x[(size_t)row_tok[r] * d + m]);
             dyr[(size_t)r * d + m] = bf16_to_f64(dY[(size_t)row_tok[r] * d + m]);

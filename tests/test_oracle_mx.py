@@ -388,9 +388,15 @@ def test_mx_rows_matmul_blocks_start_at_row_zero():
     assert np.abs(shifted - oracle.mx_rows_matmul(A, B)).max() > 1e-6
 
 
+def _round_bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).double().numpy()
+
+
 def test_expert_wgrad_mx_assembles_the_rows():
-    # dW2 = rows-MX(dY rows, w h~) and dW13 = rows-MX([dg|du], x rows), with
-    # h~ and [dg|du] the MX backward's, and both near the exact gradients
+    # dW2 = rows-MX(dY rows, bf16(w h~)) and dW13 = rows-MX(bf16([dg|du]), x
+    # rows), with h~ and [dg|du] the MX backward's (stored in bf16 like the
+    # bf16 layer's weight-gradient operands; torch's cast is the rounding
+    # routine), and both near the exact gradients
     x, dY, W13, W2, rt, re, rw = _bwd_case(grid=False, seed=13)
     e = 1
     sel = re == e
@@ -399,8 +405,9 @@ def test_expert_wgrad_mx_assembles_the_rows():
     rows = oracle.expert_rows_mx_backward(x, W13[e:e + 1], W2[e:e + 1], dY, rt_e,
                                           np.zeros(len(rt_e), np.int32), rw_e, 7.0)
     xr, dyr = x.double().numpy()[rt_e], dY.double().numpy()[rt_e]
-    np.testing.assert_array_equal(out["dW2"], oracle.mx_rows_matmul(dyr, rw_e[:, None] * rows["h"]))
-    np.testing.assert_array_equal(out["dW13"], oracle.mx_rows_matmul(rows["dgu"], xr))
+    np.testing.assert_array_equal(out["dW2"],
+                                  oracle.mx_rows_matmul(dyr, _round_bf16(rw_e[:, None] * rows["h"])))
+    np.testing.assert_array_equal(out["dW13"], oracle.mx_rows_matmul(_round_bf16(rows["dgu"]), xr))
     ex = oracle.expert_wgrad(x, W13, W2, dY, e, rt_e, rw_e, 7.0, exact=True)
     for k in ("dW2", "dW13"):
         rel = np.linalg.norm(out[k] - ex[k]) / np.linalg.norm(ex[k])
