@@ -519,7 +519,7 @@ def run_mx_only(args):
 MX_STEP_CALLS = ["quantize_weights", "route", "dispatch", "expert_gemm1", "expert_gemm2",
                  "combine"]
 MX_MATMUL_STAGES = {"expert_gemm1", "expert_gemm2", "bwd_recompute_gemm1", "bwd_dgrad2",
-                    "bwd_dgrad1"}
+                    "bwd_dgrad1", "bwd_wgrad2", "bwd_wgrad1"}
 
 
 def mx_step_work(D, counts):
@@ -540,12 +540,15 @@ def mx_step_work(D, counts):
     bwd = {
         "recompute_gather": (0, T * d * 2 + R * d * 2),
         "recompute_gemm1": (4 * R * d * I, used * 2 * I * d + R * d + R * 2 * I * 4 + R * I),
-        "gather_dY": (0, 2 * T * d * 2 + R * d * 2 + R * d + sc(R * d)),
+        "gather_dY": (0, T * d * 2 + R * d + sc(R * d)),
         "dgrad2": (2 * R * d * I, used * d * I + R * d + R * 2 * I * 4 + R * I
                    + R * 2 * I * 2 + R * 2 * I + R * I * 2),
-        "wgrad2": (2 * R * d * I, G * d * I * 4 + R * d * 2 + R * I * 2),
+        # the operands quantised along the rows (read bf16, write codes, read
+        # the codes back in the matmul), then fp32 dW2
+        "wgrad2": (2 * R * d * I, T * d * 2 + R * I * 2 + 2 * (d + I) * R + G * d * I * 4),
         "dgrad1": (4 * R * I * d, used * 2 * I * d + R * 2 * I + R * d * 2),
-        "wgrad1": (4 * R * I * d, G * 2 * I * d * 4 + R * 2 * I * 2 + R * d * 2),
+        "wgrad1": (4 * R * I * d, R * 2 * I * 2 + R * d * 2 + 2 * (2 * I + d) * R
+                   + G * 2 * I * d * 4),
         "router_bwd": (0, S * 4 * 6 + T * E * 4),
         "dX": (2 * S * d, R * d * 2 + T * d * 2 + S * 8),
         "dW_g": (2 * S * d, S * d * 2 + E * d * 4),
@@ -557,7 +560,7 @@ def run_mx_fwd_bwd(args, weights, dev, world, hbm, bf16_sus, wl=None):
     """One MXFP8 training step of the workload (the headline's by default):
     the expert weights quantised from bf16 (both orientations, as after an
     optimizer update), the forward with MX expert matmuls and the MX backward
-    (dgrad matmuls on MX operands, bf16 weight gradients), CUDA events around
+    (dgrad and weight-gradient matmuls on MX operands), CUDA events around
     each call and backward stage."""
     from moe_expert_layer_04_gb300 import _lib
     from moe_expert_layer_04_gb300 import workloads as W
@@ -635,8 +638,8 @@ def run_mx_fwd_bwd(args, weights, dev, world, hbm, bf16_sus, wl=None):
                        + (", recompute" if wl.recompute else ""),
            "value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
            "ms_per_step": round(ms, 4), "steps": K,
-           "dtype": "mxfp8 matmul operands (e4m3 + e8m0 per 32) in the forward and both dgrad "
-                    "matmuls, bf16 weight gradients, fp32 accumulate",
+           "dtype": "mxfp8 operands (e4m3 + e8m0 per 32) in every matmul of the step, "
+                    "fp32 accumulate, fp32 weight gradients",
            "peak_note": "MX matmul stages against 2x the measured sustained bf16 peak",
            "kernels": kernels}
     del layer, inp

@@ -531,15 +531,16 @@ moe_status moe_mx_quantize_both(const uint16_t *src, int G, int R, int C, uint8_
  *   dH = w dA;  [dg|du][r] = clamped-SwiGLU backward as in moe_backward, from
  *                                     the forward's fp32 g|u
  *   dX_perm[r] = bf16( MX([dg|du][r]) (W13^T)~[g]^T )   along 2I
- *   dW2[g]  = sum_r dY_perm[r]^T bf16(w h~[r])            (bf16 operands,
- *   dW13[g] = sum_r bf16([dg|du][r])^T x_perm[r]           fp32 sums)
- * The weight gradients are bf16 matmuls of the same rows (the MX recipe
- * leaves them open; these keep the bf16 layer's weight-gradient arithmetic).
+ *   dW2[g]  = sum_r MXr(dY_perm)[r]^T MXr(bf16(w h~))[r]
+ *   dW13[g] = sum_r MXr(bf16([dg|du]))[r]^T MXr(x_perm)[r]
+ * MXr: quantised along the group's rows, in blocks of 32 rows from the
+ * group's first row (the last block zero-padded), every column of a block one
+ * MX block; w h~ and [dg|du] are stored in bf16 first (fp32 sums).
  * gu_save = NULL recomputes g|u and h~ with MX GEMM 1 into the workspace
  * (then x_perm_q/sf and W13_q/sf are read, h_q/h_sf are not); otherwise the
  * forward's gu_save and h_q/h_sf are read.  Needs d % 256 == 0 and
  * I % 128 == 0 (else MOE_ERR_UNSUPPORTED).  Workspace:
- * moe_expert_bwd_mx_workspace_size(max_rows, d, I, gu_save == NULL). */
+ * moe_expert_bwd_mx_workspace_size(G, max_rows, d, I, gu_save == NULL). */
 typedef struct {
     int G, max_rows, S, d, I;
     float clamp;
@@ -567,14 +568,14 @@ typedef struct {
     void *ws;
     size_t ws_bytes;
 } moe_expert_bwd_mx_args;
-size_t moe_expert_bwd_mx_workspace_size(int max_rows, int d, int I, int recompute);
+size_t moe_expert_bwd_mx_workspace_size(int G, int max_rows, int d, int I, int recompute);
 moe_status moe_expert_ffn_backward_mx(const moe_expert_bwd_mx_args *args, void *stream);
 
 /* Backward of the whole layer with the MX expert matmuls: moe_backward with
- * the expert part of moe_expert_ffn_backward_mx (dY gathered twice: bf16 for
- * dW2, MX along d for dgrad 2) and the same routing and combine chain.  The
- * bf16 x_perm (dW13, dW_g) is gathered from x; the stages and their events
- * are those of moe_backward.  Workspace:
+ * the expert part of moe_expert_ffn_backward_mx (dY gathered into MX rows
+ * for dgrad 2; dW2's operand reads dY's rows through row_token) and the same
+ * routing and combine chain.  The bf16 x_perm (dW13, dW_g) is gathered from
+ * x; the stages and their events are those of moe_backward.  Workspace:
  * moe_backward_mx_workspace_size(T, d, E, k, I, gu_save == NULL). */
 typedef struct {
     int T, d, E, k, I;
@@ -592,6 +593,7 @@ typedef struct {
     const float *scores_sel;      /* [T,k] */
     const float *row_weight;      /* [S] */
     const int32_t *offsets;       /* [E+2] */
+    const int32_t *row_token;     /* [S+T] */
     const int32_t *slot_row;      /* [S] */
     const uint8_t *x_perm_q;      /* [S+T,d] (moe_mx_gather; recompute only) */
     const uint8_t *x_perm_sf;

@@ -155,8 +155,8 @@ class BwdMxArgs(ctypes.Structure):
                 ("x", _P), ("W_g", _P), ("W13_q", _P), ("W13_sf", _P), ("W2t_q", _P),
                 ("W2t_sf", _P), ("W13t_q", _P), ("W13t_sf", _P),
                 ("ids", _P), ("weights", _P), ("scores_sel", _P), ("row_weight", _P),
-                ("offsets", _P), ("slot_row", _P), ("x_perm_q", _P), ("x_perm_sf", _P),
-                ("gu_save", _P), ("h_q", _P), ("h_sf", _P), ("dY", _P),
+                ("offsets", _P), ("row_token", _P), ("slot_row", _P), ("x_perm_q", _P),
+                ("x_perm_sf", _P), ("gu_save", _P), ("h_q", _P), ("h_sf", _P), ("dY", _P),
                 ("dX", _P), ("dW_g", _P), ("dW13", _P), ("dW2", _P),
                 ("dlogits", _P), ("dweights", _P), ("ws", _P), ("ws_bytes", _Z),
                 ("stage_events", ctypes.POINTER(_P))]
@@ -204,7 +204,7 @@ _SIGS = {
     "moe_expert_gemm1_mx": ([_P, _P, _P, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P, _P], _I),
     "moe_mx_quantize_t": ([_P, _I, _I, _I, _P, _P, _P], _I),
     "moe_mx_quantize_both": ([_P, _I, _I, _I, _P, _P, _P, _P, _P], _I),
-    "moe_expert_bwd_mx_workspace_size": ([_I, _I, _I, _I], _Z),
+    "moe_expert_bwd_mx_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "moe_expert_ffn_backward_mx": ([ctypes.POINTER(ExpertBwdMxArgs), _P], _I),
     "moe_backward_mx_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
     "moe_backward_mx": ([ctypes.POINTER(BwdMxArgs), _P], _I),
@@ -421,8 +421,8 @@ def moe_mx_quantize_both(src, G, R, C, q, sf, qt, sft, stream=None):
     _check("moe_mx_quantize_both", st)
 
 
-def moe_expert_bwd_mx_workspace_size(max_rows, d, I, recompute) -> int:
-    return int(load().moe_expert_bwd_mx_workspace_size(max_rows, d, I, int(bool(recompute))))
+def moe_expert_bwd_mx_workspace_size(G, max_rows, d, I, recompute) -> int:
+    return int(load().moe_expert_bwd_mx_workspace_size(G, max_rows, d, I, int(bool(recompute))))
 
 
 def moe_backward_mx_workspace_size(T, d, E, k, I, recompute) -> int:
@@ -433,7 +433,8 @@ _MX_BWD_TYPES = dict(offsets=I32, x_perm=BF16, x_perm_q=U8, x_perm_sf=U8, W13_q=
                      gu_save=F32, h_q=U8, h_sf=U8, W2t_q=U8, W2t_sf=U8, W13t_q=U8, W13t_sf=U8,
                      row_weight=F32, dY_perm=BF16, dY_perm_q=U8, dY_perm_sf=U8, dX_perm=BF16,
                      dw_rows=F32, dW13=F32, dW2=F32, ws=U8, x=BF16, W_g=BF16, ids=I32,
-                     weights=F32, scores_sel=F32, slot_row=I32, dY=BF16, dX=BF16, dW_g=F32,
+                     weights=F32, scores_sel=F32, slot_row=I32, row_token=I32, dY=BF16,
+                     dX=BF16, dW_g=F32,
                      dlogits=F32, dweights=F32)
 
 

@@ -136,14 +136,21 @@ struct MxBwdWorkspace {
     uint8_t *dGUq, *dGUsf;
     float *dw_part, *gu;
     uint8_t *hq, *hsf;
-    uint16_t *x_perm, *dY_perm, *dX_perm;
+    uint16_t *x_perm, *dX_perm;
     uint8_t *dYq, *dYsf;
+    // the weight gradients' operands, quantised along each group's rows and
+    // stored transposed, K-chunk-major (k_chunks chunks of 128 codes and
+    // sf_slots 16-byte scale slots per column), and the groups' padded
+    // contraction plan
+    int32_t *kofs, *sofs;
+    uint8_t *dYt, *dYtsf, *hwt, *hwtsf, *dGUt, *dGUtsf, *xt, *xtsf;
+    int k_chunks, sf_slots;
     RouterBwdWorkspace router;
     size_t bytes;
 };
 
-MxBwdWorkspace carve_mx_bwd(uint8_t *base, int R, int d, int I, bool recompute, bool layer, int T,
-                            int E, int k) {
+MxBwdWorkspace carve_mx_bwd(uint8_t *base, int G, int R, int d, int I, bool recompute, bool layer,
+                            int T, int E, int k) {
     MxBwdWorkspace w;
     std::memset(&w, 0, sizeof w);
     size_t off = 0;
@@ -158,6 +165,21 @@ MxBwdWorkspace carve_mx_bwd(uint8_t *base, int R, int d, int I, bool recompute, 
     w.dGUq = take(r * 2 * I);
     w.dGUsf = take(r * mx_sf_pitch(2 * I));
     w.dw_part = reinterpret_cast<float *>(take(r * mx_dgrad2_n_part(I) * 4));
+    // each group's rows padded to a multiple of 128; its scale bytes to 16
+    const long long kmax = (long long)R + 127LL * G;
+    w.k_chunks = (int)(kmax / 128 + 1);
+    w.sf_slots = (int)((kmax / 32 + 16LL * G) / 16 + 1);
+    w.kofs = reinterpret_cast<int32_t *>(take((size_t)(G + 1) * 4));
+    w.sofs = reinterpret_cast<int32_t *>(take((size_t)(G + 1) * 4));
+    const size_t kp = (size_t)w.k_chunks * 128, sp = (size_t)w.sf_slots * 16;
+    w.dYt = take((size_t)d * kp);
+    w.dYtsf = take((size_t)d * sp);
+    w.hwt = take((size_t)I * kp);
+    w.hwtsf = take((size_t)I * sp);
+    w.dGUt = take((size_t)2 * I * kp);
+    w.dGUtsf = take((size_t)2 * I * sp);
+    w.xt = take((size_t)d * kp);
+    w.xtsf = take((size_t)d * sp);
     if (recompute) {
         w.gu = reinterpret_cast<float *>(take((r + 31) / 32 * 32 * 2 * I * 4));
         w.hq = take(r * I);
@@ -165,7 +187,6 @@ MxBwdWorkspace carve_mx_bwd(uint8_t *base, int R, int d, int I, bool recompute, 
     }
     if (layer) {
         w.x_perm = reinterpret_cast<uint16_t *>(take(r * d * 2));
-        w.dY_perm = reinterpret_cast<uint16_t *>(take(r * d * 2));
         w.dX_perm = reinterpret_cast<uint16_t *>(take(r * d * 2));
         w.dYq = take(r * d);
         w.dYsf = take(r * mx_sf_pitch(d));
@@ -579,7 +600,8 @@ struct MxExpertBwd {
     const float *gu_save;
     const uint8_t *h_q, *h_sf, *W2t_q, *W2t_sf, *W13t_q, *W13t_sf;
     const float *row_weight;
-    const uint16_t *dY_perm;
+    const uint16_t *dY_rows;      // dY of row r at dY_rows[dY_idx ? dY_idx[r] : r]
+    const int32_t *dY_idx;
     const uint8_t *dY_perm_q, *dY_perm_sf;
     uint16_t *dX_perm;
     float *dW13, *dW2;
@@ -604,8 +626,18 @@ moe_status run_mx_expert_bwd(const MxExpertBwd &a, const MxBwdWorkspace &w, int 
                               gu, hq, hsf, a.row_weight, a.S, a.d, a.I, a.clamp, w.dGU, w.dGUq,
                               w.dGUsf, w.hw, w.dw_part, n_part, st)) != MOE_OK)
         return s;
+    // the weight gradients in the MX training form: their operands quantised
+    // along each group's rows (padded to 128), stored transposed
     if (!mark(MOE_BWD_WGRAD2)) return MOE_ERR_CUDA;
-    if ((s = launch_wgrad(a.dY_perm, a.d, w.hw, a.I, a.offsets, a.G, a.R, a.dW2, st)) != MOE_OK)
+    if ((s = launch_mx_kpad_plan(a.offsets, a.G, w.kofs, w.sofs, st)) != MOE_OK) return s;
+    auto rows_t = [&](const uint16_t *src, const int32_t *idx, int C, uint8_t *q, uint8_t *sf) {
+        return launch_mx_quantize_rows_t(src, idx, a.offsets, w.kofs, w.sofs, a.G, w.k_chunks, C,
+                                         q, sf, st);
+    };
+    if ((s = rows_t(a.dY_rows, a.dY_idx, a.d, w.dYt, w.dYtsf)) != MOE_OK) return s;
+    if ((s = rows_t(w.hw, nullptr, a.I, w.hwt, w.hwtsf)) != MOE_OK) return s;
+    if ((s = launch_mx_wgrad(w.dYt, w.dYtsf, w.hwt, w.hwtsf, w.kofs, w.sofs, a.G, a.d, a.I,
+                             w.k_chunks, w.sf_slots, a.dW2, st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_DGRAD1)) return MOE_ERR_CUDA;
     // dgrad 1 is MX GEMM 2 with the contraction over 2I and no row weight
@@ -613,14 +645,19 @@ moe_status run_mx_expert_bwd(const MxExpertBwd &a, const MxBwdWorkspace &w, int 
                             a.d, 2 * a.I, a.dX_perm, st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_WGRAD1)) return MOE_ERR_CUDA;
-    return launch_wgrad(w.dGU, 2 * a.I, a.x_perm, a.d, a.offsets, a.G, a.R, a.dW13, st);
+    if ((s = rows_t(w.dGU, nullptr, 2 * a.I, w.dGUt, w.dGUtsf)) != MOE_OK) return s;
+    if ((s = rows_t(a.x_perm, nullptr, a.d, w.xt, w.xtsf)) != MOE_OK) return s;
+    return launch_mx_wgrad(w.dGUt, w.dGUtsf, w.xt, w.xtsf, w.kofs, w.sofs, a.G, 2 * a.I, a.d,
+                           w.k_chunks, w.sf_slots, a.dW13, st);
 }
 
 }  // namespace
 
-size_t moe_expert_bwd_mx_workspace_size(int max_rows, int d, int I, int recompute) {
-    if (max_rows < 1 || d < 32 || I < 128 || I % 128 != 0 || d % 32 != 0) return 0;
-    return carve_mx_bwd(nullptr, max_rows, d, I, recompute != 0, false, 0, 0, 0).bytes;
+size_t moe_expert_bwd_mx_workspace_size(int G, int max_rows, int d, int I, int recompute) {
+    if (G < 1 || G > 1025 || max_rows < 1 || d < 128 || d % 128 != 0 || I < 128 ||
+        I % 128 != 0)
+        return 0;
+    return carve_mx_bwd(nullptr, G, max_rows, d, I, recompute != 0, false, 0, 0, 0).bytes;
 }
 
 moe_status moe_expert_ffn_backward_mx(const moe_expert_bwd_mx_args *a, void *stream) {
@@ -640,15 +677,17 @@ moe_status moe_expert_ffn_backward_mx(const moe_expert_bwd_mx_args *a, void *str
         if (rec && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
     for (const void *p : need_saved)
         if (!rec && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
-    if (!a->ws || a->ws_bytes < moe_expert_bwd_mx_workspace_size(a->max_rows, a->d, a->I, rec))
+    if (!a->ws ||
+        a->ws_bytes < moe_expert_bwd_mx_workspace_size(a->G, a->max_rows, a->d, a->I, rec))
         return MOE_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const MxBwdWorkspace w =
-        carve_mx_bwd(static_cast<uint8_t *>(a->ws), a->max_rows, a->d, a->I, rec, false, 0, 0, 0);
+    const MxBwdWorkspace w = carve_mx_bwd(static_cast<uint8_t *>(a->ws), a->G, a->max_rows, a->d,
+                                          a->I, rec, false, 0, 0, 0);
     const MxExpertBwd e{a->G, a->max_rows, a->S, a->d, a->I, a->clamp, a->offsets, a->x_perm,
                         a->x_perm_q, a->x_perm_sf, a->W13_q, a->W13_sf, a->gu_save, a->h_q,
                         a->h_sf, a->W2t_q, a->W2t_sf, a->W13t_q, a->W13t_sf, a->row_weight,
-                        a->dY_perm, a->dY_perm_q, a->dY_perm_sf, a->dX_perm, a->dW13, a->dW2};
+                        a->dY_perm, nullptr, a->dY_perm_q, a->dY_perm_sf, a->dX_perm, a->dW13,
+                        a->dW2};
     int n_part = 0;
     if ((s = run_mx_expert_bwd(e, w, &n_part, [](int) { return true; }, st)) != MOE_OK) return s;
     if (a->dw_rows && a->S > 0) return launch_row_sum(w.dw_part, a->S, n_part, a->dw_rows, st);
@@ -658,7 +697,7 @@ moe_status moe_expert_ffn_backward_mx(const moe_expert_bwd_mx_args *a, void *str
 size_t moe_backward_mx_workspace_size(int T, int d, int E, int k, int I, int recompute) {
     if (check_shapes(T, d, E, k, I) != MOE_OK || d % 256 != 0 || I % 128 != 0) return 0;
     const int R = T * k + T;
-    return carve_mx_bwd(nullptr, R, d, I, recompute != 0, true, T, E, k).bytes;
+    return carve_mx_bwd(nullptr, E + 1, R, d, I, recompute != 0, true, T, E, k).bytes;
 }
 
 moe_status moe_backward_mx(const moe_bwd_mx_args *a, void *stream) {
@@ -670,7 +709,7 @@ moe_status moe_backward_mx(const moe_bwd_mx_args *a, void *stream) {
     const bool rec = a->gu_save == nullptr;
     const void *need[] = {a->x,        a->W_g,    a->W2t_q,  a->W2t_sf, a->W13t_q, a->W13t_sf,
                           a->ids,      a->weights, a->scores_sel, a->row_weight, a->offsets,
-                          a->slot_row, a->dY,     a->dX,     a->dW_g,   a->dW13,   a->dW2};
+                          a->row_token, a->slot_row, a->dY, a->dX, a->dW_g, a->dW13, a->dW2};
     for (const void *p : need)
         if (!p) return MOE_ERR_INVALID_ARG;
     const void *al[] = {a->x,      a->W_g,    a->W2t_q, a->W2t_sf, a->W13t_q, a->W13t_sf,
@@ -696,21 +735,20 @@ moe_status moe_backward_mx(const moe_bwd_mx_args *a, void *stream) {
     const int R = S + T;
     const int G = E + 1;
     const MxBwdWorkspace w =
-        carve_mx_bwd(static_cast<uint8_t *>(a->ws), R, d, I, rec, true, T, E, k);
-    // the bf16 rows of x (dW13 and dW_g), and of dY (dW2) and its MX rows (dgrad 2)
+        carve_mx_bwd(static_cast<uint8_t *>(a->ws), G, R, d, I, rec, true, T, E, k);
+    // the bf16 rows of x (dW13's operand and dW_g), and the MX rows of dY
+    // (dgrad 2); dW2's operand reads dY's rows through row_token
     if (!mark(MOE_BWD_RECOMPUTE_GATHER)) return MOE_ERR_CUDA;
     if ((s = launch_gather_rows(a->x, a->slot_row, T, d, k, w.x_perm, st)) != MOE_OK) return s;
     const MxExpertBwd e{G, R, S, d, I, a->clamp, a->offsets, w.x_perm, a->x_perm_q, a->x_perm_sf,
                         a->W13_q, a->W13_sf, a->gu_save, a->h_q, a->h_sf, a->W2t_q, a->W2t_sf,
-                        a->W13t_q, a->W13t_sf, a->row_weight, w.dY_perm, w.dYq, w.dYsf,
-                        w.dX_perm, a->dW13, a->dW2};
+                        a->W13t_q, a->W13t_sf, a->row_weight, a->dY, a->row_token, w.dYq,
+                        w.dYsf, w.dX_perm, a->dW13, a->dW2};
     // the expert stages mark their own starts; the dY gathers sit between the
     // GEMM-1 recompute and dgrad 2
     const std::function<bool(int)> mark_expert = [&](int i) -> bool {
         if (i == MOE_BWD_DGRAD2) {
             if (!mark(MOE_BWD_GATHER_DY)) return false;
-            if (launch_gather_rows(a->dY, a->slot_row, T, d, k, w.dY_perm, st) != MOE_OK)
-                return false;
             if (launch_mx_gather(a->dY, a->slot_row, T, d, k, w.dYq, w.dYsf, st) != MOE_OK)
                 return false;
         }

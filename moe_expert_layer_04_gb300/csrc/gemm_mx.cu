@@ -11,6 +11,10 @@
 //               (bf16)
 //   MX dgrad 1  dX = dGU~ (W13^T)~[g]^T, with W13 quantised along 2I: GEMM 2
 //               with K = 2I and no row weight
+//   MX wgrad    dW[g] = A~^T B~ over group g's rows, both operands quantised
+//               along the rows (blocks of 32 from the group's first row,
+//               padded to 128) and stored transposed, K-chunk-major (each
+//               stage one contiguous 16 KB box); fp32 out through TMA stores
 // ("DeepSeek-V4昇腾训练支持：基于 CANN 平台的TorchTitan-NPU + AutoFuse 极简训练优化
 // 实践", 性能结果与未来展望: FP8 training on MxFP8 compute; the expert matmuls
 // themselves: "HyperParallel加速DeepSeek-V4.1多模态1M长序列训练" §2.3 MegaMoE.)
@@ -65,13 +69,14 @@
 namespace moe {
 namespace {
 
-enum MxMode : int { MX_FFN1 = 0, MX_FFN2 = 1, MX_DGRAD2 = 2 };
+enum MxMode : int { MX_FFN1 = 0, MX_FFN2 = 1, MX_DGRAD2 = 2, MX_WGRAD = 3 };
 
 struct MxParams {
     CUtensorMap tmA;   // A codes [rows, K] u8, boxes 128 x 128, 128-byte swizzle
     CUtensorMap tmO;   // dgrad 2: dG|dU [rows, 2I] bf16, boxes 32 x 32, 64-byte swizzle
     CUtensorMap tmO2;  // dgrad 2: w h~ [rows, I] bf16, boxes 32 x 32, 64-byte swizzle
     CUtensorMap tmOQ;  // dgrad 2: dG|dU codes [rows, 2I] u8, boxes 32 x 32
+                       // weight gradients: fp32 output [G * M, N], boxes 32 x 32
     CUtensorMap tmB;   // B codes [G * b_rows_per_group, K] u8, boxes 128 x 64 (GEMM 1) / 128 x 128
     CUtensorMap tmSA;  // A scale codes [rows, pitch] u8, boxes 16 x 128
     CUtensorMap tmSB;  // B scale codes, boxes 16 x 64 (GEMM 1) / 16 x 128
@@ -99,6 +104,9 @@ struct MxParams {
     int dgu_pitch;
     uint16_t *hw;          // dgrad 2: w h~ [rows, I] bf16
     float *dw_part;        // dgrad 2: [rows, n_tiles * NEPI / 4] partials of <h~, dA>
+    int M;                 // weight gradients: output rows per group (A rows)
+    const int32_t *sofs;   // weight gradients: [G+1] first scale byte of each group
+                           // (offsets holds the first code column, kofs)
     int *status;
     long long wait_limit;
 };
@@ -108,7 +116,11 @@ constexpr int kMxCodeA = 128 * 128;   // A codes of a stage
 constexpr int kMxSfA = 128 * kMxSfRow;
 constexpr int kMxSfWarps = 4;
 constexpr int kMxSfSlots = 2;         // scale slots, 4 stages each
-constexpr int kMxBarBytes = 256;
+constexpr int kMxBarBytes = 512;
+// weight gradients: operand stages, and fp32 staging blocks per epilogue warp
+// (two let a block be staged while the previous one's TMA store reads)
+constexpr int kMxWgradStages = 5;
+constexpr int kMxWgradStageBufs = 2;
 constexpr uint32_t kMxTmemCols = 512;
 
 template <int MODE, int BN>
@@ -116,7 +128,9 @@ struct MxShape {
     static constexpr int CODE_B = BN * 128;
     static constexpr int STAGE = kMxCodeA + CODE_B;              // codes of a stage
     static constexpr int SF_SLOT = kMxSfA + BN * kMxSfRow;        // scales of 4 stages
-    static constexpr int STAGES = 4;
+    // the weight gradients' tiles have short contractions (a group's rows):
+    // more stages keep more copies in flight
+    static constexpr int STAGES = MODE == MX_WGRAD ? kMxWgradStages : 4;
     static constexpr int NACC = BN == 256 ? 1 : 2;                // accumulators
     // epilogue warps: two per lane quadrant for the wide tiles and for the
     // heavy epilogue of dgrad 2
@@ -127,7 +141,9 @@ struct MxShape {
     // dgrad 2: per epilogue warp one staging block for each of its five
     // outputs of 32 rows x 32 columns (dg, du, w h~ in bf16; dg, du codes)
     static constexpr int EPI_WARP = 3 * 2048 + 2 * 1024;
-    static constexpr int EPI = MODE == MX_DGRAD2 ? NEPI * EPI_WARP : 0;
+    static constexpr int EPI = MODE == MX_DGRAD2 ? NEPI * EPI_WARP
+                               : MODE == MX_WGRAD ? NEPI * 4096 * kMxWgradStageBufs
+                                                  : 0;
     static constexpr int FIXED = STAGES * STAGE + kMxSfSlots * SF_SLOT + EPI;
     static_assert(SF_COL0 + SF_COLS * STAGES <= kMxTmemCols, "tensor memory columns");
     static_assert((4 * STAGES + 2 * kMxSfSlots + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
@@ -152,11 +168,26 @@ __device__ __forceinline__ void e4m3x4_values(uint32_t w, float (&v)[4]) {
     v[3] = __high2float(h);
 }
 
+template <int MODE>
 __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int *mt_start,
                                             const int *offs) {
     TileInfo ti{};
     ti.nt = t % p.n_tiles;
     const int q = t / p.n_tiles;
+    if constexpr (MODE == MX_WGRAD) {
+        // (group, 128 output rows, BN output columns); the contraction is the
+        // group's padded rows: code columns [offs[g], offs[g + 1]), scale
+        // bytes from mt_start[g]
+        const int mp = p.M / 128;
+        ti.g = q / mp;
+        ti.m0 = (q - ti.g * mp) * 128;
+        ti.krow0 = offs[ti.g];
+        ti.krows = mt_start[ti.g];
+        ti.kb = (offs[ti.g + 1] - offs[ti.g]) / 128;
+        ti.row0 = ti.m0;
+        ti.rows_valid = 128;
+        return ti;
+    }
     int lo = 0, hi = p.G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -233,7 +264,13 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         tmem_alloc(tmem_base_s, kMxTmemCols);
         tmem_relinquish();
     }
-    if (warp == 2) {
+    if (MODE == MX_WGRAD && warp == 2) {
+        // the groups' code column and scale byte offsets
+        for (int g = lane; g <= p.G; g += 32) {
+            offs[g] = p.offsets[g];
+            mt_start[g] = p.sofs[g];
+        }
+    } else if (warp == 2) {
         // group offsets and the exclusive prefix of their 128-row tiles
         int carry = 0;
         for (int base = 0; base <= p.G; base += 32) {
@@ -264,7 +301,8 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
 
     const uint32_t tmem_base = *tmem_base_s;
     const WaitCtl wc{abort_s, p.status, p.wait_limit};
-    const int total_tiles = mt_start[p.G] * p.n_tiles;
+    const int total_tiles =
+        MODE == MX_WGRAD ? p.G * (p.M / 128) * p.n_tiles : mt_start[p.G] * p.n_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -277,10 +315,14 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
             uint32_t s = 0, ph = 0, js = 0, phs = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-                const TileInfo ti = mx_tile(p, t, mt_start, offs);
+                const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
                 // B rows of the tile: GEMM 1 the gate rows and the up rows of its
                 // BN/2 h columns, GEMM 2 BN consecutive output rows
                 const int brow = ti.g * p.b_rows_per_group + ti.nt * (MODE == MX_FFN1 ? BN / 2 : BN);
+                // weight gradients (K-chunk-major operands): the group's first
+                // chunk of 128 codes and first 16-byte scale slot
+                const int kc0 = MODE == MX_WGRAD ? ti.krow0 / 128 : 0;
+                const int ks0 = MODE == MX_WGRAD ? ti.krows / kMxSfRow : 0;
                 for (int kb = 0; kb < ti.kb; ++kb) {
                     if ((kb & 3) == 0) {
                         // the scale codes of this and the next three stages (16 bytes a row)
@@ -289,8 +331,15 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                         uint8_t *sa = sSf + js * SH::SF_SLOT;
                         uint8_t *sb = sa + kMxSfA;
                         const int x = (kb >> 2) * kMxSfRow;
-                        tma_load_2d(sa, &p.tmSA, &sffull[js], x, ti.row0);
-                        if constexpr (MODE == MX_FFN1) {
+                        if constexpr (MODE == MX_WGRAD) {
+                            const int slot = ks0 + (kb >> 2);
+                            tma_load_2d(sa, &p.tmSA, &sffull[js], 0, slot * p.M + ti.m0);
+                            tma_load_2d(sb, &p.tmSB, &sffull[js], 0, slot * p.N + brow);
+                        } else {
+                            tma_load_2d(sa, &p.tmSA, &sffull[js], x, ti.row0);
+                        }
+                        if constexpr (MODE == MX_WGRAD) {
+                        } else if constexpr (MODE == MX_FFN1) {
                             tma_load_2d(sb, &p.tmSB, &sffull[js], x, brow);
                             tma_load_2d(sb + (BN / 2) * kMxSfRow, &p.tmSB, &sffull[js], x,
                                         brow + p.I);
@@ -304,11 +353,16 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                     mbar_arrive_expect_tx(&full[s], SH::STAGE);
                     uint8_t *a = sCodes + s * SH::STAGE;
                     uint8_t *b = a + kMxCodeA;
-                    tma_load_2d(a, &p.tmA, &full[s], kb * 128, ti.row0);
-                    if constexpr (MODE == MX_FFN1) {
+                    if constexpr (MODE == MX_WGRAD) {
+                        const int kc = kc0 + kb;
+                        tma_load_2d(a, &p.tmA, &full[s], 0, kc * p.M + ti.m0);
+                        tma_load_2d(b, &p.tmB, &full[s], 0, kc * p.N + brow);
+                    } else if constexpr (MODE == MX_FFN1) {
+                        tma_load_2d(a, &p.tmA, &full[s], kb * 128, ti.row0);
                         tma_load_2d(b, &p.tmB, &full[s], kb * 128, brow);
                         tma_load_2d(b + (BN / 2) * 128, &p.tmB, &full[s], kb * 128, brow + p.I);
                     } else {
+                        tma_load_2d(a, &p.tmA, &full[s], kb * 128, ti.row0);
                         tma_load_2d(b, &p.tmB, &full[s], kb * 128, brow);
                     }
                     last_par[s] = (int)ph;
@@ -331,7 +385,7 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
-            const TileInfo ti = mx_tile(p, t, mt_start, offs);
+            const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
             const uint32_t acc = NACC == 2 ? (it & 1) : 0;
             const uint32_t aph = NACC == 2 ? ((it >> 1) & 1) : (it & 1);
             if (!mbar_wait(&tempty[acc], aph ^ 1u, wc)) { ok = false; break; }
@@ -379,7 +433,7 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         uint32_t s = 0, ph = 0, js = 0, phs = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = mx_tile(p, t, mt_start, offs);
+            const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
             for (int kb = 0; kb < ti.kb; ++kb) {
                 if ((kb & 3) == 0 && !mbar_wait(&sffull[js], phs, wc)) { ok = false; break; }
                 if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
@@ -422,7 +476,7 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         const int r_local = q * 32 + lane;
         int it = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
-            const TileInfo ti = mx_tile(p, t, mt_start, offs);
+            const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
             const uint32_t acc = NACC == 2 ? (it & 1) : 0;
             const uint32_t aph = NACC == 2 ? ((it >> 1) & 1) : (it & 1);
             if (!mbar_wait(&tfull[acc], aph, wc)) break;
@@ -576,6 +630,43 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
                 }
                 // one partial of <h~, dA> per (row, column tile, warp part)
                 if (valid) p.dw_part[((size_t)row * p.n_tiles + ti.nt) * NPART + part] = dw;
+            } else if constexpr (MODE == MX_WGRAD) {
+                // fp32 blocks of 32 rows x 32 columns through shared memory
+                // (128-byte swizzle), one TMA store each; a group without rows
+                // gets zeros (its accumulator was never written)
+                constexpr int WC = BN / NPART;
+                uint8_t *stg0 = sEpi + (size_t)(warp - 2) * 4096 * kMxWgradStageBufs;
+                const uint32_t sw = (uint32_t)(lane & 7);
+                const bool has_k = ti.kb > 0;
+#pragma unroll 1
+                for (int c = part * WC; c < (part + 1) * WC; c += 32) {
+                    uint8_t *stg = stg0 + (kMxWgradStageBufs == 2 ? ((c >> 5) & 1) * 4096 : 0);
+                    const uint32_t row_addr = smem_u32(stg) + (uint32_t)lane * 128u;
+                    uint32_t r[32];
+                    if (has_k) {
+                        tmem_ld32(tb + c, r);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    // the store that last read this staging block is done with it
+                    if (lane == 0) {
+                        if constexpr (kMxWgradStageBufs == 2) bulk_wait_group_read<1>();
+                        else bulk_wait_group_read<0>();
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(row_addr + ((((uint32_t)j) ^ sw) << 4), r[4 * j], r[4 * j + 1],
+                                     r[4 * j + 2], r[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmOQ, stg, ti.nt * BN + c, ti.g * p.M + ti.m0 + q * 32);
+                        bulk_commit_group();
+                    }
+                }
             } else {
                 constexpr int YC = BN / NPART;       // output columns of this warp
                 float w = 1.0f;
@@ -605,7 +696,7 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
             mbar_arrive(&tempty[acc]);
         }
         // the TMA stores must have left shared memory (and landed) before exit
-        if (MODE == MX_DGRAD2 && lane == 0) bulk_wait_group_all();
+        if ((MODE == MX_DGRAD2 || MODE == MX_WGRAD) && lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -743,6 +834,30 @@ moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32
     if (n_part) *n_part = mx_dgrad2_n_part(I);
     const int tiles = row_tile_bound(max_rows, G) * p.n_tiles;
     return launch_mx<MX_DGRAD2, BN>(p, tiles, st);
+}
+
+moe_status launch_mx_wgrad(const uint8_t *At, const uint8_t *Atsf, const uint8_t *Bt,
+                           const uint8_t *Btsf, const int32_t *kofs, const int32_t *sofs, int G,
+                           int M, int N, int k_chunks, int sf_slots, float *dW, cudaStream_t st) {
+    if (M % 128 != 0 || N % 128 != 0 || k_chunks < 1 || sf_slots < 1) return MOE_ERR_UNSUPPORTED;
+    constexpr int BN = 128;
+    MxParams p;
+    std::memset(&p, 0, sizeof p);
+    // K-chunk-major operands: [chunks x rows, 128 codes] and [slots x rows, 16 scale codes]
+    if (!encode_tmap_u8_2d(&p.tmA, At, 128, (uint64_t)k_chunks * M, 128, 128, 128, 128) ||
+        !encode_tmap_u8_2d(&p.tmB, Bt, 128, (uint64_t)k_chunks * N, 128, 128, BN, 128) ||
+        !encode_tmap_u8_2d(&p.tmSA, Atsf, 16, (uint64_t)sf_slots * M, 16, 16, 128, 0) ||
+        !encode_tmap_u8_2d(&p.tmSB, Btsf, 16, (uint64_t)sf_slots * N, 16, 16, BN, 0) ||
+        !encode_tmap_f32_2d(&p.tmOQ, dW, N, (uint64_t)G * M, (uint64_t)N * 4, 32, 32))
+        return MOE_ERR_CUDA;
+    p.offsets = kofs;
+    p.sofs = sofs;
+    p.G = G;
+    p.M = M;
+    p.N = N;
+    p.n_tiles = N / BN;
+    p.b_rows_per_group = 0;
+    return launch_mx<MX_WGRAD, BN>(p, G * (M / 128) * (N / BN), st);
 }
 
 int mx_dgrad2_n_part(int I) { return I / 128 * (MxShape<MX_DGRAD2, 128>::NEPI / 4); }

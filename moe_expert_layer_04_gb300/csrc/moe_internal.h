@@ -112,6 +112,22 @@ moe_status launch_mx_ffn1(const uint8_t *xq, const uint8_t *xsf, const int32_t *
 moe_status launch_mx_ffn2(const uint8_t *hq, const uint8_t *hsf, const int32_t *offsets, int G,
                           int max_rows, const uint8_t *W2q, const uint8_t *W2sf,
                           const float *row_w, int S, int d, int I, uint16_t *y, cudaStream_t st);
+// MX weight gradients: the padded contraction plan (kofs, sofs [G+1]), the
+// quantisation of each group's rows along the rows, written transposed in
+// the K-chunk-major layout (codes of (c, k) at ((k/128) C + c) 128 + k%128,
+// scale codes in 16-byte slots likewise; row r read from src[row_idx[r]]
+// when row_idx is given), and dW[g] (M x N fp32) over group g's padded
+// contraction of At (C = M) and Bt (C = N) in that layout; k_chunks and
+// sf_slots bound the chunks of 128 codes and the 16-byte scale slots.
+moe_status launch_mx_kpad_plan(const int32_t *offsets, int G, int32_t *kofs, int32_t *sofs,
+                               cudaStream_t st);
+moe_status launch_mx_quantize_rows_t(const uint16_t *src, const int32_t *row_idx,
+                                     const int32_t *offsets, const int32_t *kofs,
+                                     const int32_t *sofs, int G, int max_tiles, int C,
+                                     uint8_t *qt, uint8_t *sft, cudaStream_t st);
+moe_status launch_mx_wgrad(const uint8_t *At, const uint8_t *Atsf, const uint8_t *Bt,
+                           const uint8_t *Btsf, const int32_t *kofs, const int32_t *sofs, int G,
+                           int M, int N, int k_chunks, int sf_slots, float *dW, cudaStream_t st);
 // Partials of <h~, dA> per row written by launch_mx_dgrad2.
 int mx_dgrad2_n_part(int I);
 moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32_t *offsets, int G,

@@ -235,7 +235,198 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The padded contraction of the MX weight gradients: group g's rows occupy
+// kpad_g = cnt_g rounded up to 128 columns of the transposed operands,
+// starting at kofs[g]; its scale codes kpad_g / 32 bytes starting at
+// sofs[g], a multiple of 16 (16-byte TMA rows).  One warp, a scan over the
+// groups in chunks of 32.
+__global__ void mx_kpad_plan_kernel(const int32_t *__restrict__ offsets, int G,
+                                    int32_t *__restrict__ kofs, int32_t *__restrict__ sofs) {
+    const int lane = threadIdx.x & 31;
+    int kc = 0, sc = 0;
+    for (int base = 0; base <= G; base += 32) {
+        const int g = base + lane;
+        int kp = 0, sp = 0;
+        if (g < G) {
+            const int cnt = offsets[g + 1] - offsets[g];
+            kp = (cnt + 127) / 128 * 128;
+            sp = (kp / 32 + 15) / 16 * 16;
+        }
+        int ki = kp, si = sp;
+#pragma unroll
+        for (int sft = 1; sft < 32; sft <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, ki, sft);
+            const int b = __shfl_up_sync(0xffffffffu, si, sft);
+            if (lane >= sft) { ki += a; si += b; }
+        }
+        if (g <= G) {
+            kofs[g] = kc + ki - kp;
+            sofs[g] = sc + si - sp;
+        }
+        kc += __shfl_sync(0xffffffffu, ki, 31);
+        sc += __shfl_sync(0xffffffffu, si, 31);
+    }
+}
+
+// Quantisation along the rows of each group, written transposed: for the
+// permuted rows src [R, C] bf16 (row r read from src row row_idx[r] when
+// row_idx is given), column c of group g's rows, in blocks of 32 rows from
+// the group's first row (the last block zero-padded).  The transposed
+// operand is K-chunk-major, so that each stage of the weight-gradient GEMM
+// reads one contiguous box: code (c, k) of the padded contraction
+// k in [kofs[g], kofs[g] + kpad_g) at qt[((k / 128) * C + c) * 128 + k % 128];
+// scale code (c, j) of the group's j-th block at
+// sft[((sofs[g] / 16 + j / 16) * C + c) * 16 + j % 16].  A CTA takes 128 x 128
+// tiles (128 padded rows of one group, 128 columns): its 256 threads stage
+// the tile in shared memory (rows past the group's end as zeros), each
+// thread quantises two 32-row blocks of one column into a staging tile of
+// codes, and all threads copy the codes out with coalesced 16-byte stores.
+__global__ void __launch_bounds__(256, 3)
+    mx_quantize_rows_t_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ row_idx,
+                              const int32_t *__restrict__ offsets,
+                              const int32_t *__restrict__ kofs, const int32_t *__restrict__ sofs,
+                              int G, int C, uint8_t *__restrict__ qt, uint8_t *__restrict__ sft) {
+    extern __shared__ __align__(16) uint8_t qsm[];
+    uint8_t *tile = qsm;                         // [128 rows][kQTPitch] bf16
+    uint8_t *cqt = qsm + kQT * kQTPitch;         // [128 columns][kQCPitch] codes
+    // per group: first row tile, first row, first scale slot ([G+1] each)
+    int *s_tile0 = reinterpret_cast<int *>(cqt + kQT * kQCPitch);
+    int *s_row0 = s_tile0 + (G + 1);
+    int *s_slot0 = s_row0 + (G + 1);
+    const int t = threadIdx.x;
+    for (int g = t; g <= G; g += blockDim.x) {
+        s_tile0[g] = kofs[g] / kQT;
+        s_row0[g] = offsets[g];
+        s_slot0[g] = sofs[g] / 16;
+    }
+    __syncthreads();
+    const int tc = C / kQT;
+    const long long n_tiles = (long long)s_tile0[G] * tc;
+    struct Tile {
+        int g, rt, r0, valid, c0;
+    };
+    auto locate = [&](long long i) {
+        Tile tl;
+        const int rtg = (int)(i / tc);          // row tile over all groups
+        int lo = 0, hi = G - 1;                 // the group holding it
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_tile0[mid] <= rtg) lo = mid; else hi = mid - 1;
+        }
+        tl.g = lo;
+        tl.rt = rtg - s_tile0[lo];
+        tl.r0 = s_row0[lo] + tl.rt * kQT;
+        tl.valid = min(kQT, s_row0[lo + 1] - tl.r0);
+        tl.c0 = (int)(i % tc) * kQT;
+        return tl;
+    };
+    // the tile's 16-byte chunks of this thread (16 per row; rows past the
+    // group's end are zeros), loaded into registers one tile ahead
+    uint4 v[8];
+    auto load = [&](const Tile &tl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int chunk = t + 256 * j;
+            const int r = chunk >> 4;
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < tl.valid) {
+                const int sr = row_idx ? row_idx[tl.r0 + r] : tl.r0 + r;
+                v[j] = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)sr * C + tl.c0) +
+                             (chunk & 15));
+            }
+        }
+    };
+    Tile cur{};
+    if ((long long)blockIdx.x < n_tiles) {
+        cur = locate(blockIdx.x);
+        load(cur);
+    }
+    for (long long i = blockIdx.x; i < n_tiles; i += gridDim.x) {
+        const Tile tl = cur;
+        __syncthreads();   // the previous tile's readers and copiers are done
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int chunk = t + 256 * j;
+            *reinterpret_cast<uint4 *>(tile + (chunk >> 4) * kQTPitch + (chunk & 15) * 16) = v[j];
+        }
+        __syncthreads();
+        if (i + gridDim.x < n_tiles) {
+            cur = locate(i + gridDim.x);
+            load(cur);
+        }
+        // column c, blocks 2h and 2h + 1 (rows 64h .. 64h + 63)
+        const int c = t & (kQT - 1);
+        const int h = t >> 7;
+        uint32_t codes = 0;
+#pragma unroll 1
+        for (int bb = 0; bb < 2; ++bb) {
+            const int b = 2 * h + bb;
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                f[j] = __uint_as_float(
+                    (uint32_t)*reinterpret_cast<const uint16_t *>(tile + (b * 32 + j) * kQTPitch +
+                                                                  c * 2)
+                    << 16);
+            uint32_t w[8];
+            codes |= mx_quantize_block(f, w) << (8 * bb);
+            store_block(cqt + c * kQCPitch + b * 32, w);
+        }
+        // this tile's blocks 4 rt .. 4 rt + 3 of the group: bytes 4 (rt % 4) ..
+        // of 16-byte slot sofs[g] / 16 + rt / 4
+        const size_t slot = (size_t)(s_slot0[tl.g] + tl.rt / 4);
+        *reinterpret_cast<uint16_t *>(sft + (slot * C + tl.c0 + c) * 16 + 4 * (tl.rt & 3) + 2 * h) =
+            (uint16_t)codes;
+        __syncthreads();
+        // the code tile out: one contiguous 16 KB chunk (128 columns x 128 k)
+        uint8_t *dst = qt + ((size_t)(s_tile0[tl.g] + tl.rt) * C + tl.c0) * kQT;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int chunk = t + 256 * j;
+            const int row = chunk >> 3, c16 = (chunk & 7) * 16;
+            *reinterpret_cast<uint4 *>(dst + (size_t)row * kQT + c16) =
+                *reinterpret_cast<const uint4 *>(cqt + row * kQCPitch + c16);
+        }
+    }
+}
+
 }  // namespace
+
+moe_status launch_mx_kpad_plan(const int32_t *offsets, int G, int32_t *kofs, int32_t *sofs,
+                               cudaStream_t st) {
+    if (G < 1) return MOE_ERR_INVALID_ARG;
+    mx_kpad_plan_kernel<<<1, 32, 0, st>>>(offsets, G, kofs, sofs);
+    return cuda_status(cudaGetLastError());
+}
+
+moe_status launch_mx_quantize_rows_t(const uint16_t *src, const int32_t *row_idx,
+                                     const int32_t *offsets, const int32_t *kofs,
+                                     const int32_t *sofs, int G, int max_tiles, int C,
+                                     uint8_t *qt, uint8_t *sft, cudaStream_t st) {
+    if (C % kQT != 0) return MOE_ERR_UNSUPPORTED;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    // the bf16 tile, one code tile and the groups' tables: three CTAs per SM
+    const int smem = kQT * kQTPitch + kQT * kQCPitch + 3 * 4 * (G + 1);
+    if (G > 1025) return MOE_ERR_UNSUPPORTED;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(mx_quantize_rows_t_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kQT * kQTPitch + kQT * kQCPitch + 3 * 4 * 1026) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const long long n = (long long)max_tiles * (C / kQT);
+    if (n <= 0) return MOE_OK;
+    const long long cap = (long long)num_sms() * 3;
+    const int blocks = (int)(n < cap ? n : cap);
+    mx_quantize_rows_t_kernel<<<blocks, 256, smem, st>>>(src, row_idx, offsets, kofs, sofs, G, C,
+                                                         qt, sft);
+    return cuda_status(cudaGetLastError());
+}
 
 moe_status launch_mx_quantize_both(const uint16_t *src, int G, int R, int C, uint8_t *q,
                                    uint8_t *sf, uint8_t *qt, uint8_t *sft, cudaStream_t st) {

@@ -273,8 +273,8 @@ class MoELayer:
                 x=self.x, W_g=self.w["W_g"], W13_q=self.W13_q, W13_sf=self.W13_sf,
                 W2t_q=self.W2t_q, W2t_sf=self.W2t_sf, W13t_q=self.W13t_q, W13t_sf=self.W13t_sf,
                 ids=self.ids, weights=self.weights, scores_sel=self.scores_sel,
-                row_weight=self.row_weight, offsets=self.offsets, slot_row=self.slot_row,
-                x_perm_q=self.x_perm_q, x_perm_sf=self.x_perm_sf, gu_save=self.gu_save,
+                row_weight=self.row_weight, offsets=self.offsets, row_token=self.row_token,
+                slot_row=self.slot_row, x_perm_q=self.x_perm_q, x_perm_sf=self.x_perm_sf, gu_save=self.gu_save,
                 h_q=None if self.recompute else self.h_q,
                 h_sf=None if self.recompute else self.h_sf,
                 dY=dY, dX=self.dX, dW_g=self.dW_g, dW13=self.dW13, dW2=self.dW2,

@@ -155,8 +155,8 @@ def test_mx_calls_host_logic():
     ws0 = lib.moe_backward_mx_workspace_size(64, 256, 8, 2, 128, 0)
     ws1 = lib.moe_backward_mx_workspace_size(64, 256, 8, 2, 128, 1)
     assert 0 < ws0 < ws1
-    assert 0 < lib.moe_expert_bwd_mx_workspace_size(300, 256, 128, 0) < \
-        lib.moe_expert_bwd_mx_workspace_size(300, 256, 128, 1)
+    assert 0 < lib.moe_expert_bwd_mx_workspace_size(3, 300, 256, 128, 0) < \
+        lib.moe_expert_bwd_mx_workspace_size(3, 300, 256, 128, 1)
     a = _lib.BwdMxArgs()
     a.T, a.d, a.E, a.k, a.I, a.scaling, a.clamp = 64, 256, 8, 2, 128, 2.5, 7.0
     for name, _ in _lib.BwdMxArgs._fields_[7:]:
@@ -177,7 +177,7 @@ def test_mx_calls_host_logic():
     for name, _ in _lib.ExpertBwdMxArgs._fields_[6:]:
         if name not in ("ws_bytes", "dw_rows"):
             setattr(e, name, 256)
-    e.ws_bytes = lib.moe_expert_bwd_mx_workspace_size(300, 256, 128, 0) - 1
+    e.ws_bytes = lib.moe_expert_bwd_mx_workspace_size(3, 300, 256, 128, 0) - 1
     assert lib.moe_expert_ffn_backward_mx(ctypes.byref(e), nul) == _lib.MOE_ERR_WORKSPACE
     e.dY_perm_q = 264                                 # 8-byte aligned only
     assert lib.moe_expert_ffn_backward_mx(ctypes.byref(e), nul) == _lib.MOE_ERR_INVALID_ARG

@@ -22,7 +22,7 @@ import oracle
 from moe_expert_layer_04_gb300 import _lib
 from moe_expert_layer_04_gb300 import workloads as W
 from moe_expert_layer_04_gb300.layer import Dims, MoELayer
-from tests.helpers import assert_close, assert_wgrad_bf16_bound, cpu, np64
+from tests.helpers import assert_close, check_mx_wgrad, cpu, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -105,29 +105,23 @@ def _rows_meta(layer, w):
 
 
 def _check_expert_wgrads(w, inp, layer, experts):
-    """dW2[e] against fp64 sums over the GPU's own MX h (its codes are checked
-    against the oracle in the forward tests), dW13[e] against the oracle's
-    pre-quantisation [dg | du] of the expert's rows."""
+    """Each listed expert's MX weight gradients against the oracle
+    (tests.helpers.check_mx_wgrad); an expert without rows gets zeros."""
     offs, rt, grp, rw = _rows_meta(layer, w)
     x, dY = cpu(inp["x"]), cpu(inp["dY"])
     for e in experts:
         rows = np.arange(offs[e], offs[e + 1])
         ex = torch.tensor([e]).cuda()
-        W13e, W2e = cpu(inp["W13"][ex]), cpu(inp["W2"][ex])
         if len(rows) == 0:
             assert float(layer.dW13[e].abs().max()) == 0.0
             assert float(layer.dW2[e].abs().max()) == 0.0
             continue
-        ref = oracle.expert_rows_mx_backward(x, W13e, W2e, dY, rt[rows],
-                                             np.zeros(len(rows), np.int32), rw[rows], w.clamp)
-        xr = x.double().numpy()[rt[rows]]
-        dyr = dY.double().numpy()[rt[rows]]
         ridx = torch.from_numpy(rows).cuda()
         h_gpu = oracle.mx_dequantize(cpu(layer.h_q[ridx]).numpy(),
                                      cpu(layer.h_sf[ridx]).numpy()[:, : w.I // 32])
-        assert np.mean(np.abs(h_gpu - ref["h"]) > 0) <= 2e-3
-        assert_wgrad_bf16_bound(layer.dW2[e], dyr, rw[rows, None] * h_gpu, f"{w.name} dW2[{e}]")
-        assert_wgrad_bf16_bound(layer.dW13[e].t(), xr, ref["dgu"], f"{w.name} dW13[{e}]")
+        check_mx_wgrad(layer.dW2[e], layer.dW13[e], x, cpu(inp["W13"][ex][0]),
+                       cpu(inp["W2"][ex][0]), dY, rt[rows], rw[rows], w.clamp, h_gpu,
+                       f"{w.name} expert {e} ({len(rows)} rows)")
 
 
 # name, T, d, E, k, I, experts forced empty, recompute, tokens checked (None: all)
@@ -200,7 +194,7 @@ def test_mx_expert_backward_rows(recompute):
     dw_rows = torch.empty(D.S, dtype=torch.float32, device="cuda")
     dW13 = torch.empty_like(layer.dW13)
     dW2 = torch.empty_like(layer.dW2)
-    ws = torch.empty(_lib.moe_expert_bwd_mx_workspace_size(R, d, I, recompute),
+    ws = torch.empty(_lib.moe_expert_bwd_mx_workspace_size(G, R, d, I, recompute),
                      dtype=torch.uint8, device="cuda")
     _lib.moe_expert_ffn_backward_mx(dict(
         G=G, max_rows=R, S=D.S, d=d, I=I, clamp=w.clamp, offsets=layer.offsets, x_perm=x_perm,

@@ -7,8 +7,8 @@ dX, dlogits and dw of sampled tokens against the oracle's MX layer backward
 (tokens whose routing the oracle reproduces; a disagreement is allowed only
 at a near-tie of the keys); every entry of the weight gradients of three
 routed experts (the coldest non-empty one, the median one and a seeded one,
-all their rows through the oracle's MX expert backward) within the bf16
-rounding bound; dW_g rows as the oracle's reduction of the GPU's logit
+all their rows through the oracle's MX weight gradients, stage-wise and end
+to end); dW_g rows as the oracle's reduction of the GPU's logit
 gradients; the backward's transposed weight copies of one expert bit for
 bit.  Routing and permutation at this size are checked bit for bit in
 test_gpu_fullsize.py (the MX layer runs the same kernels for them)."""
@@ -20,7 +20,7 @@ import oracle
 from moe_expert_layer_04_gb300 import _lib
 from moe_expert_layer_04_gb300 import workloads as W
 from moe_expert_layer_04_gb300.layer import Dims, MoELayer
-from tests.helpers import assert_close, assert_wgrad_bf16_bound, cpu, np64
+from tests.helpers import assert_close, check_mx_wgrad, cpu, np64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -71,24 +71,17 @@ def test_long_slice_mx_training_step():
     dwg_ref = oracle.gate_wgrad_rows(x, np64(layer.dlogits), pick)
     assert_close(layer.dW_g[torch.from_numpy(pick).long().cuda()], dwg_ref, "MX dW_g rows",
                  max_abs=max(5e-2, 1e-3 * np.abs(dwg_ref).max()))
-    # whole weight gradients of three routed experts
+    # whole MX weight gradients of three routed experts
     rt_all = cpu(layer.row_token).numpy().astype(np.int64)
     rw_all = np64(layer.row_weight)
-    xd, dyd = x.double().numpy(), dY.double().numpy()
     for e in experts:
         rows = np.arange(offs[e], offs[e + 1])
-        ex = torch.tensor([e])
-        r_ref = oracle.expert_rows_mx_backward(x, host["W13"][ex], host["W2"][ex], dY,
-                                               rt_all[rows], np.zeros(len(rows), np.int32),
-                                               rw_all[rows], w.clamp)
         ridx = torch.from_numpy(rows).cuda()
         h_gpu = oracle.mx_dequantize(cpu(layer.h_q[ridx]).numpy(),
                                      cpu(layer.h_sf[ridx]).numpy()[:, : w.I // 32])
-        assert np.mean(np.abs(h_gpu - r_ref["h"]) > 0) <= 2e-3
-        assert_wgrad_bf16_bound(layer.dW2[e], dyd[rt_all[rows]], rw_all[rows, None] * h_gpu,
-                                f"MX dW2[{e}] ({len(rows)} rows)")
-        assert_wgrad_bf16_bound(layer.dW13[e].t(), xd[rt_all[rows]], r_ref["dgu"],
-                                f"MX dW13[{e}] ({len(rows)} rows)")
+        check_mx_wgrad(layer.dW2[e], layer.dW13[e], x, host["W13"][e], host["W2"][e], dY,
+                       rt_all[rows], rw_all[rows], w.clamp, h_gpu,
+                       f"MX expert {e} ({len(rows)} rows)")
     # the backward's weight copies (quantised along d and 2I) of one expert
     e = experts[1]
     q, sf = oracle.mx_quantize(host["W2"][e].t().contiguous())
