@@ -947,38 +947,54 @@ def run_headline(args, weights, dev, world, hbm, bf16_sus):
 
 
 def run_headline_e2e(args, h, world):
-    """The headline step end to end through moe_layer_step_host: x and dY
-    copied in from pinned host memory and y and dX copied back every step
-    (dY's upload overlaps the forward and y's download the backward)."""
+    """The headline step end to end through the C ABI with host buffers: x
+    and dY copied in from pinned host memory and y and dX copied back every
+    step.  moe_layer_steps_host pipelines the steps (the next step's uploads
+    and the last step's downloads overlap the compute; two sets of host
+    buffers in turn); moe_layer_step_host, one step per call, is timed beside
+    it."""
     layer, inp, D = h["layer"], h["inp"], h["D"]
     stream = torch.cuda.current_stream()
-    x_h = inp["x"].cpu().pin_memory()
-    dY_h = inp["dY"].cpu().pin_memory()
-    y_h = torch.empty_like(x_h).pin_memory()
-    dX_h = torch.empty_like(x_h).pin_memory()
+    x_h = [inp["x"].cpu().pin_memory() for _ in range(2)]
+    dY_h = [inp["dY"].cpu().pin_memory() for _ in range(2)]
+    y_h = [torch.empty_like(x_h[0]).pin_memory() for _ in range(2)]
+    dX_h = [torch.empty_like(x_h[0]).pin_memory() for _ in range(2)]
+    ci, co = torch.cuda.Stream(), torch.cuda.Stream()
+    route = dict(bias=inp["bias"], is_vision=inp["is_vision"], logit_offset=inp["logit_offset"])
+
+    def steps(n):
+        pick = lambda b: [b[i % 2] for i in range(n)]
+        layer.steps_host(pick(x_h), pick(y_h), pick(dY_h), pick(dX_h), copy_in_stream=ci,
+                         copy_out_stream=co, **route)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        dist_barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return dist_max(e0.elapsed_time(e1) / args.steps, world)
+
+    steps(args.warmup)
+    ms = timed(lambda: steps(args.steps))
     cs = torch.cuda.Stream()
-    route = (inp["bias"], inp["is_vision"], inp["logit_offset"])
 
-    def step():
-        layer.step_host(x_h, y_h, dY_h, dX_h, *route, copy_stream=cs)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    dist_barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = dist_max(e0.elapsed_time(e1) / args.steps, world)
+    def one_by_one():
+        for i in range(args.steps):
+            layer.step_host(x_h[i % 2], y_h[i % 2], dY_h[i % 2], dX_h[i % 2], copy_stream=cs,
+                            **route)
+    one_by_one()
+    ms1 = timed(one_by_one)
     nb = D.T * D.d * 2
     return {"value": round(replica_throughput(world, D.T, ms), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": 2 * nb, "d2h_bytes_per_step": 2 * nb,
             "ms_per_step": round(ms, 4),
-            "path": "moe_layer_step_host (C ABI, host x and dY in, host y and dX out every "
-                    "step; dY's upload overlaps the forward, y's download the backward)"}
+            "path": "moe_layer_steps_host (C ABI; host x and dY in, host y and dX out every "
+                    "step; the next step's uploads and the last step's downloads overlap "
+                    "the compute)",
+            "one_step_per_call_ms": round(ms1, 4)}
 
 
 # --------------------------------------------- forward + backward alone

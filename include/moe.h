@@ -432,6 +432,29 @@ moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_hos
                                const uint16_t *dY_host, uint16_t *y_host, uint16_t *dX_host,
                                void *stream, void *copy_stream);
 
+/* A second set of the layer's device rows ([T,d] bf16 each; dY and dX NULL
+ * for forward-only steps). */
+typedef struct {
+    uint16_t *x, *dY, *y, *dX;
+} moe_layer_io;
+
+/* n_steps steps of the layer from and to HOST memory, pipelined: step i
+ * copies x_host[i] (and dY_host[i]) in and y_host[i] (and dX_host[i]) out,
+ * as moe_layer_step_host, with the steps alternating between L's device rows
+ * and `second`, so that step i + 1's uploads (on copy_in_stream) and step i's
+ * downloads (on copy_out_stream) overlap the neighbouring steps' compute on
+ * `stream`.  Three distinct streams; the pointer arrays hold n_steps host
+ * buffers each (page-locked for asynchronous copies; dY_host and dX_host both
+ * NULL for forward-only steps).  The results are those of n_steps calls of
+ * moe_layer_step_host (the weight gradients are the last step's).  `stream`
+ * ends after every copy of the call; it creates and releases a few CUDA
+ * events and allocates no memory.  Returns the first failing call's status. */
+moe_status moe_layer_steps_host(const moe_layer_buffers *L, const moe_layer_io *second,
+                                int n_steps, const uint16_t *const *x_host,
+                                const uint16_t *const *dY_host, uint16_t *const *y_host,
+                                uint16_t *const *dX_host, void *stream, void *copy_in_stream,
+                                void *copy_out_stream);
+
 /* ---------------------------------------------------------------- MXFP8
  * Low-precision expert matmuls ([TTN] outlook: FP8 training on MxFP8
  * compute).  The pages fix no format; these calls use the OCP Microscaling

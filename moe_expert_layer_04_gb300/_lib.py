@@ -37,7 +37,7 @@ EXPORTS = ["moe_workspace_size", "moe_route", "moe_route_logits", "moe_gate_rout
            "moe_permute_noalloc",
            "moe_expert_ffn", "moe_expert_ffn_fused", "moe_expert_gemm1", "moe_expert_gemm2", "moe_combine", "moe_backward", "moe_status_string",
            "moe_last_device_status", "moe_selftest_wait_timeout", "moe_selftest_ffn_fused_stall",
-           "moe_layer_step_host", "moe_gather_rows", "moe_expert_bwd_workspace_size",
+           "moe_layer_step_host", "moe_layer_steps_host", "moe_gather_rows", "moe_expert_bwd_workspace_size",
            "moe_expert_ffn_backward", "moe_router_bwd_workspace_size", "moe_router_backward",
            "moe_set_gemm_pairs", "moe_mx_sf_pitch", "moe_mx_quantize", "moe_mx_gather", "moe_expert_ffn_mx",
            "moe_expert_gemm1_mx", "moe_expert_gemm2_mx", "moe_mx_quantize_t",
@@ -137,6 +137,11 @@ class LayerBuffers(ctypes.Structure):
                 ("ws", _P), ("ws_bytes", _Z)]
 
 
+class LayerIo(ctypes.Structure):
+    """Mirror of moe_layer_io."""
+    _fields_ = [("x", _P), ("dY", _P), ("y", _P), ("dX", _P)]
+
+
 class ExpertBwdMxArgs(ctypes.Structure):
     """Mirror of moe_expert_bwd_mx_args."""
     _fields_ = [("G", _I), ("max_rows", _I), ("S", _I), ("d", _I), ("I", _I), ("clamp", _F),
@@ -194,6 +199,9 @@ _SIGS = {
     "moe_router_backward": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P,
                              _P, _P, _Z, _P], _I),
     "moe_layer_step_host": ([ctypes.POINTER(LayerBuffers), _P, _P, _P, _P, _P, _P], _I),
+    "moe_layer_steps_host": ([ctypes.POINTER(LayerBuffers), ctypes.POINTER(LayerIo), _I,
+                              ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                              ctypes.POINTER(_P), _P, _P, _P], _I),
     "moe_selftest_ffn_fused_stall": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _Z,
                                       _I, _LL, _P], _I),
     "moe_mx_sf_pitch": ([_I], _I),
@@ -588,6 +596,32 @@ def moe_layer_step_host(L: LayerBuffers, x_host, dY_host, y_host, dX_host, strea
                                     _host_ptr(dY_host, "dY_host"), _host_ptr(y_host, "y_host"),
                                     _host_ptr(dX_host, "dX_host"), _stream(stream), cs)
     _check("moe_layer_step_host", st)
+
+
+def moe_layer_steps_host(L: LayerBuffers, second: dict, x_host, dY_host, y_host, dX_host,
+                         stream=None, copy_in_stream=None, copy_out_stream=None):
+    """len(x_host) pipelined layer steps from and to host memory: lists of
+    pinned CPU [T,d] bf16 tensors (dY_host / dX_host None for forward-only
+    steps); `second` holds the second set of device rows (x, dY, y, dX CUDA
+    tensors)."""
+    n = len(x_host)
+    io = LayerIo(_ptr(second.get("x"), BF16, "x"), _ptr(second.get("dY"), BF16, "dY"),
+                 _ptr(second.get("y"), BF16, "y"), _ptr(second.get("dX"), BF16, "dX"))
+
+    def arr(ts, name):
+        if ts is None:
+            return None
+        if len(ts) != n:
+            raise ValueError(f"{name}: {n} tensors expected")
+        return (_P * n)(*[_host_ptr(t, name) for t in ts])
+    xs, dys, ys, dxs = arr(x_host, "x_host"), arr(dY_host, "dY_host"), arr(y_host, "y_host"), \
+        arr(dX_host, "dX_host")
+    cast = lambda a: None if a is None else ctypes.cast(a, ctypes.POINTER(_P))
+    ci = None if copy_in_stream is None else ctypes.c_void_p(copy_in_stream.cuda_stream)
+    co = None if copy_out_stream is None else ctypes.c_void_p(copy_out_stream.cuda_stream)
+    st = load().moe_layer_steps_host(ctypes.byref(L), ctypes.byref(io), n, cast(xs), cast(dys),
+                                     cast(ys), cast(dxs), _stream(stream), ci, co)
+    _check("moe_layer_steps_host", st)
 
 
 def moe_gather_rows(src, idx, dst, stream=None):

@@ -972,6 +972,56 @@ moe_status moe_router_backward(const float *dw_rows, const uint16_t *dX_perm,
     return launch_dwg(x_perm, w.dz_row, offsets, d, E, w.dwg_part, dW_g, st);
 }
 
+namespace {
+
+// One forward of the layer described by L from the device rows x into y.
+moe_status layer_forward(const moe_layer_buffers *L, const uint16_t *x, uint16_t *y,
+                         void *stream) {
+    const int T = L->T, d = L->d, E = L->E, k = L->k, I = L->I;
+    moe_status s;
+    if (L->modality_counts)
+        s = moe_gate_route(x, L->W_g, L->logit_offset, L->bias, L->is_vision, L->input_ids,
+                           L->tid2eid, L->vocab, T, d, E, k, L->scaling,
+                           static_cast<moe_route_mode>(L->mode), L->logits, L->ids, L->weights,
+                           L->scores_sel, L->modality_counts, stream);
+    else
+        s = moe_route(x, L->W_g, L->logit_offset, L->bias, L->is_vision, L->input_ids,
+                      L->tid2eid, L->vocab, T, d, E, k, L->scaling,
+                      static_cast<moe_route_mode>(L->mode), L->logits, L->ids, L->weights,
+                      L->scores_sel, stream);
+    if (s != MOE_OK) return s;
+    s = moe_permute(L->ids, L->weights, x, T, d, E, k, L->counts, L->offsets, L->row_token,
+                    L->slot_row, L->row_weight, L->x_perm, L->ws, L->ws_bytes, stream);
+    if (s != MOE_OK) return s;
+    const int R = T * k + T;
+    s = moe_expert_ffn(L->x_perm, L->offsets, E + 1, R, L->W13, L->W2, L->row_weight, T * k, d,
+                       I, L->clamp, (L->flags & MOE_FLAG_RECOMPUTE) ? nullptr : L->gu_save,
+                       L->h_perm, L->y_perm, nullptr, 0, stream);
+    if (s != MOE_OK) return s;
+    return moe_combine(L->y_perm, L->slot_row, T, d, k, 1, y, stream);
+}
+
+// The backward of the last forward of L (input rows x) for the upstream
+// gradient dY into dX and L's weight gradients.
+moe_status layer_backward(const moe_layer_buffers *L, const uint16_t *x, const uint16_t *dY,
+                          uint16_t *dX, void *stream) {
+    moe_bwd_args a;
+    std::memset(&a, 0, sizeof a);
+    a.T = L->T; a.d = L->d; a.E = L->E; a.k = L->k; a.I = L->I;
+    a.scaling = L->scaling;
+    a.clamp = L->clamp;
+    a.flags = L->flags & MOE_FLAG_RECOMPUTE;
+    a.x = x; a.W_g = L->W_g; a.W13 = L->W13; a.W2 = L->W2;
+    a.ids = L->ids; a.weights = L->weights; a.scores_sel = L->scores_sel;
+    a.row_weight = L->row_weight; a.offsets = L->offsets; a.row_token = L->row_token;
+    a.slot_row = L->slot_row; a.x_perm = L->x_perm; a.gu_save = L->gu_save;
+    a.dY = dY; a.dX = dX; a.dW_g = L->dW_g; a.dW13 = L->dW13; a.dW2 = L->dW2;
+    a.ws = L->ws; a.ws_bytes = L->ws_bytes;
+    return moe_backward(&a, stream);
+}
+
+}  // namespace
+
 moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_host,
                                const uint16_t *dY_host, uint16_t *y_host, uint16_t *dX_host,
                                void *stream, void *copy_stream) {
@@ -981,8 +1031,7 @@ moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_hos
     if (train && (!L->dY || !L->dX)) return MOE_ERR_INVALID_ARG;
     moe_status s = check_shapes(L->T, L->d, L->E, L->k, L->I);
     if (s != MOE_OK) return s;
-    const int T = L->T, d = L->d, E = L->E, k = L->k, I = L->I;
-    const size_t row_bytes = (size_t)T * d * sizeof(uint16_t);
+    const size_t row_bytes = (size_t)L->T * L->d * sizeof(uint16_t);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
     const bool overlap = train && cs != nullptr && cs != st;
@@ -1008,28 +1057,7 @@ moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_hos
             !ok(cudaEventRecord(ev[1], cs)))
             return cleanup(MOE_ERR_CUDA);
     }
-    // forward
-    if (L->modality_counts)
-        s = moe_gate_route(L->x, L->W_g, L->logit_offset, L->bias, L->is_vision, L->input_ids,
-                           L->tid2eid, L->vocab, T, d, E, k, L->scaling,
-                           static_cast<moe_route_mode>(L->mode), L->logits, L->ids, L->weights,
-                           L->scores_sel, L->modality_counts, stream);
-    else
-        s = moe_route(L->x, L->W_g, L->logit_offset, L->bias, L->is_vision, L->input_ids,
-                      L->tid2eid, L->vocab, T, d, E, k, L->scaling,
-                      static_cast<moe_route_mode>(L->mode), L->logits, L->ids, L->weights,
-                      L->scores_sel, stream);
-    if (s != MOE_OK) return cleanup(s);
-    s = moe_permute(L->ids, L->weights, L->x, T, d, E, k, L->counts, L->offsets, L->row_token,
-                    L->slot_row, L->row_weight, L->x_perm, L->ws, L->ws_bytes, stream);
-    if (s != MOE_OK) return cleanup(s);
-    const int R = T * k + T;
-    s = moe_expert_ffn(L->x_perm, L->offsets, E + 1, R, L->W13, L->W2, L->row_weight, T * k, d,
-                       I, L->clamp, (L->flags & MOE_FLAG_RECOMPUTE) ? nullptr : L->gu_save,
-                       L->h_perm, L->y_perm, nullptr, 0, stream);
-    if (s != MOE_OK) return cleanup(s);
-    s = moe_combine(L->y_perm, L->slot_row, T, d, k, 1, L->y, stream);
-    if (s != MOE_OK) return cleanup(s);
+    if ((s = layer_forward(L, L->x, L->y, stream)) != MOE_OK) return cleanup(s);
     if (overlap) {
         if (!ok(cudaEventRecord(ev[2], st)) || !ok(cudaStreamWaitEvent(cs, ev[2], 0)) ||
             !ok(cudaMemcpyAsync(y_host, L->y, row_bytes, cudaMemcpyDeviceToHost, cs)) ||
@@ -1043,25 +1071,98 @@ moe_status moe_layer_step_host(const moe_layer_buffers *L, const uint16_t *x_hos
             return cleanup(MOE_ERR_CUDA);
     }
     if (train) {
-        moe_bwd_args a;
-        std::memset(&a, 0, sizeof a);
-        a.T = T; a.d = d; a.E = E; a.k = k; a.I = I;
-        a.scaling = L->scaling;
-        a.clamp = L->clamp;
-        a.flags = L->flags & MOE_FLAG_RECOMPUTE;
-        a.x = L->x; a.W_g = L->W_g; a.W13 = L->W13; a.W2 = L->W2;
-        a.ids = L->ids; a.weights = L->weights; a.scores_sel = L->scores_sel;
-        a.row_weight = L->row_weight; a.offsets = L->offsets; a.row_token = L->row_token;
-        a.slot_row = L->slot_row; a.x_perm = L->x_perm; a.gu_save = L->gu_save;
-        a.dY = L->dY; a.dX = L->dX; a.dW_g = L->dW_g; a.dW13 = L->dW13; a.dW2 = L->dW2;
-        a.ws = L->ws; a.ws_bytes = L->ws_bytes;
-        s = moe_backward(&a, stream);
-        if (s != MOE_OK) return cleanup(s);
+        if ((s = layer_backward(L, L->x, L->dY, L->dX, stream)) != MOE_OK) return cleanup(s);
         if (!ok(cudaMemcpyAsync(dX_host, L->dX, row_bytes, cudaMemcpyDeviceToHost, st)))
             return cleanup(MOE_ERR_CUDA);
     }
     // `stream` ends after every copy of the step
     if (overlap && !ok(cudaStreamWaitEvent(st, ev[3], 0))) return cleanup(MOE_ERR_CUDA);
+    return cleanup(MOE_OK);
+}
+
+moe_status moe_layer_steps_host(const moe_layer_buffers *L, const moe_layer_io *second,
+                                int n_steps, const uint16_t *const *x_host,
+                                const uint16_t *const *dY_host, uint16_t *const *y_host,
+                                uint16_t *const *dX_host, void *stream, void *copy_in_stream,
+                                void *copy_out_stream) {
+    if (!L || !second || n_steps < 0 || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+    if (n_steps == 0) return MOE_OK;
+    const bool train = dY_host != nullptr;
+    if (train != (dX_host != nullptr)) return MOE_ERR_INVALID_ARG;
+    // the two sets of device rows the steps alternate between
+    const moe_layer_io io[2] = {{L->x, L->dY, L->y, L->dX}, *second};
+    for (const moe_layer_io &b : io) {
+        if (!b.x || !b.y || !aligned16(b.x) || !aligned16(b.y)) return MOE_ERR_INVALID_ARG;
+        if (train && (!b.dY || !b.dX || !aligned16(b.dY) || !aligned16(b.dX)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < n_steps; ++i)
+        if (!x_host[i] || !y_host[i] || (train && (!dY_host[i] || !dX_host[i])))
+            return MOE_ERR_INVALID_ARG;
+    moe_status s = check_shapes(L->T, L->d, L->E, L->k, L->I);
+    if (s != MOE_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t ci = static_cast<cudaStream_t>(copy_in_stream);
+    cudaStream_t co = static_cast<cudaStream_t>(copy_out_stream);
+    if (!ci || !co || ci == st || co == st || ci == co) return MOE_ERR_INVALID_ARG;
+    const size_t row_bytes = (size_t)L->T * L->d * sizeof(uint16_t);
+    // per set: its inputs landed, the step that uses it has finished reading
+    // them (backward, or forward without one), its outputs have been read
+    // back; and the call's start on `stream`
+    cudaEvent_t in_done[2] = {}, used[2] = {}, out_done[2] = {}, fwd_done[2] = {}, start = nullptr;
+    auto cleanup = [&](moe_status r) {
+        for (int j = 0; j < 2; ++j)
+            for (cudaEvent_t e : {in_done[j], used[j], out_done[j], fwd_done[j]})
+                if (e) cudaEventDestroy(e);
+        if (start) cudaEventDestroy(start);
+        return r;
+    };
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    for (int j = 0; j < 2; ++j)
+        for (cudaEvent_t *e : {&in_done[j], &used[j], &out_done[j], &fwd_done[j]})
+            if (!ok(cudaEventCreateWithFlags(e, cudaEventDisableTiming)))
+                return cleanup(MOE_ERR_CUDA);
+    if (!ok(cudaEventCreateWithFlags(&start, cudaEventDisableTiming))) return cleanup(MOE_ERR_CUDA);
+    // the uploads wait for whatever `stream` ran before this call
+    if (!ok(cudaEventRecord(start, st)) || !ok(cudaStreamWaitEvent(ci, start, 0)))
+        return cleanup(MOE_ERR_CUDA);
+    auto upload = [&](int i) {
+        const moe_layer_io &b = io[i & 1];
+        if (i >= 2 && !ok(cudaStreamWaitEvent(ci, used[i & 1], 0))) return false;
+        if (!ok(cudaMemcpyAsync(b.x, x_host[i], row_bytes, cudaMemcpyHostToDevice, ci)))
+            return false;
+        if (train &&
+            !ok(cudaMemcpyAsync(b.dY, dY_host[i], row_bytes, cudaMemcpyHostToDevice, ci)))
+            return false;
+        return ok(cudaEventRecord(in_done[i & 1], ci));
+    };
+    if (!upload(0)) return cleanup(MOE_ERR_CUDA);
+    for (int i = 0; i < n_steps; ++i) {
+        const int j = i & 1;
+        const moe_layer_io &b = io[j];
+        // step i's inputs are in, and the outputs step i - 2 left in this set
+        // have been read back
+        if (!ok(cudaStreamWaitEvent(st, in_done[j], 0))) return cleanup(MOE_ERR_CUDA);
+        if (i >= 2 && !ok(cudaStreamWaitEvent(st, out_done[j], 0))) return cleanup(MOE_ERR_CUDA);
+        if ((s = layer_forward(L, b.x, b.y, stream)) != MOE_OK) return cleanup(s);
+        if (!ok(cudaEventRecord(fwd_done[j], st)) || !ok(cudaStreamWaitEvent(co, fwd_done[j], 0)) ||
+            !ok(cudaMemcpyAsync(y_host[i], b.y, row_bytes, cudaMemcpyDeviceToHost, co)))
+            return cleanup(MOE_ERR_CUDA);
+        if (!train && !ok(cudaEventRecord(used[j], st))) return cleanup(MOE_ERR_CUDA);
+        // the next step's inputs go up while this step computes
+        if (i + 1 < n_steps && !upload(i + 1)) return cleanup(MOE_ERR_CUDA);
+        if (train) {
+            if ((s = layer_backward(L, b.x, b.dY, b.dX, stream)) != MOE_OK) return cleanup(s);
+            if (!ok(cudaEventRecord(used[j], st)) || !ok(cudaStreamWaitEvent(co, used[j], 0)) ||
+                !ok(cudaMemcpyAsync(dX_host[i], b.dX, row_bytes, cudaMemcpyDeviceToHost, co)))
+                return cleanup(MOE_ERR_CUDA);
+        }
+        if (!ok(cudaEventRecord(out_done[j], co))) return cleanup(MOE_ERR_CUDA);
+    }
+    // `stream` ends after every copy of the call
+    for (int j = 0; j < 2 && j < n_steps; ++j)
+        if (!ok(cudaStreamWaitEvent(st, out_done[j], 0))) return cleanup(MOE_ERR_CUDA);
+    if (!ok(cudaStreamWaitEvent(st, in_done[(n_steps - 1) & 1], 0))) return cleanup(MOE_ERR_CUDA);
     return cleanup(MOE_OK);
 }
 

@@ -306,10 +306,34 @@ class MoELayer:
         ([T,d] bf16, pinned CPU) in, y_host out; with dY_host / dX_host also the
         backward (dX out, weight gradients in self.dW13 / dW2 / dW_g).  The
         routing inputs are device tensors as for forward()."""
+        self._ensure_host_struct(dY_host is not None, bias, is_vision, logit_offset, mode,
+                                 input_ids, tid2eid)
+        self.x = self.x_dev
+        _lib.moe_layer_step_host(self._host_struct, x_host, dY_host, y_host, dX_host, stream,
+                                 copy_stream)
+
+    def steps_host(self, x_hosts, y_hosts, dY_hosts=None, dX_hosts=None, bias=None,
+                   is_vision=None, logit_offset=None, mode=MOE_ROUTE_TOPK, input_ids=None,
+                   tid2eid=None, stream=None, copy_in_stream=None, copy_out_stream=None):
+        """len(x_hosts) steps from and to host memory through
+        moe_layer_steps_host, pipelined: the next step's uploads and the last
+        step's downloads overlap the compute (lists of pinned CPU [T,d] bf16
+        tensors; dY_hosts / dX_hosts for training steps)."""
+        D = self.dims
+        self._ensure_host_struct(dY_hosts is not None, bias, is_vision, logit_offset, mode,
+                                 input_ids, tid2eid)
+        if getattr(self, "_io2", None) is None:
+            mk = lambda: torch.empty(D.T, D.d, dtype=torch.bfloat16, device=self.y.device)
+            self._io2 = dict(x=mk(), y=mk(), dY=mk() if self.backward_enabled else None,
+                             dX=mk() if self.backward_enabled else None)
+        _lib.moe_layer_steps_host(self._host_struct, self._io2, x_hosts, dY_hosts, y_hosts,
+                                  dX_hosts, stream, copy_in_stream, copy_out_stream)
+
+    def _ensure_host_struct(self, train, bias, is_vision, logit_offset, mode, input_ids,
+                            tid2eid):
         D = self.dims
         if self.mx:
-            raise RuntimeError("moe_layer_step_host runs the bf16 layer")
-        train = dY_host is not None
+            raise RuntimeError("the host-memory steps run the bf16 layer")
         if train and not self.backward_enabled:
             raise RuntimeError("layer built without backward buffers")
         key = (id(bias), id(is_vision), id(logit_offset), mode, id(input_ids), id(tid2eid))
@@ -337,9 +361,6 @@ class MoELayer:
                 dW_g=getattr(self, "dW_g", None), dW13=getattr(self, "dW13", None),
                 dW2=getattr(self, "dW2", None), ws=self.ws))
             self._host_key = key
-        self.x = self.x_dev
-        _lib.moe_layer_step_host(self._host_struct, x_host, dY_host, y_host, dX_host, stream,
-                                 copy_stream)
 
 
 __all__ = ["Dims", "MoELayer", "MOE_ROUTE_TOPK", "MOE_ROUTE_HASH"]

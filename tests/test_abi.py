@@ -31,7 +31,8 @@ def test_library_builds_and_exports_every_declared_symbol():
                                            ("moe_layer_buffers", _lib.LayerBuffers),
                                            ("moe_expert_bwd_args", _lib.ExpertBwdArgs),
                                            ("moe_expert_bwd_mx_args", _lib.ExpertBwdMxArgs),
-                                           ("moe_bwd_mx_args", _lib.BwdMxArgs)])
+                                           ("moe_bwd_mx_args", _lib.BwdMxArgs),
+                                           ("moe_layer_io", _lib.LayerIo)])
 def test_structs_match_header(struct, mirror):
     m = re.search(r"typedef struct \{((?:(?!typedef struct).)*?)\} " + struct + ";", HEADER,
                   flags=re.S)
