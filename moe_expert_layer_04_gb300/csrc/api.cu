@@ -84,6 +84,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 struct ExpertBwdWorkspace {
     uint16_t *dGU, *hw;
     float *dw_part, *gu;
+    uint8_t *tail_maps;   // per-group tensor maps of the weight gradients
     size_t bytes;
 };
 
@@ -100,6 +101,7 @@ ExpertBwdWorkspace carve_expert_bwd(uint8_t *base, int R, int d, int I, bool rec
     w.hw = reinterpret_cast<uint16_t *>(take((size_t)R * I * 2));
     w.dw_part = reinterpret_cast<float *>(take((size_t)R * dgrad2_n_tiles(I) * 4));
     if (recompute) w.gu = reinterpret_cast<float *>(take(((size_t)R + 31) / 32 * 32 * 2 * I * 4));
+    w.tail_maps = take(kWgradTailMapsBytes);
     w.bytes = off;
     (void)d;
     return w;
@@ -200,6 +202,7 @@ MxBwdWorkspace carve_mx_bwd(uint8_t *base, int G, int R, int d, int I, bool reco
 struct BwdWorkspace {
     uint16_t *dY_perm, *dGU, *hw, *dX_perm, *x_perm;
     float *gu, *dw_part, *dz_sel, *dz_row, *dwg_part;
+    uint8_t *tail_maps;   // per-group tensor maps of the weight gradients
     size_t bytes;
 };
 
@@ -221,6 +224,7 @@ BwdWorkspace carve_bwd(uint8_t *base, int T, int d, int E, int k, int I, int fla
     w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
+    w.tail_maps = take(kWgradTailMapsBytes);
     if (flags & MOE_FLAG_RECOMPUTE) {
         w.x_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
         w.gu = reinterpret_cast<float *>(take((R + 31) / 32 * 32 * 2 * I * 4));
@@ -860,12 +864,15 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
                            a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_WGRAD2)) return MOE_ERR_CUDA;
-    if ((s = launch_wgrad(w.dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, st)) != MOE_OK) return s;
+    if ((s = launch_wgrad(w.dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, w.tail_maps, st)) !=
+        MOE_OK)
+        return s;
     if (!mark(MOE_BWD_DGRAD1)) return MOE_ERR_CUDA;
     if ((s = launch_dgrad1(w.dGU, a->offsets, G, R, a->W13, d, I, w.dX_perm, st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_WGRAD1)) return MOE_ERR_CUDA;
-    if ((s = launch_wgrad(w.dGU, 2 * I, x_perm, d, a->offsets, G, R, a->dW13, st)) != MOE_OK)
+    if ((s = launch_wgrad(w.dGU, 2 * I, x_perm, d, a->offsets, G, R, a->dW13, w.tail_maps, st)) !=
+        MOE_OK)
         return s;
     if (!mark(MOE_BWD_ROUTER)) return MOE_ERR_CUDA;
     if ((s = launch_router_bwd(w.dw_part, n_part, a->slot_row, a->ids, a->weights, a->scores_sel,
@@ -929,11 +936,13 @@ moe_status moe_expert_ffn_backward(const moe_expert_bwd_args *a, void *stream) {
     if ((s = launch_dgrad2(a->dY_perm, a->offsets, G, R, a->W2, gu, a->row_weight, a->S, d, I,
                            a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
         return s;
-    if ((s = launch_wgrad(a->dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, st)) != MOE_OK)
+    if ((s = launch_wgrad(a->dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, w.tail_maps, st)) !=
+        MOE_OK)
         return s;
     if ((s = launch_dgrad1(w.dGU, a->offsets, G, R, a->W13, d, I, a->dX_perm, st)) != MOE_OK)
         return s;
-    if ((s = launch_wgrad(w.dGU, 2 * I, a->x_perm, d, a->offsets, G, R, a->dW13, st)) != MOE_OK)
+    if ((s = launch_wgrad(w.dGU, 2 * I, a->x_perm, d, a->offsets, G, R, a->dW13, w.tail_maps,
+                          st)) != MOE_OK)
         return s;
     if (a->dw_rows && a->S > 0)
         return launch_row_sum(w.dw_part, a->S, n_part, a->dw_rows, st);

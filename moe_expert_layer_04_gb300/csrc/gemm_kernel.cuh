@@ -34,9 +34,12 @@
 // barrier of the stage (cta_group::2 TMA), so the even CTA issues the MMAs
 // once both CTAs' halves have landed, and releases stages and accumulators to
 // both CTAs with one commit; every epilogue warp of the pair hands its drained
-// accumulator back to the even CTA.  In a ragged contraction's last stage the
-// even CTA also zeroes the rows past the group's end in the odd CTA's A,
-// through distributed shared memory, before its MMAs.
+// accumulator back to the even CTA.
+//
+// K-grouped tiles whose rows end inside a 16-row MMA step: the producer loads
+// that k-block's A through a copy of A's tensor map whose rows end at the
+// group's last row (built on the device before the launch), so the rows past
+// the group's end land as zeros (TMA fill) and no thread has to clear them.
 //
 // Every wait is bounded (moe_ptx.cuh): on a timeout the CTA records
 // MOE_ERR_TIMEOUT, drains its own TMA copies and MMAs, frees TMEM and exits.
@@ -54,6 +57,8 @@ struct GemmParams {
     CUtensorMap tmO;         // GM_WGRAD: fp32 output [G*M, N]; GM_DGRAD2: dGU [rows, 2I] bf16
     CUtensorMap tmO2;        // GM_DGRAD2: w h [rows, I] bf16 (boxes of 32 x 32)
     const int32_t *offsets;  // [G+1] group row offsets (grouped modes)
+    // GM_WGRAD: per group, tmA with rows ending at the group's last row
+    const CUtensorMap *tail_maps;
     int G;
     int rows;                // GM_GATE: rows of A
     int n_tiles;             // column tiles per row tile
@@ -97,21 +102,31 @@ struct ModeTraits {
     static constexpr bool ROWGROUP = !DENSE && !KGROUP;
 };
 
-// Epilogue staging of the TMA-store paths, per epilogue warp:
-//   GM_WGRAD   one 32 x 32 fp32 block (4 KB, 128-byte swizzle);
+// Epilogue staging, per epilogue warp:
+//   GM_WGRAD   one 32 x 32 fp32 block (4 KB): written one row per lane
+//              (128-byte swizzle, conflict-free), read back four rows per
+//              instruction and stored as full 128-byte lines with st.global.
+//              The staging is free again as soon as it has been read back, so
+//              one 4 KB buffer per warp keeps the SM's store path busy (TMA
+//              stores would hold it until the copy engine has read it: with
+//              one buffer per warp they reach ~20 B/cycle per SM, against the
+//              ~30 that plain coalesced stores reach).
 //   GM_DGRAD2  one 32 x 32 bf16 block (2 KB, 64-byte swizzle) that dg, du and
-//              w h pass through in turn: the smaller staging leaves room for a
-//              fourth operand stage, which the contraction over d = 4096 needs
-//              more than the epilogue needs three blocks in flight.
-constexpr int kWgradStageBufs = 1;    // fp32 staging buffers per weight-gradient warp
-constexpr int kEpiWarpBytes = kWgradStageBufs * 4096;
+//              w h pass through in turn on their way to TMA stores: the
+//              smaller staging leaves room for a fourth operand stage, which
+//              the contraction over d = 4096 needs more than the epilogue
+//              needs three blocks in flight.
+constexpr int kEpiWarpBytes = 4096;
 constexpr int kEpiWarpBytesDgrad2 = 2048;
-// Operand stages plus staging of the TMA-store path.
+// Barriers, TMEM base and abort flag of one CTA.
+constexpr int kBarBlockBytes = 256;
+// Operand stages plus epilogue staging of the staged-epilogue modes.
 constexpr int kStoreModeBudget = 216 * 1024;
 
 template <int BN, int MODE, int CL = 1>
 struct TileShape {
-    static constexpr bool TMA_STORE = (MODE == GM_WGRAD || MODE == GM_DGRAD2);
+    static constexpr bool TMA_STORE = (MODE == GM_DGRAD2);
+    static constexpr bool STAGED_EPI = (MODE == GM_WGRAD || MODE == GM_DGRAD2);
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = (BN / CL) * 64 * 2;   // this CTA's share of the B tile
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -120,7 +135,7 @@ struct TileShape {
         : MODE == GM_DGRAD2 ? ModeTraits<MODE>::NEPI * kEpiWarpBytesDgrad2
                             : 0;
     static constexpr int STAGES =
-        ((TMA_STORE ? kStoreModeBudget : kStageBudget) - EPI_BYTES) / STAGE_BYTES;
+        ((STAGED_EPI ? kStoreModeBudget : kStageBudget) - EPI_BYTES) / STAGE_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * BN;  // BN in {64, 128, 256}: a power of two
 };
 
@@ -128,7 +143,7 @@ struct TileShape {
 template <int BN, int MODE, int CL = 1>
 inline size_t gemm_smem_bytes(int G) {
     using TS = TileShape<BN, MODE, CL>;
-    return 1024 + (size_t)TS::STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256 +
+    return 1024 + (size_t)TS::STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + kBarBlockBytes +
            8 * (size_t)(G + 2);
 }
 
@@ -196,6 +211,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
         ti.kb = (ti.krows + 63) >> 6;
     }
     return ti;
+}
+
+// K-grouped modes: the group's rows end inside the last 16-row MMA step of
+// k-block kb of the tile (the rest of that step would be the next group's
+// rows).
+__device__ __forceinline__ bool kgroup_ragged(const TileInfo &ti, int kb) {
+    const int valid = ti.krows - kb * 64;
+    return valid < 64 && (valid & 15) != 0;
 }
 
 // Offset (in floats) of element (row, col) of the saved fp32 [g | u] buffer.
@@ -299,10 +322,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                   "the pair form: row- or K-grouped modes, 64-column B boxes per CTA");
     using TS = TileShape<BN, MODE, CL>;
     constexpr int STAGES = TS::STAGES;
-    // the barrier block (full/empty per stage, two tfull, two tempty, done,
-    // the TMEM base and the abort flag) must fit the 256 bytes the layout
+    // the barrier block (full and empty per stage, two tfull, two tempty,
+    // done, the TMEM base and the abort flag) must fit the bytes the layout
     // reserves
-    static_assert((2 * STAGES + 5) * 8 + 8 <= 256, "too many operand stages for the barrier block");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBlockBytes,
+                  "too many operand stages for the barrier block");
     constexpr uint32_t IDESC = idesc_bf16_f32(128 * CL, BN, MT::A_MN, MT::B_MN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -320,7 +344,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     uint64_t *done = tempty + 2;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
-    int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + TS::EPI_BYTES + 256);
+    int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + TS::EPI_BYTES +
+                                        kBarBlockBytes);
     int *mt_start = offs + (p.G + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -432,8 +457,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 for (int kb = 0; kb < ti.kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, wc)) { ok = false; break; }
                     // CL = 2: the even CTA's barrier takes both CTAs' halves of
-                    // every stage (the even CTA zeroes the rows of a ragged
-                    // contraction's tail stage in both CTAs before its MMAs)
+                    // every stage
                     const bool to_even = CL == 2 && rank == 1;
                     uint32_t bar_even = 0;
                     if (to_even)
@@ -447,8 +471,17 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                     uint8_t *a_dst = sA + s * TS::A_BYTES;
                     uint8_t *b_dst = sB + s * TS::B_BYTES;
                     if constexpr (MT::A_MN) {
-                        load(a_dst, &p.tmA, ti.m0, ti.krow0 + kb * 64);
-                        load(a_dst + 8192, &p.tmA, ti.m0 + 64, ti.krow0 + kb * 64);
+                        // a k-block whose last 16-row step reaches past the
+                        // group: A through the group's own map, whose rows end
+                        // at the group's last row, so the rows past it land as
+                        // zeros (TMA fill) and nothing has to clear them
+                        const CUtensorMap *ta = &p.tmA;
+                        if (kgroup_ragged(ti, kb)) {
+                            ta = p.tail_maps + ti.g;
+                            fence_tmap_acquire(ta);
+                        }
+                        load(a_dst, ta, ti.m0, ti.krow0 + kb * 64);
+                        load(a_dst + 8192, ta, ti.m0 + 64, ti.krow0 + kb * 64);
                     } else if (MODE == GM_FFN12 && ti.phase == 1) {
                         load(a_dst, &p.tmO, kb * 64, ti.row0);
                     } else {
@@ -534,33 +567,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         bool ok = true;
         bool issued = false;
         // ragged contraction: only the 16-row MMA steps that hold rows of this
-        // group run; inside the last one, rows past the group's end (the next
-        // group's rows) are zeroed in A.  B's rows there are finite data or TMA
-        // zero fill, so they add nothing.  In a pair the even CTA zeroes them in
-        // both CTAs' A (each CTA's output rows read only its own A).  A first
-        // form had each CTA zero its own rows and the odd CTA signal the even
-        // one through a barrier: about 2000 cycles per tail stage, most of it
-        // in that handshake.  Returns the number of 16-row steps.
-        auto zero_tail = [&](int valid) {
-            const int n_kk = (valid + 15) >> 4;
-            const int nrows = n_kk * 16 - valid;  // 0..15
-            for (int i = lane; i < 2 * nrows * 8; i += 32) {
-                const int box = i / (nrows * 8);
-                const int rem = i - box * nrows * 8;
-                uint8_t *dst = sA + s * TS::A_BYTES + box * 8192 + (valid + (rem >> 3)) * 128 +
-                               (rem & 7) * 16;
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
-                // a pair's odd CTA: the same rows of its own A, through
-                // distributed shared memory
-                if constexpr (CL == 2) st_cluster_v4(dsmem_map(dst, 1), 0u, 0u, 0u, 0u);
-            }
-            if (nrows > 0) {
-                if constexpr (CL == 2) fence_proxy_async_cluster();
-                else fence_proxy_async_smem();
-            }
-            __syncwarp();
-            return n_kk;
-        };
+        // group run; A's rows of the last one past the group's end landed as
+        // zeros (the producer loads them through the group's own tensor map).
+        // B's rows there are finite data or TMA zero fill, so they add nothing.
         for (int t = cid; ok && t < total_tiles; t += ncl, ++it) {
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
@@ -574,7 +583,6 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
             const uint32_t d_tmem = tmem_base + acc * BN;
             for (int kb = 0; kb < ti.kb; ++kb) {
                 const int valid = MT::KGROUP ? ti.krows - kb * 64 : 64;
-                const bool tail = valid < 64;
                 if constexpr (CL == 2) {
                     if (rank == 1) {
                         if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -585,10 +593,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + s * TS::A_BYTES);
                 const uint32_t b_addr = smem_u32(sB + s * TS::B_BYTES);
-                int n_kk = 4;
-                if constexpr (MT::KGROUP) {
-                    if (tail) n_kk = zero_tail(valid);
-                }
+                const int n_kk = valid < 64 ? (valid + 15) >> 4 : 4;
 
                 if (lane == 0) {
 #pragma unroll
@@ -796,32 +801,37 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 // one partial of <h, dA> per (row, column tile, warp half)
                 if (valid)
                     p.out4[((size_t)row * p.n_tiles + ti.nt) * (MT::NEPI / 4) + (ew >> 2)] = dw;
-            } else {  // GM_WGRAD: TMA stores of 32 x 32 fp32 blocks through shared memory
+            } else {  // GM_WGRAD: fp32 rows through shared memory to coalesced stores
                 uint8_t *stg = sEpi + (size_t)ew * kEpiWarpBytes;
                 const uint32_t sw = (uint32_t)(lane & 7);
                 const bool has_k = ti.kb > 0;
                 // this warp's share of the columns
                 constexpr int CW = BN / (MT::NEPI / 4);
                 const int c_lo = (ew >> 2) * CW;
-                // stage one 32 x 32 block (this thread's row) and store it with TMA
+                // rows [m0 + 32 q, m0 + 32 q + 32) of the group's output, from
+                // column nt BN
+                float *obase = static_cast<float *>(p.out) +
+                               ((size_t)ti.g * p.M + ti.m0 + q * 32) * (size_t)p.N +
+                               (size_t)ti.nt * BN;
                 auto store_block = [&](const uint32_t (&v)[32], int c) {
-                    uint8_t *buf = stg + (kWgradStageBufs == 2 ? ((c >> 5) & 1) * 4096 : 0);
-                    // the store that last used this buffer must have read it
-                    if (lane == 0) {
-                        if constexpr (kWgradStageBufs == 2) bulk_wait_group_read<1>();
-                        else bulk_wait_group_read<0>();
-                    }
-                    __syncwarp();
-                    const uint32_t row_addr = smem_u32(buf) + (uint32_t)lane * 128u;
+                    // transpose through the warp's 4 KB: rows written one per
+                    // lane (128-byte swizzle), read back four rows per
+                    // instruction, each row leaving as one full 128-byte line
+                    const uint32_t sb = smem_u32(stg);
+                    __syncwarp();   // every lane has read the previous block back
+                    const uint32_t wa = sb + (uint32_t)lane * 128u;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        st_shared_v4(row_addr + ((((uint32_t)j) ^ sw) << 4), v[4 * j], v[4 * j + 1],
+                        st_shared_v4(wa + ((((uint32_t)j) ^ sw) << 4), v[4 * j], v[4 * j + 1],
                                      v[4 * j + 2], v[4 * j + 3]);
-                    fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&p.tmO, buf, ti.nt * BN + c, ti.g * p.M + ti.m0 + q * 32);
-                        bulk_commit_group();
+                    const int ch = lane & 7;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 4 * i + (lane >> 3);
+                        const uint4 x = ld_shared_v4(sb + (uint32_t)r * 128u +
+                                                     ((uint32_t)(ch ^ (r & 7)) << 4));
+                        st_global_v4(obase + (size_t)r * p.N + c + 4 * ch, x.x, x.y, x.z, x.w);
                     }
                 };
                 // two register sets: the TMEM load of the next block is in flight
@@ -854,7 +864,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if (rank == 0) mbar_arrive(&tempty[acc]);
-                    else mbar_arrive_remote(dsmem_map(&tempty[acc], 0));
+                    else mbar_arrive_remote_relaxed(dsmem_map(&tempty[acc], 0));
                 }
             } else {
                 mbar_arrive(&tempty[acc]);

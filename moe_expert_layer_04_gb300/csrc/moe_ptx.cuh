@@ -151,6 +151,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
                  : "memory");
 }
 
+// The same arrival without release semantics: for a signal that orders no
+// memory operation of this thread (an accumulator whose tcgen05.ld reads have
+// already completed).  A release at cluster scope would first wait until every
+// earlier global store of the thread has been performed.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -499,6 +508,33 @@ __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, ui
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+// Per-group tensor maps (copies of one map with another row extent), written
+// on the device: the new extent of dimension 1 of a map in global memory, the
+// release of the writes to the tensor-map proxy, and the acquire a TMA user
+// makes before its first copy through the map.
+__device__ __forceinline__ void tmap_replace_dim1(void *tm, uint32_t rows) {
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(tm),
+                 "r"(rows)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_tmap_release() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_tmap_acquire(const void *tm) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tm) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void record_status(int *status, moe_status s) {
