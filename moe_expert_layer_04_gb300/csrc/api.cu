@@ -84,7 +84,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 struct ExpertBwdWorkspace {
     uint16_t *dGU, *hw;
     float *dw_part, *gu;
-    uint8_t *tail_maps;   // per-group tensor maps of the weight gradients
+    uint8_t *tail_maps;   // weight-gradient scratch (per-group tensor maps, group order)
     size_t bytes;
 };
 
@@ -101,7 +101,7 @@ ExpertBwdWorkspace carve_expert_bwd(uint8_t *base, int R, int d, int I, bool rec
     w.hw = reinterpret_cast<uint16_t *>(take((size_t)R * I * 2));
     w.dw_part = reinterpret_cast<float *>(take((size_t)R * dgrad2_n_tiles(I) * 4));
     if (recompute) w.gu = reinterpret_cast<float *>(take(((size_t)R + 31) / 32 * 32 * 2 * I * 4));
-    w.tail_maps = take(kWgradTailMapsBytes);
+    w.tail_maps = take(kWgradScratchBytes);
     w.bytes = off;
     (void)d;
     return w;
@@ -202,7 +202,7 @@ MxBwdWorkspace carve_mx_bwd(uint8_t *base, int G, int R, int d, int I, bool reco
 struct BwdWorkspace {
     uint16_t *dY_perm, *dGU, *hw, *dX_perm, *x_perm;
     float *gu, *dw_part, *dz_sel, *dz_row, *dwg_part;
-    uint8_t *tail_maps;   // per-group tensor maps of the weight gradients
+    uint8_t *tail_maps;   // weight-gradient scratch (per-group tensor maps, group order)
     size_t bytes;
 };
 
@@ -224,7 +224,7 @@ BwdWorkspace carve_bwd(uint8_t *base, int T, int d, int E, int k, int I, int fla
     w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
-    w.tail_maps = take(kWgradTailMapsBytes);
+    w.tail_maps = take(kWgradScratchBytes);
     if (flags & MOE_FLAG_RECOMPUTE) {
         w.x_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
         w.gu = reinterpret_cast<float *>(take((R + 31) / 32 * 32 * 2 * I * 4));

@@ -82,30 +82,44 @@ moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int
                      : launch_gemm<GM_DGRAD1, 128>(p, tiles, st);
 }
 
-// One thread per group: a copy of A's tensor map whose rows end at the
-// group's last row.  The weight-gradient producer loads a group's ragged last
-// k-block through it, so that the rows past the group land as zeros.
-__global__ void wgrad_tail_maps_kernel(const __grid_constant__ CUtensorMap tmpl,
-                                       const int32_t *offsets, int G, CUtensorMap *maps) {
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;
-    if (g >= G) return;
-    const uint4 *src = reinterpret_cast<const uint4 *>(&tmpl);
-    uint4 *dst = reinterpret_cast<uint4 *>(maps + g);
+// One CTA, a thread per group (G <= 1025):
+//   maps[g]    a copy of A's tensor map whose rows end at the group's last
+//              row; the weight-gradient producer loads a group's ragged last
+//              k-block through it, so that the rows past the group land as
+//              zeros;
+//   korder[r]  the group of rank r in order of decreasing rows (ties by
+//              index): the schedule takes the long contractions first.
+__global__ void __launch_bounds__(1024) wgrad_prep_kernel(const __grid_constant__ CUtensorMap tmpl,
+                                                         const int32_t *offsets, int G,
+                                                         CUtensorMap *maps, int32_t *korder) {
+    __shared__ int32_t rows_s[1025];
+    for (int g = threadIdx.x; g < G; g += blockDim.x) rows_s[g] = offsets[g + 1] - offsets[g];
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(&tmpl);
+        uint4 *dst = reinterpret_cast<uint4 *>(maps + g);
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) dst[i] = src[i];
-    const int end = offsets[g + 1];
-    tmap_replace_dim1(maps + g, (uint32_t)(end > 0 ? end : 1));
+        for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) dst[i] = src[i];
+        const int end = offsets[g + 1];
+        tmap_replace_dim1(maps + g, (uint32_t)(end > 0 ? end : 1));
+        const int rg = rows_s[g];
+        int rank = 0;
+        for (int h = 0; h < G; ++h) {
+            const int rh = rows_s[h];
+            rank += (rh > rg || (rh == rg && h < g)) ? 1 : 0;
+        }
+        korder[rank] = g;
+    }
     fence_tmap_release();
 }
 
 moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, const int32_t *offsets,
-                        int G, int R, float *dW, void *tail_maps, cudaStream_t st) {
+                        int G, int R, float *dW, void *scratch, cudaStream_t st) {
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     if (M % 128 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
     static_assert(sizeof(CUtensorMap) == 128, "tensor maps of 128 bytes");
-    if (G < 1 || (size_t)G * sizeof(CUtensorMap) > kWgradTailMapsBytes || !tail_maps ||
-        (reinterpret_cast<uintptr_t>(tail_maps) & 63u) != 0)
+    if (G < 1 || G > 1025 || !scratch || (reinterpret_cast<uintptr_t>(scratch) & 63u) != 0)
         return MOE_ERR_INVALID_ARG;
     // Short contractions (few rows per group) make the fp32 output stream the
     // bound: 128-wide tiles keep more operand stages in flight.  Long ones are
@@ -114,10 +128,13 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     const int BN = (long_k && N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
     if (!encode_tmap_bf16_2d(&p.tmA, A, M, R, (uint64_t)M * 2, 64, 64)) return MOE_ERR_CUDA;
     if (!encode_tmap_bf16_2d(&p.tmB, B, N, R, (uint64_t)N * 2, 64, 64)) return MOE_ERR_CUDA;
-    CUtensorMap *maps = static_cast<CUtensorMap *>(tail_maps);
-    wgrad_tail_maps_kernel<<<(G + 127) / 128, 128, 0, st>>>(p.tmA, offsets, G, maps);
+    CUtensorMap *maps = static_cast<CUtensorMap *>(scratch);
+    int32_t *korder = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(scratch) +
+                                                  (size_t)1025 * sizeof(CUtensorMap));
+    wgrad_prep_kernel<<<1, 1024, 0, st>>>(p.tmA, offsets, G, maps, korder);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     p.tail_maps = maps;
+    p.korder = korder;
     p.offsets = offsets;
     p.G = G;
     p.m_tiles = M / 128;

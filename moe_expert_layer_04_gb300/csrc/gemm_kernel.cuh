@@ -57,8 +57,10 @@ struct GemmParams {
     CUtensorMap tmO;         // GM_WGRAD: fp32 output [G*M, N]; GM_DGRAD2: dGU [rows, 2I] bf16
     CUtensorMap tmO2;        // GM_DGRAD2: w h [rows, I] bf16 (boxes of 32 x 32)
     const int32_t *offsets;  // [G+1] group row offsets (grouped modes)
-    // GM_WGRAD: per group, tmA with rows ending at the group's last row
+    // GM_WGRAD: per group, tmA with rows ending at the group's last row; the
+    // groups in order of decreasing rows (ties by index)
     const CUtensorMap *tail_maps;
+    const int32_t *korder;
     int G;
     int rows;                // GM_GATE: rows of A
     int n_tiles;             // column tiles per row tile
@@ -201,8 +203,10 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
         ti.rows_valid = min(128, offs[lo + 1] - ti.row0);
         ti.kb = ti.phase ? p.k_blocks2 : p.k_blocks;
     } else {
+        // groups by decreasing rows (mt_start holds that order here): the
+        // largest contractions first, the short ones last
         const int mp = p.m_tiles / CL;
-        ti.g = q / mp;
+        ti.g = mt_start[q / mp];
         ti.m0 = ((q % mp) * CL + rank) * 128;
         ti.row0 = 0;
         ti.rows_valid = 128;
@@ -219,6 +223,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, cons
 __device__ __forceinline__ bool kgroup_ragged(const TileInfo &ti, int kb) {
     const int valid = ti.krows - kb * 64;
     return valid < 64 && (valid & 15) != 0;
+}
+
+// The i-th tile of cluster cid (ncl clusters).  Row modes: round robin.
+// K-grouped modes, whose tiles differ in length (ordered longest first):
+// rounds of ncl tiles dealt in alternating direction, which evens out the
+// clusters' totals better than a fixed direction.
+template <int MODE>
+__device__ __forceinline__ int tile_at(int i, int cid, int ncl) {
+    if constexpr (ModeTraits<MODE>::KGROUP) return i * ncl + ((i & 1) ? ncl - 1 - cid : cid);
+    else return i * ncl + cid;
 }
 
 // Offset (in floats) of element (row, col) of the saved fp32 [g | u] buffer.
@@ -407,6 +421,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 if (g <= p.G) mt_start[g] = carry + incl - mt;
                 carry += __shfl_sync(0xffffffffu, incl, 31);
             }
+            // K-grouped modes: the group order of the schedule in place of the
+            // (unused) tile prefix
+            if constexpr (MT::KGROUP)
+                for (int g = lane; g < p.G; g += 32) mt_start[g] = p.korder[g];
         }
     }
     tc_fence_before();
@@ -438,7 +456,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
             for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             uint32_t s = 0, ph = 0;
             bool ok = true;
-            for (int t = cid; ok && t < total_tiles; t += ncl) {
+            for (int i = 0, t = tile_at<MODE>(0, cid, ncl); ok && t < total_tiles;
+                 t = tile_at<MODE>(++i, cid, ncl)) {
                 const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
                 if constexpr (MODE == GM_FFN12) {
                     if (ti.phase == 1) {
@@ -570,7 +589,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         // group run; A's rows of the last one past the group's end landed as
         // zeros (the producer loads them through the group's own tensor map).
         // B's rows there are finite data or TMA zero fill, so they add nothing.
-        for (int t = cid; ok && t < total_tiles; t += ncl, ++it) {
+        for (int t = tile_at<MODE>(0, cid, ncl); ok && t < total_tiles;
+             ++it, t = tile_at<MODE>(it, cid, ncl)) {
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
@@ -640,7 +660,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         const int ew = warp - 2;          // epilogue warp index
         const int r_local = q * 32 + lane;
         int it = 0;
-        for (int t = cid; t < total_tiles; t += ncl, ++it) {
+        for (int t = tile_at<MODE>(0, cid, ncl); t < total_tiles;
+             ++it, t = tile_at<MODE>(it, cid, ncl)) {
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;

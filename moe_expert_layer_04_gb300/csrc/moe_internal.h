@@ -85,11 +85,12 @@ int dgrad2_n_tiles(int I);
 moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int max_rows,
                          const uint16_t *W13, int d, int I, uint16_t *dX_perm, cudaStream_t st);
 // dW[g] (M x N, fp32) = A[rows of g]^T B[rows of g]; A [R, M] and B [R, N] bf16.
-// tail_maps: device scratch of kWgradTailMapsBytes (64-byte aligned) for the
-// per-group tensor maps of A; calls in order on one stream may share it.
-constexpr size_t kWgradTailMapsBytes = (size_t)1025 * 128;
+// scratch: kWgradScratchBytes of device memory (64-byte aligned) for the
+// per-group tensor maps of A and the schedule's group order; calls in order
+// on one stream may share it.
+constexpr size_t kWgradScratchBytes = (size_t)1025 * 128 + (size_t)1025 * 4;
 moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, const int32_t *offsets,
-                        int G, int R, float *dW, void *tail_maps, cudaStream_t st);
+                        int G, int R, float *dW, void *scratch, cudaStream_t st);
 
 // Row gather: dst[row] = src[row_token[row]] for the S routed rows plus the
 // T identity rows, reading each token row once (permute.cu).
