@@ -88,11 +88,14 @@ moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int
 //              k-block through it, so that the rows past the group land as
 //              zeros;
 //   korder[r]  the group of rank r in order of decreasing rows (ties by
-//              index): the schedule takes the long contractions first.
+//              index): the schedule takes the long contractions first;
+//   *counter   0, the tiles the GEMM has handed out.
 __global__ void __launch_bounds__(1024) wgrad_prep_kernel(const __grid_constant__ CUtensorMap tmpl,
                                                          const int32_t *offsets, int G,
-                                                         CUtensorMap *maps, int32_t *korder) {
+                                                         CUtensorMap *maps, int32_t *korder,
+                                                         int *counter) {
     __shared__ int32_t rows_s[1025];
+    if (threadIdx.x == 0) *counter = 0;
     for (int g = threadIdx.x; g < G; g += blockDim.x) rows_s[g] = offsets[g + 1] - offsets[g];
     __syncthreads();
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
@@ -131,10 +134,13 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     CUtensorMap *maps = static_cast<CUtensorMap *>(scratch);
     int32_t *korder = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(scratch) +
                                                   (size_t)1025 * sizeof(CUtensorMap));
-    wgrad_prep_kernel<<<1, 1024, 0, st>>>(p.tmA, offsets, G, maps, korder);
+    int *counter = reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) +
+                                           (size_t)1025 * sizeof(CUtensorMap) + (size_t)1025 * 4);
+    wgrad_prep_kernel<<<1, 1024, 0, st>>>(p.tmA, offsets, G, maps, korder, counter);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     p.tail_maps = maps;
     p.korder = korder;
+    p.tile_counter = counter;
     p.offsets = offsets;
     p.G = G;
     p.m_tiles = M / 128;

@@ -58,9 +58,11 @@ struct GemmParams {
     CUtensorMap tmO2;        // GM_DGRAD2: w h [rows, I] bf16 (boxes of 32 x 32)
     const int32_t *offsets;  // [G+1] group row offsets (grouped modes)
     // GM_WGRAD: per group, tmA with rows ending at the group's last row; the
-    // groups in order of decreasing rows (ties by index)
+    // groups in order of decreasing rows (ties by index); the tiles handed out
+    // so far (zero before the launch)
     const CUtensorMap *tail_maps;
     const int32_t *korder;
+    int *tile_counter;
     int G;
     int rows;                // GM_GATE: rows of A
     int n_tiles;             // column tiles per row tile
@@ -120,8 +122,14 @@ struct ModeTraits {
 //              needs three blocks in flight.
 constexpr int kEpiWarpBytes = 4096;
 constexpr int kEpiWarpBytesDgrad2 = 2048;
-// Barriers, TMEM base and abort flag of one CTA.
-constexpr int kBarBlockBytes = 256;
+// Barriers, TMEM base, abort flag and tile-index ring of one CTA.
+constexpr int kBarBlockBytes = 512;
+// K-grouped modes: slots of the ring that hands the run-time tile order from
+// the scheduling thread to the other roles.
+constexpr int kSchedSlots = 8;
+// Weight gradients' L2 policies: bit 0 operand loads evict-last, bit 1 the
+// fp32 output stores evict-first.
+constexpr int kWgradL2Hints = 3;
 // Operand stages plus epilogue staging of the staged-epilogue modes.
 constexpr int kStoreModeBudget = 216 * 1024;
 
@@ -225,15 +233,9 @@ __device__ __forceinline__ bool kgroup_ragged(const TileInfo &ti, int kb) {
     return valid < 64 && (valid & 15) != 0;
 }
 
-// The i-th tile of cluster cid (ncl clusters).  Row modes: round robin.
-// K-grouped modes, whose tiles differ in length (ordered longest first):
-// rounds of ncl tiles dealt in alternating direction, which evens out the
-// clusters' totals better than a fixed direction.
-template <int MODE>
-__device__ __forceinline__ int tile_at(int i, int cid, int ncl) {
-    if constexpr (ModeTraits<MODE>::KGROUP) return i * ncl + ((i & 1) ? ncl - 1 - cid : cid);
-    else return i * ncl + cid;
-}
+// The i-th tile of cluster cid (ncl clusters) in the static modes: round
+// robin (their tiles all have the same length).
+__device__ __forceinline__ int tile_at(int i, int cid, int ncl) { return i * ncl + cid; }
 
 // Offset (in floats) of element (row, col) of the saved fp32 [g | u] buffer.
 // Layout: blocks of 32 rows; inside a block, groups of 4 columns; inside a
@@ -337,9 +339,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     using TS = TileShape<BN, MODE, CL>;
     constexpr int STAGES = TS::STAGES;
     // the barrier block (full and empty per stage, two tfull, two tempty,
-    // done, the TMEM base and the abort flag) must fit the bytes the layout
-    // reserves
-    static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBlockBytes,
+    // done, sfull and sempty per ring slot, the TMEM base, the abort flag and
+    // the ring) must fit the bytes the layout reserves
+    static_assert((2 * STAGES + 5 + 2 * kSchedSlots) * 8 + 8 + 4 * kSchedSlots <= kBarBlockBytes,
                   "too many operand stages for the barrier block");
     constexpr uint32_t IDESC = idesc_bf16_f32(128 * CL, BN, MT::A_MN, MT::B_MN);
 
@@ -356,8 +358,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
-    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
+    // K-grouped modes: ring of run-time tile indices (sched), filled by the
+    // scheduling thread (sfull) and released by every other role (sempty)
+    uint64_t *sfull = done + 1;
+    uint64_t *sempty = sfull + kSchedSlots;
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(sempty + kSchedSlots);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
+    volatile int *sched = abort_s + 1;
     int *offs = reinterpret_cast<int *>(smem + STAGES * TS::STAGE_BYTES + TS::EPI_BYTES +
                                         kBarBlockBytes);
     int *mt_start = offs + (p.G + 1);
@@ -376,6 +383,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
             mbar_init(&tempty[a], CL == 1 ? 32 * MT::NEPI : 2 * MT::NEPI);
         }
         mbar_init(done, 1);
+        for (int j = 0; j < kSchedSlots; ++j) {
+            mbar_init(&sfull[j], 1);
+            // readers: CL = 2 both issuers, the odd producer and every epilogue
+            // warp of both CTAs; CL = 1 the issuer and the epilogue warps
+            mbar_init(&sempty[j], CL == 2 ? 3 + 2 * MT::NEPI : 1 + MT::NEPI);
+        }
         *abort_s = 0;
         fence_barrier_init();
     }
@@ -448,16 +461,60 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         total_tiles = p.G * (p.m_tiles / CL) * p.n_tiles;
     }
 
+    // K-grouped modes hand the tiles out at run time, in the order of the group
+    // list (longest contraction first), from a global counter.  The tiles in
+    // flight at any moment are then a window of about one tile per cluster, so
+    // the tiles that share an expert's operand rows run together and find them
+    // in L2; under a static round robin the clusters drifted apart by thousands
+    // of tiles (tile lengths differ from group to group) and those rows were
+    // read from DRAM four to seven times over.  The even CTA's producer takes
+    // each index and passes it through the ring (sched) to every other role of
+    // both CTAs; total_tiles marks the end.  Other modes deal tiles statically.
+    auto sched_put = [&](int i) -> int {
+        const int j = i % kSchedSlots;
+        if (!mbar_wait(&sempty[j], ((uint32_t)(i / kSchedSlots) & 1u) ^ 1u, wc)) return -1;
+        int t = atomicAdd(p.tile_counter, 1);
+        if (t > total_tiles) t = total_tiles;
+        sched[j] = t;
+        if constexpr (CL == 2) {
+            dsmem_st_u32(dsmem_map(const_cast<int *>(&sched[j]), 1), (uint32_t)t);
+            mbar_arrive_remote(dsmem_map(&sfull[j], 1));
+        }
+        mbar_arrive(&sfull[j]);
+        return t;
+    };
+    // a reader of slot i % kSchedSlots (mask: the lanes of the calling warp
+    // that read it; lane 0 releases the slot once the index has been read)
+    auto sched_get = [&](int i, uint32_t mask) -> int {
+        const int j = i % kSchedSlots;
+        const uint32_t sp = (uint32_t)(i / kSchedSlots) & 1u;
+        const bool got = rank == 0 ? mbar_wait(&sfull[j], sp, wc) : mbar_wait_cluster(&sfull[j], sp, wc);
+        if (!got) return -1;
+        const int t = sched[j];
+        __syncwarp(mask);
+        // the arrival depends on the index read, so it cannot pass that read
+        if (lane == 0 && t >= 0) {
+            if (rank == 0) mbar_arrive(&sempty[j]);
+            else mbar_arrive_remote_relaxed(dsmem_map(&sempty[j], 0));
+        }
+        return t;
+    };
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint64_t pol_op = policy_evict_last();
             int last_par[STAGES];
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             uint32_t s = 0, ph = 0;
             bool ok = true;
-            for (int i = 0, t = tile_at<MODE>(0, cid, ncl); ok && t < total_tiles;
-                 t = tile_at<MODE>(++i, cid, ncl)) {
+            for (int i = 0; ok; ++i) {
+                int t;
+                if constexpr (MT::KGROUP) t = rank == 0 ? sched_put(i) : sched_get(i, 1u);
+                else t = tile_at(i, cid, ncl);
+                if (t < 0) { ok = false; break; }
+                if (t >= total_tiles) break;
                 const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
                 if constexpr (MODE == GM_FFN12) {
                     if (ti.phase == 1) {
@@ -484,8 +541,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                     else
                         mbar_arrive_expect_tx(&full[s], (uint32_t)(CL * TS::STAGE_BYTES));
                     auto load = [&](void *dst, const CUtensorMap *tm, int c0, int c1) {
-                        if (to_even) tma_load_2d_pairbar(dst, tm, bar_even, c0, c1);
-                        else tma_load_2d(dst, tm, &full[s], c0, c1);
+                        if constexpr (MT::KGROUP && (kWgradL2Hints & 1)) {
+                            if (to_even) tma_load_2d_pairbar_hint(dst, tm, bar_even, c0, c1, pol_op);
+                            else tma_load_2d_hint(dst, tm, &full[s], c0, c1, pol_op);
+                        } else {
+                            if (to_even) tma_load_2d_pairbar(dst, tm, bar_even, c0, c1);
+                            else tma_load_2d(dst, tm, &full[s], c0, c1);
+                        }
                     };
                     uint8_t *a_dst = sA + s * TS::A_BYTES;
                     uint8_t *b_dst = sB + s * TS::B_BYTES;
@@ -589,8 +651,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         // group run; A's rows of the last one past the group's end landed as
         // zeros (the producer loads them through the group's own tensor map).
         // B's rows there are finite data or TMA zero fill, so they add nothing.
-        for (int t = tile_at<MODE>(0, cid, ncl); ok && t < total_tiles;
-             ++it, t = tile_at<MODE>(it, cid, ncl)) {
+        for (; ok; ++it) {
+            int t;
+            if constexpr (MT::KGROUP) t = sched_get(it, 0xffffffffu);
+            else t = tile_at(it, cid, ncl);
+            if (t < 0) { ok = false; break; }
+            if (t >= total_tiles) break;
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
@@ -660,8 +726,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         const int ew = warp - 2;          // epilogue warp index
         const int r_local = q * 32 + lane;
         int it = 0;
-        for (int t = tile_at<MODE>(0, cid, ncl); t < total_tiles;
-             ++it, t = tile_at<MODE>(it, cid, ncl)) {
+        for (;; ++it) {
+            int t;
+            if constexpr (MT::KGROUP) t = sched_get(it, 0xffffffffu);
+            else t = tile_at(it, cid, ncl);
+            if (t < 0 || t >= total_tiles) break;
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);
             const uint32_t acc = it & 1;
             const uint32_t aph = (it >> 1) & 1;
@@ -831,6 +900,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                 const int c_lo = (ew >> 2) * CW;
                 // rows [m0 + 32 q, m0 + 32 q + 32) of the group's output, from
                 // column nt BN
+                const uint64_t pol_out = policy_evict_first();
                 float *obase = static_cast<float *>(p.out) +
                                ((size_t)ti.g * p.M + ti.m0 + q * 32) * (size_t)p.N +
                                (size_t)ti.nt * BN;
@@ -852,7 +922,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
                         const int r = 4 * i + (lane >> 3);
                         const uint4 x = ld_shared_v4(sb + (uint32_t)r * 128u +
                                                      ((uint32_t)(ch ^ (r & 7)) << 4));
-                        st_global_v4(obase + (size_t)r * p.N + c + 4 * ch, x.x, x.y, x.z, x.w);
+                        if constexpr (kWgradL2Hints & 2)
+                            st_global_v4_hint(obase + (size_t)r * p.N + c + 4 * ch, x.x, x.y, x.z,
+                                              x.w, pol_out);
+                        else
+                            st_global_v4(obase + (size_t)r * p.N + c + 4 * ch, x.x, x.y, x.z, x.w);
                     }
                 };
                 // two register sets: the TMEM load of the next block is in flight

@@ -86,9 +86,9 @@ moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int
                          const uint16_t *W13, int d, int I, uint16_t *dX_perm, cudaStream_t st);
 // dW[g] (M x N, fp32) = A[rows of g]^T B[rows of g]; A [R, M] and B [R, N] bf16.
 // scratch: kWgradScratchBytes of device memory (64-byte aligned) for the
-// per-group tensor maps of A and the schedule's group order; calls in order
-// on one stream may share it.
-constexpr size_t kWgradScratchBytes = (size_t)1025 * 128 + (size_t)1025 * 4;
+// per-group tensor maps of A, the schedule's group order and its tile
+// counter; calls in order on one stream may share it.
+constexpr size_t kWgradScratchBytes = (size_t)1025 * 128 + (size_t)1025 * 4 + 64;
 moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, const int32_t *offsets,
                         int G, int R, float *dW, void *scratch, cudaStream_t st);
 

@@ -119,6 +119,17 @@ __device__ __forceinline__ void tma_load_2d_pairbar(void *smem_dst, const CUtens
         : "memory");
 }
 
+// tma_load_2d_pairbar with an L2 cache policy (createpolicy result).
+__device__ __forceinline__ void tma_load_2d_pairbar_hint(void *smem_dst, const CUtensorMap *tm,
+                                                         uint32_t bar, int c0, int c1,
+                                                         uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -526,6 +537,13 @@ __device__ __forceinline__ void fence_tmap_release() {
 
 __device__ __forceinline__ void fence_tmap_acquire(const void *tm) {
     asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tm) : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4_hint(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
