@@ -861,7 +861,8 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
     if ((s = launch_gather_rows(a->dY, a->slot_row, T, d, k, w.dY_perm, st)) != MOE_OK) return s;
     if (!mark(MOE_BWD_DGRAD2)) return MOE_ERR_CUDA;
     if ((s = launch_dgrad2(w.dY_perm, a->offsets, G, R, a->W2, gu, a->row_weight, S, d, I,
-                           a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
+                           a->clamp, w.dGU, w.hw, w.dw_part, &n_part,
+                           scratch_tile_counter(w.tail_maps), st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_WGRAD2)) return MOE_ERR_CUDA;
     if ((s = launch_wgrad(w.dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, w.tail_maps, st)) !=
@@ -934,7 +935,8 @@ moe_status moe_expert_ffn_backward(const moe_expert_bwd_args *a, void *stream) {
     }
     int n_part = 0;
     if ((s = launch_dgrad2(a->dY_perm, a->offsets, G, R, a->W2, gu, a->row_weight, a->S, d, I,
-                           a->clamp, w.dGU, w.hw, w.dw_part, &n_part, st)) != MOE_OK)
+                           a->clamp, w.dGU, w.hw, w.dw_part, &n_part,
+                           scratch_tile_counter(w.tail_maps), st)) != MOE_OK)
         return s;
     if ((s = launch_wgrad(a->dY_perm, d, w.hw, I, a->offsets, G, R, a->dW2, w.tail_maps, st)) !=
         MOE_OK)

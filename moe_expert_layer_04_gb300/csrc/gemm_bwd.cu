@@ -21,10 +21,14 @@ int dgrad2_n_tiles(int I) { return I / dgrad2_bn(I) * 2; }
 moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G, int max_rows,
                          const uint16_t *W2, const float *gu, const float *row_w, int S,
                          int d, int I, float clamp, uint16_t *dGU, uint16_t *hw, float *dw_part,
-                         int *dw_tiles, cudaStream_t st) {
+                         int *dw_tiles, int *tile_counter, cudaStream_t st) {
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     const int BN = dgrad2_bn(I);
+    // tiles handed out at run time (see the grouped GEMM): the counter starts at 0
+    if (!tile_counter) return MOE_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    p.tile_counter = tile_counter;
     if (!encode_tmap_bf16_2d(&p.tmA, dY_perm, d, max_rows, (uint64_t)d * 2, 64, 128))
         return MOE_ERR_CUDA;
     // W2 as [G*d rows (contraction), I columns (output)], MN-major boxes
@@ -134,8 +138,7 @@ moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, cons
     CUtensorMap *maps = static_cast<CUtensorMap *>(scratch);
     int32_t *korder = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(scratch) +
                                                   (size_t)1025 * sizeof(CUtensorMap));
-    int *counter = reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) +
-                                           (size_t)1025 * sizeof(CUtensorMap) + (size_t)1025 * 4);
+    int *counter = scratch_tile_counter(scratch);
     wgrad_prep_kernel<<<1, 1024, 0, st>>>(p.tmA, offsets, G, maps, korder, counter);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     p.tail_maps = maps;

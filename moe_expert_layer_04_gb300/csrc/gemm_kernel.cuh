@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
     static_assert((2 * STAGES + 5 + 2 * kSchedSlots) * 8 + 8 + 4 * kSchedSlots <= kBarBlockBytes,
                   "too many operand stages for the barrier block");
     constexpr uint32_t IDESC = idesc_bf16_f32(128 * CL, BN, MT::A_MN, MT::B_MN);
+    // tiles handed out at run time through the ring (see below): the K-grouped
+    // weight gradients and dgrad 2, whose clusters otherwise drift apart
+    constexpr bool DYN = MT::KGROUP || MODE == GM_DGRAD2;
 
     extern __shared__ uint8_t smem_raw[];
     // aligned to 1024 B by pointer arithmetic on the shared array itself, so
@@ -461,13 +464,14 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         total_tiles = p.G * (p.m_tiles / CL) * p.n_tiles;
     }
 
-    // K-grouped modes hand the tiles out at run time, in the order of the group
-    // list (longest contraction first), from a global counter.  The tiles in
-    // flight at any moment are then a window of about one tile per cluster, so
-    // the tiles that share an expert's operand rows run together and find them
-    // in L2; under a static round robin the clusters drifted apart by thousands
-    // of tiles (tile lengths differ from group to group) and those rows were
-    // read from DRAM four to seven times over.  The even CTA's producer takes
+    // DYN modes hand the tiles out at run time, in tile order (K-grouped: the
+    // group list, longest contraction first), from a global counter.  The tiles
+    // in flight at any moment are then a window of about one tile per cluster,
+    // so the tiles that share an expert's operand rows run together and find
+    // them in L2.  Under a static round robin the clusters drifted apart (the
+    // weight gradients' tile lengths differ from group to group; dgrad 2's
+    // epilogue time varies) by thousands, or hundreds, of tiles, and those rows
+    // were read from DRAM several times over.  The even CTA's producer takes
     // each index and passes it through the ring (sched) to every other role of
     // both CTAs; total_tiles marks the end.  Other modes deal tiles statically.
     auto sched_put = [&](int i) -> int {
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
             bool ok = true;
             for (int i = 0; ok; ++i) {
                 int t;
-                if constexpr (MT::KGROUP) t = rank == 0 ? sched_put(i) : sched_get(i, 1u);
+                if constexpr (DYN) t = rank == 0 ? sched_put(i) : sched_get(i, 1u);
                 else t = tile_at(i, cid, ncl);
                 if (t < 0) { ok = false; break; }
                 if (t >= total_tiles) break;
@@ -653,7 +657,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         // B's rows there are finite data or TMA zero fill, so they add nothing.
         for (; ok; ++it) {
             int t;
-            if constexpr (MT::KGROUP) t = sched_get(it, 0xffffffffu);
+            if constexpr (DYN) t = sched_get(it, 0xffffffffu);
             else t = tile_at(it, cid, ncl);
             if (t < 0) { ok = false; break; }
             if (t >= total_tiles) break;
@@ -728,7 +732,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::THREADS, 1)
         int it = 0;
         for (;; ++it) {
             int t;
-            if constexpr (MT::KGROUP) t = sched_get(it, 0xffffffffu);
+            if constexpr (DYN) t = sched_get(it, 0xffffffffu);
             else t = tile_at(it, cid, ncl);
             if (t < 0 || t >= total_tiles) break;
             const TileInfo ti = decode_tile<MODE, BN, CL>(p, t, mt_start, offs, rank);

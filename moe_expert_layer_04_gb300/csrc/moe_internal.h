@@ -80,7 +80,7 @@ moe_status launch_ffn2(const uint16_t *h, const int32_t *offsets, int G, int max
 moe_status launch_dgrad2(const uint16_t *dY_perm, const int32_t *offsets, int G, int max_rows,
                          const uint16_t *W2, const float *gu, const float *row_w, int S,
                          int d, int I, float clamp, uint16_t *dGU, uint16_t *hw, float *dw_part,
-                         int *dw_tiles, cudaStream_t st);
+                         int *dw_tiles, int *tile_counter, cudaStream_t st);
 int dgrad2_n_tiles(int I);
 moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int max_rows,
                          const uint16_t *W13, int d, int I, uint16_t *dX_perm, cudaStream_t st);
@@ -89,6 +89,11 @@ moe_status launch_dgrad1(const uint16_t *dGU, const int32_t *offsets, int G, int
 // per-group tensor maps of A, the schedule's group order and its tile
 // counter; calls in order on one stream may share it.
 constexpr size_t kWgradScratchBytes = (size_t)1025 * 128 + (size_t)1025 * 4 + 64;
+// The tile counter inside that scratch (also dgrad 2's, which runs first).
+inline int *scratch_tile_counter(void *scratch) {
+    return reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) + (size_t)1025 * 128 +
+                                   (size_t)1025 * 4);
+}
 moe_status launch_wgrad(const uint16_t *A, int M, const uint16_t *B, int N, const int32_t *offsets,
                         int G, int R, float *dW, void *scratch, cudaStream_t st);
 
