@@ -43,6 +43,18 @@ FALLBACK_HBM_GBS = 6800.0
 # proportion to the experts streamed, so a full launch is this ratio times its
 # algorithmic bytes.
 GEMM1_DRAM_PER_ALGORITHMIC_BYTE = 1.0154
+# DRAM bytes (read + write) per launch of each grouped-GEMM kernel at the
+# 64K-token slice, averaged over the kernel's launches in one step: one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum, one pass) of the
+# current kernels, command and per-launch figures in
+# profiles/dram_traffic_long_slice_fwd_bwd.md.
+LONG_SLICE_DRAM_BYTES_PER_LAUNCH = {
+    "expert GEMM 1": (21.61e9 + 30.63e9) / 2,   # forward; recompute (saves g|u)
+    "weight gradients": (19.92e9 + 41.26e9) / 2,  # dW2; dW13
+    "dgrad 1": 23.99e9,
+    "dgrad 2": 24.07e9,
+    "expert GEMM 2": 12.06e9,
+}
 FALLBACK_BF16_TFLOPS = 1900.0
 # library kernels of one forward: routing (one fused gate + route kernel, or the
 # gate GEMM and the routing kernel), rank, scan, scatter, gather, GEMM1, GEMM2,
@@ -929,9 +941,16 @@ def run_headline(args, weights, dev, world, hbm, bf16_sus):
     name = max(groups, key=lambda g: tot(groups[g], "ms"))
     g_ms, g_fl, n_launch = tot(groups[name], "ms"), tot(groups[name], "flops"), len(groups[name])
     achieved = g_fl / (g_ms / 1e3) / 1e12
+    traffic = None
+    if wl.name == HEADLINE and not args.tokens and not args.experts:
+        traffic = next((round(v) for k, v in LONG_SLICE_DRAM_BYTES_PER_LAUNCH.items()
+                        if name.startswith(k)), None)
     roofline = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": bf16_sus, "unit": "TFLOP/s", "frac": round(achieved / bf16_sus, 4),
-                "traffic": None, "launches_per_step": n_launch,
+                "traffic": traffic,
+                "traffic_source": "ncu dram read+write per launch at this workload "
+                                  "(profiles/dram_traffic_long_slice_fwd_bwd.md)",
+                "launches_per_step": n_launch,
                 "flops_per_launch": int(g_fl / n_launch),
                 "ms_per_launch": round(g_ms / n_launch, 4),
                 "peak_source": "measured sustained bf16 (cuBLAS loop under the power cap)"}
