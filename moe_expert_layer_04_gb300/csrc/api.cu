@@ -145,6 +145,9 @@ struct MxBwdWorkspace {
     // sf_slots 16-byte scale slots per column), and the groups' padded
     // contraction plan
     int32_t *kofs, *sofs;
+    // the weight gradients' group order and the run-time tile counter
+    int32_t *korder;
+    int *tile_counter;
     uint8_t *dYt, *dYtsf, *hwt, *hwtsf, *dGUt, *dGUtsf, *xt, *xtsf;
     int k_chunks, sf_slots;
     RouterBwdWorkspace router;
@@ -173,6 +176,8 @@ MxBwdWorkspace carve_mx_bwd(uint8_t *base, int G, int R, int d, int I, bool reco
     w.sf_slots = (int)((kmax / 32 + 16LL * G) / 16 + 1);
     w.kofs = reinterpret_cast<int32_t *>(take((size_t)(G + 1) * 4));
     w.sofs = reinterpret_cast<int32_t *>(take((size_t)(G + 1) * 4));
+    w.korder = reinterpret_cast<int32_t *>(take((size_t)(G + 1) * 4));
+    w.tile_counter = reinterpret_cast<int *>(take(64));
     const size_t kp = (size_t)w.k_chunks * 128, sp = (size_t)w.sf_slots * 16;
     w.dYt = take((size_t)d * kp);
     w.dYtsf = take((size_t)d * sp);
@@ -628,7 +633,7 @@ moe_status run_mx_expert_bwd(const MxExpertBwd &a, const MxBwdWorkspace &w, int 
     if (!mark(MOE_BWD_DGRAD2)) return MOE_ERR_CUDA;
     if ((s = launch_mx_dgrad2(a.dY_perm_q, a.dY_perm_sf, a.offsets, a.G, a.R, a.W2t_q, a.W2t_sf,
                               gu, hq, hsf, a.row_weight, a.S, a.d, a.I, a.clamp, w.dGU, w.dGUq,
-                              w.dGUsf, w.hw, w.dw_part, n_part, st)) != MOE_OK)
+                              w.dGUsf, w.hw, w.dw_part, n_part, w.tile_counter, st)) != MOE_OK)
         return s;
     // the weight gradients in the MX training form: their operands quantised
     // along each group's rows (padded to 128), stored transposed
@@ -641,7 +646,8 @@ moe_status run_mx_expert_bwd(const MxExpertBwd &a, const MxBwdWorkspace &w, int 
     if ((s = rows_t(a.dY_rows, a.dY_idx, a.d, w.dYt, w.dYtsf)) != MOE_OK) return s;
     if ((s = rows_t(w.hw, nullptr, a.I, w.hwt, w.hwtsf)) != MOE_OK) return s;
     if ((s = launch_mx_wgrad(w.dYt, w.dYtsf, w.hwt, w.hwtsf, w.kofs, w.sofs, a.G, a.d, a.I,
-                             w.k_chunks, w.sf_slots, a.dW2, st)) != MOE_OK)
+                             w.k_chunks, w.sf_slots, a.dW2, w.korder, w.tile_counter, st)) !=
+        MOE_OK)
         return s;
     if (!mark(MOE_BWD_DGRAD1)) return MOE_ERR_CUDA;
     // dgrad 1 is MX GEMM 2 with the contraction over 2I and no row weight
@@ -652,7 +658,7 @@ moe_status run_mx_expert_bwd(const MxExpertBwd &a, const MxBwdWorkspace &w, int 
     if ((s = rows_t(w.dGU, nullptr, 2 * a.I, w.dGUt, w.dGUtsf)) != MOE_OK) return s;
     if ((s = rows_t(a.x_perm, nullptr, a.d, w.xt, w.xtsf)) != MOE_OK) return s;
     return launch_mx_wgrad(w.dGUt, w.dGUtsf, w.xt, w.xtsf, w.kofs, w.sofs, a.G, 2 * a.I, a.d,
-                           w.k_chunks, w.sf_slots, a.dW13, st);
+                           w.k_chunks, w.sf_slots, a.dW13, w.korder, w.tile_counter, st);
 }
 
 }  // namespace

@@ -107,6 +107,11 @@ struct MxParams {
     int M;                 // weight gradients: output rows per group (A rows)
     const int32_t *sofs;   // weight gradients: [G+1] first scale byte of each group
                            // (offsets holds the first code column, kofs)
+    // weight gradients and dgrad 2: tiles handed out at run time (as in the
+    // bf16 grouped GEMM) from this counter, zero before the launch; the
+    // weight gradients take the groups in korder (longest contraction first)
+    int *tile_counter;
+    const int32_t *korder;
     int *status;
     long long wait_limit;
 };
@@ -146,7 +151,9 @@ struct MxShape {
                                                   : 0;
     static constexpr int FIXED = STAGES * STAGE + kMxSfSlots * SF_SLOT + EPI;
     static_assert(SF_COL0 + SF_COLS * STAGES <= kMxTmemCols, "tensor memory columns");
-    static_assert((4 * STAGES + 2 * kMxSfSlots + 5) * 8 + 8 <= kMxBarBytes, "barrier block");
+    static_assert((4 * STAGES + 2 * kMxSfSlots + 5 + 2 * kSchedSlots) * 8 + 8 + 4 * kSchedSlots <=
+                      kMxBarBytes,
+                  "barrier block");
 };
 
 template <int MODE, int BN>
@@ -179,8 +186,9 @@ __device__ __forceinline__ TileInfo mx_tile(const MxParams &p, int t, const int 
         // group's padded rows: code columns [offs[g], offs[g + 1]), scale
         // bytes from mt_start[g]
         const int mp = p.M / 128;
-        ti.g = q / mp;
-        ti.m0 = (q - ti.g * mp) * 128;
+        const int qg = q / mp;   // the group's rank in the schedule
+        ti.g = p.korder ? p.korder[qg] : qg;
+        ti.m0 = (q - qg * mp) * 128;
         ti.krow0 = offs[ti.g];
         ti.krows = mt_start[ti.g];
         ti.kb = (offs[ti.g + 1] - offs[ti.g]) / 128;
@@ -222,8 +230,11 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
     uint64_t *tfull = sfempty + kMxSfSlots;
     uint64_t *tempty = tfull + 2;
     uint64_t *done = tempty + 2;
-    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *sfull = done + 1;              // ring of run-time tile indices
+    uint64_t *sempty = sfull + kSchedSlots;
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(sempty + kSchedSlots);
     volatile int *abort_s = reinterpret_cast<volatile int *>(tmem_base_s + 1);
+    volatile int *sched = abort_s + 1;
     int *offs = reinterpret_cast<int *>(smem + SH::FIXED + kMxBarBytes);
     int *mt_start = offs + (p.G + 1);
 
@@ -246,6 +257,11 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
             mbar_init(&tempty[a], 32 * NEPI);
         }
         mbar_init(done, 1);
+        for (int j = 0; j < kSchedSlots; ++j) {
+            mbar_init(&sfull[j], 1);
+            // readers: the MMA issuer, the scale writers and the epilogue warps
+            mbar_init(&sempty[j], 1 + kMxSfWarps + NEPI);
+        }
         *abort_s = 0;
         fence_barrier_init();
     }
@@ -304,6 +320,32 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
     const int total_tiles =
         MODE == MX_WGRAD ? p.G * (p.M / 128) * p.n_tiles : mt_start[p.G] * p.n_tiles;
 
+    // Run-time tile order (the weight gradients and dgrad 2, when the launcher
+    // passes a counter): the producer takes each index from the counter and
+    // passes it to the other roles through the ring, as in the bf16 grouped
+    // GEMM, so the tiles in flight stay a window of about one per CTA and
+    // share their operand rows in L2.  Otherwise a static round robin.
+    const bool DYN = (MODE == MX_WGRAD || MODE == MX_DGRAD2) && p.tile_counter != nullptr;
+    auto next_tile = [&](int i, bool writer, uint32_t mask) -> int {
+        if (!DYN) return blockIdx.x + i * gridDim.x;
+        const int j = i % kSchedSlots;
+        const uint32_t sp = (uint32_t)(i / kSchedSlots) & 1u;
+        if (writer) {
+            if (!mbar_wait(&sempty[j], sp ^ 1u, wc)) return -1;
+            int t = atomicAdd(p.tile_counter, 1);
+            if (t > total_tiles) t = total_tiles;
+            sched[j] = t;
+            mbar_arrive(&sfull[j]);
+            return t;
+        }
+        if (!mbar_wait(&sfull[j], sp, wc)) return -1;
+        const int t = sched[j];
+        __syncwarp(mask);
+        // the arrival depends on the index read, so it cannot pass that read
+        if (lane == 0 && t >= 0) mbar_arrive(&sempty[j]);
+        return t;
+    };
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -314,7 +356,10 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
             for (int i = 0; i < kMxSfSlots; ++i) last_sf[i] = -1;
             uint32_t s = 0, ph = 0, js = 0, phs = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            for (int i = 0; ok; ++i) {
+                const int t = next_tile(i, true, 1u);
+                if (t < 0) { ok = false; break; }
+                if (t >= total_tiles) break;
                 const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
                 // B rows of the tile: GEMM 1 the gate rows and the up rows of its
                 // BN/2 h columns, GEMM 2 BN consecutive output rows
@@ -384,7 +429,10 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         uint32_t s = 0, ph = 0;
         int it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
+        for (; ok; ++it) {
+            const int t = next_tile(it, false, 0xffffffffu);
+            if (t < 0) { ok = false; break; }
+            if (t >= total_tiles) break;
             const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
             const uint32_t acc = NACC == 2 ? (it & 1) : 0;
             const uint32_t aph = NACC == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -432,7 +480,9 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t s = 0, ph = 0, js = 0, phs = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        for (int i = 0; ok; ++i) {
+            const int t = next_tile(i, false, 0xffffffffu);
+            if (t < 0 || t >= total_tiles) break;
             const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
             for (int kb = 0; kb < ti.kb; ++kb) {
                 if ((kb & 3) == 0 && !mbar_wait(&sffull[js], phs, wc)) { ok = false; break; }
@@ -475,7 +525,9 @@ __global__ void __launch_bounds__(MxShape<MODE, BN>::THREADS, 1)
         constexpr int NPART = NEPI / 4;
         const int r_local = q * 32 + lane;
         int it = 0;
-        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        for (;; ++it) {
+            const int t = next_tile(it, false, 0xffffffffu);
+            if (t < 0 || t >= total_tiles) break;
             const TileInfo ti = mx_tile<MODE>(p, t, mt_start, offs);
             const uint32_t acc = NACC == 2 ? (it & 1) : 0;
             const uint32_t aph = NACC == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -797,11 +849,15 @@ moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32
                             const float *gu, const uint8_t *hq, const uint8_t *hsf,
                             const float *row_w, int S, int d, int I, float clamp, uint16_t *dGU,
                             uint8_t *dGUq, uint8_t *dGUsf, uint16_t *hw, float *dw_part,
-                            int *n_part, cudaStream_t st) {
+                            int *n_part, int *tile_counter, cudaStream_t st) {
     if (d % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
     constexpr int BN = 128;   // two accumulators: a tile's epilogue overlaps the next's MMAs
     MxParams p;
     std::memset(&p, 0, sizeof p);
+    // tiles handed out at run time from a counter that starts at 0
+    if (!tile_counter) return MOE_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    p.tile_counter = tile_counter;
     const int sfd = mx_sf_pitch(d);
     const uint64_t brows = (uint64_t)G * I;
     if (!encode_tmap_u8_2d(&p.tmA, dYq, d, max_rows, d, 128, 128, 128) ||
@@ -836,13 +892,39 @@ moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32
     return launch_mx<MX_DGRAD2, BN>(p, tiles, st);
 }
 
+// One CTA, a thread per group (G <= 1025): korder, the groups in order of
+// decreasing padded rows (ties by index), and the tile counter set to 0.
+__global__ void __launch_bounds__(1024) mx_wgrad_order_kernel(const int32_t *kofs, int G,
+                                                             int32_t *korder, int *counter) {
+    __shared__ int32_t rows_s[1025];
+    if (threadIdx.x == 0) *counter = 0;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) rows_s[g] = kofs[g + 1] - kofs[g];
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const int rg = rows_s[g];
+        int rank = 0;
+        for (int h = 0; h < G; ++h) {
+            const int rh = rows_s[h];
+            rank += (rh > rg || (rh == rg && h < g)) ? 1 : 0;
+        }
+        korder[rank] = g;
+    }
+}
+
 moe_status launch_mx_wgrad(const uint8_t *At, const uint8_t *Atsf, const uint8_t *Bt,
                            const uint8_t *Btsf, const int32_t *kofs, const int32_t *sofs, int G,
-                           int M, int N, int k_chunks, int sf_slots, float *dW, cudaStream_t st) {
+                           int M, int N, int k_chunks, int sf_slots, float *dW, int32_t *korder,
+                           int *tile_counter, cudaStream_t st) {
     if (M % 128 != 0 || N % 128 != 0 || k_chunks < 1 || sf_slots < 1) return MOE_ERR_UNSUPPORTED;
+    if (G < 1 || G > 1025 || !korder || !tile_counter) return MOE_ERR_INVALID_ARG;
     constexpr int BN = 128;
     MxParams p;
     std::memset(&p, 0, sizeof p);
+    // longest contraction first, tiles handed out at run time
+    mx_wgrad_order_kernel<<<1, 1024, 0, st>>>(kofs, G, korder, tile_counter);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    p.korder = korder;
+    p.tile_counter = tile_counter;
     // K-chunk-major operands: [chunks x rows, 128 codes] and [slots x rows, 16 scale codes]
     if (!encode_tmap_u8_2d(&p.tmA, At, 128, (uint64_t)k_chunks * M, 128, 128, 128, 128) ||
         !encode_tmap_u8_2d(&p.tmB, Bt, 128, (uint64_t)k_chunks * N, 128, 128, BN, 128) ||

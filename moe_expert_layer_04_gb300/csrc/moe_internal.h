@@ -136,7 +136,8 @@ moe_status launch_mx_quantize_rows_t(const uint16_t *src, const int32_t *row_idx
                                      uint8_t *qt, uint8_t *sft, cudaStream_t st);
 moe_status launch_mx_wgrad(const uint8_t *At, const uint8_t *Atsf, const uint8_t *Bt,
                            const uint8_t *Btsf, const int32_t *kofs, const int32_t *sofs, int G,
-                           int M, int N, int k_chunks, int sf_slots, float *dW, cudaStream_t st);
+                           int M, int N, int k_chunks, int sf_slots, float *dW, int32_t *korder,
+                           int *tile_counter, cudaStream_t st);
 // Partials of <h~, dA> per row written by launch_mx_dgrad2.
 int mx_dgrad2_n_part(int I);
 moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32_t *offsets, int G,
@@ -144,7 +145,7 @@ moe_status launch_mx_dgrad2(const uint8_t *dYq, const uint8_t *dYsf, const int32
                             const float *gu, const uint8_t *hq, const uint8_t *hsf,
                             const float *row_w, int S, int d, int I, float clamp, uint16_t *dGU,
                             uint8_t *dGUq, uint8_t *dGUsf, uint16_t *hw, float *dw_part,
-                            int *n_part, cudaStream_t st);
+                            int *n_part, int *tile_counter, cudaStream_t st);
 
 moe_status launch_selftest_timeout(long long limit, cudaStream_t st);
 
