@@ -39,10 +39,10 @@ METRIC = ("MoE layer tokens/s (fwd, fwd+bwd) at 1 GB300; grouped-GEMM % of BF16 
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per algorithmic byte of expert GEMM 1, from an ncu
 # capture of the current kernel on a small case of the same workload
-# (T=640, E=64: 2.270 GB measured for 2.236 GB algorithmic); traffic grows in
+# (T=640, E=64: 2.262 GB measured for 2.236 GB algorithmic); traffic grows in
 # proportion to the experts streamed, so a full launch is this ratio times its
 # algorithmic bytes.
-GEMM1_DRAM_PER_ALGORITHMIC_BYTE = 1.0154
+GEMM1_DRAM_PER_ALGORITHMIC_BYTE = 1.0116
 # DRAM bytes (read + write) per launch of each grouped-GEMM kernel at the
 # 64K-token slice, averaged over the kernel's launches in one step: one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum, one pass) of the
