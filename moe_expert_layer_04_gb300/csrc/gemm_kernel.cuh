@@ -1,14 +1,16 @@
 // gemm_kernel.cuh -- persistent tcgen05 grouped GEMM for the expert matmuls.
 //
-// One CTA per SM, 6 warps:
+// One CTA per SM (or a 2-SM pair per SM pair), 2 + NEPI warps:
 //   warp 0      TMA producer (one elected thread): A and B tiles of 64 K
 //               elements per stage into 128-byte-swizzled shared memory.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma (M = 128, N = BN,
 //               K = 16) from shared-memory descriptors into a fp32
 //               accumulator in TMEM; two accumulators so that the epilogue of
 //               one tile overlaps the main loop of the next.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = row),
-//               mode-specific arithmetic, direct global stores.
+//   warps 2..   epilogue (4 warps, 8 for dgrad 2): tcgen05.ld of the
+//               accumulator (thread = row), mode-specific arithmetic, direct
+//               global stores or shared-memory staging (TMA stores for dgrad
+//               2, a transpose to coalesced stores for the weight gradients).
 //
 // Tiles are 128 rows x BN columns.  Three tile spaces:
 //   dense        (GM_GATE)   rows of A in order;
@@ -22,8 +24,11 @@
 // expert GEMM 2 in one launch: a GEMM-2 row tile's producer waits (bounded)
 // until every epilogue warp of the GEMM-1 tiles of that row tile has
 // released its h rows through a counter.
-// Tiles are handed out round-robin (tile = blockIdx.x + i * gridDim.x), so
-// the schedule is static and the results are deterministic.
+// The forward GEMMs and dgrad 1, whose tiles all cost the same, take them in
+// a static round robin (tile = cluster + i * clusters); dgrad 2 and the weight
+// gradients take them at run time from a global counter (see DYN in the
+// kernel).  Either way each output tile is computed whole by one CTA (or
+// pair) in a fixed contraction order, so the results are deterministic.
 //
 // CL = 2 (row-grouped and K-grouped modes): clusters of two CTAs run 2-SM
 // MMAs (tcgen05.mma.cta_group::2, M = 256).  The pair computes two 128-row
@@ -124,8 +129,8 @@ constexpr int kEpiWarpBytes = 4096;
 constexpr int kEpiWarpBytesDgrad2 = 2048;
 // Barriers, TMEM base, abort flag and tile-index ring of one CTA.
 constexpr int kBarBlockBytes = 512;
-// K-grouped modes: slots of the ring that hands the run-time tile order from
-// the scheduling thread to the other roles.
+// Run-time tile order (dgrad 2, the weight gradients): slots of the ring that
+// hands each tile index from the scheduling thread to the other roles.
 constexpr int kSchedSlots = 8;
 // Weight gradients' L2 policies: bit 0 operand loads evict-last, bit 1 the
 // fp32 output stores evict-first.
