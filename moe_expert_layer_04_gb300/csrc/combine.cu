@@ -48,8 +48,11 @@ __device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
 // in a row.  The sum is fp32 in a fixed order: shared row first, then the
 // slots in order.  KM = 0 is the generic form for any k (one row at a time).
 // When dz != nullptr the gate term sum_j dz_j W_g[ids_j] is added as well (the
-// dX assembly of the backward).
-template <int KM>
+// dX assembly of the backward), after the slots.  GATE = true (KM > 0) is that
+// form: the slot rows, the gate's ids and dz are read together, then all row
+// loads (k + 1 rows of dX_perm, k rows of W_g) are issued before the first
+// add, so the gate term costs no extra memory latency.
+template <int KM, bool GATE = false>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ yp,
                                                       const int32_t *__restrict__ slot_row,
                                                       int T, int vecs, int k, int with_shared,
@@ -73,6 +76,30 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4 *__restrict__ 
                     fma_bf16x8(acc, dz[(size_t)t * k + j],
                                Wg[(size_t)ids[(size_t)t * k + j] * vecs + c]);
             }
+        } else if constexpr (GATE) {
+            int rows[KM], gid[KM];
+            float a[KM];
+#pragma unroll
+            for (int j = 0; j < KM; ++j) {
+                rows[j] = j < k ? sr[j] : 0;
+                gid[j] = j < k ? ids[(size_t)t * k + j] : 0;
+                a[j] = j < k ? dz[(size_t)t * k + j] : 0.0f;
+            }
+            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 vs = with_shared ? yp[(S + t) * vecs + c] : zero;
+            uint4 v[KM], w[KM];
+#pragma unroll
+            for (int j = 0; j < KM; ++j) {
+                v[j] = j < k ? yp[(size_t)rows[j] * vecs + c] : zero;
+                w[j] = j < k ? Wg[(size_t)gid[j] * vecs + c] : zero;
+            }
+            if (with_shared) add_bf16x8(acc, vs);
+#pragma unroll
+            for (int j = 0; j < KM; ++j)
+                if (j < k) add_bf16x8(acc, v[j]);
+#pragma unroll
+            for (int j = 0; j < KM; ++j)
+                if (j < k) fma_bf16x8(acc, a[j], w[j]);
         } else {
             int rows[KM];
 #pragma unroll
@@ -230,7 +257,15 @@ moe_status launch_combine(const uint16_t *y_perm, const int32_t *slot_row, int T
     const uint4 *yp = reinterpret_cast<const uint4 *>(y_perm);
     const uint4 *wg = reinterpret_cast<const uint4 *>(Wg);
     uint4 *yo = reinterpret_cast<uint4 *>(y);
-    if (k <= 8)
+    // the gate form holds 2 KM row chunks in registers: KM = 6 (the usual
+    // top-6) keeps it at three blocks per SM
+    if (k <= 6 && dz)
+        combine_kernel<6, true><<<grid, 256, 0, st>>>(yp, slot_row, T, d / 8, k, with_shared, dz,
+                                                      ids, wg, yo);
+    else if (k <= 8 && dz)
+        combine_kernel<8, true><<<grid, 256, 0, st>>>(yp, slot_row, T, d / 8, k, with_shared, dz,
+                                                      ids, wg, yo);
+    else if (k <= 8)
         combine_kernel<8><<<grid, 256, 0, st>>>(yp, slot_row, T, d / 8, k, with_shared, dz, ids,
                                                 wg, yo);
     else

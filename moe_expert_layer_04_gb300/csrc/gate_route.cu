@@ -14,20 +14,27 @@
 // one tile overlaps the MMAs of the next.
 //
 // Epilogue, one token per thread (its TMEM lane), per tile:
-//   pass 1  each of the CTA's logits (+ offset) goes out through a swizzled
-//           staging buffer and a TMA store.  Its approximate key (fast
-//           sigmoid + bias) is compared with the smallest of a sorted
-//           register list of the L largest so far; per 32-expert chunk each
-//           lane collects its candidates in a bit mask and inserts only
-//           those, so a warp pays for its busiest lane.  TMEM is handed back
-//           to the MMA warp right after.
+//   pass A  each of the CTA's logits (+ offset) goes out through a swizzled
+//           staging buffer and a TMA store; its approximate key (fast
+//           sigmoid + bias) goes back into the logit's TMEM column.  The
+//           maxima of the keys' groups of 4 columns run through a keys-only
+//           list of the L largest: its last entry is a lower bound of the
+//           L-th largest key (L distinct keys reach it).
+//   pass B  the keys come back from TMEM; per 32-expert chunk each lane
+//           marks, in a bit mask, the keys above both that bound and the
+//           smallest entry of its sorted register list of the L largest
+//           (key, id) so far, and inserts only those, so a warp pays for
+//           its busiest lane (about 8 candidates of 192 per token instead of
+//           35 with one pass).  TMEM is handed back to the MMA warp right
+//           after.
 //   merge   (CS = 2) rank r owns tokens 64r .. 64r+63 of the tile.  For the
 //           other 64 it sends its list to the peer's shared memory
 //           (distributed shared memory, bounded mbarrier handshakes); for
 //           its own it merges the peer's list into its own.
-//   pass 2  the owner gives the list entries within twice the approximate
-//           error of the k-th key the exact key (sigmoid in fp64 rounded once
-//           to fp32, one fp32 add of the bias) and takes the exact top-k among
+//   exact   the owner gives the list entries within twice the approximate
+//           error of the k-th key the exact key (their logits read back from
+//           global memory; sigmoid in fp64 rounded once to fp32, one fp32 add
+//           of the bias) and takes the exact top-k among
 //           them, equal keys to the lower id.  When the window could reach
 //           past the list (many near-equal keys), it rescans the token's
 //           logits row from global memory instead (every writer completed and
@@ -108,26 +115,22 @@ __device__ __forceinline__ float exact_key(float se, float b) {
     return (kk == kk) ? kk : -FLT_MAX;
 }
 
-// Inserts (key, id, z) into the descending list when it beats the smallest
-// entry, without branches: the slot comes after every entry not below the key
-// (independent compares), then the tail shifts.
+// Inserts (key, id) into the descending list when it beats the smallest
+// entry, without branches: the new entry sinks from the top and swaps with
+// every entry it beats, so it lands after all entries not below it (equal
+// keys keep the earlier entry first) and the smallest drops out.
 template <int L>
-__device__ __forceinline__ void list_insert(float (&kv)[L], int (&iv)[L], float (&zv)[L],
-                                            float key, int id, float z) {
-    int pos = key > kv[L - 1] ? 0 : L;   // L: no slot, nothing moves
+__device__ __forceinline__ void list_insert(float (&kv)[L], int (&iv)[L], float key, int id) {
 #pragma unroll
-    for (int q = 0; q < L - 1; ++q) pos += kv[q] >= key ? 1 : 0;
-#pragma unroll
-    for (int q = L - 1; q > 0; --q) {
-        const bool sh = q > pos, put = q == pos;
-        kv[q] = sh ? kv[q - 1] : (put ? key : kv[q]);
-        iv[q] = sh ? iv[q - 1] : (put ? id : iv[q]);
-        zv[q] = sh ? zv[q - 1] : (put ? z : zv[q]);
+    for (int q = 0; q < L; ++q) {
+        const bool sw = key > kv[q];
+        const float tk = kv[q];
+        const int ti = iv[q];
+        kv[q] = sw ? key : tk;
+        iv[q] = sw ? id : ti;
+        key = sw ? tk : key;
+        id = sw ? ti : id;
     }
-    const bool put0 = pos == 0;
-    kv[0] = put0 ? key : kv[0];
-    iv[0] = put0 ? id : iv[0];
-    zv[0] = put0 ? z : zv[0];
 }
 
 // L: approximate candidates kept per token (more than k); CS: CTAs per tile.
@@ -288,7 +291,6 @@ __global__ void __launch_bounds__(kGrThreads, 1)
         const bool topk = p.mode == MOE_ROUTE_TOPK;
         uint8_t *stg = stg_all + (size_t)(warp - 2) * 4096;
         const uint32_t stg_row = smem_u32(stg) + (uint32_t)lane * 128u;
-        const uint8_t *row_s = stg + lane * 128;
         // this lane's row of approximate keys, laid out like its logits row
         uint8_t *krow = stg_all + 4 * 4096 + (size_t)(warp - 2) * 4096 + lane * 128;
         const uint32_t sw = (uint32_t)(lane & 7);
@@ -334,15 +336,11 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                 }
             }
 
-            // ---- pass 1: logits out, approximate keys into the sorted list
-            float kv[L], zv[L];
-            int iv[L];
+            // ---- pass A: logits out; approximate keys back into TMEM; the L
+            // largest group-of-4 maxima of the keys
+            float gl[L];
 #pragma unroll
-            for (int j = 0; j < L; ++j) {
-                kv[j] = -INFINITY;
-                zv[j] = 0.0f;
-                iv[j] = INT_MAX;
-            }
+            for (int j = 0; j < L; ++j) gl[j] = -INFINITY;
             uint32_t ra[32], rb[32];
             tmem_ld32(tb, ra);
             tmem_wait_ld();
@@ -375,54 +373,27 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                 }
                 if (cc + 32 < NE) tmem_ld32(tb + cc + 32, rb);
                 if (topk) {
-                    {
-                        // (every lane: the insertion loop below is warp-wide; rows
-                        // past T get no candidates)
-                        float kc[32];
+                    uint32_t kc[32];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 b4 = *reinterpret_cast<const float4 *>(bt + c + j);
-                            kc[j] = approx_key(__uint_as_float(ra[j]), b4.x);
-                            kc[j + 1] = approx_key(__uint_as_float(ra[j + 1]), b4.y);
-                            kc[j + 2] = approx_key(__uint_as_float(ra[j + 2]), b4.z);
-                            kc[j + 3] = approx_key(__uint_as_float(ra[j + 3]), b4.w);
-                        }
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(bt + c + j);
+                        kc[j] = __float_as_uint(approx_key(__uint_as_float(ra[j]), b4.x));
+                        kc[j + 1] = __float_as_uint(approx_key(__uint_as_float(ra[j + 1]), b4.y));
+                        kc[j + 2] = __float_as_uint(approx_key(__uint_as_float(ra[j + 2]), b4.z));
+                        kc[j + 3] = __float_as_uint(approx_key(__uint_as_float(ra[j + 3]), b4.w));
+                    }
+                    tmem_st32(tb + cc, kc);
+                    // the L largest group maxima are L distinct keys, so the
+                    // L-th largest of them bounds the L-th largest key from below
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<float4 *>(krow + ((((uint32_t)j) ^ sw) << 4)) =
-                                make_float4(kc[4 * j], kc[4 * j + 1], kc[4 * j + 2], kc[4 * j + 3]);
-                        // candidates: keys above the list's smallest so far and, for
-                        // L = 8, not below the smallest of the chunk's 8 group-of-4
-                        // maxima (those are 8 distinct keys at least that large, so
-                        // nothing below it can be among the 8 largest), as a bit
-                        // mask.  Each lane then inserts only its own, in increasing
-                        // expert order, reading key and z back from its rows.
-                        const float thr0 = kv[L - 1];
-                        float gmin = -INFINITY;
-                        if constexpr (L == 8) {
-                            gmin = INFINITY;
+                    for (int g = 0; g < 8; ++g) {
+                        float x = fmaxf(fmaxf(__uint_as_float(kc[4 * g]), __uint_as_float(kc[4 * g + 1])),
+                                        fmaxf(__uint_as_float(kc[4 * g + 2]), __uint_as_float(kc[4 * g + 3])));
 #pragma unroll
-                            for (int g = 0; g < 8; ++g)
-                                gmin = fminf(gmin, fmaxf(fmaxf(kc[4 * g], kc[4 * g + 1]),
-                                                         fmaxf(kc[4 * g + 2], kc[4 * g + 3])));
-                        }
-                        uint32_t m = 0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            m |= (kc[j] > thr0 && kc[j] >= gmin ? 1u : 0u) << j;
-                        if (!valid) m = 0;
-                        // a converged loop: every lane runs the warp's largest count,
-                        // lanes out of candidates insert nothing (a divergent loop
-                        // costs several times more per trip here)
-                        const int trips = __reduce_max_sync(0xffffffffu, __popc(m));
-                        for (int r = 0; r < trips; ++r) {
-                            const bool act = m != 0u;
-                            const int j = act ? __ffs(m) - 1 : 0;
-                            m &= m - 1u;
-                            const uint32_t off = ((((uint32_t)(j >> 2)) ^ sw) << 4) + (j & 3) * 4;
-                            const float zz = *reinterpret_cast<const float *>(row_s + off);
-                            const float key = *reinterpret_cast<const float *>(krow + off);
-                            list_insert<L>(kv, iv, zv, act ? key : -INFINITY, c + j, zz);
+                        for (int i = 0; i < L; ++i) {
+                            const float hi = fmaxf(gl[i], x);
+                            x = fminf(gl[i], x);
+                            gl[i] = hi;
                         }
                     }
                 } else if (valid) {
@@ -440,6 +411,57 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) ra[j] = rb[j];
+                }
+            }
+
+            // ---- pass B (top-k): the keys not below that bound, into the
+            // sorted list of the L largest (ids in increasing order)
+            float kv[L];
+            int iv[L];
+#pragma unroll
+            for (int j = 0; j < L; ++j) {
+                kv[j] = -INFINITY;
+                iv[j] = INT_MAX;
+            }
+            if (topk) {
+                tmem_wait_st();
+                const float thrg = gl[L - 1];
+                tmem_ld32(tb, ra);
+                tmem_wait_ld();
+#pragma unroll 1
+                for (int cc = 0; cc < NE; cc += 32) {
+                    const int c = col0 + cc;
+                    if (cc + 32 < NE) tmem_ld32(tb + cc + 32, rb);
+                    // this lane's keys, for the candidates' reads by index
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(krow + ((((uint32_t)j) ^ sw) << 4)) =
+                            make_uint4(ra[4 * j], ra[4 * j + 1], ra[4 * j + 2], ra[4 * j + 3]);
+                    const float thr0 = kv[L - 1];
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float kk = __uint_as_float(ra[j]);
+                        m |= (kk > thr0 && kk >= thrg ? 1u : 0u) << j;
+                    }
+                    if (!valid) m = 0;
+                    // a converged loop: every lane runs the warp's largest count,
+                    // lanes out of candidates insert nothing (a divergent loop
+                    // costs several times more per trip here)
+                    const int trips = __reduce_max_sync(0xffffffffu, __popc(m));
+                    for (int r = 0; r < trips; ++r) {
+                        const bool act = m != 0u;
+                        const int j = act ? __ffs(m) - 1 : 0;
+                        m &= m - 1u;
+                        const uint32_t off = ((((uint32_t)(j >> 2)) ^ sw) << 4) + (j & 3) * 4;
+                        const float key = *reinterpret_cast<const float *>(krow + off);
+                        list_insert<L>(kv, iv, act ? key : -INFINITY, c + j);
+                    }
+                    if (cc + 32 < NE) {
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) ra[j] = rb[j];
+                    }
                 }
             }
             // TMEM is free for the next tile
@@ -460,14 +482,14 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                     const uint32_t dst = dsmem_map(my_mrg, (uint32_t)(rank ^ 1));
 #pragma unroll
                     for (int i = 0; i < L; ++i) {
-                        float zsend = zv[i];
-                        if (!topk) zsend = i < kGrKmax ? hz[i % kGrKmax] : 0.0f;
+                        // top-k: the list; hash: the picked logits (field 2)
                         dsmem_st_u32(dst + (uint32_t)((0 * L + i) * 32 + lane) * 4u,
                                      __float_as_uint(kv[i]));
                         dsmem_st_u32(dst + (uint32_t)((1 * L + i) * 32 + lane) * 4u,
                                      (uint32_t)iv[i]);
-                        dsmem_st_u32(dst + (uint32_t)((2 * L + i) * 32 + lane) * 4u,
-                                     __float_as_uint(zsend));
+                        if (!topk)
+                            dsmem_st_u32(dst + (uint32_t)((2 * L + i) * 32 + lane) * 4u,
+                                         __float_as_uint(i < kGrKmax ? hz[i % kGrKmax] : 0.0f));
                     }
                     mbar_arrive_remote(dsmem_map(&lfull[qq], (uint32_t)(rank ^ 1)));
                     continue;
@@ -480,12 +502,12 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                 for (int i = 0; i < L; ++i) {
                     pk[i] = my_mrg[(0 * L + i) * 32 + lane];
                     pi[i] = __float_as_int(my_mrg[(1 * L + i) * 32 + lane]);
-                    pz[i] = my_mrg[(2 * L + i) * 32 + lane];
+                    pz[i] = topk ? 0.0f : my_mrg[(2 * L + i) * 32 + lane];
                 }
                 mbar_arrive_remote(dsmem_map(&lempty[qq], (uint32_t)(rank ^ 1)));
                 if (topk) {
 #pragma unroll
-                    for (int i = 0; i < L; ++i) list_insert<L>(kv, iv, zv, pk[i], pi[i], pz[i]);
+                    for (int i = 0; i < L; ++i) list_insert<L>(kv, iv, pk[i], pi[i]);
                 } else {
                     // the peer picked the logits of the experts in its columns
 #pragma unroll
@@ -514,9 +536,9 @@ __global__ void __launch_bounds__(kGrThreads, 1)
             const float tol = 4e-6f * fmaxf(1.0f, fabsf(kth));
             const float thr = kth - 2.0f * tol;
             const bool rescan = topk && valid && !(kv[L - 1] < thr);
-            if (topk && __any_sync(0xffffffffu, rescan)) {
-                // the window may hold experts the list dropped: stream the token's
-                // whole logits row through an exact top-k.  Our own stores must be
+            if (topk) {
+                // the exact keys start from the logits in global memory (the
+                // list holds keys and ids only).  Our own stores must be
                 // complete and visible first (the peer's are: it fenced them
                 // before it signalled).
                 if (lane == 0) {
@@ -524,6 +546,10 @@ __global__ void __launch_bounds__(kGrThreads, 1)
                     fence_proxy_async_global();
                 }
                 __syncwarp();
+            }
+            if (topk && __any_sync(0xffffffffu, rescan)) {
+                // the window may hold experts the list dropped: stream the token's
+                // whole logits row through an exact top-k
                 if (rescan) {
                     float ek[kGrKmax], es[kGrKmax];
                     int ei[kGrKmax];
@@ -566,13 +592,18 @@ __global__ void __launch_bounds__(kGrThreads, 1)
             }
 
             if (topk && valid && !rescan) {
-                float ek[L], es[L];
+                float ek[L], es[L], zw[L];
+                const float *zrow = p.logits + (size_t)row * E;
+#pragma unroll
+                for (int i = 0; i < L; ++i)
+                    zw[i] = kv[i] >= thr && (unsigned)iv[i] < (unsigned)E ? __ldcg(zrow + iv[i])
+                                                                        : 0.0f;
 #pragma unroll
                 for (int i = 0; i < L; ++i) {
                     ek[i] = -INFINITY;
                     es[i] = 0.0f;
                     if (kv[i] >= thr) {
-                        es[i] = sigmoid_exact_f(zv[i]);
+                        es[i] = sigmoid_exact_f(zw[i]);
                         ek[i] = exact_key(es[i], bt[iv[i]]);
                     }
                 }
