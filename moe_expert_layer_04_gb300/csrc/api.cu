@@ -29,7 +29,7 @@ moe_status launch_permute(const int32_t *ids, const float *weights, const uint16
                           int d, int E, int k, int32_t *counts, int32_t *offsets,
                           int32_t *row_token, int32_t *slot_row, float *row_weight,
                           uint16_t *x_perm, void *ws, cudaStream_t st);
-size_t dwg_workspace_bytes(int d, int E);
+size_t dwg_workspace_bytes(int d, int E, long long S);
 moe_status launch_combine(const uint16_t *y_perm, const int32_t *slot_row, int T, int d, int k,
                           int with_shared, const float *dz, const int32_t *ids,
                           const uint16_t *Wg, uint16_t *y, cudaStream_t st);
@@ -38,7 +38,7 @@ moe_status launch_router_bwd(const float *dw_part, int n_part, const int32_t *sl
                              int E, int k, float scaling, float *dz_sel, float *dz_row,
                              float *dlogits, float *dweights, cudaStream_t st);
 moe_status launch_dwg(const uint16_t *x_perm, const float *dz_row, const int32_t *offsets, int d,
-                      int E, float *part, float *dWg, cudaStream_t st);
+                      int E, long long S, float *part, float *dWg, cudaStream_t st);
 
 namespace {
 
@@ -124,7 +124,7 @@ RouterBwdWorkspace carve_router_bwd(uint8_t *base, int T, int d, int E, int k) {
     };
     w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
-    w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
+    w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E, (long long)T * k)));
     w.bytes = off;
     return w;
 }
@@ -228,7 +228,7 @@ BwdWorkspace carve_bwd(uint8_t *base, int T, int d, int E, int k, int I, int fla
     w.dw_part = reinterpret_cast<float *>(take(R * dgrad2_n_tiles(I) * 4));
     w.dz_sel = reinterpret_cast<float *>(take((size_t)T * k * 4));
     w.dz_row = reinterpret_cast<float *>(take((size_t)T * k * 4));
-    w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E)));
+    w.dwg_part = reinterpret_cast<float *>(take(dwg_workspace_bytes(d, E, (long long)T * k)));
     w.tail_maps = take(kWgradScratchBytes);
     if (flags & MOE_FLAG_RECOMPUTE) {
         w.x_perm = reinterpret_cast<uint16_t *>(take(R * d * 2));
@@ -776,7 +776,8 @@ moe_status moe_backward_mx(const moe_bwd_mx_args *a, void *stream) {
                             a->dX, st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_DWG)) return MOE_ERR_CUDA;
-    if ((s = launch_dwg(w.x_perm, w.router.dz_row, a->offsets, d, E, w.router.dwg_part, a->dW_g,
+    if ((s = launch_dwg(w.x_perm, w.router.dz_row, a->offsets, d, E, (long long)T * k,
+                        w.router.dwg_part, a->dW_g,
                         st)) != MOE_OK)
         return s;
     return mark(MOE_BWD_STAGES) ? MOE_OK : MOE_ERR_CUDA;
@@ -891,7 +892,8 @@ moe_status moe_backward(const moe_bwd_args *a, void *stream) {
                             st)) != MOE_OK)
         return s;
     if (!mark(MOE_BWD_DWG)) return MOE_ERR_CUDA;
-    if ((s = launch_dwg(x_perm, w.dz_row, a->offsets, d, E, w.dwg_part, a->dW_g, st)) != MOE_OK)
+    if ((s = launch_dwg(x_perm, w.dz_row, a->offsets, d, E, (long long)T * k, w.dwg_part,
+                        a->dW_g, st)) != MOE_OK)
         return s;
     return mark(MOE_BWD_STAGES) ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -986,7 +988,7 @@ moe_status moe_router_backward(const float *dw_rows, const uint16_t *dX_perm,
         return s;
     if ((s = launch_combine(dX_perm, slot_row, T, d, k, 1, w.dz_sel, ids, W_g, dX, st)) != MOE_OK)
         return s;
-    return launch_dwg(x_perm, w.dz_row, offsets, d, E, w.dwg_part, dW_g, st);
+    return launch_dwg(x_perm, w.dz_row, offsets, d, E, (long long)T * k, w.dwg_part, dW_g, st);
 }
 
 namespace {

@@ -179,54 +179,122 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
     }
 }
 
-// Block (e, column chunk of 512, row split p): partial sums of dz_row * x_perm
-// over the split's share of expert e's rows.  64 threads x 8 columns.
+// dW_g[e] = sum over expert e's rows of dz_row * x_perm[row].  The rows are
+// cut into chunks of kDwgChunk rows that never cross an expert (an expert of
+// n rows has ceil(n / kDwgChunk) chunks), so every block streams about the
+// same bytes however skewed the load.  Each chunk's sum lands in its own row
+// of the workspace; the reduction adds an expert's chunks in chunk order, and
+// a chunk sums its rows in row order, so the result does not depend on the
+// schedule.
+constexpr int kDwgChunk = 256;
+
+// One block of 1024 threads (E <= 1024): chunk_first[e] = chunks before
+// expert e (chunk_first[E] = all of them, at most nc_max), chunk_expert[c] =
+// the expert of chunk c, -1 for the unused rest of the bound.
+__global__ void __launch_bounds__(1024) dwg_plan_kernel(const int32_t *__restrict__ offsets, int E,
+                                                        int nc_max, int32_t *__restrict__ chunk_first,
+                                                        int32_t *__restrict__ chunk_expert) {
+    __shared__ int32_t warp_sum[32];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    int n = 0;
+    if (t < E) {
+        const int rows = offsets[t + 1] - offsets[t];
+        n = rows > 0 ? (rows + kDwgChunk - 1) / kDwgChunk : 0;
+    }
+    // inclusive scan of n over the block
+    int v = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_sum[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        warp_sum[lane] = w;
+    }
+    __syncthreads();
+    const int incl = v + (wid > 0 ? warp_sum[wid - 1] : 0);
+    const int first = incl - n;
+    if (t < E) {
+        chunk_first[t] = first < nc_max ? first : nc_max;
+        for (int j = 0; j < n && first + j < nc_max; ++j) chunk_expert[first + j] = t;
+    }
+    if (t == E - 1 || (E == 0 && t == 0)) chunk_first[E] = incl < nc_max ? incl : nc_max;
+    const int total = warp_sum[31] < nc_max ? warp_sum[31] : nc_max;
+    for (int c = total + t; c < nc_max; c += blockDim.x) chunk_expert[c] = -1;
+}
+
+// Block (chunk, 512 columns): 64 threads x 8 columns, eight rows in flight.
 __global__ void __launch_bounds__(64) dwg_partial_kernel(const uint4 *__restrict__ xp,
                                                          const float *__restrict__ dz_row,
                                                          const int32_t *__restrict__ offsets,
-                                                         int vecs, int E, int splits,
-                                                         float *__restrict__ part) {
-    const int e = blockIdx.x;
+                                                         const int32_t *__restrict__ chunk_first,
+                                                         const int32_t *__restrict__ chunk_expert,
+                                                         int vecs, float *__restrict__ part) {
+    const int ch = blockIdx.x;
+    const int e = chunk_expert[ch];
     const int c = blockIdx.y * 64 + threadIdx.x;
-    const int sp = blockIdx.z;
-    const int lo = offsets[e], hi = offsets[e + 1];
-    const int n = hi - lo;
-    const int r0 = lo + (int)((long long)n * sp / splits);
-    const int r1 = lo + (int)((long long)n * (sp + 1) / splits);
+    if (e < 0 || c >= vecs) return;
+    const int lo = offsets[e] + (ch - chunk_first[e]) * kDwgChunk;
+    const int end = offsets[e + 1];
+    const int hi = end < lo + kDwgChunk ? end : lo + kDwgChunk;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (c < vecs) {
-        int r = r0;
-        // four rows in flight per step, summed in row order
-        for (; r + 4 <= r1; r += 4) {
-            const uint4 v0 = xp[(size_t)r * vecs + c];
-            const uint4 v1 = xp[(size_t)(r + 1) * vecs + c];
-            const uint4 v2 = xp[(size_t)(r + 2) * vecs + c];
-            const uint4 v3 = xp[(size_t)(r + 3) * vecs + c];
-            fma_bf16x8(acc, dz_row[r], v0);
-            fma_bf16x8(acc, dz_row[r + 1], v1);
-            fma_bf16x8(acc, dz_row[r + 2], v2);
-            fma_bf16x8(acc, dz_row[r + 3], v3);
+    int r = lo;
+    for (; r + 8 <= hi; r += 8) {
+        uint4 v[8];
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            v[j] = xp[(size_t)(r + j) * vecs + c];
+            a[j] = dz_row[r + j];
         }
-        for (; r < r1; ++r) fma_bf16x8(acc, dz_row[r], xp[(size_t)r * vecs + c]);
-        float4 *dst = reinterpret_cast<float4 *>(part + (((size_t)sp * E + e) * vecs + c) * 8);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) fma_bf16x8(acc, a[j], v[j]);
     }
+    for (; r < hi; ++r) fma_bf16x8(acc, dz_row[r], xp[(size_t)r * vecs + c]);
+    float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)ch * vecs + c) * 8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
+__device__ __forceinline__ void add4(float4 &a, const float4 b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+// One thread per (expert, 4 columns): the expert's chunks in order, four
+// loads in flight.  An expert without rows gets zeros.
 __global__ void __launch_bounds__(256) dwg_reduce_kernel(const float4 *__restrict__ part,
-                                                         size_t n4, int splits,
-                                                         float4 *__restrict__ dWg) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+                                                         const int32_t *__restrict__ chunk_first,
+                                                         int E, int d4, float4 *__restrict__ dWg) {
+    const size_t n = (size_t)E * d4;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x) {
-        float4 a = part[i];
-        for (int sp = 1; sp < splits; ++sp) {
-            const float4 b = part[(size_t)sp * n4 + i];
-            a.x += b.x;
-            a.y += b.y;
-            a.z += b.z;
-            a.w += b.w;
+        const int e = (int)(i / d4);
+        const int c = (int)(i - (size_t)e * d4);
+        const int f = chunk_first[e], m = chunk_first[e + 1] - f;
+        float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        int j = 0;
+        for (; j + 4 <= m; j += 4) {
+            const float4 b0 = part[(size_t)(f + j) * d4 + c];
+            const float4 b1 = part[(size_t)(f + j + 1) * d4 + c];
+            const float4 b2 = part[(size_t)(f + j + 2) * d4 + c];
+            const float4 b3 = part[(size_t)(f + j + 3) * d4 + c];
+            add4(a, b0);
+            add4(a, b1);
+            add4(a, b2);
+            add4(a, b3);
         }
+        for (; j < m; ++j) add4(a, part[(size_t)(f + j) * d4 + c]);
         dWg[i] = a;
     }
 }
@@ -239,12 +307,13 @@ int token_blocks(int T) {
 
 }  // namespace
 
-// Row splits of each expert's dW_g sum: the hottest expert of a skewed load
-// holds ~40 % of a 64K-token slice's rows, and each split is one block.
-constexpr int kDwgSplits = 32;
+// Upper bound of the chunks: sum_e ceil(n_e / kDwgChunk) <= S / kDwgChunk + E.
+static size_t dwg_chunks_max(int E, long long S) { return (size_t)(S / kDwgChunk) + (size_t)E; }
 
-size_t dwg_workspace_bytes(int d, int E) {
-    return ((size_t)kDwgSplits * E * d * 4 + 255) / 256 * 256;
+size_t dwg_workspace_bytes(int d, int E, long long S) {
+    const size_t nc = dwg_chunks_max(E, S);
+    return (nc * d * 4 + 255) / 256 * 256 + ((size_t)(E + 1) * 4 + 255) / 256 * 256 +
+           (nc * 4 + 255) / 256 * 256;
 }
 
 moe_status launch_combine(const uint16_t *y_perm, const int32_t *slot_row, int T, int d, int k,
@@ -285,16 +354,28 @@ moe_status launch_router_bwd(const float *dw_part, int n_part, const int32_t *sl
 }
 
 moe_status launch_dwg(const uint16_t *x_perm, const float *dz_row, const int32_t *offsets, int d,
-                      int E, float *part, float *dWg, cudaStream_t st) {
+                      int E, long long S, float *part, float *dWg, cudaStream_t st) {
+    if (E > 1024) return MOE_ERR_UNSUPPORTED;
     const int vecs = d / 8;
-    dim3 grid(E, (vecs + 63) / 64, kDwgSplits);
-    dwg_partial_kernel<<<grid, 64, 0, st>>>(reinterpret_cast<const uint4 *>(x_perm), dz_row,
-                                            offsets, vecs, E, kDwgSplits, part);
-    const size_t n4 = (size_t)E * d / 4;
+    const size_t nc = dwg_chunks_max(E, S);
+    if (nc > 0x7fffffff) return MOE_ERR_UNSUPPORTED;
+    uint8_t *base = reinterpret_cast<uint8_t *>(part);
+    int32_t *chunk_first = reinterpret_cast<int32_t *>(base + (nc * d * 4 + 255) / 256 * 256);
+    int32_t *chunk_expert =
+        reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(chunk_first) +
+                                    ((size_t)(E + 1) * 4 + 255) / 256 * 256);
+    dwg_plan_kernel<<<1, 1024, 0, st>>>(offsets, E, (int)nc, chunk_first, chunk_expert);
+    if (nc > 0) {
+        dim3 grid((unsigned)nc, (vecs + 63) / 64);
+        dwg_partial_kernel<<<grid, 64, 0, st>>>(reinterpret_cast<const uint4 *>(x_perm), dz_row,
+                                                offsets, chunk_first, chunk_expert, vecs, part);
+    }
+    const int d4 = d / 4;
+    const size_t n4 = (size_t)E * d4;
     const int blocks = (int)((n4 + 255) / 256 < (size_t)num_sms() * 8 ? (n4 + 255) / 256
                                                                        : (size_t)num_sms() * 8);
-    dwg_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(part), n4,
-                                              kDwgSplits, reinterpret_cast<float4 *>(dWg));
+    dwg_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(part), chunk_first,
+                                              E, d4, reinterpret_cast<float4 *>(dWg));
     return cuda_status(cudaGetLastError());
 }
 
