@@ -125,7 +125,8 @@ moe_status moe_route_logits(const float *logits, const float *bias, const uint8_
  *   row 1 vision); rows sum to T*k.  Overwritten (zeroed on `stream` first).
  * The logits of each 128-token block stay in tensor memory (of one CTA, or
  * split by experts over a pair of CTAs when E % 64 == 0) and are routed
- * there, so they are written once and never read back.
+ * there: they are written once, and only the few logits within each token's
+ * selection window (its whole row when many keys tie) are read back.
  * Supported: d % 64 == 0, E % 32 == 0, 32 <= E <= 512, 1 <= k <= min(8, E);
  * other sizes return MOE_ERR_UNSUPPORTED (use moe_route).  Needs logits 16-
  * byte aligned; ids, weights, scores_sel and modality_counts 4-byte aligned. */
