@@ -75,8 +75,17 @@ __global__ void __launch_bounds__(kPermThreads) perm_chunk_scan_kernel(int32_t *
     const int e = blockIdx.x;
     const int per = (nchunks + kPermThreads - 1) / kPermThreads;
     const int c0 = threadIdx.x * per;
+    // up to kHeld counts stay in registers between the two passes, loaded
+    // together (one memory latency instead of one per chunk)
+    constexpr int kHeld = 8;
+    int held[kHeld];
+#pragma unroll
+    for (int u = 0; u < kHeld; ++u)
+        held[u] = u < per && c0 + u < nchunks ? part[(size_t)(c0 + u) * E + e] : 0;
     int local = 0;
-    for (int c = c0; c < c0 + per && c < nchunks; ++c) local += part[(size_t)c * E + e];
+#pragma unroll
+    for (int u = 0; u < kHeld; ++u) local += held[u];
+    for (int c = c0 + kHeld; c < c0 + per && c < nchunks; ++c) local += part[(size_t)c * E + e];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int incl = local;
 #pragma unroll
@@ -89,7 +98,14 @@ __global__ void __launch_bounds__(kPermThreads) perm_chunk_scan_kernel(int32_t *
     int before = 0;
     for (int w = 0; w < wid; ++w) before += wsum[w];
     int run = before + incl - local;
-    for (int c = c0; c < c0 + per && c < nchunks; ++c) {
+#pragma unroll
+    for (int u = 0; u < kHeld; ++u) {
+        if (u < per && c0 + u < nchunks) {
+            part[(size_t)(c0 + u) * E + e] = run;
+            run += held[u];
+        }
+    }
+    for (int c = c0 + kHeld; c < c0 + per && c < nchunks; ++c) {
         const int v = part[(size_t)c * E + e];
         part[(size_t)c * E + e] = run;
         run += v;
