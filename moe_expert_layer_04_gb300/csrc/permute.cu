@@ -220,7 +220,7 @@ moe_status launch_gather_rows(const uint16_t *src, const int32_t *slot_row, int 
     const int want = (T + 7) / 8;
     const int blocks = want < num_sms() * 8 ? want : num_sms() * 8;
     // eight 16-byte loads in flight per lane (56 registers): 4 -> 8 took the
-    // 64K-token gathers from 90 to ~92 % of the copy bandwidth
+    // 64K-token gathers from 90 to 92-94 % of the copy bandwidth
     gather_rows_kernel<8><<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4 *>(src), slot_row,
                                                   T, vecs, k, reinterpret_cast<uint4 *>(dst));
     return cuda_status(cudaGetLastError());
