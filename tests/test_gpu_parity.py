@@ -247,6 +247,35 @@ def test_backward_layer_hash_router(recompute):
         assert_close(layer.dW2[e], g["dW2"], f"hash dW2[{e}]")
 
 
+def test_backward_gate_wgrad_chunk_boundaries():
+    # dW_g sums each expert's rows in chunks of 256 that never cross an expert:
+    # a hash table that gives the experts 256, 257, 127, 512, 127, 1, 0 and 0
+    # rows puts groups exactly at, one past and twice the chunk length, a
+    # one-row group and empty groups
+    T, E, k = 640, 8, 2
+    w = W.Workload("gate_chunks", T, 128, E, k, 64, 2.5, vision_frac=0.25)
+    layer, inp = make_layer(w, backward=True)
+    t = np.arange(T)
+    first = np.where(t < 256, 0, np.where(t < 513, 1, 2))
+    second = np.where(t < 512, 3, np.where(t < 639, 4, 5))
+    tid2eid = torch.tensor(np.stack([first, second], 1), dtype=torch.int32, device="cuda")
+    input_ids = torch.arange(T, dtype=torch.int32, device="cuda")
+    layer.forward(inp["x"], inp["bias"], inp["is_vision"], None, mode=MOE_ROUTE_HASH,
+                  input_ids=input_ids, tid2eid=tid2eid)
+    layer.backward(inp["dY"], want_dlogits=True)
+    torch.cuda.synchronize()
+    assert _lib.moe_last_device_status() == _lib.MOE_OK
+    counts = np.diff(cpu(layer.offsets).numpy())[:E]
+    np.testing.assert_array_equal(counts, [256, 257, 127, 512, 127, 1, 0, 0])
+    x, Wg, W13, W2, dY = (cpu(inp[k_]) for k_ in ("x", "W_g", "W13", "W2", "dY"))
+    hk = dict(is_vision=cpu(inp["is_vision"]), mode=1, input_ids=cpu(input_ids),
+              tid2eid=cpu(tid2eid))
+    ref = oracle.layer_backward(x, Wg, W13, W2, dY, cpu(inp["bias"]), k, w.rho, w.clamp, **hk)
+    assert_close(layer.dlogits, ref["dz"], "chunks dlogits")
+    assert_close(layer.dW_g, oracle.gate_wgrad_rows(x, ref["dz"], np.arange(E)), "chunks dW_g")
+    assert torch.count_nonzero(layer.dW_g[6:]).item() == 0
+
+
 def test_zero_routed_scaling_gives_zero_routing_gradients():
     # with scaling 0 every routing weight is 0: y is the shared expert alone,
     # and the routing chain passes no gradient (and no NaN) to the logits
