@@ -110,9 +110,11 @@ def test_route_hash_exact():
     np.testing.assert_allclose(np64(wt), r_w, rtol=W_RTOL, atol=0)
 
 
+# the last case has more than 2048 chunks of 256 slots, so each thread of the
+# chunk scan takes more chunks than it holds in registers
 @pytest.mark.parametrize("T,E,k,skew,d", [(64, 16, 2, 0.0, 128), (1, 4, 3, 0.0, 8),
                                           (2000, 384, 6, 1.1, 64), (700, 50, 5, 2.5, 128),
-                                          (5000, 1000, 8, 0.0, 16)])
+                                          (5000, 1000, 8, 0.0, 16), (70000, 64, 8, 1.1, 8)])
 def test_permute_exact(T, E, k, skew, d):
     ids = W.random_ids(T, E, k, seed=T + E, skew=skew).cuda()
     wts = torch.rand(T, k, device="cuda")
